@@ -1,0 +1,185 @@
+"""The oracle against its pins (CPU only).
+
+The oracle is the fp64 token-by-token recurrence in ``oracle/kda_oracle.c``. Nothing
+here compares it with itself: every check is a closed form, an invariant, a different
+algebra (unrolled transition products, the 16-token chunked form), or a number printed
+by the source pages (``golden/bound_arithmetic.json``).
+"""
+import inspect
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import recurrence
+from oracle.chunked import chunked_forward, inverse_unit_lower
+from tests import oracle_pins as P
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                     "bound_arithmetic.json")))
+
+
+def oracle_fwd(mutant=0):
+    def fwd(q, k, v, a, beta, h0, cu):
+        return recurrence.kda_forward(q, k, v, a, beta, h0, cu, mutant=mutant, threads=2)
+    return fwd
+
+
+# ---------------------------------------------------------------- printed numbers
+
+def test_golden_bound_arithmetic():
+    g = GOLDEN
+    C = g["tile_tokens"]["value"]
+    gmin = g["g_min"]["value"]
+    assert C * gmin == g["worst_chunk_log_decay"]["value"] == -80.0
+    lo, hi = math.exp(C * gmin), math.exp(-C * gmin)
+    for key, val in (("min_cumulative_decay", lo), ("max_reciprocal_decay", hi)):
+        assert abs(val / g[key]["value"] - 1) <= g[key]["rtol"], (key, val)
+    bf = torch.finfo(torch.bfloat16)
+    # the printed normal-range top is bf16's (and fp32's) largest finite value
+    assert abs(bf.max / g["normal_range_top"]["value"] - 1) <= g["normal_range_top"]["rtol"]
+    # "a representable range of roughly 1e-38 to 3e38", shared by bf16 and fp32
+    for fi in (bf, torch.finfo(torch.float32)):
+        assert math.floor(math.log10(fi.tiny)) == math.floor(
+            math.log10(g["bf16_fp32_range_low"]["value"]))
+        assert math.floor(math.log10(fi.max)) == math.floor(
+            math.log10(g["bf16_fp32_range_high"]["value"]))
+    # exp(+-80) are finite, normal bf16 numbers
+    hi_bf = torch.tensor(hi, dtype=torch.float32).to(torch.bfloat16).float().item()
+    lo_bf = torch.tensor(lo, dtype=torch.float32).to(torch.bfloat16).float().item()
+    assert math.isfinite(hi_bf) and abs(hi_bf / hi - 1) < 2 ** -8
+    assert lo_bf >= bf.tiny and abs(lo_bf / lo - 1) < 2 ** -8
+    # "about three orders of magnitude of headroom above the BF16 lower bound"
+    assert round(math.log10(lo / bf.tiny)) == g["headroom_above_bf16_floor_orders"]["value"]
+    # the 15-power reading: exp(-g_min * 15) = exp(75), also representable
+    assert -gmin * (C - 1) == g["fifteen_power_bound_exponent"]["value"]
+    assert math.exp(75.0) < hi < bf.max
+    # single-step floor exp(-5) ~ 0.0067 and "forgetting has exceeded 99%"
+    step = math.exp(gmin)
+    assert abs(step / g["single_step_decay_floor"]["value"] - 1) <= 0.01
+    assert 1 - step > g["forgetting_at_bound_exceeds"]["value"]
+    # the unbounded counter-example: -40 per step, -640 per chunk, 1/Gamma = inf
+    span = C * g["unbounded_step_example"]["value"]
+    assert span == g["unbounded_chunk_example"]["value"]
+    for dt in (torch.float32, torch.bfloat16):
+        Gam = torch.exp(torch.tensor(span, dtype=dt))
+        assert Gam.item() == 0.0 and torch.isinf(1.0 / Gam).item()
+        assert torch.isfinite(torch.exp(torch.tensor(-C * gmin, dtype=dt))).item()
+
+
+def test_oracle_bound_value():
+    assert P.pin_bound_value(oracle_fwd(), GOLDEN) < 1e-13
+
+
+# ---------------------------------------------------------------- pins
+
+@pytest.mark.parametrize("name", sorted(P.PINS))
+def test_oracle_pin(name):
+    fn, tol = P.PINS[name]
+    err = fn(oracle_fwd())
+    assert err <= tol, f"{name}: {err:.3e} > {tol:.0e}"
+
+
+def _run_pin_for_mutant(name, fwd, square):
+    fn, tol = P.PINS[name]
+    kw = {}
+    if square:
+        params = inspect.signature(fn).parameters
+        if "dk" in params and "dv" in params:
+            kw = {"dk": 4, "dv": 4}
+    try:
+        return fn(fwd, **kw) <= tol
+    except AssertionError:
+        return False
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
+def test_planted_mistakes_are_caught(mutant):
+    """Each mutant plants one plausible mistake in a copy of the oracle (decay after
+    the write, output before the write, transposed state, flipped correction sign,
+    bound dropped from the gate, output scale dropped); at least one pin must fail."""
+    recurrence.build(mutant)
+    fwd = oracle_fwd(mutant)
+    square = mutant == 3   # the transposed-read mutant is only memory-safe for d_k == d_v
+    passed = {name: _run_pin_for_mutant(name, fwd, square) for name in P.PINS}
+    try:
+        passed["bound_value"] = P.pin_bound_value(fwd, GOLDEN) < 1e-13
+    except AssertionError:
+        passed["bound_value"] = False
+    assert not all(passed.values()), f"mutant {mutant} passed every pin: {passed}"
+
+
+# ---------------------------------------------------------------- chunked algebra
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 53, 64])
+@pytest.mark.parametrize("d", [4, 8, 16])
+@pytest.mark.parametrize("gate", ["random", "bound", "mixed"])
+def test_chunked_algebra_equals_recurrence(T, d, gate):
+    rng = np.random.default_rng(100 + T * 7 + d)
+    lengths = [T, max(1, T // 3)]
+    q, k, v, a, beta, h0, cu = P._rand(rng, lengths, 2, d, d + 2)
+    if gate == "bound":
+        a[:] = np.inf                      # g = -5 exactly on every channel
+    elif gate == "mixed":
+        a[:, 0] = np.inf
+        a[:, 1] = rng.normal(6.0, 1.0, size=a[:, 1].shape)
+    o_ref, h_ref = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    for inverse in ("solve", "doubling"):
+        o, hf = chunked_forward(q, k, v, a, beta, h0, cu, inverse=inverse)
+        assert P.rel(o, o_ref) < 1e-12 and P.rel(hf, h_ref) < 1e-12, inverse
+
+
+def test_doubling_inverse_is_exact():
+    rng = np.random.default_rng(11)
+    for _ in range(5):
+        A = np.tril(rng.standard_normal((16, 16)), -1)
+        ref = np.linalg.inv(np.eye(16) + A)
+        for m in ("solve", "doubling"):
+            T = inverse_unit_lower(A, m)
+            assert np.abs(T - ref).max() / np.abs(ref).max() < 1e-12
+
+
+# ---------------------------------------------------------------- host-side behaviour
+
+def test_packing_equals_separate_calls():
+    rng = np.random.default_rng(12)
+    lengths = [5, 0, 33, 16, 1]
+    q, k, v, a, beta, h0, cu = P._rand(rng, lengths, 3, 6, 4)
+    o, hf = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    for n, L in enumerate(lengths):
+        s, e = cu[n], cu[n + 1]
+        o1, h1 = recurrence.kda_forward(q[s:e], k[s:e], v[s:e], a[s:e], beta[s:e],
+                                        h0[n:n + 1], [0, L])
+        assert np.array_equal(o[s:e], o1) and np.array_equal(hf[n], h1[0])
+    assert np.array_equal(hf[1], h0[1])          # empty sequence keeps h0
+
+
+def test_resume_equals_one_run():
+    rng = np.random.default_rng(13)
+    T = 50
+    q, k, v, a, beta, h0, cu = P._rand(rng, [T], 2, 5, 5)
+    o, hf = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    for t1 in (1, 16, 23):
+        oa, ha = recurrence.kda_forward(q[:t1], k[:t1], v[:t1], a[:t1], beta[:t1], h0, [0, t1])
+        ob, hb = recurrence.kda_forward(q[t1:], k[t1:], v[t1:], a[t1:], beta[t1:], ha,
+                                        [0, T - t1])
+        assert np.allclose(np.concatenate([oa, ob]), o, rtol=0, atol=1e-13)
+        assert np.allclose(hb, hf, rtol=0, atol=1e-13)
+
+
+def test_thread_count_does_not_change_result():
+    rng = np.random.default_rng(14)
+    q, k, v, a, beta, h0, cu = P._rand(rng, [40, 7, 19], 4, 8, 8)
+    r1 = recurrence.kda_forward(q, k, v, a, beta, h0, cu, threads=1)
+    r8 = recurrence.kda_forward(q, k, v, a, beta, h0, cu, threads=8)
+    assert np.array_equal(r1[0], r8[0]) and np.array_equal(r1[1], r8[1])
+
+
+def test_rejects_bad_offsets():
+    rng = np.random.default_rng(15)
+    q, k, v, a, beta, _, _ = P._rand(rng, [4], 1, 2, 2)
+    with pytest.raises(AssertionError):
+        recurrence.kda_forward(q, k, v, a, beta, None, [0, 3, 2])
