@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Throughput of the chunked KDA forward pass on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+A step is one ``kda_chunk_fwd`` call over the whole workload (every row of the hot
+path: gate prologue, diagonal tile, serial state recurrence, varlen front end), with
+inputs resident in HBM. The default workload is the 64K-token context (B=1, H=32,
+T=65536, d_k = d_v = 128, bf16 q/k/v/o, fp32 gates/beta/state); its 3.2 GB of inputs
+are 25x the 129 MB L2, so no flush is needed between steps. Under torchrun with N > 1
+every rank runs the same per-GPU workload on its own device with its own seed (weak
+scaling, independent sequences: no collective on the data path; one max-reduction of
+the elapsed time for the report).
+
+Reported alongside the device-timed value:
+  e2e          the same metric through ``kda_chunk_fwd_from_host`` with pinned host
+               buffers: H2D copies of the inputs, the kernel and D2H copies of the
+               outputs inside the timed region;
+  roofline     algorithmic bytes per launch / CUDA-event launch time against the
+               measured HBM copy bandwidth (MEASURED_PEAKS.json);
+  cpu_baseline the fp64 oracle on the host cores on a bounded sample (rank 0, N = 1);
+  clocks       nvidia-smi samples taken during the timed region.
+``--impl reference`` times the oracle alone (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA chunked-forward tokens/s (1 GB300) and % of tensor-core/HBM roofline"
+UNIT = "tokens/s"
+KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu",
+                  "chunked_linear_attention_kda_gb300/csrc/kda_simt.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
+
+
+# ------------------------------------------------------------------ accounting
+
+def bytes_per_token_head(d_k: int, d_v: int, io_bytes: int) -> int:
+    """Algorithmic HBM bytes per token and head: q, k read and v read, o written in the
+    I/O dtype; gate logits (d_k fp32) and beta (fp32) read."""
+    return io_bytes * (2 * d_k + 2 * d_v) + 4 * d_k + 4
+
+
+def flops_per_token_head(d_k: int, d_v: int, C: int = 16) -> int:
+    """Algorithmic flops per token and head of the chunked form (a multiply-add is 2):
+    W S, Q~ S and K'^T U (3 x 2 d_k d_v); K~ K^^T and Q~ K^^T (2 x 2 C d_k);
+    TB K~ (2 C d_k); TB V and P U (2 x 2 C d_v)."""
+    return 6 * d_k * d_v + 6 * C * d_k + 4 * C * d_v
+
+
+def state_bytes(x) -> int:
+    per = x.n_seq * x.n_heads * x.d_k * x.d_v * 4
+    return per * (2 if x.h0 is not None else 1)   # h0 read (if given), h_final written
+
+
+def algorithmic_bytes(x) -> int:
+    io = 2 if str(x.dtype).endswith("bfloat16") else 4
+    return x.n_tok * x.n_heads * bytes_per_token_head(x.d_k, x.d_v, io) + state_bytes(x)
+
+
+def algorithmic_flops(x) -> int:
+    return x.n_tok * x.n_heads * flops_per_token_head(x.d_k, x.d_v)
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES + ["chunked_linear_attention_kda_gb300/csrc/kda_internal.h"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, only if it was taken on
+    the current kernel sources (the digest must match)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    digest = kernel_source_digest()
+    for line in open(TRAFFIC_FILE):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("digest") == digest and f.get("workload") == workload:
+            try:
+                return int(float(f["dram_bytes_per_launch"]))
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, local):
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world > 1
+
+
+def barrier(on):
+    if on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, on: bool, device) -> float:
+    if not on:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_sample(x, max_tokens: int, heads=None):
+    """The oracle on the first ``max_tokens`` tokens of every sequence (and the given
+    heads). Returns (seconds, token-heads processed, threads)."""
+    import kda_inputs as K
+    from oracle import recurrence
+    px = K.prefix(x, max_tokens)
+    if heads is not None:
+        px = K.slice_heads(px, heads)
+    cpu = lambda t: None if t is None else t.detach().to("cpu")  # noqa: E731
+    args = [cpu(px.q), cpu(px.k), cpu(px.v), cpu(px.a), cpu(px.beta), cpu(px.h0)]
+    threads = recurrence.default_threads()
+    recurrence.build()
+    t0 = time.perf_counter()
+    recurrence.kda_forward(*args, px.cu_host, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, px.n_tok * px.n_heads, threads
+
+
+def cpu_baseline(x, budget_s: float = 15.0):
+    """Time the oracle on a bounded prefix sample, growing it until it takes a few
+    seconds, scaled to the workload's tokens/s (a token counts all H heads)."""
+    tokens = 256
+    while True:
+        dt, th, threads = oracle_sample(x, tokens)
+        if dt > budget_s / 4 or tokens >= max(x.lengths()):
+            break
+        tokens = min(tokens * 4, max(x.lengths()))
+    value = th / x.n_heads / dt
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"fp64 token-by-token oracle on the first {tokens} tokens of every "
+                      f"sequence, all {x.n_heads} heads ({th} token-heads), "
+                      f"{threads} host threads"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import chunked_linear_attention_kda_gb300 as kda
+    import kda_inputs as K
+
+    world, rank, local = dist_env()
+    on = init_dist(world, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load_library(build_if_missing=True)
+
+    x = K.make_workload(args.workload, dev, seed=K.SEED_BASE + args.workload + 7919 * rank)
+    out = torch.empty((x.n_tok, x.n_heads, x.d_v), dtype=x.dtype, device=dev)
+    hf = torch.empty((x.n_seq, x.n_heads, x.d_k, x.d_v), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.chunk_fwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, out=out, h_final=hf)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    n0 = kda.kernel_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(on)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(on)
+    launches = kda.kernel_launch_count() - n0
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(total_ms, on, dev)
+    ms_per_step = total_ms / args.steps
+    tokens_all = x.n_tok * world
+    value = tokens_all * args.steps / (total_ms * 1e-3)
+
+    # roofline for the (single) kernel of a step
+    peaks = measured_peaks()
+    bytes_launch = algorithmic_bytes(x)
+    flops_launch = algorithmic_flops(x)
+    launches_per_step = max(1, launches // max(1, args.steps))
+    mean_launch_s = statistics.mean(per_launch_ms) * 1e-3 / launches_per_step
+    achieved_gbs = bytes_launch / launches_per_step / mean_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic(x.name),
+                "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)",
+                "algorithmic_bytes_per_launch": bytes_launch,
+                "tensor_tflops": round(flops_launch / mean_launch_s / 1e12, 1),
+                "tensor_frac_of_bf16_peak": round(flops_launch / mean_launch_s / 1e12 /
+                                                  peaks["bf16_tflops"], 4)}
+
+    # end-to-end through the host-buffer entry point
+    e2e = measure_e2e(x, dev, stream, max(1, min(args.steps, 5)), kda)
+    e2e["value"] = e2e["value"] * world
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if x.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic",
+            "config": {"workload": x.name, "tokens_per_gpu": x.n_tok, "heads": x.n_heads,
+                       "d_k": x.d_k, "d_v": x.d_v, "chunk": 16, "n_seq": x.n_seq,
+                       "global_batch_tokens": tokens_all,
+                       "parallelism": f"independent replicas x{world}" if world > 1 else
+                       "single GPU",
+                       "l2": "inputs (%.2f GB) exceed the 129 MB L2; no flush between steps"
+                             % (bytes_launch / 1e9)},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk.summary(), "kernel_digest": kernel_source_digest()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(x, dev, stream, steps, kda):
+    """Host inputs -> device -> kernel -> host outputs, timed with CUDA events."""
+    import torch
+    pin = lambda t: None if t is None else t.detach().to("cpu").pin_memory()  # noqa: E731
+    host = {"q": pin(x.q), "k": pin(x.k), "v": pin(x.v), "gate_logits": pin(x.a),
+            "beta": pin(x.beta), "h0": pin(x.h0), "cu_seqlens": pin(x.cu_seqlens)}
+    h_out = torch.empty((x.n_tok, x.n_heads, x.d_v), dtype=x.dtype).pin_memory()
+    h_hf = torch.empty((x.n_seq, x.n_heads, x.d_k, x.d_v), dtype=torch.float32).pin_memory()
+    devb = {k: torch.empty_like(v, device=dev) if v is not None else None
+            for k, v in host.items()}
+    devb["out"] = torch.empty(h_out.shape, dtype=x.dtype, device=dev)
+    devb["h_final"] = torch.empty(h_hf.shape, dtype=torch.float32, device=dev)
+
+    def call():
+        kda.chunk_fwd_from_host(host["q"], host["k"], host["v"], host["gate_logits"],
+                                host["beta"], host["h0"], host["cu_seqlens"], h_out, h_hf,
+                                devb, stream)
+    call()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = h_out.numel() * h_out.element_size() + h_hf.numel() * 4
+    return {"value": round(x.n_tok / (ms * 1e-3), 1), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "api": "kda_chunk_fwd_from_host (pinned host buffers)"}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, each step a bounded
+    prefix sample of the same workload, reported in the same unit."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    import kda_inputs as K
+    # the same recipe, generated on the host only up to the longest prefix sampled
+    x = K.make_workload(args.workload, "cpu", max_len=16384)
+    tokens = 512
+    # size one step to about a second of host work
+    while True:
+        dt, th, threads = oracle_sample(x, tokens)
+        if dt > 0.5 or tokens >= max(x.lengths()):
+            break
+        tokens = min(tokens * 2, max(x.lengths()))
+    for _ in range(args.warmup):
+        oracle_sample(x, tokens)
+    t0 = time.perf_counter()
+    total_th = 0
+    for _ in range(args.steps):
+        _, th, threads = oracle_sample(x, tokens)
+        total_th += th
+    el = time.perf_counter() - t0
+    value = total_th / x.n_heads / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": x.name, "heads": x.n_heads, "d_k": x.d_k, "d_v": x.d_v,
+                       "chunk": 16},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"first {tokens} tokens of every sequence, all "
+                                       f"{x.n_heads} heads, per step"},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    _ = torch
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=3, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+"""GB300 (sm_103a) chunked forward pass of gated delta-rule linear attention with the
+lower-bounded decay g = -5*sigmoid(a) (Kimi Delta Attention style).
+
+This package is a thin ctypes binding of the C ABI in ``include/kda.h``: it checks
+tensor metadata, passes raw pointers and the current CUDA stream, and allocates
+outputs with torch. Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path. If the compiled library is missing, every call raises.
+
+    out, h_final = chunk_fwd(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None)
+
+Shapes (packed, token-major, contiguous): q, k, gate_logits [N, H, d_k]; v [N, H, d_v];
+beta [N, H]; h0 / h_final [n_seq, H, d_k, d_v] fp32; cu_seqlens int32 [n_seq + 1]
+(None = one sequence of N tokens). q/k/v/out are bf16 or fp32; gate_logits, beta and
+the states are fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build_mod
+
+__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "load_library",
+           "kernel_launch_count", "read_device_flags",
+           "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA"}
+KDA_F32, KDA_BF16 = 0, 1
+EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
+                    "kda_kernel_launch_count", "kda_read_device_flags", "kda_chunk_fwd",
+                    "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+
+
+def library_path() -> str:
+    """The in-tree build, unless KDA_GB300_LIBRARY names another build of the same
+    library (for A/B comparisons of kernel variants)."""
+    return os.environ.get("KDA_GB300_LIBRARY") or _build_mod.LIB
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``libkda_gb300.so``. Raises if it is absent (unless asked to build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"CUDA library {path} is not built; run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            _build_mod.build()
+        lib = ctypes.CDLL(path)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        fwd_args = [P] * 9 + [I64, I32, I32, I32, I32, ctypes.c_int, P]
+        for name in ("kda_chunk_fwd", "kda_chunk_fwd_simt"):
+            fn = getattr(lib, name)
+            fn.argtypes = fwd_args
+            fn.restype = ctypes.c_int
+        lib.kda_chunk_fwd_from_host.argtypes = [P] * 18 + [I64, I32, I32, I32, I32,
+                                                          ctypes.c_int, P]
+        lib.kda_chunk_fwd_from_host.restype = ctypes.c_int
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_version.restype = ctypes.c_int
+        lib.kda_kernel_launch_count.argtypes = []
+        lib.kda_kernel_launch_count.restype = ctypes.c_uint64
+        lib.kda_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, P]
+        lib.kda_read_device_flags.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(lib, status: int):
+    if status != 0:
+        raise KDAError(status, lib.kda_last_error().decode() or
+                       lib.kda_status_string(status).decode())
+
+
+def _ptr(t):
+    # an empty tensor has no meaningful address: pass NULL (the ABI needs none then)
+    return None if t is None or t.numel() == 0 else ctypes.c_void_p(t.data_ptr())
+
+
+def _dims(q, k, v, gate_logits, beta, h0, cu_seqlens, device_check=True):
+    import torch
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, d_k] (packed, token-major)")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q/k/v must be bfloat16 or float32")
+    for name, t, shape, dt in (("k", k, (N, H, dk), q.dtype), ("v", v, (N, H, dv), q.dtype),
+                               ("gate_logits", gate_logits, (N, H, dk), torch.float32),
+                               ("beta", beta, (N, H), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt:
+            raise ValueError(f"{name} must be {dt} with shape {shape}, got "
+                             f"{t.dtype} {tuple(t.shape)}")
+    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    if h0 is not None and (tuple(h0.shape) != (n_seq, H, dk, dv) or h0.dtype != torch.float32):
+        raise ValueError(f"h0 must be float32 with shape {(n_seq, H, dk, dv)}")
+    tensors = [q, k, v, gate_logits, beta, h0, cu_seqlens]
+    for t in tensors:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if device_check and t is not None and t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+    return N, H, dk, dv, n_seq
+
+
+def _forward(symbol, q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=None,
+             h_final=None, output_final_state=True):
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("chunk_fwd runs on CUDA tensors only (there is no CPU path)")
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if h_final is None and output_final_state:
+        h_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = getattr(lib, symbol)(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta),
+                              _ptr(h0), _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
+                              N, n_seq, H, dk, dv,
+                              KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+                              ctypes.c_void_p(stream))
+    _check(lib, st)
+    return out, h_final
+
+
+def chunk_fwd(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=None,
+              h_final=None, output_final_state=True):
+    """Chunked KDA forward through ``kda_chunk_fwd``. Returns ``(out, h_final)``;
+    ``h_final`` is None when ``output_final_state`` is False."""
+    return _forward("kda_chunk_fwd", q, k, v, gate_logits, beta, h0, cu_seqlens, out=out,
+                    h_final=h_final, output_final_state=output_final_state)
+
+
+def chunk_fwd_simt(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=None,
+                   h_final=None, output_final_state=True):
+    """Same operation on the fp32 SIMT kernel (``kda_chunk_fwd_simt``)."""
+    return _forward("kda_chunk_fwd_simt", q, k, v, gate_logits, beta, h0, cu_seqlens,
+                    out=out, h_final=h_final, output_final_state=output_final_state)
+
+
+def chunk_fwd_from_host(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final,
+                        dev: dict, stream=None):
+    """End-to-end call on host tensors through ``kda_chunk_fwd_from_host``.
+
+    ``q ... cu_seqlens`` are CPU tensors (pinned for asynchronous copies); ``out`` and
+    ``h_final`` are CPU tensors that receive the results (``h_final`` may be None).
+    ``dev`` holds the caller's device buffers with keys q, k, v, gate_logits, beta, h0,
+    cu_seqlens, out, h_final. The call only queues work on ``stream`` (default: the
+    current stream); synchronise before reading ``out``.
+    """
+    import torch
+    lib = load_library()
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens,
+                                device_check=False)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev["q"].device)
+    st = lib.kda_chunk_fwd_from_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0),
+        _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
+        _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["gate_logits"]),
+        _ptr(dev["beta"]), _ptr(dev.get("h0")), _ptr(dev["cu_seqlens"]),
+        _ptr(dev["out"]), _ptr(dev.get("h_final")),
+        N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+        ctypes.c_void_p(stream.cuda_stream))
+    _check(lib, st)
+    return out, h_final
+
+
+def kernel_launch_count() -> int:
+    """Kernels the library has launched in this process (``kda_kernel_launch_count``)."""
+    return int(load_library().kda_kernel_launch_count())
+
+
+def read_device_flags(reset: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the library's device status word (bit 0: a
+    pipeline wait in the tensor-core kernel timed out). Clears it when ``reset``."""
+    import torch
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    v = ctypes.c_uint32(0)
+    _check(lib, lib.kda_read_device_flags(ctypes.byref(v), int(reset),
+                                          ctypes.c_void_p(stream.cuda_stream)))
+    return int(v.value)

@@ -1,0 +1,188 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument validation, kernel
+// choice and launch. Holds no arithmetic of the method.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <string>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+kda_status fail(kda_status s, const std::string &why) {
+    g_last_error = why;
+    return s;
+}
+
+kda_status ok() {
+    g_last_error.clear();
+    return KDA_OK;
+}
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+kda_status validate(const kda::FwdArgs &a, int dtype) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "dtype must be KDA_F32 or KDA_BF16");
+    if (a.n_tok < 0 || a.n_seq < 0 || a.n_heads <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_tok and n_seq must be >= 0, n_heads > 0");
+    if (a.d_k <= 0 || a.d_v <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "d_k and d_v must be positive");
+    if (a.d_k > 128 || a.d_v > 128)
+        return fail(KDA_ERR_UNSUPPORTED, "d_k and d_v above 128 are not built");
+    if (a.n_tok > 0 && a.n_seq == 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_tok > 0 needs at least one sequence");
+    if (a.n_seq > 0 && a.cu_seqlens == nullptr)
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (a.n_tok > 0 && (!a.q || !a.k || !a.v || !a.a || !a.beta || !a.out))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, gate_logits, beta and out are required");
+    if ((int64_t)a.n_seq * a.n_heads > 0x7fffffffLL)
+        return fail(KDA_ERR_INVALID_ARG, "n_seq * n_heads exceeds 2^31 - 1");
+    const void *ptrs[] = {a.q, a.k, a.v, a.a, a.beta, a.h0, a.cu_seqlens, a.out, a.h_final};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    return KDA_OK;
+}
+
+kda::FwdArgs pack(const void *q, const void *k, const void *v, const float *a,
+                  const float *beta, const float *h0, const int32_t *cu, void *out,
+                  float *h_final, int64_t n_tok, int32_t n_seq, int32_t n_heads,
+                  int32_t d_k, int32_t d_v, kda_dtype dtype) {
+    kda::FwdArgs p;
+    p.q = q; p.k = k; p.v = v; p.a = a; p.beta = beta; p.h0 = h0; p.cu_seqlens = cu;
+    p.out = out; p.h_final = h_final;
+    p.n_tok = n_tok; p.n_seq = n_seq; p.n_heads = n_heads; p.d_k = d_k; p.d_v = d_v;
+    p.bf16 = dtype == KDA_BF16;
+    return p;
+}
+
+kda_status launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess)
+        return fail(KDA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    return ok();
+}
+
+enum class Path { kAuto, kSimt };
+
+kda_status run(const kda::FwdArgs &p, kda_dtype dtype, void *stream, Path path) {
+    kda_status s = validate(p, dtype);
+    if (s != KDA_OK) return s;
+    if (p.n_seq == 0) return ok();
+    cudaStream_t st = (cudaStream_t)stream;
+    if (path == Path::kAuto && kda::tc_supported(p))
+        return launched(kda::launch_tc(p, st), "tensor-core kernel launch");
+    return launched(kda::launch_simt(p, st), "SIMT kernel launch");
+}
+
+}  // namespace
+
+namespace kda {
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace kda
+
+extern "C" {
+
+uint64_t kda_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int kda_version(void) { return 100; }
+
+const char *kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: dtype or head dimension not built";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+    }
+    return "unknown kda_status";
+}
+
+const char *kda_last_error(void) { return g_last_error.c_str(); }
+
+kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
+    if (!flags) return fail(KDA_ERR_INVALID_ARG, "flags is NULL");
+    unsigned int v = 0;
+    cudaError_t e = kda::read_device_flags(&v, reset != 0, (cudaStream_t)stream);
+    if (e != cudaSuccess) return launched(e, "reading the device status word");
+    *flags = v;
+    return ok();
+}
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *gate_logits, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, void *out, float *h_final,
+                         int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                         int32_t d_v, kda_dtype dtype, void *stream) {
+    return run(pack(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final, n_tok, n_seq,
+                    n_heads, d_k, d_v, dtype),
+               dtype, stream, Path::kAuto);
+}
+
+kda_status kda_chunk_fwd_simt(const void *q, const void *k, const void *v,
+                              const float *gate_logits, const float *beta,
+                              const float *h0, const int32_t *cu_seqlens, void *out,
+                              float *h_final, int64_t n_tok, int32_t n_seq,
+                              int32_t n_heads, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                              void *stream) {
+    return run(pack(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final, n_tok, n_seq,
+                    n_heads, d_k, d_v, dtype),
+               dtype, stream, Path::kSimt);
+}
+
+kda_status kda_chunk_fwd_from_host(
+    const void *host_q, const void *host_k, const void *host_v,
+    const float *host_gate_logits, const float *host_beta, const float *host_h0,
+    const int32_t *host_cu_seqlens, void *host_out, float *host_h_final, void *dev_q,
+    void *dev_k, void *dev_v, float *dev_gate_logits, float *dev_beta, float *dev_h0,
+    int32_t *dev_cu_seqlens, void *dev_out, float *dev_h_final, int64_t n_tok,
+    int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v, kda_dtype dtype,
+    void *stream) {
+    kda::FwdArgs p = pack(dev_q, dev_k, dev_v, dev_gate_logits, dev_beta,
+                          host_h0 ? dev_h0 : nullptr, dev_cu_seqlens, dev_out,
+                          host_h_final ? dev_h_final : nullptr, n_tok, n_seq, n_heads, d_k,
+                          d_v, dtype);
+    kda_status s = validate(p, dtype);
+    if (s != KDA_OK) return s;
+    if (n_seq > 0 && !host_cu_seqlens)
+        return fail(KDA_ERR_INVALID_ARG, "host_cu_seqlens is NULL");
+    if (n_tok > 0 && (!host_q || !host_k || !host_v || !host_gate_logits || !host_beta ||
+                      !host_out))
+        return fail(KDA_ERR_INVALID_ARG, "host input/output pointers are required");
+    if ((host_h0 && !dev_h0) || (host_h_final && !dev_h_final))
+        return fail(KDA_ERR_INVALID_ARG, "a host state buffer needs its device buffer");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t es = dtype == KDA_BF16 ? 2 : 4;
+    const size_t nk = (size_t)n_tok * n_heads * d_k, nv = (size_t)n_tok * n_heads * d_v;
+    const size_t ns = (size_t)n_seq * n_heads * d_k * d_v;
+    struct Copy { void *dst; const void *src; size_t bytes; };
+    const Copy in[] = {{dev_q, host_q, nk * es},
+                       {dev_k, host_k, nk * es},
+                       {dev_v, host_v, nv * es},
+                       {dev_gate_logits, host_gate_logits, nk * 4},
+                       {dev_beta, host_beta, (size_t)n_tok * n_heads * 4},
+                       {dev_h0, host_h0, host_h0 ? ns * 4 : 0},
+                       {dev_cu_seqlens, host_cu_seqlens, n_seq > 0 ? (size_t)(n_seq + 1) * 4 : 0}};
+    for (const Copy &c : in) {
+        if (c.bytes == 0) continue;
+        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return launched(e, "host-to-device copy");
+    }
+    s = run(p, dtype, stream, Path::kAuto);
+    if (s != KDA_OK) return s;
+    if (nv > 0) {
+        cudaError_t e = cudaMemcpyAsync(host_out, dev_out, nv * es, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return launched(e, "device-to-host copy");
+    }
+    if (host_h_final && ns > 0) {
+        cudaError_t e = cudaMemcpyAsync(host_h_final, dev_h_final, ns * 4,
+                                        cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return launched(e, "device-to-host copy");
+    }
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// Internal declarations shared by the CUDA translation units of the library.
+// Not part of the C ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Tile length in tokens and the lower bound of the log-decay. Both are fixed by
+// the method: a 16-token tile is co-designed with g_min = -5 so that every
+// in-tile factor exp(+-G) stays within exp(+-80) ("From Numerical Stability to
+// Load Balancing", §2.2-2.3).
+constexpr int kChunk = 16;
+constexpr float kGMin = -5.0f;
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    const float *a, *beta, *h0;
+    const int32_t *cu_seqlens;
+    void *out;
+    float *h_final;
+    int64_t n_tok;
+    int32_t n_seq, n_heads, d_k, d_v;
+    bool bf16;  // q/k/v/out element type: bf16 when true, fp32 otherwise
+};
+
+// Each returns cudaSuccess or the launch error; all work is queued on `stream`.
+cudaError_t launch_simt(const FwdArgs &args, cudaStream_t stream);
+cudaError_t launch_tc(const FwdArgs &args, cudaStream_t stream);
+
+// True when the tensor-core kernel handles this shape and dtype.
+bool tc_supported(const FwdArgs &args);
+
+// Copies (and optionally clears) the device-side status word; synchronises stream.
+cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
+
+// Adds n to the process-wide kernel launch counter (kda_kernel_launch_count).
+void count_launches(uint64_t n);
+
+}  // namespace kda

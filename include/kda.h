@@ -1,0 +1,153 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked forward pass of gated delta-rule
+ * linear attention with the lower-bounded per-key-channel decay (Kimi Delta
+ * Attention style).
+ *
+ * The operation, per sequence and head, with state S in R^{d_k x d_v}:
+ *
+ *   g_t  = g_min * sigmoid(a_t),  g_min = -5           (per key channel)
+ *   S   <- Diag(exp g_t) S
+ *   S   <- S + beta_t k_t (v_t - S^T k_t)^T
+ *   o_t  = d_k^-1/2 S^T q_t                              (state after the write)
+ *
+ * Sources: the bounded gate g = g_min * sigmoid(.) with g_min = -5 and its range
+ * [g_min, 0) -- "Demystifying Trillion-Parameter MoE Models", Breakthrough 1 §2,
+ * and "From Numerical Stability to Load Balancing", §2.2. The state that forgets
+ * through a cumulative decay and writes key-value outer products, computed with a
+ * chunked strategy in which chunks run serially through the state recurrence while
+ * the inside of a chunk is matrix products scaled by exp(G_i - G_j) -- the same
+ * page, §2.1. Chunks of 16 tokens, whose worst-case log-decay span 16 x (-5) = -80
+ * keeps exp(+-G) representable in BF16 so the diagonal tile stays a dense
+ * tensor-core product with no per-position branch -- the same page, §2.2-2.3, and
+ * "Architecting Long-Context LLMs: From Sparse Attention to Stable MoE in
+ * Production", §2.2-2.3. The delta-rule form of the write is what those pages call
+ * "Kimi Delta Attention" / "Delta networks"; g_min = -5 and the 16-token chunk are
+ * compile-time constants of this library, not parameters.
+ *
+ * Memory layout (all buffers contiguous, row-major, token-major, owned by the
+ * caller; the library allocates nothing and keeps no state between calls):
+ *   q, k          [n_tok, n_heads, d_k]   dtype (KDA_BF16 or KDA_F32)
+ *   v             [n_tok, n_heads, d_v]   dtype
+ *   gate_logits   [n_tok, n_heads, d_k]   float32  (a; the gate is -5*sigmoid(a))
+ *   beta          [n_tok, n_heads]        float32
+ *   h0            [n_seq, n_heads, d_k, d_v] float32, or NULL for a zero state
+ *   cu_seqlens    [n_seq + 1] int32, device memory: sequence n owns tokens
+ *                 [cu_seqlens[n], cu_seqlens[n+1]); cu_seqlens[0] = 0,
+ *                 non-decreasing, cu_seqlens[n_seq] = n_tok. Empty sequences are
+ *                 allowed (their final state is h0). Sequences need not be
+ *                 multiples of 16 tokens.
+ *   out           [n_tok, n_heads, d_v]   dtype
+ *   h_final       [n_seq, n_heads, d_k, d_v] float32, or NULL to skip writing it
+ * Device pointers must be 16-byte aligned. out and h_final must not overlap any
+ * input. The state and all accumulation are float32.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream). The return value reports argument validation and launch
+ * errors only; device-side faults surface at the next synchronising CUDA call.
+ * Calls are thread-safe (the only mutable global is the launch counter below). cu_seqlens is read on the
+ * device only, so its contents are not validated; breaking the rules above is
+ * undefined behaviour.
+ */
+#ifndef KDA_GB300_H_
+#define KDA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, bad layout */
+    KDA_ERR_UNSUPPORTED = 2, /* valid but not built: dtype or head dimension */
+    KDA_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Library version as an integer MAJOR*10000 + MINOR*100 + PATCH. */
+int kda_version(void);
+
+/* Static description of a status code. Never NULL. */
+const char *kda_status_string(kda_status status);
+
+/* Human-readable detail of the last non-OK status returned on the calling host
+ * thread (empty string if none). Valid until the next call on that thread. */
+const char *kda_last_error(void);
+
+/* Number of CUDA kernels this library has launched in the process so far (all
+ * threads, all devices). A diagnostic counter for benchmarks and tests: the only
+ * mutable global of the library, updated atomically, never read by a kernel. */
+uint64_t kda_kernel_launch_count(void);
+
+/*
+ * kda_read_device_flags -- synchronise `stream`, then copy the library's device-side
+ * status word into *flags (and clear it when `reset` is non-zero). Bit 0 set: a
+ * pipeline wait inside the tensor-core kernel exceeded its time limit (about two
+ * seconds); that kernel then stopped early and its outputs are unspecified. A
+ * healthy run leaves the word 0. Returns KDA_ERR_INVALID_ARG for a NULL `flags`,
+ * KDA_ERR_CUDA if the copy or the synchronisation fails.
+ */
+kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream);
+
+/*
+ * kda_chunk_fwd -- the chunked forward pass (all of the operation above).
+ *
+ * Kernel choice is made from the arguments, not from any global setting:
+ *   dtype KDA_BF16 with d_k = d_v = 128: the tensor-core kernel (bf16 operands,
+ *     fp32 accumulation and state) on thread-block clusters;
+ *   any other supported case (KDA_F32, or 1 <= d_k, d_v <= 128): the fp32 SIMT
+ *     kernel. Both compute the same chunked algebra.
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG (null required pointer, n_tok < 0,
+ * n_seq < 0, n_heads <= 0, misaligned pointer), KDA_ERR_UNSUPPORTED (dtype or
+ * d_k/d_v outside 1..128) or KDA_ERR_CUDA (launch failed; see kda_last_error).
+ * n_seq = 0 or n_tok = 0 with all-empty sequences is valid (h_final = h0 is still
+ * written when requested).
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *gate_logits, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, void *out, float *h_final,
+                         int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                         int32_t d_v, kda_dtype dtype, void *stream);
+
+/*
+ * kda_chunk_fwd_simt -- the same operation forced onto the fp32 SIMT kernel
+ * (fp32 FMA arithmetic throughout, bf16 or fp32 I/O). Same arguments, layout,
+ * ownership and errors as kda_chunk_fwd. Used to cross-check the tensor-core
+ * kernel and where bf16 operand rounding is not wanted.
+ */
+kda_status kda_chunk_fwd_simt(const void *q, const void *k, const void *v,
+                              const float *gate_logits, const float *beta,
+                              const float *h0, const int32_t *cu_seqlens, void *out,
+                              float *h_final, int64_t n_tok, int32_t n_seq,
+                              int32_t n_heads, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                              void *stream);
+
+/*
+ * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
+ * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
+ * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs
+ * kda_chunk_fwd on them, and copies out (and h_final when host_h_final is not
+ * NULL) back to host memory on the same stream. cu_seqlens is given on the host
+ * (host_cu_seqlens, int32 [n_seq + 1]) and copied to dev_cu_seqlens. host_h0 /
+ * dev_h0 may both be NULL (zero start state); dev_h_final may be NULL only when
+ * host_h_final is NULL. Nothing is allocated. The call returns after queuing; the
+ * host buffers must stay valid until the stream reaches the last copy. Errors as
+ * for kda_chunk_fwd, plus KDA_ERR_CUDA when a copy cannot be queued.
+ */
+kda_status kda_chunk_fwd_from_host(
+    const void *host_q, const void *host_k, const void *host_v,
+    const float *host_gate_logits, const float *host_beta, const float *host_h0,
+    const int32_t *host_cu_seqlens, void *host_out, float *host_h_final,
+    void *dev_q, void *dev_k, void *dev_v, float *dev_gate_logits, float *dev_beta,
+    float *dev_h0, int32_t *dev_cu_seqlens, void *dev_out, float *dev_h_final,
+    int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
+    kda_dtype dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H_ */

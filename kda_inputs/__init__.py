@@ -146,12 +146,17 @@ def workload_lengths(index: int, gen: Optional[torch.Generator] = None) -> list:
     raise ValueError(f"unknown workload {index}")
 
 
-def make_workload(index: int, device="cpu", seed: Optional[int] = None) -> KDAInputs:
-    """Workload ``index`` (0..4) exactly as listed in the module docstring."""
+def make_workload(index: int, device="cpu", seed: Optional[int] = None,
+                  max_len: Optional[int] = None) -> KDAInputs:
+    """Workload ``index`` (0..4) exactly as listed in the module docstring.
+    ``max_len`` truncates every sequence (same recipe, fewer tokens), for host-side
+    samples of the large workloads."""
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(SEED_BASE + index if seed is None else seed)
     lengths = workload_lengths(index, gen)
+    if max_len is not None:
+        lengths = [min(L, max_len) for L in lengths]
     name = WORKLOADS[index]
     if index == 0:
         return make_inputs(lengths, 1, 16, 16, dtype=torch.float32, device=device,

@@ -1,0 +1,87 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol that
+``include/kda.h`` declares, and rejects bad arguments on the host before any CUDA call.
+
+Only calls that fail host validation (or have nothing to do) are made here, so no
+pointer is ever dereferenced and no kernel is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_linear_attention_kda_gb300 as kda
+from chunked_linear_attention_kda_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(kda.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_has_no_torch_or_python_dependency():
+    out = os.popen(f"ldd {kbuild.LIB}").read()
+    assert "torch" not in out and "python" not in out
+
+
+def test_version_and_status_strings(lib):
+    assert lib.kda_version() >= 100
+    for s in range(4):
+        assert lib.kda_status_string(s).decode().startswith(kda.STATUS[s])
+    assert lib.kda_status_string(99) == b"unknown kda_status"
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced by these calls
+
+
+def call(lib, *, q=FAKE, k=FAKE, v=FAKE, a=FAKE, beta=FAKE, h0=None, cu=FAKE, out=FAKE,
+         hf=None, n_tok=64, n_seq=1, H=2, dk=128, dv=128, dtype=1, symbol="kda_chunk_fwd"):
+    P = ctypes.c_void_p
+    return getattr(lib, symbol)(P(q), P(k), P(v), P(a), P(beta), P(h0), P(cu), P(out),
+                                P(hf), n_tok, n_seq, H, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("symbol", ["kda_chunk_fwd", "kda_chunk_fwd_simt"])
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(a=None), 1),
+    (dict(beta=None), 1), (dict(out=None), 1), (dict(cu=None), 1),
+    (dict(n_tok=-1), 1), (dict(n_seq=-1), 1), (dict(H=0), 1), (dict(dk=0), 1),
+    (dict(dv=-3), 1), (dict(n_seq=0), 1),          # tokens but no sequence
+    (dict(dk=129), 2), (dict(dv=256), 2), (dict(dtype=7), 2),
+    (dict(q=FAKE + 2), 1), (dict(out=FAKE + 8), 1), (dict(hf=FAKE + 4), 1),
+])
+def test_host_validation(lib, symbol, kw, status):
+    st = call(lib, symbol=symbol, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_nothing_to_do_is_ok(lib):
+    assert call(lib, n_tok=0, n_seq=0) == 0
+    assert lib.kda_last_error() == b""
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(16, 1, 16)
+    with pytest.raises(ValueError):
+        kda.chunk_fwd(x, x, x, x, torch.zeros(16, 1))

@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs, element by element in rel-L2 over whole tensors.
+
+Bars: rel-L2 <= 1e-4 for fp32 inputs and <= 1e-2 for bf16 inputs, on outputs and on
+final states, plus finiteness everywhere. Both kernels are checked: the automatic
+choice (tensor-core kernel for bf16 with d_k = d_v = 128) and the fp32 SIMT kernel.
+"""
+import pytest
+import torch
+
+import kda_inputs as K
+from tests.gpu_helpers import TOL, assert_finite, gpu_forward, oracle_forward, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+PATHS = ["auto", "simt"]
+
+
+def check(x, path, heads=None, tol=None):
+    out, hf = gpu_forward(x, path=path)
+    assert_finite(out, hf)
+    o_ref, h_ref = oracle_forward(x, heads=heads)
+    tol = TOL[x.dtype] if tol is None else tol
+    eo = rel_l2(to_np(out, heads), o_ref)
+    eh = rel_l2(to_np(hf, heads), h_ref)
+    assert eo <= tol and eh <= tol, f"{x.name} [{path}]: out {eo:.3e}, h_final {eh:.3e}"
+    return eo, eh
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_workload0_tiny_fp32(path):
+    check(K.make_workload(0, DEV), path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_workload1_single_sequence_bf16(path):
+    check(K.make_workload(1, DEV), path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_workload2_decay_at_the_bound(path):
+    x = K.make_workload(2, DEV)
+    check(x, path)
+
+
+def test_workload3_context_64k_sampled_heads():
+    """Full 64K-token, 32-head workload on the GPU; the oracle checks 4 whole heads."""
+    check(K.make_workload(3, DEV), "auto", heads=[0, 9, 18, 31])
+
+
+def test_workload4_packed_varlen_1m():
+    """Full packed workload (16 sequences of 4K-131K tokens plus one of 1M) on the
+    GPU in one call. By causality the outputs of the first 65536 tokens of every
+    sequence depend on nothing after them, so the oracle checks those prefixes (two
+    heads); the final states are checked by a second call on the prefix packing."""
+    x = K.make_workload(4, DEV)
+    out, hf = gpu_forward(x)
+    assert_finite(out, hf)
+    heads = [3, 12]
+    px = K.prefix(x, 65536)
+    o_ref, h_ref = oracle_forward(px, heads=heads)
+    rows = torch.cat([torch.arange(s, s + min(e - s, 65536), device=out.device)
+                      for s, e in zip(x.cu_host[:-1], x.cu_host[1:])])
+    eo = rel_l2(to_np(out.index_select(0, rows), heads), o_ref)
+    pout, phf = gpu_forward(px)
+    eh = rel_l2(to_np(phf, heads), h_ref)
+    ep = rel_l2(to_np(pout, heads), o_ref)
+    assert max(eo, eh, ep) <= TOL[torch.bfloat16], (eo, eh, ep)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ragged_lengths_and_states(path, dtype):
+    lengths = [0, 1, 15, 16, 17, 33, 0, 100, 257]
+    x = K.make_inputs(lengths, 3, 128, 128, dtype=dtype, device=DEV, seed=7, h0_std=0.1)
+    check(x, path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("gate", ["bound", "no_decay"])
+def test_pinned_gates(path, gate):
+    """a = +inf gives g = -5 exactly on every channel (each chunk spans exactly -80);
+    a = -inf gives g = 0 (the plain delta rule). Neither may produce NaN/Inf."""
+    x = K.make_inputs([300, 77], 4, 128, 128, device=DEV, seed=8, h0_std=0.1)
+    x.a.fill_(float("inf") if gate == "bound" else float("-inf"))
+    check(x, path)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (64, 32), (32, 128), (128, 64), (7, 5)])
+def test_other_head_dims_fp32(dk, dv):
+    x = K.make_inputs([40, 1, 129], 2, dk, dv, dtype=torch.float32, device=DEV, seed=9,
+                      h0_std=0.1)
+    check(x, "auto")
+
+
+def test_all_sequences_empty_keeps_h0():
+    x = K.make_inputs([0, 0], 2, 128, 128, device=DEV, seed=10, h0_std=0.1)
+    out, hf = gpu_forward(x)
+    assert out.numel() == 0 and torch.equal(hf, x.h0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_resume_equals_one_run(path):
+    """Running tokens [0, t1) then [t1, T) from the first call's final state equals one
+    call over [0, T) (t1 not a multiple of 16)."""
+    T, t1 = 1000, 333
+    x = K.make_inputs([T], 4, 128, 128, device=DEV, seed=11, h0_std=0.1)
+    out, hf = gpu_forward(x, path=path)
+    sl = lambda t, a, b: t[a:b].contiguous()  # noqa: E731
+    xa = K.KDAInputs("a", sl(x.q, 0, t1), sl(x.k, 0, t1), sl(x.v, 0, t1), sl(x.a, 0, t1),
+                     sl(x.beta, 0, t1), x.h0, torch.tensor([0, t1], dtype=torch.int32,
+                                                           device=DEV), [0, t1], x.dtype)
+    oa, ha = gpu_forward(xa, path=path)
+    xb = K.KDAInputs("b", sl(x.q, t1, T), sl(x.k, t1, T), sl(x.v, t1, T), sl(x.a, t1, T),
+                     sl(x.beta, t1, T), ha, torch.tensor([0, T - t1], dtype=torch.int32,
+                                                         device=DEV), [0, T - t1], x.dtype)
+    ob, hb = gpu_forward(xb, path=path)
+    assert rel_l2(to_np(torch.cat([oa, ob])), to_np(out)) < 1e-2
+    assert rel_l2(to_np(hb), to_np(hf)) < 1e-3
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_packing_is_bitwise_equal_to_separate_calls(path):
+    lengths = [37, 0, 160, 5]
+    x = K.make_inputs(lengths, 2, 128, 128, device=DEV, seed=12, h0_std=0.1)
+    out, hf = gpu_forward(x, path=path)
+    for n, L in enumerate(lengths):
+        s, e = x.cu_host[n], x.cu_host[n + 1]
+        xn = K.KDAInputs("n", x.q[s:e].contiguous(), x.k[s:e].contiguous(),
+                         x.v[s:e].contiguous(), x.a[s:e].contiguous(),
+                         x.beta[s:e].contiguous(), x.h0[n:n + 1].contiguous(),
+                         torch.tensor([0, L], dtype=torch.int32, device=DEV), [0, L],
+                         x.dtype)
+        on, hn = gpu_forward(xn, path=path)
+        assert torch.equal(on, out[s:e]) and torch.equal(hn[0], hf[n])
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic(path):
+    x = K.make_inputs([500, 64], 4, 128, 128, device=DEV, seed=13)
+    o1, h1 = gpu_forward(x, path=path)
+    o2, h2 = gpu_forward(x, path=path)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_no_final_state_requested():
+    x = K.make_inputs([100], 2, 128, 128, device=DEV, seed=14)
+    out, hf = gpu_forward(x, want_state=False)
+    assert hf is None
+    o2, _ = gpu_forward(x)
+    assert torch.equal(out, o2)
