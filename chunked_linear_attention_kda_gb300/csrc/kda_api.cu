@@ -43,9 +43,16 @@ kda_status validate(const kda::FwdArgs &a, int dtype) {
         return fail(KDA_ERR_INVALID_ARG, "q, k, v, gate_logits, beta and out are required");
     if ((int64_t)a.n_seq * a.n_heads > 0x7fffffffLL)
         return fail(KDA_ERR_INVALID_ARG, "n_seq * n_heads exceeds 2^31 - 1");
-    const void *ptrs[] = {a.q, a.k, a.v, a.a, a.beta, a.h0, a.cu_seqlens, a.out, a.h_final};
-    for (const void *p : ptrs)
-        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    // tiles moved by TMA or 16-byte vector accesses need 16-byte alignment; the rest
+    // are read and written as 4-byte scalars
+    const void *tiles[] = {a.q, a.k, a.v, a.a, a.out};
+    for (const void *p : tiles)
+        if (!aligned16(p))
+            return fail(KDA_ERR_INVALID_ARG, "q, k, v, gate_logits and out must be 16-byte aligned");
+    const void *scalars[] = {a.beta, a.h0, a.cu_seqlens, a.h_final};
+    for (const void *p : scalars)
+        if (((uintptr_t)p & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "beta, h0, cu_seqlens and h_final must be 4-byte aligned");
     return KDA_OK;
 }
 

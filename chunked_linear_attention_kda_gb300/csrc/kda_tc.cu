@@ -49,58 +49,104 @@ namespace kda {
 
 __device__ unsigned int g_device_flags;  // bit 0: a pipeline wait exceeded its limit
 
+// Phase timestamps (SM clock) of the first cluster, first 64 chunks: a profiling aid
+// compiled only with -DKDA_TC_TRACE; the default build has no trace code. Stamps go to
+// shared memory and are copied out when the CTA finishes, so that tracing adds no
+// global stores to the pipeline.
+#ifdef KDA_TC_TRACE
+__device__ long long g_trace[4][64][16];
+#define KDA_TRACE(n, slot)                                                              \
+    do {                                                                                \
+        if ((n) < 64)                                                                   \
+            reinterpret_cast<long long *>(sm + SM_TRACE)[(n) * 16 + (slot)] = clock64(); \
+    } while (0)
+#else
+#define KDA_TRACE(n, slot) \
+    do {                   \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int D = 128;          // d_k = d_v
 constexpr int C = kChunk;       // 16 tokens
 constexpr int kCS = 4;          // CTAs per (sequence, head) = cluster size
 constexpr int VB = D / kCS;     // value columns per CTA (32)
-constexpr int NSW = VB / 16;    // state warps per CTA (2)
+constexpr int NSW = VB / 16;    // state warps per CTA (2), and as many output warps
 constexpr int NPW = 4;          // prologue warps
-constexpr int kThreads = 32 * (1 + NPW + NSW);
+constexpr int kThreads = 32 * (1 + NPW + 2 * NSW);
 constexpr int NP = 8;           // product-ring depth (multiple of kCS)
-constexpr int NR = 2;           // raw-input ring depth (owned chunks)
+constexpr int NR = 2;           // raw-input ring depth (owned chunks); prefetch distance 1
 constexpr int LDP = 136;        // pitch (elements) of 16 x 128 bf16 tiles: 272 B rows
 constexpr int LDS = 24;         // pitch of 16 x 16 bf16 tiles: 48 B rows
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (~2 s) before a wait gives up
 
 static_assert(NP % kCS == 0, "slot ownership must be static");
 
+// Channel-major 128 x 16 bf16 tiles ("[c][t]"): one 32-byte row per key channel c
+// holding its 16 tokens; the two 16-byte halves of a row swap places every four rows,
+// which keeps 8-row ldmatrix accesses free of bank conflicts without padding.
+__device__ __forceinline__ uint32_t cmaj(int c, int t0) {
+    return (uint32_t)(c * 32 + ((((t0 >> 3) ^ (c >> 2)) & 1) << 4));
+}
+constexpr int CMAJ_BYTES = D * C * 2;  // 4096
+
 // ---- shared-memory layout (bytes) ----
-constexpr int OFF_PQ = 0;                        // Q~   [16][LDP] bf16
-constexpr int OFF_PW = OFF_PQ + C * LDP * 2;     // -W   [16][LDP] bf16
-constexpr int OFF_PK = OFF_PW + C * LDP * 2;     // K'   [16][LDP] bf16
-constexpr int OFF_PTB = OFF_PK + C * LDP * 2;    // TB   [16][LDS] bf16
-constexpr int OFF_PP = OFF_PTB + C * LDS * 2;    // P    [16][LDS] bf16
-constexpr int OFF_PG = OFF_PP + C * LDS * 2;     // gamma_L [128] f32
-constexpr int SLOT_BYTES = OFF_PG + D * 4;       // 15104
+// product slot: everything the state warps need for one chunk
+constexpr int OFF_PQ = 0;                        // Q~ [c][t] bf16, channel-major
+constexpr int OFF_PW = OFF_PQ + CMAJ_BYTES;      // -W [16][LDP] bf16, token-major
+constexpr int OFF_PK = OFF_PW + C * LDP * 2;     // K' [c][t] bf16, channel-major
+constexpr int OFF_PTB = OFF_PK + CMAJ_BYTES;     // TB [16][LDS] bf16
+constexpr int OFF_PP = OFF_PTB + C * LDS * 2;    // P  [16][LDS] bf16
+constexpr int OFF_PG = OFF_PP + C * LDS * 2;     // gamma_L [128] f32, permuted (gperm)
+constexpr int SLOT_BYTES = OFF_PG + D * 4;       // 14592
 static_assert(SLOT_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 
+// raw slot: the owner's TMA tiles of one chunk plus beta
 constexpr int RAW_Q = 0, RAW_K = C * D * 2, RAW_A = 2 * C * D * 2;
-constexpr int RAW_BYTES = RAW_A + C * D * 4;     // 16384
-constexpr int V_BYTES = C * VB * 2;              // 1024
+constexpr int RAW_TMA_BYTES = RAW_A + C * D * 4;  // 16384 (q, k, a)
+constexpr int RAW_STRIDE = RAW_TMA_BYTES;
+constexpr int V_BYTES = C * VB * 2;               // 1024
+constexpr int OST_BYTES = C * 16 * 2;             // one 16 x 16 bf16 output tile
 
 constexpr int SM_RAW = 0;
-constexpr int SM_V = SM_RAW + NR * RAW_BYTES;
+constexpr int SM_V = SM_RAW + NR * RAW_STRIDE;
 constexpr int SM_PROD = SM_V + NP * V_BYTES;
-constexpr int SM_KT = SM_PROD + NP * SLOT_BYTES; // K~ [16][LDP] bf16 (prologue scratch)
-constexpr int SM_KH = SM_KT + C * LDP * 2;       // K^ [16][LDP] bf16
-constexpr int SM_A = SM_KH + C * LDP * 2;        // A  [16][16] f32
-constexpr int SM_BETA = SM_A + C * C * 4;        // beta [16] f32
-constexpr int SM_OST = SM_BETA + C * 4;          // O staging [NSW][16][LDS] bf16
-constexpr int SM_BAR = SM_OST + NSW * C * LDS * 2;
-constexpr int NBARS = 3 * NP + 2 * NR;
+constexpr int SM_KT = SM_PROD + NP * SLOT_BYTES; // K~ [c][t] (prologue scratch)
+constexpr int SM_KH = SM_KT + CMAJ_BYTES;        // K^ [c][t]
+constexpr int SM_A = SM_KH + CMAJ_BYTES;         // A  [16][16] f32
+constexpr int SM_BETA = SM_A + C * C * 4;        // beta [2][16] f32 (double buffer)
+constexpr int SM_OST = (SM_BETA + 2 * C * 4 + 127) / 128 * 128;  // output tiles [NSW][2][16][16] bf16
+constexpr int HO_LANE = 36 * 4;                   // handoff: 36 registers per lane
+constexpr int HO_BYTES = 32 * HO_LANE;            // one state -> output warp handoff
+constexpr int SM_HO = SM_OST + NSW * 2 * OST_BYTES;  // [NSW][2][32 lanes][36] u32
+constexpr int SM_BAR = SM_HO + NSW * 2 * HO_BYTES;
+constexpr int NBARS = 3 * NP + NR + 4 * NSW;
 constexpr int SM_MISC = SM_BAR + NBARS * 8;
+#ifdef KDA_TC_TRACE
+constexpr int SM_TRACE = SM_MISC + 64;
+constexpr int SMEM_BYTES = SM_TRACE + 64 * 16 * 8;
+#else
 constexpr int SMEM_BYTES = SM_MISC + 64;
-static_assert(SM_V % 128 == 0 && SM_PROD % 16 == 0 && SM_BAR % 8 == 0, "alignment");
+#endif
+static_assert(RAW_STRIDE % 128 == 0 && SM_V % 128 == 0 && SM_PROD % 128 == 0, "TMA alignment");
+static_assert(SM_KT % 16 == 0 && SM_OST % 128 == 0 && SM_BAR % 8 == 0, "alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+// gamma_L[c], c = 16 np + 8 h + 2 l4 + e, is stored at 32 l4 + 4 np + 2 h + e so that
+// the lanes holding S^T columns 2 l4 (+1, +8, +9) of every 16-column group read
+// their 32 decay factors as 8 contiguous float4
+__host__ __device__ constexpr int gperm(int c) {
+    return ((c >> 1) & 3) * 32 + (c >> 4) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
+}
 
 // barrier indices
 __host__ __device__ constexpr int B_FULL(int s) { return s; }           // products + V in
 __host__ __device__ constexpr int B_FREE(int s) { return NP + s; }      // local state warps done
 __host__ __device__ constexpr int B_CFREE(int s) { return 2 * NP + s; } // all CTAs done (owner)
 __host__ __device__ constexpr int B_RFULL(int s) { return 3 * NP + s; }
-__host__ __device__ constexpr int B_REMPTY(int s) { return 3 * NP + NR + s; }
+__host__ __device__ constexpr int B_HFULL(int w, int b) { return 3 * NP + NR + 2 * w + b; }
+__host__ __device__ constexpr int B_HEMPTY(int w, int b) { return 3 * NP + NR + 2 * NSW + 2 * w + b; }
 
 struct TcParams {
     const float *beta, *h0;
@@ -209,10 +255,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t &r0, uint32_t &r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-                 : "=r"(r0), "=r"(r1) : "r"(a));
-}
 __device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2,
                                           uint32_t r3) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};"
@@ -220,15 +262,46 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, 
 }
 // D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, flushes denormals
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {  // 1/x; 1/inf = 0
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2 e)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (lower address)
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
+                                             uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+        ::"l"(map), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_le1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Item for this cluster: sequences ordered longest first (ties by index), heads
@@ -259,7 +332,7 @@ template <bool kShare>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v,
-                  const TcParams p) {
+                  const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
     extern __shared__ __align__(128) unsigned char sm[];
     const uint32_t sbase = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -277,50 +350,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
             mbar_init(bar(B_FULL(s)), owner(s) == rank ? 2 : 1);
-            mbar_init(bar(B_FREE(s)), NSW);
-            mbar_init(bar(B_CFREE(s)), (kShare ? kCS : 1) * NSW);
+            mbar_init(bar(B_FREE(s)), 2 * NSW);  // state and output warps
+            mbar_init(bar(B_CFREE(s)), kShare ? kCS : 1);
         }
-        for (int s = 0; s < NR; ++s) {
-            mbar_init(bar(B_RFULL(s)), 1);
-            mbar_init(bar(B_REMPTY(s)), 1);
-        }
+        for (int s = 0; s < NR; ++s) mbar_init(bar(B_RFULL(s)), 1);
+        for (int w = 0; w < NSW; ++w)
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar(B_HFULL(w, b)), 1);
+                mbar_init(bar(B_HEMPTY(w, b)), 1);
+            }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+#ifdef KDA_TC_TRACE
+    for (int i = threadIdx.x; i < 64 * 16; i += blockDim.x)
+        reinterpret_cast<long long *>(sm + SM_TRACE)[i] = 0;
+#endif
     if (kShare) cluster_sync(); else __syncthreads();
 
     if (warp == 0) {
-        // ------------------------------------------------ producer (one lane)
-        if (lane == 0) {
-            int owned = 0;
-            for (int n = 0; n < nchunks; ++n) {
-                const int s = n % NP, use = n / NP;
-                if (!mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1)) break;
-                const bool mine = owner(n) == rank;
-                mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
-                tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head, t0 + n * C,
-                            bar(B_FULL(s)));
-                if (mine) {
-                    const int rs = owned % NR, ru = owned / NR;
-                    ++owned;
-                    if (!mbar_wait<false>(bar(B_REMPTY(rs)), (ru & 1) ^ 1)) break;
-                    mbar_arrive_tx(bar(B_RFULL(rs)), RAW_BYTES);
-                    const uint32_t dst = sbase + SM_RAW + rs * RAW_BYTES;
-                    tma_load_3d(dst + RAW_Q, &tm_q, 0, head, t0 + n * C, bar(B_RFULL(rs)));
-                    tma_load_3d(dst + RAW_K, &tm_k, 0, head, t0 + n * C, bar(B_RFULL(rs)));
-                    tma_load_3d(dst + RAW_A, &tm_a, 0, head, t0 + n * C, bar(B_RFULL(rs)));
+        // ------------------------------------------------ producer warp
+        // Lane 0 loads the v tiles by TMA and forwards slot releases to the slot's
+        // owner (the owner's prologue loads q, k and the gate logits itself). Releases
+        // travel through this thread because a cluster-scope release waits for all of
+        // the issuing thread's earlier generic memory operations, and this thread has
+        // none in flight (TMA belongs to the async proxy).
+        for (int n = 0; n < nchunks; ++n) {
+            const int s = n % NP, use = n / NP;
+            KDA_TRACE(n, 0);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            KDA_TRACE(n, 1);
+            const bool mine = owner(n) == rank;
+            const int c0 = t0 + n * C;
+            if (lane == 0) {
+                if (n >= NP) {  // chunk n - NP (same slot, same owner) is consumed here
+                    if (kShare)
+                        mbar_arrive_remote(map_to_rank(bar(B_CFREE(s)), owner(n)));
+                    else
+                        mbar_arrive(bar(B_CFREE(s)));
                 }
+                mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
+                tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head, c0,
+                            bar(B_FULL(s)));
             }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp <= NPW) {
         // ------------------------------------------------ prologue (4 warps, 128 threads)
         const int c = threadIdx.x - 32;  // key channel of the gate pass
         const int pw = warp - 1;
-        const int nt = 128;
-        __nv_bfloat16 *Kt = reinterpret_cast<__nv_bfloat16 *>(sm + SM_KT);
-        __nv_bfloat16 *Kh = reinterpret_cast<__nv_bfloat16 *>(sm + SM_KH);
+        const int nt = 32 * NPW;
+        unsigned char *KtB = sm + SM_KT;  // K~ [c][t]
+        unsigned char *KhB = sm + SM_KH;  // K^ [c][t]
+        const uint32_t Kt_s = sbase + SM_KT, Kh_s = sbase + SM_KH;
         float *As = reinterpret_cast<float *>(sm + SM_A);
-        float *bs = reinterpret_cast<float *>(sm + SM_BETA);
+        const int i8 = lane >> 3, r8 = lane & 7;
+        const int nstep = kShare ? kCS : 1;
+        // beta of owned chunk n (zero past the end) into buffer b, by warp 1's lanes
+        // 0-15 with cp.async, which no barrier or fence of another thread waits for
+        auto fetch_beta = [&](int n, int b) {
+            if (pw == 1 && lane < C && n < nchunks) {
+                const int row = t0 + n * C + lane;
+                const bool in = row < t1;
+                cp_async_4(sbase + SM_BETA + (b * C + lane) * 4,
+                           p.beta + (size_t)(in ? row : t0) * H + head, in ? 4u : 0u);
+            }
+            if (pw == 1) asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // q, k and gate-logit tiles of owned chunk n into raw slot rs, by TMA (thread 0)
+        auto fetch_raw = [&](int n, int rs) {
+            if (c == 0 && n < nchunks) {
+                const uint32_t dst = sbase + SM_RAW + rs * RAW_STRIDE;
+                const int c0n = t0 + n * C;
+                mbar_arrive_tx(bar(B_RFULL(rs)), RAW_TMA_BYTES);
+                tma_load_3d(dst + RAW_Q, &tm_q, 0, head, c0n, bar(B_RFULL(rs)));
+                tma_load_3d(dst + RAW_K, &tm_k, 0, head, c0n, bar(B_RFULL(rs)));
+                tma_load_3d(dst + RAW_A, &tm_a, 0, head, c0n, bar(B_RFULL(rs)));
+                KDA_TRACE(n, 2);
+            }
+        };
+        fetch_beta(kShare ? (int)rank : 0, 0);
+        fetch_raw(kShare ? (int)rank : 0, 0);
         int owned = 0;
         for (int n = 0; n < nchunks; ++n) {
             if (owner(n) != rank) continue;
@@ -329,82 +440,117 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = n % NP, use = n / NP;
             const int c0 = t0 + n * C;
             const int L = min(C, t1 - c0);
+            if (c == 0) KDA_TRACE(n, 3);
+            // the next owned chunk's tiles go into the slot the previous one used
+            fetch_raw(n + nstep, owned % NR);
             bool bad = !mbar_wait<false>(bar(B_RFULL(rs)), ru & 1);
             bad |= !mbar_wait<true>(bar(B_CFREE(s)), (use & 1) ^ 1);
             if (named_sync_or(1, nt, bad)) break;
+            if (c == 0) KDA_TRACE(n, 4);
+            const float *bs = reinterpret_cast<const float *>(sm + SM_BETA) + ((owned - 1) & 1) * C;
+            if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's beta
+            fetch_beta(n + nstep, owned & 1);                               // next owned chunk's
             unsigned char *slot = sm + SM_PROD + s * SLOT_BYTES;
-            __nv_bfloat16 *Pq = reinterpret_cast<__nv_bfloat16 *>(slot + OFF_PQ);
-            __nv_bfloat16 *Pk = reinterpret_cast<__nv_bfloat16 *>(slot + OFF_PK);
+            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             float *Pg = reinterpret_cast<float *>(slot + OFF_PG);
-            const unsigned char *raw = sm + SM_RAW + rs * RAW_BYTES;
+            const unsigned char *raw = sm + SM_RAW + rs * RAW_STRIDE;
             const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_Q);
             const __nv_bfloat16 *rk = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_K);
             const float *ra = reinterpret_cast<const float *>(raw + RAW_A);
-            // -- gate pass: one key channel per thread, 16 tokens in order
+            // -- gate pass: one key channel per thread, 16 tokens in order; outputs are
+            //    written channel-major as packed bf16 pairs, 16 bytes at a time
             {
-                float eg[C], kk[C];
+                // rows past the end hold another sequence's (finite) data or TMA
+                // zeros: compute every row, then select, in separate passes so that
+                // the 16 independent exponential chains overlap
+                float eg[C], kk[C], qq[C];
+#pragma unroll
+                for (int r = 0; r < C; ++r) eg[r] = ra[r * D + c];
+#pragma unroll
+                for (int r = 0; r < C; ++r)  // sigmoid(a) = 1 / (1 + exp(-a))
+                    eg[r] = rcp_approx(1.f + ex2_approx(-kLog2e * eg[r]));
+#pragma unroll
+                for (int r = 0; r < C; ++r) {  // exp(g), g = -5 sigmoid(a)
+                    const float e = ex2_approx((kGMin * kLog2e) * eg[r]);
+                    eg[r] = r < L ? e : 1.f;
+                    qq[r] = r < L ? __bfloat162float(rq[r * D + c]) : 0.f;
+                    kk[r] = r < L ? __bfloat162float(rk[r * D + c]) : 0.f;
+                }
+                uint32_t wq[C / 2], wk[C / 2];
                 float gam = 1.f;
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    float qv = 0.f, kv = 0.f, e = 1.f;
-                    if (r < L) {
-                        qv = __bfloat162float(rq[r * D + c]);
-                        kv = __bfloat162float(rk[r * D + c]);
-                        const float sig = __fdividef(1.f, 1.f + __expf(-ra[r * D + c]));
-                        e = __expf(kGMin * sig);  // exp(g), g = -5 sigmoid(a)
-                    }
-                    eg[r] = e;
-                    kk[r] = kv;
-                    gam *= e;  // Gamma_r = exp(G_r)
-                    Pq[r * LDP + c] = __float2bfloat16_rn(qv * gam);
-                    Kt[r * LDP + c] = __float2bfloat16_rn(kv * gam);
+                for (int r = 0; r < C; r += 2) {
+                    const float g0 = gam * eg[r];  // Gamma_r = exp(G_r)
+                    const float g1 = g0 * eg[r + 1];
+                    gam = g1;
+                    wq[r >> 1] = pack_bf16(qq[r] * g0, qq[r + 1] * g1);
+                    wk[r >> 1] = pack_bf16(kk[r] * g0, kk[r + 1] * g1);
                 }
-                Pg[c] = gam;                        // gamma_L = exp(G_L)
-                const float inv_gl = __fdividef(1.f, gam);  // exp(-G_L) <= exp(80)
-                float suf = 1.f;                     // exp(G_L - G_r)
+                *reinterpret_cast<uint4 *>(slot + OFF_PQ + cmaj(c, 0)) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                *reinterpret_cast<uint4 *>(slot + OFF_PQ + cmaj(c, 8)) = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+                *reinterpret_cast<uint4 *>(KtB + cmaj(c, 0)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                *reinterpret_cast<uint4 *>(KtB + cmaj(c, 8)) = make_uint4(wk[4], wk[5], wk[6], wk[7]);
+                Pg[gperm(c)] = gam;                         // gamma_L = exp(G_L)
+                const float inv_gl = rcp_approx(gam);  // exp(-G_L) <= exp(80)
+                float suf = 1.f;                            // exp(G_L - G_r)
+                uint32_t wp[C / 2], wh[C / 2];
+                float hp = 0.f, hh = 0.f;
 #pragma unroll
                 for (int r = C - 1; r >= 0; --r) {
-                    Pk[r * LDP + c] = __float2bfloat16_rn(kk[r] * suf);
-                    Kh[r * LDP + c] = __float2bfloat16_rn(kk[r] * (suf * inv_gl));
+                    const float kp = kk[r] * suf, kh = kk[r] * (suf * inv_gl);
+                    if (r & 1) {
+                        hp = kp;
+                        hh = kh;
+                    } else {
+                        wp[r >> 1] = pack_bf16(kp, hp);
+                        wh[r >> 1] = pack_bf16(kh, hh);
+                    }
                     suf *= eg[r];
                 }
-                if (c < C) bs[c] = c < L ? p.beta[(size_t)(c0 + c) * H + head] : 0.f;
+                *reinterpret_cast<uint4 *>(slot + OFF_PK + cmaj(c, 0)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                *reinterpret_cast<uint4 *>(slot + OFF_PK + cmaj(c, 8)) = make_uint4(wp[4], wp[5], wp[6], wp[7]);
+                *reinterpret_cast<uint4 *>(KhB + cmaj(c, 0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4 *>(KhB + cmaj(c, 8)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
             }
             named_sync(1, nt);
-            if (c == 0) mbar_arrive(bar(B_REMPTY(rs)));  // raw tile consumed
-            // -- A = strict_lower(beta K~ K^^T), P = lower(Q~ K^^T): warps 0, 1 (token halves)
-            if (pw < 2) {
-                float accA[2][4] = {}, accP[2][4] = {};
+            if (c == 0) KDA_TRACE(n, 5);
+            // -- A = strict_lower(beta K~ K^^T) on warps 0, 1 and P = lower(Q~ K^^T) on
+            //    warps 2, 3; each warp one 8-token column tile (j in [8 jh, 8 jh + 8))
+            {
+                const bool isA = pw < 2;
+                const int jh = pw & 1;
+                const uint32_t lhs = isA ? Kt_s : slot_s + OFF_PQ;
+                uint32_t b[D / 32][4], a[D / 16][4];
 #pragma unroll
-                for (int kt = 0; kt < D / 16; ++kt) {
-                    const int i = lane >> 3;
-                    const int ra_ = (i & 1) * 8 + (lane & 7), ca = kt * 16 + (i >> 1) * 8;
-                    uint32_t a[4], aq[4], b0, b1;
-                    ldsm_x4(smem_u32(Kt + ra_ * LDP + ca), a[0], a[1], a[2], a[3]);
-                    ldsm_x4(smem_u32(Pq + ra_ * LDP + ca), aq[0], aq[1], aq[2], aq[3]);
-                    const int rb = pw * 8 + (lane & 7), cb = kt * 16 + ((lane >> 3) & 1) * 8;
-                    ldsm_x2(smem_u32(Kh + rb * LDP + cb), b0, b1);
-                    mma16816(accA[kt & 1], a, b0, b1);
-                    mma16816(accP[kt & 1], aq, b0, b1);
-                }
+                for (int kp = 0; kp < D / 32; ++kp)  // K^^T fragments of key tiles 2kp, 2kp+1
+                    ldsm_x4_t(Kh_s + cmaj(kp * 32 + i8 * 8 + r8, jh * 8), b[kp][0], b[kp][1],
+                              b[kp][2], b[kp][3]);
+#pragma unroll
+                for (int kt = 0; kt < D / 16; ++kt)
+                    ldsm_x4_t(lhs + cmaj(kt * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), a[kt][0],
+                              a[kt][1], a[kt][2], a[kt][3]);
+                float acc[2][4] = {};
+#pragma unroll
+                for (int kt = 0; kt < D / 16; ++kt)
+                    mma16816(acc[kt & 1], a[kt], b[kt >> 1][2 * (kt & 1)], b[kt >> 1][2 * (kt & 1) + 1]);
                 __nv_bfloat16 *Pp = reinterpret_cast<__nv_bfloat16 *>(slot + OFF_PP);
-                const int r0 = lane >> 2, j0 = pw * 8 + 2 * (lane & 3);
+                const int r0 = lane >> 2, j0 = jh * 8 + 2 * (lane & 3);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = r0 + 8 * hh;
-                    float pv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = j0 + e;
-                        const float va = accA[0][2 * hh + e] + accA[1][2 * hh + e];
-                        const float vp = accP[0][2 * hh + e] + accP[1][2 * hh + e];
-                        As[r * C + j] = j < r ? bs[r] * va : 0.f;
-                        pv[e] = j <= r ? vp : 0.f;
+                    const float v0 = acc[0][2 * hh] + acc[1][2 * hh];
+                    const float v1 = acc[0][2 * hh + 1] + acc[1][2 * hh + 1];
+                    if (isA) {
+                        As[r * C + j0] = j0 < r ? bs[r] * v0 : 0.f;
+                        As[r * C + j0 + 1] = j0 + 1 < r ? bs[r] * v1 : 0.f;
+                    } else {
+                        *reinterpret_cast<uint32_t *>(Pp + r * LDS + j0) =
+                            pack_bf16(j0 <= r ? v0 : 0.f, j0 + 1 <= r ? v1 : 0.f);
                     }
-                    *reinterpret_cast<uint32_t *>(Pp + r * LDS + j0) = pack_bf16(pv[0], pv[1]);
                 }
             }
             named_sync(1, nt);
+            if (c == 0) KDA_TRACE(n, 6);
             // -- TB = (I + A)^-1 diag(beta): forward substitution, one column per lane
             if (pw == 0 && lane < C) {
                 const int j = lane;
@@ -422,23 +568,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < C; ++r) Ptb[r * LDS + j] = __float2bfloat16_rn(x[r] * bj);
             }
             named_sync(1, nt);
+            if (c == 0) KDA_TRACE(n, 7);
             // -- -W = -TB K~: warp pw covers key channels [32 pw, 32 pw + 32)
             {
-                const __nv_bfloat16 *Ptb = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PTB);
                 __nv_bfloat16 *Pw = reinterpret_cast<__nv_bfloat16 *>(slot + OFF_PW);
                 uint32_t tb[4];
                 {
-                    const int i = lane >> 3;
-                    const int r = (i & 1) * 8 + (lane & 7), j = (i >> 1) * 8;
-                    ldsm_x4(smem_u32(Ptb + r * LDS + j), tb[0], tb[1], tb[2], tb[3]);
+                    const int r = (i8 & 1) * 8 + r8, j = (i8 >> 1) * 8;
+                    ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
                 }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int cb = pw * 32 + half * 16;
-                    const int i = lane >> 3;
-                    const int j = (i & 1) * 8 + (lane & 7), cc = cb + (i >> 1) * 8;
                     uint32_t k0, k1, k2, k3;
-                    ldsm_x4_t(smem_u32(Kt + j * LDP + cc), k0, k1, k2, k3);
+                    ldsm_x4(Kt_s + cmaj(cb + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), k0, k1, k2, k3);
                     float acc0[4] = {}, acc1[4] = {};
                     mma16816(acc0, tb, k0, k1);
                     mma16816(acc1, tb, k2, k3);
@@ -451,24 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async();  // generic writes of the slot -> async-proxy bulk reads
             named_sync(1, nt);
+            if (c == 0) KDA_TRACE(n, 8);
             if (c == 0) {
                 if (kShare) {
-                    const uint32_t src = sbase + SM_PROD + s * SLOT_BYTES;
 #pragma unroll
                     for (uint32_t peer = 0; peer < (uint32_t)kCS; ++peer) {
                         if (peer == rank) continue;
-                        bulk_copy_to_peer(map_to_rank(src, peer), src, SLOT_BYTES,
+                        bulk_copy_to_peer(map_to_rank(slot_s, peer), slot_s, SLOT_BYTES,
                                           map_to_rank(bar(B_FULL(s)), peer));
                     }
                 }
                 mbar_arrive(bar(B_FULL(s)));  // own state warps
+                KDA_TRACE(n, 9);
             }
         }
-    } else {
+    } else if (warp <= NPW + NSW) {
         // ------------------------------------------------ state warps
+        // Own 16 rows of S^T for the whole sequence. Per chunk: U^T, then hand the
+        // bf16 S^T and U^T fragments to the paired output warp, then update S^T.
         const int sw = warp - 1 - NPW;  // 0 .. NSW-1
         const int vrow0 = (int)rank * VB + sw * 16;  // first value column (row of S^T)
         const int g4 = lane >> 2, l4 = lane & 3;
+        const int i8 = lane >> 3, r8 = lane & 7;
         const size_t sidx = ((size_t)seq * H + head) * D * D;
         float S[16][4];  // S^T fragments: n-tile j covers key channels 8j .. 8j+7
 #pragma unroll
@@ -483,32 +630,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
             }
         }
-        const float scale = rsqrtf((float)D);
-        __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + SM_OST) + sw * C * LDS;
         for (int n = 0; n < nchunks; ++n) {
             const int s = n % NP, use = n / NP;
-            const bool ok = mbar_wait<false>(bar(B_FULL(s)), use & 1);
+            const int hb = n & 1;
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 10);
+            bool ok = mbar_wait<false>(bar(B_FULL(s)), use & 1);
             if (__any_sync(0xffffffffu, !ok)) break;
-            const unsigned char *slot = sm + SM_PROD + s * SLOT_BYTES;
-            const __nv_bfloat16 *Pq = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PQ);
-            const __nv_bfloat16 *Pw = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PW);
-            const __nv_bfloat16 *Pk = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PK);
-            const __nv_bfloat16 *Ptb = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PTB);
-            const __nv_bfloat16 *Pp = reinterpret_cast<const __nv_bfloat16 *>(slot + OFF_PP);
-            const float *Pg = reinterpret_cast<const float *>(slot + OFF_PG);
-            const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_V + s * V_BYTES);
-            const int i8 = lane >> 3, r8 = lane & 7;
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 11);
+            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
+            const float *Pg = reinterpret_cast<const float *>(sm + SM_PROD + s * SLOT_BYTES + OFF_PG);
+            const uint32_t vs = sbase + SM_V + s * V_BYTES;
 
-            // U~^T = V^T TB^T  (initial value of the U^T accumulators)
-            float accU[2][2][4] = {};  // [k parity][token n-tile][frag]
+            // operand fragments for U^T: V^T, TB^T and (-W)^T, all loads first
+            uint32_t va[4], tb[4], wf[8][4];
             {
-                uint32_t va[4], tb[4];
                 const int t = (i8 >> 1) * 8 + r8, vv = sw * 16 + (i8 & 1) * 8;
-                ldsm_x4_t(smem_u32(Vs + t * VB + vv), va[0], va[1], va[2], va[3]);
+                ldsm_x4_t(vs + (t * VB + vv) * 2, va[0], va[1], va[2], va[3]);
                 const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
-                ldsm_x4(smem_u32(Ptb + r * LDS + j), tb[0], tb[1], tb[2], tb[3]);
-                mma16816(accU[0][0], va, tb[0], tb[1]);
-                mma16816(accU[0][1], va, tb[2], tb[3]);
+                ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
+#pragma unroll
+                for (int kt = 0; kt < 8; ++kt)
+                    ldsm_x4(slot_s + OFF_PW + (r * LDP + kt * 16 + (i8 & 1) * 8) * 2,
+                            wf[kt][0], wf[kt][1], wf[kt][2], wf[kt][3]);
             }
             // S^T as bf16 A fragments
             uint32_t Sa[8][4];
@@ -519,84 +662,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Sa[kt][2] = pack_bf16(S[2 * kt + 1][0], S[2 * kt + 1][1]);
                 Sa[kt][3] = pack_bf16(S[2 * kt + 1][2], S[2 * kt + 1][3]);
             }
-            // U^T += S^T (-W)^T
+            // U^T = V^T TB^T + S^T (-W)^T, four independent accumulator chains
+            float accU[2][2][4] = {};  // [k parity][token n-tile][frag]
+            mma16816(accU[0][0], va, tb[0], tb[1]);
+            mma16816(accU[0][1], va, tb[2], tb[3]);
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt) {
-                uint32_t w0, w1, w2, w3;
-                const int r = (i8 >> 1) * 8 + r8, cc = kt * 16 + (i8 & 1) * 8;
-                ldsm_x4(smem_u32(Pw + r * LDP + cc), w0, w1, w2, w3);
-                mma16816(accU[kt & 1][0], Sa[kt], w0, w1);
-                mma16816(accU[kt & 1][1], Sa[kt], w2, w3);
+                mma16816(accU[kt & 1][0], Sa[kt], wf[kt][0], wf[kt][1]);
+                mma16816(accU[kt & 1][1], Sa[kt], wf[kt][2], wf[kt][3]);
             }
+            // operands of the state update, loaded while the U^T products run
+            uint32_t kf[8][4];
+#pragma unroll
+            for (int np = 0; np < 8; ++np)
+                ldsm_x4(slot_s + OFF_PK + cmaj(np * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8),
+                        kf[np][0], kf[np][1], kf[np][2], kf[np][3]);
+            float4 gl[8];
+#pragma unroll
+            for (int np = 0; np < 8; ++np) gl[np] = reinterpret_cast<const float4 *>(Pg)[l4 * 8 + np];
             uint32_t Ua[4];
             Ua[0] = pack_bf16(accU[0][0][0] + accU[1][0][0], accU[0][0][1] + accU[1][0][1]);
             Ua[1] = pack_bf16(accU[0][0][2] + accU[1][0][2], accU[0][0][3] + accU[1][0][3]);
             Ua[2] = pack_bf16(accU[0][1][0] + accU[1][1][0], accU[0][1][1] + accU[1][1][1]);
             Ua[3] = pack_bf16(accU[0][1][2] + accU[1][1][2], accU[0][1][3] + accU[1][1][3]);
-            // O^T = S^T Q~^T + U^T P^T  (uses the state before this chunk's update)
-            float accO[2][2][4] = {};
-#pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-                uint32_t q0, q1, q2, q3;
-                const int r = (i8 >> 1) * 8 + r8, cc = kt * 16 + (i8 & 1) * 8;
-                ldsm_x4(smem_u32(Pq + r * LDP + cc), q0, q1, q2, q3);
-                mma16816(accO[kt & 1][0], Sa[kt], q0, q1);
-                mma16816(accO[kt & 1][1], Sa[kt], q2, q3);
-            }
-            {
-                uint32_t p0, p1, p2, p3;
-                const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
-                ldsm_x4(smem_u32(Pp + r * LDS + j), p0, p1, p2, p3);
-                mma16816(accO[0][0], Ua, p0, p1);
-                mma16816(accO[0][1], Ua, p2, p3);
-            }
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 12);
             // S^T <- S^T diag(gamma_L) + U^T K'
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
-                const float2 g0 = *reinterpret_cast<const float2 *>(Pg + 16 * np + 2 * l4);
-                const float2 g1 = *reinterpret_cast<const float2 *>(Pg + 16 * np + 8 + 2 * l4);
-                S[2 * np][0] *= g0.x; S[2 * np][1] *= g0.y; S[2 * np][2] *= g0.x; S[2 * np][3] *= g0.y;
-                S[2 * np + 1][0] *= g1.x; S[2 * np + 1][1] *= g1.y;
-                S[2 * np + 1][2] *= g1.x; S[2 * np + 1][3] *= g1.y;
-                uint32_t k0, k1, k2, k3;
-                const int t = (i8 & 1) * 8 + r8, cc = np * 16 + (i8 >> 1) * 8;
-                ldsm_x4_t(smem_u32(Pk + t * LDP + cc), k0, k1, k2, k3);
-                mma16816(S[2 * np], Ua, k0, k1);
-                mma16816(S[2 * np + 1], Ua, k2, k3);
+                const float4 g = gl[np];  // columns 16np + 2l4 (+1), 16np + 8 + 2l4 (+1)
+                S[2 * np][0] *= g.x; S[2 * np][1] *= g.y; S[2 * np][2] *= g.x; S[2 * np][3] *= g.y;
+                S[2 * np + 1][0] *= g.z; S[2 * np + 1][1] *= g.w;
+                S[2 * np + 1][2] *= g.z; S[2 * np + 1][3] *= g.w;
+                mma16816(S[2 * np], Ua, kf[np][0], kf[np][1]);
+                mma16816(S[2 * np + 1], Ua, kf[np][2], kf[np][3]);
             }
-            // release the slot (V tile and products) to the producer and the owner
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_FREE(s)));
-                if (kShare)
-                    mbar_arrive_remote(map_to_rank(bar(B_CFREE(s)), owner(n)));
-                else
-                    mbar_arrive(bar(B_CFREE(s)));
-            }
-            // output tile: scale, bf16, transpose through shared memory, 16-byte stores
+            // hand S^T (before this chunk's update) and U^T to the output warp
+            ok = mbar_wait<false>(bar(B_HEMPTY(sw, hb)), ((n >> 1) & 1) ^ 1);
+            if (__any_sync(0xffffffffu, !ok)) break;
             {
-                uint32_t o0 = pack_bf16(scale * (accO[0][0][0] + accO[1][0][0]),
-                                        scale * (accO[0][0][1] + accO[1][0][1]));
-                uint32_t o1 = pack_bf16(scale * (accO[0][0][2] + accO[1][0][2]),
-                                        scale * (accO[0][0][3] + accO[1][0][3]));
-                uint32_t o2 = pack_bf16(scale * (accO[0][1][0] + accO[1][1][0]),
-                                        scale * (accO[0][1][1] + accO[1][1][1]));
-                uint32_t o3 = pack_bf16(scale * (accO[0][1][2] + accO[1][1][2]),
-                                        scale * (accO[0][1][3] + accO[1][1][3]));
-                // matrices: (v 0-7, t 0-7), (v 8-15, t 0-7), (v 0-7, t 8-15), (v 8-15, t 8-15)
-                const int t = (i8 >> 1) * 8 + r8, vv = (i8 & 1) * 8;
-                stsm_x4_t(smem_u32(ost + t * LDS + vv), o0, o1, o2, o3);
-                __syncwarp();
-                const int c0 = t0 + n * C;
-                const int L = min(C, t1 - c0);
-                const int tt = lane >> 1, hv = (lane & 1) * 8;
-                if (tt < L) {
-                    const uint4 val = *reinterpret_cast<const uint4 *>(ost + tt * LDS + hv);
-                    *reinterpret_cast<uint4 *>(p.out + ((size_t)(c0 + tt) * H + head) * D +
-                                               vrow0 + hv) = val;
-                }
-                __syncwarp();
+                uint4 *ho = reinterpret_cast<uint4 *>(sm + SM_HO + (sw * 2 + hb) * HO_BYTES +
+                                                      lane * HO_LANE);
+#pragma unroll
+                for (int kt = 0; kt < 8; ++kt)
+                    ho[kt] = make_uint4(Sa[kt][0], Sa[kt][1], Sa[kt][2], Sa[kt][3]);
+                ho[8] = make_uint4(Ua[0], Ua[1], Ua[2], Ua[3]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_HFULL(sw, hb)));
+            // every read of the slot by this warp is done
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
         }
         if (p.h_final) {
 #pragma unroll
@@ -608,10 +724,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.h_final[sidx + (size_t)(kc + 1) * D + v0 + 8] = S[j][3];
             }
         }
+    } else {
+        // ------------------------------------------------ output warps
+        // O^T = S^T Q~^T + U^T P^T for the paired state warp's 16 value columns, scaled
+        // by d_k^-1/2, then a TMA store of the 16-token x 16-column tile.
+        const int ow = warp - 1 - NPW - NSW;  // pairs with state warp ow
+        const int vrow0 = (int)rank * VB + ow * 16;
+        const int i8 = lane >> 3, r8 = lane & 7;
+        const float scale = rsqrtf((float)D);
+        const uint32_t ost_s = sbase + SM_OST + ow * 2 * OST_BYTES;
+        const __nv_bfloat16 *ost = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_OST) + ow * 2 * C * 16;
+        for (int n = 0; n < nchunks; ++n) {
+            const int s = n % NP, use = n / NP;
+            const int hb = n & 1;
+            bool ok = mbar_wait<false>(bar(B_FULL(s)), use & 1);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
+            uint32_t qf[8][4], pf[4];
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt)
+                ldsm_x4_t(slot_s + OFF_PQ + cmaj(kt * 16 + (i8 & 1) * 8 + r8, (i8 >> 1) * 8),
+                          qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3]);
+            {
+                const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
+                ldsm_x4(slot_s + OFF_PP + (r * LDS + j) * 2, pf[0], pf[1], pf[2], pf[3]);
+            }
+            ok = mbar_wait<false>(bar(B_HFULL(ow, hb)), (n >> 1) & 1);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            uint32_t Sa[8][4], Ua[4];
+            {
+                const uint4 *ho = reinterpret_cast<const uint4 *>(sm + SM_HO + (ow * 2 + hb) * HO_BYTES +
+                                                                  lane * HO_LANE);
+#pragma unroll
+                for (int kt = 0; kt < 8; ++kt) {
+                    const uint4 v = ho[kt];
+                    Sa[kt][0] = v.x; Sa[kt][1] = v.y; Sa[kt][2] = v.z; Sa[kt][3] = v.w;
+                }
+                const uint4 v = ho[8];
+                Ua[0] = v.x; Ua[1] = v.y; Ua[2] = v.z; Ua[3] = v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_HEMPTY(ow, hb)));
+            float accO[2][2][4] = {};
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt) {
+                mma16816(accO[kt & 1][0], Sa[kt], qf[kt][0], qf[kt][1]);
+                mma16816(accO[kt & 1][1], Sa[kt], qf[kt][2], qf[kt][3]);
+            }
+            mma16816(accO[0][0], Ua, pf[0], pf[1]);
+            mma16816(accO[0][1], Ua, pf[2], pf[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
+            // output tile: scale, bf16, transpose into a staging tile, TMA store
+            {
+                const int buf = n & 1;
+                if (lane == 0) bulk_wait_read_le1();  // the store issued 2 chunks ago has read it
+                __syncwarp();
+                uint32_t o0 = pack_bf16(scale * (accO[0][0][0] + accO[1][0][0]),
+                                        scale * (accO[0][0][1] + accO[1][0][1]));
+                uint32_t o1 = pack_bf16(scale * (accO[0][0][2] + accO[1][0][2]),
+                                        scale * (accO[0][0][3] + accO[1][0][3]));
+                uint32_t o2 = pack_bf16(scale * (accO[0][1][0] + accO[1][1][0]),
+                                        scale * (accO[0][1][1] + accO[1][1][1]));
+                uint32_t o3 = pack_bf16(scale * (accO[0][1][2] + accO[1][1][2]),
+                                        scale * (accO[0][1][3] + accO[1][1][3]));
+                // matrices: (v 0-7, t 0-7), (v 8-15, t 0-7), (v 0-7, t 8-15), (v 8-15, t 8-15)
+                const int t = (i8 >> 1) * 8 + r8, vv = (i8 & 1) * 8;
+                const uint32_t tile = ost_s + buf * OST_BYTES;
+                stsm_x4_t(tile + (t * 16 + vv) * 2, o0, o1, o2, o3);
+                const int c0 = t0 + n * C;
+                const int L = min(C, t1 - c0);
+                if (L == C) {
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_o, vrow0, head, c0, tile);
+                        bulk_commit();
+                    }
+                } else {  // partial last chunk: plain stores of the valid rows only
+                    __syncwarp();
+                    const int tt = lane >> 1, hv = (lane & 1) * 8;
+                    if (tt < L) {
+                        const uint4 val = *reinterpret_cast<const uint4 *>(ost + buf * C * 16 + tt * 16 + hv);
+                        *reinterpret_cast<uint4 *>(p.out + ((size_t)(c0 + tt) * H + head) * D +
+                                                   vrow0 + hv) = val;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) KDA_TRACE(n, 14 + ow);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     // no CTA may leave while a peer can still write into its shared memory
     __syncwarp();
     if (kShare) cluster_sync();
+#ifdef KDA_TC_TRACE
+    __syncthreads();
+    if (blockIdx.x < 4)
+        for (int i = threadIdx.x; i < 64 * 16; i += blockDim.x)
+            g_trace[blockIdx.x][i / 16][i % 16] = reinterpret_cast<long long *>(sm + SM_TRACE)[i];
+#endif
 }
 
 // ------------------------------------------------------------------ host side
@@ -630,6 +844,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x) {
+    // [n_tok][H][128] row-major viewed as a 3-D tensor (channel, head, token); boxes
+    // are box_x channels x 1 head x 16 tokens. Out-of-range tokens read as zero.
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t es = f32 ? 4 : 2;
@@ -646,11 +862,12 @@ bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H
 
 template <bool kShare>
 cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
-    CUtensorMap mq, mk, ma, mv;
+    CUtensorMap mq, mk, ma, mv, mo;
     if (!encode_map(&mq, a.q, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&mk, a.k, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&ma, a.a, true, a.n_tok, a.n_heads, D) ||
-        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB))
+        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB) ||
+        !encode_map(&mo, a.out, false, a.n_tok, a.n_heads, 16))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel<kShare>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -671,7 +888,7 @@ cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel<kShare>, mq, mk, ma, mv, p);
+    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel<kShare>, mq, mk, ma, mv, mo, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
@@ -690,6 +907,12 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
     return launch_tc_t<true>(a, stream);
 #endif
 }
+
+#ifdef KDA_TC_TRACE
+extern "C" int kda_debug_trace_dump(long long *host) {
+    return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
+}
+#endif
 
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_device_flags, sizeof(unsigned int), 0,

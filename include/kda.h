@@ -38,8 +38,9 @@
  *                 multiples of 16 tokens.
  *   out           [n_tok, n_heads, d_v]   dtype
  *   h_final       [n_seq, n_heads, d_k, d_v] float32, or NULL to skip writing it
- * Device pointers must be 16-byte aligned. out and h_final must not overlap any
- * input. The state and all accumulation are float32.
+ * q, k, v, gate_logits and out must be 16-byte aligned; beta, h0, cu_seqlens and
+ * h_final 4-byte aligned. out and h_final must not overlap any input. The state and
+ * all accumulation are float32.
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  * legacy default stream). The return value reports argument validation and launch

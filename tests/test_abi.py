@@ -67,7 +67,8 @@ def call(lib, *, q=FAKE, k=FAKE, v=FAKE, a=FAKE, beta=FAKE, h0=None, cu=FAKE, ou
     (dict(n_tok=-1), 1), (dict(n_seq=-1), 1), (dict(H=0), 1), (dict(dk=0), 1),
     (dict(dv=-3), 1), (dict(n_seq=0), 1),          # tokens but no sequence
     (dict(dk=129), 2), (dict(dv=256), 2), (dict(dtype=7), 2),
-    (dict(q=FAKE + 2), 1), (dict(out=FAKE + 8), 1), (dict(hf=FAKE + 4), 1),
+    (dict(q=FAKE + 2), 1), (dict(out=FAKE + 8), 1), (dict(a=FAKE + 4), 1),
+    (dict(hf=FAKE + 2), 1), (dict(beta=FAKE + 1), 1), (dict(cu=FAKE + 2), 1),
 ])
 def test_host_validation(lib, symbol, kw, status):
     st = call(lib, symbol=symbol, **kw)
