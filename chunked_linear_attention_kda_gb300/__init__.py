@@ -22,13 +22,14 @@ import threading
 from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "load_library",
-           "kernel_launch_count", "read_device_flags",
+           "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA"}
 KDA_F32, KDA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
-                    "kda_kernel_launch_count", "kda_read_device_flags", "kda_chunk_fwd",
+                    "kda_kernel_launch_count", "kda_read_device_flags",
+                    "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host")
 
 _lock = threading.Lock()
@@ -79,6 +80,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_kernel_launch_count.restype = ctypes.c_uint64
         lib.kda_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, P]
         lib.kda_read_device_flags.restype = ctypes.c_int
+        lib.kda_selftest_bounded_wait.argtypes = [I64, P, P]
+        lib.kda_selftest_bounded_wait.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -204,3 +207,17 @@ def read_device_flags(reset: bool = True, stream=None) -> int:
     _check(lib, lib.kda_read_device_flags(ctypes.byref(v), int(reset),
                                           ctypes.c_void_p(stream.cuda_stream)))
     return int(v.value)
+
+
+def selftest_bounded_wait(limit_cycles: int = 2_000_000):
+    """Run the bounded-wait self-test; returns ``(returned_code, flags)`` where 1 and a
+    set bit 0 mean the never-completing wait gave up as designed. Clears the flags."""
+    import torch
+    lib = load_library()
+    read_device_flags(reset=True)
+    d = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    _check(lib, lib.kda_selftest_bounded_wait(int(limit_cycles), ctypes.c_void_p(d.data_ptr()),
+                                              ctypes.c_void_p(st.cuda_stream)))
+    flags = read_device_flags(reset=True)
+    return int(d.item()), flags

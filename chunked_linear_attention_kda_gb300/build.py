@@ -20,6 +20,7 @@ LIB = os.path.join(BUILD, "libkda_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+PER_FILE = {}  # per-source extra nvcc flags
 
 
 def nvcc() -> str:
@@ -56,7 +57,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *PER_FILE.get(os.path.basename(src), []), *extra_flags,
+               "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

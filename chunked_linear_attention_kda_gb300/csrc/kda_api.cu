@@ -110,6 +110,13 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_last_error.c_str(); }
 
+kda_status kda_selftest_bounded_wait(int64_t limit_cycles, int32_t *d_returned, void *stream) {
+    if (!d_returned || limit_cycles <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "d_returned must be non-NULL and the limit positive");
+    return launched(kda::bounded_wait_selftest(limit_cycles, d_returned, (cudaStream_t)stream),
+                    "self-test launch");
+}
+
 kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     if (!flags) return fail(KDA_ERR_INVALID_ARG, "flags is NULL");
     unsigned int v = 0;

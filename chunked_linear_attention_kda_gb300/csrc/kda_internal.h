@@ -32,6 +32,10 @@ cudaError_t launch_tc(const FwdArgs &args, cudaStream_t stream);
 // True when the tensor-core kernel handles this shape and dtype.
 bool tc_supported(const FwdArgs &args);
 
+// Launches a one-thread kernel whose pipeline wait can never complete; it gives up
+// after limit_cycles, sets bit 0 of the status word and writes 1 to *d_returned.
+cudaError_t bounded_wait_selftest(long long limit_cycles, int *d_returned, cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

@@ -54,11 +54,20 @@ __device__ unsigned int g_device_flags;  // bit 0: a pipeline wait exceeded its 
 // shared memory and are copied out when the CTA finishes, so that tracing adds no
 // global stores to the pipeline.
 #ifdef KDA_TC_TRACE
-__device__ long long g_trace[4][64][16];
+__device__ long long g_trace[4][64][32];
+__device__ __forceinline__ long long trace_clock() {
+#ifdef KDA_TC_TRACE_GLOBALTIMER
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+#else
+    return clock64();
+#endif
+}
 #define KDA_TRACE(n, slot)                                                              \
     do {                                                                                \
         if ((n) < 64)                                                                   \
-            reinterpret_cast<long long *>(sm + SM_TRACE)[(n) * 16 + (slot)] = clock64(); \
+            reinterpret_cast<long long *>(sm + SM_TRACE)[(n) * 32 + (slot)] = trace_clock(); \
     } while (0)
 #else
 #define KDA_TRACE(n, slot) \
@@ -72,11 +81,14 @@ constexpr int D = 128;          // d_k = d_v
 constexpr int C = kChunk;       // 16 tokens
 constexpr int kCS = 4;          // CTAs per (sequence, head) = cluster size
 constexpr int VB = D / kCS;     // value columns per CTA (32)
-constexpr int NSW = VB / 16;    // state warps per CTA (2), and as many output warps
-constexpr int NPW = 4;          // prologue warps
-constexpr int kThreads = 32 * (1 + NPW + 2 * NSW);
+constexpr int NSW = VB / 16;    // state warps per CTA (2), 16 value columns each, and as
+                                // many output warps
+constexpr int NGRP = 2;         // prologue groups, alternating owned chunks
+constexpr int NPW = 4;          // warps per prologue group (one key channel per thread)
+constexpr int W_STATE0 = 1 + NGRP * NPW;  // first state warp
+constexpr int W_OUT0 = W_STATE0 + NSW;    // first output warp
+constexpr int kThreads = 32 * (W_OUT0 + NSW);
 constexpr int NP = 8;           // product-ring depth (multiple of kCS)
-constexpr int NR = 2;           // raw-input ring depth (owned chunks); prefetch distance 1
 constexpr int LDP = 136;        // pitch (elements) of 16 x 128 bf16 tiles: 272 B rows
 constexpr int LDS = 24;         // pitch of 16 x 16 bf16 tiles: 48 B rows
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (~2 s) before a wait gives up
@@ -102,40 +114,42 @@ constexpr int OFF_PG = OFF_PP + C * LDS * 2;     // gamma_L [128] f32, permuted 
 constexpr int SLOT_BYTES = OFF_PG + D * 4;       // 14592
 static_assert(SLOT_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 
-// raw slot: the owner's TMA tiles of one chunk plus beta
+// raw slot (one per prologue group): the owner's TMA tiles of one chunk
 constexpr int RAW_Q = 0, RAW_K = C * D * 2, RAW_A = 2 * C * D * 2;
-constexpr int RAW_TMA_BYTES = RAW_A + C * D * 4;  // 16384 (q, k, a)
-constexpr int RAW_STRIDE = RAW_TMA_BYTES;
-constexpr int V_BYTES = C * VB * 2;               // 1024
-constexpr int OST_BYTES = C * 16 * 2;             // one 16 x 16 bf16 output tile
+constexpr int RAW_BYTES = RAW_A + C * D * 4;     // 16384 (q, k, a)
+constexpr int V_BYTES = C * VB * 2;              // 1024
+// prologue-group scratch
+constexpr int GS_KT = 0;                         // K~ [c][t]
+constexpr int GS_KH = GS_KT + CMAJ_BYTES;        // K^ [c][t]
+constexpr int GS_A = GS_KH + CMAJ_BYTES;         // A  [16][16] f32
+constexpr int GS_BETA = GS_A + C * C * 4;        // beta [2][16] f32 (double buffer)
+constexpr int GS_BYTES = GS_BETA + 2 * C * 4;
+// state -> output warp handoff: [state warp][2 buffers][32 lanes][36 u32]
+constexpr int HO_LANE = 36 * 4;
+constexpr int HO_BYTES = 32 * HO_LANE;
 
 constexpr int SM_RAW = 0;
-constexpr int SM_V = SM_RAW + NR * RAW_STRIDE;
+constexpr int SM_V = SM_RAW + NGRP * RAW_BYTES;
 constexpr int SM_PROD = SM_V + NP * V_BYTES;
-constexpr int SM_KT = SM_PROD + NP * SLOT_BYTES; // K~ [c][t] (prologue scratch)
-constexpr int SM_KH = SM_KT + CMAJ_BYTES;        // K^ [c][t]
-constexpr int SM_A = SM_KH + CMAJ_BYTES;         // A  [16][16] f32
-constexpr int SM_BETA = SM_A + C * C * 4;        // beta [2][16] f32 (double buffer)
-constexpr int SM_OST = (SM_BETA + 2 * C * 4 + 127) / 128 * 128;  // output tiles [NSW][2][16][16] bf16
-constexpr int HO_LANE = 36 * 4;                   // handoff: 36 registers per lane
-constexpr int HO_BYTES = 32 * HO_LANE;            // one state -> output warp handoff
-constexpr int SM_HO = SM_OST + NSW * 2 * OST_BYTES;  // [NSW][2][32 lanes][36] u32
+constexpr int SM_GS = SM_PROD + NP * SLOT_BYTES;
+constexpr int SM_HO = (SM_GS + NGRP * GS_BYTES + 127) / 128 * 128;
 constexpr int SM_BAR = SM_HO + NSW * 2 * HO_BYTES;
-constexpr int NBARS = 3 * NP + NR + 4 * NSW;
+constexpr int NBARS = 3 * NP + NGRP + 4 * NSW;
 constexpr int SM_MISC = SM_BAR + NBARS * 8;
 #ifdef KDA_TC_TRACE
 constexpr int SM_TRACE = SM_MISC + 64;
-constexpr int SMEM_BYTES = SM_TRACE + 64 * 16 * 8;
+constexpr int SMEM_BYTES = SM_TRACE + 64 * 32 * 8;
 #else
 constexpr int SMEM_BYTES = SM_MISC + 64;
 #endif
-static_assert(RAW_STRIDE % 128 == 0 && SM_V % 128 == 0 && SM_PROD % 128 == 0, "TMA alignment");
-static_assert(SM_KT % 16 == 0 && SM_OST % 128 == 0 && SM_BAR % 8 == 0, "alignment");
+static_assert(RAW_BYTES % 128 == 0 && SM_V % 128 == 0 && SM_PROD % 128 == 0, "TMA alignment");
+static_assert(SM_GS % 16 == 0 && GS_BYTES % 16 == 0 && SM_HO % 16 == 0, "alignment");
+static_assert(SM_BAR % 8 == 0, "alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // gamma_L[c], c = 16 np + 8 h + 2 l4 + e, is stored at 32 l4 + 4 np + 2 h + e so that
 // the lanes holding S^T columns 2 l4 (+1, +8, +9) of every 16-column group read
-// their 32 decay factors as 8 contiguous float4
+// their decay factors as contiguous float4
 __host__ __device__ constexpr int gperm(int c) {
     return ((c >> 1) & 3) * 32 + (c >> 4) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
 }
@@ -144,9 +158,9 @@ __host__ __device__ constexpr int gperm(int c) {
 __host__ __device__ constexpr int B_FULL(int s) { return s; }           // products + V in
 __host__ __device__ constexpr int B_FREE(int s) { return NP + s; }      // local state warps done
 __host__ __device__ constexpr int B_CFREE(int s) { return 2 * NP + s; } // all CTAs done (owner)
-__host__ __device__ constexpr int B_RFULL(int s) { return 3 * NP + s; }
-__host__ __device__ constexpr int B_HFULL(int w, int b) { return 3 * NP + NR + 2 * w + b; }
-__host__ __device__ constexpr int B_HEMPTY(int w, int b) { return 3 * NP + NR + 2 * NSW + 2 * w + b; }
+__host__ __device__ constexpr int B_RFULL(int g) { return 3 * NP + g; } // group g's raw tiles in
+__host__ __device__ constexpr int B_HFULL(int w, int b) { return 3 * NP + NGRP + 2 * w + b; }
+__host__ __device__ constexpr int B_HEMPTY(int w, int b) { return 3 * NP + NGRP + 2 * NSW + 2 * w + b; }
 
 struct TcParams {
     const float *beta, *h0;
@@ -177,7 +191,8 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
         : "=r"(ok) : "r"(a), "r"(parity) : "memory");
     return ok != 0;
 }
@@ -191,14 +206,15 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t a, uint32_t parity) {
 }
 // Bounded wait. Returns false when this or any other wait of the grid gave up.
 template <bool kClusterScope>
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity,
+                                          long long limit = kWaitLimit) {
     if (kClusterScope ? mbar_try_cluster(a, parity) : mbar_try(a, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (kClusterScope ? mbar_try_cluster(a, parity) : mbar_try(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*(volatile unsigned int *)&g_device_flags != 0u) return false;
-            if (clock64() - t0 > kWaitLimit) {
+            if (clock64() - t0 > limit) {
                 atomicOr(&g_device_flags, 1u);
                 return false;
             }
@@ -255,10 +271,11 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
 }
-__device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2,
-                                          uint32_t r3) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};"
-                 ::"r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+// transpose of an 8 x 8 b16 matrix held in mma fragment layout (one warp)
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 // D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
@@ -287,21 +304,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
                  "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
-                                             uint32_t src) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
-        ::"l"(map), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_le1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Item for this cluster: sequences ordered longest first (ties by index), heads
@@ -332,7 +334,7 @@ template <bool kShare>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
+                  const TcParams p) {
     extern __shared__ __align__(128) unsigned char sm[];
     const uint32_t sbase = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -346,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (t1 - t0 + C - 1) / C;
     auto bar = [&](int i) { return sbase + SM_BAR + 8u * (uint32_t)i; };
     auto owner = [&](int n) -> uint32_t { return kShare ? (uint32_t)(n % kCS) : rank; };
+    const int nstep = kShare ? kCS : 1;  // distance between consecutive owned chunks
+    const int first = kShare ? (int)rank : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_FREE(s)), 2 * NSW);  // state and output warps
             mbar_init(bar(B_CFREE(s)), kShare ? kCS : 1);
         }
-        for (int s = 0; s < NR; ++s) mbar_init(bar(B_RFULL(s)), 1);
+        for (int g = 0; g < NGRP; ++g) mbar_init(bar(B_RFULL(g)), 1);
         for (int w = 0; w < NSW; ++w)
             for (int b = 0; b < 2; ++b) {
                 mbar_init(bar(B_HFULL(w, b)), 1);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
 #ifdef KDA_TC_TRACE
-    for (int i = threadIdx.x; i < 64 * 16; i += blockDim.x)
+    for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x)
         reinterpret_cast<long long *>(sm + SM_TRACE)[i] = 0;
 #endif
     if (kShare) cluster_sync(); else __syncthreads();
@@ -382,7 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             KDA_TRACE(n, 1);
             const bool mine = owner(n) == rank;
-            const int c0 = t0 + n * C;
             if (lane == 0) {
                 if (n >= NP) {  // chunk n - NP (same slot, same owner) is consumed here
                     if (kShare)
@@ -391,69 +394,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(bar(B_CFREE(s)));
                 }
                 mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
-                tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head, c0,
+                tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head, t0 + n * C,
                             bar(B_FULL(s)));
             }
             __syncwarp();
         }
-    } else if (warp <= NPW) {
-        // ------------------------------------------------ prologue (4 warps, 128 threads)
-        const int c = threadIdx.x - 32;  // key channel of the gate pass
-        const int pw = warp - 1;
+    } else if (warp < W_STATE0) {
+        // ------------------------------------------------ prologue groups
+        // Group g handles every other owned chunk (owned index j with j % 2 == g).
+        const int g = (warp - 1) / NPW;
+        const int pw = (warp - 1) % NPW;
+        const int c = threadIdx.x - 32 - 32 * NPW * g;  // key channel of the gate pass
         const int nt = 32 * NPW;
-        unsigned char *KtB = sm + SM_KT;  // K~ [c][t]
-        unsigned char *KhB = sm + SM_KH;  // K^ [c][t]
-        const uint32_t Kt_s = sbase + SM_KT, Kh_s = sbase + SM_KH;
-        float *As = reinterpret_cast<float *>(sm + SM_A);
+        const int bar_id = 1 + g;
+        unsigned char *gs = sm + SM_GS + g * GS_BYTES;
+        unsigned char *KtB = gs + GS_KT;  // K~ [c][t]
+        unsigned char *KhB = gs + GS_KH;  // K^ [c][t]
+        const uint32_t Kt_s = smem_u32(KtB), Kh_s = smem_u32(KhB);
+        float *As = reinterpret_cast<float *>(gs + GS_A);
         const int i8 = lane >> 3, r8 = lane & 7;
-        const int nstep = kShare ? kCS : 1;
-        // beta of owned chunk n (zero past the end) into buffer b, by warp 1's lanes
-        // 0-15 with cp.async, which no barrier or fence of another thread waits for
-        auto fetch_beta = [&](int n, int b) {
-            if (pw == 1 && lane < C && n < nchunks) {
-                const int row = t0 + n * C + lane;
-                const bool in = row < t1;
-                cp_async_4(sbase + SM_BETA + (b * C + lane) * 4,
-                           p.beta + (size_t)(in ? row : t0) * H + head, in ? 4u : 0u);
-            }
-            if (pw == 1) asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        // q, k and gate-logit tiles of owned chunk n into raw slot rs, by TMA (thread 0)
-        auto fetch_raw = [&](int n, int rs) {
-            if (c == 0 && n < nchunks) {
-                const uint32_t dst = sbase + SM_RAW + rs * RAW_STRIDE;
-                const int c0n = t0 + n * C;
-                mbar_arrive_tx(bar(B_RFULL(rs)), RAW_TMA_BYTES);
-                tma_load_3d(dst + RAW_Q, &tm_q, 0, head, c0n, bar(B_RFULL(rs)));
-                tma_load_3d(dst + RAW_K, &tm_k, 0, head, c0n, bar(B_RFULL(rs)));
-                tma_load_3d(dst + RAW_A, &tm_a, 0, head, c0n, bar(B_RFULL(rs)));
+        const uint32_t raw_s = sbase + SM_RAW + g * RAW_BYTES;
+        const unsigned char *raw = sm + SM_RAW + g * RAW_BYTES;
+        // q, k and gate-logit tiles of chunk n into this group's raw slot (thread 0),
+        // beta of chunk n into beta buffer b (warp 1's lanes 0-15, cp.async, which no
+        // barrier or fence of another thread waits for)
+        auto fetch = [&](int n, int b) {
+            if (n >= nchunks) return;
+            const int c0n = t0 + n * C;
+            if (c == 0) {
+                mbar_arrive_tx(bar(B_RFULL(g)), RAW_BYTES);
+                tma_load_3d(raw_s + RAW_Q, &tm_q, 0, head, c0n, bar(B_RFULL(g)));
+                tma_load_3d(raw_s + RAW_K, &tm_k, 0, head, c0n, bar(B_RFULL(g)));
+                tma_load_3d(raw_s + RAW_A, &tm_a, 0, head, c0n, bar(B_RFULL(g)));
                 KDA_TRACE(n, 2);
             }
+            if (pw == 1) {
+                if (lane < C) {
+                    const int row = c0n + lane;
+                    const bool in = row < t1;
+                    cp_async_4(smem_u32(gs + GS_BETA) + (b * C + lane) * 4,
+                               p.beta + (size_t)(in ? row : t0) * H + head, in ? 4u : 0u);
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
         };
-        fetch_beta(kShare ? (int)rank : 0, 0);
-        fetch_raw(kShare ? (int)rank : 0, 0);
-        int owned = 0;
-        for (int n = 0; n < nchunks; ++n) {
-            if (owner(n) != rank) continue;
-            const int rs = owned % NR, ru = owned / NR;
-            ++owned;
+        fetch(first + g * nstep, 0);
+        int k = 0;  // chunks this group has processed
+        for (int n = first + g * nstep; n < nchunks; n += NGRP * nstep, ++k) {
             const int s = n % NP, use = n / NP;
             const int c0 = t0 + n * C;
             const int L = min(C, t1 - c0);
             if (c == 0) KDA_TRACE(n, 3);
-            // the next owned chunk's tiles go into the slot the previous one used
-            fetch_raw(n + nstep, owned % NR);
-            bool bad = !mbar_wait<false>(bar(B_RFULL(rs)), ru & 1);
-            bad |= !mbar_wait<true>(bar(B_CFREE(s)), (use & 1) ^ 1);
-            if (named_sync_or(1, nt, bad)) break;
-            if (c == 0) KDA_TRACE(n, 4);
-            const float *bs = reinterpret_cast<const float *>(sm + SM_BETA) + ((owned - 1) & 1) * C;
+            // one thread waits on the pipeline; the rest of the group blocks on the
+            // hardware named barrier, then observes the completed phases once
+            bool bad = false;
+            if (c == 0) {
+                bad = !mbar_wait<false>(bar(B_RFULL(g)), k & 1);
+                bad |= !mbar_wait<true>(bar(B_CFREE(s)), (use & 1) ^ 1);
+            }
             if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's beta
-            fetch_beta(n + nstep, owned & 1);                               // next owned chunk's
+            if (named_sync_or(bar_id, nt, bad)) break;
+            if (c != 0) {  // acquire the completed phases (they do not block now)
+                mbar_try(bar(B_RFULL(g)), k & 1);
+                mbar_try_cluster(bar(B_CFREE(s)), (use & 1) ^ 1);
+            }
+            if (c == 0) KDA_TRACE(n, 4);
+            const float *bs = reinterpret_cast<const float *>(gs + GS_BETA) + (k & 1) * C;
             unsigned char *slot = sm + SM_PROD + s * SLOT_BYTES;
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             float *Pg = reinterpret_cast<float *>(slot + OFF_PG);
-            const unsigned char *raw = sm + SM_RAW + rs * RAW_STRIDE;
             const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_Q);
             const __nv_bfloat16 *rk = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_K);
             const float *ra = reinterpret_cast<const float *>(raw + RAW_A);
@@ -490,20 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(slot + OFF_PQ + cmaj(c, 8)) = make_uint4(wq[4], wq[5], wq[6], wq[7]);
                 *reinterpret_cast<uint4 *>(KtB + cmaj(c, 0)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
                 *reinterpret_cast<uint4 *>(KtB + cmaj(c, 8)) = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-                Pg[gperm(c)] = gam;                         // gamma_L = exp(G_L)
+                Pg[gperm(c)] = gam;                    // gamma_L = exp(G_L)
                 const float inv_gl = rcp_approx(gam);  // exp(-G_L) <= exp(80)
-                float suf = 1.f;                            // exp(G_L - G_r)
+                float suf = 1.f;                       // exp(G_L - G_r)
                 uint32_t wp[C / 2], wh[C / 2];
-                float hp = 0.f, hh = 0.f;
+                float hp = 0.f, hk = 0.f;
 #pragma unroll
                 for (int r = C - 1; r >= 0; --r) {
                     const float kp = kk[r] * suf, kh = kk[r] * (suf * inv_gl);
                     if (r & 1) {
                         hp = kp;
-                        hh = kh;
+                        hk = kh;
                     } else {
                         wp[r >> 1] = pack_bf16(kp, hp);
-                        wh[r >> 1] = pack_bf16(kh, hh);
+                        wh[r >> 1] = pack_bf16(kh, hk);
                     }
                     suf *= eg[r];
                 }
@@ -512,8 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(KhB + cmaj(c, 0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
                 *reinterpret_cast<uint4 *>(KhB + cmaj(c, 8)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
             }
-            named_sync(1, nt);
+            named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 5);
+            // the raw slot is free again: request this group's next chunk now
+            fetch(n + NGRP * nstep, (k + 1) & 1);
             // -- A = strict_lower(beta K~ K^^T) on warps 0, 1 and P = lower(Q~ K^^T) on
             //    warps 2, 3; each warp one 8-token column tile (j in [8 jh, 8 jh + 8))
             {
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            named_sync(1, nt);
+            named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 6);
             // -- TB = (I + A)^-1 diag(beta): forward substitution, one column per lane
             if (pw == 0 && lane < C) {
@@ -567,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < C; ++r) Ptb[r * LDS + j] = __float2bfloat16_rn(x[r] * bj);
             }
-            named_sync(1, nt);
+            named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 7);
             // -- -W = -TB K~: warp pw covers key channels [32 pw, 32 pw + 32)
             {
@@ -593,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async();  // generic writes of the slot -> async-proxy bulk reads
-            named_sync(1, nt);
+            named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 8);
             if (c == 0) {
                 if (kShare) {
@@ -608,11 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 KDA_TRACE(n, 9);
             }
         }
-    } else if (warp <= NPW + NSW) {
+        if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else if (warp < W_OUT0) {
         // ------------------------------------------------ state warps
-        // Own 16 rows of S^T for the whole sequence. Per chunk: U^T, then hand the
-        // bf16 S^T and U^T fragments to the paired output warp, then update S^T.
-        const int sw = warp - 1 - NPW;  // 0 .. NSW-1
+        // State warp sw owns value columns [vrow0, vrow0 + 16) of the state, i.e. 16
+        // rows of S^T over all 128 key channels, in registers for the whole sequence.
+        // Per chunk: U^T = V^T TB^T - S^T W^T, then S^T <- S^T diag(gamma_L) + U^T K'.
+        // The bf16 S^T (before the update) and U^T fragments go to the paired output
+        // warp, which forms the output; nothing on this serial chain waits for it.
+        const int sw = warp - W_STATE0;
         const int vrow0 = (int)rank * VB + sw * 16;  // first value column (row of S^T)
         const int g4 = lane >> 2, l4 = lane & 3;
         const int i8 = lane >> 3, r8 = lane & 7;
@@ -640,7 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             const float *Pg = reinterpret_cast<const float *>(sm + SM_PROD + s * SLOT_BYTES + OFF_PG);
             const uint32_t vs = sbase + SM_V + s * V_BYTES;
-
             // operand fragments for U^T: V^T, TB^T and (-W)^T, all loads first
             uint32_t va[4], tb[4], wf[8][4];
             {
@@ -664,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // U^T = V^T TB^T + S^T (-W)^T, four independent accumulator chains
             float accU[2][2][4] = {};  // [k parity][token n-tile][frag]
-            mma16816(accU[0][0], va, tb[0], tb[1]);
-            mma16816(accU[0][1], va, tb[2], tb[3]);
+            mma16816(accU[1][0], va, tb[0], tb[1]);
+            mma16816(accU[1][1], va, tb[2], tb[3]);
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt) {
                 mma16816(accU[kt & 1][0], Sa[kt], wf[kt][0], wf[kt][1]);
@@ -689,14 +703,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S^T <- S^T diag(gamma_L) + U^T K'
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
-                const float4 g = gl[np];  // columns 16np + 2l4 (+1), 16np + 8 + 2l4 (+1)
+                const float4 g = gl[np];  // channels 16np + 2l4 (+1), 16np + 8 + 2l4 (+1)
                 S[2 * np][0] *= g.x; S[2 * np][1] *= g.y; S[2 * np][2] *= g.x; S[2 * np][3] *= g.y;
                 S[2 * np + 1][0] *= g.z; S[2 * np + 1][1] *= g.w;
                 S[2 * np + 1][2] *= g.z; S[2 * np + 1][3] *= g.w;
                 mma16816(S[2 * np], Ua, kf[np][0], kf[np][1]);
                 mma16816(S[2 * np + 1], Ua, kf[np][2], kf[np][3]);
             }
-            // hand S^T (before this chunk's update) and U^T to the output warp
+            // every read of the slot by this warp is done (fragments are in registers)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
+            // hand the bf16 S^T (before this chunk's update) and U^T to the output warp:
+            // plain stores, then a release on the handoff barrier; no wait unless the
+            // output warp is two chunks behind
             ok = mbar_wait<false>(bar(B_HEMPTY(sw, hb)), ((n >> 1) & 1) ^ 1);
             if (__any_sync(0xffffffffu, !ok)) break;
             {
@@ -709,10 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_HFULL(sw, hb)));
-            // every read of the slot by this warp is done
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
         }
         if (p.h_final) {
 #pragma unroll
@@ -727,13 +743,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ output warps
         // O^T = S^T Q~^T + U^T P^T for the paired state warp's 16 value columns, scaled
-        // by d_k^-1/2, then a TMA store of the 16-token x 16-column tile.
-        const int ow = warp - 1 - NPW - NSW;  // pairs with state warp ow
+        // by d_k^-1/2; the 16 x 16 tile is transposed in registers (movmatrix) and
+        // written with 4-byte global stores, rows past the sequence end skipped.
+        const int ow = warp - W_OUT0;  // pairs with state warp ow
         const int vrow0 = (int)rank * VB + ow * 16;
+        const int g4 = lane >> 2, l4 = lane & 3;
         const int i8 = lane >> 3, r8 = lane & 7;
         const float scale = rsqrtf((float)D);
-        const uint32_t ost_s = sbase + SM_OST + ow * 2 * OST_BYTES;
-        const __nv_bfloat16 *ost = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_OST) + ow * 2 * C * 16;
         for (int n = 0; n < nchunks; ++n) {
             const int s = n % NP, use = n / NP;
             const int hb = n & 1;
@@ -775,47 +791,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma16816(accO[0][1], Ua, pf[2], pf[3]);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FREE(s)));
-            // output tile: scale, bf16, transpose into a staging tile, TMA store
-            {
-                const int buf = n & 1;
-                if (lane == 0) bulk_wait_read_le1();  // the store issued 2 chunks ago has read it
-                __syncwarp();
-                uint32_t o0 = pack_bf16(scale * (accO[0][0][0] + accO[1][0][0]),
-                                        scale * (accO[0][0][1] + accO[1][0][1]));
-                uint32_t o1 = pack_bf16(scale * (accO[0][0][2] + accO[1][0][2]),
-                                        scale * (accO[0][0][3] + accO[1][0][3]));
-                uint32_t o2 = pack_bf16(scale * (accO[0][1][0] + accO[1][1][0]),
-                                        scale * (accO[0][1][1] + accO[1][1][1]));
-                uint32_t o3 = pack_bf16(scale * (accO[0][1][2] + accO[1][1][2]),
-                                        scale * (accO[0][1][3] + accO[1][1][3]));
-                // matrices: (v 0-7, t 0-7), (v 8-15, t 0-7), (v 0-7, t 8-15), (v 8-15, t 8-15)
-                const int t = (i8 >> 1) * 8 + r8, vv = (i8 & 1) * 8;
-                const uint32_t tile = ost_s + buf * OST_BYTES;
-                stsm_x4_t(tile + (t * 16 + vv) * 2, o0, o1, o2, o3);
-                const int c0 = t0 + n * C;
-                const int L = min(C, t1 - c0);
-                if (L == C) {
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&tm_o, vrow0, head, c0, tile);
-                        bulk_commit();
-                    }
-                } else {  // partial last chunk: plain stores of the valid rows only
-                    __syncwarp();
-                    const int tt = lane >> 1, hv = (lane & 1) * 8;
-                    if (tt < L) {
-                        const uint4 val = *reinterpret_cast<const uint4 *>(ost + buf * C * 16 + tt * 16 + hv);
-                        *reinterpret_cast<uint4 *>(p.out + ((size_t)(c0 + tt) * H + head) * D +
-                                                   vrow0 + hv) = val;
-                    }
+            // 8x8 blocks (value rows x tokens) transposed to (tokens x value columns)
+            const int c0 = t0 + n * C;
+            const int L = min(C, t1 - c0);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hv = 0; hv < 2; ++hv) {
+                    const uint32_t blk = movm_t(pack_bf16(
+                        scale * (accO[0][nt][2 * hv] + accO[1][nt][2 * hv]),
+                        scale * (accO[0][nt][2 * hv + 1] + accO[1][nt][2 * hv + 1])));
+                    const int t = nt * 8 + g4;
+                    if (t < L)
+                        *reinterpret_cast<uint32_t *>(p.out + ((size_t)(c0 + t) * H + head) * D +
+                                                      vrow0 + hv * 8 + 2 * l4) = blk;
                 }
-                __syncwarp();
-                if (lane == 0) KDA_TRACE(n, 14 + ow);
-            }
+            if (ow == 0 && lane == 0) KDA_TRACE(n, 14);
         }
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
     }
     // no CTA may leave while a peer can still write into its shared memory
     __syncwarp();
@@ -823,9 +815,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef KDA_TC_TRACE
     __syncthreads();
     if (blockIdx.x < 4)
-        for (int i = threadIdx.x; i < 64 * 16; i += blockDim.x)
-            g_trace[blockIdx.x][i / 16][i % 16] = reinterpret_cast<long long *>(sm + SM_TRACE)[i];
+        for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x)
+            g_trace[blockIdx.x][i / 32][i % 32] = reinterpret_cast<long long *>(sm + SM_TRACE)[i];
 #endif
+}
+
+// A wait on an mbarrier that nothing ever completes: exercises the bounded-wait path
+// (flag set, wait returns) without any fault. One thread; `limit` in SM cycles.
+__global__ void bounded_wait_selftest_kernel(long long limit, int *returned) {
+    __shared__ __align__(8) unsigned long long mbar;
+    const uint32_t a = smem_u32(&mbar);
+    mbar_init(a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const bool completed = mbar_wait<false>(a, 0, limit);
+    *returned = completed ? 2 : 1;  // 1: gave up as designed
 }
 
 // ------------------------------------------------------------------ host side
@@ -843,7 +846,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x) {
+bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x,
+                int box_t = C) {
     // [n_tok][H][128] row-major viewed as a 3-D tensor (channel, head, token); boxes
     // are box_x channels x 1 head x 16 tokens. Out-of-range tokens read as zero.
     auto enc = tensor_map_encoder();
@@ -851,7 +855,7 @@ bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H
     const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)n_tok};
     cuuint64_t strides[2] = {D * es, (cuuint64_t)H * D * es};
-    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_t};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estr,
@@ -862,12 +866,11 @@ bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H
 
 template <bool kShare>
 cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
-    CUtensorMap mq, mk, ma, mv, mo;
+    CUtensorMap mq, mk, ma, mv;
     if (!encode_map(&mq, a.q, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&mk, a.k, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&ma, a.a, true, a.n_tok, a.n_heads, D) ||
-        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB) ||
-        !encode_map(&mo, a.out, false, a.n_tok, a.n_heads, 16))
+        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel<kShare>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -888,7 +891,7 @@ cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel<kShare>, mq, mk, ma, mv, mo, p);
+    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel<kShare>, mq, mk, ma, mv, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
@@ -913,6 +916,13 @@ extern "C" int kda_debug_trace_dump(long long *host) {
     return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
 }
 #endif
+
+cudaError_t bounded_wait_selftest(long long limit_cycles, int *d_returned, cudaStream_t stream) {
+    bounded_wait_selftest_kernel<<<1, 1, 0, stream>>>(limit_cycles, d_returned);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_device_flags, sizeof(unsigned int), 0,

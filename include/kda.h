@@ -94,6 +94,18 @@ uint64_t kda_kernel_launch_count(void);
 kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream);
 
 /*
+ * kda_selftest_bounded_wait -- failure-detection self-test; no counterpart in the
+ * method. Launches one thread that waits on a pipeline barrier nothing will ever
+ * complete, through the same bounded-wait routine the tensor-core kernel uses, with
+ * a limit of `limit_cycles` SM cycles. The wait gives up, sets bit 0 of the device
+ * status word (see kda_read_device_flags) and the kernel writes 1 to the int32 at
+ * device address `d_returned` (2 would mean the wait wrongly completed). Nothing
+ * faults, traps or hangs. Returns KDA_ERR_INVALID_ARG for a NULL `d_returned` or a
+ * non-positive limit, KDA_ERR_CUDA if the launch fails.
+ */
+kda_status kda_selftest_bounded_wait(int64_t limit_cycles, int32_t *d_returned, void *stream);
+
+/*
  * kda_chunk_fwd -- the chunked forward pass (all of the operation above).
  *
  * Kernel choice is made from the arguments, not from any global setting:
