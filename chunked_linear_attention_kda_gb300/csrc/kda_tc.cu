@@ -85,9 +85,22 @@ constexpr int NSW = VB / 16;    // state warps per CTA (2), 16 value columns eac
                                 // many output warps
 constexpr int NGRP = 2;         // prologue groups, alternating owned chunks
 constexpr int NPW = 4;          // warps per prologue group (one key channel per thread)
-constexpr int W_STATE0 = 1 + NGRP * NPW;  // first state warp
-constexpr int W_OUT0 = W_STATE0 + NSW;    // first output warp
-constexpr int kThreads = 32 * (W_OUT0 + NSW);
+// Warp roles by warpgroup: 0 = producer warp (+ 3 idle warps), 1 and 2 = the prologue
+// groups, 3 = state warps then output warps.
+constexpr int W_PRO0 = 4;                      // first prologue warp
+constexpr int W_STATE0 = W_PRO0 + NGRP * NPW;  // first state warp
+constexpr int W_OUT0 = W_STATE0 + NSW;         // first output warp
+constexpr int kThreads = 32 * (W_OUT0 + NSW);  // 512
+// Registers per thread. The block is launched with kRegsLaunch for every thread; each
+// warpgroup then moves to its own allotment (setmaxnreg), and the allotments add up to
+// the launch total, so every increase is covered by the decreases. The state and output
+// warps need the room: 64 fp32 state values plus their bf16 copy plus ~100 registers of
+// operand fragments are live at once.
+constexpr int kRegsLaunch = 128, kRegsProducer = 40, kRegsPrologue = 120, kRegsConsumer = 232;
+static_assert(kThreads == 512 && NGRP == 2 && NPW == 4 && NSW == 2, "one warpgroup per role");
+static_assert(kRegsProducer + NGRP * kRegsPrologue + kRegsConsumer == 4 * kRegsLaunch,
+              "warpgroup register allotments must add up to the launch allotment");
+static_assert(kRegsLaunch * kThreads == 65536, "the launch takes the whole register file");
 constexpr int NP = 8;           // product-ring depth (multiple of kCS)
 constexpr int LDP = 136;        // pitch (elements) of 16 x 128 bf16 tiles: 272 B rows
 constexpr int LDS = 24;         // pitch of 16 x 16 bf16 tiles: 48 B rows
@@ -285,6 +298,15 @@ __device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// warpgroup-wide register reallocation; all four warps of the warpgroup execute it
+template <int R>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
 __device__ __forceinline__ float ex2_approx(float x) {  // 2^x, flushes denormals
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -371,40 +393,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
     if (kShare) cluster_sync(); else __syncthreads();
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer warp
-        // Lane 0 loads the v tiles by TMA and forwards slot releases to the slot's
-        // owner (the owner's prologue loads q, k and the gate logits itself). Releases
-        // travel through this thread because a cluster-scope release waits for all of
-        // the issuing thread's earlier generic memory operations, and this thread has
-        // none in flight (TMA belongs to the async proxy).
-        for (int n = 0; n < nchunks; ++n) {
-            const int s = n % NP, use = n / NP;
-            KDA_TRACE(n, 0);
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            KDA_TRACE(n, 1);
-            const bool mine = owner(n) == rank;
+    if (warp < W_PRO0) {
+        regs_decrease<kRegsProducer>();
+        if (warp == 0) {
+            // -------------------------------------------- producer warp
+            // Lane 0 loads the v tiles by TMA once the slot is free locally (the owner's
+            // prologue loads q, k and the gate logits itself).
+            for (int n = 0; n < nchunks; ++n) {
+                const int s = n % NP, use = n / NP;
+                KDA_TRACE(n, 0);
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                KDA_TRACE(n, 1);
+                if (lane == 0) {
+                    const bool mine = owner(n) == rank;
+                    mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
+                    tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head,
+                                t0 + n * C, bar(B_FULL(s)));
+                }
+                __syncwarp();
+            }
+        } else if (warp == 1) {
+            // -------------------------------------------- release forwarder
+            // Lane 0 tells the owner of chunk n - NP that this CTA has consumed it, so that
+            // the owner may overwrite the slot with chunk n. A cluster-scope release waits
+            // for the issuing thread's earlier memory operations -- including, as
+            // measured, TMA loads still in flight -- so it is issued by a thread that
+            // has no memory operations of its own.
             if (lane == 0) {
-                if (n >= NP) {  // chunk n - NP (same slot, same owner) is consumed here
+                for (int n = NP; n < nchunks; ++n) {
+                    const int s = n % NP, use = n / NP;
+                    if (!mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1)) break;
                     if (kShare)
                         mbar_arrive_remote(map_to_rank(bar(B_CFREE(s)), owner(n)));
                     else
                         mbar_arrive(bar(B_CFREE(s)));
                 }
-                mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
-                tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head, t0 + n * C,
-                            bar(B_FULL(s)));
             }
             __syncwarp();
         }
+        // warps 2 and 3 only hold registers back for the consumers
     } else if (warp < W_STATE0) {
+        regs_decrease<kRegsPrologue>();
         // ------------------------------------------------ prologue groups
         // Group g handles every other owned chunk (owned index j with j % 2 == g).
-        const int g = (warp - 1) / NPW;
-        const int pw = (warp - 1) % NPW;
-        const int c = threadIdx.x - 32 - 32 * NPW * g;  // key channel of the gate pass
+        const int g = (warp - W_PRO0) / NPW;
+        const int pw = (warp - W_PRO0) % NPW;
+        const int c = threadIdx.x - 32 * (W_PRO0 + NPW * g);  // key channel of the gate pass
         const int nt = 32 * NPW;
         const int bar_id = 1 + g;
         unsigned char *gs = sm + SM_GS + g * GS_BYTES;
@@ -620,7 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
-    } else if (warp < W_OUT0) {
+    } else {
+        regs_increase<kRegsConsumer>();
+        if (warp < W_OUT0) {
         // ------------------------------------------------ state warps
         // State warp sw owns value columns [vrow0, vrow0 + 16) of the state, i.e. 16
         // rows of S^T over all 128 key channels, in registers for the whole sequence.
@@ -808,6 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             if (ow == 0 && lane == 0) KDA_TRACE(n, 14);
         }
+        }
     }
     // no CTA may leave while a peer can still write into its shared memory
     __syncwarp();
@@ -875,6 +914,12 @@ cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel<kShare>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register increase is only covered when the block is launched with
+    // exactly kRegsLaunch registers per thread; with fewer it could never be granted.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kda_tc_kernel<kShare>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     TcParams p;
     p.beta = a.beta; p.h0 = a.h0; p.cu = a.cu_seqlens;
     p.out = reinterpret_cast<__nv_bfloat16 *>(a.out); p.h_final = a.h_final;
