@@ -49,12 +49,12 @@ namespace kda {
 
 __device__ unsigned int g_device_flags;  // bit 0: a pipeline wait exceeded its limit
 
-// Phase timestamps (SM clock) of the first cluster, first 64 chunks: a profiling aid
+// Phase timestamps (SM clock) of the first cluster, first 32 chunks: a profiling aid
 // compiled only with -DKDA_TC_TRACE; the default build has no trace code. Stamps go to
 // shared memory and are copied out when the CTA finishes, so that tracing adds no
 // global stores to the pipeline.
 #ifdef KDA_TC_TRACE
-__device__ long long g_trace[4][64][32];
+__device__ long long g_trace[4][32][16];
 __device__ __forceinline__ long long trace_clock() {
 #ifdef KDA_TC_TRACE_GLOBALTIMER
     long long t;
@@ -66,8 +66,8 @@ __device__ __forceinline__ long long trace_clock() {
 }
 #define KDA_TRACE(n, slot)                                                              \
     do {                                                                                \
-        if ((n) < 64)                                                                   \
-            reinterpret_cast<long long *>(sm + SM_TRACE)[(n) * 32 + (slot)] = trace_clock(); \
+        if ((n) < 32)                                                                   \
+            reinterpret_cast<long long *>(sm + SM_TRACE)[(n) * 16 + (slot)] = trace_clock(); \
     } while (0)
 #else
 #define KDA_TRACE(n, slot) \
@@ -144,36 +144,46 @@ constexpr int HO_BYTES = 32 * HO_LANE;
 constexpr int SM_RAW = 0;
 constexpr int SM_V = SM_RAW + NGRP * RAW_BYTES;
 constexpr int SM_PROD = SM_V + NP * V_BYTES;
-constexpr int SM_GS = SM_PROD + NP * SLOT_BYTES;
+constexpr int SM_STAGE = SM_PROD + NP * SLOT_BYTES;  // one product staging buffer per group
+constexpr int SM_GS = SM_STAGE + NGRP * SLOT_BYTES;
 constexpr int SM_HO = (SM_GS + NGRP * GS_BYTES + 127) / 128 * 128;
 constexpr int SM_BAR = SM_HO + NSW * 2 * HO_BYTES;
-constexpr int NBARS = 3 * NP + NGRP + 4 * NSW;
+constexpr int NBARS = 2 * NP + NGRP * kCS + 2 * NGRP + 4 * NSW;
 constexpr int SM_MISC = SM_BAR + NBARS * 8;
 #ifdef KDA_TC_TRACE
 constexpr int SM_TRACE = SM_MISC + 64;
-constexpr int SMEM_BYTES = SM_TRACE + 64 * 32 * 8;
+constexpr int SMEM_BYTES = SM_TRACE + 32 * 16 * 8;
 #else
 constexpr int SMEM_BYTES = SM_MISC + 64;
 #endif
 static_assert(RAW_BYTES % 128 == 0 && SM_V % 128 == 0 && SM_PROD % 128 == 0, "TMA alignment");
-static_assert(SM_GS % 16 == 0 && GS_BYTES % 16 == 0 && SM_HO % 16 == 0, "alignment");
+static_assert(SM_STAGE % 16 == 0 && SM_GS % 16 == 0 && GS_BYTES % 16 == 0 && SM_HO % 16 == 0,
+              "alignment");
 static_assert(SM_BAR % 8 == 0, "alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
-// gamma_L[c], c = 16 np + 8 h + 2 l4 + e, is stored at 32 l4 + 4 np + 2 h + e so that
-// the lanes holding S^T columns 2 l4 (+1, +8, +9) of every 16-column group read
-// their decay factors as contiguous float4
+// gamma_L[c], c = 16 np + 8 h + 2 l4 + e, is stored at 16 np + 4 l4 + 2 h + e: the lane
+// holding S^T columns 2 l4 (+1, +8, +9) of 16-column group np reads its four decay
+// factors as one float4, and the four lanes l4 = 0..3 read 64 contiguous bytes (one
+// conflict-free shared-memory access)
 __host__ __device__ constexpr int gperm(int c) {
-    return ((c >> 1) & 3) * 32 + (c >> 4) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
+    return ((c >> 4) * 4 + ((c >> 1) & 3)) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
 }
 
-// barrier indices
-__host__ __device__ constexpr int B_FULL(int s) { return s; }           // products + V in
-__host__ __device__ constexpr int B_FREE(int s) { return NP + s; }      // local state warps done
-__host__ __device__ constexpr int B_CFREE(int s) { return 2 * NP + s; } // all CTAs done (owner)
-__host__ __device__ constexpr int B_RFULL(int g) { return 3 * NP + g; } // group g's raw tiles in
-__host__ __device__ constexpr int B_HFULL(int w, int b) { return 3 * NP + NGRP + 2 * w + b; }
-__host__ __device__ constexpr int B_HEMPTY(int w, int b) { return 3 * NP + NGRP + 2 * NSW + 2 * w + b; }
+// Barrier indices. Slot s of every CTA is filled by CTA s % kCS (the owner of the chunks
+// n with n % NP == s), from the staging buffer of its group s / kCS.
+__host__ __device__ constexpr int B_FULL(int s) { return s; }       // products + V of slot s in
+__host__ __device__ constexpr int B_FREE(int s) { return NP + s; }  // local consumers done with s
+// (owner side) CTA p has consumed the previous chunk of the group-g slot
+__host__ __device__ constexpr int B_PFREE(int g, int p) { return 2 * NP + kCS * g + p; }
+// (owner side) all CTAs have received group g's last copy: its staging buffer is free
+__host__ __device__ constexpr int B_RECV(int g) { return 2 * NP + kCS * NGRP + g; }
+__host__ __device__ constexpr int B_RFULL(int g) { return 2 * NP + kCS * NGRP + NGRP + g; }  // raw tiles
+__host__ __device__ constexpr int B_HFULL(int w, int b) { return 2 * NP + kCS * NGRP + 2 * NGRP + 2 * w + b; }
+__host__ __device__ constexpr int B_HEMPTY(int w, int b) {
+    return 2 * NP + kCS * NGRP + 2 * NGRP + 2 * NSW + 2 * w + b;
+}
+static_assert(NP == NGRP * kCS, "each slot belongs to one group of one owner");
 
 struct TcParams {
     const float *beta, *h0;
@@ -201,10 +211,27 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// Remote arrive without release semantics. Measured: a cluster-scope release arrive
+// costs the issuing thread well over a thousand cycles, which paced the whole pipeline.
+// Used only for signals that order no memory accesses of their own: "the slot's reads
+// have completed" (the values were already consumed) and "the copy has landed".
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    return ok != 0;
+}
+// non-blocking probe of a phase (never suspends the thread)
+__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
         "selp.u32 %0, 1, 0, p; }"
         : "=r"(ok) : "r"(a), "r"(parity) : "memory");
     return ok != 0;
@@ -307,6 +334,12 @@ template <int R>
 __device__ __forceinline__ void regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
+// (a, b) *= (ga, gb) as one packed f32x2 multiply
+__device__ __forceinline__ void mul2(float &a, float &b, float ga, float gb) {
+    asm("{ .reg .b64 x, y; mov.b64 x, {%0, %1}; mov.b64 y, {%2, %3}; mul.rn.f32x2 x, x, y; "
+        "mov.b64 {%0, %1}, x; }"
+        : "+f"(a), "+f"(b) : "f"(ga), "f"(gb));
+}
 __device__ __forceinline__ float ex2_approx(float x) {  // 2^x, flushes denormals
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -352,7 +385,6 @@ __device__ void resolve_item(const TcParams &p, int ci, int *seq_out, int *head_
     __syncthreads();
 }
 
-template <bool kShare>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v,
@@ -360,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(128) unsigned char sm[];
     const uint32_t sbase = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = kShare ? cluster_rank() : (uint32_t)(blockIdx.x % kCS);
+    const uint32_t rank = cluster_rank();
     const int ci = blockIdx.x / kCS;
     int *misc = reinterpret_cast<int *>(sm + SM_MISC);
     resolve_item(p, ci, &misc[0], &misc[1]);
@@ -369,17 +401,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t0 = p.cu[seq], t1 = p.cu[seq + 1];
     const int nchunks = (t1 - t0 + C - 1) / C;
     auto bar = [&](int i) { return sbase + SM_BAR + 8u * (uint32_t)i; };
-    auto owner = [&](int n) -> uint32_t { return kShare ? (uint32_t)(n % kCS) : rank; };
-    const int nstep = kShare ? kCS : 1;  // distance between consecutive owned chunks
-    const int first = kShare ? (int)rank : 0;
+    auto owner = [&](int n) -> uint32_t { return (uint32_t)(n % kCS); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
-            mbar_init(bar(B_FULL(s)), owner(s) == rank ? 2 : 1);
+            mbar_init(bar(B_FULL(s)), 1);        // producer (expects V and the product copy)
             mbar_init(bar(B_FREE(s)), 2 * NSW);  // state and output warps
-            mbar_init(bar(B_CFREE(s)), kShare ? kCS : 1);
         }
-        for (int g = 0; g < NGRP; ++g) mbar_init(bar(B_RFULL(g)), 1);
+        for (int g = 0; g < NGRP; ++g) {
+            for (int q = 0; q < kCS; ++q) mbar_init(bar(B_PFREE(g, q)), 1);
+            mbar_init(bar(B_RECV(g)), kCS);
+            mbar_init(bar(B_RFULL(g)), 1);
+        }
         for (int w = 0; w < NSW; ++w)
             for (int b = 0; b < 2; ++b) {
                 mbar_init(bar(B_HFULL(w, b)), 1);
@@ -388,10 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
 #ifdef KDA_TC_TRACE
-    for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x)
+    for (int i = threadIdx.x; i < 32 * 16; i += blockDim.x)
         reinterpret_cast<long long *>(sm + SM_TRACE)[i] = 0;
 #endif
-    if (kShare) cluster_sync(); else __syncthreads();
+    cluster_sync();
 
     if (warp < W_PRO0) {
         regs_decrease<kRegsProducer>();
@@ -407,8 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
                 KDA_TRACE(n, 1);
                 if (lane == 0) {
-                    const bool mine = owner(n) == rank;
-                    mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + (mine ? 0 : SLOT_BYTES));
+                    mbar_arrive_tx(bar(B_FULL(s)), V_BYTES + SLOT_BYTES);
                     tma_load_3d(sbase + SM_V + s * V_BYTES, &tm_v, (int)rank * VB, head,
                                 t0 + n * C, bar(B_FULL(s)));
                 }
@@ -416,28 +448,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1) {
             // -------------------------------------------- release forwarder
-            // Lane 0 tells the owner of chunk n - NP that this CTA has consumed it, so that
-            // the owner may overwrite the slot with chunk n. A cluster-scope release waits
-            // for the issuing thread's earlier memory operations -- including, as
-            // measured, TMA loads still in flight -- so it is issued by a thread that
-            // has no memory operations of its own.
+            // Lane 0 tells the owner of chunk n that this CTA has consumed chunk n - NP, the
+            // previous occupant of slot n % NP, so the owner may copy chunk n into it. A
+            // cluster-scope release waits for the issuing thread's earlier memory
+            // operations -- including, as measured, TMA loads still in flight -- so these
+            // signals come from threads that have no memory operations of their own.
             if (lane == 0) {
                 for (int n = NP; n < nchunks; ++n) {
                     const int s = n % NP, use = n / NP;
                     if (!mbar_wait<false>(bar(B_FREE(s)), (use & 1) ^ 1)) break;
-                    if (kShare)
-                        mbar_arrive_remote(map_to_rank(bar(B_CFREE(s)), owner(n)));
-                    else
-                        mbar_arrive(bar(B_CFREE(s)));
+                    mbar_arrive_remote_relaxed(map_to_rank(bar(B_PFREE(s / kCS, (int)rank)), owner(n)));
+                }
+            }
+            __syncwarp();
+        } else if (warp == 2) {
+            // -------------------------------------------- receipt forwarder
+            // Lane 0 tells the owner of chunk n that its copy of chunk n has landed here, so
+            // that once every CTA has it the owner may reuse the staging buffer for chunk
+            // n + NP. (Slot n % NP cannot be refilled before this thread has seen the
+            // phase: the refill needs this very signal.)
+            if (lane == 0) {
+                for (int n = 0; n + NP < nchunks; ++n) {
+                    const int s = n % NP, use = n / NP;
+                    if (!mbar_wait<false>(bar(B_FULL(s)), use & 1)) break;
+                    KDA_TRACE(n, 15);
+                    mbar_arrive_remote_relaxed(map_to_rank(bar(B_RECV(s / kCS)), owner(n)));
                 }
             }
             __syncwarp();
         }
-        // warps 2 and 3 only hold registers back for the consumers
+        // warp 3 only holds registers back for the consumers
     } else if (warp < W_STATE0) {
         regs_decrease<kRegsPrologue>();
         // ------------------------------------------------ prologue groups
-        // Group g handles every other owned chunk (owned index j with j % 2 == g).
+        // Group g of owner CTA r handles the chunks n with n % NP == r + kCS g, i.e. the
+        // chunks of slot r + kCS g. It computes a chunk's products into its staging
+        // buffer as soon as every CTA has received the previous copy out of it, then
+        // copies them into each CTA's slot as soon as that CTA has consumed the slot's
+        // previous chunk.
         const int g = (warp - W_PRO0) / NPW;
         const int pw = (warp - W_PRO0) % NPW;
         const int c = threadIdx.x - 32 * (W_PRO0 + NPW * g);  // key channel of the gate pass
@@ -474,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("cp.async.commit_group;" ::: "memory");
             }
         };
-        fetch(first + g * nstep, 0);
-        int k = 0;  // chunks this group has processed
-        for (int n = first + g * nstep; n < nchunks; n += NGRP * nstep, ++k) {
-            const int s = n % NP, use = n / NP;
+        fetch((int)rank + kCS * g, 0);
+        int k = 0;  // chunks this group has processed (= n / NP)
+        for (int n = (int)rank + kCS * g; n < nchunks; n += NP, ++k) {
+            const int s = n % NP;
             const int c0 = t0 + n * C;
             const int L = min(C, t1 - c0);
             if (c == 0) KDA_TRACE(n, 3);
@@ -486,18 +534,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool bad = false;
             if (c == 0) {
                 bad = !mbar_wait<false>(bar(B_RFULL(g)), k & 1);
-                bad |= !mbar_wait<true>(bar(B_CFREE(s)), (use & 1) ^ 1);
+                if (k > 0) bad |= !mbar_wait<true>(bar(B_RECV(g)), (k & 1) ^ 1);
             }
             if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's beta
             if (named_sync_or(bar_id, nt, bad)) break;
             if (c != 0) {  // acquire the completed phases (they do not block now)
                 mbar_try(bar(B_RFULL(g)), k & 1);
-                mbar_try_cluster(bar(B_CFREE(s)), (use & 1) ^ 1);
+                if (k > 0) mbar_try_cluster(bar(B_RECV(g)), (k & 1) ^ 1);
             }
             if (c == 0) KDA_TRACE(n, 4);
             const float *bs = reinterpret_cast<const float *>(gs + GS_BETA) + (k & 1) * C;
-            unsigned char *slot = sm + SM_PROD + s * SLOT_BYTES;
-            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
+            // this group's staging buffer, laid out as a slot
+            unsigned char *slot = sm + SM_STAGE + g * SLOT_BYTES;
+            const uint32_t slot_s = sbase + SM_STAGE + g * SLOT_BYTES;
             float *Pg = reinterpret_cast<float *>(slot + OFF_PG);
             const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_Q);
             const __nv_bfloat16 *rk = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_K);
@@ -560,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 5);
             // the raw slot is free again: request this group's next chunk now
-            fetch(n + NGRP * nstep, (k + 1) & 1);
+            fetch(n + NP, (k + 1) & 1);
             // -- A = strict_lower(beta K~ K^^T) on warps 0, 1 and P = lower(Q~ K^^T) on
             //    warps 2, 3; each warp one 8-token column tile (j in [8 jh, 8 jh + 8))
             {
@@ -643,15 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 8);
             if (c == 0) {
-                if (kShare) {
-#pragma unroll
-                    for (uint32_t peer = 0; peer < (uint32_t)kCS; ++peer) {
-                        if (peer == rank) continue;
-                        bulk_copy_to_peer(map_to_rank(slot_s, peer), slot_s, SLOT_BYTES,
-                                          map_to_rank(bar(B_FULL(s)), peer));
-                    }
+                // into slot s of every CTA (this one last), each once it has consumed the
+                // slot's previous chunk; completion lands on that CTA's FULL barrier
+                const uint32_t dst = sbase + SM_PROD + s * SLOT_BYTES;
+                for (uint32_t q = 1; q <= (uint32_t)kCS; ++q) {
+                    const uint32_t peer = (rank + q) % kCS;
+                    if (k > 0 && !mbar_wait<true>(bar(B_PFREE(g, (int)peer)), (k & 1) ^ 1)) break;
+                    bulk_copy_to_peer(map_to_rank(dst, peer), slot_s, SLOT_BYTES,
+                                      map_to_rank(bar(B_FULL(s)), peer));
                 }
-                mbar_arrive(bar(B_FULL(s)));  // own state warps
                 KDA_TRACE(n, 9);
             }
         }
@@ -683,90 +732,149 @@ __global__ void __launch_bounds__(kThreads, 1)
                 S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
             }
         }
-        for (int n = 0; n < nchunks; ++n) {
-            const int s = n % NP, use = n / NP;
-            const int hb = n & 1;
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 10);
-            bool ok = mbar_wait<false>(bar(B_FULL(s)), use & 1);
-            if (__any_sync(0xffffffffu, !ok)) break;
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 11);
+        // handoff buffer b of this state warp, this lane's row (9 x 16 bytes)
+        auto handoff = [&](int b) {
+            return reinterpret_cast<uint4 *>(sm + SM_HO + (sw * 2 + b) * HO_BYTES + lane * HO_LANE);
+        };
+        // U^T operands of the chunk in slot s: V^T, TB^T and (-W)^T fragments
+        auto load_u_ops = [&](int s, uint32_t (&va)[4], uint32_t (&tb)[4], uint32_t (&wf)[8][4]) {
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
-            const float *Pg = reinterpret_cast<const float *>(sm + SM_PROD + s * SLOT_BYTES + OFF_PG);
             const uint32_t vs = sbase + SM_V + s * V_BYTES;
-            // operand fragments for U^T: V^T, TB^T and (-W)^T, all loads first
-            uint32_t va[4], tb[4], wf[8][4];
-            {
-                const int t = (i8 >> 1) * 8 + r8, vv = sw * 16 + (i8 & 1) * 8;
-                ldsm_x4_t(vs + (t * VB + vv) * 2, va[0], va[1], va[2], va[3]);
-                const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
-                ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
+            const int t = (i8 >> 1) * 8 + r8, vv = sw * 16 + (i8 & 1) * 8;
+            ldsm_x4_t(vs + (t * VB + vv) * 2, va[0], va[1], va[2], va[3]);
+            const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
+            ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
 #pragma unroll
-                for (int kt = 0; kt < 8; ++kt)
-                    ldsm_x4(slot_s + OFF_PW + (r * LDP + kt * 16 + (i8 & 1) * 8) * 2,
-                            wf[kt][0], wf[kt][1], wf[kt][2], wf[kt][3]);
-            }
-            // S^T as bf16 A fragments
-            uint32_t Sa[8][4];
-#pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-                Sa[kt][0] = pack_bf16(S[2 * kt][0], S[2 * kt][1]);
-                Sa[kt][1] = pack_bf16(S[2 * kt][2], S[2 * kt][3]);
-                Sa[kt][2] = pack_bf16(S[2 * kt + 1][0], S[2 * kt + 1][1]);
-                Sa[kt][3] = pack_bf16(S[2 * kt + 1][2], S[2 * kt + 1][3]);
-            }
-            // U^T = V^T TB^T + S^T (-W)^T, four independent accumulator chains
-            float accU[2][2][4] = {};  // [k parity][token n-tile][frag]
-            mma16816(accU[1][0], va, tb[0], tb[1]);
-            mma16816(accU[1][1], va, tb[2], tb[3]);
-#pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-                mma16816(accU[kt & 1][0], Sa[kt], wf[kt][0], wf[kt][1]);
-                mma16816(accU[kt & 1][1], Sa[kt], wf[kt][2], wf[kt][3]);
-            }
-            // operands of the state update, loaded while the U^T products run
-            uint32_t kf[8][4];
-#pragma unroll
-            for (int np = 0; np < 8; ++np)
-                ldsm_x4(slot_s + OFF_PK + cmaj(np * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8),
-                        kf[np][0], kf[np][1], kf[np][2], kf[np][3]);
-            float4 gl[8];
-#pragma unroll
-            for (int np = 0; np < 8; ++np) gl[np] = reinterpret_cast<const float4 *>(Pg)[l4 * 8 + np];
-            uint32_t Ua[4];
+            for (int kt = 0; kt < 8; ++kt)
+                ldsm_x4(slot_s + OFF_PW + (r * LDP + kt * 16 + (i8 & 1) * 8) * 2, wf[kt][0], wf[kt][1],
+                        wf[kt][2], wf[kt][3]);
+        };
+        // one 16-key step of U^T = V^T TB^T + S^T (-W)^T: S^T key tile kt as bf16 A fragment,
+        // also handed to the output warp
+        auto u_step = [&](int kt, const uint32_t (&wf)[8][4], float (&accU)[2][2][4], uint4 *ho) {
+            uint32_t a[4];
+            a[0] = pack_bf16(S[2 * kt][0], S[2 * kt][1]);
+            a[1] = pack_bf16(S[2 * kt][2], S[2 * kt][3]);
+            a[2] = pack_bf16(S[2 * kt + 1][0], S[2 * kt + 1][1]);
+            a[3] = pack_bf16(S[2 * kt + 1][2], S[2 * kt + 1][3]);
+            mma16816(accU[kt & 1][0], a, wf[kt][0], wf[kt][1]);
+            mma16816(accU[kt & 1][1], a, wf[kt][2], wf[kt][3]);
+            ho[kt] = make_uint4(a[0], a[1], a[2], a[3]);
+        };
+        auto u_finish = [&](const float (&accU)[2][2][4], uint32_t (&Ua)[4]) {
             Ua[0] = pack_bf16(accU[0][0][0] + accU[1][0][0], accU[0][0][1] + accU[1][0][1]);
             Ua[1] = pack_bf16(accU[0][0][2] + accU[1][0][2], accU[0][0][3] + accU[1][0][3]);
             Ua[2] = pack_bf16(accU[0][1][0] + accU[1][1][0], accU[0][1][1] + accU[1][1][1]);
             Ua[3] = pack_bf16(accU[0][1][2] + accU[1][1][2], accU[0][1][3] + accU[1][1][3]);
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 12);
-            // S^T <- S^T diag(gamma_L) + U^T K'
+        };
+        // one 16-key step of S^T <- S^T diag(gamma_L) + U^T K'
+        auto s_step = [&](int np, const float4 &g, const uint32_t (&kf)[4], const uint32_t (&Ua)[4]) {
+            mul2(S[2 * np][0], S[2 * np][1], g.x, g.y);
+            mul2(S[2 * np][2], S[2 * np][3], g.x, g.y);
+            mul2(S[2 * np + 1][0], S[2 * np + 1][1], g.z, g.w);
+            mul2(S[2 * np + 1][2], S[2 * np + 1][3], g.z, g.w);
+            mma16816(S[2 * np], Ua, kf[0], kf[1]);
+            mma16816(S[2 * np + 1], Ua, kf[2], kf[3]);
+        };
+        // state-update operands of the chunk in slot s: K' fragments and gamma_L
+        auto load_s_ops = [&](int s, uint32_t (&kf)[8][4], float4 (&gl)[8]) {
+            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
+            const float4 *Pg = reinterpret_cast<const float4 *>(sm + SM_PROD + s * SLOT_BYTES + OFF_PG);
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
-                const float4 g = gl[np];  // channels 16np + 2l4 (+1), 16np + 8 + 2l4 (+1)
-                S[2 * np][0] *= g.x; S[2 * np][1] *= g.y; S[2 * np][2] *= g.x; S[2 * np][3] *= g.y;
-                S[2 * np + 1][0] *= g.z; S[2 * np + 1][1] *= g.w;
-                S[2 * np + 1][2] *= g.z; S[2 * np + 1][3] *= g.w;
-                mma16816(S[2 * np], Ua, kf[np][0], kf[np][1]);
-                mma16816(S[2 * np + 1], Ua, kf[np][2], kf[np][3]);
+                ldsm_x4(slot_s + OFF_PK + cmaj(np * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), kf[np][0],
+                        kf[np][1], kf[np][2], kf[np][3]);
+                gl[np] = Pg[np * 4 + l4];
             }
-            // every read of the slot by this warp is done (fragments are in registers)
+        };
+        // chunk m's products are in, and its handoff buffer is free
+        auto wait_chunk = [&](int m) {
+            bool ok = mbar_wait<false>(bar(B_FULL(m % NP)), (m / NP) & 1);
+            ok = ok && mbar_wait<false>(bar(B_HEMPTY(sw, m & 1)), ((m >> 1) & 1) ^ 1);
+            return !__any_sync(0xffffffffu, !ok);
+        };
+        // Software pipeline. Iteration n applies chunk n's state update and, interleaved
+        // with it key tile by key tile, forms U^T of chunk n + 1 from the freshly updated
+        // tiles, so the two serial halves of consecutive chunks overlap. Every operand of
+        // iteration n is loaded at the end of iteration n - 1, and the barriers of chunk
+        // n + 2 are probed (without blocking) at the start of iteration n, so neither the
+        // shared-memory nor the barrier latency sits on the chain. U^T of chunk 0 is
+        // formed before the loop.
+        uint32_t Ua[4] = {0u, 0u, 0u, 0u};
+        uint32_t va[4], tb[4], wf[8][4], kf[8][4];
+        float4 gl[8];
+        int n_end = 0;  // iterations that may run (all operands of iteration n are loaded)
+        if (nchunks > 0 && wait_chunk(0)) {
+            load_u_ops(0, va, tb, wf);
+            float accU[2][2][4] = {};
+            mma16816(accU[1][0], va, tb[0], tb[1]);
+            mma16816(accU[1][1], va, tb[2], tb[3]);
+            uint4 *ho = handoff(0);
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt) u_step(kt, wf, accU, ho);
+            u_finish(accU, Ua);
+            ho[8] = make_uint4(Ua[0], Ua[1], Ua[2], Ua[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_HFULL(sw, 0)));
+            n_end = 1;
+            if (nchunks > 1) {
+                if (wait_chunk(1)) {
+                    load_u_ops(1, va, tb, wf);
+                } else {
+                    n_end = 0;
+                }
+            }
+            load_s_ops(0, kf, gl);
+        }
+        for (int n = 0; n < n_end; ++n) {
+            const int s = n % NP;
+            const bool has_next = n + 1 < nchunks, has_next2 = n + 2 < nchunks;
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 10);
+            bool ready2 = true;
+            if (has_next2) {
+                const int m = n + 2;
+                ready2 = mbar_test(bar(B_FULL(m % NP)), (m / NP) & 1) &&
+                         mbar_test(bar(B_HEMPTY(sw, m & 1)), ((m >> 1) & 1) ^ 1);
+            }
+            if (has_next) {
+                float accU[2][2][4] = {};
+                mma16816(accU[1][0], va, tb[0], tb[1]);
+                mma16816(accU[1][1], va, tb[2], tb[3]);
+                uint4 *ho = handoff((n + 1) & 1);
+                s_step(0, gl[0], kf[0], Ua);
+#pragma unroll
+                for (int np = 1; np < 8; ++np) {
+                    s_step(np, gl[np], kf[np], Ua);
+                    u_step(np - 1, wf, accU, ho);
+                }
+                u_step(7, wf, accU, ho);
+                if (sw == 0 && lane == 0) KDA_TRACE(n, 11);
+                u_finish(accU, Ua);
+                ho[8] = make_uint4(Ua[0], Ua[1], Ua[2], Ua[3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_HFULL(sw, (n + 1) & 1)));
+            } else {
+#pragma unroll
+                for (int np = 0; np < 8; ++np) s_step(np, gl[np], kf[np], Ua);
+            }
+            // every read of slot n by this warp has completed (its values were consumed)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FREE(s)));
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
-            // hand the bf16 S^T (before this chunk's update) and U^T to the output warp:
-            // plain stores, then a release on the handoff barrier; no wait unless the
-            // output warp is two chunks behind
-            ok = mbar_wait<false>(bar(B_HEMPTY(sw, hb)), ((n >> 1) & 1) ^ 1);
-            if (__any_sync(0xffffffffu, !ok)) break;
-            {
-                uint4 *ho = reinterpret_cast<uint4 *>(sm + SM_HO + (sw * 2 + hb) * HO_BYTES +
-                                                      lane * HO_LANE);
-#pragma unroll
-                for (int kt = 0; kt < 8; ++kt)
-                    ho[kt] = make_uint4(Sa[kt][0], Sa[kt][1], Sa[kt][2], Sa[kt][3]);
-                ho[8] = make_uint4(Ua[0], Ua[1], Ua[2], Ua[3]);
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 12);
+            // operands of iteration n + 1: K' and gamma_L of chunk n + 1 (its products are
+            // known to be in), U^T operands of chunk n + 2
+            if (has_next) {
+                load_s_ops((n + 1) % NP, kf, gl);
+                n_end = n + 2;
+                if (has_next2) {
+                    if (!__all_sync(0xffffffffu, ready2) && !wait_chunk(n + 2)) {
+                        n_end = n + 1;  // a wait gave up: stop after the next iteration
+                    } else {
+                        load_u_ops((n + 2) % NP, va, tb, wf);
+                    }
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_HFULL(sw, hb)));
+            if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
         }
         if (p.h_final) {
 #pragma unroll
@@ -850,12 +958,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // no CTA may leave while a peer can still write into its shared memory
     __syncwarp();
-    if (kShare) cluster_sync();
+    cluster_sync();
 #ifdef KDA_TC_TRACE
     __syncthreads();
     if (blockIdx.x < 4)
-        for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x)
-            g_trace[blockIdx.x][i / 32][i % 32] = reinterpret_cast<long long *>(sm + SM_TRACE)[i];
+        for (int i = threadIdx.x; i < 32 * 16; i += blockDim.x)
+            g_trace[blockIdx.x][i / 16][i % 16] = reinterpret_cast<long long *>(sm + SM_TRACE)[i];
 #endif
 }
 
@@ -903,21 +1011,20 @@ bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H
     return r == CUDA_SUCCESS;
 }
 
-template <bool kShare>
-cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
+cudaError_t launch_tc_impl(const FwdArgs &a, cudaStream_t stream) {
     CUtensorMap mq, mk, ma, mv;
     if (!encode_map(&mq, a.q, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&mk, a.k, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&ma, a.a, true, a.n_tok, a.n_heads, D) ||
         !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel<kShare>,
+    cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // The warpgroups' register increase is only covered when the block is launched with
     // exactly kRegsLaunch registers per thread; with fewer it could never be granted.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kda_tc_kernel<kShare>);
+    e = cudaFuncGetAttributes(&fa, kda_tc_kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     TcParams p;
@@ -931,12 +1038,12 @@ cudaError_t launch_tc_t(const FwdArgs &a, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kShare ? kCS : 1;
+    attr[0].val.clusterDim.x = kCS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel<kShare>, mq, mk, ma, mv, p);
+    e = cudaLaunchKernelEx(&cfg, kda_tc_kernel, mq, mk, ma, mv, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
@@ -949,11 +1056,7 @@ bool tc_supported(const FwdArgs &a) {
 }
 
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
-#ifdef KDA_TC_NO_CLUSTER
-    return launch_tc_t<false>(a, stream);
-#else
-    return launch_tc_t<true>(a, stream);
-#endif
+    return launch_tc_impl(a, stream);
 }
 
 #ifdef KDA_TC_TRACE
