@@ -203,12 +203,13 @@ __device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t a) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
 }
+// arrive without release semantics: for "these reads have completed" signals, whose
+// values the arriving warp has already consumed
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t a) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t a, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 // Remote arrive without release semantics. Measured: a cluster-scope release arrive
@@ -736,18 +737,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto handoff = [&](int b) {
             return reinterpret_cast<uint4 *>(sm + SM_HO + (sw * 2 + b) * HO_BYTES + lane * HO_LANE);
         };
-        // U^T operands of the chunk in slot s: V^T, TB^T and (-W)^T fragments
-        auto load_u_ops = [&](int s, uint32_t (&va)[4], uint32_t (&tb)[4], uint32_t (&wf)[8][4]) {
+        // U^T operands of the chunk in slot s: V^T and TB^T fragments, and key tile kt of
+        // the (-W)^T fragments
+        auto load_vt = [&](int s, uint32_t (&va)[4], uint32_t (&tb)[4]) {
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             const uint32_t vs = sbase + SM_V + s * V_BYTES;
             const int t = (i8 >> 1) * 8 + r8, vv = sw * 16 + (i8 & 1) * 8;
             ldsm_x4_t(vs + (t * VB + vv) * 2, va[0], va[1], va[2], va[3]);
             const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
             ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
+        };
+        auto load_w = [&](int s, int kt, uint32_t (&w)[4]) {
+            const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
+            const int r = (i8 >> 1) * 8 + r8;
+            ldsm_x4(slot_s + OFF_PW + (r * LDP + kt * 16 + (i8 & 1) * 8) * 2, w[0], w[1], w[2], w[3]);
+        };
+        auto load_u_ops = [&](int s, uint32_t (&va)[4], uint32_t (&tb)[4], uint32_t (&wf)[8][4]) {
+            load_vt(s, va, tb);
 #pragma unroll
-            for (int kt = 0; kt < 8; ++kt)
-                ldsm_x4(slot_s + OFF_PW + (r * LDP + kt * 16 + (i8 & 1) * 8) * 2, wf[kt][0], wf[kt][1],
-                        wf[kt][2], wf[kt][3]);
+            for (int kt = 0; kt < 8; ++kt) load_w(s, kt, wf[kt]);
         };
         // one 16-key step of U^T = V^T TB^T + S^T (-W)^T: S^T key tile kt as bf16 A fragment,
         // also handed to the output warp
@@ -776,16 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma16816(S[2 * np], Ua, kf[0], kf[1]);
             mma16816(S[2 * np + 1], Ua, kf[2], kf[3]);
         };
-        // state-update operands of the chunk in slot s: K' fragments and gamma_L
-        auto load_s_ops = [&](int s, uint32_t (&kf)[8][4], float4 (&gl)[8]) {
+        // state-update operands of the chunk in slot s, key tile np: K' fragments and
+        // gamma_L
+        auto load_s = [&](int s, int np, uint32_t (&k)[4], float4 &g) {
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             const float4 *Pg = reinterpret_cast<const float4 *>(sm + SM_PROD + s * SLOT_BYTES + OFF_PG);
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                ldsm_x4(slot_s + OFF_PK + cmaj(np * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), kf[np][0],
-                        kf[np][1], kf[np][2], kf[np][3]);
-                gl[np] = Pg[np * 4 + l4];
-            }
+            ldsm_x4(slot_s + OFF_PK + cmaj(np * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), k[0], k[1], k[2],
+                    k[3]);
+            g = Pg[np * 4 + l4];
         };
         // chunk m's products are in, and its handoff buffer is free
         auto wait_chunk = [&](int m) {
@@ -795,11 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // Software pipeline. Iteration n applies chunk n's state update and, interleaved
         // with it key tile by key tile, forms U^T of chunk n + 1 from the freshly updated
-        // tiles, so the two serial halves of consecutive chunks overlap. Every operand of
-        // iteration n is loaded at the end of iteration n - 1, and the barriers of chunk
-        // n + 2 are probed (without blocking) at the start of iteration n, so neither the
-        // shared-memory nor the barrier latency sits on the chain. U^T of chunk 0 is
-        // formed before the loop.
+        // tiles, so the two serial halves of consecutive chunks overlap. Each operand tile
+        // of the next iteration is loaded into the registers of the tile just consumed
+        // (K' and gamma_L of chunk n + 1, (-W)^T of chunk n + 2), so loads stream through
+        // the iteration; the barriers of chunk n + 2 are probed without blocking at the
+        // start of iteration n. U^T of chunk 0 is formed before the loop.
         uint32_t Ua[4] = {0u, 0u, 0u, 0u};
         uint32_t va[4], tb[4], wf[8][4], kf[8][4];
         float4 gl[8];
@@ -824,7 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     n_end = 0;
                 }
             }
-            load_s_ops(0, kf, gl);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) load_s(0, np, kf[np], gl[np]);
         }
         for (int n = 0; n < n_end; ++n) {
             const int s = n % NP;
@@ -837,42 +844,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                          mbar_test(bar(B_HEMPTY(sw, m & 1)), ((m >> 1) & 1) ^ 1);
             }
             if (has_next) {
+                const int s1 = (n + 1) % NP, s2 = (n + 2) % NP;
+                // chunk n + 2's operands may stream in during this iteration
+                const bool roll = has_next2 && __all_sync(0xffffffffu, ready2);
                 float accU[2][2][4] = {};
                 mma16816(accU[1][0], va, tb[0], tb[1]);
                 mma16816(accU[1][1], va, tb[2], tb[3]);
+                if (roll) load_vt(s2, va, tb);
                 uint4 *ho = handoff((n + 1) & 1);
                 s_step(0, gl[0], kf[0], Ua);
 #pragma unroll
                 for (int np = 1; np < 8; ++np) {
                     s_step(np, gl[np], kf[np], Ua);
+                    load_s(s1, np - 1, kf[np - 1], gl[np - 1]);
                     u_step(np - 1, wf, accU, ho);
+                    if (roll) load_w(s2, np - 1, wf[np - 1]);
                 }
+                // every read of slot n by this warp has completed (its values were consumed)
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(B_FREE(s)));
+                load_s(s1, 7, kf[7], gl[7]);
                 u_step(7, wf, accU, ho);
+                if (roll) load_w(s2, 7, wf[7]);
                 if (sw == 0 && lane == 0) KDA_TRACE(n, 11);
                 u_finish(accU, Ua);
                 ho[8] = make_uint4(Ua[0], Ua[1], Ua[2], Ua[3]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_HFULL(sw, (n + 1) & 1)));
+                if (sw == 0 && lane == 0) KDA_TRACE(n, 12);
+                n_end = n + 2;
+                if (has_next2 && !roll) {  // chunk n + 2 was not in yet: wait, then load
+                    if (!wait_chunk(n + 2)) break;
+                    load_u_ops(s2, va, tb, wf);
+                }
             } else {
 #pragma unroll
                 for (int np = 0; np < 8; ++np) s_step(np, gl[np], kf[np], Ua);
-            }
-            // every read of slot n by this warp has completed (its values were consumed)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
-            if (sw == 0 && lane == 0) KDA_TRACE(n, 12);
-            // operands of iteration n + 1: K' and gamma_L of chunk n + 1 (its products are
-            // known to be in), U^T operands of chunk n + 2
-            if (has_next) {
-                load_s_ops((n + 1) % NP, kf, gl);
-                n_end = n + 2;
-                if (has_next2) {
-                    if (!__all_sync(0xffffffffu, ready2) && !wait_chunk(n + 2)) {
-                        n_end = n + 1;  // a wait gave up: stop after the next iteration
-                    } else {
-                        load_u_ops((n + 2) % NP, va, tb, wf);
-                    }
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(B_FREE(s)));
             }
             if (sw == 0 && lane == 0) KDA_TRACE(n, 13);
         }
@@ -936,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma16816(accO[0][0], Ua, pf[0], pf[1]);
             mma16816(accO[0][1], Ua, pf[2], pf[3]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FREE(s)));
+            if (lane == 0) mbar_arrive_relaxed(bar(B_FREE(s)));
             // 8x8 blocks (value rows x tokens) transposed to (tokens x value columns)
             const int c0 = t0 + n * C;
             const int L = min(C, t1 - c0);
