@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -74,10 +75,16 @@ def algorithmic_flops(x) -> int:
 
 
 def kernel_source_digest() -> str:
+    """Digest of the kernel sources with comments and whitespace removed, so that the
+    recorded ncu traffic stays valid across comment edits and is dropped on any code
+    change."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES + ["chunked_linear_attention_kda_gb300/csrc/kda_internal.h"]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,11 +32,12 @@
 // in registers with no shuffles and no shared-memory round trip.
 //
 // Data movement: q, k, gate logits and v tiles arrive by TMA (cp.async.bulk.tensor)
-// into mbarrier-tracked rings; prologue products travel between the CTAs of a
-// cluster by cp.async.bulk shared::cta -> shared::cluster with complete_tx on the
-// receiver's mbarrier. Every wait is bounded: a wait that exceeds its limit sets a
-// device flag (kda_read_device_flags), releases every other wait in the grid and lets
-// the kernel finish with unspecified output.
+// into mbarrier-tracked rings. Prologue products are computed into a per-group staging
+// buffer and copied into every CTA's ring slot by cp.async.bulk shared::cta ->
+// shared::cluster, completing on the receiver's mbarrier; two forwarding warps tell the
+// owner when a CTA has freed a slot and when a copy has landed. Every wait is bounded: a
+// wait that exceeds its limit sets a device flag (kda_read_device_flags), releases every
+// other wait in the grid and lets the kernel finish with unspecified output.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -552,9 +553,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_Q);
             const __nv_bfloat16 *rk = reinterpret_cast<const __nv_bfloat16 *>(raw + RAW_K);
             const float *ra = reinterpret_cast<const float *>(raw + RAW_A);
-            // -- gate pass: one key channel per thread, 16 tokens in order; outputs are
-            //    written channel-major as packed bf16 pairs, 16 bytes at a time
-            {
+            // -- gate pass: one key channel at a time, 16 tokens in order; outputs are
+            //    written channel-major as packed bf16 pairs, 16 bytes at a time. Only the
+            //    group's warps 2 and 3 run it (two channels per thread): warps 0 and 1 share
+            //    their schedulers with the state warps, whose chain this arithmetic would
+            //    slow (measured: 3 % on the 64K workload).
+            if (pw >= 2)
+#pragma unroll 1
+            for (int rep = 0; rep < 2; ++rep) {
+                const int c = 32 * (pw - 2) + lane + 64 * rep;
                 // rows past the end hold another sequence's (finite) data or TMA
                 // zeros: compute every row, then select, in separate passes so that
                 // the 16 independent exponential chains overlap
