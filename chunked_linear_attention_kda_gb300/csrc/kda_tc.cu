@@ -618,17 +618,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c == 0) KDA_TRACE(n, 5);
             // the raw slot is free again: request this group's next chunk now
             fetch(n + NP, (k + 1) & 1);
-            // -- A = strict_lower(beta K~ K^^T) on warps 0, 1 and P = lower(Q~ K^^T) on
-            //    warps 2, 3; each warp one 8-token column tile (j in [8 jh, 8 jh + 8))
-            {
-                const bool isA = pw < 2;
+            // -- A = strict_lower(beta K~ K^^T) and P = lower(Q~ K^^T) on the group's warps 2
+            //    and 3 (the warps that share no scheduler with the state warps); each warp
+            //    one 8-token column tile (j in [8 jh, 8 jh + 8)) of both
+            if (pw >= 2) {
                 const int jh = pw & 1;
-                const uint32_t lhs = isA ? Kt_s : slot_s + OFF_PQ;
-                uint32_t b[D / 32][4], a[D / 16][4];
+                uint32_t b[D / 32][4];
 #pragma unroll
                 for (int kp = 0; kp < D / 32; ++kp)  // K^^T fragments of key tiles 2kp, 2kp+1
                     ldsm_x4_t(Kh_s + cmaj(kp * 32 + i8 * 8 + r8, jh * 8), b[kp][0], b[kp][1],
                               b[kp][2], b[kp][3]);
+#pragma unroll 1
+                for (int prod = 0; prod < 2; ++prod) {
+                const bool isA = prod == 0;
+                const uint32_t lhs = isA ? Kt_s : slot_s + OFF_PQ;
+                uint32_t a[D / 16][4];
 #pragma unroll
                 for (int kt = 0; kt < D / 16; ++kt)
                     ldsm_x4_t(lhs + cmaj(kt * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), a[kt][0],
@@ -652,11 +656,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pack_bf16(j0 <= r ? v0 : 0.f, j0 + 1 <= r ? v1 : 0.f);
                     }
                 }
+                }
             }
             named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 6);
             // -- TB = (I + A)^-1 diag(beta): forward substitution, one column per lane
-            if (pw == 0 && lane < C) {
+            if (pw == 2 && lane < C) {
                 const int j = lane;
                 float x[C];
 #pragma unroll
@@ -673,8 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_sync(bar_id, nt);
             if (c == 0) KDA_TRACE(n, 7);
-            // -- -W = -TB K~: warp pw covers key channels [32 pw, 32 pw + 32)
-            {
+            // -- -W = -TB K~: warps 2 and 3, warp pw covering key channels
+            //    [64 (pw - 2), 64 (pw - 2) + 64)
+            if (pw >= 2) {
                 __nv_bfloat16 *Pw = reinterpret_cast<__nv_bfloat16 *>(slot + OFF_PW);
                 uint32_t tb[4];
                 {
@@ -682,8 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
                 }
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int cb = pw * 32 + half * 16;
+                for (int half = 0; half < 4; ++half) {
+                    const int cb = (pw - 2) * 64 + half * 16;
                     uint32_t k0, k1, k2, k3;
                     ldsm_x4(Kt_s + cmaj(cb + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), k0, k1, k2, k3);
                     float acc0[4] = {}, acc1[4] = {};
