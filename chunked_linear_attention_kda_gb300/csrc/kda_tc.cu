@@ -493,6 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = threadIdx.x - 32 * (W_PRO0 + NPW * g);  // key channel of the gate pass
         const int nt = 32 * NPW;
         const int bar_id = 1 + g;
+        // the thread that waits, issues the TMA loads and the product copies, and the
+        // warp that fetches beta: both on the group's warps 2 and 3, which share no
+        // scheduler with the state warps
+        constexpr int kLead = 64;
         unsigned char *gs = sm + SM_GS + g * GS_BYTES;
         unsigned char *KtB = gs + GS_KT;  // K~ [c][t]
         unsigned char *KhB = gs + GS_KH;  // K^ [c][t]
@@ -501,20 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i8 = lane >> 3, r8 = lane & 7;
         const uint32_t raw_s = sbase + SM_RAW + g * RAW_BYTES;
         const unsigned char *raw = sm + SM_RAW + g * RAW_BYTES;
-        // q, k and gate-logit tiles of chunk n into this group's raw slot (thread 0),
-        // beta of chunk n into beta buffer b (warp 1's lanes 0-15, cp.async, which no
-        // barrier or fence of another thread waits for)
+        // q, k and gate-logit tiles of chunk n into this group's raw slot (the lead
+        // thread), beta of chunk n into beta buffer b (warp 3's lanes 0-15, cp.async,
+        // which no barrier or fence of another thread waits for)
         auto fetch = [&](int n, int b) {
             if (n >= nchunks) return;
             const int c0n = t0 + n * C;
-            if (c == 0) {
+            if (c == kLead) {
                 mbar_arrive_tx(bar(B_RFULL(g)), RAW_BYTES);
                 tma_load_3d(raw_s + RAW_Q, &tm_q, 0, head, c0n, bar(B_RFULL(g)));
                 tma_load_3d(raw_s + RAW_K, &tm_k, 0, head, c0n, bar(B_RFULL(g)));
                 tma_load_3d(raw_s + RAW_A, &tm_a, 0, head, c0n, bar(B_RFULL(g)));
                 KDA_TRACE(n, 2);
             }
-            if (pw == 1) {
+            if (pw == 3) {
                 if (lane < C) {
                     const int row = c0n + lane;
                     const bool in = row < t1;
@@ -530,21 +534,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = n % NP;
             const int c0 = t0 + n * C;
             const int L = min(C, t1 - c0);
-            if (c == 0) KDA_TRACE(n, 3);
+            if (c == kLead) KDA_TRACE(n, 3);
             // one thread waits on the pipeline; the rest of the group blocks on the
             // hardware named barrier, then observes the completed phases once
             bool bad = false;
-            if (c == 0) {
+            if (c == kLead) {
                 bad = !mbar_wait<false>(bar(B_RFULL(g)), k & 1);
                 if (k > 0) bad |= !mbar_wait<true>(bar(B_RECV(g)), (k & 1) ^ 1);
             }
-            if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's beta
+            if (pw == 3) asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's beta
             if (named_sync_or(bar_id, nt, bad)) break;
-            if (c != 0) {  // acquire the completed phases (they do not block now)
+            if (c != kLead) {  // acquire the completed phases (they do not block now)
                 mbar_try(bar(B_RFULL(g)), k & 1);
                 if (k > 0) mbar_try_cluster(bar(B_RECV(g)), (k & 1) ^ 1);
             }
-            if (c == 0) KDA_TRACE(n, 4);
+            if (c == kLead) KDA_TRACE(n, 4);
             const float *bs = reinterpret_cast<const float *>(gs + GS_BETA) + (k & 1) * C;
             // this group's staging buffer, laid out as a slot
             unsigned char *slot = sm + SM_STAGE + g * SLOT_BYTES;
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(KhB + cmaj(c, 8)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
             }
             named_sync(bar_id, nt);
-            if (c == 0) KDA_TRACE(n, 5);
+            if (c == kLead) KDA_TRACE(n, 5);
             // the raw slot is free again: request this group's next chunk now
             fetch(n + NP, (k + 1) & 1);
             // -- A = strict_lower(beta K~ K^^T) and P = lower(Q~ K^^T) on the group's warps 2
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             named_sync(bar_id, nt);
-            if (c == 0) KDA_TRACE(n, 6);
+            if (c == kLead) KDA_TRACE(n, 6);
             // -- TB = (I + A)^-1 diag(beta): forward substitution, one column per lane
             if (pw == 2 && lane < C) {
                 const int j = lane;
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < C; ++r) Ptb[r * LDS + j] = __float2bfloat16_rn(x[r] * bj);
             }
             named_sync(bar_id, nt);
-            if (c == 0) KDA_TRACE(n, 7);
+            if (c == kLead) KDA_TRACE(n, 7);
             // -- -W = -TB K~: warps 2 and 3, warp pw covering key channels
             //    [64 (pw - 2), 64 (pw - 2) + 64)
             if (pw >= 2) {
@@ -704,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async();  // generic writes of the slot -> async-proxy bulk reads
             named_sync(bar_id, nt);
-            if (c == 0) KDA_TRACE(n, 8);
-            if (c == 0) {
+            if (c == kLead) KDA_TRACE(n, 8);
+            if (c == kLead) {
                 // into slot s of every CTA (this one last), each once it has consumed the
                 // slot's previous chunk; completion lands on that CTA's FULL barrier
                 const uint32_t dst = sbase + SM_PROD + s * SLOT_BYTES;
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 KDA_TRACE(n, 9);
             }
         }
-        if (pw == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (pw == 3) asm volatile("cp.async.wait_group 0;" ::: "memory");
     } else {
         regs_increase<kRegsConsumer>();
         if (warp < W_OUT0) {
