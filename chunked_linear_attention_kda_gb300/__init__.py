@@ -21,7 +21,8 @@ import threading
 
 from . import build as _build_mod
 
-__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "load_library",
+__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
+           "segmented_fwd", "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
@@ -30,7 +31,7 @@ KDA_F32, KDA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_kernel_launch_count", "kda_read_device_flags",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
-                    "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host")
+                    "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_read_device_flags.restype = ctypes.c_int
         lib.kda_selftest_bounded_wait.argtypes = [I64, P, P]
         lib.kda_selftest_bounded_wait.restype = ctypes.c_int
+        lib.kda_affine_combine.argtypes = [P, P, P, P, I32, I32, I32, P]
+        lib.kda_affine_combine.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -221,3 +224,79 @@ def selftest_bounded_wait(limit_cycles: int = 2_000_000):
                                               ctypes.c_void_p(st.cuda_stream)))
     flags = read_device_flags(reset=True)
     return int(d.item()), flags
+
+
+def affine_combine(M, S, B, out=None):
+    """``out = M S + B`` per head through ``kda_affine_combine`` (fp32 CUDA tensors;
+    ``M`` [H, d_k, d_k], ``S`` and ``B`` [H, d_k, d_v]): the combine step of the segment
+    scan -- a segment of tokens maps its start state S to M S + B."""
+    import torch
+    lib = load_library()
+    if M.device.type != "cuda":
+        raise ValueError("affine_combine runs on CUDA tensors only (there is no CPU path)")
+    H, dk, dk2 = M.shape
+    dv = S.shape[-1]
+    if dk2 != dk or tuple(S.shape) != (H, dk, dv) or tuple(B.shape) != (H, dk, dv):
+        raise ValueError("M must be [H, d_k, d_k], S and B [H, d_k, d_v]")
+    for t in (M, S, B):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.device != M.device:
+            raise ValueError("M, S and B must be contiguous float32 on one device")
+    if out is None:
+        out = torch.empty_like(B)
+    stream = torch.cuda.current_stream(M.device).cuda_stream
+    _check(lib, lib.kda_affine_combine(_ptr(M), _ptr(S), _ptr(B), _ptr(out), H, dk, dv,
+                                       ctypes.c_void_p(stream)))
+    return out
+
+
+def segmented_fwd(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, segments: int,
+                  output_final_state=True):
+    """The forward pass of ONE sequence split into ``segments`` time segments that run
+    side by side: for inputs whose heads alone leave most of the GPU idle.
+
+    Scheduling only; every step runs in the library's kernels (three ``kda_chunk_fwd``
+    calls and ``segments - 2`` ``kda_affine_combine`` calls):
+      1. all segments from a zero start (the first from h0): the first segment's outputs
+         and end state are final, every other segment gives its affine offset B_j;
+      2. segments 1.. from h0 = I with v = 0 (and d_v = d_k): their transitions M_j;
+      3. S_{j+1} = M_j S_j + B_j chains the true start states;
+      4. segments 1.. replay from their start states, writing the final outputs.
+    Costs about 3x the state-chain work of segments 1.. in exchange for a serial chain
+    ``segments`` times shorter. Returns ``(out, h_final)`` like ``chunk_fwd``.
+    """
+    import torch
+    from . import sharding
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens)
+    if n_seq != 1:
+        raise ValueError("segmented_fwd takes a single sequence")
+    if segments < 1:
+        raise ValueError("segments must be >= 1")
+    bounds = [(a, b) for a, b in sharding.segment_bounds(N, segments) if b > a]
+    if len(bounds) <= 1:
+        return chunk_fwd(q, k, v, gate_logits, beta, h0, cu_seqlens,
+                         output_final_state=output_final_state)
+    dev = q.device
+    P = len(bounds)
+    cu = torch.tensor([a for a, _ in bounds] + [N], dtype=torch.int32, device=dev)
+    # 1. zero start everywhere except the first segment
+    start = torch.zeros((P, H, dk, dv), dtype=torch.float32, device=dev)
+    if h0 is not None:
+        start[0].copy_(h0[0])
+    out, ends = chunk_fwd(q, k, v, gate_logits, beta, start, cu)
+    # 2. transitions of segments 1..P-1 (a contiguous token range)
+    b1 = bounds[1][0]
+    cu_t = (cu[1:] - b1).contiguous()
+    eye = torch.eye(dk, dtype=torch.float32, device=dev).expand(P - 1, H, dk, dk).contiguous()
+    v0 = torch.zeros((N - b1, H, dk), dtype=v.dtype, device=dev)
+    _, trans = chunk_fwd(q[b1:], k[b1:], v0, gate_logits[b1:], beta[b1:], eye, cu_t)
+    del v0
+    # 3. true start states of segments 1..P-1
+    starts = torch.empty((P - 1, H, dk, dv), dtype=torch.float32, device=dev)
+    starts[0].copy_(ends[0])
+    for j in range(1, P - 1):
+        affine_combine(trans[j - 1], starts[j - 1], ends[j], out=starts[j])
+    # 4. replay segments 1..P-1 into their slice of out
+    _, h_last = chunk_fwd(q[b1:], k[b1:], v[b1:], gate_logits[b1:], beta[b1:], starts, cu_t,
+                          out=out[b1:])
+    h_final = h_last[P - 2:P - 1].clone() if output_final_state else None
+    return out, h_final

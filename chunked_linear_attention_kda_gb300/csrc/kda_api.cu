@@ -126,6 +126,25 @@ kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     return ok();
 }
 
+kda_status kda_affine_combine(const float *M, const float *S_in, const float *B, float *S_out,
+                              int32_t n_heads, int32_t d_k, int32_t d_v, void *stream) {
+    if (!M || !S_in || !B || !S_out)
+        return fail(KDA_ERR_INVALID_ARG, "M, S_in, B and S_out are required");
+    if (n_heads <= 0 || d_k <= 0 || d_v <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_heads, d_k and d_v must be positive");
+    if (d_k > 128 || d_v > 128)
+        return fail(KDA_ERR_UNSUPPORTED, "d_k and d_v above 128 are not built");
+    const void *ptrs[] = {M, S_in, B, S_out};
+    for (const void *p : ptrs)
+        if (((uintptr_t)p & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "M, S_in, B and S_out must be 4-byte aligned");
+    if (S_out == M || S_out == S_in || S_out == B)
+        return fail(KDA_ERR_INVALID_ARG, "S_out may not alias an input");
+    return launched(kda::launch_affine_combine(M, S_in, B, S_out, n_heads, d_k, d_v,
+                                               (cudaStream_t)stream),
+                    "affine combine launch");
+}
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *gate_logits, const float *beta, const float *h0,
                          const int32_t *cu_seqlens, void *out, float *h_final,

@@ -36,6 +36,11 @@ bool tc_supported(const FwdArgs &args);
 // after limit_cycles, sets bit 0 of the status word and writes 1 to *d_returned.
 cudaError_t bounded_wait_selftest(long long limit_cycles, int *d_returned, cudaStream_t stream);
 
+// Per head, O = M S + B in fp32 (M: d_k x d_k; S, B, O: d_k x d_v; row-major, heads
+// contiguous): the combine step of the segment scan.
+cudaError_t launch_affine_combine(const float *M, const float *S, const float *B, float *O,
+                                  int n_heads, int d_k, int d_v, cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

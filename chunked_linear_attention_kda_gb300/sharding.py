@@ -12,9 +12,13 @@ Two ways to spread the work:
   serially through the state recurrence", "From Numerical Stability to Load
   Balancing", §2.1), so a sequence cut into segments needs exactly one exchange per
   boundary: the final state of segment r is the initial state of segment r + 1.
-  ``time_split_forward`` runs that hand-off with point-to-point send/recv. (It
-  pipelines rather than parallelises a single sequence; with several sequences in
-  flight the segments overlap.)
+  ``time_split_forward`` runs that hand-off with point-to-point send/recv (it
+  pipelines rather than parallelises a single sequence). ``affine_time_split_forward``
+  parallelises it: the recurrence is affine in its start state, so each rank first
+  computes its segment's map S_end = M S_start + B (two ordinary forward passes: from
+  h0 = I with v = 0, and from h0 = 0), one all-gather shares the maps, each rank chains
+  the maps of the ranks before it to get its true start state, and all ranks replay
+  their segments at once.
 
 Nothing here computes any part of the method: ``fwd`` is the caller's forward function
 (``chunk_fwd`` on a GPU).
@@ -95,3 +99,39 @@ def time_split_forward(fwd: Callable, segment_inputs: dict, h0, rank: int, world
     if rank < world - 1:
         dist.send(h_final.contiguous(), dst=rank + 1, group=group)
     return out, h_final
+
+
+def affine_time_split_forward(fwd: Callable, combine: Callable, segment_inputs: dict, h0,
+                              rank: int, world: int, group=None):
+    """This rank's segment of one sequence, all ranks in parallel (see the module note).
+
+    ``segment_inputs`` is as for ``time_split_forward``; ``h0`` is the sequence's start
+    state ([1, H, d_k, d_v], or None for zeros) -- rank 0's copy is broadcast. ``fwd`` is
+    the forward function (``fwd(q, k, v, gate_logits, beta, h0, cu_seqlens) -> (out,
+    h_final)``), ``combine(M, S, B)`` returns M S + B per head (``affine_combine`` on a
+    GPU). Returns ``(out, h_final)`` of the segment; the last rank's ``h_final`` is the
+    sequence's.
+    """
+    import torch
+    import torch.distributed as dist
+    q, v = segment_inputs["q"], segment_inputs["v"]
+    H, dk, dv = q.shape[1], q.shape[2], v.shape[2]
+    cu = segment_inputs["cu_seqlens"]
+    args = (segment_inputs["k"], segment_inputs["gate_logits"], segment_inputs["beta"])
+    sdt = torch.float32 if h0 is None else h0.dtype
+    zero = torch.zeros((1, H, dk, dv), dtype=sdt, device=q.device)
+    start = zero.clone() if h0 is None else h0.clone()
+    dist.broadcast(start, src=0, group=group)
+    # this segment's affine map
+    eye = torch.eye(dk, dtype=sdt, device=q.device).expand(1, H, dk, dk).contiguous()
+    v0 = torch.zeros((q.shape[0], H, dk), dtype=v.dtype, device=q.device)
+    _, M = fwd(q, args[0], v0, args[1], args[2], eye, cu)
+    _, B = fwd(q, args[0], v, args[1], args[2], zero, cu)
+    Ms = [torch.empty_like(M) for _ in range(world)]
+    Bs = [torch.empty_like(B) for _ in range(world)]
+    dist.all_gather(Ms, M.contiguous(), group=group)
+    dist.all_gather(Bs, B.contiguous(), group=group)
+    # exclusive scan of the maps of the ranks before this one
+    for r in range(rank):
+        start = combine(Ms[r][0], start[0], Bs[r][0]).unsqueeze(0)
+    return fwd(q, args[0], v, args[1], args[2], start.contiguous(), cu)

@@ -139,6 +139,22 @@ kda_status kda_chunk_fwd_simt(const void *q, const void *k, const void *v,
                               void *stream);
 
 /*
+ * kda_affine_combine -- combine step of the segment scan for one sequence split in
+ * time (an addition of this library; the pages describe only the serial recurrence,
+ * "From Numerical Stability to Load Balancing", §2.1, and this step follows from it).
+ * Over any span of tokens the recurrence is affine in its start state, so a segment
+ * maps S_start to S_end = M S_start + B, where M (d_k x d_k) is the segment's end state
+ * when run (kda_chunk_fwd) from h0 = I with v = 0 and B (d_k x d_v) its end state from
+ * h0 = 0. This call computes, per head, S_out = M S_in + B in fp32.
+ * Layout: M [n_heads][d_k][d_k]; S_in, B, S_out [n_heads][d_k][d_v]; row-major fp32 in
+ * device memory, 4-byte aligned, caller-owned; S_out may not alias an input. Queued on
+ * `stream`. Returns KDA_ERR_INVALID_ARG (NULL or misaligned pointer, aliasing,
+ * non-positive size), KDA_ERR_UNSUPPORTED (d_k or d_v above 128) or KDA_ERR_CUDA.
+ */
+kda_status kda_affine_combine(const float *M, const float *S_in, const float *B, float *S_out,
+                              int32_t n_heads, int32_t d_k, int32_t d_v, void *stream);
+
+/*
  * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
  * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
  * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs

@@ -86,3 +86,26 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(16, 1, 16)
     with pytest.raises(ValueError):
         kda.chunk_fwd(x, x, x, x, torch.zeros(16, 1))
+
+
+def combine(lib, *, M=FAKE, S=FAKE + 256, B=FAKE + 512, O=FAKE + 768, H=2, dk=128, dv=128):
+    P = ctypes.c_void_p
+    return lib.kda_affine_combine(P(M), P(S), P(B), P(O), H, dk, dv, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=None), 1), (dict(S=None), 1), (dict(B=None), 1), (dict(O=None), 1),
+    (dict(H=0), 1), (dict(dk=0), 1), (dict(dv=-1), 1), (dict(dk=129), 2), (dict(dv=200), 2),
+    (dict(M=FAKE + 2), 1), (dict(O=FAKE), 1), (dict(O=FAKE + 512), 1),
+])
+def test_affine_combine_host_validation(lib, kw, status):
+    st = combine(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_binding_refuses_cpu_combine():
+    import torch
+    m = torch.zeros(1, 4, 4)
+    with pytest.raises(ValueError):
+        kda.affine_combine(m, m, m)

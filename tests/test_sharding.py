@@ -109,6 +109,33 @@ def test_time_split_state_handoff_two_ranks_gloo():
     _run_ranks(_time_split_rank)
 
 
+def _affine_split_rank(rank, world, port):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    T = 101
+    q, k, v, a, beta, h0, cu = _inputs(23, [T], H=2, dk=4, dv=3)
+    s, t = sharding.segment_bounds(T, world)[rank]
+    seg = {"q": q[s:t], "k": k[s:t], "v": v[s:t], "gate_logits": a[s:t], "beta": beta[s:t],
+           "cu_seqlens": torch.tensor([0, t - s])}
+    start = h0.clone() if rank == 0 else torch.full_like(h0, float("nan"))  # only rank 0's counts
+    combine = lambda M, S, B: torch.einsum("hij,hjk->hik", M, S) + B  # noqa: E731
+    o, hf = sharding.affine_time_split_forward(_oracle_fwd, combine, seg, start, rank, world)
+    outs = [None] * world
+    dist.all_gather_object(outs, (s, t, o.numpy(), hf.numpy()))
+    if rank == 0:
+        o_ref, h_ref = _oracle_fwd(q, k, v, a, beta, h0, cu)
+        got = np.concatenate([x[2] for x in sorted(outs, key=lambda x: x[0])])
+        assert np.abs(got - o_ref.numpy()).max() < 1e-10
+        assert np.abs(outs[-1][3] - h_ref.numpy()).max() < 1e-10
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_affine_time_split_parallel_segments_gloo(world):
+    _run_ranks(_affine_split_rank, world=world)
+
+
 def test_time_split_needs_receive_buffer():
     with pytest.raises(ValueError):
         sharding.time_split_forward(_oracle_fwd, {}, None, 1, 2)
