@@ -82,6 +82,7 @@ constexpr int D = 128;          // d_k = d_v
 constexpr int C = kChunk;       // 16 tokens
 constexpr int kCS = 4;          // CTAs per (sequence, head) = cluster size
 constexpr int VB = D / kCS;     // value columns per CTA (32)
+static_assert(VB * 2 == 64, "the v tile rows are one 64-byte swizzle span");
 constexpr int NSW = VB / 16;    // state warps per CTA (2), 16 value columns each, and as
                                 // many output warps
 constexpr int NGRP = 2;         // prologue groups, alternating owned chunks
@@ -759,8 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_vt = [&](int s, uint32_t (&va)[4], uint32_t (&tb)[4]) {
             const uint32_t slot_s = sbase + SM_PROD + s * SLOT_BYTES;
             const uint32_t vs = sbase + SM_V + s * V_BYTES;
-            const int t = (i8 >> 1) * 8 + r8, vv = sw * 16 + (i8 & 1) * 8;
-            ldsm_x4_t(vs + (t * VB + vv) * 2, va[0], va[1], va[2], va[3]);
+            // the v tile arrives 64-byte swizzled (16-byte granule g of each 64-byte token
+            // row sits at g ^ address bits 7-8), so the 8 rows an 8 x 8 transposed read
+            // touches fall in 8 different bank groups
+            const int t = (i8 >> 1) * 8 + r8, g = sw * 2 + (i8 & 1);
+            const uint32_t row = vs + (uint32_t)(t * VB * 2);
+            ldsm_x4_t(row + 16u * ((uint32_t)g ^ ((row >> 7) & 3u)), va[0], va[1], va[2], va[3]);
             const int r = (i8 >> 1) * 8 + r8, j = (i8 & 1) * 8;
             ldsm_x4(slot_s + OFF_PTB + (r * LDS + j) * 2, tb[0], tb[1], tb[2], tb[3]);
         };
@@ -1020,7 +1025,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x,
-                int box_t = C) {
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE, int box_t = C) {
     // [n_tok][H][128] row-major viewed as a 3-D tensor (channel, head, token); boxes
     // are box_x channels x 1 head x 16 tokens. Out-of-range tokens read as zero.
     auto enc = tensor_map_encoder();
@@ -1032,7 +1037,7 @@ bool encode_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1042,7 +1047,7 @@ cudaError_t launch_tc_impl(const FwdArgs &a, cudaStream_t stream) {
     if (!encode_map(&mq, a.q, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&mk, a.k, false, a.n_tok, a.n_heads, D) ||
         !encode_map(&ma, a.a, true, a.n_tok, a.n_heads, D) ||
-        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB))
+        !encode_map(&mv, a.v, false, a.n_tok, a.n_heads, VB, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
