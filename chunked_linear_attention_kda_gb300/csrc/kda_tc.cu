@@ -867,12 +867,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (has_next) {
                 const int s1 = (n + 1) % NP, s2 = (n + 2) % NP;
-                // chunk n + 2's operands may stream in during this iteration
-                const bool roll = has_next2 && __all_sync(0xffffffffu, ready2);
+                // whether chunk n + 2's operands may stream in during this iteration is
+                // decided at key tile 2, when the probe's result has long arrived
+                bool roll = false;
                 float accU[2][2][4] = {};
                 mma16816(accU[1][0], va, tb[0], tb[1]);
                 mma16816(accU[1][1], va, tb[2], tb[3]);
-                if (roll) load_vt(s2, va, tb);
                 uint4 *ho = handoff((n + 1) & 1);
                 s_step(0, gl[0], kf[0], Ua);
 #pragma unroll
@@ -880,7 +880,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s_step(np, gl[np], kf[np], Ua);
                     load_s(s1, np - 1, kf[np - 1], gl[np - 1]);
                     u_step(np - 1, wf, accU, ho);
-                    if (roll) load_w(s2, np - 1, wf[np - 1]);
+                    if (np == 2) {
+                        roll = has_next2 && __all_sync(0xffffffffu, ready2);
+                        if (roll) {
+                            load_vt(s2, va, tb);
+                            load_w(s2, 0, wf[0]);
+                        }
+                    }
+                    if (roll && np >= 2) load_w(s2, np - 1, wf[np - 1]);
                 }
                 // every read of slot n by this warp has completed (its values were consumed)
                 __syncwarp();
