@@ -76,6 +76,17 @@ def test_ragged_lengths_and_states(path, dtype):
     check(x, path)
 
 
+@pytest.mark.parametrize("lengths", [
+    [128, 144, 160],            # 8, 9, 10 chunks: around the 8-slot ring
+    [16, 32, 48],               # 1, 2, 3 chunks: shorter than the prefetch distance
+    [255, 256, 257, 272, 127],  # ragged tails on both sides of 16 chunks
+    [1] * 7 + [4096],           # many tiny sequences next to a long one
+])
+def test_pipeline_edge_lengths(lengths):
+    x = K.make_inputs(lengths, 2, 128, 128, device=DEV, seed=17, h0_std=0.1)
+    check(x, "auto")
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("gate", ["bound", "no_decay"])
 def test_pinned_gates(path, gate):
