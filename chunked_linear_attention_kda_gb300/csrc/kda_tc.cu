@@ -7,8 +7,11 @@
 // whole sequence. Columns of the state evolve independently, so the four CTAs of a
 // head never exchange state. What they share is the per-chunk "prologue" -- the gate,
 // the in-chunk cumulative decay and the diagonal (intra-chunk) tile -- which does not
-// depend on the state: chunk n's prologue is computed once, by CTA n mod 4, and
-// broadcast into the other three CTAs' shared memory with DSMEM bulk copies.
+// depend on the state: chunk n's prologue is computed once, by CTA n mod 4, and copied
+// into every CTA's ring slot (its own included) with DSMEM bulk copies. Per CTA, two
+// state warps carry the serial chain, two output warps form the outputs from the bf16
+// state the state warps hand them, and two prologue groups of four warps alternate over
+// the CTA's own chunks.
 //
 // Per chunk of L <= 16 tokens (rows past L act as q = k = v = 0, beta = 0, g = 0):
 //   prologue   g = -5 sigmoid(a) per key channel; Gamma_r = prod_{i<=r} exp(g_i)
@@ -53,7 +56,10 @@ __device__ unsigned int g_device_flags;  // bit 0: a pipeline wait exceeded its 
 // Phase timestamps (SM clock) of the first cluster, first 32 chunks: a profiling aid
 // compiled only with -DKDA_TC_TRACE; the default build has no trace code. Stamps go to
 // shared memory and are copied out when the CTA finishes, so that tracing adds no
-// global stores to the pipeline.
+// global stores to the pipeline. Slots: 0/1 producer loop top / slot free; 2 raw tiles
+// requested; 3/4 prologue group loop top / inputs in; 5-8 gate, A and P, solve, W done;
+// 9 copies issued; 10-13 state warp iteration top / chain done / handoff published /
+// iteration end; 14 output warp done; 15 receipt forwarder saw the products land.
 #ifdef KDA_TC_TRACE
 __device__ long long g_trace[4][32][16];
 __device__ __forceinline__ long long trace_clock() {
