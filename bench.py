@@ -21,6 +21,11 @@ Reported alongside the device-timed value:
   cpu_baseline the fp64 oracle on the host cores on a bounded sample (rank 0, N = 1);
   clocks       nvidia-smi samples taken during the timed region.
 ``--impl reference`` times the oracle alone (the reference arm of this build).
+
+``--op decode`` measures the recurrent decode step instead (``kda_decode_step``: B = 256
+sequences x H = 32 heads, d = 128, bf16, each step advances every sequence by one
+token; the 512 MiB fp32 state, 4x the L2, is read and rewritten in place), with the
+same timing rules and its own JSON line.
 """
 from __future__ import annotations
 
@@ -39,9 +44,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA chunked-forward tokens/s (1 GB300) and % of tensor-core/HBM roofline"
+DECODE_METRIC = "KDA recurrent decode tokens/s (1 GB300) and % of HBM roofline"
+DECODE_B, DECODE_H, DECODE_D = 256, 32, 128
 UNIT = "tokens/s"
 KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu",
                   "chunked_linear_attention_kda_gb300/csrc/kda_simt.cu"]
+DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
 
 
@@ -74,12 +82,12 @@ def algorithmic_flops(x) -> int:
     return x.n_tok * x.n_heads * flops_per_token_head(x.d_k, x.d_v)
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(sources=None) -> str:
     """Digest of the kernel sources with comments and whitespace removed, so that the
     recorded ncu traffic stays valid across comment edits and is dropped on any code
     change."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES + ["chunked_linear_attention_kda_gb300/csrc/kda_internal.h"]:
+    for rel in (sources or KERNEL_SOURCES) + ["chunked_linear_attention_kda_gb300/csrc/kda_internal.h"]:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -88,12 +96,12 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=None):
     """DRAM bytes per launch from the committed ncu summary, only if it was taken on
     the current kernel sources (the digest must match)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(sources)
     for line in open(TRAFFIC_FILE):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("digest") == digest and f.get("workload") == workload:
@@ -369,6 +377,144 @@ def measure_e2e(x, dev, stream, steps, kda):
             "steps": steps, "api": "kda_chunk_fwd_from_host (pinned host buffers)"}
 
 
+# ------------------------------------------------------------------ decode step
+
+def decode_bytes_per_seq_head(d_k: int, d_v: int, io_bytes: int) -> int:
+    """Algorithmic HBM bytes of one decode step per sequence and head: the fp32 state
+    read and written, q, k, v read and o written in the I/O dtype, gate logits and beta
+    read."""
+    return 8 * d_k * d_v + io_bytes * (2 * d_k + 2 * d_v) + 4 * d_k + 4
+
+
+def run_decode(args):
+    import torch
+    import chunked_linear_attention_kda_gb300 as kda
+    import kda_inputs as K
+
+    world, rank, local = dist_env()
+    on = init_dist(world, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load_library(build_if_missing=True)
+    B, H, d = DECODE_B, DECODE_H, DECODE_D
+    x = K.make_inputs([1] * B, H, d, d, dtype=torch.bfloat16, device=dev,
+                      seed=K.SEED_BASE + 99 + 7919 * rank, h0_std=0.5, name="decode")
+    state = x.h0.clone()
+    out = torch.empty((B, H, d), dtype=x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.decode_step(x.q, x.k, x.v, x.a, x.beta, state, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n0 = kda.kernel_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(on)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(on)
+    launches = kda.kernel_launch_count() - n0
+    total_ms = max_over_ranks(t0.elapsed_time(t1), on, dev)
+    value = B * world * args.steps / (total_ms * 1e-3)
+    peaks = measured_peaks()
+    bytes_launch = B * H * decode_bytes_per_seq_head(d, d, 2)
+    mean_launch_s = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) * 1e-3
+    achieved = bytes_launch / mean_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic("decode-B256-H32-d128", DECODE_SOURCES),
+                "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)",
+                "algorithmic_bytes_per_launch": bytes_launch}
+
+    # end to end through the public API: this step's inputs copied from pinned host
+    # memory, the step, its outputs copied back; the state stays resident on the device
+    host = [t.detach().to("cpu").pin_memory() for t in (x.q, x.k, x.v, x.a, x.beta)]
+    devb = [torch.empty_like(t, device=dev) for t in host]
+    h_out = torch.empty((B, H, d), dtype=x.dtype).pin_memory()
+    e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        for hb, db in zip(host, devb):
+            db.copy_(hb, non_blocking=True)
+        o = kda.decode_step(*devb, state)
+        h_out.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": round(B * world / (e_ms * 1e-3), 1), "unit": "tokens/s",
+           "ms_per_step": round(e_ms, 4),
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
+           "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e_steps,
+           "api": "decode_step with pinned host inputs and outputs (state resident)"}
+    line = {"metric": DECODE_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode-B256-H32-d128", "sequences_per_gpu": B, "heads": H,
+                       "d_k": d, "d_v": d, "state_bytes": B * H * d * d * 4,
+                       "l2": "state (%.0f MiB) exceeds the 129 MB L2; no flush between steps"
+                             % (B * H * d * d * 4 / 2**20)},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk.summary(), "kernel_digest": kernel_source_digest(DECODE_SOURCES)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(x)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def decode_cpu_baseline(x, budget_s: float = 10.0):
+    """The oracle's decode step on the host cores, on the first n sequences of the batch
+    (all heads), n grown until a call takes a few seconds; scaled to tokens/s."""
+    from oracle import recurrence
+    cpu = lambda t: t.detach().to("cpu")  # noqa: E731
+    threads = recurrence.default_threads()
+    recurrence.build()
+    n = 8
+    while True:
+        args = [cpu(t[:n]) for t in (x.q, x.k, x.v, x.a, x.beta, x.h0)]
+        t0 = time.perf_counter()
+        recurrence.decode_step(*args, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or n >= x.q.shape[0]:
+            break
+        n = min(n * 4, x.q.shape[0])
+    # repeat the step (each from the previous state) until the sample takes a few seconds
+    reps, state = 0, args[5]
+    t0 = time.perf_counter()
+    while True:
+        _, state = recurrence.decode_step(*args[:5], state, threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s / 4:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * reps / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "sample": f"{reps} fp64 oracle decode steps on {n} sequences x "
+                                     f"{x.q.shape[1]} heads, {threads} host threads"}
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -421,10 +567,20 @@ def main():
     ap.add_argument("--workload", type=int, default=3, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="forward", choices=["forward", "decode"],
+                    help="forward: the chunked forward pass (default); decode: the "
+                         "recurrent decode step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.op == "decode":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the decode line has no reference arm; its cpu_baseline is "
+                              "the oracle"}), flush=True)
+        else:
+            run_decode(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

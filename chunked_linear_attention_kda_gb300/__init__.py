@@ -22,7 +22,7 @@ import threading
 from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
-           "segmented_fwd", "load_library",
+           "segmented_fwd", "decode_step", "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
@@ -31,7 +31,8 @@ KDA_F32, KDA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_kernel_launch_count", "kda_read_device_flags",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
-                    "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine")
+                    "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
+                    "kda_decode_step")
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_selftest_bounded_wait.restype = ctypes.c_int
         lib.kda_affine_combine.argtypes = [P, P, P, P, I32, I32, I32, P]
         lib.kda_affine_combine.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [P] * 7 + [I32, I32, I32, I32, ctypes.c_int, P]
+        lib.kda_decode_step.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -246,6 +249,40 @@ def affine_combine(M, S, B, out=None):
     stream = torch.cuda.current_stream(M.device).cuda_stream
     _check(lib, lib.kda_affine_combine(_ptr(M), _ptr(S), _ptr(B), _ptr(out), H, dk, dv,
                                        ctypes.c_void_p(stream)))
+    return out
+
+
+def decode_step(q, k, v, gate_logits, beta, state, *, out=None):
+    """One recurrent decode step through ``kda_decode_step``: every sequence advances by
+    one token. ``q, k, gate_logits`` [B, H, d_k]; ``v`` [B, H, d_v]; ``beta`` [B, H];
+    ``state`` [B, H, d_k, d_v] fp32, updated in place. Returns ``out`` [B, H, d_v]."""
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("decode_step runs on CUDA tensors only (there is no CPU path)")
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, d_k]")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q/k/v must be bfloat16 or float32")
+    for name, t, shape, dt in (("k", k, (B, H, dk), q.dtype), ("v", v, (B, H, dv), q.dtype),
+                               ("gate_logits", gate_logits, (B, H, dk), torch.float32),
+                               ("beta", beta, (B, H), torch.float32),
+                               ("state", state, (B, H, dk, dv), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt:
+            raise ValueError(f"{name} must be {dt} with shape {shape}, got "
+                             f"{t.dtype} {tuple(t.shape)}")
+    for t in (q, k, v, gate_logits, beta, state):
+        if not t.is_contiguous() or t.device != q.device:
+            raise ValueError("all tensors must be contiguous and on one device")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib, lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta),
+                                    _ptr(state), _ptr(out), B, H, dk, dv,
+                                    KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+                                    ctypes.c_void_p(stream)))
     return out
 
 

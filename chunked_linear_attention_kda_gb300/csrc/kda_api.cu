@@ -145,6 +145,51 @@ kda_status kda_affine_combine(const float *M, const float *S_in, const float *B,
                     "affine combine launch");
 }
 
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *gate_logits, const float *beta, float *state, void *out,
+                           int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
+                           kda_dtype dtype, void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "dtype must be KDA_F32 or KDA_BF16");
+    if (n_seq < 0 || n_heads <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_seq must be >= 0 and n_heads > 0");
+    if (d_k <= 0 || d_v <= 0) return fail(KDA_ERR_INVALID_ARG, "d_k and d_v must be positive");
+    if (d_k > 128 || d_v > 128)
+        return fail(KDA_ERR_UNSUPPORTED, "d_k and d_v above 128 are not built");
+    if ((int64_t)n_seq * n_heads > 0x7fffffffLL)
+        return fail(KDA_ERR_INVALID_ARG, "n_seq * n_heads exceeds 2^31 - 1");
+    if (n_seq == 0) return ok();
+    if (!q || !k || !v || !gate_logits || !beta || !state || !out)
+        return fail(KDA_ERR_INVALID_ARG, "every pointer is required");
+    const size_t es = dtype == KDA_BF16 ? 2 : 4;
+    const void *elems[] = {q, k, v, out};
+    for (const void *p : elems)
+        if (((uintptr_t)p % es) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "q, k, v and out must be aligned to their element size");
+    const void *f32s[] = {gate_logits, beta, state};
+    for (const void *p : f32s)
+        if (((uintptr_t)p & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "gate_logits, beta and state must be 4-byte aligned");
+    const size_t bh = (size_t)n_seq * n_heads;
+    struct Range { const void *p; size_t bytes; };
+    const Range ins[] = {{q, bh * d_k * es}, {k, bh * d_k * es}, {v, bh * d_v * es},
+                         {gate_logits, bh * d_k * 4}, {beta, bh * 4}};
+    const Range st_r = {state, bh * d_k * d_v * 4}, out_r = {out, bh * d_v * es};
+    auto overlap = [](const Range &x, const Range &y) {
+        const uintptr_t a = (uintptr_t)x.p, b = (uintptr_t)y.p;
+        return a < b + y.bytes && b < a + x.bytes;
+    };
+    for (const Range &r : ins)
+        if (overlap(r, st_r) || overlap(r, out_r))
+            return fail(KDA_ERR_INVALID_ARG, "state and out may not overlap an input");
+    if (overlap(st_r, out_r)) return fail(KDA_ERR_INVALID_ARG, "state and out may not overlap");
+    kda::DecodeArgs p;
+    p.q = q; p.k = k; p.v = v; p.a = gate_logits; p.beta = beta; p.state = state; p.out = out;
+    p.n_seq = n_seq; p.n_heads = n_heads; p.d_k = d_k; p.d_v = d_v;
+    p.bf16 = dtype == KDA_BF16;
+    return launched(kda::launch_decode_step(p, (cudaStream_t)stream), "decode step launch");
+}
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *gate_logits, const float *beta, const float *h0,
                          const int32_t *cu_seqlens, void *out, float *h_final,

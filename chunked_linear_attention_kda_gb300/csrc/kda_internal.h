@@ -41,6 +41,18 @@ cudaError_t bounded_wait_selftest(long long limit_cycles, int *d_returned, cudaS
 cudaError_t launch_affine_combine(const float *M, const float *S, const float *B, float *O,
                                   int n_heads, int d_k, int d_v, cudaStream_t stream);
 
+// One recurrent decode step: q, k, a [n_seq, H, d_k]; v, out [n_seq, H, d_v]; beta
+// [n_seq, H]; state [n_seq, H, d_k, d_v] fp32, read and overwritten.
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *a, *beta;
+    float *state;
+    void *out;
+    int32_t n_seq, n_heads, d_k, d_v;
+    bool bf16;  // q/k/v/out element type: bf16 when true, fp32 otherwise
+};
+cudaError_t launch_decode_step(const DecodeArgs &args, cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

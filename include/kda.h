@@ -155,6 +155,34 @@ kda_status kda_affine_combine(const float *M, const float *S_in, const float *B,
                               int32_t n_heads, int32_t d_k, int32_t d_v, void *stream);
 
 /*
+ * kda_decode_step -- one recurrent decode step: each of n_seq sequences advances by
+ * one token, from its state to the next, per head:
+ *   S' = Diag(exp g) S,  g = -5 sigmoid(a);  u = beta (v - S'^T k);
+ *   S <- S' + k u^T;  o = d_k^-1/2 S^T q   (the state after the write)
+ * -- the operation above for a single token ("From Numerical Stability to Load
+ * Balancing", §2.1-2.2), i.e. what kda_chunk_fwd computes for a one-token sequence
+ * started from `state`. Pairs with kda_chunk_fwd for generation: the prompt's h_final
+ * is the first decode step's state.
+ * Layout (contiguous, row-major, caller-owned device memory):
+ *   q, k          [n_seq, n_heads, d_k]        dtype
+ *   v             [n_seq, n_heads, d_v]        dtype
+ *   gate_logits   [n_seq, n_heads, d_k]        float32
+ *   beta          [n_seq, n_heads]             float32
+ *   state         [n_seq, n_heads, d_k, d_v]   float32, read and overwritten in place
+ *   out           [n_seq, n_heads, d_v]        dtype
+ * q, k, v and out must be aligned to their element size, gate_logits, beta and state
+ * to 4 bytes; state and out may not overlap each other or any input. Any 1 <= d_k,
+ * d_v <= 128. Asynchronous on `stream`; nothing is allocated. Returns
+ * KDA_ERR_INVALID_ARG (NULL pointer, negative or zero size, misalignment, overlap),
+ * KDA_ERR_UNSUPPORTED (dtype, or d_k/d_v above 128) or KDA_ERR_CUDA; n_seq = 0 is a
+ * valid no-op.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *gate_logits, const float *beta, float *state,
+                           void *out, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                           int32_t d_v, kda_dtype dtype, void *stream);
+
+/*
  * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
  * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
  * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs

@@ -128,3 +128,17 @@ def kda_forward(q, k, v, a, beta, h0=None, cu_seqlens=None, *, g_min: float = -5
     if rc != 0:
         raise RuntimeError(f"kda_oracle_fwd failed with code {rc}")
     return out, hf
+
+
+def decode_step(q, k, v, a, beta, state, *, g_min: float = -5.0, scale: float | None = None,
+                threads: int | None = None, mutant: int = 0):
+    """One recurrent decode step: each of B sequences advances by one token from its own
+    state. By definition this is the recurrence run on B one-token sequences started from
+    ``state``, so it calls ``kda_forward`` with ``cu_seqlens = [0, 1, ..., B]``.
+
+    ``q, k, a`` [B, H, d_k]; ``v`` [B, H, d_v]; ``beta`` [B, H]; ``state``
+    [B, H, d_k, d_v]. Returns ``(out [B, H, d_v], new_state [B, H, d_k, d_v])`` in fp64.
+    """
+    B = (q.shape[0])
+    return kda_forward(q, k, v, a, beta, state, np.arange(B + 1, dtype=np.int64),
+                       g_min=g_min, scale=scale, threads=threads, mutant=mutant)

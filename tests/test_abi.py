@@ -109,3 +109,38 @@ def test_binding_refuses_cpu_combine():
     m = torch.zeros(1, 4, 4)
     with pytest.raises(ValueError):
         kda.affine_combine(m, m, m)
+
+
+def decode(lib, *, q=FAKE, k=2 * FAKE, v=3 * FAKE, a=4 * FAKE, beta=5 * FAKE, state=6 * FAKE,
+           out=8 * FAKE, n_seq=2, H=2, dk=128, dv=128, dtype=1):
+    P = ctypes.c_void_p
+    return lib.kda_decode_step(P(q), P(k), P(v), P(a), P(beta), P(state), P(out), n_seq, H, dk,
+                               dv, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(a=None), 1),
+    (dict(beta=None), 1), (dict(state=None), 1), (dict(out=None), 1),
+    (dict(n_seq=-1), 1), (dict(H=0), 1), (dict(dk=0), 1), (dict(dv=-2), 1),
+    (dict(dk=129), 2), (dict(dv=256), 2), (dict(dtype=5), 2),
+    (dict(q=FAKE + 1), 1), (dict(dtype=0, v=3 * FAKE + 2), 1), (dict(a=4 * FAKE + 2), 1),
+    (dict(state=6 * FAKE + 1), 1),
+    (dict(state=FAKE + 256), 1),          # state overlaps q
+    (dict(out=6 * FAKE + 4096), 1),       # out inside the state
+    (dict(out=5 * FAKE), 1),              # out on beta
+])
+def test_decode_step_host_validation(lib, kw, status):
+    st = decode(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_decode_step_nothing_to_do_is_ok(lib):
+    assert decode(lib, n_seq=0) == 0
+
+
+def test_binding_refuses_cpu_decode():
+    import torch
+    x = torch.zeros(1, 1, 16)
+    with pytest.raises(ValueError):
+        kda.decode_step(x, x, x, x, torch.zeros(1, 1), torch.zeros(1, 1, 16, 16))

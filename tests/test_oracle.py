@@ -183,3 +183,40 @@ def test_rejects_bad_offsets():
     q, k, v, a, beta, _, _ = P._rand(rng, [4], 1, 2, 2)
     with pytest.raises(AssertionError):
         recurrence.kda_forward(q, k, v, a, beta, None, [0, 3, 2])
+
+
+# ---------------------------------------------------------------- decode step
+
+def test_decode_steps_chain_to_the_forward_pass():
+    """T decode steps from h0, each feeding the next its state, reproduce the T-token
+    forward pass of every sequence (the recurrence consumes tokens one at a time)."""
+    rng = np.random.default_rng(16)
+    B, T, H, dk, dv = 3, 7, 2, 5, 4
+    q, k, v, a, beta, h0, cu = P._rand(rng, [T] * B, H, dk, dv)
+    o_ref, h_ref = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    state = h0.copy()
+    outs = []
+    for t in range(T):
+        rows = [b * T + t for b in range(B)]
+        o, state = recurrence.decode_step(q[rows], k[rows], v[rows], a[rows], beta[rows], state)
+        outs.append(o)
+    got = np.stack(outs, axis=1).reshape(B * T, H, dv)   # [B, T] -> packed token order
+    assert np.allclose(got, o_ref, rtol=0, atol=1e-13)
+    assert np.allclose(state, h_ref, rtol=0, atol=1e-13)
+
+
+def test_decode_step_pure_decay_closed_form():
+    """beta = 0 writes nothing and a saturated gate decays every channel by exactly
+    exp(-5): the state becomes exp(-5) S and the output d_k^-1/2 exp(-5) S^T q."""
+    rng = np.random.default_rng(17)
+    B, H, dk, dv = 2, 3, 6, 5
+    q = rng.standard_normal((B, H, dk))
+    k = rng.standard_normal((B, H, dk))
+    v = rng.standard_normal((B, H, dv))
+    a = np.full((B, H, dk), 80.0)            # sigmoid(80) = 1 to double precision
+    beta = np.zeros((B, H))
+    S = rng.standard_normal((B, H, dk, dv))
+    o, S1 = recurrence.decode_step(q, k, v, a, beta, S)
+    assert np.allclose(S1, math.exp(-5.0) * S, rtol=1e-14, atol=0)
+    want = math.exp(-5.0) / math.sqrt(dk) * np.einsum("bhkv,bhk->bhv", S, q)
+    assert np.allclose(o, want, rtol=1e-13, atol=1e-15)
