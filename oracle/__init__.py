@@ -12,5 +12,10 @@ Contents
                 to pin that the chunked form equals the recurrence.
 ``brute``       an fp64 NumPy unrolled transition-matrix form, used only on tiny
                 inputs to pin the recurrence.
+``backward``    the gradients of the recurrence (its vector-Jacobian product), by
+                PyTorch reverse-mode differentiation of a plain fp64 token loop;
+                pinned to central finite differences of ``recurrence``.
+
+``recurrence.decode_step`` is the recurrence on one-token sequences (a decode step).
 """
 from .recurrence import build, kda_forward, oracle_library_path  # noqa: F401

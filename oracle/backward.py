@@ -1,0 +1,90 @@
+"""fp64 gradients of the recurrence by reverse-mode automatic differentiation.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The pages define the forward operation only; its backward pass is by definition the
+gradient of that forward. The function differentiated here is the token-by-token
+recurrence, the same definition the C oracle (``kda_oracle.c``) implements:
+
+    g_t = g_min * sigmoid(a_t)                      per key channel, g_min = -5
+    S   <- Diag(exp g_t) S
+    S   <- S + beta_t k_t (v_t - S^T k_t)^T
+    o_t  = scale * S^T q_t                          scale = d_k^-1/2
+
+("From Numerical Stability to Load Balancing", §2.1-2.2; "Demystifying
+Trillion-Parameter MoE Models", Breakthrough 1 §2), written as plain PyTorch fp64 CPU
+operations one token at a time (all heads at once). ``torch.autograd`` then gives the
+gradients of
+
+    L = <dout, out> + <dh_final, h_final>
+
+with respect to q, k, v, the gate logits a, beta and h0 -- the vector-Jacobian product
+a backward kernel computes. The forward written here is pinned to the C oracle, and the
+gradients to central finite differences and a one-token closed form, in the tests.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def _t(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu", torch.float64).clone()
+    return torch.as_tensor(np.asarray(x, dtype=np.float64)).clone()
+
+
+def forward_torch(q, k, v, a, beta, h0, cu, *, g_min=-5.0, scale=None):
+    """The recurrence on fp64 torch tensors (differentiable). Shapes as
+    ``recurrence.kda_forward``; ``cu`` is a sequence of int offsets. Returns
+    ``(out [N, H, d_v], h_final [n_seq, H, d_k, d_v])``."""
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if scale is None:
+        scale = dk ** -0.5
+    outs, finals = [], []
+    for n in range(len(cu) - 1):
+        S = h0[n] if h0 is not None else torch.zeros((H, dk, dv), dtype=torch.float64)
+        for t in range(int(cu[n]), int(cu[n + 1])):
+            gamma = torch.exp(g_min * torch.sigmoid(a[t]))            # [H, dk]
+            S = gamma[:, :, None] * S
+            pred = torch.einsum("hkv,hk->hv", S, k[t])               # S^T k
+            S = S + beta[t][:, None, None] * torch.einsum("hk,hv->hkv", k[t], v[t] - pred)
+            outs.append(scale * torch.einsum("hkv,hk->hv", S, q[t]))  # S^T q
+        finals.append(S)
+    out = torch.stack(outs) if outs else torch.zeros((0, H, dv), dtype=torch.float64)
+    return out, torch.stack(finals)
+
+
+def kda_backward(q, k, v, a, beta, h0, cu_seqlens, dout, dh_final=None, *, g_min=-5.0,
+                 scale=None):
+    """Gradients of ``<dout, out> + <dh_final, h_final>``.
+
+    Shapes (packed, token-major): ``q, k, a`` [N, H, d_k]; ``v``, ``dout`` [N, H, d_v];
+    ``beta`` [N, H]; ``h0``, ``dh_final`` [n_seq, H, d_k, d_v] or None (zeros);
+    ``cu_seqlens`` [n_seq + 1] or None (one sequence). Returns a dict of fp64 numpy
+    arrays ``dq, dk, dv, da, dbeta, dh0``.
+    """
+    q, k, v, a, beta, dout = (_t(x) for x in (q, k, v, a, beta, dout))
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is None:
+        cu = [0, N]
+    else:
+        cu = [int(c) for c in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
+                               else cu_seqlens)]
+    n_seq = len(cu) - 1
+    h0 = _t(h0) if h0 is not None else torch.zeros((n_seq, H, dk, dv), dtype=torch.float64)
+    leaves = [q, k, v, a, beta, h0]
+    for x in leaves:
+        x.requires_grad_(True)
+    out, hf = forward_torch(q, k, v, a, beta, h0, cu, g_min=g_min, scale=scale)
+    loss = (out * dout).sum()
+    if dh_final is not None:
+        loss = loss + (hf * _t(dh_final)).sum()
+    grads = torch.autograd.grad(loss, leaves, allow_unused=True)
+    names = ["dq", "dk", "dv", "da", "dbeta", "dh0"]
+    return {nm: (g.numpy() if g is not None else np.zeros(x.shape))
+            for nm, g, x in zip(names, grads, leaves)}

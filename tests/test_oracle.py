@@ -220,3 +220,81 @@ def test_decode_step_pure_decay_closed_form():
     assert np.allclose(S1, math.exp(-5.0) * S, rtol=1e-14, atol=0)
     want = math.exp(-5.0) / math.sqrt(dk) * np.einsum("bhkv,bhk->bhv", S, q)
     assert np.allclose(o, want, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- backward oracle
+
+from oracle import backward as B  # noqa: E402
+
+
+def test_backward_oracle_forward_is_the_recurrence():
+    """The function the backward oracle differentiates equals the pinned C oracle."""
+    rng = np.random.default_rng(21)
+    q, k, v, a, beta, h0, cu = P._rand(rng, [6, 0, 17], 2, 5, 4)
+    o_ref, h_ref = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    t = lambda x: torch.as_tensor(x)  # noqa: E731
+    o, hf = B.forward_torch(t(q), t(k), t(v), t(a), t(beta), t(h0), list(cu))
+    assert np.allclose(o.numpy(), o_ref, rtol=0, atol=1e-13)
+    assert np.allclose(hf.numpy(), h_ref, rtol=0, atol=1e-13)
+
+
+def _loss(q, k, v, a, beta, h0, cu, dout, dhf):
+    o, hf = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    return float(np.sum(o * dout) + np.sum(hf * dhf))
+
+
+def test_backward_oracle_matches_finite_differences():
+    """Central differences of the C oracle's loss, element by element for every input
+    (independent of automatic differentiation)."""
+    rng = np.random.default_rng(22)
+    lengths, H, dk, dv = [5, 0, 3], 2, 3, 2
+    q, k, v, a, beta, h0, cu = P._rand(rng, lengths, H, dk, dv)
+    N = sum(lengths)
+    dout = rng.standard_normal((N, H, dv))
+    dhf = rng.standard_normal((len(lengths), H, dk, dv))
+    g = B.kda_backward(q, k, v, a, beta, h0, cu, dout, dhf)
+    args = {"dq": q, "dk": k, "dv": v, "da": a, "dbeta": beta, "dh0": h0}
+    eps = 1e-6
+    for name, x in args.items():
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            lp = _loss(q, k, v, a, beta, h0, cu, dout, dhf)
+            x[idx] = keep - eps
+            lm = _loss(q, k, v, a, beta, h0, cu, dout, dhf)
+            x[idx] = keep
+            fd[idx] = (lp - lm) / (2 * eps)
+        err = np.abs(g[name] - fd).max() / max(np.abs(fd).max(), 1e-12)
+        assert err < 1e-7, (name, err)
+
+
+def test_backward_oracle_one_token_closed_form():
+    """One token from a zero state: S = beta k v^T, o = s beta (q.k) v, so
+    dv = s beta (q.k) dO, dbeta = s (q.k)(v.dO), dq = s beta (v.dO) k,
+    dk = s beta (v.dO) q, da = 0 (the decay multiplies a zero state); and since
+    S_1 = (I - beta k k^T) Diag(gamma) S_0 + beta k v^T, dh0 = Diag(gamma) (I - beta k k^T)
+    s q dO^T."""
+    rng = np.random.default_rng(23)
+    H, dk, dv = 3, 4, 5
+    q = rng.standard_normal((1, H, dk))
+    k = rng.standard_normal((1, H, dk))
+    v = rng.standard_normal((1, H, dv))
+    a = rng.standard_normal((1, H, dk))
+    beta = rng.uniform(0.1, 0.9, (1, H))
+    dO = rng.standard_normal((1, H, dv))
+    g = B.kda_backward(q, k, v, a, beta, None, [0, 1], dO)
+    s = dk ** -0.5
+    qk = np.einsum("hk,hk->h", q[0], k[0])
+    vdo = np.einsum("hv,hv->h", v[0], dO[0])
+    b = beta[0]
+    assert np.allclose(g["dv"][0], (s * b * qk)[:, None] * dO[0], atol=1e-14)
+    assert np.allclose(g["dbeta"][0], s * qk * vdo, atol=1e-14)
+    assert np.allclose(g["dq"][0], (s * b * vdo)[:, None] * k[0], atol=1e-14)
+    assert np.allclose(g["dk"][0], (s * b * vdo)[:, None] * q[0], atol=1e-14)
+    assert np.allclose(g["da"], 0.0, atol=1e-15)
+    gam = np.exp(-5.0 / (1.0 + np.exp(-a[0])))
+    for h in range(H):
+        Ph = np.eye(dk) - b[h] * np.outer(k[0, h], k[0, h])
+        want = gam[h][:, None] * (Ph @ (s * np.outer(q[0, h], dO[0, h])))
+        assert np.allclose(g["dh0"][0, h], want, atol=1e-13)
