@@ -22,7 +22,7 @@ import threading
 from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
-           "segmented_fwd", "decode_step", "load_library",
+           "segmented_fwd", "decode_step", "chunk_bwd", "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_kernel_launch_count", "kda_read_device_flags",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
-                    "kda_decode_step")
+                    "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +88,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_affine_combine.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P] * 7 + [I32, I32, I32, I32, ctypes.c_int, P]
         lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_chunk_bwd_workspace_bytes.argtypes = [I64, I32, I32, I32, I32]
+        lib.kda_chunk_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_chunk_bwd.argtypes = [P] * 16 + [ctypes.c_size_t, I64, I32, I32, I32, I32,
+                                                 ctypes.c_int, P]
+        lib.kda_chunk_bwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -284,6 +289,48 @@ def decode_step(q, k, v, gate_logits, beta, state, *, out=None):
                                     KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
                                     ctypes.c_void_p(stream)))
     return out
+
+
+def chunk_bwd(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final=None, *,
+              want_dh0=True, workspace=None):
+    """Backward pass through ``kda_chunk_bwd``: the gradients of ``<dout, out> +
+    <dh_final, h_final>`` for the forward ``chunk_fwd(q, k, v, gate_logits, beta, h0,
+    cu_seqlens)``. Returns ``(dq, dk, dv, dgate_logits, dbeta, dh0)`` (``dh0`` None unless
+    ``want_dh0``). ``workspace``: an optional uint8 CUDA tensor of at least
+    ``kda_chunk_bwd_workspace_bytes`` bytes (allocated here when None)."""
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("chunk_bwd runs on CUDA tensors only (there is no CPU path)")
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens)
+    if tuple(dout.shape) != (N, H, dv) or dout.dtype != q.dtype or not dout.is_contiguous():
+        raise ValueError(f"dout must be contiguous {q.dtype} with shape {(N, H, dv)}")
+    if dh_final is not None and (tuple(dh_final.shape) != (n_seq, H, dk, dv) or
+                                 dh_final.dtype != torch.float32 or
+                                 not dh_final.is_contiguous()):
+        raise ValueError(f"dh_final must be contiguous float32 {(n_seq, H, dk, dv)}")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    need = int(lib.kda_chunk_bwd_workspace_bytes(N, n_seq, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    dq = torch.empty_like(q)
+    dk_ = torch.empty_like(k)
+    dv_ = torch.empty_like(v)
+    da = torch.empty_like(gate_logits)
+    db = torch.empty_like(beta)
+    dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 \
+        else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib, lib.kda_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+        _ptr(dout), _ptr(dh_final), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(da), _ptr(db),
+        _ptr(dh0), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+        ctypes.c_void_p(stream)))
+    return dq, dk_, dv_, da, db, dh0
 
 
 def segmented_fwd(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, segments: int,

@@ -190,6 +190,74 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
     return launched(kda::launch_decode_step(p, (cudaStream_t)stream), "decode step launch");
 }
 
+size_t kda_chunk_bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads,
+                                     int32_t d_k, int32_t d_v) {
+    if (n_tok < 0 || n_seq < 0 || n_heads <= 0 || d_k <= 0 || d_v <= 0) return 0;
+    return kda::bwd_workspace_bytes(n_tok, n_seq, n_heads, d_k, d_v);
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const float *gate_logits,
+                         const float *beta, const float *h0, const int32_t *cu_seqlens,
+                         const void *dout, const float *dh_final, void *dq, void *dk, void *dv,
+                         float *dgate_logits, float *dbeta, float *dh0, void *workspace,
+                         size_t workspace_bytes, int64_t n_tok, int32_t n_seq,
+                         int32_t n_heads, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                         void *stream) {
+    // the forward's argument rules for the shared inputs (out stands in for dout)
+    kda_status s = validate(pack(q, k, v, gate_logits, beta, h0, cu_seqlens,
+                                 const_cast<void *>(dout), nullptr, n_tok, n_seq, n_heads, d_k,
+                                 d_v, dtype),
+                            dtype);
+    if (s != KDA_OK) return s;
+    if (n_seq == 0) return ok();
+    if (n_tok > 0 && (!dq || !dk || !dv || !dgate_logits || !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "dq, dk, dv, dgate_logits and dbeta are required");
+    const size_t need = kda::bwd_workspace_bytes(n_tok, n_seq, n_heads, d_k, d_v);
+    if (!workspace || workspace_bytes < need)
+        return fail(KDA_ERR_INVALID_ARG, "workspace is NULL or smaller than "
+                                         "kda_chunk_bwd_workspace_bytes()");
+    const size_t es = dtype == KDA_BF16 ? 2 : 4;
+    const void *outs_io[] = {dq, dk, dv};
+    for (const void *p : outs_io)
+        if (((uintptr_t)p % es) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "dq, dk and dv must be aligned to their element size");
+    const void *outs_f32[] = {dgate_logits, dbeta, dh0, dh_final, workspace};
+    for (const void *p : outs_f32)
+        if (((uintptr_t)p & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "dgate_logits, dbeta, dh0, dh_final and workspace must be 4-byte aligned");
+    struct Range { const void *p; size_t bytes; };
+    const size_t nk = (size_t)n_tok * n_heads * d_k, nv = (size_t)n_tok * n_heads * d_v;
+    const size_t ns = (size_t)n_seq * n_heads * d_k * d_v;
+    const Range ins[] = {{q, nk * es}, {k, nk * es}, {v, nv * es}, {gate_logits, nk * 4},
+                         {beta, (size_t)n_tok * n_heads * 4}, {h0, h0 ? ns * 4 : 0},
+                         {dout, nv * es}, {dh_final, dh_final ? ns * 4 : 0},
+                         {cu_seqlens, (size_t)(n_seq + 1) * 4}};
+    const Range outs[] = {{dq, nk * es}, {dk, nk * es}, {dv, nv * es}, {dgate_logits, nk * 4},
+                          {dbeta, (size_t)n_tok * n_heads * 4}, {dh0, dh0 ? ns * 4 : 0},
+                          {workspace, need}};
+    auto overlap = [](const Range &x, const Range &y) {
+        if (!x.p || !y.p || !x.bytes || !y.bytes) return false;
+        const uintptr_t a = (uintptr_t)x.p, b = (uintptr_t)y.p;
+        return a < b + y.bytes && b < a + x.bytes;
+    };
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const Range &r : ins)
+            if (overlap(outs[i], r))
+                return fail(KDA_ERR_INVALID_ARG, "gradients and workspace may not overlap an input");
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (overlap(outs[i], outs[j]))
+                return fail(KDA_ERR_INVALID_ARG, "gradients and workspace may not overlap");
+    }
+    kda::BwdArgs p;
+    p.q = q; p.k = k; p.v = v; p.dout = dout; p.a = gate_logits; p.beta = beta; p.h0 = h0;
+    p.dh_final = dh_final; p.cu_seqlens = cu_seqlens; p.dq = dq; p.dk = dk; p.dv = dv;
+    p.da = dgate_logits; p.dbeta = dbeta; p.dh0 = dh0; p.workspace = (float *)workspace;
+    p.n_tok = n_tok; p.n_seq = n_seq; p.n_heads = n_heads; p.d_k = d_k; p.d_v = d_v;
+    p.bf16 = dtype == KDA_BF16;
+    return launched(kda::launch_bwd(p, (cudaStream_t)stream), "backward launch");
+}
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *gate_logits, const float *beta, const float *h0,
                          const int32_t *cu_seqlens, void *out, float *h_final,

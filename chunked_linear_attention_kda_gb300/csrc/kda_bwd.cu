@@ -1,0 +1,561 @@
+// kda_bwd.cu -- backward pass of the chunked forward: the gradients of
+//   L = <dout, out> + <dh_final, h_final>
+// with respect to q, k, v, the gate logits a, beta and h0 (its vector-Jacobian product).
+// The pages give the forward only ("From Numerical Stability to Load Balancing", §2.1-2.2);
+// this is the derivative of the chunked form of it that kda_simt.cu computes. Chunk-local
+// notation (L <= 16 tokens, rows past L acting as q = k = v = 0, beta = 0, g = 0):
+//
+//   G = inclusive cumsum of g = -5 sigmoid(a), Gamma = e^G, gamma_L = e^{G_15}
+//   Q~ = Q Gamma, K~ = K Gamma, K^ = K / Gamma, K' = K gamma_L / Gamma
+//   Z = K~ K^^T, A = strict_lower(diag(beta) Z), T = (I + A)^-1, M = T diag(beta)
+//   W = M K~, U~ = M V, P = lower(Q~ K^^T), U = U~ - W S
+//   O = s (Q~ S + P U),  S_end = Diag(gamma_L) S + K'^T U          (s = d_k^-1/2)
+//
+// Three kernels, fp32 arithmetic throughout, the caller's workspace holding two
+// d_k x d_v fp32 states per (chunk, head):
+//   1. checkpoints: the forward recurrence per (sequence, head), storing the state at the
+//      start of every chunk (ck);
+//   2. reverse chain per (sequence, head), last chunk first. dS, the gradient with respect
+//      to the current chunk's end state, is stored (dck), then carried to its start:
+//        X = K' dS + s P^T dO,   dS <- Diag(gamma_L) dS + s Q~^T dO - W^T X
+//      (the transpose of the chunk's affine state map: S_end = (Diag(gamma_L) - K'^T W)
+//      S + K'^T U~ and O = s (Q~ - P W) S + s P U~); dh0 is the dS left at the first chunk;
+//   3. local gradients, all (sequence, head, chunk) independent given ck and dck:
+//        dU = s P^T dO + K' dS_end            dP = lower(s dO U^T)
+//        dQ~ = s dO S^T + dP K^                dK' = U dS_end^T
+//        dW = -dU S^T                          dgamma_L = rowsum(dS_end . S)
+//        dM = dW K~^T + dU V^T                 dV = M^T dU,  dK~ = M^T dW + dZ K^
+//        dbeta_j = sum_i dM_ij T_ij + sum_i dA_ji Z_ji,  dA = strict_lower(-T^T dM diag(beta) T^T)
+//        dZ = diag(beta) dA,                   dK^ = dP^T Q~ + dZ^T K~
+//        dQ = dQ~ Gamma,  dK = dK~ Gamma + dK^ / Gamma + dK' gamma_L / Gamma
+//        dG = dQ~ Q~ + dK~ K~ - dK^ K^ - dK' K'  (+ gamma_L dgamma_L + colsum(dK' K') at row 15)
+//        dg = reverse cumsum of dG,  da = dg (-5) sigmoid(a) (1 - sigmoid(a))
+//      S and dS_end are read 32 columns at a time, so every sum over value columns
+//      accumulates block by block.
+// The chunk of token start t in sequence n has the workspace slot (cu[n] >> 4) + c + n:
+// strictly increasing over all chunks, below (n_tok >> 4) + n_seq + 1.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int C = kChunk;
+constexpr int kThreads = 256;
+constexpr int JB = 32;  // value columns of S / dS_end per block in the local-gradient kernel
+
+__device__ __forceinline__ float ld_io(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_io(float *p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_io(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ size_t slot_of(const int32_t *cu, int n, int c) {
+    return (size_t)(cu[n] >> 4) + (size_t)c + (size_t)n;
+}
+
+// Shared-memory views of one chunk's prologue products (pitches lk = d_k + 1, lv = d_v + 1).
+struct Chunk {
+    float *Qt, *Kt, *Kh, *Kp, *Gs, *W;  // [16][lk]: Q~, K~, K^, K', G, W
+    float *V, *Ut;                      // [16][lv]: V, U~
+    float *Z, *T, *M, *P;               // [16][16]: K~ K^^T, (I + A)^-1, T diag(beta), P
+    float *gl, *bt;                     // [d_k] gamma_L, [16] beta
+};
+
+__host__ __device__ constexpr size_t chunk_floats(int dk, int dv) {
+    return (size_t)6 * C * (dk + 1) + (size_t)2 * C * (dv + 1) + 4 * C * C + dk + C;
+}
+
+__device__ Chunk carve_chunk(float *p, int dk, int dv) {
+    const int lk = dk + 1, lv = dv + 1;
+    Chunk b;
+    b.Qt = p; p += C * lk;
+    b.Kt = p; p += C * lk;
+    b.Kh = p; p += C * lk;
+    b.Kp = p; p += C * lk;
+    b.Gs = p; p += C * lk;
+    b.W = p; p += C * lk;
+    b.V = p; p += C * lv;
+    b.Ut = p; p += C * lv;
+    b.Z = p; p += C * C;
+    b.T = p; p += C * C;
+    b.M = p; p += C * C;
+    b.P = p; p += C * C;
+    b.gl = p; p += dk;
+    b.bt = p;
+    return b;
+}
+
+// The chunk prologue of tokens [c0, c0 + L) of head h: every product above that does not
+// involve the state. want_q: also Q~ and P. Ends with a barrier.
+template <typename IO>
+__device__ void prologue(const Chunk &b, const IO *q, const IO *k, const IO *v, const float *a,
+                         const float *beta, int64_t c0, int L, int H, int h, int dk, int dv,
+                         bool want_q) {
+    const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
+    __syncthreads();  // the previous user of the buffers is done
+    for (int i = tid; i < C * dk; i += kThreads) {
+        const int r = i / dk, c = i % dk;
+        float qv = 0.f, kv = 0.f, g = 0.f;
+        if (r < L) {
+            const size_t o = ((size_t)(c0 + r) * H + h) * dk + c;
+            if (want_q) qv = ld_io(q, o);
+            kv = ld_io(k, o);
+            g = kGMin / (1.f + expf(-a[o]));
+        }
+        b.Qt[r * lk + c] = qv;
+        b.Kt[r * lk + c] = kv;
+        b.Gs[r * lk + c] = g;
+    }
+    for (int i = tid; i < C * dv; i += kThreads) {
+        const int r = i / dv, c = i % dv;
+        b.V[r * lv + c] = r < L ? ld_io(v, ((size_t)(c0 + r) * H + h) * dv + c) : 0.f;
+    }
+    if (tid < C) b.bt[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+    __syncthreads();
+    for (int c = tid; c < dk; c += kThreads) {  // cumulative log-decay, scaled operands
+        float G = 0.f;
+        for (int r = 0; r < C; ++r) {
+            G += b.Gs[r * lk + c];
+            b.Gs[r * lk + c] = G;
+        }
+        const float GL = G;
+        b.gl[c] = expf(GL);
+        for (int r = 0; r < C; ++r) {
+            const float Gr = b.Gs[r * lk + c], kv = b.Kt[r * lk + c];
+            b.Qt[r * lk + c] *= expf(Gr);
+            b.Kt[r * lk + c] = kv * expf(Gr);
+            b.Kh[r * lk + c] = kv * expf(-Gr);
+            b.Kp[r * lk + c] = kv * expf(GL - Gr);
+        }
+    }
+    __syncthreads();
+    {  // Z = K~ K^^T, A = strict_lower(beta Z) (kept in M for the solve), P = lower(Q~ K^^T)
+        const int r = tid / C, j = tid % C;
+        float z = 0.f, pq = 0.f;
+        for (int c = 0; c < dk; ++c) {
+            const float kh = b.Kh[j * lk + c];
+            z = fmaf(b.Kt[r * lk + c], kh, z);
+            if (want_q) pq = fmaf(b.Qt[r * lk + c], kh, pq);
+        }
+        b.Z[r * C + j] = z;
+        b.M[r * C + j] = j < r ? b.bt[r] * z : 0.f;
+        b.P[r * C + j] = (want_q && j <= r) ? pq : 0.f;
+    }
+    __syncthreads();
+    if (tid < C) {  // T = (I + A)^-1 by forward substitution, one column per thread
+        const int j = tid;
+        float col[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            float x = r == j ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) x = fmaf(-b.M[r * C + i], col[i], x);
+            col[r] = x;
+        }
+#pragma unroll
+        for (int r = 0; r < C; ++r) b.T[r * C + j] = col[r];
+    }
+    __syncthreads();
+    {  // M = T diag(beta)
+        const int r = tid / C, j = tid % C;
+        b.M[r * C + j] = b.T[r * C + j] * b.bt[j];
+    }
+    __syncthreads();
+    for (int i = tid; i < C * dk; i += kThreads) {  // W = M K~
+        const int r = i / dk, c = i % dk;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc = fmaf(b.M[r * C + j], b.Kt[j * lk + c], acc);
+        b.W[r * lk + c] = acc;
+    }
+    for (int i = tid; i < C * dv; i += kThreads) {  // U~ = M V
+        const int r = i / dv, c = i % dv;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc = fmaf(b.M[r * C + j], b.V[j * lv + c], acc);
+        b.Ut[r * lv + c] = acc;
+    }
+    __syncthreads();
+}
+
+// ---- 1. forward recurrence with a checkpoint at every chunk start
+template <typename IO>
+__global__ void __launch_bounds__(kThreads)
+    ckpt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+                const float *__restrict__ a, const float *__restrict__ beta,
+                const float *__restrict__ h0, const int32_t *__restrict__ cu,
+                float *__restrict__ ck, int H, int dk, int dv) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    float *S = sm;
+    float *U = S + (size_t)dk * dv;  // [16][lv]
+    const Chunk b = carve_chunk(U + C * lv, dk, dv);
+    const size_t st = (size_t)dk * dv;
+    for (int i = tid; i < dk * dv; i += kThreads)
+        S[i] = h0 ? h0[((size_t)n * H + h) * st + i] : 0.f;
+    const int64_t t0 = cu[n], t1 = cu[n + 1];
+    for (int c = 0; t0 + (int64_t)c * C < t1; ++c) {
+        const int64_t c0 = t0 + (int64_t)c * C;
+        const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
+        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, false);
+        float *dst = ck + (slot_of(cu, n, c) * H + h) * st;
+        for (int i = tid; i < dk * dv; i += kThreads) dst[i] = S[i];
+        for (int i = tid; i < C * dv; i += kThreads) {  // U = U~ - W S
+            const int r = i / dv, j = i % dv;
+            float acc = b.Ut[r * lv + j];
+            for (int x = 0; x < dk; ++x) acc = fmaf(-b.W[r * lk + x], S[x * dv + j], acc);
+            U[r * lv + j] = acc;
+        }
+        __syncthreads();
+        for (int i = tid; i < dk * dv; i += kThreads) {  // S <- Diag(gamma_L) S + K'^T U
+            const int x = i / dv, j = i % dv;
+            float acc = b.gl[x] * S[i];
+#pragma unroll
+            for (int r = 0; r < C; ++r) acc = fmaf(b.Kp[r * lk + x], U[r * lv + j], acc);
+            S[i] = acc;
+        }
+    }
+}
+
+// ---- 2. reverse chain of the state gradient
+template <typename IO>
+__global__ void __launch_bounds__(kThreads)
+    chain_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+                 const float *__restrict__ a, const float *__restrict__ beta,
+                 const int32_t *__restrict__ cu, const IO *__restrict__ dout,
+                 const float *__restrict__ dh_final, float *__restrict__ dck,
+                 float *__restrict__ dh0, int H, int dk, int dv, float scale) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    float *dS = sm;
+    float *dO = dS + (size_t)dk * dv;  // [16][lv]
+    float *X = dO + C * lv;            // [16][lv]
+    const Chunk b = carve_chunk(X + C * lv, dk, dv);
+    const size_t st = (size_t)dk * dv;
+    for (int i = tid; i < dk * dv; i += kThreads)
+        dS[i] = dh_final ? dh_final[((size_t)n * H + h) * st + i] : 0.f;
+    const int64_t t0 = cu[n], t1 = cu[n + 1];
+    const int nc = (int)((t1 - t0 + C - 1) / C);
+    for (int c = nc - 1; c >= 0; --c) {
+        const int64_t c0 = t0 + (int64_t)c * C;
+        const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
+        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
+        for (int i = tid; i < C * dv; i += kThreads) {
+            const int r = i / dv, j = i % dv;
+            dO[r * lv + j] = r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
+        }
+        float *dst = dck + (slot_of(cu, n, c) * H + h) * st;
+        for (int i = tid; i < dk * dv; i += kThreads) dst[i] = dS[i];
+        __syncthreads();
+        for (int i = tid; i < C * dv; i += kThreads) {  // X = K' dS + s P^T dO
+            const int r = i / dv, j = i % dv;
+            float acc = 0.f;
+            for (int x = 0; x < dk; ++x) acc = fmaf(b.Kp[r * lk + x], dS[x * dv + j], acc);
+            float pd = 0.f;
+            for (int i2 = r; i2 < C; ++i2) pd = fmaf(b.P[i2 * C + r], dO[i2 * lv + j], pd);
+            X[r * lv + j] = fmaf(scale, pd, acc);
+        }
+        __syncthreads();
+        for (int i = tid; i < dk * dv; i += kThreads) {  // dS <- gamma_L dS + s Q~^T dO - W^T X
+            const int x = i / dv, j = i % dv;
+            float qd = 0.f, wx = 0.f;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                qd = fmaf(b.Qt[r * lk + x], dO[r * lv + j], qd);
+                wx = fmaf(b.W[r * lk + x], X[r * lv + j], wx);
+            }
+            dS[i] = b.gl[x] * dS[i] + scale * qd - wx;
+        }
+    }
+    if (dh0) {
+        __syncthreads();
+        for (int i = tid; i < dk * dv; i += kThreads) dh0[((size_t)n * H + h) * st + i] = dS[i];
+    }
+}
+
+// ---- 3. local gradients of every chunk
+__host__ __device__ constexpr size_t local_floats(int dk, int dv) {
+    return chunk_floats(dk, dv) + (size_t)C * (dv + 1)  // dO
+           + (size_t)2 * dk * (JB + 1)                  // S, dS_end column blocks
+           + (size_t)2 * C * (JB + 1)                   // U, dU column blocks
+           + (size_t)5 * C * (dk + 1)                   // dQ~, dW, dK', dK~, dK^
+           + (size_t)4 * C * C                          // dP, dM, dT / Y, dA
+           + dk + C;                                    // dgamma_L, dbeta
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads)
+    local_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+                 const float *__restrict__ a, const float *__restrict__ beta,
+                 const int32_t *__restrict__ cu, const IO *__restrict__ dout,
+                 const float *__restrict__ ck, const float *__restrict__ dck,
+                 IO *__restrict__ dq, IO *__restrict__ dk_out, IO *__restrict__ dv_out,
+                 float *__restrict__ da, float *__restrict__ dbeta, int H, int dk, int dv,
+                 float scale) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1, lj = JB + 1;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const Chunk b = carve_chunk(sm, dk, dv);
+    float *p = sm + chunk_floats(dk, dv);
+    float *dO = p; p += C * lv;
+    float *Sb = p; p += dk * lj;
+    float *dSb = p; p += dk * lj;
+    float *Ub = p; p += C * lj;
+    float *dUb = p; p += C * lj;
+    float *dQt = p; p += C * lk;
+    float *dW = p; p += C * lk;
+    float *dKp = p; p += C * lk;
+    float *dKt = p; p += C * lk;
+    float *dKh = p; p += C * lk;
+    float *dP = p; p += C * C;
+    float *dM = p; p += C * C;
+    float *dT = p; p += C * C;
+    float *dA = p; p += C * C;
+    float *dgl = p; p += dk;
+    float *db = p;
+    const size_t st = (size_t)dk * dv;
+    const int64_t t0 = cu[n], t1 = cu[n + 1];
+    const int nc = (int)((t1 - t0 + C - 1) / C);
+    for (int c = blockIdx.y; c < nc; c += gridDim.y) {
+        const int64_t c0 = t0 + (int64_t)c * C;
+        const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
+        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
+        const float *S = ck + (slot_of(cu, n, c) * H + h) * st;
+        const float *dSe = dck + (slot_of(cu, n, c) * H + h) * st;
+        for (int i = tid; i < C * dv; i += kThreads) {
+            const int r = i / dv, j = i % dv;
+            dO[r * lv + j] = r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
+        }
+        for (int i = tid; i < C * dk; i += kThreads) {
+            const int r = i / dk, x = i % dk;
+            dQt[r * lk + x] = dW[r * lk + x] = dKp[r * lk + x] = 0.f;
+        }
+        for (int i = tid; i < dk; i += kThreads) dgl[i] = 0.f;
+        float dp_acc = 0.f, dm_acc = 0.f;  // element tid of s dO U^T and dU V^T
+        for (int j0 = 0; j0 < dv; j0 += JB) {
+            const int w = dv - j0 < JB ? dv - j0 : JB;
+            __syncthreads();  // previous block's readers are done
+            for (int i = tid; i < dk * JB; i += kThreads) {
+                const int x = i / JB, jj = i % JB;
+                const bool in = jj < w;
+                Sb[x * lj + jj] = in ? S[(size_t)x * dv + j0 + jj] : 0.f;
+                dSb[x * lj + jj] = in ? dSe[(size_t)x * dv + j0 + jj] : 0.f;
+            }
+            __syncthreads();
+            for (int i = tid; i < C * JB; i += kThreads) {  // U and dU of this block
+                const int r = i / JB, jj = i % JB;
+                float u = 0.f, du = 0.f;
+                if (jj < w) {
+                    const int j = j0 + jj;
+                    u = b.Ut[r * lv + j];
+                    for (int x = 0; x < dk; ++x) {
+                        u = fmaf(-b.W[r * lk + x], Sb[x * lj + jj], u);
+                        du = fmaf(b.Kp[r * lk + x], dSb[x * lj + jj], du);
+                    }
+                    float pd = 0.f;
+                    for (int i2 = r; i2 < C; ++i2) pd = fmaf(b.P[i2 * C + r], dO[i2 * lv + j], pd);
+                    du = fmaf(scale, pd, du);
+                }
+                Ub[r * lj + jj] = u;
+                dUb[r * lj + jj] = du;
+            }
+            __syncthreads();
+            for (int i = tid; i < C * JB; i += kThreads) {  // dV = M^T dU
+                const int r = i / JB, jj = i % JB;
+                if (r < L && jj < w) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i2 = 0; i2 < C; ++i2) acc = fmaf(b.M[i2 * C + r], dUb[i2 * lj + jj], acc);
+                    st_io(dv_out, ((size_t)(c0 + r) * H + h) * dv + j0 + jj, acc);
+                }
+            }
+            for (int i = tid; i < C * dk; i += kThreads) {  // sums over this block's columns
+                const int r = i / dk, x = i % dk;
+                float qs = 0.f, ws = 0.f, kp = 0.f;
+                for (int jj = 0; jj < w; ++jj) {
+                    const float s = Sb[x * lj + jj];
+                    qs = fmaf(dO[r * lv + j0 + jj], s, qs);
+                    ws = fmaf(dUb[r * lj + jj], s, ws);
+                    kp = fmaf(Ub[r * lj + jj], dSb[x * lj + jj], kp);
+                }
+                dQt[r * lk + x] += scale * qs;
+                dW[r * lk + x] -= ws;
+                dKp[r * lk + x] += kp;
+            }
+            for (int x = tid; x < dk; x += kThreads) {
+                float acc = 0.f;
+                for (int jj = 0; jj < w; ++jj) acc = fmaf(dSb[x * lj + jj], Sb[x * lj + jj], acc);
+                dgl[x] += acc;
+            }
+            {
+                const int r = tid / C, i2 = tid % C;
+                float pa = 0.f, ma = 0.f;
+                for (int jj = 0; jj < w; ++jj) {
+                    pa = fmaf(dO[r * lv + j0 + jj], Ub[i2 * lj + jj], pa);
+                    ma = fmaf(dUb[r * lj + jj], b.V[i2 * lv + j0 + jj], ma);
+                }
+                dp_acc = fmaf(scale, pa, dp_acc);
+                dm_acc += ma;
+            }
+        }
+        {
+            const int r = tid / C, i2 = tid % C;
+            dP[r * C + i2] = i2 <= r ? dp_acc : 0.f;
+            dM[r * C + i2] = dm_acc;
+        }
+        __syncthreads();
+        for (int i = tid; i < C * dk; i += kThreads) {  // dQ~ += dP K^
+            const int r = i / dk, x = i % dk;
+            float acc = 0.f;
+            for (int i2 = 0; i2 <= r; ++i2) acc = fmaf(dP[r * C + i2], b.Kh[i2 * lk + x], acc);
+            dQt[r * lk + x] += acc;
+        }
+        {  // dM += dW K~^T
+            const int r = tid / C, j = tid % C;
+            float acc = 0.f;
+            for (int x = 0; x < dk; ++x) acc = fmaf(dW[r * lk + x], b.Kt[j * lk + x], acc);
+            dM[r * C + j] += acc;
+        }
+        __syncthreads();
+        {  // dT = dM diag(beta)
+            const int r = tid / C, j = tid % C;
+            dT[r * C + j] = dM[r * C + j] * b.bt[j];
+        }
+        if (tid < C) {  // dbeta from M = T diag(beta)
+            float acc = 0.f;
+            for (int i2 = 0; i2 < C; ++i2) acc = fmaf(dM[i2 * C + tid], b.T[i2 * C + tid], acc);
+            db[tid] = acc;
+        }
+        __syncthreads();
+        {  // Y = dT T^T (into dA)
+            const int r = tid / C, j = tid % C;
+            float acc = 0.f;
+#pragma unroll
+            for (int l = 0; l < C; ++l) acc = fmaf(dT[r * C + l], b.T[j * C + l], acc);
+            dA[r * C + j] = acc;
+        }
+        __syncthreads();
+        {  // dA = strict_lower(-T^T Y), then dZ = diag(beta) dA (into dT)
+            const int r = tid / C, j = tid % C;
+            float acc = 0.f;
+#pragma unroll
+            for (int l = 0; l < C; ++l) acc = fmaf(b.T[l * C + r], dA[l * C + j], acc);
+            const float d = j < r ? -acc : 0.f;
+            __syncthreads();
+            dA[r * C + j] = d;
+            dT[r * C + j] = b.bt[r] * d;
+        }
+        __syncthreads();
+        if (tid < C) {  // dbeta from A = strict_lower(diag(beta) Z)
+            float acc = 0.f;
+            for (int j = 0; j < tid; ++j) acc = fmaf(dA[tid * C + j], b.Z[tid * C + j], acc);
+            db[tid] += acc;
+        }
+        for (int i = tid; i < C * dk; i += kThreads) {  // dK~ and dK^
+            const int r = i / dk, x = i % dk;
+            float kt = 0.f, kh = 0.f;
+#pragma unroll
+            for (int i2 = 0; i2 < C; ++i2) {
+                kt = fmaf(b.M[i2 * C + r], dW[i2 * lk + x], kt);
+                kt = fmaf(dT[r * C + i2], b.Kh[i2 * lk + x], kt);
+                kh = fmaf(dP[i2 * C + r], b.Qt[i2 * lk + x], kh);
+                kh = fmaf(dT[i2 * C + r], b.Kt[i2 * lk + x], kh);
+            }
+            dKt[r * lk + x] = kt;
+            dKh[r * lk + x] = kh;
+        }
+        __syncthreads();
+        if (tid < L) dbeta[(size_t)(c0 + tid) * H + h] = db[tid];
+        for (int x = tid; x < dk; x += kThreads) {  // per key channel: dq, dk, the log-decay
+            float dG[C];
+            float kpsum = 0.f;
+            const float GL = b.Gs[(C - 1) * lk + x];
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float Gr = b.Gs[r * lk + x];
+                const float qt = dQt[r * lk + x], kt = dKt[r * lk + x], kh = dKh[r * lk + x],
+                            kp = dKp[r * lk + x];
+                const float kpk = kp * b.Kp[r * lk + x];
+                dG[r] = qt * b.Qt[r * lk + x] + kt * b.Kt[r * lk + x] - kh * b.Kh[r * lk + x] - kpk;
+                kpsum += kpk;
+                if (r < L) {
+                    const size_t o = ((size_t)(c0 + r) * H + h) * dk + x;
+                    st_io(dq, o, qt * expf(Gr));
+                    st_io(dk_out, o, kt * expf(Gr) + kh * expf(-Gr) + kp * expf(GL - Gr));
+                }
+            }
+            dG[C - 1] += b.gl[x] * dgl[x] + kpsum;
+            float acc = 0.f;
+#pragma unroll
+            for (int r = C - 1; r >= 0; --r) {
+                acc += dG[r];
+                if (r < L) {
+                    const size_t o = ((size_t)(c0 + r) * H + h) * dk + x;
+                    const float sg = 1.f / (1.f + expf(-a[o]));
+                    da[o] = acc * (kGMin * sg * (1.f - sg));
+                }
+            }
+        }
+    }
+}
+
+template <typename IO>
+cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
+    const int H = p.n_heads, dk = p.d_k, dv = p.d_v;
+    const float scale = 1.0f / sqrtf((float)dk);
+    const unsigned items = (unsigned)p.n_seq * (unsigned)H;
+    const size_t slots = bwd_slots(p.n_tok, p.n_seq);
+    float *ck = p.workspace;
+    float *dck = ck + slots * (size_t)H * dk * dv;
+    const IO *q = (const IO *)p.q, *k = (const IO *)p.k, *v = (const IO *)p.v;
+    const IO *dout = (const IO *)p.dout;
+
+    const size_t sm1 = ((size_t)dk * dv + (size_t)C * (dv + 1) + chunk_floats(dk, dv)) * 4;
+    const size_t sm2 = ((size_t)dk * dv + (size_t)2 * C * (dv + 1) + chunk_floats(dk, dv)) * 4;
+    const size_t sm3 = local_floats(dk, dv) * 4;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(ckpt_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
+        return e;
+    ckpt_kernel<IO><<<items, kThreads, sm1, stream>>>(q, k, v, p.a, p.beta, p.h0, p.cu_seqlens,
+                                                     ck, H, dk, dv);
+    chain_kernel<IO><<<items, kThreads, sm2, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, dout,
+                                                      p.dh_final, dck, p.dh0, H, dk, dv, scale);
+    // the chunks of a sequence spread over gridDim.y CTAs: about four per SM over the
+    // launch (one resident at a time: shared memory), so uneven sequences balance
+    const int64_t max_chunks = (p.n_tok + C - 1) / C;
+    int64_t gy = (4 * 152 + (int64_t)items - 1) / (int64_t)items;
+    if (gy > max_chunks) gy = max_chunks;
+    if (gy < 1) gy = 1;
+    if (gy > 65535) gy = 65535;
+    local_kernel<IO><<<dim3(items, (unsigned)gy), kThreads, sm3, stream>>>(
+        q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk, (IO *)p.dv,
+        p.da, p.dbeta, H, dk, dv, scale);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(3);
+    return e;
+}
+
+}  // namespace
+
+size_t bwd_slots(int64_t n_tok, int32_t n_seq) { return (size_t)(n_tok >> 4) + (size_t)n_seq + 1; }
+
+size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                           int32_t d_v) {
+    return 2 * bwd_slots(n_tok, n_seq) * (size_t)n_heads * d_k * d_v * sizeof(float);
+}
+
+cudaError_t launch_bwd(const BwdArgs &p, cudaStream_t stream) {
+    if (p.n_seq == 0) return cudaSuccess;
+    return p.bf16 ? launch_bwd_t<__nv_bfloat16>(p, stream) : launch_bwd_t<float>(p, stream);
+}
+
+}  // namespace kda

@@ -53,6 +53,24 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode_step(const DecodeArgs &args, cudaStream_t stream);
 
+// Backward pass: inputs as FwdArgs plus dout [n_tok, H, d_v] (dtype) and dh_final
+// (nullable); gradients dq, dk [n_tok, H, d_k], dv [n_tok, H, d_v] (dtype), da [n_tok,
+// H, d_k], dbeta [n_tok, H] (fp32), dh0 (nullable); workspace of bwd_workspace_bytes().
+struct BwdArgs {
+    const void *q, *k, *v, *dout;
+    const float *a, *beta, *h0, *dh_final;
+    const int32_t *cu_seqlens;
+    void *dq, *dk, *dv;
+    float *da, *dbeta, *dh0, *workspace;
+    int64_t n_tok;
+    int32_t n_seq, n_heads, d_k, d_v;
+    bool bf16;
+};
+size_t bwd_slots(int64_t n_tok, int32_t n_seq);
+size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                           int32_t d_v);
+cudaError_t launch_bwd(const BwdArgs &args, cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

@@ -183,6 +183,38 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            int32_t d_v, kda_dtype dtype, void *stream);
 
 /*
+ * kda_chunk_bwd -- backward pass of kda_chunk_fwd: the gradients of
+ *   L = <dout, out> + <dh_final, h_final>
+ * with respect to q, k, v, the gate logits, beta and h0 (the vector-Jacobian product of
+ * the operation above; the pages define the forward only -- "From Numerical Stability
+ * to Load Balancing", §2.1-2.2 -- and this is its derivative, taken through the same
+ * 16-token chunked form).
+ * Inputs: q, k, v, gate_logits, beta, h0 (NULL = zero start), cu_seqlens exactly as
+ * for kda_chunk_fwd; dout [n_tok, n_heads, d_v] in dtype; dh_final [n_seq, n_heads,
+ * d_k, d_v] float32 or NULL (zero).
+ * Outputs (caller-owned, fully overwritten): dq, dk [n_tok, n_heads, d_k] and dv
+ * [n_tok, n_heads, d_v] in dtype; dgate_logits [n_tok, n_heads, d_k] and dbeta
+ * [n_tok, n_heads] float32; dh0 [n_seq, n_heads, d_k, d_v] float32, or NULL to skip.
+ * workspace: caller-owned device memory of at least kda_chunk_bwd_workspace_bytes()
+ * bytes, 4-byte aligned, contents ignored on entry (it receives the state at the start
+ * and the state gradient at the end of every chunk). Arithmetic is fp32 throughout.
+ * Alignment as for kda_chunk_fwd for the inputs; outputs aligned to their element size.
+ * No output or the workspace may overlap an input or another output. Asynchronous on
+ * `stream`; nothing is allocated. Errors as for kda_chunk_fwd, plus
+ * KDA_ERR_INVALID_ARG for a missing gradient buffer, overlap, or a NULL or too small
+ * workspace.
+ */
+size_t kda_chunk_bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads,
+                                     int32_t d_k, int32_t d_v);
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *gate_logits, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, const void *dout, const float *dh_final,
+                         void *dq, void *dk, void *dv, float *dgate_logits, float *dbeta,
+                         float *dh0, void *workspace, size_t workspace_bytes,
+                         int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                         int32_t d_v, kda_dtype dtype, void *stream);
+
+/*
  * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
  * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
  * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs

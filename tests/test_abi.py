@@ -144,3 +144,41 @@ def test_binding_refuses_cpu_decode():
     x = torch.zeros(1, 1, 16)
     with pytest.raises(ValueError):
         kda.decode_step(x, x, x, x, torch.zeros(1, 1), torch.zeros(1, 1, 16, 16))
+
+
+def bwd(lib, *, q=FAKE, k=2 * FAKE, v=3 * FAKE, a=4 * FAKE, beta=5 * FAKE, h0=None, cu=6 * FAKE,
+        dout=7 * FAKE, dhf=None, dq=8 * FAKE, dk_=9 * FAKE, dv_=10 * FAKE, da=11 * FAKE,
+        db=12 * FAKE, dh0=None, ws=16 * FAKE, ws_bytes=None, n_tok=64, n_seq=1, H=2, dk=128,
+        dv=128, dtype=1):
+    P = ctypes.c_void_p
+    if ws_bytes is None:
+        ws_bytes = lib.kda_chunk_bwd_workspace_bytes(n_tok, n_seq, H, dk, dv) if n_tok >= 0 else 0
+    return lib.kda_chunk_bwd(P(q), P(k), P(v), P(a), P(beta), P(h0), P(cu), P(dout), P(dhf),
+                             P(dq), P(dk_), P(dv_), P(da), P(db), P(dh0), P(ws), ws_bytes,
+                             n_tok, n_seq, H, dk, dv, dtype, None)
+
+
+def test_backward_workspace_size(lib):
+    # two fp32 states per (chunk slot, head): slots = (n_tok >> 4) + n_seq + 1
+    assert lib.kda_chunk_bwd_workspace_bytes(64, 1, 2, 128, 128) == 2 * 6 * 2 * 128 * 128 * 4
+    assert lib.kda_chunk_bwd_workspace_bytes(-1, 1, 2, 128, 128) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(dout=None), 1), (dict(dq=None), 1), (dict(dk_=None), 1),
+    (dict(dv_=None), 1), (dict(da=None), 1), (dict(db=None), 1), (dict(ws=None), 1),
+    (dict(ws_bytes=1024), 1), (dict(cu=None), 1), (dict(H=0), 1), (dict(dk=129), 2),
+    (dict(dtype=9), 2), (dict(dq=8 * FAKE + 1), 1), (dict(da=11 * FAKE + 2), 1),
+    (dict(ws=16 * FAKE + 2), 1),
+    (dict(dq=FAKE), 1),                  # dq on q
+    (dict(ws=10 * FAKE + 64), 1),        # workspace inside dv
+    (dict(db=11 * FAKE), 1),             # dbeta on dgate_logits
+])
+def test_backward_host_validation(lib, kw, status):
+    st = bwd(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_backward_nothing_to_do_is_ok(lib):
+    assert bwd(lib, n_tok=0, n_seq=0) == 0
