@@ -25,7 +25,8 @@ Reported alongside the device-timed value:
 ``--op decode`` measures the recurrent decode step instead (``kda_decode_step``: B = 256
 sequences x H = 32 heads, d = 128, bf16, each step advances every sequence by one
 token; the 512 MiB fp32 state, 4x the L2, is read and rewritten in place), with the
-same timing rules and its own JSON line.
+same timing rules and its own JSON line. ``--op backward`` measures the backward pass
+(``kda_chunk_bwd``: every gradient of the forward) on the same workload as the forward.
 """
 from __future__ import annotations
 
@@ -50,6 +51,10 @@ UNIT = "tokens/s"
 KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu",
                   "chunked_linear_attention_kda_gb300/csrc/kda_simt.cu"]
 DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
+BACKWARD_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_bwd.cu"]
+BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of fp32 ALU roofline"
+# fp32 FMA peak of the SIMT backward: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
 
 
@@ -515,6 +520,135 @@ def decode_cpu_baseline(x, budget_s: float = 10.0):
                                      f"{x.q.shape[1]} heads, {threads} host threads"}
 
 
+# ------------------------------------------------------------------ backward pass
+
+def run_backward(args):
+    import torch
+    import chunked_linear_attention_kda_gb300 as kda
+    import kda_inputs as K
+
+    world, rank, local = dist_env()
+    on = init_dist(world, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = kda.load_library(build_if_missing=True)
+    x = K.make_workload(args.workload, dev, seed=K.SEED_BASE + args.workload + 7919 * rank)
+    g = torch.Generator(device="cpu").manual_seed(1234 + rank)
+    dout = torch.randn((x.n_tok, x.n_heads, x.d_v), generator=g).to(dev, x.dtype)
+    ws = torch.empty(lib.kda_chunk_bwd_workspace_bytes(x.n_tok, x.n_seq, x.n_heads, x.d_k,
+                                                       x.d_v), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, None,
+                             want_dh0=x.h0 is not None, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n0 = kda.kernel_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(on)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(on)
+    launches = kda.kernel_launch_count() - n0
+    total_ms = max_over_ranks(t0.elapsed_time(t1), on, dev)
+    value = x.n_tok * world * args.steps / (total_ms * 1e-3)
+    mean_s = statistics.mean(s_.elapsed_time(e) for s_, e in zip(starts, ends)) * 1e-3
+    flops = 2 * algorithmic_flops(x)       # a gradient product for each operand of each product
+    achieved = flops / mean_s / 1e12
+    roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_ALU_TFLOPS, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz "
+                               "(nominal unit counts and maximum SM clock)",
+                "algorithmic_flops_per_step": flops,
+                "hbm_gbs": round(algorithmic_bytes(x) * 2 / mean_s / 1e9, 1)}
+
+    # end to end through the public API: inputs and upstream gradients from pinned host
+    # memory, the backward, the gradients back to pinned host memory
+    host_in = [t.detach().to("cpu").pin_memory() for t in (x.q, x.k, x.v, x.a, x.beta, dout)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for t in (x.q, x.k, x.v, x.a, x.beta)]
+
+    def e2e_step():
+        for hb, db in zip(host_in, dev_in):
+            db.copy_(hb, non_blocking=True)
+        grads = kda.chunk_bwd(*dev_in[:5], x.h0, x.cu_seqlens, dev_in[5], None,
+                              want_dh0=False, workspace=ws)
+        for hb, gd in zip(host_out, grads[:5]):
+            hb.copy_(gd, non_blocking=True)
+
+    e_steps = max(1, min(args.steps, 3))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": round(x.n_tok * world / (e_ms * 1e-3), 1), "unit": UNIT,
+           "ms_per_step": round(e_ms, 3),
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+           "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out),
+           "steps": e_steps, "api": "chunk_bwd with pinned host inputs and gradients"}
+    line = {"metric": BACKWARD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 arithmetic, bf16 I/O" if x.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic",
+            "config": {"workload": x.name, "tokens_per_gpu": x.n_tok, "heads": x.n_heads,
+                       "d_k": x.d_k, "d_v": x.d_v, "chunk": 16,
+                       "workspace_bytes": int(ws.numel()),
+                       "l2": "inputs and workspace exceed the 129 MB L2; no flush"},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk.summary(), "kernel_digest": kernel_source_digest(BACKWARD_SOURCES)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = backward_cpu_baseline(x, dout)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def backward_cpu_baseline(x, dout, budget_s: float = 10.0):
+    """The reverse-mode oracle on the host cores on a prefix of the workload (all heads),
+    grown until it takes a few seconds; scaled to tokens/s."""
+    import torch
+    from oracle import backward as B
+    cpu = lambda t: None if t is None else t.detach().to("cpu")  # noqa: E731
+    tokens = 8
+    while True:
+        sl = slice(0, tokens)
+        t0 = time.perf_counter()
+        B.kda_backward(cpu(x.q[sl]), cpu(x.k[sl]), cpu(x.v[sl]), cpu(x.a[sl]), cpu(x.beta[sl]),
+                       cpu(x.h0[:1]) if x.h0 is not None else None, [0, tokens],
+                       cpu(dout[sl]))
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or tokens >= 4096:
+            break
+        tokens *= 2
+    return {"value": tokens / dt, "unit": UNIT, "cores": torch.get_num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"fp64 reverse-mode oracle on the first {tokens} tokens of the first "
+                      f"sequence, all {x.n_heads} heads"}
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -567,13 +701,20 @@ def main():
     ap.add_argument("--workload", type=int, default=3, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="forward", choices=["forward", "decode"],
+    ap.add_argument("--op", default="forward", choices=["forward", "decode", "backward"],
                     help="forward: the chunked forward pass (default); decode: the "
-                         "recurrent decode step")
+                         "recurrent decode step; backward: the backward pass")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.op == "decode":
+    if args.op == "backward":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the backward line has no reference arm; its cpu_baseline is "
+                              "the oracle"}), flush=True)
+        else:
+            run_backward(args)
+    elif args.op == "decode":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               "the decode line has no reference arm; its cpu_baseline is "
