@@ -22,7 +22,8 @@ import threading
 from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
-           "segmented_fwd", "decode_step", "chunk_bwd", "load_library",
+           "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
+           "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
@@ -32,7 +33,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_kernel_launch_count", "kda_read_device_flags",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
-                    "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd")
+                    "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd",
+                    "kda_chunk_bwd_static_scratch")
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +95,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_bwd.argtypes = [P] * 16 + [ctypes.c_size_t, I64, I32, I32, I32, I32,
                                                  ctypes.c_int, P]
         lib.kda_chunk_bwd.restype = ctypes.c_int
+        lib.kda_chunk_bwd_static_scratch.argtypes = [P] * 15 + [I64, I32, I32, I32, I32,
+                                                                ctypes.c_int, P]
+        lib.kda_chunk_bwd_static_scratch.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -331,6 +336,32 @@ def chunk_bwd(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final=None, *
         N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
         ctypes.c_void_p(stream)))
     return dq, dk_, dv_, da, db, dh0
+
+
+def chunk_bwd_static_scratch(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final=None,
+                             *, want_dh0=True):
+    """``chunk_bwd`` through ``kda_chunk_bwd_static_scratch``: no workspace is passed or
+    allocated for the checkpoints (the library's fixed 64 MiB scratch holds them; calls
+    must not overlap in time). Returns ``(dq, dk, dv, dgate_logits, dbeta, dh0)``."""
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("chunk_bwd_static_scratch runs on CUDA tensors only")
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens)
+    if tuple(dout.shape) != (N, H, dv) or dout.dtype != q.dtype or not dout.is_contiguous():
+        raise ValueError(f"dout must be contiguous {q.dtype} with shape {(N, H, dv)}")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    grads = [torch.empty_like(t) for t in (q, k, v, gate_logits, beta)]
+    dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 \
+        else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib, lib.kda_chunk_bwd_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+        _ptr(dout), _ptr(dh_final), *[_ptr(g) for g in grads], _ptr(dh0),
+        N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+        ctypes.c_void_p(stream)))
+    return (*grads, dh0)
 
 
 def segmented_fwd(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, segments: int,

@@ -258,6 +258,29 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     return launched(kda::launch_bwd(p, (cudaStream_t)stream), "backward launch");
 }
 
+kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void *v,
+                                        const float *gate_logits, const float *beta,
+                                        const float *h0, const int32_t *cu_seqlens,
+                                        const void *dout, const float *dh_final, void *dq,
+                                        void *dk, void *dv, float *dgate_logits, float *dbeta,
+                                        float *dh0, int64_t n_tok, int32_t n_seq,
+                                        int32_t n_heads, int32_t d_k, int32_t d_v,
+                                        kda_dtype dtype, void *stream) {
+    static_assert(KDA_STATIC_SCRATCH_BYTES == kda::kStaticScratchBytes, "one scratch size");
+    if (n_tok >= 0 && n_seq >= 0 && n_heads > 0 && d_k > 0 && d_v > 0 &&
+        kda::bwd_workspace_bytes(n_tok, n_seq, n_heads, d_k, d_v) > kda::kStaticScratchBytes)
+        return fail(KDA_ERR_UNSUPPORTED, "the problem needs more checkpoint space than the "
+                                         "static scratch holds (KDA_STATIC_SCRATCH_BYTES)");
+    void *scratch = nullptr;
+    if (n_seq > 0) {
+        const cudaError_t e = kda::static_scratch(&scratch);
+        if (e != cudaSuccess) return launched(e, "static scratch lookup");
+    }
+    return kda_chunk_bwd(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final, dq, dk, dv,
+                         dgate_logits, dbeta, dh0, scratch, kda::kStaticScratchBytes, n_tok,
+                         n_seq, n_heads, d_k, d_v, dtype, stream);
+}
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *gate_logits, const float *beta, const float *h0,
                          const int32_t *cu_seqlens, void *out, float *h_final,

@@ -71,6 +71,11 @@ size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_
                            int32_t d_v);
 cudaError_t launch_bwd(const BwdArgs &args, cudaStream_t stream);
 
+// Size of the library's fixed backward scratch array (kda_bwd_static.cu) and the lookup
+// of its device address on the current device (cached per device).
+constexpr size_t kStaticScratchBytes = (size_t)64 << 20;
+cudaError_t static_scratch(void **ptr);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

@@ -215,6 +215,30 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
                          int32_t d_v, kda_dtype dtype, void *stream);
 
 /*
+ * kda_chunk_bwd_static_scratch -- kda_chunk_bwd without a caller workspace and without
+ * any allocation: the checkpoints go to a fixed scratch array of
+ * KDA_STATIC_SCRATCH_BYTES compiled into the library (static device memory of the
+ * loaded module, one per device, its address looked up once per device). An addition
+ * of this library: the pages have no counterpart.
+ * Same arguments, layout, results and errors as kda_chunk_bwd minus the workspace;
+ * problems with kda_chunk_bwd_workspace_bytes() > KDA_STATIC_SCRATCH_BYTES return
+ * KDA_ERR_UNSUPPORTED before any device work. No part of the scratch has to start at
+ * zero: every slot a call reads, that call has written first. The scratch is shared by
+ * every call on the device: two calls that may run at the same time (different streams,
+ * or host threads whose streams are not ordered) race on it and both results are
+ * undefined -- order them on one stream.
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void *v,
+                                        const float *gate_logits, const float *beta,
+                                        const float *h0, const int32_t *cu_seqlens,
+                                        const void *dout, const float *dh_final, void *dq,
+                                        void *dk, void *dv, float *dgate_logits,
+                                        float *dbeta, float *dh0, int64_t n_tok,
+                                        int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                        int32_t d_v, kda_dtype dtype, void *stream);
+
+/*
  * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
  * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
  * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs
