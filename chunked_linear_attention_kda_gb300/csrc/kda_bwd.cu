@@ -183,100 +183,238 @@ __device__ void prologue(const Chunk &b, const IO *q, const IO *k, const IO *v, 
     __syncthreads();
 }
 
-// ---- 1. forward recurrence with a checkpoint at every chunk start
+// ---- 0. the state-independent products of every chunk, all chunks in parallel
+// Record per (chunk slot, head): K', W, Q~ [16][d_k], U~ [16][d_v], P [16][16], gamma_L
+// [d_k], fp32, unpadded.
+__host__ __device__ constexpr size_t prep_floats(int dk, int dv) {
+    return (size_t)3 * C * dk + (size_t)C * dv + C * C + dk;
+}
+__host__ __device__ constexpr size_t P_KP(int) { return 0; }
+__host__ __device__ constexpr size_t P_W(int dk) { return (size_t)C * dk; }
+__host__ __device__ constexpr size_t P_QT(int dk) { return (size_t)2 * C * dk; }
+__host__ __device__ constexpr size_t P_UT(int dk) { return (size_t)3 * C * dk; }
+__host__ __device__ constexpr size_t P_P(int dk, int dv) { return (size_t)3 * C * dk + (size_t)C * dv; }
+__host__ __device__ constexpr size_t P_GL(int dk, int dv) { return P_P(dk, dv) + C * C; }
+
 template <typename IO>
 __global__ void __launch_bounds__(kThreads)
-    ckpt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+    prep_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                 const float *__restrict__ a, const float *__restrict__ beta,
-                const float *__restrict__ h0, const int32_t *__restrict__ cu,
-                float *__restrict__ ck, int H, int dk, int dv) {
+                const int32_t *__restrict__ cu, float *__restrict__ prep, int H, int dk, int dv) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
-    float *S = sm;
-    float *U = S + (size_t)dk * dv;  // [16][lv]
-    const Chunk b = carve_chunk(U + C * lv, dk, dv);
-    const size_t st = (size_t)dk * dv;
-    for (int i = tid; i < dk * dv; i += kThreads)
-        S[i] = h0 ? h0[((size_t)n * H + h) * st + i] : 0.f;
+    const Chunk b = carve_chunk(sm, dk, dv);
+    const size_t rec = prep_floats(dk, dv);
     const int64_t t0 = cu[n], t1 = cu[n + 1];
-    for (int c = 0; t0 + (int64_t)c * C < t1; ++c) {
+    const int nc = (int)((t1 - t0 + C - 1) / C);
+    for (int c = blockIdx.y; c < nc; c += gridDim.y) {
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
-        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, false);
+        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
+        float *o = prep + (slot_of(cu, n, c) * H + h) * rec;
+        for (int i = tid; i < C * dk; i += kThreads) {
+            const int r = i / dk, x = i % dk;
+            o[P_KP(dk) + i] = b.Kp[r * lk + x];
+            o[P_W(dk) + i] = b.W[r * lk + x];
+            o[P_QT(dk) + i] = b.Qt[r * lk + x];
+        }
+        for (int i = tid; i < C * dv; i += kThreads) o[P_UT(dk) + i] = b.Ut[(i / dv) * lv + i % dv];
+        o[P_P(dk, dv) + tid] = b.P[tid];  // kThreads == C * C
+        for (int x = tid; x < dk; x += kThreads) o[P_GL(dk, dv) + x] = b.gl[x];
+    }
+}
+
+// The serial passes split the value columns: column j of S (and of dS) evolves on its own
+// given the chunk products, so CTA (sequence, head, block) carries JS columns of one
+// chain, thread t holding rows [RPT (t / JS), RPT (t / JS) + RPT) of column t mod JS in
+// registers. The chunk's products are staged into shared memory with 4-byte cp.async one
+// chunk ahead (any d_k, d_v).
+constexpr int JS = 16;                 // value columns per CTA
+constexpr int RG = kThreads / JS;      // row groups (16)
+constexpr int RPT = 128 / RG;          // rows per thread (8): d_k <= 128
+
+__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Stage one chunk's products for value columns [j0, j0 + JS): K' and W (and Q~, P when
+// chain) whole, U~ only for those columns, gamma_L.
+__device__ void stage(float *dst, const float *rec, int dk, int dv, int j0, bool chain) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < C * dk; i += kThreads) {
+        cp_async4(dst + i, rec + P_KP(dk) + i);
+        cp_async4(dst + C * dk + i, rec + P_W(dk) + i);
+        if (chain) cp_async4(dst + 2 * C * dk + i, rec + P_QT(dk) + i);
+    }
+    float *d2 = dst + 3 * C * dk;
+    for (int i = tid; i < C * JS; i += kThreads) {
+        const int r = i / JS, jj = i % JS;
+        if (!chain && j0 + jj < dv) cp_async4(d2 + i, rec + P_UT(dk) + (size_t)r * dv + j0 + jj);
+    }
+    if (chain) cp_async4(d2 + C * JS + tid, rec + P_P(dk, dv) + tid);
+    for (int x = tid; x < dk; x += kThreads) cp_async4(d2 + C * JS + C * C + x, rec + P_GL(dk, dv) + x);
+    cp_async_commit();
+}
+__host__ __device__ constexpr int stage_floats(int dk) { return 3 * C * dk + C * JS + C * C + dk; }
+
+// ---- 1. forward recurrence with a checkpoint at every chunk start (column blocks)
+__global__ void __launch_bounds__(kThreads)
+    ckpt_kernel(const float *__restrict__ h0, const int32_t *__restrict__ cu,
+                const float *__restrict__ prep, float *__restrict__ ck, int H, int dk, int dv) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x, jj = tid % JS, rg = tid / JS;
+    const int n = blockIdx.x / H, h = blockIdx.x % H, j0 = blockIdx.y * JS, j = j0 + jj;
+    const bool col = j < dv;
+    const int sf = stage_floats(dk);
+    auto buf = [&](int i) { return sm + (i & 1) * sf; };  // two staging buffers
+    float *part = sm + 2 * sf;          // [RG][16][JS] partial sums of W S
+    float *U = part + RG * C * JS;      // [16][JS]
+    const size_t st = (size_t)dk * dv, rec = prep_floats(dk, dv);
+    float s[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int x = rg * RPT + i;
+        s[i] = (h0 && col && x < dk) ? h0[((size_t)n * H + h) * st + (size_t)x * dv + j] : 0.f;
+    }
+    const int64_t t0 = cu[n], t1 = cu[n + 1];
+    const int nc = (int)((t1 - t0 + C - 1) / C);
+    if (nc > 0) stage(buf(0), prep + (slot_of(cu, n, 0) * H + h) * rec, dk, dv, j0, false);
+    for (int c = 0; c < nc; ++c) {
+        cp_async_wait_all();
+        __syncthreads();  // chunk c staged; every reader of the other buffer is done
+        if (c + 1 < nc) stage(buf(c + 1), prep + (slot_of(cu, n, c + 1) * H + h) * rec, dk, dv, j0, false);
+        const float *Kp = buf(c), *W = Kp + C * dk, *Ut = Kp + 3 * C * dk;
+        const float *gl = Ut + C * JS + C * C;
         float *dst = ck + (slot_of(cu, n, c) * H + h) * st;
-        for (int i = tid; i < dk * dv; i += kThreads) dst[i] = S[i];
-        for (int i = tid; i < C * dv; i += kThreads) {  // U = U~ - W S
-            const int r = i / dv, j = i % dv;
-            float acc = b.Ut[r * lv + j];
-            for (int x = 0; x < dk; ++x) acc = fmaf(-b.W[r * lk + x], S[x * dv + j], acc);
-            U[r * lv + j] = acc;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int x = rg * RPT + i;
+            if (col && x < dk) dst[(size_t)x * dv + j] = s[i];
+        }
+#pragma unroll
+        for (int r = 0; r < C; ++r) {  // this thread's rows of (W S)[r][j]
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                const int x = rg * RPT + i;
+                if (x < dk) acc = fmaf(W[r * dk + x], s[i], acc);
+            }
+            part[(rg * C + r) * JS + jj] = acc;
         }
         __syncthreads();
-        for (int i = tid; i < dk * dv; i += kThreads) {  // S <- Diag(gamma_L) S + K'^T U
-            const int x = i / dv, j = i % dv;
-            float acc = b.gl[x] * S[i];
+        {  // U = U~ - W S, one (r, column) per thread
+            const int r = tid / JS;
+            float acc = Ut[r * JS + jj];
 #pragma unroll
-            for (int r = 0; r < C; ++r) acc = fmaf(b.Kp[r * lk + x], U[r * lv + j], acc);
-            S[i] = acc;
+            for (int g = 0; g < RG; ++g) acc -= part[(g * C + r) * JS + jj];
+            U[r * JS + jj] = acc;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {  // S <- Diag(gamma_L) S + K'^T U
+            const int x = rg * RPT + i;
+            if (x < dk) {
+                float acc = gl[x] * s[i];
+#pragma unroll
+                for (int r = 0; r < C; ++r) acc = fmaf(Kp[r * dk + x], U[r * JS + jj], acc);
+                s[i] = acc;
+            }
         }
     }
 }
 
-// ---- 2. reverse chain of the state gradient
+// ---- 2. reverse chain of the state gradient (column blocks)
 template <typename IO>
 __global__ void __launch_bounds__(kThreads)
-    chain_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
-                 const float *__restrict__ a, const float *__restrict__ beta,
-                 const int32_t *__restrict__ cu, const IO *__restrict__ dout,
-                 const float *__restrict__ dh_final, float *__restrict__ dck,
-                 float *__restrict__ dh0, int H, int dk, int dv, float scale) {
+    chain_kernel(const int32_t *__restrict__ cu, const IO *__restrict__ dout,
+                 const float *__restrict__ dh_final, const float *__restrict__ prep,
+                 float *__restrict__ dck, float *__restrict__ dh0, int H, int dk, int dv,
+                 float scale) {
     extern __shared__ float sm[];
-    const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
-    float *dS = sm;
-    float *dO = dS + (size_t)dk * dv;  // [16][lv]
-    float *X = dO + C * lv;            // [16][lv]
-    const Chunk b = carve_chunk(X + C * lv, dk, dv);
-    const size_t st = (size_t)dk * dv;
-    for (int i = tid; i < dk * dv; i += kThreads)
-        dS[i] = dh_final ? dh_final[((size_t)n * H + h) * st + i] : 0.f;
+    const int tid = threadIdx.x, jj = tid % JS, rg = tid / JS;
+    const int n = blockIdx.x / H, h = blockIdx.x % H, j0 = blockIdx.y * JS, j = j0 + jj;
+    const bool col = j < dv;
+    const int sf = stage_floats(dk);
+    auto buf = [&](int i) { return sm + (i & 1) * sf; };  // two staging buffers
+    float *part = sm + 2 * sf;          // [RG][16][JS] partial sums of K' dS
+    float *X = part + RG * C * JS;      // [16][JS]
+    float *dO = X + C * JS;             // [16][JS]
+    const size_t st = (size_t)dk * dv, rec = prep_floats(dk, dv);
+    float ds[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int x = rg * RPT + i;
+        ds[i] = (dh_final && col && x < dk)
+                    ? dh_final[((size_t)n * H + h) * st + (size_t)x * dv + j] : 0.f;
+    }
     const int64_t t0 = cu[n], t1 = cu[n + 1];
     const int nc = (int)((t1 - t0 + C - 1) / C);
+    if (nc > 0) stage(buf(nc - 1), prep + (slot_of(cu, n, nc - 1) * H + h) * rec, dk, dv, j0, true);
     for (int c = nc - 1; c >= 0; --c) {
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
-        prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
-        for (int i = tid; i < C * dv; i += kThreads) {
-            const int r = i / dv, j = i % dv;
-            dO[r * lv + j] = r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
+        cp_async_wait_all();
+        __syncthreads();
+        if (c > 0) stage(buf(c - 1), prep + (slot_of(cu, n, c - 1) * H + h) * rec, dk, dv, j0, true);
+        const float *Kp = buf(c), *W = Kp + C * dk, *Qt = Kp + 2 * C * dk;
+        const float *P = Qt + C * dk + C * JS, *gl = P + C * C;
+        {
+            const int r = tid / JS;
+            dO[r * JS + jj] = (r < L && col) ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
         }
         float *dst = dck + (slot_of(cu, n, c) * H + h) * st;
-        for (int i = tid; i < dk * dv; i += kThreads) dst[i] = dS[i];
-        __syncthreads();
-        for (int i = tid; i < C * dv; i += kThreads) {  // X = K' dS + s P^T dO
-            const int r = i / dv, j = i % dv;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int x = rg * RPT + i;
+            if (col && x < dk) dst[(size_t)x * dv + j] = ds[i];
+        }
+#pragma unroll
+        for (int r = 0; r < C; ++r) {  // this thread's rows of (K' dS)[r][j]
             float acc = 0.f;
-            for (int x = 0; x < dk; ++x) acc = fmaf(b.Kp[r * lk + x], dS[x * dv + j], acc);
-            float pd = 0.f;
-            for (int i2 = r; i2 < C; ++i2) pd = fmaf(b.P[i2 * C + r], dO[i2 * lv + j], pd);
-            X[r * lv + j] = fmaf(scale, pd, acc);
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                const int x = rg * RPT + i;
+                if (x < dk) acc = fmaf(Kp[r * dk + x], ds[i], acc);
+            }
+            part[(rg * C + r) * JS + jj] = acc;
         }
         __syncthreads();
-        for (int i = tid; i < dk * dv; i += kThreads) {  // dS <- gamma_L dS + s Q~^T dO - W^T X
-            const int x = i / dv, j = i % dv;
-            float qd = 0.f, wx = 0.f;
+        {  // X = K' dS + s P^T dO
+            const int r = tid / JS;
+            float acc = 0.f;
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                qd = fmaf(b.Qt[r * lk + x], dO[r * lv + j], qd);
-                wx = fmaf(b.W[r * lk + x], X[r * lv + j], wx);
+            for (int g = 0; g < RG; ++g) acc += part[(g * C + r) * JS + jj];
+            float pd = 0.f;
+            for (int i2 = r; i2 < C; ++i2) pd = fmaf(P[i2 * C + r], dO[i2 * JS + jj], pd);
+            X[r * JS + jj] = fmaf(scale, pd, acc);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {  // dS <- Diag(gamma_L) dS + s Q~^T dO - W^T X
+            const int x = rg * RPT + i;
+            if (x < dk) {
+                float qd = 0.f, wx = 0.f;
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    qd = fmaf(Qt[r * dk + x], dO[r * JS + jj], qd);
+                    wx = fmaf(W[r * dk + x], X[r * JS + jj], wx);
+                }
+                ds[i] = gl[x] * ds[i] + scale * qd - wx;
             }
-            dS[i] = b.gl[x] * dS[i] + scale * qd - wx;
         }
     }
     if (dh0) {
-        __syncthreads();
-        for (int i = tid; i < dk * dv; i += kThreads) dh0[((size_t)n * H + h) * st + i] = dS[i];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int x = rg * RPT + i;
+            if (col && x < dk) dh0[((size_t)n * H + h) * st + (size_t)x * dv + j] = ds[i];
+        }
     }
 }
 
@@ -514,33 +652,38 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const size_t slots = bwd_slots(p.n_tok, p.n_seq);
     float *ck = p.workspace;
     float *dck = ck + slots * (size_t)H * dk * dv;
+    float *prep = dck + slots * (size_t)H * dk * dv;
     const IO *q = (const IO *)p.q, *k = (const IO *)p.k, *v = (const IO *)p.v;
     const IO *dout = (const IO *)p.dout;
 
-    const size_t sm1 = ((size_t)dk * dv + (size_t)C * (dv + 1) + chunk_floats(dk, dv)) * 4;
-    const size_t sm2 = ((size_t)dk * dv + (size_t)2 * C * (dv + 1) + chunk_floats(dk, dv)) * 4;
+    const size_t sm0 = chunk_floats(dk, dv) * 4;
+    const size_t sm1 = ((size_t)2 * stage_floats(dk) + (size_t)RG * C * JS + C * JS) * 4;
+    const size_t sm2 = sm1 + (size_t)C * JS * 4;
     const size_t sm3 = local_floats(dk, dv) * 4;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(ckpt_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
+    if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
         return e;
-    ckpt_kernel<IO><<<items, kThreads, sm1, stream>>>(q, k, v, p.a, p.beta, p.h0, p.cu_seqlens,
-                                                     ck, H, dk, dv);
-    chain_kernel<IO><<<items, kThreads, sm2, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, dout,
-                                                      p.dh_final, dck, p.dh0, H, dk, dv, scale);
-    // the chunks of a sequence spread over gridDim.y CTAs: about four per SM over the
-    // launch (one resident at a time: shared memory), so uneven sequences balance
+    // the chunks of a sequence spread over gridDim.y CTAs: a few per SM over the launch,
+    // so uneven sequences balance
     const int64_t max_chunks = (p.n_tok + C - 1) / C;
     int64_t gy = (4 * 152 + (int64_t)items - 1) / (int64_t)items;
     if (gy > max_chunks) gy = max_chunks;
     if (gy < 1) gy = 1;
     if (gy > 65535) gy = 65535;
-    local_kernel<IO><<<dim3(items, (unsigned)gy), kThreads, sm3, stream>>>(
+    const dim3 par(items, (unsigned)gy), cols(items, (unsigned)((dv + JS - 1) / JS));
+    prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep, H,
+                                                   dk, dv);
+    ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
+    chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep, dck,
+                                                     p.dh0, H, dk, dv, scale);
+    local_kernel<IO><<<par, kThreads, sm3, stream>>>(
         q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk, (IO *)p.dv,
         p.da, p.dbeta, H, dk, dv, scale);
     e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(3);
+    if (e == cudaSuccess) count_launches(4);
     return e;
 }
 
@@ -550,7 +693,8 @@ size_t bwd_slots(int64_t n_tok, int32_t n_seq) { return (size_t)(n_tok >> 4) + (
 
 size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
                            int32_t d_v) {
-    return 2 * bwd_slots(n_tok, n_seq) * (size_t)n_heads * d_k * d_v * sizeof(float);
+    return bwd_slots(n_tok, n_seq) * (size_t)n_heads *
+           ((size_t)2 * d_k * d_v + prep_floats(d_k, d_v)) * sizeof(float);
 }
 
 cudaError_t launch_bwd(const BwdArgs &p, cudaStream_t stream) {

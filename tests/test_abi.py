@@ -159,8 +159,10 @@ def bwd(lib, *, q=FAKE, k=2 * FAKE, v=3 * FAKE, a=4 * FAKE, beta=5 * FAKE, h0=No
 
 
 def test_backward_workspace_size(lib):
-    # two fp32 states per (chunk slot, head): slots = (n_tok >> 4) + n_seq + 1
-    assert lib.kda_chunk_bwd_workspace_bytes(64, 1, 2, 128, 128) == 2 * 6 * 2 * 128 * 128 * 4
+    # per (chunk slot, head): two fp32 states and the chunk's products (K', W, Q~ 16 x d_k,
+    # U~ 16 x d_v, P 16 x 16, gamma_L d_k); slots = (n_tok >> 4) + n_seq + 1
+    per = 2 * 128 * 128 + 3 * 16 * 128 + 16 * 128 + 16 * 16 + 128
+    assert lib.kda_chunk_bwd_workspace_bytes(64, 1, 2, 128, 128) == 6 * 2 * per * 4
     assert lib.kda_chunk_bwd_workspace_bytes(-1, 1, 2, 128, 128) == 0
 
 
