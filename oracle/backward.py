@@ -36,10 +36,24 @@ def _t(x):
     return torch.as_tensor(np.asarray(x, dtype=np.float64)).clone()
 
 
-def forward_torch(q, k, v, a, beta, h0, cu, *, g_min=-5.0, scale=None):
+def log_decay(a, gate="bounded", g_min=-5.0):
+    """Per-channel log-decay g from the gate logits: ``bounded`` is the method's
+    g = g_min sigmoid(a) ("Demystifying Trillion-Parameter MoE Models", Breakthrough 1 §2;
+    "From Numerical Stability to Load Balancing", §2.2); ``softplus`` is the unbounded
+    prior art it replaces, g = -softplus(a) = -log(1 + e^a), which reaches any negative
+    value ("Architecture Analysis of Ultra-Long Context Sparse MoE Models", §2.1-2.2;
+    "Demystifying Trillion-Parameter MoE Models", Breakthrough 1 §1)."""
+    if gate == "bounded":
+        return g_min * torch.sigmoid(a)
+    if gate == "softplus":
+        return -torch.nn.functional.softplus(a)
+    raise ValueError(f"unknown gate {gate!r}")
+
+
+def forward_torch(q, k, v, a, beta, h0, cu, *, g_min=-5.0, scale=None, gate="bounded"):
     """The recurrence on fp64 torch tensors (differentiable). Shapes as
-    ``recurrence.kda_forward``; ``cu`` is a sequence of int offsets. Returns
-    ``(out [N, H, d_v], h_final [n_seq, H, d_k, d_v])``."""
+    ``recurrence.kda_forward``; ``cu`` is a sequence of int offsets; ``gate`` selects the
+    log-decay (``log_decay``). Returns ``(out [N, H, d_v], h_final [n_seq, H, d_k, d_v])``."""
     N, H, dk = q.shape
     dv = v.shape[2]
     if scale is None:
@@ -48,7 +62,7 @@ def forward_torch(q, k, v, a, beta, h0, cu, *, g_min=-5.0, scale=None):
     for n in range(len(cu) - 1):
         S = h0[n] if h0 is not None else torch.zeros((H, dk, dv), dtype=torch.float64)
         for t in range(int(cu[n]), int(cu[n + 1])):
-            gamma = torch.exp(g_min * torch.sigmoid(a[t]))            # [H, dk]
+            gamma = torch.exp(log_decay(a[t], gate, g_min))           # [H, dk]
             S = gamma[:, :, None] * S
             pred = torch.einsum("hkv,hk->hv", S, k[t])               # S^T k
             S = S + beta[t][:, None, None] * torch.einsum("hk,hv->hkv", k[t], v[t] - pred)
@@ -88,3 +102,16 @@ def kda_backward(q, k, v, a, beta, h0, cu_seqlens, dout, dh_final=None, *, g_min
     names = ["dq", "dk", "dv", "da", "dbeta", "dh0"]
     return {nm: (g.numpy() if g is not None else np.zeros(x.shape))
             for nm, g, x in zip(names, grads, leaves)}
+
+
+def kda_forward_gate(q, k, v, a, beta, h0=None, cu_seqlens=None, *, gate="bounded",
+                     scale=None):
+    """The forward recurrence with either gate (fp64, no gradients). Returns numpy
+    ``(out [N, H, d_v], h_final [n_seq, H, d_k, d_v])``."""
+    q, k, v, a, beta = (_t(x) for x in (q, k, v, a, beta))
+    N = q.shape[0]
+    cu = [0, N] if cu_seqlens is None else [int(c) for c in (
+        cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    with torch.no_grad():
+        out, hf = forward_torch(q, k, v, a, beta, _t(h0), cu, scale=scale, gate=gate)
+    return out.numpy(), hf.numpy()

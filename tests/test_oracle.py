@@ -298,3 +298,42 @@ def test_backward_oracle_one_token_closed_form():
         Ph = np.eye(dk) - b[h] * np.outer(k[0, h], k[0, h])
         want = gam[h][:, None] * (Ph @ (s * np.outer(q[0, h], dO[0, h])))
         assert np.allclose(g["dh0"][0, h], want, atol=1e-13)
+
+
+# ---------------------------------------------------------------- unbounded contrast gate
+
+def test_softplus_gate_oracle_equals_the_c_oracle_reparameterised():
+    """g = -softplus(a) is g_min sigmoid(a') with g_min = -1000 and
+    a' = logit(softplus(a) / 1000): the C oracle, given those, runs the softplus-gated
+    recurrence, and must agree with the torch loop's softplus gate."""
+    rng = np.random.default_rng(24)
+    q, k, v, a, beta, h0, cu = P._rand(rng, [9, 20], 2, 5, 4)
+    a = a * 3.0
+    o, hf = B.kda_forward_gate(q, k, v, a, beta, h0, cu, gate="softplus")
+    sp = np.logaddexp(0.0, a)                   # softplus, stable
+    r = sp / 1000.0
+    a2 = np.log(r) - np.log1p(-r)              # logit
+    o2, hf2 = recurrence.kda_forward(q, k, v, a2, beta, h0, cu, g_min=-1000.0)
+    assert np.allclose(o, o2, rtol=0, atol=1e-11)
+    assert np.allclose(hf, hf2, rtol=0, atol=1e-11)
+
+
+def test_bounded_gate_of_the_torch_loop_is_the_c_oracle():
+    rng = np.random.default_rng(25)
+    q, k, v, a, beta, h0, cu = P._rand(rng, [13], 3, 4, 6)
+    o, hf = B.kda_forward_gate(q, k, v, a, beta, h0, cu, gate="bounded")
+    o2, hf2 = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    assert np.allclose(o, o2, rtol=0, atol=1e-13) and np.allclose(hf, hf2, rtol=0, atol=1e-13)
+
+
+def test_unbounded_chunk_overflows_where_the_bound_cannot():
+    """A log-decay of -40 per token over a 16-token chunk gives G = -640 and
+    exp(-G) = exp(640), which overflows fp32 and bf16; the bound keeps |G| <= 80 and
+    exp(80) = 5.54e34 finite in both."""
+    assert np.isinf(np.float32(np.exp(np.float64(640.0))))
+    assert float(torch.tensor(640.0).exp().to(torch.bfloat16)) == float("inf")
+    assert np.isfinite(np.float32(np.exp(80.0)))
+    assert np.isfinite(float(torch.tensor(80.0).exp().to(torch.bfloat16)))
+    a = torch.tensor(40.0, dtype=torch.float64)
+    assert abs(float(B.log_decay(a, "softplus")) + 40.0) < 1e-15  # softplus(40) = 40 + 4e-18
+    assert float(B.log_decay(torch.tensor(1e6, dtype=torch.float64), "bounded")) >= -5.0
