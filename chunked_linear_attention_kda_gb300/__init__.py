@@ -23,6 +23,7 @@ from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
+           "chunk_fwd_variant",
            "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
                     "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd",
-                    "kda_chunk_bwd_static_scratch")
+                    "kda_chunk_bwd_static_scratch", "kda_chunk_fwd_variant")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = fwd_args
             fn.restype = ctypes.c_int
+        lib.kda_chunk_fwd_variant.argtypes = fwd_args[:-1] + [I32, I32, P]
+        lib.kda_chunk_fwd_variant.restype = ctypes.c_int
         lib.kda_chunk_fwd_from_host.argtypes = [P] * 18 + [I64, I32, I32, I32, I32,
                                                           ctypes.c_int, P]
         lib.kda_chunk_fwd_from_host.restype = ctypes.c_int
@@ -177,6 +180,36 @@ def chunk_fwd_simt(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=
     """Same operation on the fp32 SIMT kernel (``kda_chunk_fwd_simt``)."""
     return _forward("kda_chunk_fwd_simt", q, k, v, gate_logits, beta, h0, cu_seqlens,
                     out=out, h_final=h_final, output_final_state=output_final_state)
+
+
+GATES = {"bounded": 0, "softplus": 1}
+DIAG_PATHS = {"dense": 0, "pairs": 1}
+
+
+def chunk_fwd_variant(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *,
+                      gate="bounded", diag="dense", out=None, h_final=None):
+    """Contrast variants through ``kda_chunk_fwd_variant`` (fp32 SIMT kernel): ``gate``
+    "bounded" (-5 sigmoid(a), the method) or "softplus" (-softplus(a), unbounded);
+    ``diag`` "dense" (the method's dense diagonal tile) or "pairs" (one exponential per
+    position pair). softplus + dense overflows on strong decay, by design."""
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("chunk_fwd_variant runs on CUDA tensors only (there is no CPU path)")
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if h_final is None:
+        h_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib, lib.kda_chunk_fwd_variant(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+        _ptr(out), _ptr(h_final), N, n_seq, H, dk, dv,
+        KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32, GATES[gate], DIAG_PATHS[diag],
+        ctypes.c_void_p(stream)))
+    return out, h_final
 
 
 def chunk_fwd_from_host(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final,

@@ -291,6 +291,26 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                dtype, stream, Path::kAuto);
 }
 
+kda_status kda_chunk_fwd_variant(const void *q, const void *k, const void *v,
+                                 const float *gate_logits, const float *beta, const float *h0,
+                                 const int32_t *cu_seqlens, void *out, float *h_final,
+                                 int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                 int32_t d_v, kda_dtype dtype, int32_t gate_kind,
+                                 int32_t diag_path, void *stream) {
+    if (gate_kind != KDA_GATE_BOUNDED && gate_kind != KDA_GATE_SOFTPLUS)
+        return fail(KDA_ERR_INVALID_ARG, "gate_kind must be KDA_GATE_BOUNDED or KDA_GATE_SOFTPLUS");
+    if (diag_path != KDA_DIAG_DENSE && diag_path != KDA_DIAG_PAIRS)
+        return fail(KDA_ERR_INVALID_ARG, "diag_path must be KDA_DIAG_DENSE or KDA_DIAG_PAIRS");
+    const kda::FwdArgs p = pack(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final, n_tok,
+                                n_seq, n_heads, d_k, d_v, dtype);
+    kda_status s = validate(p, dtype);
+    if (s != KDA_OK) return s;
+    if (p.n_seq == 0) return ok();
+    return launched(kda::launch_simt_variant(p, gate_kind, diag_path == KDA_DIAG_PAIRS,
+                                             (cudaStream_t)stream),
+                    "variant kernel launch");
+}
+
 kda_status kda_chunk_fwd_simt(const void *q, const void *k, const void *v,
                               const float *gate_logits, const float *beta,
                               const float *h0, const int32_t *cu_seqlens, void *out,

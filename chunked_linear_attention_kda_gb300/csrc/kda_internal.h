@@ -27,6 +27,9 @@ struct FwdArgs {
 
 // Each returns cudaSuccess or the launch error; all work is queued on `stream`.
 cudaError_t launch_simt(const FwdArgs &args, cudaStream_t stream);
+// The SIMT kernel's contrast variants: gate 0 = -5 sigmoid(a), 1 = -softplus(a); pair =
+// position-pair diagonal tile instead of the dense K~ K^^T, Q~ K^^T products.
+cudaError_t launch_simt_variant(const FwdArgs &args, int gate, bool pair, cudaStream_t stream);
 cudaError_t launch_tc(const FwdArgs &args, cudaStream_t stream);
 
 // True when the tensor-core kernel handles this shape and dtype.

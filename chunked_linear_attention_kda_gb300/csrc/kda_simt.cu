@@ -15,6 +15,13 @@
 //   U = U~ - W S, O = d_k^-1/2 (Q~ S + P U)
 //   S <- Diag(e^G_L) S + K'^T U       (serial state recurrence between chunks,
 //       same page §2.1)
+//
+// The same kernel also builds the contrast variants (kda_chunk_fwd_variant): the
+// unbounded gate g = -softplus(a) that the bound replaces, and the position-pair
+// diagonal tile A_rj = beta_r sum_c k_rc k_jc e^{G_rc - G_jc}, P_rj = sum_c q_rc k_jc
+// e^{G_rc - G_jc} (one exponential per pair and channel, no e^-G factor) that an
+// unbounded decay forces ("Architecture Analysis of Ultra-Long Context Sparse MoE
+// Models", §2.1-2.2; "Demystifying Trillion-Parameter MoE Models", Breakthrough 1 §1).
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -41,13 +48,22 @@ __device__ __forceinline__ void store_io<__nv_bfloat16>(__nv_bfloat16 *p, float 
     *p = __float2bfloat16_rn(x);
 }
 
-__host__ __device__ inline size_t simt_smem_floats(int dk, int dv) {
+__host__ __device__ inline size_t simt_smem_floats(int dk, int dv, bool pair = false) {
     const int lk = dk + 1, lv = dv + 1;  // odd row pitch: column walks hit distinct banks
     return (size_t)dk * dv + (size_t)6 * kChunk * lk + (size_t)3 * kChunk * lv +
-           3 * kChunk * kChunk + dk + kChunk;
+           3 * kChunk * kChunk + dk + kChunk + (pair ? (size_t)kChunk * lk : 0);
 }
 
-template <typename IO>
+enum Gate { kBounded = 0, kSoftplus = 1 };
+
+// log-decay of one channel from its gate logit
+template <int GATE>
+__device__ __forceinline__ float log_decay(float a) {
+    if (GATE == kBounded) return kGMin / (1.f + expf(-a));          // -5 sigmoid(a)
+    return -(fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))));              // -softplus(a)
+}
+
+template <typename IO, int GATE, bool PAIR>
 __global__ void __launch_bounds__(kSimtThreads)
     kda_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                     const IO *__restrict__ v, const float *__restrict__ a,
@@ -71,6 +87,7 @@ __global__ void __launch_bounds__(kSimtThreads)
     float *P = TB + kChunk * kChunk;      // [16][16]
     float *gl = P + kChunk * kChunk;      // [dk]  e^{G_L}
     float *bt = gl + dk;                  // [16]
+    float *Qr = bt + kChunk;              // [16][lk]  q, position-pair tile only
 
     const int tid = threadIdx.x;
     const int item = blockIdx.x;
@@ -92,11 +109,12 @@ __global__ void __launch_bounds__(kSimtThreads)
                 const size_t o = ((size_t)(c0 + r) * H + h) * dk + c;
                 qv = load_io(q + o);
                 kv = load_io(k + o);
-                g = kGMin / (1.f + expf(-a[o]));
+                g = log_decay<GATE>(a[o]);
             }
             Qt[r * lk + c] = qv;
             Kt[r * lk + c] = kv;
             Gs[r * lk + c] = g;
+            if (PAIR) Qr[r * lk + c] = qv;
         }
         for (int i = tid; i < kChunk * dv; i += kSimtThreads) {
             const int r = i / dv, c = i % dv;
@@ -119,7 +137,7 @@ __global__ void __launch_bounds__(kSimtThreads)
                 const float kv = Kt[r * lk + c];
                 Qt[r * lk + c] *= eg;
                 Kt[r * lk + c] = kv * eg;
-                Kh[r * lk + c] = kv * emg;
+                Kh[r * lk + c] = PAIR ? kv : kv * emg;  // the pair tile keeps k itself
                 Kp[r * lk + c] = kv * expf(GL - Gr);
             }
         }
@@ -128,10 +146,19 @@ __global__ void __launch_bounds__(kSimtThreads)
         {
             const int r = tid / kChunk, j = tid % kChunk;
             float dkk = 0.f, dqk = 0.f;
-            for (int c = 0; c < dk; ++c) {
-                const float kh = Kh[j * lk + c];
-                dkk = fmaf(Kt[r * lk + c], kh, dkk);
-                dqk = fmaf(Qt[r * lk + c], kh, dqk);
+            if (!PAIR) {
+                for (int c = 0; c < dk; ++c) {
+                    const float kh = Kh[j * lk + c];
+                    dkk = fmaf(Kt[r * lk + c], kh, dkk);
+                    dqk = fmaf(Qt[r * lk + c], kh, dqk);
+                }
+            } else if (j <= r) {  // position pairs: e^{G_r - G_j} <= 1 for j <= r
+                for (int c = 0; c < dk; ++c) {
+                    const float e = expf(Gs[r * lk + c] - Gs[j * lk + c]);
+                    const float kj = Kh[j * lk + c] * e;
+                    dkk = fmaf(Kh[r * lk + c], kj, dkk);
+                    dqk = fmaf(Qr[r * lk + c], kj, dqk);
+                }
             }
             A[r * kChunk + j] = j < r ? bt[r] * dkk : 0.f;
             P[r * kChunk + j] = j <= r ? dqk : 0.f;
@@ -202,15 +229,15 @@ __global__ void __launch_bounds__(kSimtThreads)
     }
 }
 
-template <typename IO>
+template <typename IO, int GATE = kBounded, bool PAIR = false>
 cudaError_t launch_simt_t(const FwdArgs &p, cudaStream_t stream) {
-    const size_t smem = simt_smem_floats(p.d_k, p.d_v) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(kda_simt_kernel<IO>,
+    const size_t smem = simt_smem_floats(p.d_k, p.d_v, PAIR) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(kda_simt_kernel<IO, GATE, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)p.n_seq * (unsigned)p.n_heads;
-    kda_simt_kernel<IO><<<grid, kSimtThreads, smem, stream>>>(
+    kda_simt_kernel<IO, GATE, PAIR><<<grid, kSimtThreads, smem, stream>>>(
         (const IO *)p.q, (const IO *)p.k, (const IO *)p.v, p.a, p.beta, p.h0,
         p.cu_seqlens, (IO *)p.out, p.h_final, p.n_heads, p.d_k, p.d_v);
     e = cudaGetLastError();
@@ -223,6 +250,23 @@ cudaError_t launch_simt_t(const FwdArgs &p, cudaStream_t stream) {
 cudaError_t launch_simt(const FwdArgs &p, cudaStream_t stream) {
     if (p.n_seq == 0) return cudaSuccess;
     return p.bf16 ? launch_simt_t<__nv_bfloat16>(p, stream) : launch_simt_t<float>(p, stream);
+}
+
+namespace {
+template <typename IO>
+cudaError_t launch_variant_t(const FwdArgs &p, int gate, bool pair, cudaStream_t stream) {
+    if (gate == kBounded)
+        return pair ? launch_simt_t<IO, kBounded, true>(p, stream)
+                    : launch_simt_t<IO, kBounded, false>(p, stream);
+    return pair ? launch_simt_t<IO, kSoftplus, true>(p, stream)
+                : launch_simt_t<IO, kSoftplus, false>(p, stream);
+}
+}  // namespace
+
+cudaError_t launch_simt_variant(const FwdArgs &p, int gate, bool pair, cudaStream_t stream) {
+    if (p.n_seq == 0) return cudaSuccess;
+    return p.bf16 ? launch_variant_t<__nv_bfloat16>(p, gate, pair, stream)
+                  : launch_variant_t<float>(p, gate, pair, stream);
 }
 
 }  // namespace kda

@@ -139,6 +139,34 @@ kda_status kda_chunk_fwd_simt(const void *q, const void *k, const void *v,
                               void *stream);
 
 /*
+ * kda_chunk_fwd_variant -- contrast variants of the forward pass, on the fp32 SIMT
+ * kernel, for measuring what the bounded decay buys. They are not the method: the
+ * pages replace the unbounded gate g = -softplus(a) with g = -5 sigmoid(a) precisely so
+ * that the diagonal tile can be the dense products A = strict_lower(beta K~ K^^T),
+ * P = lower(Q~ K^^T) with K^ = K e^-G, instead of a position-by-position computation
+ * ("Architecture Analysis of Ultra-Long Context Sparse MoE Models", §2.1-2.2;
+ * "Demystifying Trillion-Parameter MoE Models", Breakthrough 1 §1-2).
+ *   gate_kind  KDA_GATE_BOUNDED: g = -5 sigmoid(a) (as kda_chunk_fwd);
+ *              KDA_GATE_SOFTPLUS: g = -softplus(a) = -log(1 + e^a), unbounded below.
+ *   diag_path  KDA_DIAG_DENSE: the dense tile above (as kda_chunk_fwd);
+ *              KDA_DIAG_PAIRS: A_rj = beta_r sum_c k_rc k_jc e^{G_rc - G_jc} and
+ *              P_rj = sum_c q_rc k_jc e^{G_rc - G_jc} for j <= r, one exponential per
+ *              position pair and channel (finite for any decay).
+ * With KDA_GATE_SOFTPLUS and KDA_DIAG_DENSE a chunk whose log-decay sums below about
+ * -88 makes e^-G overflow fp32 and the outputs non-finite: the failure the bound
+ * removes, reproduced on purpose. Other arguments, layout and errors as
+ * kda_chunk_fwd, plus KDA_ERR_INVALID_ARG for an unknown gate_kind or diag_path.
+ */
+enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 };
+enum { KDA_DIAG_DENSE = 0, KDA_DIAG_PAIRS = 1 };
+kda_status kda_chunk_fwd_variant(const void *q, const void *k, const void *v,
+                                 const float *gate_logits, const float *beta,
+                                 const float *h0, const int32_t *cu_seqlens, void *out,
+                                 float *h_final, int64_t n_tok, int32_t n_seq,
+                                 int32_t n_heads, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                                 int32_t gate_kind, int32_t diag_path, void *stream);
+
+/*
  * kda_affine_combine -- combine step of the segment scan for one sequence split in
  * time (an addition of this library; the pages describe only the serial recurrence,
  * "From Numerical Stability to Load Balancing", §2.1, and this step follows from it).

@@ -184,3 +184,11 @@ def test_backward_host_validation(lib, kw, status):
 
 def test_backward_nothing_to_do_is_ok(lib):
     assert bwd(lib, n_tok=0, n_seq=0) == 0
+
+
+@pytest.mark.parametrize("gate,diag,status", [(2, 0, 1), (-1, 0, 1), (0, 2, 1), (1, 7, 1)])
+def test_variant_rejects_unknown_gate_or_path(lib, gate, diag, status):
+    P = ctypes.c_void_p
+    st = lib.kda_chunk_fwd_variant(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE),
+                                   P(FAKE), None, 64, 1, 2, 128, 128, 1, gate, diag, None)
+    assert st == status and lib.kda_last_error().decode() != ""
