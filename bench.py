@@ -51,8 +51,8 @@ METRIC = "KDA chunked-forward tokens/s (1 GB300) and % of tensor-core/HBM roofli
 DECODE_METRIC = "KDA recurrent decode tokens/s (1 GB300) and % of HBM roofline"
 DECODE_B, DECODE_H, DECODE_D = 256, 32, 128
 UNIT = "tokens/s"
-KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu",
-                  "chunked_linear_attention_kda_gb300/csrc/kda_simt.cu"]
+# the bench workload's kernel (bf16, d = 128 always takes the tensor-core kernel)
+KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu"]
 DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
 BACKWARD_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_bwd.cu"]
 BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of fp32 ALU roofline"
