@@ -30,6 +30,8 @@ same timing rules and its own JSON line. ``--op backward`` measures the backward
 ``--op contrast`` times the contrast variants (``kda_chunk_fwd_variant``) on that workload:
 the fp32 SIMT forward with the dense diagonal tile against the position-pair tile, with
 the bounded and the unbounded softplus gate, beside the tensor-core kernel.
+``--op projection`` measures the gate projection (``kda_gate_projection``, a tcgen05 GEMM:
+a = x W^T + b for the 64K workload's tokens, d_model = 4096, 32 heads x 128 outputs).
 """
 from __future__ import annotations
 
@@ -652,6 +654,84 @@ def backward_cpu_baseline(x, dout, budget_s: float = 10.0):
                       f"sequence, all {x.n_heads} heads"}
 
 
+# ------------------------------------------------------------------ gate projection
+
+PROJ_M, PROJ_D, PROJ_N = 65536, 4096, 4096
+PROJ_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_gemm.cu"]
+
+
+def run_projection(args):
+    import torch
+    import chunked_linear_attention_kda_gb300 as kda
+    dev = torch.device("cuda", 0)
+    kda.load_library(build_if_missing=True)
+    M, D, N = PROJ_M, PROJ_D, PROJ_N
+    g = torch.Generator(device="cpu").manual_seed(77)
+    x = torch.randn((M, D), generator=g).to(dev, torch.bfloat16)
+    w = (torch.randn((N, D), generator=g) * D ** -0.5).to(dev, torch.bfloat16)
+    b = torch.randn((N,), generator=g).to(dev)
+    out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.gate_projection(x, w, b, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n0 = kda.kernel_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = kda.kernel_launch_count() - n0
+    total_ms = t0.elapsed_time(t1)
+    mean_s = statistics.mean(s_.elapsed_time(e) for s_, e in zip(starts, ends)) * 1e-3
+    flops = 2 * M * N * D
+    peaks = measured_peaks()
+    achieved = flops / mean_s / 1e12
+    # context: the same product through cuBLAS (torch.mm, bf16 out), not on the product path
+    for _ in range(3):
+        torch.mm(x, w.t())
+    torch.cuda.synchronize(dev)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(10):
+        torch.mm(x, w.t())
+    c1.record(stream)
+    torch.cuda.synchronize(dev)
+    cublas_ms = c0.elapsed_time(c1) / 10
+    line = {"metric": "KDA gate projection tokens/s (a = x W^T + b, tcgen05 GEMM) and % of "
+                      "bf16 tensor roofline",
+            "value": round(M * args.steps / (total_ms * 1e-3), 1), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 products, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": f"gate-projection-M{M}-K{D}-N{N}", "tokens": M,
+                       "d_model": D, "n_out": N,
+                       "l2": "x (512 MiB) and a (1 GiB) exceed the 129 MB L2; no flush"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                         "peak_source": f"{peaks['source']} (cuBLAS bf16 burst, "
+                                        "MEASURED_PEAKS.json)",
+                         "algorithmic_flops_per_launch": flops},
+            "cublas_bf16_mm_ms_context": round(cublas_ms, 4),
+            "gpu_launches": int(launches), "clocks": clk.summary(),
+            "kernel_digest": kernel_source_digest(PROJ_SOURCES)}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ contrast variants
 
 def run_contrast(args):
@@ -751,14 +831,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="forward",
-                    choices=["forward", "decode", "backward", "contrast"],
+                    choices=["forward", "decode", "backward", "contrast", "projection"],
                     help="forward: the chunked forward pass (default); decode: the "
                          "recurrent decode step; backward: the backward pass; contrast: "
-                         "the unbounded-gate and position-pair variants")
+                         "the unbounded-gate and position-pair variants; projection: "
+                         "the gate projection GEMM")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.op == "contrast":
+    if args.op == "projection":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the projection line has no reference arm"}), flush=True)
+        else:
+            run_projection(args)
+    elif args.op == "contrast":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               "the contrast line compares variants of this library only"}),

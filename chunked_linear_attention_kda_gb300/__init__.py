@@ -23,7 +23,7 @@ from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
-           "chunk_fwd_variant",
+           "chunk_fwd_variant", "gate_projection",
            "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
@@ -35,7 +35,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
                     "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd",
-                    "kda_chunk_bwd_static_scratch", "kda_chunk_fwd_variant")
+                    "kda_chunk_bwd_static_scratch", "kda_chunk_fwd_variant",
+                    "kda_gate_projection")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         lib.kda_chunk_fwd_variant.argtypes = fwd_args[:-1] + [I32, I32, P]
         lib.kda_chunk_fwd_variant.restype = ctypes.c_int
+        lib.kda_gate_projection.argtypes = [P, P, P, P, I64, I32, I32, P]
+        lib.kda_gate_projection.restype = ctypes.c_int
         lib.kda_chunk_fwd_from_host.argtypes = [P] * 18 + [I64, I32, I32, I32, I32,
                                                           ctypes.c_int, P]
         lib.kda_chunk_fwd_from_host.restype = ctypes.c_int
@@ -180,6 +183,33 @@ def chunk_fwd_simt(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=
     """Same operation on the fp32 SIMT kernel (``kda_chunk_fwd_simt``)."""
     return _forward("kda_chunk_fwd_simt", q, k, v, gate_logits, beta, h0, cu_seqlens,
                     out=out, h_final=h_final, output_final_state=output_final_state)
+
+
+def gate_projection(x, weight, bias=None, *, out=None):
+    """Gate logits ``a = x weight^T + bias`` through ``kda_gate_projection`` (tcgen05 GEMM):
+    ``x`` [N, d_model] bf16, ``weight`` [n_out, d_model] bf16, ``bias`` [n_out] fp32 or
+    None. Returns ``a`` [N, n_out] fp32 (view it as [N, H, d_k] for ``chunk_fwd``)."""
+    import torch
+    lib = load_library()
+    if x.device.type != "cuda":
+        raise ValueError("gate_projection runs on CUDA tensors only (there is no CPU path)")
+    if x.dim() != 2 or weight.dim() != 2 or x.shape[1] != weight.shape[1]:
+        raise ValueError("x must be [N, d_model] and weight [n_out, d_model]")
+    if x.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise ValueError("x and weight must be bfloat16")
+    N, D = x.shape
+    n_out = weight.shape[0]
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (n_out,)):
+        raise ValueError(f"bias must be float32 with shape {(n_out,)}")
+    for t in (x, weight, bias):
+        if t is not None and (not t.is_contiguous() or t.device != x.device):
+            raise ValueError("all tensors must be contiguous and on one device")
+    if out is None:
+        out = torch.empty((N, n_out), dtype=torch.float32, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    _check(lib, lib.kda_gate_projection(_ptr(x), _ptr(weight), _ptr(bias), _ptr(out), N, D, n_out,
+                                        ctypes.c_void_p(stream)))
+    return out
 
 
 GATES = {"bounded": 0, "softplus": 1}

@@ -119,10 +119,12 @@ kda_status kda_selftest_bounded_wait(int64_t limit_cycles, int32_t *d_returned, 
 
 kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     if (!flags) return fail(KDA_ERR_INVALID_ARG, "flags is NULL");
-    unsigned int v = 0;
+    unsigned int v = 0, g = 0;
     cudaError_t e = kda::read_device_flags(&v, reset != 0, (cudaStream_t)stream);
     if (e != cudaSuccess) return launched(e, "reading the device status word");
-    *flags = v;
+    e = kda::read_gemm_flags(&g, reset != 0, (cudaStream_t)stream);
+    if (e != cudaSuccess) return launched(e, "reading the device status word");
+    *flags = v | g;
     return ok();
 }
 
@@ -279,6 +281,34 @@ kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void
     return kda_chunk_bwd(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final, dq, dk, dv,
                          dgate_logits, dbeta, dh0, scratch, kda::kStaticScratchBytes, n_tok,
                          n_seq, n_heads, d_k, d_v, dtype, stream);
+}
+
+kda_status kda_gate_projection(const void *x, const void *weight, const float *bias,
+                               float *gate_logits, int64_t n_tok, int32_t d_model,
+                               int32_t n_out, void *stream) {
+    if (!x || !weight || !gate_logits)
+        return n_tok == 0 ? ok() : fail(KDA_ERR_INVALID_ARG, "x, weight and gate_logits are required");
+    if (n_tok < 0 || d_model <= 0 || n_out <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_tok must be >= 0, d_model and n_out positive");
+    if (n_tok > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "n_tok above 2^31 - 1");
+    if (d_model % 8 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "d_model must be a multiple of 8 (16-byte rows for TMA)");
+    const void *a16[] = {x, weight, gate_logits};
+    for (const void *p : a16)
+        if (!aligned16(p))
+            return fail(KDA_ERR_INVALID_ARG, "x, weight and gate_logits must be 16-byte aligned");
+    if (((uintptr_t)bias & 3u) != 0) return fail(KDA_ERR_INVALID_ARG, "bias must be 4-byte aligned");
+    const uintptr_t o = (uintptr_t)gate_logits, ob = (uintptr_t)n_tok * n_out * 4;
+    struct Range { const void *p; size_t bytes; };
+    const Range ins[] = {{x, (size_t)n_tok * d_model * 2}, {weight, (size_t)n_out * d_model * 2},
+                         {bias, bias ? (size_t)n_out * 4 : 0}};
+    for (const Range &r : ins)
+        if (r.p && r.bytes && (uintptr_t)r.p < o + ob && o < (uintptr_t)r.p + r.bytes)
+            return fail(KDA_ERR_INVALID_ARG, "gate_logits may not overlap an input");
+    if (n_tok == 0) return ok();
+    return launched(kda::launch_gate_proj(x, weight, bias, gate_logits, (int)n_tok, n_out, d_model,
+                                          (cudaStream_t)stream),
+                    "gate projection launch");
 }
 
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,

@@ -79,6 +79,13 @@ cudaError_t launch_bwd(const BwdArgs &args, cudaStream_t stream);
 constexpr size_t kStaticScratchBytes = (size_t)64 << 20;
 cudaError_t static_scratch(void **ptr);
 
+// Gate projection a[M, N] = x[M, K] W[N, K]^T (+ b[N]): bf16 x and W, fp32 a and b
+// (tcgen05 GEMM, kda_gemm.cu). K % 8 == 0, x, W and a 16-byte aligned.
+cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, float *out, int M,
+                             int N, int K, cudaStream_t stream);
+// The GEMM's own status word (bit 1: a pipeline wait gave up); synchronises stream.
+cudaError_t read_gemm_flags(unsigned int *flags, bool reset, cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

@@ -167,6 +167,27 @@ kda_status kda_chunk_fwd_variant(const void *q, const void *k, const void *v,
                                  int32_t gate_kind, int32_t diag_path, void *stream);
 
 /*
+ * kda_gate_projection -- the gate logits from the layer input: a = x W^T + b, the
+ * "projection(x)" inside the bounded gate g = -5 sigmoid(projection(x)) ("Architecture
+ * Analysis of Ultra-Long Context Sparse MoE Models", §2.2; "From Numerical Stability to
+ * Load Balancing", §2.2). Its output is kda_chunk_fwd's gate_logits.
+ *   x            [n_tok, d_model] bf16, row-major
+ *   weight       [n_out, d_model] bf16, row-major (a linear layer's weight; n_out is
+ *                n_heads * d_k)
+ *   bias         [n_out] float32, or NULL for none
+ *   gate_logits  [n_tok, n_out] float32 (= [n_tok, n_heads, d_k]), fully overwritten
+ * bf16 products accumulated in fp32 on the tensor cores (tcgen05). d_model must be a
+ * multiple of 8; x, weight and gate_logits 16-byte aligned, bias 4-byte aligned;
+ * gate_logits may not overlap an input. Asynchronous on `stream`; nothing is allocated.
+ * Returns KDA_ERR_INVALID_ARG (NULL pointer, negative or zero size, misalignment,
+ * overlap), KDA_ERR_UNSUPPORTED (d_model not a multiple of 8, n_tok >= 2^31) or
+ * KDA_ERR_CUDA. A pipeline wait that gives up sets bit 1 of kda_read_device_flags.
+ */
+kda_status kda_gate_projection(const void *x, const void *weight, const float *bias,
+                               float *gate_logits, int64_t n_tok, int32_t d_model,
+                               int32_t n_out, void *stream);
+
+/*
  * kda_affine_combine -- combine step of the segment scan for one sequence split in
  * time (an addition of this library; the pages describe only the serial recurrence,
  * "From Numerical Stability to Load Balancing", §2.1, and this step follows from it).

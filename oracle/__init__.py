@@ -16,6 +16,8 @@ Contents
                 PyTorch reverse-mode differentiation of a plain fp64 token loop;
                 pinned to central finite differences of ``recurrence``.
 
+``projection``  the gate projection a = x W^T + b (one fp64 matrix product).
+
 ``recurrence.decode_step`` is the recurrence on one-token sequences (a decode step).
 """
 from .recurrence import build, kda_forward, oracle_library_path  # noqa: F401

@@ -192,3 +192,24 @@ def test_variant_rejects_unknown_gate_or_path(lib, gate, diag, status):
     st = lib.kda_chunk_fwd_variant(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE),
                                    P(FAKE), None, 64, 1, 2, 128, 128, 1, gate, diag, None)
     assert st == status and lib.kda_last_error().decode() != ""
+
+
+def proj(lib, *, x=FAKE, w=2 * FAKE, b=None, a=4 * FAKE, n_tok=64, d=128, n_out=256):
+    P = ctypes.c_void_p
+    return lib.kda_gate_projection(P(x), P(w), P(b), P(a), n_tok, d, n_out, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(w=None), 1), (dict(a=None), 1), (dict(n_tok=-1), 1),
+    (dict(d=0), 1), (dict(n_out=0), 1), (dict(d=100), 2), (dict(x=FAKE + 8), 1),
+    (dict(a=4 * FAKE + 4), 1), (dict(b=3 * FAKE + 2), 1), (dict(a=FAKE + 64), 1),
+    (dict(a=2 * FAKE), 1),
+])
+def test_gate_projection_host_validation(lib, kw, status):
+    st = proj(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_gate_projection_nothing_to_do_is_ok(lib):
+    assert proj(lib, n_tok=0) == 0

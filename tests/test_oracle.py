@@ -337,3 +337,27 @@ def test_unbounded_chunk_overflows_where_the_bound_cannot():
     a = torch.tensor(40.0, dtype=torch.float64)
     assert abs(float(B.log_decay(a, "softplus")) + 40.0) < 1e-15  # softplus(40) = 40 + 4e-18
     assert float(B.log_decay(torch.tensor(1e6, dtype=torch.float64), "bounded")) >= -5.0
+
+
+# ---------------------------------------------------------------- gate projection oracle
+
+def test_gate_projection_oracle_brute_force_and_exact_integers():
+    """The fp64 product against a triple loop, and exactly on small integers (every
+    partial sum an integer below 2^53)."""
+    from oracle import projection
+    rng = np.random.default_rng(26)
+    x = rng.standard_normal((5, 7))
+    w = rng.standard_normal((3, 7))
+    b = rng.standard_normal(3)
+    a = projection.gate_projection(x, w, b)
+    for i in range(5):
+        for j in range(3):
+            ref = b[j]
+            for kk in range(7):
+                ref += x[i, kk] * w[j, kk]
+            assert abs(a[i, j] - ref) < 1e-12
+    xi = rng.integers(-50, 50, (6, 64)).astype(np.float64)
+    wi = rng.integers(-50, 50, (4, 64)).astype(np.float64)
+    ai = projection.gate_projection(xi, wi)
+    assert np.array_equal(ai, (xi[:, None, :] * wi[None, :, :]).sum(-1))
+    assert np.array_equal(projection.gate_projection(xi, wi, None), ai)
