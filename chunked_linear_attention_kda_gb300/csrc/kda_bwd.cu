@@ -183,6 +183,78 @@ __device__ void prologue(const Chunk &b, const IO *q, const IO *k, const IO *v, 
     __syncthreads();
 }
 
+// ---- tensor-core fragments (mma.sync m16n8k16, bf16 operands, fp32 accumulation)
+__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// A fragment: rows [0, 16), columns [k0, k0 + 16) of a row-major bf16 tile
+__device__ __forceinline__ void ld_a(uint32_t base, int pitch, int k0, uint32_t (&a)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4(base + (uint32_t)(((l & 15) * pitch + k0 + (l >> 4) * 8) * 2), a);
+}
+// B fragments of the two n8 tiles [n0, n0 + 16) x k16 [k0, k0 + 16): from [n][k] storage
+// (b[0], b[1] the first tile, b[2], b[3] the second), or from [k][n] storage (transposed read)
+__device__ __forceinline__ void ld_b_nk(uint32_t base, int pitch, int n0, int k0, uint32_t (&b)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4(base + (uint32_t)(((n0 + (l & 7) + ((l >> 4) << 3)) * pitch + k0 + ((l >> 3) & 1) * 8) * 2), b);
+}
+__device__ __forceinline__ void ld_b_kn(uint32_t base, int pitch, int k0, int n0, uint32_t (&b)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4t(base + (uint32_t)(((k0 + (l & 7) + (((l >> 3) & 1) << 3)) * pitch + n0 + (l >> 4) * 8) * 2), b);
+}
+// acc (16 rows x columns [n0, n0 + 16)) += A (16 x K) B, B read from [k][n] (KN) or [n][k]
+template <bool KN>
+__device__ __forceinline__ void warp_mma(float (&acc)[2][4], uint32_t a_base, int pa, uint32_t b_base,
+                                         int pb, int n0, int K) {
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        uint32_t af[4], bf[4];
+        ld_a(a_base, pa, k0, af);
+        if (KN) ld_b_kn(b_base, pb, k0, n0, bf);
+        else ld_b_nk(b_base, pb, n0, k0, bf);
+        mma16816(acc[0], af, bf[0], bf[1]);
+        mma16816(acc[1], af, bf[2], bf[3]);
+    }
+}
+// the accumulator tile into fp32 (times alpha) or bf16 row-major storage
+__device__ __forceinline__ void store_c(float *dst, int pitch, int n0, const float (&acc)[2][4],
+                                        float alpha) {
+    const int l = threadIdx.x & 31, g4 = l >> 2, l4 = l & 3;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int col = n0 + 8 * t + 2 * l4;
+        dst[g4 * pitch + col] = alpha * acc[t][0];
+        dst[g4 * pitch + col + 1] = alpha * acc[t][1];
+        dst[(g4 + 8) * pitch + col] = alpha * acc[t][2];
+        dst[(g4 + 8) * pitch + col + 1] = alpha * acc[t][3];
+    }
+}
+__device__ __forceinline__ void store_c16(__nv_bfloat16 *dst, int pitch, int n0,
+                                          const float (&acc)[2][4]) {
+    const int l = threadIdx.x & 31, g4 = l >> 2, l4 = l & 3;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int col = n0 + 8 * t + 2 * l4;
+        *reinterpret_cast<__nv_bfloat162 *>(dst + g4 * pitch + col) = __floats2bfloat162_rn(acc[t][0], acc[t][1]);
+        *reinterpret_cast<__nv_bfloat162 *>(dst + (g4 + 8) * pitch + col) =
+            __floats2bfloat162_rn(acc[t][2], acc[t][3]);
+    }
+}
+constexpr int PB = 136;  // bf16 pitch of 128-wide operand tiles: 272-byte rows, conflict-free
+constexpr int PS = 24;   // bf16 pitch of 16-wide operand tiles
+
 // ---- 0. the state-independent products of every chunk, all chunks in parallel
 // Record per (chunk slot, head): K', W, Q~ [16][d_k], U~ [16][d_v], P [16][16], gamma_L
 // [d_k], fp32, unpadded.
@@ -243,19 +315,45 @@ __device__ __forceinline__ void cp_async4(float *dst, const float *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
 // Stage one chunk's products for value columns [j0, j0 + JS): K' and W (and Q~, P when
-// chain) whole, U~ only for those columns, gamma_L.
+// chain) whole, U~ only for those columns, gamma_L. 16-byte copies when every piece is a
+// multiple of 4 floats (d_k, d_v multiples of 4), 4-byte copies otherwise.
 __device__ void stage(float *dst, const float *rec, int dk, int dv, int j0, bool chain) {
     const int tid = threadIdx.x;
-    for (int i = tid; i < C * dk; i += kThreads) {
-        cp_async4(dst + i, rec + P_KP(dk) + i);
-        cp_async4(dst + C * dk + i, rec + P_W(dk) + i);
-        if (chain) cp_async4(dst + 2 * C * dk + i, rec + P_QT(dk) + i);
+    const bool v4 = (dk & 3) == 0 && (dv & 3) == 0;
+    if (v4) {
+        for (int i = tid; i < C * dk / 4; i += kThreads) {
+            cp_async16(dst + 4 * i, rec + P_KP(dk) + 4 * i);
+            cp_async16(dst + C * dk + 4 * i, rec + P_W(dk) + 4 * i);
+            if (chain) cp_async16(dst + 2 * C * dk + 4 * i, rec + P_QT(dk) + 4 * i);
+        }
+    } else {
+        for (int i = tid; i < C * dk; i += kThreads) {
+            cp_async4(dst + i, rec + P_KP(dk) + i);
+            cp_async4(dst + C * dk + i, rec + P_W(dk) + i);
+            if (chain) cp_async4(dst + 2 * C * dk + i, rec + P_QT(dk) + i);
+        }
     }
     float *d2 = dst + 3 * C * dk;
-    for (int i = tid; i < C * JS; i += kThreads) {
-        const int r = i / JS, jj = i % JS;
-        if (!chain && j0 + jj < dv) cp_async4(d2 + i, rec + P_UT(dk) + (size_t)r * dv + j0 + jj);
+    if (!chain) {
+        if (v4 && j0 + JS <= dv) {
+            for (int i = tid; i < C * JS / 4; i += kThreads) {
+                const int r = i / (JS / 4), q4 = i % (JS / 4);
+                cp_async16(d2 + 4 * i, rec + P_UT(dk) + (size_t)r * dv + j0 + 4 * q4);
+            }
+        } else {
+            for (int i = tid; i < C * JS; i += kThreads) {
+                const int r = i / JS, jj = i % JS;
+                if (j0 + jj < dv) cp_async4(d2 + i, rec + P_UT(dk) + (size_t)r * dv + j0 + jj);
+            }
+        }
     }
     if (chain) cp_async4(d2 + C * JS + tid, rec + P_P(dk, dv) + tid);
     for (int x = tid; x < dk; x += kThreads) cp_async4(d2 + C * JS + C * C + x, rec + P_GL(dk, dv) + x);
@@ -297,6 +395,18 @@ __global__ void __launch_bounds__(kThreads)
             const int x = rg * RPT + i;
             if (col && x < dk) dst[(size_t)x * dv + j] = s[i];
         }
+        if (dk == RG * RPT) {  // full height: this thread's 8 rows as two float4 per product row
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float4 w0 = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT);
+                const float4 w1 = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT + 4);
+                float acc = w0.x * s[0];
+                acc = fmaf(w0.y, s[1], acc); acc = fmaf(w0.z, s[2], acc); acc = fmaf(w0.w, s[3], acc);
+                acc = fmaf(w1.x, s[4], acc); acc = fmaf(w1.y, s[5], acc); acc = fmaf(w1.z, s[6], acc);
+                acc = fmaf(w1.w, s[7], acc);
+                part[(rg * C + r) * JS + jj] = acc;
+            }
+        } else {
 #pragma unroll
         for (int r = 0; r < C; ++r) {  // this thread's rows of (W S)[r][j]
             float acc = 0.f;
@@ -307,6 +417,7 @@ __global__ void __launch_bounds__(kThreads)
             }
             part[(rg * C + r) * JS + jj] = acc;
         }
+        }
         __syncthreads();
         {  // U = U~ - W S, one (r, column) per thread
             const int r = tid / JS;
@@ -316,6 +427,23 @@ __global__ void __launch_bounds__(kThreads)
             U[r * JS + jj] = acc;
         }
         __syncthreads();
+        if (dk == RG * RPT) {  // S <- Diag(gamma_L) S + K'^T U, float4 rows
+            float u[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) u[r] = U[r * JS + jj];
+#pragma unroll
+            for (int i = 0; i < RPT; i += 4) {
+                const float4 g = *reinterpret_cast<const float4 *>(gl + rg * RPT + i);
+                float a0 = g.x * s[i], a1 = g.y * s[i + 1], a2 = g.z * s[i + 2], a3 = g.w * s[i + 3];
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    const float4 kp = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT + i);
+                    a0 = fmaf(kp.x, u[r], a0); a1 = fmaf(kp.y, u[r], a1);
+                    a2 = fmaf(kp.z, u[r], a2); a3 = fmaf(kp.w, u[r], a3);
+                }
+                s[i] = a0; s[i + 1] = a1; s[i + 2] = a2; s[i + 3] = a3;
+            }
+        } else {
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {  // S <- Diag(gamma_L) S + K'^T U
             const int x = rg * RPT + i;
@@ -325,6 +453,7 @@ __global__ void __launch_bounds__(kThreads)
                 for (int r = 0; r < C; ++r) acc = fmaf(Kp[r * dk + x], U[r * JS + jj], acc);
                 s[i] = acc;
             }
+        }
         }
     }
 }
@@ -374,6 +503,18 @@ __global__ void __launch_bounds__(kThreads)
             const int x = rg * RPT + i;
             if (col && x < dk) dst[(size_t)x * dv + j] = ds[i];
         }
+        if (dk == RG * RPT) {  // full height: two float4 per product row
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float4 k0 = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT);
+                const float4 k1 = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT + 4);
+                float acc = k0.x * ds[0];
+                acc = fmaf(k0.y, ds[1], acc); acc = fmaf(k0.z, ds[2], acc); acc = fmaf(k0.w, ds[3], acc);
+                acc = fmaf(k1.x, ds[4], acc); acc = fmaf(k1.y, ds[5], acc); acc = fmaf(k1.z, ds[6], acc);
+                acc = fmaf(k1.w, ds[7], acc);
+                part[(rg * C + r) * JS + jj] = acc;
+            }
+        } else {
 #pragma unroll
         for (int r = 0; r < C; ++r) {  // this thread's rows of (K' dS)[r][j]
             float acc = 0.f;
@@ -383,6 +524,7 @@ __global__ void __launch_bounds__(kThreads)
                 if (x < dk) acc = fmaf(Kp[r * dk + x], ds[i], acc);
             }
             part[(rg * C + r) * JS + jj] = acc;
+        }
         }
         __syncthreads();
         {  // X = K' dS + s P^T dO
@@ -395,6 +537,29 @@ __global__ void __launch_bounds__(kThreads)
             X[r * JS + jj] = fmaf(scale, pd, acc);
         }
         __syncthreads();
+        if (dk == RG * RPT) {  // dS <- Diag(gamma_L) dS + s Q~^T dO - W^T X, float4 rows
+            float od[C], xr[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                od[r] = scale * dO[r * JS + jj];
+                xr[r] = X[r * JS + jj];
+            }
+#pragma unroll
+            for (int i = 0; i < RPT; i += 4) {
+                const float4 g = *reinterpret_cast<const float4 *>(gl + rg * RPT + i);
+                float a0 = g.x * ds[i], a1 = g.y * ds[i + 1], a2 = g.z * ds[i + 2], a3 = g.w * ds[i + 3];
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    const float4 qt = *reinterpret_cast<const float4 *>(Qt + r * dk + rg * RPT + i);
+                    const float4 w = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT + i);
+                    a0 = fmaf(qt.x, od[r], fmaf(-w.x, xr[r], a0));
+                    a1 = fmaf(qt.y, od[r], fmaf(-w.y, xr[r], a1));
+                    a2 = fmaf(qt.z, od[r], fmaf(-w.z, xr[r], a2));
+                    a3 = fmaf(qt.w, od[r], fmaf(-w.w, xr[r], a3));
+                }
+                ds[i] = a0; ds[i + 1] = a1; ds[i + 2] = a2; ds[i + 3] = a3;
+            }
+        } else {
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {  // dS <- Diag(gamma_L) dS + s Q~^T dO - W^T X
             const int x = rg * RPT + i;
@@ -408,6 +573,7 @@ __global__ void __launch_bounds__(kThreads)
                 ds[i] = gl[x] * ds[i] + scale * qd - wx;
             }
         }
+        }
     }
     if (dh0) {
 #pragma unroll
@@ -419,16 +585,144 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---- 3. local gradients of every chunk
-__host__ __device__ constexpr size_t local_floats(int dk, int dv) {
-    return chunk_floats(dk, dv) + (size_t)C * (dv + 1)  // dO
-           + (size_t)2 * dk * (JB + 1)                  // S, dS_end column blocks
-           + (size_t)2 * C * (JB + 1)                   // U, dU column blocks
+// Tensor-core middle of the local-gradient kernel (d_k = d_v = 128, 8 warps; warp w owns
+// value / key columns [16 w, 16 w + 16) of every 128-wide product). Produces what the
+// SIMT middle does: dQ~ = s dO S^T, dW = -dU S^T, dK' = U dS_end^T, dgamma_L =
+// rowsum(dS_end . S), dP = lower(s dO U^T), dM = dU V^T, and dV = M^T dU written out.
+// S and dS_end are staged as bf16 through one buffer: S (U, dQ~), then dS_end (dU, dK',
+// with dgamma_L from the fp32 values), then S again (dW).
+template <typename IO>
+__device__ void mma_middle(const Chunk &b, const float *S, const float *dSe, const IO *dout,
+                           IO *dv_out, int64_t c0, int L, int H, int h, float scale,
+                           __nv_bfloat16 *SB16, __nv_bfloat16 *W16, __nv_bfloat16 *Kp16,
+                           __nv_bfloat16 *dO16, __nv_bfloat16 *U16, __nv_bfloat16 *dU16,
+                           __nv_bfloat16 *V16, __nv_bfloat16 *sPT16, __nv_bfloat16 *MT16, float *dQt,
+                           float *dW, float *dKp, float *dgl, float *dP, float *dM) {
+    constexpr int D = 128, lk = D + 1, lv = D + 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n0 = 16 * warp;
+    auto u32 = [](const void *ptr) { return static_cast<uint32_t>(__cvta_generic_to_shared(ptr)); };
+    // state tile: 4096 float4 of S (or dS_end), row x of 32 float4 per warp and step
+    auto stage_state = [&](const float *src, bool with_dgl) {
+        for (int it = 0; it < D * D / 4 / kThreads; ++it) {
+            const int i = tid + it * kThreads, x = i >> 5, c4 = (i & 31) * 4;
+            const float4 v = *reinterpret_cast<const float4 *>(src + (size_t)x * D + c4);
+            __nv_bfloat162 *d2 = reinterpret_cast<__nv_bfloat162 *>(SB16 + x * PB + c4);
+            d2[0] = __floats2bfloat162_rn(v.x, v.y);
+            d2[1] = __floats2bfloat162_rn(v.z, v.w);
+            if (with_dgl) {  // rowsum(dS_end . S) in fp32: one row per warp and step
+                const float4 s4 = *reinterpret_cast<const float4 *>(S + (size_t)x * D + c4);
+                float acc = v.x * s4.x + v.y * s4.y + v.z * s4.z + v.w * s4.w;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (lane == 0) dgl[x] = acc;
+            }
+        }
+    };
+    // bf16 operand copies of the chunk products and of dO
+    for (int i = tid; i < C * D; i += kThreads) {
+        const int r = i / D, x = i % D;
+        W16[r * PB + x] = __float2bfloat16_rn(b.W[r * lk + x]);
+        Kp16[r * PB + x] = __float2bfloat16_rn(b.Kp[r * lk + x]);
+        V16[r * PB + x] = __float2bfloat16_rn(b.V[r * lv + x]);
+        dO16[r * PB + x] = __float2bfloat16_rn(
+            r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * D + x) : 0.f);
+    }
+    {
+        const int r = tid / C, i2 = tid % C;
+        sPT16[r * PS + i2] = __float2bfloat16_rn(scale * b.P[i2 * C + r]);
+        MT16[r * PS + i2] = __float2bfloat16_rn(b.M[i2 * C + r]);
+    }
+    stage_state(S, false);
+    __syncthreads();
+    {  // U = U~ - W S (bf16 copy); dQ~ = s dO S^T
+        float acc[2][4] = {};
+        warp_mma<true>(acc, u32(W16), PB, u32(SB16), PB, n0, D);
+        const int g4 = lane >> 2, l4 = lane & 3;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int col = n0 + 8 * t + 2 * l4;
+            acc[t][0] = b.Ut[g4 * lv + col] - acc[t][0];
+            acc[t][1] = b.Ut[g4 * lv + col + 1] - acc[t][1];
+            acc[t][2] = b.Ut[(g4 + 8) * lv + col] - acc[t][2];
+            acc[t][3] = b.Ut[(g4 + 8) * lv + col + 1] - acc[t][3];
+        }
+        store_c16(U16, PB, n0, acc);
+        float dq[2][4] = {};
+        warp_mma<false>(dq, u32(dO16), PB, u32(SB16), PB, n0, D);
+        store_c(dQt, lk, n0, dq, scale);
+    }
+    __syncthreads();  // every reader of S is done; U complete
+    stage_state(dSe, true);
+    __syncthreads();
+    {  // dU = K' dS_end + s P^T dO (bf16 copy); dK' = U dS_end^T; dV = M^T dU (this warp's columns)
+        float acc[2][4] = {};
+        warp_mma<true>(acc, u32(Kp16), PB, u32(SB16), PB, n0, D);
+        warp_mma<true>(acc, u32(sPT16), PS, u32(dO16), PB, n0, C);
+        store_c16(dU16, PB, n0, acc);
+        float kp[2][4] = {};
+        warp_mma<false>(kp, u32(U16), PB, u32(SB16), PB, n0, D);
+        store_c(dKp, lk, n0, kp, 1.f);
+        __syncwarp();  // this warp's dU columns are in shared memory
+        float dv[2][4] = {};
+        warp_mma<true>(dv, u32(MT16), PS, u32(dU16), PB, n0, C);
+        const int g4 = lane >> 2, l4 = lane & 3;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int col = n0 + 8 * t + 2 * l4;
+            if (g4 < L) {
+                st_io(dv_out, ((size_t)(c0 + g4) * H + h) * D + col, dv[t][0]);
+                st_io(dv_out, ((size_t)(c0 + g4) * H + h) * D + col + 1, dv[t][1]);
+            }
+            if (g4 + 8 < L) {
+                st_io(dv_out, ((size_t)(c0 + g4 + 8) * H + h) * D + col, dv[t][2]);
+                st_io(dv_out, ((size_t)(c0 + g4 + 8) * H + h) * D + col + 1, dv[t][3]);
+            }
+        }
+    }
+    __syncthreads();  // every reader of dS_end is done; dU complete
+    stage_state(S, false);
+    if (warp == 0) {  // dP = lower(s dO U^T)
+        float acc[2][4] = {};
+        warp_mma<false>(acc, u32(dO16), PB, u32(U16), PB, 0, D);
+        const int g4 = lane >> 2, l4 = lane & 3;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int col = 8 * t + 2 * l4;
+            dP[g4 * C + col] = col <= g4 ? scale * acc[t][0] : 0.f;
+            dP[g4 * C + col + 1] = col + 1 <= g4 ? scale * acc[t][1] : 0.f;
+            dP[(g4 + 8) * C + col] = col <= g4 + 8 ? scale * acc[t][2] : 0.f;
+            dP[(g4 + 8) * C + col + 1] = col + 1 <= g4 + 8 ? scale * acc[t][3] : 0.f;
+        }
+    } else if (warp == 1) {  // dM = dU V^T
+        float acc[2][4] = {};
+        warp_mma<false>(acc, u32(dU16), PB, u32(V16), PB, 0, D);
+        store_c(dM, C, 0, acc, 1.f);
+    }
+    __syncthreads();
+    {  // dW = -dU S^T
+        float acc[2][4] = {};
+        warp_mma<false>(acc, u32(dU16), PB, u32(SB16), PB, n0, D);
+        store_c(dW, lk, n0, acc, -1.f);
+    }
+}
+
+__host__ __device__ constexpr size_t local_mid_floats(int dk, int dv, bool mma) {
+    return mma ? (size_t)(128 * PB + 6 * C * PB + 2 * C * PS) / 2  // bf16 operand tiles
+               : (size_t)C * (dv + 1)                              // dO
+                     + (size_t)2 * dk * (JB + 1)                   // S, dS_end column blocks
+                     + (size_t)2 * C * (JB + 1);                   // U, dU column blocks
+}
+__host__ __device__ constexpr size_t local_floats(int dk, int dv, bool mma) {
+    return chunk_floats(dk, dv) + local_mid_floats(dk, dv, mma)
            + (size_t)5 * C * (dk + 1)                   // dQ~, dW, dK', dK~, dK^
            + (size_t)4 * C * C                          // dP, dM, dT / Y, dA
            + dk + C;                                    // dgamma_L, dbeta
 }
 
-template <typename IO>
+// MMA: the sums over value columns on the tensor cores (bf16 operands, fp32 accumulation;
+// bf16 I/O with d_k = d_v = 128), reading S and dS_end whole; otherwise fp32 FMA loops
+// over 32-column blocks.
+template <typename IO, bool MMA>
 __global__ void __launch_bounds__(kThreads)
     local_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                  const float *__restrict__ a, const float *__restrict__ beta,
@@ -442,11 +736,19 @@ __global__ void __launch_bounds__(kThreads)
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const Chunk b = carve_chunk(sm, dk, dv);
     float *p = sm + chunk_floats(dk, dv);
-    float *dO = p; p += C * lv;
-    float *Sb = p; p += dk * lj;
-    float *dSb = p; p += dk * lj;
-    float *Ub = p; p += C * lj;
-    float *dUb = p; p += C * lj;
+    float *mid = p;
+    p += local_mid_floats(dk, dv, MMA);
+    // SIMT middle
+    float *dO = mid;
+    float *Sb = dO + C * lv;
+    float *dSb = Sb + dk * lj;
+    float *Ub = dSb + dk * lj;
+    float *dUb = Ub + C * lj;
+    // tensor-core middle: S or dS_end [128][PB], W, K', dO, U, dU, V [16][PB], s P^T, M^T [16][PS]
+    __nv_bfloat16 *SB16 = reinterpret_cast<__nv_bfloat16 *>(mid);
+    __nv_bfloat16 *W16 = SB16 + 128 * PB, *Kp16 = W16 + C * PB, *dO16 = Kp16 + C * PB;
+    __nv_bfloat16 *U16 = dO16 + C * PB, *dU16 = U16 + C * PB, *V16 = dU16 + C * PB;
+    __nv_bfloat16 *sPT16 = V16 + C * PB, *MT16 = sPT16 + C * PS;
     float *dQt = p; p += C * lk;
     float *dW = p; p += C * lk;
     float *dKp = p; p += C * lk;
@@ -467,6 +769,10 @@ __global__ void __launch_bounds__(kThreads)
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
         const float *S = ck + (slot_of(cu, n, c) * H + h) * st;
         const float *dSe = dck + (slot_of(cu, n, c) * H + h) * st;
+        if constexpr (MMA) {
+            mma_middle(b, S, dSe, dout, dv_out, c0, L, H, h, scale, SB16, W16, Kp16, dO16, U16, dU16,
+                       V16, sPT16, MT16, dQt, dW, dKp, dgl, dP, dM);
+        } else {
         for (int i = tid; i < C * dv; i += kThreads) {
             const int r = i / dv, j = i % dv;
             dO[r * lv + j] = r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
@@ -547,6 +853,7 @@ __global__ void __launch_bounds__(kThreads)
             const int r = tid / C, i2 = tid % C;
             dP[r * C + i2] = i2 <= r ? dp_acc : 0.f;
             dM[r * C + i2] = dm_acc;
+        }
         }
         __syncthreads();
         for (int i = tid; i < C * dk; i += kThreads) {  // dQ~ += dP K^
@@ -659,12 +966,17 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const size_t sm0 = chunk_floats(dk, dv) * 4;
     const size_t sm1 = ((size_t)2 * stage_floats(dk) + (size_t)RG * C * JS + C * JS) * 4;
     const size_t sm2 = sm1 + (size_t)C * JS * 4;
-    const size_t sm3 = local_floats(dk, dv) * 4;
+    // the local gradients on the tensor cores for bf16 I/O at d_k = d_v = 128 (bf16 operand
+    // rounding is within that I/O's precision); fp32 FMA loops otherwise
+    constexpr bool kBf16 = sizeof(IO) == 2;
+    const bool use_mma = kBf16 && dk == 128 && dv == 128;
+    const size_t sm3 = local_floats(dk, dv, use_mma) * 4;
+    auto local = use_mma ? local_kernel<IO, kBf16> : local_kernel<IO, false>;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
+        (e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
         return e;
     // the chunks of a sequence spread over gridDim.y CTAs: a few per SM over the launch,
     // so uneven sequences balance
@@ -679,7 +991,7 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
     chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep, dck,
                                                      p.dh0, H, dk, dv, scale);
-    local_kernel<IO><<<par, kThreads, sm3, stream>>>(
+    local<<<par, kThreads, sm3, stream>>>(
         q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk, (IO *)p.dv,
         p.da, p.dbeta, H, dk, dv, scale);
     e = cudaGetLastError();
