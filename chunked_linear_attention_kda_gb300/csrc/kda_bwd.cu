@@ -183,6 +183,11 @@ __device__ void prologue(const Chunk &b, const IO *q, const IO *k, const IO *v, 
     __syncthreads();
 }
 
+// bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- tensor-core fragments (mma.sync m16n8k16, bf16 operands, fp32 accumulation)
 __device__ __forceinline__ void ldsm4(uint32_t a, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -766,6 +771,11 @@ __global__ void __launch_bounds__(kThreads)
     for (int c = blockIdx.y; c < nc; c += gridDim.y) {
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
+        if (MMA && tid < 2 && c + (int)gridDim.y < nc) {
+            // the next chunk's two states into L2 while this one is processed
+            const size_t nx = (slot_of(cu, n, c + gridDim.y) * H + h) * st;
+            prefetch_l2((tid == 0 ? ck : dck) + nx, (uint32_t)(st * sizeof(float)));
+        }
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
         const float *S = ck + (slot_of(cu, n, c) * H + h) * st;
         const float *dSe = dck + (slot_of(cu, n, c) * H + h) * st;
