@@ -400,15 +400,16 @@ __global__ void __launch_bounds__(kThreads)
             const int x = rg * RPT + i;
             if (col && x < dk) dst[(size_t)x * dv + j] = s[i];
         }
-        if (dk == RG * RPT) {  // full height: this thread's 8 rows as two float4 per product row
+        if (dk == RG * RPT) {  // full height: this thread's rows as float4 per product row
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float4 w0 = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT);
-                const float4 w1 = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT + 4);
-                float acc = w0.x * s[0];
-                acc = fmaf(w0.y, s[1], acc); acc = fmaf(w0.z, s[2], acc); acc = fmaf(w0.w, s[3], acc);
-                acc = fmaf(w1.x, s[4], acc); acc = fmaf(w1.y, s[5], acc); acc = fmaf(w1.z, s[6], acc);
-                acc = fmaf(w1.w, s[7], acc);
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < RPT; i += 4) {
+                    const float4 w = *reinterpret_cast<const float4 *>(W + r * dk + rg * RPT + i);
+                    acc = fmaf(w.x, s[i], acc); acc = fmaf(w.y, s[i + 1], acc);
+                    acc = fmaf(w.z, s[i + 2], acc); acc = fmaf(w.w, s[i + 3], acc);
+                }
                 part[(rg * C + r) * JS + jj] = acc;
             }
         } else {
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kThreads)
         }
         }
         __syncthreads();
-        {  // U = U~ - W S, one (r, column) per thread
+        if (tid < C * JS) {  // U = U~ - W S, one (r, column) per thread
             const int r = tid / JS;
             float acc = Ut[r * JS + jj];
 #pragma unroll
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kThreads)
         if (c > 0) stage(buf(c - 1), prep + (slot_of(cu, n, c - 1) * H + h) * rec, dk, dv, j0, true);
         const float *Kp = buf(c), *W = Kp + C * dk, *Qt = Kp + 2 * C * dk;
         const float *P = Qt + C * dk + C * JS, *gl = P + C * C;
-        {
+        if (tid < C * JS) {
             const int r = tid / JS;
             dO[r * JS + jj] = (r < L && col) ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
         }
@@ -508,15 +509,16 @@ __global__ void __launch_bounds__(kThreads)
             const int x = rg * RPT + i;
             if (col && x < dk) dst[(size_t)x * dv + j] = ds[i];
         }
-        if (dk == RG * RPT) {  // full height: two float4 per product row
+        if (dk == RG * RPT) {  // full height: this thread's rows as float4 per product row
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float4 k0 = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT);
-                const float4 k1 = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT + 4);
-                float acc = k0.x * ds[0];
-                acc = fmaf(k0.y, ds[1], acc); acc = fmaf(k0.z, ds[2], acc); acc = fmaf(k0.w, ds[3], acc);
-                acc = fmaf(k1.x, ds[4], acc); acc = fmaf(k1.y, ds[5], acc); acc = fmaf(k1.z, ds[6], acc);
-                acc = fmaf(k1.w, ds[7], acc);
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < RPT; i += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(Kp + r * dk + rg * RPT + i);
+                    acc = fmaf(k4.x, ds[i], acc); acc = fmaf(k4.y, ds[i + 1], acc);
+                    acc = fmaf(k4.z, ds[i + 2], acc); acc = fmaf(k4.w, ds[i + 3], acc);
+                }
                 part[(rg * C + r) * JS + jj] = acc;
             }
         } else {
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(kThreads)
         }
         }
         __syncthreads();
-        {  // X = K' dS + s P^T dO
+        if (tid < C * JS) {  // X = K' dS + s P^T dO
             const int r = tid / JS;
             float acc = 0.f;
 #pragma unroll
