@@ -609,19 +609,32 @@ __device__ void mma_middle(const Chunk &b, const float *S, const float *dSe, con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n0 = 16 * warp;
     auto u32 = [](const void *ptr) { return static_cast<uint32_t>(__cvta_generic_to_shared(ptr)); };
     // state tile: 4096 float4 of S (or dS_end), row x of 32 float4 per warp and step
+    // (loads are issued in batches of 8 per thread before any is consumed, so that their
+    // latencies overlap)
     auto stage_state = [&](const float *src, bool with_dgl) {
-        for (int it = 0; it < D * D / 4 / kThreads; ++it) {
-            const int i = tid + it * kThreads, x = i >> 5, c4 = (i & 31) * 4;
-            const float4 v = *reinterpret_cast<const float4 *>(src + (size_t)x * D + c4);
-            __nv_bfloat162 *d2 = reinterpret_cast<__nv_bfloat162 *>(SB16 + x * PB + c4);
-            d2[0] = __floats2bfloat162_rn(v.x, v.y);
-            d2[1] = __floats2bfloat162_rn(v.z, v.w);
-            if (with_dgl) {  // rowsum(dS_end . S) in fp32: one row per warp and step
-                const float4 s4 = *reinterpret_cast<const float4 *>(S + (size_t)x * D + c4);
-                float acc = v.x * s4.x + v.y * s4.y + v.z * s4.z + v.w * s4.w;
+        constexpr int kSteps = D * D / 4 / kThreads, kBatch = 8;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (lane == 0) dgl[x] = acc;
+        for (int it0 = 0; it0 < kSteps; it0 += kBatch) {
+            float4 v[kBatch], s4[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = tid + (it0 + u) * kThreads, x = i >> 5, c4 = (i & 31) * 4;
+                v[u] = *reinterpret_cast<const float4 *>(src + (size_t)x * D + c4);
+                if (with_dgl) s4[u] = *reinterpret_cast<const float4 *>(S + (size_t)x * D + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = tid + (it0 + u) * kThreads, x = i >> 5, c4 = (i & 31) * 4;
+                __nv_bfloat162 *d2 = reinterpret_cast<__nv_bfloat162 *>(SB16 + x * PB + c4);
+                d2[0] = __floats2bfloat162_rn(v[u].x, v[u].y);
+                d2[1] = __floats2bfloat162_rn(v[u].z, v[u].w);
+                if (with_dgl) {  // rowsum(dS_end . S) in fp32: one row per warp and step
+                    float acc = v[u].x * s4[u].x + v[u].y * s4[u].y + v[u].z * s4[u].z +
+                                v[u].w * s4[u].w;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                    if (lane == 0) dgl[x] = acc;
+                }
             }
         }
     };
