@@ -124,7 +124,10 @@ kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     if (e != cudaSuccess) return launched(e, "reading the device status word");
     e = kda::read_gemm_flags(&g, reset != 0, (cudaStream_t)stream);
     if (e != cudaSuccess) return launched(e, "reading the device status word");
-    *flags = v | g;
+    unsigned int bw = 0;
+    e = kda::read_bwd_flags(&bw, reset != 0, (cudaStream_t)stream);
+    if (e != cudaSuccess) return launched(e, "reading the device status word");
+    *flags = v | g | bw;
     return ok();
 }
 

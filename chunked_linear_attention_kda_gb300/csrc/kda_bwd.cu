@@ -39,6 +39,9 @@
 #include "kda_internal.h"
 
 namespace kda {
+
+__device__ unsigned int g_bwd_flags;  // bit 2: a serial-pass wait exceeded its limit
+
 namespace {
 
 constexpr int C = kChunk;
@@ -273,11 +276,30 @@ __host__ __device__ constexpr size_t P_UT(int dk) { return (size_t)3 * C * dk; }
 __host__ __device__ constexpr size_t P_P(int dk, int dv) { return (size_t)3 * C * dk + (size_t)C * dv; }
 __host__ __device__ constexpr size_t P_GL(int dk, int dv) { return P_P(dk, dv) + C * C; }
 
+// Operand-tile record per (chunk slot, head) for the tensor-core serial passes (d_k = d_v =
+// 128), written by the prep kernel in place of its fp32 record (the local-gradient kernel
+// recomputes its own products), read into shared memory by bulk copies: K', -W, Q~ as bf16 [16][PB], P bf16 [16][PS], gamma_L fp32 in
+// the chain warps' float4 order, then U~^T fp32 [32][16] for each of the four 32-column
+// blocks (bytes).
+constexpr int T128 = C * 136 * 2;        // a [16][PB] bf16 tile
+constexpr int TR_K = 0, TR_W = T128, TR_Q = 2 * T128, TR_P = 3 * T128;
+constexpr int TR_G = TR_P + C * 24 * 2;
+constexpr int TR_OPS = TR_G + 128 * 4;   // bytes one bulk copy moves per chunk
+constexpr int TR_UT = TR_OPS;            // + 2048 * r: block r's U~^T
+constexpr int TREC = TR_UT + 4 * 32 * C * 4;
+static_assert(TR_G % 16 == 0 && TR_OPS % 16 == 0 && TREC % 16 == 0, "16-byte record parts");
+static_assert((size_t)TREC <= prep_floats(128, 128) * 4 && prep_floats(128, 128) % 4 == 0,
+              "the tile record fits the fp32 record's 16-byte aligned place");
+__device__ __forceinline__ int gperm_tc(int c) {
+    return ((c >> 4) * 4 + ((c >> 1) & 3)) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(kThreads)
     prep_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                 const float *__restrict__ a, const float *__restrict__ beta,
-                const int32_t *__restrict__ cu, float *__restrict__ prep, int H, int dk, int dv) {
+                const int32_t *__restrict__ cu, float *__restrict__ prep,
+                bool tile_rec, int H, int dk, int dv) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -290,15 +312,40 @@ __global__ void __launch_bounds__(kThreads)
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
         float *o = prep + (slot_of(cu, n, c) * H + h) * rec;
-        for (int i = tid; i < C * dk; i += kThreads) {
-            const int r = i / dk, x = i % dk;
-            o[P_KP(dk) + i] = b.Kp[r * lk + x];
-            o[P_W(dk) + i] = b.W[r * lk + x];
-            o[P_QT(dk) + i] = b.Qt[r * lk + x];
+        if (!tile_rec) {
+            for (int i = tid; i < C * dk; i += kThreads) {
+                const int r = i / dk, x = i % dk;
+                o[P_KP(dk) + i] = b.Kp[r * lk + x];
+                o[P_W(dk) + i] = b.W[r * lk + x];
+                o[P_QT(dk) + i] = b.Qt[r * lk + x];
+            }
+            for (int i = tid; i < C * dv; i += kThreads)
+                o[P_UT(dk) + i] = b.Ut[(i / dv) * lv + i % dv];
+            o[P_P(dk, dv) + tid] = b.P[tid];  // kThreads == C * C
+            for (int x = tid; x < dk; x += kThreads) o[P_GL(dk, dv) + x] = b.gl[x];
+        } else {  // d_k = d_v = 128: the operand-tile record, in place of the fp32 one
+            unsigned char *tr = reinterpret_cast<unsigned char *>(o);
+            __nv_bfloat16 *tk = reinterpret_cast<__nv_bfloat16 *>(tr + TR_K);
+            __nv_bfloat16 *tw = reinterpret_cast<__nv_bfloat16 *>(tr + TR_W);
+            __nv_bfloat16 *tq = reinterpret_cast<__nv_bfloat16 *>(tr + TR_Q);
+            for (int i = tid; i < C * 136; i += kThreads) {
+                const int r = i / 136, x = i % 136;
+                const bool in = x < 128;
+                tk[i] = __float2bfloat16_rn(in ? b.Kp[r * lk + x] : 0.f);
+                tw[i] = __float2bfloat16_rn(in ? -b.W[r * lk + x] : 0.f);
+                tq[i] = __float2bfloat16_rn(in ? b.Qt[r * lk + x] : 0.f);
+            }
+            __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(tr + TR_P);
+            for (int i = tid; i < C * 24; i += kThreads)
+                tp[i] = __float2bfloat16_rn(i % 24 < C ? b.P[(i / 24) * C + i % 24] : 0.f);
+            float *tg = reinterpret_cast<float *>(tr + TR_G);
+            for (int x = tid; x < 128; x += kThreads) tg[gperm_tc(x)] = b.gl[x];
+            float *tu = reinterpret_cast<float *>(tr + TR_UT);  // [r][32 v][16 t]
+            for (int i = tid; i < 128 * C; i += kThreads) {
+                const int v = i / C, t = i % C;
+                tu[i] = b.Ut[t * lv + v];
+            }
         }
-        for (int i = tid; i < C * dv; i += kThreads) o[P_UT(dk) + i] = b.Ut[(i / dv) * lv + i % dv];
-        o[P_P(dk, dv) + tid] = b.P[tid];  // kThreads == C * C
-        for (int x = tid; x < dk; x += kThreads) o[P_GL(dk, dv) + x] = b.gl[x];
     }
 }
 
@@ -589,6 +636,249 @@ __global__ void __launch_bounds__(kThreads)
             if (col && x < dk) dh0[((size_t)n * H + h) * st + (size_t)x * dv + j] = ds[i];
         }
     }
+}
+
+// ---- 1b/2b. the two serial passes on the tensor cores (bf16 I/O, d_k = d_v = 128)
+// CTA (sequence, head, r) carries value columns [32 r, 32 r + 32) of one chain: two chain
+// warps hold 16 rows each of S^T (or dS^T, d_v x d_k) as fp32 mma fragments in registers
+// for the whole sequence, and two loader warps convert each chunk's products from its prep
+// record into bf16 operand tiles a few chunks ahead (a ring of NS slots). Per chunk, with
+// a warp's rows of the state A = S^T as bf16 A fragments (mma.sync m16n8k16):
+//   forward:  write S^T (the chunk's start state); U^T = U~^T + S^T (-W)^T;
+//             S^T <- S^T Diag(gamma_L) + U^T K'
+//   reverse:  write dS^T (the gradient at the chunk's end); X^T = dS^T K'^T + (s dO)^T P;
+//             dS^T <- dS^T Diag(gamma_L) + (s dO)^T Q~ + X^T (-W)
+// the transposed forms of the two chains above, the state an fp32 accumulator throughout.
+constexpr int NS = 4;                    // ring slots
+constexpr int PO = 40;                   // bf16 pitch of the [16][32] (s dO) slice (80-byte rows)
+// slot layout (bytes): the record's operand part [0, TR_OPS) (K', -W, Q~, P, gamma_L), then
+// U~^T [32][16] fp32 (forward) or (s dO) [16][PO] bf16 (reverse)
+constexpr int SL_K = TR_K, SL_W = TR_W, SL_Q = TR_Q, SL_P = TR_P, SL_G = TR_G, SL_X = TR_OPS;
+constexpr int SLOT = SL_X + 32 * C * 4;
+static_assert(SL_X % 16 == 0 && SLOT % 16 == 0, "16-byte aligned slot parts");
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_tx(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bar_init(uint32_t a, uint32_t c) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(c));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t a) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    return ok != 0;
+}
+// bounded wait; false when this or another wait of the grid gave up
+__device__ bool bar_wait(uint32_t a, uint32_t parity) {
+    if (bar_try(a, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (bar_try(a, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*(volatile unsigned int *)&g_bwd_flags != 0u) return false;
+            if (clock64() - t0 > 4000000000LL) {
+                atomicOr(&g_bwd_flags, 4u);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void mul2(float &a, float &b, float ga, float gb) {
+    asm("{ .reg .b64 x, y; mov.b64 x, {%0, %1}; mov.b64 y, {%2, %3}; mul.rn.f32x2 x, x, y; "
+        "mov.b64 {%0, %1}, x; }"
+        : "+f"(a), "+f"(b) : "f"(ga), "f"(gb));
+}
+
+template <bool REVERSE>
+__global__ void __launch_bounds__(128, 1)
+    chain_tc_kernel(const int32_t *__restrict__ cu, const float *__restrict__ prep,
+                    const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ init,
+                    float *__restrict__ states, float *__restrict__ final_state, int H,
+                    float scale) {
+    constexpr int D = 128;
+    extern __shared__ __align__(16) unsigned char smc[];
+    __shared__ __align__(8) unsigned long long bars[2 * NS];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int item = blockIdx.x / 4, r4 = blockIdx.x % 4;
+    const int n = item / H, h = item % H;
+    const int v0 = 32 * r4;  // first value column of this CTA
+    const int64_t t0 = cu[n], t1 = cu[n + 1];
+    const int nc = (int)((t1 - t0 + C - 1) / C);
+    const size_t st = (size_t)D * D, rec = prep_floats(D, D);
+    auto full = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[s])); };
+    auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            bar_init(full(s), REVERSE ? 2 : 1);  // the copies' issue (+ the s dO tile)
+            bar_init(empty(s), 2);  // one arrival per chain warp
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp >= 2) {
+        // ---------------------------------------------------------------- loader warp
+        if (warp == 3) return;
+        for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
+            const int s = m % NS;
+            bool ok = true;
+            if (m >= NS) ok = bar_wait(empty(s), ((m / NS) & 1) ^ 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
+            const unsigned char *tr =
+                reinterpret_cast<const unsigned char *>(prep + (slot_of(cu, n, c) * H + h) * rec);
+            if (lane == 0) {
+                if (REVERSE) {  // K', -W, Q~, P, gamma_L
+                    bar_arrive_tx(full(s), TR_OPS);
+                    bulk_g2s(sl, tr, TR_OPS, full(s));
+                } else {        // K', -W; gamma_L; this CTA's block of U~^T
+                    bar_arrive_tx(full(s), 2 * T128 + 128 * 4 + 32 * C * 4);
+                    bulk_g2s(sl + SL_K, tr + TR_K, 2 * T128, full(s));
+                    bulk_g2s(sl + SL_G, tr + TR_G, 128 * 4, full(s));
+                    bulk_g2s(sl + SL_X, tr + TR_UT + r4 * 32 * C * 4, 32 * C * 4, full(s));
+                }
+            }
+            if (REVERSE) {  // s dO, the CTA's 32 columns, as bf16 [16][PO]: a half row per lane
+                const int rr = lane >> 1, j0 = 16 * (lane & 1);
+                const int64_t tok = t0 + (int64_t)c * C + rr;
+                uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+                if (tok < t1) {
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(dout + ((size_t)tok * H + h) * D + v0 + j0);
+                    x0 = src[0];
+                    x1 = src[1];
+                }
+                uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
+                    w[i] = pack2(scale * f.x, scale * f.y);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(smc + s * SLOT + SL_X + rr * PO * 2 + j0 * 2);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                __syncwarp();
+                if (lane == 0) bar_arrive(full(s));  // release: the s dO tile is written
+            }
+        }
+        return;
+    }
+    // -------------------------------------------------------------------- chain warps
+    const int sw = warp, vr = v0 + 16 * sw;  // this warp's first value row of S^T
+    const int g4 = lane >> 2, l4 = lane & 3, i8 = lane >> 3, r8 = lane & 7;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smc));
+    float S[16][4];  // S^T (or dS^T) fragments: n-tile j = key channels 8j .. 8j + 7
+    const size_t hidx = ((size_t)n * H + h) * st;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int kc = 8 * j + 2 * l4, v = vr + g4;
+        if (init) {
+            S[j][0] = init[hidx + (size_t)kc * D + v];
+            S[j][1] = init[hidx + (size_t)(kc + 1) * D + v];
+            S[j][2] = init[hidx + (size_t)kc * D + v + 8];
+            S[j][3] = init[hidx + (size_t)(kc + 1) * D + v + 8];
+        } else {
+            S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+        }
+    }
+    auto write_state = [&](float *dst) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int kc = 8 * j + 2 * l4, v = vr + g4;
+            dst[(size_t)kc * D + v] = S[j][0];
+            dst[(size_t)(kc + 1) * D + v] = S[j][1];
+            dst[(size_t)kc * D + v + 8] = S[j][2];
+            dst[(size_t)(kc + 1) * D + v + 8] = S[j][3];
+        }
+    };
+    for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
+        const int s = m % NS;
+        const bool ok = bar_wait(full(s), (m / NS) & 1);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint32_t sl = sbase + s * SLOT;
+        const float4 *G4 = reinterpret_cast<const float4 *>(smc + s * SLOT + SL_G);
+        write_state(states + (slot_of(cu, n, c) * H + h) * st);
+        float acc[2][4];  // U^T (forward) or X^T (reverse): 16 value rows x 16 tokens
+        if (!REVERSE) {
+            const float *tu = reinterpret_cast<const float *>(smc + s * SLOT + SL_X);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int col = 8 * t + 2 * l4, row = 16 * sw + g4;
+                acc[t][0] = tu[row * C + col];
+                acc[t][1] = tu[row * C + col + 1];
+                acc[t][2] = tu[(row + 8) * C + col];
+                acc[t][3] = tu[(row + 8) * C + col + 1];
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        }
+        // (s dO)^T as the A fragment (reverse): 16 value rows x 16 tokens, read transposed
+        uint32_t oa[4] = {0u, 0u, 0u, 0u};
+        if (REVERSE)
+            ldsm4t(sl + SL_X + (uint32_t)((((i8 >> 1) * 8 + r8) + 0) * PO * 2 + (16 * sw + (i8 & 1) * 8) * 2), oa);
+#pragma unroll
+        for (int kt = 0; kt < 8; ++kt) {  // state tile kt against the chunk's 16 tokens
+            uint32_t a[4];
+            a[0] = pack2(S[2 * kt][0], S[2 * kt][1]);
+            a[1] = pack2(S[2 * kt][2], S[2 * kt][3]);
+            a[2] = pack2(S[2 * kt + 1][0], S[2 * kt + 1][1]);
+            a[3] = pack2(S[2 * kt + 1][2], S[2 * kt + 1][3]);
+            uint32_t bfr[4];
+            // forward: B[k = channel][n = token] = -W[t][c]; reverse: = K'[t][c]; [n][k] storage
+            ld_b_nk(sl + (REVERSE ? SL_K : SL_W), PB, 0, 16 * kt, bfr);
+            mma16816(acc[0], a, bfr[0], bfr[1]);
+            mma16816(acc[1], a, bfr[2], bfr[3]);
+        }
+        if (REVERSE) {  // + (s dO)^T P: B[k = token i][n = token r] = P[i][r], [k][n] storage
+            uint32_t bfr[4];
+            ld_b_kn(sl + SL_P, PS, 0, 0, bfr);
+            mma16816(acc[0], oa, bfr[0], bfr[1]);
+            mma16816(acc[1], oa, bfr[2], bfr[3]);
+        }
+        uint32_t ua[4];  // U^T / X^T as the A fragment of the update
+        ua[0] = pack2(acc[0][0], acc[0][1]);
+        ua[1] = pack2(acc[0][2], acc[0][3]);
+        ua[2] = pack2(acc[1][0], acc[1][1]);
+        ua[3] = pack2(acc[1][2], acc[1][3]);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {  // key tile np: decay, then the chunk's write
+            const float4 g = G4[np * 4 + l4];
+            mul2(S[2 * np][0], S[2 * np][1], g.x, g.y);
+            mul2(S[2 * np][2], S[2 * np][3], g.x, g.y);
+            mul2(S[2 * np + 1][0], S[2 * np + 1][1], g.z, g.w);
+            mul2(S[2 * np + 1][2], S[2 * np + 1][3], g.z, g.w);
+            uint32_t bfr[4];
+            // forward: U^T K' (B[k = token][n = channel] = K'[t][c]); reverse: X^T (-W)
+            ld_b_kn(sl + (REVERSE ? SL_W : SL_K), PB, 0, 16 * np, bfr);
+            mma16816(S[2 * np], ua, bfr[0], bfr[1]);
+            mma16816(S[2 * np + 1], ua, bfr[2], bfr[3]);
+            if (REVERSE) {  // + (s dO)^T Q~
+                ld_b_kn(sl + SL_Q, PB, 0, 16 * np, bfr);
+                mma16816(S[2 * np], oa, bfr[0], bfr[1]);
+                mma16816(S[2 * np + 1], oa, bfr[2], bfr[3]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) bar_arrive(empty(s));  // this warp's reads of the slot are done
+    }
+    if (final_state) write_state(final_state + hidx);
 }
 
 // ---- 3. local gradients of every chunk
@@ -996,6 +1286,10 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     constexpr bool kBf16 = sizeof(IO) == 2;
     const bool use_mma = kBf16 && dk == 128 && dv == 128;
     const size_t sm3 = local_floats(dk, dv, use_mma) * 4;
+    // the serial passes on the tensor cores too when the bulk copies' 16-byte alignment
+    // holds (workspace records, s dO rows)
+    const bool use_tc = use_mma && ((uintptr_t)p.workspace & 15u) == 0 &&
+                        ((uintptr_t)p.dout & 15u) == 0;
     auto local = use_mma ? local_kernel<IO, kBf16> : local_kernel<IO, false>;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess ||
@@ -1011,11 +1305,23 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     if (gy < 1) gy = 1;
     if (gy > 65535) gy = 65535;
     const dim3 par(items, (unsigned)gy), cols(items, (unsigned)((dv + JS - 1) / JS));
-    prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep, H,
-                                                   dk, dv);
+    prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
+                                                   use_tc, H, dk, dv);
+    if (use_tc) {  // the serial passes on the tensor cores, state in registers
+        const int smc = NS * SLOT;
+        if ((e = cudaFuncSetAttribute(chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess)
+            return e;
+        const __nv_bfloat16 *d16 = reinterpret_cast<const __nv_bfloat16 *>(p.dout);
+        chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, prep, d16, p.h0, ck,
+                                                                nullptr, H, scale);
+        chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, prep, d16, p.dh_final,
+                                                               dck, p.dh0, H, scale);
+    } else {
     ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
     chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep, dck,
                                                      p.dh0, H, dk, dv, scale);
+    }
     local<<<par, kThreads, sm3, stream>>>(
         q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk, (IO *)p.dv,
         p.da, p.dbeta, H, dk, dv, scale);
@@ -1039,4 +1345,19 @@ cudaError_t launch_bwd(const BwdArgs &p, cudaStream_t stream) {
     return p.bf16 ? launch_bwd_t<__nv_bfloat16>(p, stream) : launch_bwd_t<float>(p, stream);
 }
 
+}  // namespace kda
+
+namespace kda {
+cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_bwd_flags, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    if (reset) {
+        static const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_bwd_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                    stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaStreamSynchronize(stream);
+}
 }  // namespace kda

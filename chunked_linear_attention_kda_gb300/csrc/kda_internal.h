@@ -85,6 +85,8 @@ cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, fl
                              int N, int K, cudaStream_t stream);
 // The GEMM's own status word (bit 1: a pipeline wait gave up); synchronises stream.
 cudaError_t read_gemm_flags(unsigned int *flags, bool reset, cudaStream_t stream);
+// The backward serial passes' status word (bit 2); synchronises stream.
+cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
