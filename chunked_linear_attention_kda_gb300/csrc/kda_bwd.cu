@@ -222,33 +222,13 @@ __device__ __forceinline__ void ld_b_kn(uint32_t base, int pitch, int k0, int n0
     const int l = threadIdx.x & 31;
     ldsm4t(base + (uint32_t)(((k0 + (l & 7) + (((l >> 3) & 1) << 3)) * pitch + n0 + (l >> 4) * 8) * 2), b);
 }
-// acc (16 rows x columns [n0, n0 + 16)) += A (16 x K) B, B read from [k][n] (KN) or [n][k]
-template <bool KN>
-__device__ __forceinline__ void warp_mma(float (&acc)[2][4], uint32_t a_base, int pa, uint32_t b_base,
-                                         int pb, int n0, int K) {
-#pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 16) {
-        uint32_t af[4], bf[4];
-        ld_a(a_base, pa, k0, af);
-        if (KN) ld_b_kn(b_base, pb, k0, n0, bf);
-        else ld_b_nk(b_base, pb, n0, k0, bf);
-        mma16816(acc[0], af, bf[0], bf[1]);
-        mma16816(acc[1], af, bf[2], bf[3]);
-    }
+// A fragment of X^T (16 x 16) from X stored row-major [k][m]: rows [k0, k0 + 16), columns
+// [m0, m0 + 16) of the storage
+__device__ __forceinline__ void ld_a_t(uint32_t base, int pitch, int k0, int m0, uint32_t (&a)[4]) {
+    const int l = threadIdx.x & 31, j = l >> 3;
+    ldsm4t(base + (uint32_t)(((k0 + ((j >> 1) << 3) + (l & 7)) * pitch + m0 + ((j & 1) << 3)) * 2), a);
 }
-// the accumulator tile into fp32 (times alpha) or bf16 row-major storage
-__device__ __forceinline__ void store_c(float *dst, int pitch, int n0, const float (&acc)[2][4],
-                                        float alpha) {
-    const int l = threadIdx.x & 31, g4 = l >> 2, l4 = l & 3;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int col = n0 + 8 * t + 2 * l4;
-        dst[g4 * pitch + col] = alpha * acc[t][0];
-        dst[g4 * pitch + col + 1] = alpha * acc[t][1];
-        dst[(g4 + 8) * pitch + col] = alpha * acc[t][2];
-        dst[(g4 + 8) * pitch + col + 1] = alpha * acc[t][3];
-    }
-}
+// the accumulator tile (16 rows x columns [n0, n0 + 16)) into bf16 row-major storage
 __device__ __forceinline__ void store_c16(__nv_bfloat16 *dst, int pitch, int n0,
                                           const float (&acc)[2][4]) {
     const int l = threadIdx.x & 31, g4 = l >> 2, l4 = l & 3;
@@ -276,20 +256,36 @@ __host__ __device__ constexpr size_t P_UT(int dk) { return (size_t)3 * C * dk; }
 __host__ __device__ constexpr size_t P_P(int dk, int dv) { return (size_t)3 * C * dk + (size_t)C * dv; }
 __host__ __device__ constexpr size_t P_GL(int dk, int dv) { return P_P(dk, dv) + C * C; }
 
-// Operand-tile record per (chunk slot, head) for the tensor-core serial passes (d_k = d_v =
-// 128), written by the prep kernel in place of its fp32 record (the local-gradient kernel
-// recomputes its own products), read into shared memory by bulk copies: K', -W, Q~ as bf16 [16][PB], P bf16 [16][PS], gamma_L fp32 in
-// the chain warps' float4 order, then U~^T fp32 [32][16] for each of the four 32-column
-// blocks (bytes).
+// Tensor-core path (bf16 I/O, d_k = d_v = 128): the workspace holds, per (chunk slot, head),
+// REC_TC bytes -- the chunk's start state S and end-state gradient dS_end as bf16 S^T
+// tiles [128 v][136] (written by the two serial passes in the row layout shared memory
+// uses), then the prep kernel's record of the chunk's state-independent products:
+//   K', -W, Q~ bf16 [16][136]; P bf16 [16][24]; gamma_L fp32 in the serial passes' float4
+//   order (the part [0, TR_OPS) is what the serial passes copy); U~^T fp32 [128 v][16 t];
+//   K~, K^ bf16 [16][136]; M bf16 [16][24]; T, T^T, Z fp32 [16][16]; beta fp32 [16];
+//   G fp32 [16][136]; gamma_L fp32 [128].
 constexpr int T128 = C * 136 * 2;        // a [16][PB] bf16 tile
 constexpr int TR_K = 0, TR_W = T128, TR_Q = 2 * T128, TR_P = 3 * T128;
 constexpr int TR_G = TR_P + C * 24 * 2;
-constexpr int TR_OPS = TR_G + 128 * 4;   // bytes one bulk copy moves per chunk
-constexpr int TR_UT = TR_OPS;            // + 2048 * r: block r's U~^T
-constexpr int TREC = TR_UT + 4 * 32 * C * 4;
-static_assert(TR_G % 16 == 0 && TR_OPS % 16 == 0 && TREC % 16 == 0, "16-byte record parts");
-static_assert((size_t)TREC <= prep_floats(128, 128) * 4 && prep_floats(128, 128) % 4 == 0,
-              "the tile record fits the fp32 record's 16-byte aligned place");
+constexpr int TR_OPS = TR_G + 128 * 4;   // bytes the serial passes' copies start from
+constexpr int TR_UT = TR_OPS;            // + 2048 r: value block r's U~^T [32][16]
+constexpr int TR_KT = TR_UT + 128 * C * 4, TR_KH = TR_KT + T128;
+constexpr int TR_M = TR_KH + T128;
+constexpr int TR_T = TR_M + C * 24 * 2, TR_TT = TR_T + C * C * 4, TR_Z = TR_TT + C * C * 4;
+constexpr int TR_B = TR_Z + C * C * 4;
+constexpr int GP = 136;                  // pitch (floats) of the record's G rows
+constexpr int TR_GS = TR_B + C * 4, TR_GL = TR_GS + C * GP * 4;
+constexpr int RECB = TR_GL + 128 * 4;    // record bytes
+constexpr int ST16 = 128 * 136 * 2;      // a bf16 state tile
+constexpr size_t TC_S = 0, TC_DS = ST16, TC_REC = 2 * ST16;
+constexpr size_t REC_TC = TC_REC + RECB; // workspace bytes per (chunk slot, head)
+static_assert(TR_G % 16 == 0 && TR_OPS % 16 == 0 && TR_KT % 16 == 0 && TR_M % 16 == 0 &&
+                  TR_T % 16 == 0 && TR_GS % 16 == 0 && RECB % 16 == 0 && REC_TC % 16 == 0,
+              "16-byte record parts");
+static_assert(REC_TC <= ((size_t)2 * 128 * 128 + prep_floats(128, 128)) * 4,
+              "the tensor-core layout fits the workspace the fp32 layout sizes");
+// gamma_L[c], c = 16 np + 8 hh + 2 l4 + e, stored at 16 np + 4 l4 + 2 hh + e: the lane holding
+// S^T columns 2 l4 (+1, +8, +9) of 16-column group np reads its four factors as one float4
 __device__ __forceinline__ int gperm_tc(int c) {
     return ((c >> 4) * 4 + ((c >> 1) & 3)) * 4 + ((c >> 3) & 1) * 2 + (c & 1);
 }
@@ -299,7 +295,7 @@ __global__ void __launch_bounds__(kThreads)
     prep_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                 const float *__restrict__ a, const float *__restrict__ beta,
                 const int32_t *__restrict__ cu, float *__restrict__ prep,
-                bool tile_rec, int H, int dk, int dv) {
+                unsigned char *__restrict__ tc, int H, int dk, int dv) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -311,8 +307,8 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
-        float *o = prep + (slot_of(cu, n, c) * H + h) * rec;
-        if (!tile_rec) {
+        if (!tc) {
+            float *o = prep + (slot_of(cu, n, c) * H + h) * rec;
             for (int i = tid; i < C * dk; i += kThreads) {
                 const int r = i / dk, x = i % dk;
                 o[P_KP(dk) + i] = b.Kp[r * lk + x];
@@ -323,21 +319,37 @@ __global__ void __launch_bounds__(kThreads)
                 o[P_UT(dk) + i] = b.Ut[(i / dv) * lv + i % dv];
             o[P_P(dk, dv) + tid] = b.P[tid];  // kThreads == C * C
             for (int x = tid; x < dk; x += kThreads) o[P_GL(dk, dv) + x] = b.gl[x];
-        } else {  // d_k = d_v = 128: the operand-tile record, in place of the fp32 one
-            unsigned char *tr = reinterpret_cast<unsigned char *>(o);
+        } else {  // d_k = d_v = 128: the tensor-core record
+            unsigned char *tr = tc + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
             __nv_bfloat16 *tk = reinterpret_cast<__nv_bfloat16 *>(tr + TR_K);
             __nv_bfloat16 *tw = reinterpret_cast<__nv_bfloat16 *>(tr + TR_W);
             __nv_bfloat16 *tq = reinterpret_cast<__nv_bfloat16 *>(tr + TR_Q);
+            __nv_bfloat16 *tkt = reinterpret_cast<__nv_bfloat16 *>(tr + TR_KT);
+            __nv_bfloat16 *tkh = reinterpret_cast<__nv_bfloat16 *>(tr + TR_KH);
+            float *tgs = reinterpret_cast<float *>(tr + TR_GS);
             for (int i = tid; i < C * 136; i += kThreads) {
                 const int r = i / 136, x = i % 136;
                 const bool in = x < 128;
                 tk[i] = __float2bfloat16_rn(in ? b.Kp[r * lk + x] : 0.f);
                 tw[i] = __float2bfloat16_rn(in ? -b.W[r * lk + x] : 0.f);
                 tq[i] = __float2bfloat16_rn(in ? b.Qt[r * lk + x] : 0.f);
+                tkt[i] = __float2bfloat16_rn(in ? b.Kt[r * lk + x] : 0.f);
+                tkh[i] = __float2bfloat16_rn(in ? b.Kh[r * lk + x] : 0.f);
+                tgs[i] = in ? b.Gs[r * lk + x] : 0.f;
             }
             __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(tr + TR_P);
-            for (int i = tid; i < C * 24; i += kThreads)
-                tp[i] = __float2bfloat16_rn(i % 24 < C ? b.P[(i / 24) * C + i % 24] : 0.f);
+            __nv_bfloat16 *tm = reinterpret_cast<__nv_bfloat16 *>(tr + TR_M);
+            for (int i = tid; i < C * 24; i += kThreads) {
+                const bool in = i % 24 < C;
+                tp[i] = __float2bfloat16_rn(in ? b.P[(i / 24) * C + i % 24] : 0.f);
+                tm[i] = __float2bfloat16_rn(in ? b.M[(i / 24) * C + i % 24] : 0.f);
+            }
+            // kThreads == C * C
+            reinterpret_cast<float *>(tr + TR_T)[tid] = b.T[tid];
+            reinterpret_cast<float *>(tr + TR_TT)[tid] = b.T[(tid % C) * C + tid / C];
+            reinterpret_cast<float *>(tr + TR_Z)[tid] = b.Z[tid];
+            if (tid < C) reinterpret_cast<float *>(tr + TR_B)[tid] = b.bt[tid];
+            for (int x = tid; x < 128; x += kThreads) reinterpret_cast<float *>(tr + TR_GL)[x] = b.gl[x];
             float *tg = reinterpret_cast<float *>(tr + TR_G);
             for (int x = tid; x < 128; x += kThreads) tg[gperm_tc(x)] = b.gl[x];
             float *tu = reinterpret_cast<float *>(tr + TR_UT);  // [r][32 v][16 t]
@@ -708,10 +720,9 @@ __device__ __forceinline__ void mul2(float &a, float &b, float ga, float gb) {
 
 template <bool REVERSE>
 __global__ void __launch_bounds__(128, 1)
-    chain_tc_kernel(const int32_t *__restrict__ cu, const float *__restrict__ prep,
+    chain_tc_kernel(const int32_t *__restrict__ cu, unsigned char *__restrict__ ws,
                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ init,
-                    float *__restrict__ states, float *__restrict__ final_state, int H,
-                    float scale) {
+                    float *__restrict__ final_state, int H, float scale) {
     constexpr int D = 128;
     extern __shared__ __align__(16) unsigned char smc[];
     __shared__ __align__(8) unsigned long long bars[2 * NS];
@@ -721,7 +732,7 @@ __global__ void __launch_bounds__(128, 1)
     const int v0 = 32 * r4;  // first value column of this CTA
     const int64_t t0 = cu[n], t1 = cu[n + 1];
     const int nc = (int)((t1 - t0 + C - 1) / C);
-    const size_t st = (size_t)D * D, rec = prep_floats(D, D);
+    const size_t st = (size_t)D * D;
     auto full = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[s])); };
     auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
     if (tid == 0) {
@@ -741,8 +752,7 @@ __global__ void __launch_bounds__(128, 1)
             if (m >= NS) ok = bar_wait(empty(s), ((m / NS) & 1) ^ 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
-            const unsigned char *tr =
-                reinterpret_cast<const unsigned char *>(prep + (slot_of(cu, n, c) * H + h) * rec);
+            const unsigned char *tr = ws + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
             if (lane == 0) {
                 if (REVERSE) {  // K', -W, Q~, P, gamma_L
                     bar_arrive_tx(full(s), TR_OPS);
@@ -797,7 +807,7 @@ __global__ void __launch_bounds__(128, 1)
             S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
         }
     }
-    auto write_state = [&](float *dst) {
+    auto write_state = [&](float *dst) {  // fp32 [key][v] (the final state)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int kc = 8 * j + 2 * l4, v = vr + g4;
@@ -807,13 +817,21 @@ __global__ void __launch_bounds__(128, 1)
             dst[(size_t)(kc + 1) * D + v + 8] = S[j][3];
         }
     };
+    auto write_tile = [&](unsigned char *dst) {  // bf16 S^T [v][136]: rows v, key pairs
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int kc = 8 * j + 2 * l4, v = vr + g4;
+            *reinterpret_cast<uint32_t *>(dst + ((size_t)v * 136 + kc) * 2) = pack2(S[j][0], S[j][1]);
+            *reinterpret_cast<uint32_t *>(dst + ((size_t)(v + 8) * 136 + kc) * 2) = pack2(S[j][2], S[j][3]);
+        }
+    };
     for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
         const int s = m % NS;
         const bool ok = bar_wait(full(s), (m / NS) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t sl = sbase + s * SLOT;
         const float4 *G4 = reinterpret_cast<const float4 *>(smc + s * SLOT + SL_G);
-        write_state(states + (slot_of(cu, n, c) * H + h) * st);
+        write_tile(ws + (slot_of(cu, n, c) * H + h) * REC_TC + (REVERSE ? TC_DS : TC_S));
         float acc[2][4];  // U^T (forward) or X^T (reverse): 16 value rows x 16 tokens
         if (!REVERSE) {
             const float *tu = reinterpret_cast<const float *>(smc + s * SLOT + SL_X);
@@ -882,157 +900,21 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ---- 3. local gradients of every chunk
-// Tensor-core middle of the local-gradient kernel (d_k = d_v = 128, 8 warps; warp w owns
-// value / key columns [16 w, 16 w + 16) of every 128-wide product). Produces what the
-// SIMT middle does: dQ~ = s dO S^T, dW = -dU S^T, dK' = U dS_end^T, dgamma_L =
-// rowsum(dS_end . S), dP = lower(s dO U^T), dM = dU V^T, and dV = M^T dU written out.
-// S and dS_end are staged as bf16 through one buffer: S (U, dQ~), then dS_end (dU, dK',
-// with dgamma_L from the fp32 values), then S again (dW).
-template <typename IO>
-__device__ void mma_middle(const Chunk &b, const float *S, const float *dSe, const IO *dout,
-                           IO *dv_out, int64_t c0, int L, int H, int h, float scale,
-                           __nv_bfloat16 *SB16, __nv_bfloat16 *W16, __nv_bfloat16 *Kp16,
-                           __nv_bfloat16 *dO16, __nv_bfloat16 *U16, __nv_bfloat16 *dU16,
-                           __nv_bfloat16 *V16, __nv_bfloat16 *sPT16, __nv_bfloat16 *MT16, float *dQt,
-                           float *dW, float *dKp, float *dgl, float *dP, float *dM) {
-    constexpr int D = 128, lk = D + 1, lv = D + 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n0 = 16 * warp;
-    auto u32 = [](const void *ptr) { return static_cast<uint32_t>(__cvta_generic_to_shared(ptr)); };
-    // state tile: 4096 float4 of S (or dS_end), row x of 32 float4 per warp and step
-    // (loads are issued in batches of 8 per thread before any is consumed, so that their
-    // latencies overlap)
-    auto stage_state = [&](const float *src, bool with_dgl) {
-        constexpr int kSteps = D * D / 4 / kThreads, kBatch = 8;
-#pragma unroll
-        for (int it0 = 0; it0 < kSteps; it0 += kBatch) {
-            float4 v[kBatch], s4[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int i = tid + (it0 + u) * kThreads, x = i >> 5, c4 = (i & 31) * 4;
-                v[u] = *reinterpret_cast<const float4 *>(src + (size_t)x * D + c4);
-                if (with_dgl) s4[u] = *reinterpret_cast<const float4 *>(S + (size_t)x * D + c4);
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int i = tid + (it0 + u) * kThreads, x = i >> 5, c4 = (i & 31) * 4;
-                __nv_bfloat162 *d2 = reinterpret_cast<__nv_bfloat162 *>(SB16 + x * PB + c4);
-                d2[0] = __floats2bfloat162_rn(v[u].x, v[u].y);
-                d2[1] = __floats2bfloat162_rn(v[u].z, v[u].w);
-                if (with_dgl) {  // rowsum(dS_end . S) in fp32: one row per warp and step
-                    float acc = v[u].x * s4[u].x + v[u].y * s4[u].y + v[u].z * s4[u].z +
-                                v[u].w * s4[u].w;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                    if (lane == 0) dgl[x] = acc;
-                }
-            }
-        }
-    };
-    // bf16 operand copies of the chunk products and of dO
-    for (int i = tid; i < C * D; i += kThreads) {
-        const int r = i / D, x = i % D;
-        W16[r * PB + x] = __float2bfloat16_rn(b.W[r * lk + x]);
-        Kp16[r * PB + x] = __float2bfloat16_rn(b.Kp[r * lk + x]);
-        V16[r * PB + x] = __float2bfloat16_rn(b.V[r * lv + x]);
-        dO16[r * PB + x] = __float2bfloat16_rn(
-            r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * D + x) : 0.f);
-    }
-    {
-        const int r = tid / C, i2 = tid % C;
-        sPT16[r * PS + i2] = __float2bfloat16_rn(scale * b.P[i2 * C + r]);
-        MT16[r * PS + i2] = __float2bfloat16_rn(b.M[i2 * C + r]);
-    }
-    stage_state(S, false);
-    __syncthreads();
-    {  // U = U~ - W S (bf16 copy); dQ~ = s dO S^T
-        float acc[2][4] = {};
-        warp_mma<true>(acc, u32(W16), PB, u32(SB16), PB, n0, D);
-        const int g4 = lane >> 2, l4 = lane & 3;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int col = n0 + 8 * t + 2 * l4;
-            acc[t][0] = b.Ut[g4 * lv + col] - acc[t][0];
-            acc[t][1] = b.Ut[g4 * lv + col + 1] - acc[t][1];
-            acc[t][2] = b.Ut[(g4 + 8) * lv + col] - acc[t][2];
-            acc[t][3] = b.Ut[(g4 + 8) * lv + col + 1] - acc[t][3];
-        }
-        store_c16(U16, PB, n0, acc);
-        float dq[2][4] = {};
-        warp_mma<false>(dq, u32(dO16), PB, u32(SB16), PB, n0, D);
-        store_c(dQt, lk, n0, dq, scale);
-    }
-    __syncthreads();  // every reader of S is done; U complete
-    stage_state(dSe, true);
-    __syncthreads();
-    {  // dU = K' dS_end + s P^T dO (bf16 copy); dK' = U dS_end^T; dV = M^T dU (this warp's columns)
-        float acc[2][4] = {};
-        warp_mma<true>(acc, u32(Kp16), PB, u32(SB16), PB, n0, D);
-        warp_mma<true>(acc, u32(sPT16), PS, u32(dO16), PB, n0, C);
-        store_c16(dU16, PB, n0, acc);
-        float kp[2][4] = {};
-        warp_mma<false>(kp, u32(U16), PB, u32(SB16), PB, n0, D);
-        store_c(dKp, lk, n0, kp, 1.f);
-        __syncwarp();  // this warp's dU columns are in shared memory
-        float dv[2][4] = {};
-        warp_mma<true>(dv, u32(MT16), PS, u32(dU16), PB, n0, C);
-        const int g4 = lane >> 2, l4 = lane & 3;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int col = n0 + 8 * t + 2 * l4;
-            if (g4 < L) {
-                st_io(dv_out, ((size_t)(c0 + g4) * H + h) * D + col, dv[t][0]);
-                st_io(dv_out, ((size_t)(c0 + g4) * H + h) * D + col + 1, dv[t][1]);
-            }
-            if (g4 + 8 < L) {
-                st_io(dv_out, ((size_t)(c0 + g4 + 8) * H + h) * D + col, dv[t][2]);
-                st_io(dv_out, ((size_t)(c0 + g4 + 8) * H + h) * D + col + 1, dv[t][3]);
-            }
-        }
-    }
-    __syncthreads();  // every reader of dS_end is done; dU complete
-    stage_state(S, false);
-    if (warp == 0) {  // dP = lower(s dO U^T)
-        float acc[2][4] = {};
-        warp_mma<false>(acc, u32(dO16), PB, u32(U16), PB, 0, D);
-        const int g4 = lane >> 2, l4 = lane & 3;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int col = 8 * t + 2 * l4;
-            dP[g4 * C + col] = col <= g4 ? scale * acc[t][0] : 0.f;
-            dP[g4 * C + col + 1] = col + 1 <= g4 ? scale * acc[t][1] : 0.f;
-            dP[(g4 + 8) * C + col] = col <= g4 + 8 ? scale * acc[t][2] : 0.f;
-            dP[(g4 + 8) * C + col + 1] = col + 1 <= g4 + 8 ? scale * acc[t][3] : 0.f;
-        }
-    } else if (warp == 1) {  // dM = dU V^T
-        float acc[2][4] = {};
-        warp_mma<false>(acc, u32(dU16), PB, u32(V16), PB, 0, D);
-        store_c(dM, C, 0, acc, 1.f);
-    }
-    __syncthreads();
-    {  // dW = -dU S^T
-        float acc[2][4] = {};
-        warp_mma<false>(acc, u32(dU16), PB, u32(SB16), PB, n0, D);
-        store_c(dW, lk, n0, acc, -1.f);
-    }
+__host__ __device__ constexpr size_t local_mid_floats(int dk, int dv) {
+    return (size_t)C * (dv + 1)                   // dO
+           + (size_t)2 * dk * (JB + 1)            // S, dS_end column blocks
+           + (size_t)2 * C * (JB + 1);            // U, dU column blocks
 }
-
-__host__ __device__ constexpr size_t local_mid_floats(int dk, int dv, bool mma) {
-    return mma ? (size_t)(128 * PB + 6 * C * PB + 2 * C * PS) / 2  // bf16 operand tiles
-               : (size_t)C * (dv + 1)                              // dO
-                     + (size_t)2 * dk * (JB + 1)                   // S, dS_end column blocks
-                     + (size_t)2 * C * (JB + 1);                   // U, dU column blocks
-}
-__host__ __device__ constexpr size_t local_floats(int dk, int dv, bool mma) {
-    return chunk_floats(dk, dv) + local_mid_floats(dk, dv, mma)
+__host__ __device__ constexpr size_t local_floats(int dk, int dv) {
+    return chunk_floats(dk, dv) + local_mid_floats(dk, dv)
            + (size_t)5 * C * (dk + 1)                   // dQ~, dW, dK', dK~, dK^
            + (size_t)4 * C * C                          // dP, dM, dT / Y, dA
            + dk + C;                                    // dgamma_L, dbeta
 }
 
-// MMA: the sums over value columns on the tensor cores (bf16 operands, fp32 accumulation;
-// bf16 I/O with d_k = d_v = 128), reading S and dS_end whole; otherwise fp32 FMA loops
-// over 32-column blocks.
-template <typename IO, bool MMA>
+// fp32 FMA loops, the sums over value columns accumulated over 32-column blocks (any
+// d_k, d_v <= 128; the tensor-core kernel below takes bf16 I/O at d_k = d_v = 128).
+template <typename IO>
 __global__ void __launch_bounds__(kThreads)
     local_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                  const float *__restrict__ a, const float *__restrict__ beta,
@@ -1047,18 +929,12 @@ __global__ void __launch_bounds__(kThreads)
     const Chunk b = carve_chunk(sm, dk, dv);
     float *p = sm + chunk_floats(dk, dv);
     float *mid = p;
-    p += local_mid_floats(dk, dv, MMA);
-    // SIMT middle
+    p += local_mid_floats(dk, dv);
     float *dO = mid;
     float *Sb = dO + C * lv;
     float *dSb = Sb + dk * lj;
     float *Ub = dSb + dk * lj;
     float *dUb = Ub + C * lj;
-    // tensor-core middle: S or dS_end [128][PB], W, K', dO, U, dU, V [16][PB], s P^T, M^T [16][PS]
-    __nv_bfloat16 *SB16 = reinterpret_cast<__nv_bfloat16 *>(mid);
-    __nv_bfloat16 *W16 = SB16 + 128 * PB, *Kp16 = W16 + C * PB, *dO16 = Kp16 + C * PB;
-    __nv_bfloat16 *U16 = dO16 + C * PB, *dU16 = U16 + C * PB, *V16 = dU16 + C * PB;
-    __nv_bfloat16 *sPT16 = V16 + C * PB, *MT16 = sPT16 + C * PS;
     float *dQt = p; p += C * lk;
     float *dW = p; p += C * lk;
     float *dKp = p; p += C * lk;
@@ -1076,18 +952,9 @@ __global__ void __launch_bounds__(kThreads)
     for (int c = blockIdx.y; c < nc; c += gridDim.y) {
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
-        if (MMA && tid < 2 && c + (int)gridDim.y < nc) {
-            // the next chunk's two states into L2 while this one is processed
-            const size_t nx = (slot_of(cu, n, c + gridDim.y) * H + h) * st;
-            prefetch_l2((tid == 0 ? ck : dck) + nx, (uint32_t)(st * sizeof(float)));
-        }
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
         const float *S = ck + (slot_of(cu, n, c) * H + h) * st;
         const float *dSe = dck + (slot_of(cu, n, c) * H + h) * st;
-        if constexpr (MMA) {
-            mma_middle(b, S, dSe, dout, dv_out, c0, L, H, h, scale, SB16, W16, Kp16, dO16, U16, dU16,
-                       V16, sPT16, MT16, dQt, dW, dKp, dgl, dP, dM);
-        } else {
         for (int i = tid; i < C * dv; i += kThreads) {
             const int r = i / dv, j = i % dv;
             dO[r * lv + j] = r < L ? ld_io(dout, ((size_t)(c0 + r) * H + h) * dv + j) : 0.f;
@@ -1168,7 +1035,6 @@ __global__ void __launch_bounds__(kThreads)
             const int r = tid / C, i2 = tid % C;
             dP[r * C + i2] = i2 <= r ? dp_acc : 0.f;
             dM[r * C + i2] = dm_acc;
-        }
         }
         __syncthreads();
         for (int i = tid; i < C * dk; i += kThreads) {  // dQ~ += dP K^
@@ -1266,6 +1132,457 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// ---- 3b. local gradients on the tensor cores (bf16 I/O, d_k = d_v = 128)
+// One CTA per SM walks a contiguous range of items (chunk slot, head), flat index slot H + h.
+// Per item it bulk-copies the two bf16 state tiles and the prep record into shared memory:
+// the record, with the item's V and dO rows, one item ahead into a second buffer; the
+// states as soon as the previous item's last reader of them is done (prefetched into L2 an
+// item ahead). Every product runs on mma.sync (bf16 operands, fp32 accumulation). Warp w
+// owns value columns [16 w, 16 w + 16) in phase 1 (U, dU, dV) and key channels [16 w,
+// 16 w + 16) in phases 2 and 4 (dQ~, dK', dW, dgamma_L, dK~, dK^ and the per-channel
+// gradients dq, dk, da, computed on the accumulator fragments); the 16 x 16 adjoint of the
+// solve (phase 3) is one element per thread.
+constexpr int LT_THREADS = 256;
+constexpr int RBUF = RECB + 2 * T128;  // record, then V and dO rows [16][136] bf16
+constexpr int LS_S = 0, LS_DS = ST16, LS_R = 2 * ST16;
+constexpr int LS_U = LS_R + 2 * RBUF, LS_DU = LS_U + T128, LS_DW = LS_DU + T128;
+constexpr int LS_DP = LS_DW + T128, LS_DZ = LS_DP + C * PS * 2;
+constexpr int LS_PART = LS_DZ + C * PS * 2;  // per warp: dM, dP partial sums [2][16][16]
+constexpr int LS_DT = LS_PART + 8 * 2 * C * C * 4, LS_DMS = LS_DT + C * C * 4, LS_Y = LS_DMS + C * C * 4;
+constexpr int LS_DB = LS_Y + C * C * 4;
+constexpr int LS_BYTES = LS_DB + C * 4;
+static_assert(RBUF % 16 == 0 && LS_U % 16 == 0 && LS_DP % 16 == 0 && LS_BYTES <= 227 * 1024,
+              "local tensor-core kernel shared memory");
+static_assert(LT_THREADS == C * C, "one thread per element of a 16 x 16 product");
+
+struct Item {
+    int n, h, c;
+};
+// item idx = slot H + h; false when the slot holds no chunk (the gap after a sequence)
+__device__ bool decode_item(const int32_t *cu, int n_seq, int H, long long idx, Item &it) {
+    const long long slot = idx / H;
+    it.h = (int)(idx - slot * H);
+    int lo = 0, hi = n_seq - 1;  // the last sequence whose first slot is <= slot
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)(cu[mid] >> 4) + mid <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    it.n = lo;
+    it.c = (int)(slot - ((long long)(cu[lo] >> 4) + lo));
+    return it.c < (cu[lo + 1] - cu[lo] + C - 1) / C;
+}
+
+__global__ void __launch_bounds__(LT_THREADS, 1)
+    local_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
+                    const int32_t *__restrict__ cu, const __nv_bfloat16 *__restrict__ dout,
+                    const unsigned char *__restrict__ ws, __nv_bfloat16 *__restrict__ dq,
+                    __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
+                    float *__restrict__ da, float *__restrict__ dbeta, int H, int n_seq,
+                    long long n_items, float scale) {
+    constexpr int D = 128;
+    extern __shared__ __align__(128) unsigned char sl[];
+    __shared__ __align__(8) unsigned long long bars[3];  // states; record buffers 0, 1
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, l4 = lane & 3, n0 = 16 * warp;
+    const long long beg = (long long)blockIdx.x * n_items / gridDim.x;
+    const long long end = (long long)(blockIdx.x + 1) * n_items / gridDim.x;
+    const uint32_t sb = static_cast<uint32_t>(__cvta_generic_to_shared(sl));
+    auto bar = [&](int i) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[i])); };
+    float *part = reinterpret_cast<float *>(sl + LS_PART);
+    float *dTs = reinterpret_cast<float *>(sl + LS_DT), *dMs = reinterpret_cast<float *>(sl + LS_DMS);
+    float *Ys = reinterpret_cast<float *>(sl + LS_Y), *dbs = reinterpret_cast<float *>(sl + LS_DB);
+    __nv_bfloat16 *dP16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DP);
+    __nv_bfloat16 *dZ16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DZ);
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) bar_init(bar(i), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto next_valid = [&](long long i, Item &it) {
+        while (i < end && !decode_item(cu, n_seq, H, i, it)) ++i;
+        return i;
+    };
+    auto rows_of = [&](const Item &it, int64_t &c0) {
+        c0 = cu[it.n] + (int64_t)it.c * C;
+        const int64_t left = cu[it.n + 1] - c0;
+        return (int)(left < C ? left : C);
+    };
+    auto rec_of = [&](const Item &it) {
+        return ws + (slot_of(cu, it.n, it.c) * H + it.h) * REC_TC;
+    };
+    // warp 0: the record and the V, dO rows of item it into record buffer rb
+    auto issue_rec = [&](const Item &it, int rb) {
+        int64_t c0;
+        const int L = rows_of(it, c0);
+        unsigned char *buf = sl + LS_R + rb * RBUF;
+        const uint32_t bb = sb + LS_R + rb * RBUF;
+        if (L < C) {  // rows past the sequence's end read as zeros
+            const int per = (C - L) * (T128 / C / 16);  // 16-byte pieces of the missing rows
+            for (int i = lane; i < 2 * per; i += 32) {
+                const int tile = i / per, rest = i % per;
+                *reinterpret_cast<uint4 *>(buf + RECB + tile * T128 + L * (T128 / C) + rest * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) {
+            bar_arrive_tx(bar(1 + rb), (uint32_t)(RECB + 2 * L * D * 2));
+            bulk_g2s(bb, rec_of(it) + TC_REC, RECB, bar(1 + rb));
+        }
+        __syncwarp();
+        const int r = lane & 15;
+        if (r < L) {  // lane r: V row r; lane 16 + r: dO row r
+            const __nv_bfloat16 *src = (lane < 16 ? v : dout) + ((size_t)(c0 + r) * H + it.h) * D;
+            bulk_g2s(bb + RECB + (lane >> 4) * T128 + r * (T128 / C), src, D * 2, bar(1 + rb));
+        }
+    };
+    auto issue_states = [&](const Item &it) {  // one thread: S and dS_end, adjacent both sides
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bar_arrive_tx(bar(0), 2 * ST16);
+        bulk_g2s(sb + LS_S, rec_of(it) + TC_S, 2 * ST16, bar(0));
+    };
+    // warp 1: the next item's states and its q, k, a rows into L2
+    auto prefetch_next = [&](const Item &it) {
+        int64_t c0;
+        const int L = rows_of(it, c0);
+        if (lane == 0) prefetch_l2(rec_of(it) + TC_S, 2 * ST16);
+        const int r = lane & 15;
+        if (r < L) {
+            const size_t o = ((size_t)(c0 + r) * H + it.h) * D;
+            if (lane < 16) {
+                prefetch_l2(q + o, D * 2);
+                prefetch_l2(k + o, D * 2);
+            } else {
+                prefetch_l2(a + o, D * 4);
+            }
+        }
+    };
+
+    Item cur, nxt;
+    long long idx = next_valid(beg, cur);
+    if (idx < end && warp == 0) {
+        issue_rec(cur, 0);
+        if (lane == 0) issue_states(cur);
+    }
+    for (int m = 0; idx < end; ++m) {
+        const long long nidx = next_valid(idx + 1, nxt);
+        const bool more = nidx < end;
+        __syncthreads();  // the other record buffer's readers (the previous item) are done
+        if (more) {
+            if (warp == 0) issue_rec(nxt, (m + 1) & 1);
+            else if (warp == 1) prefetch_next(nxt);
+        }
+        const int rb = m & 1;
+        const bool ok = bar_wait(bar(1 + rb), (uint32_t)((m >> 1) & 1)) && bar_wait(bar(0), (uint32_t)(m & 1));
+        if (__syncthreads_or(!ok)) break;
+        int64_t c0;
+        const int L = rows_of(cur, c0);
+        const int h = cur.h;
+        const unsigned char *R = sl + LS_R + rb * RBUF;
+        const uint32_t rbase = sb + LS_R + rb * RBUF;
+        const uint32_t SB = sb + LS_S, DSB = sb + LS_DS;
+        const uint32_t KP = rbase + TR_K, WN = rbase + TR_W, QT = rbase + TR_Q, P16 = rbase + TR_P;
+        const uint32_t KT = rbase + TR_KT, KH = rbase + TR_KH, M16 = rbase + TR_M;
+        const uint32_t V16 = rbase + RECB, DO = rbase + RECB + T128;
+        const uint32_t U16 = sb + LS_U, DU16 = sb + LS_DU, DW16 = sb + LS_DW;
+        const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ;
+
+        // ---- phase 1 (value columns [n0, n0 + 16)): U = U~ - W S, dU = K' dS_end + s P^T dO,
+        // dV = M^T dU; partial sums of dO U^T and dU V^T over these columns
+        float u[2][4], du[2][4] = {}, dpp[2][4] = {}, dmp[2][4] = {};
+        {
+            const float *Ut = reinterpret_cast<const float *>(R + TR_UT);  // [v][16 t]
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int vc = n0 + 8 * tt + 2 * l4;
+                u[tt][0] = Ut[vc * C + g4];
+                u[tt][1] = Ut[(vc + 1) * C + g4];
+                u[tt][2] = Ut[vc * C + g4 + 8];
+                u[tt][3] = Ut[(vc + 1) * C + g4 + 8];
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < D; k0 += 16) {  // k = key channel
+                uint32_t aw[4], ak[4], bs[4], bd[4];
+                ld_a(WN, PB, k0, aw);
+                ld_a(KP, PB, k0, ak);
+                ld_b_nk(SB, PB, n0, k0, bs);   // B[key][v] = S^T tile [v][key]
+                ld_b_nk(DSB, PB, n0, k0, bd);
+                mma16816(u[0], aw, bs[0], bs[1]);
+                mma16816(u[1], aw, bs[2], bs[3]);
+                mma16816(du[0], ak, bd[0], bd[1]);
+                mma16816(du[1], ak, bd[2], bd[3]);
+            }
+            uint32_t ap[4], bo[4];
+            float pd[2][4] = {};
+            ld_a_t(P16, PS, 0, 0, ap);         // P^T
+            ld_b_kn(DO, PB, 0, n0, bo);        // B[i][v] = dO[i][v]
+            mma16816(pd[0], ap, bo[0], bo[1]);
+            mma16816(pd[1], ap, bo[2], bo[3]);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) du[tt][i] = fmaf(scale, pd[tt][i], du[tt][i]);
+            store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_U), PB, n0, u);
+            store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_DU), PB, n0, du);
+            // dO[:, cols] U[:, cols]^T: U's accumulator fragments are the B operand as they are
+            uint32_t ao[4];
+            ld_a(DO, PB, n0, ao);
+            mma16816(dpp[0], ao, pack2(u[0][0], u[0][1]), pack2(u[1][0], u[1][1]));
+            mma16816(dpp[1], ao, pack2(u[0][2], u[0][3]), pack2(u[1][2], u[1][3]));
+            // dU[:, cols] V[:, cols]^T: dU's fragments are the A operand as they are
+            const uint32_t adu[4] = {pack2(du[0][0], du[0][1]), pack2(du[0][2], du[0][3]),
+                                     pack2(du[1][0], du[1][1]), pack2(du[1][2], du[1][3])};
+            uint32_t bv[4];
+            ld_b_nk(V16, PB, 0, n0, bv);       // B[v][t'] = V[t'][v]
+            mma16816(dmp[0], adu, bv[0], bv[1]);
+            mma16816(dmp[1], adu, bv[2], bv[3]);
+            __syncwarp();  // this warp's dU columns are in shared memory
+            uint32_t am[4], bu[4];
+            float dvf[2][4] = {};
+            ld_a_t(M16, PS, 0, 0, am);         // M^T
+            ld_b_kn(DU16, PB, 0, n0, bu);
+            mma16816(dvf[0], am, bu[0], bu[1]);
+            mma16816(dvf[1], am, bu[2], bu[3]);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = g4 + 8 * hh;
+                    if (t < L)
+                        *reinterpret_cast<uint32_t *>(
+                            dv_out + ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4) =
+                            pack2(dvf[tt][2 * hh], dvf[tt][2 * hh + 1]);
+                }
+        }
+        __syncthreads();  // U and dU complete
+
+        // ---- phase 2 (key channels [n0, n0 + 16)): dQ~ = s dO S^T, dK' = U dS_end^T,
+        // dW = -dU S^T, dgamma_L = diag(dS_end S^T); dW K~^T into the dM partial sum
+        float dqa[2][4] = {}, dkp[2][4] = {}, dwa[2][4] = {}, dga[2][4] = {};
+#pragma unroll 2
+        for (int k0 = 0; k0 < D; k0 += 16) {  // k = value column
+            uint32_t ao[4], au[4], adu[4], ads[4], bs[4], bd[4];
+            ld_a(DO, PB, k0, ao);
+            ld_a(U16, PB, k0, au);
+            ld_a(DU16, PB, k0, adu);
+            ld_b_kn(SB, PB, k0, n0, bs);       // B[v][key] = S^T tile [v][key]
+            ld_b_kn(DSB, PB, k0, n0, bd);
+            ld_a_t(DSB, PB, k0, n0, ads);      // A[key][v] = dS_end[key][v]
+            mma16816(dqa[0], ao, bs[0], bs[1]);
+            mma16816(dqa[1], ao, bs[2], bs[3]);
+            mma16816(dkp[0], au, bd[0], bd[1]);
+            mma16816(dkp[1], au, bd[2], bd[3]);
+            mma16816(dwa[0], adu, bs[0], bs[1]);
+            mma16816(dwa[1], adu, bs[2], bs[3]);
+            mma16816(dga[0], ads, bs[0], bs[1]);
+            mma16816(dga[1], ads, bs[2], bs[3]);
+        }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dqa[tt][i] *= scale;
+                dwa[tt][i] = -dwa[tt][i];
+            }
+        // dgamma_L: the diagonal of dga sits on lanes g4 >> 1 == l4; lane 9 l4 holds keys
+        // n0 + 2 l4 and n0 + 8 + 2 l4, lane 9 l4 + 4 the keys one above
+        float dgl[2][2];
+        {
+            const float d0 = (g4 & 1) ? dga[0][1] : dga[0][0];
+            const float d1 = (g4 & 1) ? dga[1][3] : dga[1][2];
+            dgl[0][0] = __shfl_sync(0xffffffffu, d0, 9 * l4);
+            dgl[0][1] = __shfl_sync(0xffffffffu, d0, 9 * l4 + 4);
+            dgl[1][0] = __shfl_sync(0xffffffffu, d1, 9 * l4);
+            dgl[1][1] = __shfl_sync(0xffffffffu, d1, 9 * l4 + 4);
+        }
+        {
+            const uint32_t aw[4] = {pack2(dwa[0][0], dwa[0][1]), pack2(dwa[0][2], dwa[0][3]),
+                                    pack2(dwa[1][0], dwa[1][1]), pack2(dwa[1][2], dwa[1][3])};
+            uint32_t bk[4];
+            ld_b_nk(KT, PB, 0, n0, bk);        // B[key][t'] = K~[t'][key]
+            mma16816(dmp[0], aw, bk[0], bk[1]);
+            mma16816(dmp[1], aw, bk[2], bk[3]);
+            store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_DW), PB, n0, dwa);
+            float *pw = part + warp * 2 * C * C;  // summed in warp order (deterministic)
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int e = (g4 + 8 * hh) * C + 8 * tt + 2 * l4;
+                    *reinterpret_cast<float2 *>(pw + e) = make_float2(dmp[tt][2 * hh], dmp[tt][2 * hh + 1]);
+                    *reinterpret_cast<float2 *>(pw + C * C + e) =
+                        make_float2(dpp[tt][2 * hh], dpp[tt][2 * hh + 1]);
+                }
+        }
+        __syncthreads();  // the states' last readers are done; dM and dP sums complete
+        if (more && tid == 0) issue_states(nxt);
+
+        // ---- phase 3: dP = s lower(dO U^T); dT = dM diag(beta), dA = strict_lower(-T^T dT
+        // T^T), dZ = diag(beta) dA; dbeta
+        const float *T = reinterpret_cast<const float *>(R + TR_T);
+        const float *TT = reinterpret_cast<const float *>(R + TR_TT);
+        const float *Z = reinterpret_cast<const float *>(R + TR_Z);
+        const float *BT = reinterpret_cast<const float *>(R + TR_B);
+        {
+            const int r = tid >> 4, j = tid & 15;
+            float dm = 0.f, dp = 0.f;
+#pragma unroll
+            for (int w = 0; w < LT_THREADS / 32; ++w) {
+                dm += part[w * 2 * C * C + tid];
+                dp += part[w * 2 * C * C + C * C + tid];
+            }
+            dP16[r * PS + j] = __float2bfloat16_rn(j <= r ? scale * dp : 0.f);
+            dTs[tid] = dm * BT[j];
+            dMs[tid] = dm;
+        }
+        __syncthreads();
+        {
+            const int r = tid >> 4, j = tid & 15;
+            float y = 0.f;
+#pragma unroll
+            for (int l = 0; l < C; ++l) y = fmaf(dTs[r * C + l], TT[l * C + j], y);  // (dT T^T)_rj
+            Ys[tid] = y;
+            if (tid < C) {  // dbeta from M = T diag(beta)
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < C; ++i) acc = fmaf(dMs[i * C + tid], T[i * C + tid], acc);
+                dbs[tid] = acc;
+            }
+        }
+        __syncthreads();
+        {
+            const int r = tid >> 4, j = tid & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int l = 0; l < C; ++l) acc = fmaf(T[l * C + r], Ys[l * C + j], acc);
+            const float dA = j < r ? -acc : 0.f;
+            dZ16[r * PS + j] = __float2bfloat16_rn(BT[r] * dA);
+            float x = dA * Z[tid];  // dbeta from A = strict_lower(diag(beta) Z)
+#pragma unroll
+            for (int o = 1; o < C; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (j == 0 && r < L) dbeta[(size_t)(c0 + r) * H + h] = dbs[r] + x;
+        }
+        __syncthreads();  // dP, dZ complete
+
+        // ---- phase 4 (key channels [n0, n0 + 16)): dQ~ += dP K^, dK~ = M^T dW + dZ K^,
+        // dK^ = dP^T Q~ + dZ^T K~; then dq, dk and da on the fragments
+        uint32_t qv[2][2], kv[2][2];
+        float2 av[2][2];
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = g4 + 8 * hh;
+                qv[tt][hh] = kv[tt][hh] = 0u;
+                av[tt][hh] = make_float2(0.f, 0.f);
+                if (t < L) {
+                    const size_t o = ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4;
+                    qv[tt][hh] = *reinterpret_cast<const uint32_t *>(q + o);
+                    kv[tt][hh] = *reinterpret_cast<const uint32_t *>(k + o);
+                    av[tt][hh] = *reinterpret_cast<const float2 *>(a + o);
+                }
+            }
+        float dkt[2][4] = {}, dkh[2][4] = {};
+        {
+            uint32_t bkh[4], bb[4], af[4];
+            ld_b_kn(KH, PB, 0, n0, bkh);       // B[t'][key] = K^[t'][key]
+            ld_a(DP, PS, 0, af);               // dP
+            mma16816(dqa[0], af, bkh[0], bkh[1]);
+            mma16816(dqa[1], af, bkh[2], bkh[3]);
+            ld_a(DZ, PS, 0, af);               // dZ
+            mma16816(dkt[0], af, bkh[0], bkh[1]);
+            mma16816(dkt[1], af, bkh[2], bkh[3]);
+            ld_a_t(M16, PS, 0, 0, af);         // M^T
+            ld_b_kn(DW16, PB, 0, n0, bb);      // B[t'][key] = dW[t'][key]
+            mma16816(dkt[0], af, bb[0], bb[1]);
+            mma16816(dkt[1], af, bb[2], bb[3]);
+            ld_a_t(DP, PS, 0, 0, af);          // dP^T
+            ld_b_kn(QT, PB, 0, n0, bb);
+            mma16816(dkh[0], af, bb[0], bb[1]);
+            mma16816(dkh[1], af, bb[2], bb[3]);
+            ld_a_t(DZ, PS, 0, 0, af);          // dZ^T
+            ld_b_kn(KT, PB, 0, n0, bb);
+            mma16816(dkh[0], af, bb[0], bb[1]);
+            mma16816(dkh[1], af, bb[2], bb[3]);
+        }
+        const float *GS = reinterpret_cast<const float *>(R + TR_GS);
+        const float *GLv = reinterpret_cast<const float *>(R + TR_GL);
+        float dG[2][4], kps[2][2] = {};
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = g4 + 8 * hh, key = n0 + 8 * tt + 2 * l4;
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qv[tt][hh]));
+                const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kv[tt][hh]));
+                float oq[2], ok2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int fi = 2 * hh + e;
+                    const float G = GS[t * GP + key + e], GL = GS[(C - 1) * GP + key + e];
+                    const float eg = expf(G), en = expf(-G), ep = expf(GL - G);
+                    const float qx = e ? qf.y : qf.x, kx = e ? kf.y : kf.x;
+                    const float Qt = qx * eg, Kt = kx * eg, Kh = kx * en, Kp = kx * ep;
+                    const float gq = dqa[tt][fi], gt = dkt[tt][fi], gh = dkh[tt][fi], gp = dkp[tt][fi];
+                    oq[e] = gq * eg;
+                    ok2[e] = gt * eg + gh * en + gp * ep;
+                    dG[tt][fi] = gq * Qt + gt * Kt - gh * Kh - gp * Kp;
+                    kps[tt][e] += gp * Kp;
+                }
+                if (t < L) {
+                    const size_t o = ((size_t)(c0 + t) * H + h) * D + key;
+                    *reinterpret_cast<uint32_t *>(dq + o) = pack2(oq[0], oq[1]);
+                    *reinterpret_cast<uint32_t *>(dk_out + o) = pack2(ok2[0], ok2[1]);
+                }
+            }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float x = kps[tt][e];  // colsum over the 16 rows of dK' K'
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                const int key = n0 + 8 * tt + 2 * l4 + e;
+                if (g4 == 7) dG[tt][2 + e] += GLv[key] * dgl[tt][e] + x;  // row 15
+                // reverse cumulative sum over the rows: g4 + 8 (hi), then g4 (lo)
+                float hi = dG[tt][2 + e], lo = dG[tt][e];
+#pragma unroll
+                for (int d = 1; d < 8; d <<= 1) {
+                    const float yh = __shfl_down_sync(0xffffffffu, hi, 4 * d);
+                    const float yl = __shfl_down_sync(0xffffffffu, lo, 4 * d);
+                    if (g4 + d < 8) {
+                        hi += yh;
+                        lo += yl;
+                    }
+                }
+                lo += __shfl_sync(0xffffffffu, hi, l4);
+                dG[tt][2 + e] = hi;
+                dG[tt][e] = lo;
+            }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = g4 + 8 * hh;
+                if (t < L) {
+                    const float2 ax = av[tt][hh];
+                    const float s0 = 1.f / (1.f + expf(-ax.x)), s1 = 1.f / (1.f + expf(-ax.y));
+                    const size_t o = ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4;
+                    *reinterpret_cast<float2 *>(da + o) =
+                        make_float2(dG[tt][2 * hh] * (kGMin * s0 * (1.f - s0)),
+                                    dG[tt][2 * hh + 1] * (kGMin * s1 * (1.f - s1)));
+                }
+            }
+        idx = nidx;
+        cur = nxt;
+    }
+}
+
 template <typename IO>
 cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const int H = p.n_heads, dk = p.d_k, dv = p.d_v;
@@ -1281,21 +1598,15 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const size_t sm0 = chunk_floats(dk, dv) * 4;
     const size_t sm1 = ((size_t)2 * stage_floats(dk) + (size_t)RG * C * JS + C * JS) * 4;
     const size_t sm2 = sm1 + (size_t)C * JS * 4;
-    // the local gradients on the tensor cores for bf16 I/O at d_k = d_v = 128 (bf16 operand
-    // rounding is within that I/O's precision); fp32 FMA loops otherwise
-    constexpr bool kBf16 = sizeof(IO) == 2;
-    const bool use_mma = kBf16 && dk == 128 && dv == 128;
-    const size_t sm3 = local_floats(dk, dv, use_mma) * 4;
-    // the serial passes on the tensor cores too when the bulk copies' 16-byte alignment
-    // holds (workspace records, s dO rows)
-    const bool use_tc = use_mma && ((uintptr_t)p.workspace & 15u) == 0 &&
-                        ((uintptr_t)p.dout & 15u) == 0;
-    auto local = use_mma ? local_kernel<IO, kBf16> : local_kernel<IO, false>;
+    const size_t sm3 = local_floats(dk, dv) * 4;
+    // bf16 I/O at d_k = d_v = 128 runs on the tensor cores (bf16 operand rounding is within
+    // that I/O's precision) when the bulk copies' 16-byte alignment holds; fp32 FMA loops
+    // otherwise
+    auto al16 = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
+    const bool use_tc = sizeof(IO) == 2 && dk == 128 && dv == 128 && al16(p.workspace) &&
+                        al16(p.q) && al16(p.k) && al16(p.v) && al16(p.a) && al16(p.dout);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess)
         return e;
     // the chunks of a sequence spread over gridDim.y CTAs: a few per SM over the launch,
     // so uneven sequences balance
@@ -1305,26 +1616,46 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     if (gy < 1) gy = 1;
     if (gy > 65535) gy = 65535;
     const dim3 par(items, (unsigned)gy), cols(items, (unsigned)((dv + JS - 1) / JS));
+    unsigned char *wsb = use_tc ? reinterpret_cast<unsigned char *>(p.workspace) : nullptr;
     prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
-                                                   use_tc, H, dk, dv);
-    if (use_tc) {  // the serial passes on the tensor cores, state in registers
+                                                   wsb, H, dk, dv);
+    if (use_tc) {
+        // serial passes with the state in mma fragments, then the local gradients with one
+        // CTA per SM over all (chunk slot, head) items
         const int smc = NS * SLOT;
+        int dev = 0, sms = 0;
         if ((e = cudaFuncSetAttribute(chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess)
+            (e = cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LS_BYTES)) != cudaSuccess ||
+            (e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
         const __nv_bfloat16 *d16 = reinterpret_cast<const __nv_bfloat16 *>(p.dout);
-        chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, prep, d16, p.h0, ck,
+        chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0,
                                                                 nullptr, H, scale);
-        chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, prep, d16, p.dh_final,
-                                                               dck, p.dh0, H, scale);
+        chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.dh_final,
+                                                               p.dh0, H, scale);
+        const long long n_items = ((long long)(p.n_tok >> 4) + p.n_seq) * H;
+        const int grid = (int)(n_items < sms ? n_items : sms);
+        const __nv_bfloat16 *b16[3] = {reinterpret_cast<const __nv_bfloat16 *>(p.q),
+                                       reinterpret_cast<const __nv_bfloat16 *>(p.k),
+                                       reinterpret_cast<const __nv_bfloat16 *>(p.v)};
+        local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
+            b16[0], b16[1], b16[2], p.a, p.cu_seqlens, d16, wsb,
+            reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
+            reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
     } else {
-    ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
-    chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep, dck,
-                                                     p.dh0, H, dk, dv, scale);
+        if ((e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
+            return e;
+        ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
+        chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep,
+                                                         dck, p.dh0, H, dk, dv, scale);
+        local_kernel<IO><<<par, kThreads, sm3, stream>>>(
+            q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk,
+            (IO *)p.dv, p.da, p.dbeta, H, dk, dv, scale);
     }
-    local<<<par, kThreads, sm3, stream>>>(
-        q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk, (IO *)p.dv,
-        p.da, p.dbeta, H, dk, dv, scale);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(4);
     return e;
