@@ -260,7 +260,7 @@ __host__ __device__ constexpr size_t P_GL(int dk, int dv) { return P_P(dk, dv) +
 // REC_TC bytes -- the chunk's start state S and end-state gradient dS_end as bf16 S^T
 // tiles [128 v][136] (written by the two serial passes in the row layout shared memory
 // uses), then the prep kernel's record of the chunk's state-independent products:
-//   K', -W, Q~ bf16 [16][136]; P bf16 [16][24]; gamma_L fp32 in the serial passes' float4
+//   K', -W, s Q~ bf16 [16][136]; s P bf16 [16][24]; gamma_L fp32 in the serial passes' float4
 //   order (the part [0, TR_OPS) is what the serial passes copy); U~^T fp32 [128 v][16 t];
 //   K~, K^ bf16 [16][136]; M bf16 [16][24]; T, T^T, Z fp32 [16][16]; beta fp32 [16];
 //   G fp32 [16][136]; gamma_L fp32 [128].
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads)
     prep_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                 const float *__restrict__ a, const float *__restrict__ beta,
                 const int32_t *__restrict__ cu, float *__restrict__ prep,
-                unsigned char *__restrict__ tc, int H, int dk, int dv) {
+                int H, int dk, int dv) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x, lk = dk + 1, lv = dv + 1;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
         prologue(b, q, k, v, a, beta, c0, L, H, h, dk, dv, true);
-        if (!tc) {
+        {
             float *o = prep + (slot_of(cu, n, c) * H + h) * rec;
             for (int i = tid; i < C * dk; i += kThreads) {
                 const int r = i / dk, x = i % dk;
@@ -319,44 +319,6 @@ __global__ void __launch_bounds__(kThreads)
                 o[P_UT(dk) + i] = b.Ut[(i / dv) * lv + i % dv];
             o[P_P(dk, dv) + tid] = b.P[tid];  // kThreads == C * C
             for (int x = tid; x < dk; x += kThreads) o[P_GL(dk, dv) + x] = b.gl[x];
-        } else {  // d_k = d_v = 128: the tensor-core record
-            unsigned char *tr = tc + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
-            __nv_bfloat16 *tk = reinterpret_cast<__nv_bfloat16 *>(tr + TR_K);
-            __nv_bfloat16 *tw = reinterpret_cast<__nv_bfloat16 *>(tr + TR_W);
-            __nv_bfloat16 *tq = reinterpret_cast<__nv_bfloat16 *>(tr + TR_Q);
-            __nv_bfloat16 *tkt = reinterpret_cast<__nv_bfloat16 *>(tr + TR_KT);
-            __nv_bfloat16 *tkh = reinterpret_cast<__nv_bfloat16 *>(tr + TR_KH);
-            float *tgs = reinterpret_cast<float *>(tr + TR_GS);
-            for (int i = tid; i < C * 136; i += kThreads) {
-                const int r = i / 136, x = i % 136;
-                const bool in = x < 128;
-                tk[i] = __float2bfloat16_rn(in ? b.Kp[r * lk + x] : 0.f);
-                tw[i] = __float2bfloat16_rn(in ? -b.W[r * lk + x] : 0.f);
-                tq[i] = __float2bfloat16_rn(in ? b.Qt[r * lk + x] : 0.f);
-                tkt[i] = __float2bfloat16_rn(in ? b.Kt[r * lk + x] : 0.f);
-                tkh[i] = __float2bfloat16_rn(in ? b.Kh[r * lk + x] : 0.f);
-                tgs[i] = in ? b.Gs[r * lk + x] : 0.f;
-            }
-            __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(tr + TR_P);
-            __nv_bfloat16 *tm = reinterpret_cast<__nv_bfloat16 *>(tr + TR_M);
-            for (int i = tid; i < C * 24; i += kThreads) {
-                const bool in = i % 24 < C;
-                tp[i] = __float2bfloat16_rn(in ? b.P[(i / 24) * C + i % 24] : 0.f);
-                tm[i] = __float2bfloat16_rn(in ? b.M[(i / 24) * C + i % 24] : 0.f);
-            }
-            // kThreads == C * C
-            reinterpret_cast<float *>(tr + TR_T)[tid] = b.T[tid];
-            reinterpret_cast<float *>(tr + TR_TT)[tid] = b.T[(tid % C) * C + tid / C];
-            reinterpret_cast<float *>(tr + TR_Z)[tid] = b.Z[tid];
-            if (tid < C) reinterpret_cast<float *>(tr + TR_B)[tid] = b.bt[tid];
-            for (int x = tid; x < 128; x += kThreads) reinterpret_cast<float *>(tr + TR_GL)[x] = b.gl[x];
-            float *tg = reinterpret_cast<float *>(tr + TR_G);
-            for (int x = tid; x < 128; x += kThreads) tg[gperm_tc(x)] = b.gl[x];
-            float *tu = reinterpret_cast<float *>(tr + TR_UT);  // [r][32 v][16 t]
-            for (int i = tid; i < 128 * C; i += kThreads) {
-                const int v = i / C, t = i % C;
-                tu[i] = b.Ut[t * lv + v];
-            }
         }
     }
 }
@@ -658,13 +620,13 @@ __global__ void __launch_bounds__(kThreads)
 // a warp's rows of the state A = S^T as bf16 A fragments (mma.sync m16n8k16):
 //   forward:  write S^T (the chunk's start state); U^T = U~^T + S^T (-W)^T;
 //             S^T <- S^T Diag(gamma_L) + U^T K'
-//   reverse:  write dS^T (the gradient at the chunk's end); X^T = dS^T K'^T + (s dO)^T P;
-//             dS^T <- dS^T Diag(gamma_L) + (s dO)^T Q~ + X^T (-W)
+//   reverse:  write dS^T (the gradient at the chunk's end); X^T = dS^T K'^T + dO^T (s P);
+//             dS^T <- dS^T Diag(gamma_L) + dO^T (s Q~) + X^T (-W)
 // the transposed forms of the two chains above, the state an fp32 accumulator throughout.
 constexpr int NS = 4;                    // ring slots
-constexpr int PO = 40;                   // bf16 pitch of the [16][32] (s dO) slice (80-byte rows)
+constexpr int PO = 40;                   // bf16 pitch of the [16][32] dO slice (80-byte rows)
 // slot layout (bytes): the record's operand part [0, TR_OPS) (K', -W, Q~, P, gamma_L), then
-// U~^T [32][16] fp32 (forward) or (s dO) [16][PO] bf16 (reverse)
+// U~^T [32][16] fp32 (forward) or dO [16][PO] bf16 (reverse)
 constexpr int SL_K = TR_K, SL_W = TR_W, SL_Q = TR_Q, SL_P = TR_P, SL_G = TR_G, SL_X = TR_OPS;
 constexpr int SLOT = SL_X + 32 * C * 4;
 static_assert(SL_X % 16 == 0 && SLOT % 16 == 0, "16-byte aligned slot parts");
@@ -737,7 +699,7 @@ __global__ void __launch_bounds__(128, 1)
     auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            bar_init(full(s), REVERSE ? 2 : 1);  // the copies' issue (+ the s dO tile)
+            bar_init(full(s), 1);   // the copies' issue
             bar_init(empty(s), 2);  // one arrival per chain warp
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -753,38 +715,29 @@ __global__ void __launch_bounds__(128, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
             const unsigned char *tr = ws + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
-            if (lane == 0) {
-                if (REVERSE) {  // K', -W, Q~, P, gamma_L
-                    bar_arrive_tx(full(s), TR_OPS);
-                    bulk_g2s(sl, tr, TR_OPS, full(s));
-                } else {        // K', -W; gamma_L; this CTA's block of U~^T
-                    bar_arrive_tx(full(s), 2 * T128 + 128 * 4 + 32 * C * 4);
-                    bulk_g2s(sl + SL_K, tr + TR_K, 2 * T128, full(s));
-                    bulk_g2s(sl + SL_G, tr + TR_G, 128 * 4, full(s));
-                    bulk_g2s(sl + SL_X, tr + TR_UT + r4 * 32 * C * 4, 32 * C * 4, full(s));
+            if (REVERSE) {  // K', -W, s Q~, s P, gamma_L; the dO rows of the CTA's 32 columns
+                const int64_t c0 = t0 + (int64_t)c * C;
+                const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
+                if (L < C) {  // rows past the sequence's end read as zeros
+                    for (int i = lane; i < (C - L) * 4; i += 32)
+                        *reinterpret_cast<uint4 *>(smc + s * SLOT + SL_X + (L + i / 4) * PO * 2 + (i % 4) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-            }
-            if (REVERSE) {  // s dO, the CTA's 32 columns, as bf16 [16][PO]: a half row per lane
-                const int rr = lane >> 1, j0 = 16 * (lane & 1);
-                const int64_t tok = t0 + (int64_t)c * C + rr;
-                uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
-                if (tok < t1) {
-                    const uint4 *src =
-                        reinterpret_cast<const uint4 *>(dout + ((size_t)tok * H + h) * D + v0 + j0);
-                    x0 = src[0];
-                    x1 = src[1];
-                }
-                uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
-                    w[i] = pack2(scale * f.x, scale * f.y);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(smc + s * SLOT + SL_X + rr * PO * 2 + j0 * 2);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 __syncwarp();
-                if (lane == 0) bar_arrive(full(s));  // release: the s dO tile is written
+                if (lane == 0) {
+                    bar_arrive_tx(full(s), TR_OPS + L * 64);
+                    bulk_g2s(sl, tr, TR_OPS, full(s));
+                }
+                __syncwarp();
+                if (lane < L)
+                    bulk_g2s(sl + SL_X + lane * PO * 2, dout + ((size_t)(c0 + lane) * H + h) * D + v0, 64,
+                             full(s));
+            } else if (lane == 0) {  // K', -W; gamma_L; this CTA's block of U~^T
+                bar_arrive_tx(full(s), 2 * T128 + 128 * 4 + 32 * C * 4);
+                bulk_g2s(sl + SL_K, tr + TR_K, 2 * T128, full(s));
+                bulk_g2s(sl + SL_G, tr + TR_G, 128 * 4, full(s));
+                bulk_g2s(sl + SL_X, tr + TR_UT + r4 * 32 * C * 4, 32 * C * 4, full(s));
             }
         }
         return;
@@ -847,7 +800,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
         }
-        // (s dO)^T as the A fragment (reverse): 16 value rows x 16 tokens, read transposed
+        // dO^T as the A fragment (reverse): 16 value rows x 16 tokens, read transposed
         uint32_t oa[4] = {0u, 0u, 0u, 0u};
         if (REVERSE)
             ldsm4t(sl + SL_X + (uint32_t)((((i8 >> 1) * 8 + r8) + 0) * PO * 2 + (16 * sw + (i8 & 1) * 8) * 2), oa);
@@ -864,7 +817,7 @@ __global__ void __launch_bounds__(128, 1)
             mma16816(acc[0], a, bfr[0], bfr[1]);
             mma16816(acc[1], a, bfr[2], bfr[3]);
         }
-        if (REVERSE) {  // + (s dO)^T P: B[k = token i][n = token r] = P[i][r], [k][n] storage
+        if (REVERSE) {  // + dO^T (s P): B[k = token i][n = token r] = s P[i][r], [k][n] storage
             uint32_t bfr[4];
             ld_b_kn(sl + SL_P, PS, 0, 0, bfr);
             mma16816(acc[0], oa, bfr[0], bfr[1]);
@@ -887,7 +840,7 @@ __global__ void __launch_bounds__(128, 1)
             ld_b_kn(sl + (REVERSE ? SL_W : SL_K), PB, 0, 16 * np, bfr);
             mma16816(S[2 * np], ua, bfr[0], bfr[1]);
             mma16816(S[2 * np + 1], ua, bfr[2], bfr[3]);
-            if (REVERSE) {  // + (s dO)^T Q~
+            if (REVERSE) {  // + dO^T (s Q~)
                 ld_b_kn(sl + SL_Q, PB, 0, 16 * np, bfr);
                 mma16816(S[2 * np], oa, bfr[0], bfr[1]);
                 mma16816(S[2 * np + 1], oa, bfr[2], bfr[3]);
@@ -1147,7 +1100,8 @@ constexpr int RBUF = RECB + 2 * T128;  // record, then V and dO rows [16][136] b
 constexpr int LS_S = 0, LS_DS = ST16, LS_R = 2 * ST16;
 constexpr int LS_U = LS_R + 2 * RBUF, LS_DU = LS_U + T128, LS_DW = LS_DU + T128;
 constexpr int LS_DP = LS_DW + T128, LS_DZ = LS_DP + C * PS * 2;
-constexpr int LS_PART = LS_DZ + C * PS * 2;  // per warp: dM, dP partial sums [2][16][16]
+constexpr int LS_DPU = LS_DZ + C * PS * 2;  // dP / s: the partner of the record's s Q~
+constexpr int LS_PART = LS_DPU + C * PS * 2;  // per warp: dM, dP partial sums [2][16][16]
 constexpr int LS_DT = LS_PART + 8 * 2 * C * C * 4, LS_DMS = LS_DT + C * C * 4, LS_Y = LS_DMS + C * C * 4;
 constexpr int LS_DB = LS_Y + C * C * 4;
 constexpr int LS_BYTES = LS_DB + C * 4;
@@ -1172,6 +1126,16 @@ __device__ bool decode_item(const int32_t *cu, int n_seq, int H, long long idx, 
     it.c = (int)(slot - ((long long)(cu[lo] >> 4) + lo));
     return it.c < (cu[lo + 1] - cu[lo] + C - 1) / C;
 }
+__device__ long long next_valid_item(const int32_t *cu, int n_seq, int H, long long i, long long end,
+                                     Item &it) {
+    while (i < end && !decode_item(cu, n_seq, H, i, it)) ++i;
+    return i;
+}
+__device__ __forceinline__ int item_rows(const int32_t *cu, const Item &it, int64_t &c0) {
+    c0 = cu[it.n] + (int64_t)it.c * C;
+    const int64_t left = cu[it.n + 1] - c0;
+    return (int)(left < C ? left : C);
+}
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
     local_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -1195,21 +1159,15 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     float *Ys = reinterpret_cast<float *>(sl + LS_Y), *dbs = reinterpret_cast<float *>(sl + LS_DB);
     __nv_bfloat16 *dP16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DP);
     __nv_bfloat16 *dZ16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DZ);
+    __nv_bfloat16 *dPu16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DPU);
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) bar_init(bar(i), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    auto next_valid = [&](long long i, Item &it) {
-        while (i < end && !decode_item(cu, n_seq, H, i, it)) ++i;
-        return i;
-    };
-    auto rows_of = [&](const Item &it, int64_t &c0) {
-        c0 = cu[it.n] + (int64_t)it.c * C;
-        const int64_t left = cu[it.n + 1] - c0;
-        return (int)(left < C ? left : C);
-    };
+    auto next_valid = [&](long long i, Item &it) { return next_valid_item(cu, n_seq, H, i, end, it); };
+    auto rows_of = [&](const Item &it, int64_t &c0) { return item_rows(cu, it, c0); };
     auto rec_of = [&](const Item &it) {
         return ws + (slot_of(cu, it.n, it.c) * H + it.h) * REC_TC;
     };
@@ -1289,7 +1247,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         const uint32_t KT = rbase + TR_KT, KH = rbase + TR_KH, M16 = rbase + TR_M;
         const uint32_t V16 = rbase + RECB, DO = rbase + RECB + T128;
         const uint32_t U16 = sb + LS_U, DU16 = sb + LS_DU, DW16 = sb + LS_DW;
-        const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ;
+        const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ, DPU = sb + LS_DPU;
 
         // ---- phase 1 (value columns [n0, n0 + 16)): U = U~ - W S, dU = K' dS_end + s P^T dO,
         // dV = M^T dU; partial sums of dO U^T and dU V^T over these columns
@@ -1318,14 +1276,14 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             }
             uint32_t ap[4], bo[4];
             float pd[2][4] = {};
-            ld_a_t(P16, PS, 0, 0, ap);         // P^T
+            ld_a_t(P16, PS, 0, 0, ap);         // (s P)^T
             ld_b_kn(DO, PB, 0, n0, bo);        // B[i][v] = dO[i][v]
             mma16816(pd[0], ap, bo[0], bo[1]);
             mma16816(pd[1], ap, bo[2], bo[3]);
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) du[tt][i] = fmaf(scale, pd[tt][i], du[tt][i]);
+                for (int i = 0; i < 4; ++i) du[tt][i] += pd[tt][i];
             store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_U), PB, n0, u);
             store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_DU), PB, n0, du);
             // dO[:, cols] U[:, cols]^T: U's accumulator fragments are the B operand as they are
@@ -1436,6 +1394,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                 dp += part[w * 2 * C * C + C * C + tid];
             }
             dP16[r * PS + j] = __float2bfloat16_rn(j <= r ? scale * dp : 0.f);
+            dPu16[r * PS + j] = __float2bfloat16_rn(j <= r ? dp : 0.f);
             dTs[tid] = dm * BT[j];
             dMs[tid] = dm;
         }
@@ -1500,7 +1459,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             ld_b_kn(DW16, PB, 0, n0, bb);      // B[t'][key] = dW[t'][key]
             mma16816(dkt[0], af, bb[0], bb[1]);
             mma16816(dkt[1], af, bb[2], bb[3]);
-            ld_a_t(DP, PS, 0, 0, af);          // dP^T
+            ld_a_t(DPU, PS, 0, 0, af);         // (dP / s)^T against s Q~
             ld_b_kn(QT, PB, 0, n0, bb);
             mma16816(dkh[0], af, bb[0], bb[1]);
             mma16816(dkh[1], af, bb[2], bb[3]);
@@ -1583,6 +1542,282 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     }
 }
 
+// ---- 0b. the tensor-core record (bf16 I/O, d_k = d_v = 128)
+// Two CTAs per SM walk contiguous ranges of items (chunk slot, head). Per item: the q, k, v
+// and gate-logit rows arrive by bulk copies one item ahead (double-buffered); G and gamma_L
+// per key channel; Q~, K~, K^, K' elementwise; Z = K~ K^^T and P = Q~ K^^T on the tensor
+// cores with each operand split into a bf16 high and low part (hi hi + lo hi + hi lo: close
+// to fp32 products); T = (I + A)^-1 by forward substitution on one warp; W = M K~ and
+// U~ = M V with M split the same way. The record is assembled in shared memory in its
+// global layout and written by one bulk copy.
+constexpr int PT_THREADS = 256;
+constexpr int IBUF = 3 * T128 + C * 128 * 4;  // q, k, v rows [16][136] bf16; a rows [16][128] fp32
+constexpr int PS_REC = 2 * IBUF;
+constexpr int PS_QH = PS_REC + RECB, PS_QL = PS_QH + T128, PS_KTL = PS_QL + T128;
+constexpr int PS_KHL = PS_KTL + T128, PS_A = PS_KHL + T128, PS_ML = PS_A + C * C * 4;
+constexpr int PS_BT = PS_ML + C * PS * 2;
+constexpr int PS_BYTES = PS_BT + C * 4;
+static_assert(IBUF % 16 == 0 && PS_QH % 16 == 0 && PS_A % 16 == 0 && 2 * (PS_BYTES + 1024) <= 228 * 1024,
+              "two prep CTAs per SM");
+
+// hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack2(x0, x1);
+    const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi));
+    lo = pack2(x0 - h.x, x1 - h.y);
+}
+
+__global__ void __launch_bounds__(PT_THREADS, 2)
+    prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                   const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
+                   const float *__restrict__ beta, const int32_t *__restrict__ cu,
+                   unsigned char *__restrict__ ws, int H, int n_seq, long long n_items,
+                   float scale) {
+    constexpr int D = 128;
+    extern __shared__ __align__(128) unsigned char sp[];
+    __shared__ __align__(8) unsigned long long bars[2];  // input buffers 0, 1
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, l4 = lane & 3, n0 = 16 * warp;
+    const long long beg = (long long)blockIdx.x * n_items / gridDim.x;
+    const long long end = (long long)(blockIdx.x + 1) * n_items / gridDim.x;
+    const uint32_t sb = static_cast<uint32_t>(__cvta_generic_to_shared(sp));
+    auto bar = [&](int i) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[i])); };
+    unsigned char *rec = sp + PS_REC;
+    float *As = reinterpret_cast<float *>(sp + PS_A), *bts = reinterpret_cast<float *>(sp + PS_BT);
+    if (tid == 0) {
+        bar_init(bar(0), 1);
+        bar_init(bar(1), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // warp 0: the q, k, v and gate-logit rows of item it into input buffer b
+    auto issue_in = [&](const Item &it, int b) {
+        int64_t c0;
+        const int L = item_rows(cu, it, c0);
+        unsigned char *buf = sp + b * IBUF;
+        const uint32_t bb = sb + b * IBUF;
+        if (L < C) {  // rows past the sequence's end read as zeros
+            const int pt = (C - L) * (T128 / C / 16), pa = (C - L) * (D * 4 / 16);
+            for (int i = lane; i < 3 * pt + pa; i += 32) {
+                unsigned char *dst = i < 3 * pt
+                                         ? buf + (i / pt) * T128 + L * (T128 / C) + (i % pt) * 16
+                                         : buf + 3 * T128 + L * D * 4 + (i - 3 * pt) * 16;
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) bar_arrive_tx(bar(b), (uint32_t)(L * (3 * D * 2 + D * 4)));
+        __syncwarp();
+        for (int i = lane; i < 4 * L; i += 32) {
+            const int t = i / L, r = i % L;
+            const size_t o = ((size_t)(c0 + r) * H + it.h) * D;
+            if (t < 3)
+                bulk_g2s(bb + t * T128 + r * (T128 / C), (t == 0 ? q : t == 1 ? k : v) + o, D * 2, bar(b));
+            else
+                bulk_g2s(bb + 3 * T128 + r * D * 4, a + o, D * 4, bar(b));
+        }
+    };
+
+    Item cur, nxt;
+    long long idx = next_valid_item(cu, n_seq, H, beg, end, cur);
+    if (idx < end && warp == 0) issue_in(cur, 0);
+    for (int m = 0; idx < end; ++m) {
+        const long long nidx = next_valid_item(cu, n_seq, H, idx + 1, end, nxt);
+        const bool more = nidx < end;
+        int64_t c0;
+        const int L = item_rows(cu, cur, c0);
+        const int h = cur.h;
+        float bta = 0.f;
+        if (tid < L) bta = beta[(size_t)(c0 + tid) * H + h];
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncthreads();  // the record staging is free; the other input buffer's readers are done
+        if (more && warp == 0) issue_in(nxt, (m + 1) & 1);
+        if (tid < C) {
+            bts[tid] = bta;
+            reinterpret_cast<float *>(rec + TR_B)[tid] = bta;
+        }
+        const int ib = m & 1;
+        const bool ok = bar_wait(bar(ib), (uint32_t)((m >> 1) & 1));
+        if (__syncthreads_or(!ok)) break;
+        const unsigned char *in = sp + ib * IBUF;
+        const uint32_t inb = sb + ib * IBUF;
+        float *GS = reinterpret_cast<float *>(rec + TR_GS);
+
+        // ---- G = cumsum of g = -5 sigmoid(a) per key channel, gamma_L = e^{G_15}
+        if (tid < D) {
+            const float *Ain = reinterpret_cast<const float *>(in + 3 * T128);
+            float G = 0.f;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float g = r < L ? kGMin / (1.f + expf(-Ain[r * D + tid])) : 0.f;
+                G += g;
+                GS[r * GP + tid] = G;
+            }
+            const float gl = expf(G);
+            reinterpret_cast<float *>(rec + TR_GL)[tid] = gl;
+            reinterpret_cast<float *>(rec + TR_G)[gperm_tc(tid)] = gl;
+        }
+        __syncthreads();
+
+        // ---- Q~ = q e^G, K~ = k e^G, K^ = k e^-G, K' = k e^{G_15 - G}: 8 channels per thread
+        {
+            const int r = tid >> 4, x0 = (tid & 15) * 8;
+            const uint4 qr = *reinterpret_cast<const uint4 *>(in + (r * 136 + x0) * 2);
+            const uint4 kr = *reinterpret_cast<const uint4 *>(in + T128 + (r * 136 + x0) * 2);
+            const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w}, kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            uint32_t okp[4], osq[4], okt[4], okh[4], oqh[4], oql[4], oktl[4], okhl[4];
+#pragma unroll
+            for (int p2 = 0; p2 < 4; ++p2) {
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[p2]));
+                const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kw[p2]));
+                float Qt[2], Kt[2], Kh[2], Kp[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int x = x0 + 2 * p2 + e;
+                    const float G = GS[r * GP + x], GL = GS[(C - 1) * GP + x];
+                    const float qx = e ? qf.y : qf.x, kx = e ? kf.y : kf.x;
+                    Qt[e] = qx * expf(G);
+                    Kt[e] = kx * expf(G);
+                    Kh[e] = kx * expf(-G);
+                    Kp[e] = kx * expf(GL - G);
+                }
+                okp[p2] = pack2(Kp[0], Kp[1]);
+                osq[p2] = pack2(scale * Qt[0], scale * Qt[1]);
+                split2(Qt[0], Qt[1], oqh[p2], oql[p2]);
+                split2(Kt[0], Kt[1], okt[p2], oktl[p2]);
+                split2(Kh[0], Kh[1], okh[p2], okhl[p2]);
+            }
+            const int off = (r * 136 + x0) * 2;
+            auto st4 = [&](unsigned char *base, const uint32_t (&w)[4]) {
+                *reinterpret_cast<uint4 *>(base + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            };
+            st4(rec + TR_K, okp);
+            st4(rec + TR_Q, osq);
+            st4(rec + TR_KT, okt);
+            st4(rec + TR_KH, okh);
+            st4(sp + PS_QH, oqh);
+            st4(sp + PS_QL, oql);
+            st4(sp + PS_KTL, oktl);
+            st4(sp + PS_KHL, okhl);
+        }
+        __syncthreads();
+
+        // ---- Z = K~ K^^T (warp 0), P = Q~ K^^T (warp 1), split-bf16 products
+        if (warp < 2) {
+            const uint32_t ah_b = warp == 0 ? sb + PS_REC + TR_KT : sb + PS_QH;
+            const uint32_t al_b = warp == 0 ? sb + PS_KTL : sb + PS_QL;
+            const uint32_t bh_b = sb + PS_REC + TR_KH, bl_b = sb + PS_KHL;
+            float c0a[2][4] = {}, c1a[2][4] = {}, c2a[2][4] = {};
+#pragma unroll
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                uint32_t ah[4], al[4], bh[4], bl[4];
+                ld_a(ah_b, PB, k0, ah);
+                ld_a(al_b, PB, k0, al);
+                ld_b_nk(bh_b, PB, 0, k0, bh);  // B[key][t'] = K^[t'][key]
+                ld_b_nk(bl_b, PB, 0, k0, bl);
+                mma16816(c0a[0], ah, bh[0], bh[1]);
+                mma16816(c0a[1], ah, bh[2], bh[3]);
+                mma16816(c1a[0], al, bh[0], bh[1]);
+                mma16816(c1a[1], al, bh[2], bh[3]);
+                mma16816(c2a[0], ah, bl[0], bl[1]);
+                mma16816(c2a[1], ah, bl[2], bl[3]);
+            }
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = g4 + 8 * (i >> 1), j = 8 * tt + 2 * l4 + (i & 1);
+                    const float x = c0a[tt][i] + (c1a[tt][i] + c2a[tt][i]);
+                    if (warp == 0) {
+                        reinterpret_cast<float *>(rec + TR_Z)[r * C + j] = x;
+                        As[r * C + j] = j < r ? bts[r] * x : 0.f;
+                    } else {
+                        reinterpret_cast<__nv_bfloat16 *>(rec + TR_P)[r * PS + j] =
+                            __float2bfloat16_rn(j <= r ? scale * x : 0.f);
+                    }
+                }
+        }
+        __syncthreads();
+
+        // ---- T = (I + A)^-1 by forward substitution, lane j = column j; M = T diag(beta)
+        if (warp == 0) {
+            const int j = lane & 15;
+            float col[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                float x0 = r == j ? 1.f : 0.f, x1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) {
+                    if (i & 1) x1 = fmaf(-As[r * C + i], col[i], x1);
+                    else x0 = fmaf(-As[r * C + i], col[i], x0);
+                }
+                col[r] = x0 + x1;
+            }
+            if (lane < C) {
+                float *Tr = reinterpret_cast<float *>(rec + TR_T);
+                float *TTr = reinterpret_cast<float *>(rec + TR_TT);
+                __nv_bfloat16 *Mh = reinterpret_cast<__nv_bfloat16 *>(rec + TR_M);
+                __nv_bfloat16 *Ml = reinterpret_cast<__nv_bfloat16 *>(sp + PS_ML);
+                const float bj = bts[j];
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    Tr[r * C + j] = col[r];
+                    TTr[j * C + r] = col[r];
+                    const float mv = col[r] * bj;
+                    const __nv_bfloat16 mh = __float2bfloat16_rn(mv);
+                    Mh[r * PS + j] = mh;
+                    Ml[r * PS + j] = __float2bfloat16_rn(mv - __bfloat162float(mh));
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- W = M K~ (stored as -W, bf16) and U~ = M V (fp32, transposed): columns [n0, n0 + 16)
+        {
+            uint32_t mh[4], ml[4], bh[4], bl[4], bv[4];
+            ld_a(sb + PS_REC + TR_M, PS, 0, mh);
+            ld_a(sb + PS_ML, PS, 0, ml);
+            ld_b_kn(sb + PS_REC + TR_KT, PB, 0, n0, bh);  // B[t][x] = K~[t][x]
+            ld_b_kn(sb + PS_KTL, PB, 0, n0, bl);
+            ld_b_kn(inb + 2 * T128, PB, 0, n0, bv);      // B[t][v] = V[t][v]
+            float w[2][4] = {}, w2[2][4] = {}, u[2][4] = {}, u2[2][4] = {};
+            mma16816(w[0], mh, bh[0], bh[1]);
+            mma16816(w[1], mh, bh[2], bh[3]);
+            mma16816(w2[0], ml, bh[0], bh[1]);
+            mma16816(w2[1], ml, bh[2], bh[3]);
+            mma16816(w2[0], mh, bl[0], bl[1]);
+            mma16816(w2[1], mh, bl[2], bl[3]);
+            mma16816(u[0], mh, bv[0], bv[1]);
+            mma16816(u[1], mh, bv[2], bv[3]);
+            mma16816(u2[0], ml, bv[0], bv[1]);
+            mma16816(u2[1], ml, bv[2], bv[3]);
+            float *Ut = reinterpret_cast<float *>(rec + TR_UT);  // [v][16 t]
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[tt][i] = -(w[tt][i] + w2[tt][i]);
+                    const int t = g4 + 8 * (i >> 1), vc = n0 + 8 * tt + 2 * l4 + (i & 1);
+                    Ut[vc * C + t] = u[tt][i] + u2[tt][i];
+                }
+            }
+            store_c16(reinterpret_cast<__nv_bfloat16 *>(rec + TR_W), PB, n0, w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the record, to the copy
+        __syncthreads();
+        if (tid == 0) {
+            unsigned char *dst = ws + (slot_of(cu, cur.n, cur.c) * H + h) * REC_TC + TC_REC;
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         ::"l"(dst), "r"(sb + PS_REC), "r"((uint32_t)RECB) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        idx = nidx;
+        cur = nxt;
+    }
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 template <typename IO>
 cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const int H = p.n_heads, dk = p.d_k, dv = p.d_v;
@@ -1616,35 +1851,40 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     if (gy < 1) gy = 1;
     if (gy > 65535) gy = 65535;
     const dim3 par(items, (unsigned)gy), cols(items, (unsigned)((dv + JS - 1) / JS));
-    unsigned char *wsb = use_tc ? reinterpret_cast<unsigned char *>(p.workspace) : nullptr;
-    prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
-                                                   wsb, H, dk, dv);
     if (use_tc) {
         // serial passes with the state in mma fragments, then the local gradients with one
         // CTA per SM over all (chunk slot, head) items
+        unsigned char *wsb = reinterpret_cast<unsigned char *>(p.workspace);
         const int smc = NS * SLOT;
         int dev = 0, sms = 0;
         if ((e = cudaFuncSetAttribute(chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LS_BYTES)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PS_BYTES)) != cudaSuccess ||
             (e = cudaGetDevice(&dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
         const __nv_bfloat16 *d16 = reinterpret_cast<const __nv_bfloat16 *>(p.dout);
+        const long long n_items = ((long long)(p.n_tok >> 4) + p.n_seq) * H;
+        const __nv_bfloat16 *b16[3] = {reinterpret_cast<const __nv_bfloat16 *>(p.q),
+                                       reinterpret_cast<const __nv_bfloat16 *>(p.k),
+                                       reinterpret_cast<const __nv_bfloat16 *>(p.v)};
+        const int pgrid = (int)(n_items < 2 * sms ? n_items : 2 * sms);
+        prep_tc_kernel<<<pgrid, PT_THREADS, PS_BYTES, stream>>>(b16[0], b16[1], b16[2], p.a, p.beta,
+                                                               p.cu_seqlens, wsb, H, p.n_seq,
+                                                               n_items, scale);
         chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0,
                                                                 nullptr, H, scale);
         chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.dh_final,
                                                                p.dh0, H, scale);
-        const long long n_items = ((long long)(p.n_tok >> 4) + p.n_seq) * H;
         const int grid = (int)(n_items < sms ? n_items : sms);
-        const __nv_bfloat16 *b16[3] = {reinterpret_cast<const __nv_bfloat16 *>(p.q),
-                                       reinterpret_cast<const __nv_bfloat16 *>(p.k),
-                                       reinterpret_cast<const __nv_bfloat16 *>(p.v)};
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
             b16[0], b16[1], b16[2], p.a, p.cu_seqlens, d16, wsb,
             reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
             reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
     } else {
+        prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
+                                                       H, dk, dv);
         if ((e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
