@@ -260,7 +260,7 @@ __host__ __device__ constexpr size_t P_GL(int dk, int dv) { return P_P(dk, dv) +
 // REC_TC bytes -- the chunk's start state S and end-state gradient dS_end as bf16 S^T
 // tiles [128 v][136] (written by the two serial passes in the row layout shared memory
 // uses), then the prep kernel's record of the chunk's state-independent products:
-//   K', -W, s Q~ bf16 [16][136]; s P bf16 [16][24]; gamma_L fp32 in the serial passes' float4
+//   K', -W, Q~ bf16 [16][136]; P bf16 [16][24]; gamma_L fp32 in the serial passes' float4
 //   order (the part [0, TR_OPS) is what the serial passes copy); U~^T fp32 [128 v][16 t];
 //   K~, K^ bf16 [16][136]; M bf16 [16][24]; T, T^T, Z fp32 [16][16]; beta fp32 [16];
 //   G fp32 [16][136]; gamma_L fp32 [128].
@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(kThreads)
 // a warp's rows of the state A = S^T as bf16 A fragments (mma.sync m16n8k16):
 //   forward:  write S^T (the chunk's start state); U^T = U~^T + S^T (-W)^T;
 //             S^T <- S^T Diag(gamma_L) + U^T K'
-//   reverse:  write dS^T (the gradient at the chunk's end); X^T = dS^T K'^T + dO^T (s P);
-//             dS^T <- dS^T Diag(gamma_L) + dO^T (s Q~) + X^T (-W)
+//   reverse:  write dS^T (the gradient at the chunk's end); X^T = dS^T K'^T + (s dO)^T P;
+//             dS^T <- dS^T Diag(gamma_L) + (s dO)^T Q~ + X^T (-W)
 // the transposed forms of the two chains above, the state an fp32 accumulator throughout.
 constexpr int NS = 4;                    // ring slots
 constexpr int PO = 40;                   // bf16 pitch of the [16][32] dO slice (80-byte rows)
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(128, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
             const unsigned char *tr = ws + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
-            if (REVERSE) {  // K', -W, s Q~, s P, gamma_L; the dO rows of the CTA's 32 columns
+            if (REVERSE) {  // K', -W, Q~, P, gamma_L; the dO rows of the CTA's 32 columns
                 const int64_t c0 = t0 + (int64_t)c * C;
                 const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
                 if (L < C) {  // rows past the sequence's end read as zeros
@@ -800,10 +800,16 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
         }
-        // dO^T as the A fragment (reverse): 16 value rows x 16 tokens, read transposed
+        // (s dO)^T as the A fragment (reverse): 16 value rows x 16 tokens, read transposed
         uint32_t oa[4] = {0u, 0u, 0u, 0u};
-        if (REVERSE)
+        if (REVERSE) {
             ldsm4t(sl + SL_X + (uint32_t)((((i8 >> 1) * 8 + r8) + 0) * PO * 2 + (16 * sw + (i8 & 1) * 8) * 2), oa);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // s dO
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&oa[i]));
+                oa[i] = pack2(scale * f.x, scale * f.y);
+            }
+        }
 #pragma unroll
         for (int kt = 0; kt < 8; ++kt) {  // state tile kt against the chunk's 16 tokens
             uint32_t a[4];
@@ -817,7 +823,7 @@ __global__ void __launch_bounds__(128, 1)
             mma16816(acc[0], a, bfr[0], bfr[1]);
             mma16816(acc[1], a, bfr[2], bfr[3]);
         }
-        if (REVERSE) {  // + dO^T (s P): B[k = token i][n = token r] = s P[i][r], [k][n] storage
+        if (REVERSE) {  // + (s dO)^T P: B[k = token i][n = token r] = P[i][r], [k][n] storage
             uint32_t bfr[4];
             ld_b_kn(sl + SL_P, PS, 0, 0, bfr);
             mma16816(acc[0], oa, bfr[0], bfr[1]);
@@ -840,7 +846,7 @@ __global__ void __launch_bounds__(128, 1)
             ld_b_kn(sl + (REVERSE ? SL_W : SL_K), PB, 0, 16 * np, bfr);
             mma16816(S[2 * np], ua, bfr[0], bfr[1]);
             mma16816(S[2 * np + 1], ua, bfr[2], bfr[3]);
-            if (REVERSE) {  // + dO^T (s Q~)
+            if (REVERSE) {  // + (s dO)^T Q~
                 ld_b_kn(sl + SL_Q, PB, 0, 16 * np, bfr);
                 mma16816(S[2 * np], oa, bfr[0], bfr[1]);
                 mma16816(S[2 * np + 1], oa, bfr[2], bfr[3]);
@@ -1100,8 +1106,7 @@ constexpr int RBUF = RECB + 2 * T128;  // record, then V and dO rows [16][136] b
 constexpr int LS_S = 0, LS_DS = ST16, LS_R = 2 * ST16;
 constexpr int LS_U = LS_R + 2 * RBUF, LS_DU = LS_U + T128, LS_DW = LS_DU + T128;
 constexpr int LS_DP = LS_DW + T128, LS_DZ = LS_DP + C * PS * 2;
-constexpr int LS_DPU = LS_DZ + C * PS * 2;  // dP / s: the partner of the record's s Q~
-constexpr int LS_PART = LS_DPU + C * PS * 2;  // per warp: dM, dP partial sums [2][16][16]
+constexpr int LS_PART = LS_DZ + C * PS * 2;  // per warp: dM, dP partial sums [2][16][16]
 constexpr int LS_DT = LS_PART + 8 * 2 * C * C * 4, LS_DMS = LS_DT + C * C * 4, LS_Y = LS_DMS + C * C * 4;
 constexpr int LS_DB = LS_Y + C * C * 4;
 constexpr int LS_BYTES = LS_DB + C * 4;
@@ -1138,8 +1143,7 @@ __device__ __forceinline__ int item_rows(const int32_t *cu, const Item &it, int6
 }
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
-    local_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
+    local_tc_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
                     const int32_t *__restrict__ cu, const __nv_bfloat16 *__restrict__ dout,
                     const unsigned char *__restrict__ ws, __nv_bfloat16 *__restrict__ dq,
                     __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
@@ -1159,7 +1163,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     float *Ys = reinterpret_cast<float *>(sl + LS_Y), *dbs = reinterpret_cast<float *>(sl + LS_DB);
     __nv_bfloat16 *dP16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DP);
     __nv_bfloat16 *dZ16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DZ);
-    __nv_bfloat16 *dPu16 = reinterpret_cast<__nv_bfloat16 *>(sl + LS_DPU);
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) bar_init(bar(i), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1203,21 +1206,12 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         bar_arrive_tx(bar(0), 2 * ST16);
         bulk_g2s(sb + LS_S, rec_of(it) + TC_S, 2 * ST16, bar(0));
     };
-    // warp 1: the next item's states and its q, k, a rows into L2
+    // warp 1: the next item's states and gate-logit rows into L2
     auto prefetch_next = [&](const Item &it) {
         int64_t c0;
         const int L = rows_of(it, c0);
         if (lane == 0) prefetch_l2(rec_of(it) + TC_S, 2 * ST16);
-        const int r = lane & 15;
-        if (r < L) {
-            const size_t o = ((size_t)(c0 + r) * H + it.h) * D;
-            if (lane < 16) {
-                prefetch_l2(q + o, D * 2);
-                prefetch_l2(k + o, D * 2);
-            } else {
-                prefetch_l2(a + o, D * 4);
-            }
-        }
+        if (lane < L) prefetch_l2(a + ((size_t)(c0 + lane) * H + it.h) * D, D * 4);
     };
 
     Item cur, nxt;
@@ -1247,7 +1241,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         const uint32_t KT = rbase + TR_KT, KH = rbase + TR_KH, M16 = rbase + TR_M;
         const uint32_t V16 = rbase + RECB, DO = rbase + RECB + T128;
         const uint32_t U16 = sb + LS_U, DU16 = sb + LS_DU, DW16 = sb + LS_DW;
-        const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ, DPU = sb + LS_DPU;
+        const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ;
 
         // ---- phase 1 (value columns [n0, n0 + 16)): U = U~ - W S, dU = K' dS_end + s P^T dO,
         // dV = M^T dU; partial sums of dO U^T and dU V^T over these columns
@@ -1276,14 +1270,14 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             }
             uint32_t ap[4], bo[4];
             float pd[2][4] = {};
-            ld_a_t(P16, PS, 0, 0, ap);         // (s P)^T
+            ld_a_t(P16, PS, 0, 0, ap);         // P^T
             ld_b_kn(DO, PB, 0, n0, bo);        // B[i][v] = dO[i][v]
             mma16816(pd[0], ap, bo[0], bo[1]);
             mma16816(pd[1], ap, bo[2], bo[3]);
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) du[tt][i] += pd[tt][i];
+                for (int i = 0; i < 4; ++i) du[tt][i] = fmaf(scale, pd[tt][i], du[tt][i]);
             store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_U), PB, n0, u);
             store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_DU), PB, n0, du);
             // dO[:, cols] U[:, cols]^T: U's accumulator fragments are the B operand as they are
@@ -1394,7 +1388,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                 dp += part[w * 2 * C * C + C * C + tid];
             }
             dP16[r * PS + j] = __float2bfloat16_rn(j <= r ? scale * dp : 0.f);
-            dPu16[r * PS + j] = __float2bfloat16_rn(j <= r ? dp : 0.f);
             dTs[tid] = dm * BT[j];
             dMs[tid] = dm;
         }
@@ -1428,22 +1421,20 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         __syncthreads();  // dP, dZ complete
 
         // ---- phase 4 (key channels [n0, n0 + 16)): dQ~ += dP K^, dK~ = M^T dW + dZ K^,
-        // dK^ = dP^T Q~ + dZ^T K~; then dq, dk and da on the fragments
-        uint32_t qv[2][2], kv[2][2];
+        // dK^ = dP^T Q~ + dZ^T K~; then dq, dk and da on the fragments. dG takes Q~, K~, K^
+        // and K' as the bf16 values the products above used: its terms cancel pairwise
+        // across rows (dP_ri Q~_r K^_i enters row r through dQ~ and row i through dK^, and
+        // likewise for dZ), exactly only with the same operand values on both sides.
         float2 av[2][2];
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int t = g4 + 8 * hh;
-                qv[tt][hh] = kv[tt][hh] = 0u;
                 av[tt][hh] = make_float2(0.f, 0.f);
-                if (t < L) {
-                    const size_t o = ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4;
-                    qv[tt][hh] = *reinterpret_cast<const uint32_t *>(q + o);
-                    kv[tt][hh] = *reinterpret_cast<const uint32_t *>(k + o);
-                    av[tt][hh] = *reinterpret_cast<const float2 *>(a + o);
-                }
+                if (t < L)
+                    av[tt][hh] = *reinterpret_cast<const float2 *>(
+                        a + ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4);
             }
         float dkt[2][4] = {}, dkh[2][4] = {};
         {
@@ -1459,7 +1450,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             ld_b_kn(DW16, PB, 0, n0, bb);      // B[t'][key] = dW[t'][key]
             mma16816(dkt[0], af, bb[0], bb[1]);
             mma16816(dkt[1], af, bb[2], bb[3]);
-            ld_a_t(DPU, PS, 0, 0, af);         // (dP / s)^T against s Q~
+            ld_a_t(DP, PS, 0, 0, af);          // dP^T
             ld_b_kn(QT, PB, 0, n0, bb);
             mma16816(dkh[0], af, bb[0], bb[1]);
             mma16816(dkh[1], af, bb[2], bb[3]);
@@ -1476,16 +1467,19 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int t = g4 + 8 * hh, key = n0 + 8 * tt + 2 * l4;
-                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qv[tt][hh]));
-                const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kv[tt][hh]));
+                auto tile2 = [&](int off) {
+                    return __bfloat1622float2(
+                        *reinterpret_cast<const __nv_bfloat162 *>(R + off + (t * 136 + key) * 2));
+                };
+                const float2 q2 = tile2(TR_Q), t2 = tile2(TR_KT), h2 = tile2(TR_KH), p2 = tile2(TR_K);
                 float oq[2], ok2[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int fi = 2 * hh + e;
                     const float G = GS[t * GP + key + e], GL = GS[(C - 1) * GP + key + e];
                     const float eg = expf(G), en = expf(-G), ep = expf(GL - G);
-                    const float qx = e ? qf.y : qf.x, kx = e ? kf.y : kf.x;
-                    const float Qt = qx * eg, Kt = kx * eg, Kh = kx * en, Kp = kx * ep;
+                    const float Qt = e ? q2.y : q2.x, Kt = e ? t2.y : t2.x;
+                    const float Kh = e ? h2.y : h2.x, Kp = e ? p2.y : p2.x;
                     const float gq = dqa[tt][fi], gt = dkt[tt][fi], gh = dkh[tt][fi], gp = dkp[tt][fi];
                     oq[e] = gq * eg;
                     ok2[e] = gt * eg + gh * en + gp * ep;
@@ -1553,11 +1547,11 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 constexpr int PT_THREADS = 256;
 constexpr int IBUF = 3 * T128 + C * 128 * 4;  // q, k, v rows [16][136] bf16; a rows [16][128] fp32
 constexpr int PS_REC = 2 * IBUF;
-constexpr int PS_QH = PS_REC + RECB, PS_QL = PS_QH + T128, PS_KTL = PS_QL + T128;
+constexpr int PS_QL = PS_REC + RECB, PS_KTL = PS_QL + T128;
 constexpr int PS_KHL = PS_KTL + T128, PS_A = PS_KHL + T128, PS_ML = PS_A + C * C * 4;
 constexpr int PS_BT = PS_ML + C * PS * 2;
 constexpr int PS_BYTES = PS_BT + C * 4;
-static_assert(IBUF % 16 == 0 && PS_QH % 16 == 0 && PS_A % 16 == 0 && 2 * (PS_BYTES + 1024) <= 228 * 1024,
+static_assert(IBUF % 16 == 0 && PS_QL % 16 == 0 && PS_A % 16 == 0 && 2 * (PS_BYTES + 1024) <= 228 * 1024,
               "two prep CTAs per SM");
 
 // hi = bf16(x), lo = bf16(x - hi)
@@ -1666,7 +1660,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             const uint4 qr = *reinterpret_cast<const uint4 *>(in + (r * 136 + x0) * 2);
             const uint4 kr = *reinterpret_cast<const uint4 *>(in + T128 + (r * 136 + x0) * 2);
             const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w}, kw[4] = {kr.x, kr.y, kr.z, kr.w};
-            uint32_t okp[4], osq[4], okt[4], okh[4], oqh[4], oql[4], oktl[4], okhl[4];
+            uint32_t okp[4], okt[4], okh[4], oqh[4], oql[4], oktl[4], okhl[4];
 #pragma unroll
             for (int p2 = 0; p2 < 4; ++p2) {
                 const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[p2]));
@@ -1683,7 +1677,6 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                     Kp[e] = kx * expf(GL - G);
                 }
                 okp[p2] = pack2(Kp[0], Kp[1]);
-                osq[p2] = pack2(scale * Qt[0], scale * Qt[1]);
                 split2(Qt[0], Qt[1], oqh[p2], oql[p2]);
                 split2(Kt[0], Kt[1], okt[p2], oktl[p2]);
                 split2(Kh[0], Kh[1], okh[p2], okhl[p2]);
@@ -1693,10 +1686,9 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                 *reinterpret_cast<uint4 *>(base + off) = make_uint4(w[0], w[1], w[2], w[3]);
             };
             st4(rec + TR_K, okp);
-            st4(rec + TR_Q, osq);
+            st4(rec + TR_Q, oqh);
             st4(rec + TR_KT, okt);
             st4(rec + TR_KH, okh);
-            st4(sp + PS_QH, oqh);
             st4(sp + PS_QL, oql);
             st4(sp + PS_KTL, oktl);
             st4(sp + PS_KHL, okhl);
@@ -1705,7 +1697,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
 
         // ---- Z = K~ K^^T (warp 0), P = Q~ K^^T (warp 1), split-bf16 products
         if (warp < 2) {
-            const uint32_t ah_b = warp == 0 ? sb + PS_REC + TR_KT : sb + PS_QH;
+            const uint32_t ah_b = warp == 0 ? sb + PS_REC + TR_KT : sb + PS_REC + TR_Q;
             const uint32_t al_b = warp == 0 ? sb + PS_KTL : sb + PS_QL;
             const uint32_t bh_b = sb + PS_REC + TR_KH, bl_b = sb + PS_KHL;
             float c0a[2][4] = {}, c1a[2][4] = {}, c2a[2][4] = {};
@@ -1734,7 +1726,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                         As[r * C + j] = j < r ? bts[r] * x : 0.f;
                     } else {
                         reinterpret_cast<__nv_bfloat16 *>(rec + TR_P)[r * PS + j] =
-                            __float2bfloat16_rn(j <= r ? scale * x : 0.f);
+                            __float2bfloat16_rn(j <= r ? x : 0.f);
                     }
                 }
         }
@@ -1879,7 +1871,7 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
                                                                p.dh0, H, scale);
         const int grid = (int)(n_items < sms ? n_items : sms);
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
-            b16[0], b16[1], b16[2], p.a, p.cu_seqlens, d16, wsb,
+            b16[2], p.a, p.cu_seqlens, d16, wsb,
             reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
             reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
     } else {
