@@ -57,7 +57,8 @@ UNIT = "tokens/s"
 KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu"]
 DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
 BACKWARD_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_bwd.cu"]
-BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of fp32 ALU roofline"
+BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of HBM roofline (dominant kernel)"
+BACKWARD_KERNELS = ["prep", "forward_pass", "reverse_pass", "local_gradients"]
 # fp32 FMA peak of the SIMT backward: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
@@ -81,6 +82,28 @@ def flops_per_token_head(d_k: int, d_v: int, C: int = 16) -> int:
 def state_bytes(x) -> int:
     per = x.n_seq * x.n_heads * x.d_k * x.d_v * 4
     return per * (2 if x.h0 is not None else 1)   # h0 read (if given), h_final written
+
+
+def bwd_kernel_bytes(x):
+    """Bytes each kernel of the tensor-core backward (bf16, d = 128) must move per call
+    in its design, summed over the (chunk, head) items: the prep record written (44352 B)
+    from the q, k, v, gate-logit rows; each serial pass's bf16 state tiles written
+    (34816 B) and the record parts it reads (once per item from DRAM); the local kernel's
+    two state tiles and record read, its V, dO and gate-logit rows read and its gradients
+    written. None for other configurations."""
+    if not (str(x.dtype).endswith("bfloat16") and x.d_k == 128 and x.d_v == 128):
+        return None
+    rows = [max(0, b - a) for a, b in zip(x.cu_host[:-1], x.cu_host[1:])]
+    tile, rec, ops, ut = 34816, 44352, 14336, 8192
+    tot = [0, 0, 0, 0]
+    for n_rows in rows:
+        for c0 in range(0, n_rows, 16):
+            L = min(16, n_rows - c0)
+            tot[0] += L * (3 * 256 + 512 + 4) + rec
+            tot[1] += 2 * 4352 + 512 + ut + tile
+            tot[2] += ops + L * 256 + tile
+            tot[3] += 2 * tile + rec + L * (2 * 256 + 512) + L * (3 * 256 + 512 + 4)
+    return [t * x.n_heads for t in tot]
 
 
 def algorithmic_bytes(x) -> int:
@@ -556,6 +579,7 @@ def run_backward(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(on)
     torch.cuda.synchronize(dev)
+    kda.bwd_timing_start(args.steps)  # events around each kernel of every timed call
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -567,18 +591,35 @@ def run_backward(args):
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(on)
+    kernel_ms, calls = kda.bwd_timing_read()
+    kernel_ms = [t / max(1, calls) for t in kernel_ms]
     launches = kda.kernel_launch_count() - n0
     total_ms = max_over_ranks(t0.elapsed_time(t1), on, dev)
     value = x.n_tok * world * args.steps / (total_ms * 1e-3)
     mean_s = statistics.mean(s_.elapsed_time(e) for s_, e in zip(starts, ends)) * 1e-3
-    flops = 2 * algorithmic_flops(x)       # a gradient product for each operand of each product
-    achieved = flops / mean_s / 1e12
-    roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_ALU_TFLOPS, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz "
-                               "(nominal unit counts and maximum SM clock)",
-                "algorithmic_flops_per_step": flops,
-                "hbm_gbs": round(algorithmic_bytes(x) * 2 / mean_s / 1e9, 1)}
+    peaks = measured_peaks()
+    kbytes = bwd_kernel_bytes(x)
+    kernels = {nm: {"ms": round(t, 4), "share": round(t / sum(kernel_ms), 4)}
+               for nm, t in zip(BACKWARD_KERNELS, kernel_ms)}
+    if kbytes is not None:
+        for nm, b, t in zip(BACKWARD_KERNELS, kbytes, kernel_ms):
+            kernels[nm].update(bytes=b, gbs=round(b / (t * 1e-3) / 1e9, 1))
+        top = max(range(4), key=lambda i: kernel_ms[i])
+        achieved = kbytes[top] / (kernel_ms[top] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": BACKWARD_KERNELS[top], "achieved": round(achieved, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": recorded_traffic(f"{x.name}:{BACKWARD_KERNELS[top]}", BACKWARD_SOURCES),
+                    "algorithmic_bytes_per_launch": kbytes[top],
+                    "launch_ms": round(kernel_ms[top], 4),
+                    "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)"}
+    else:  # the fp32 FMA kernels
+        flops = 2 * algorithmic_flops(x)   # a gradient product for each operand of each product
+        achieved = flops / mean_s / 1e12
+        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_ALU_TFLOPS, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz "
+                                   "(nominal unit counts and maximum SM clock)"}
 
     # end to end through the public API: inputs and upstream gradients from pinned host
     # memory, the backward, the gradients back to pinned host memory
@@ -614,13 +655,14 @@ def run_backward(args):
     line = {"metric": BACKWARD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32 arithmetic, bf16 I/O" if x.dtype == torch.bfloat16 else "f32",
+            "dtype": ("bf16 tensor-core operands, f32 accumulation" if kbytes is not None
+                      else "f32"),
             "data": "synthetic",
             "config": {"workload": x.name, "tokens_per_gpu": x.n_tok, "heads": x.n_heads,
                        "d_k": x.d_k, "d_v": x.d_v, "chunk": 16,
                        "workspace_bytes": int(ws.numel()),
                        "l2": "inputs and workspace exceed the 129 MB L2; no flush"},
-            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "roofline": roofline, "kernels": kernels, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk.summary(), "kernel_digest": kernel_source_digest(BACKWARD_SOURCES)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = backward_cpu_baseline(x, dout)

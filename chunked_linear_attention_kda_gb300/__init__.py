@@ -23,7 +23,7 @@ from . import build as _build_mod
 
 __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
-           "chunk_fwd_variant", "gate_projection",
+           "bwd_timing_start", "bwd_timing_read", "chunk_fwd_variant", "gate_projection",
            "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
@@ -35,8 +35,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_selftest_bounded_wait", "kda_chunk_fwd",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
                     "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd",
-                    "kda_chunk_bwd_static_scratch", "kda_chunk_fwd_variant",
-                    "kda_gate_projection")
+                    "kda_chunk_bwd_static_scratch", "kda_bwd_timing_start",
+                    "kda_bwd_timing_read", "kda_chunk_fwd_variant", "kda_gate_projection")
 
 _lock = threading.Lock()
 _lib = None
@@ -104,6 +104,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_bwd_static_scratch.argtypes = [P] * 15 + [I64, I32, I32, I32, I32,
                                                                 ctypes.c_int, P]
         lib.kda_chunk_bwd_static_scratch.restype = ctypes.c_int
+        lib.kda_bwd_timing_start.argtypes = [ctypes.c_int]
+        lib.kda_bwd_timing_start.restype = ctypes.c_int
+        lib.kda_bwd_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                            ctypes.POINTER(ctypes.c_int)]
+        lib.kda_bwd_timing_read.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -399,6 +404,22 @@ def chunk_bwd(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final=None, *
         N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
         ctypes.c_void_p(stream)))
     return dq, dk_, dv_, da, db, dh0
+
+
+def bwd_timing_start(capacity: int) -> None:
+    """Record the device time of each backward kernel for the next ``capacity`` calls."""
+    lib = load_library()
+    _check(lib, lib.kda_bwd_timing_start(int(capacity)))
+
+
+def bwd_timing_read():
+    """``([prep, forward pass, reverse pass, local] ms summed over the recorded calls),
+    calls)``; stops recording."""
+    ms = (ctypes.c_float * 4)()
+    calls = ctypes.c_int(0)
+    lib = load_library()
+    _check(lib, lib.kda_bwd_timing_read(ms, ctypes.byref(calls)))
+    return [float(x) for x in ms], int(calls.value)
 
 
 def chunk_bwd_static_scratch(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, dh_final=None,

@@ -263,6 +263,21 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     return launched(kda::launch_bwd(p, (cudaStream_t)stream), "backward launch");
 }
 
+kda_status kda_bwd_timing_start(int capacity) {
+    if (capacity < 1 || capacity > 1024)
+        return fail(KDA_ERR_INVALID_ARG, "capacity must be in [1, 1024]");
+    const cudaError_t e = kda::bwd_timing_start(capacity);
+    if (e != cudaSuccess) return launched(e, "creating the timing events");
+    return ok();
+}
+
+kda_status kda_bwd_timing_read(float *ms, int *calls) {
+    if (!ms || !calls) return fail(KDA_ERR_INVALID_ARG, "ms and calls must not be NULL");
+    const cudaError_t e = kda::bwd_timing_read(ms, calls);
+    if (e != cudaSuccess) return launched(e, "reading the timing events");
+    return ok();
+}
+
 kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void *v,
                                         const float *gate_logits, const float *beta,
                                         const float *h0, const int32_t *cu_seqlens,

@@ -36,6 +36,9 @@
 // strictly increasing over all chunks, below (n_tok >> 4) + n_seq + 1.
 #include <cuda_bf16.h>
 
+#include <mutex>
+#include <vector>
+
 #include "kda_internal.h"
 
 namespace kda {
@@ -1810,6 +1813,36 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Per-kernel timing of backward calls (a measurement aid): events before the first kernel
+// and after each of the four, for up to `capacity` calls.
+struct BwdTiming {
+    std::mutex mu;
+    std::vector<cudaEvent_t> ev;  // capacity x 5
+    int capacity = 0, used = 0;
+    bool active = false;
+};
+BwdTiming &bwd_timing() {
+    static BwdTiming t;
+    return t;
+}
+struct CallEvents {  // the events of one call, or none
+    cudaEvent_t *ev = nullptr;
+    cudaStream_t stream = nullptr;
+    void mark(int i) const {
+        if (ev) cudaEventRecord(ev[i], stream);
+    }
+};
+CallEvents claim_events(cudaStream_t stream) {
+    BwdTiming &t = bwd_timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    CallEvents c;
+    if (t.active && t.used < t.capacity) {
+        c.ev = t.ev.data() + 5 * t.used++;
+        c.stream = stream;
+    }
+    return c;
+}
+
 template <typename IO>
 cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     const int H = p.n_heads, dk = p.d_k, dv = p.d_v;
@@ -1843,6 +1876,7 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     if (gy < 1) gy = 1;
     if (gy > 65535) gy = 65535;
     const dim3 par(items, (unsigned)gy), cols(items, (unsigned)((dv + JS - 1) / JS));
+    const CallEvents tev = claim_events(stream);
     if (use_tc) {
         // serial passes with the state in mma fragments, then the local gradients with one
         // CTA per SM over all (chunk slot, head) items
@@ -1862,31 +1896,41 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
                                        reinterpret_cast<const __nv_bfloat16 *>(p.k),
                                        reinterpret_cast<const __nv_bfloat16 *>(p.v)};
         const int pgrid = (int)(n_items < 2 * sms ? n_items : 2 * sms);
+        tev.mark(0);
         prep_tc_kernel<<<pgrid, PT_THREADS, PS_BYTES, stream>>>(b16[0], b16[1], b16[2], p.a, p.beta,
                                                                p.cu_seqlens, wsb, H, p.n_seq,
                                                                n_items, scale);
+        tev.mark(1);
         chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0,
                                                                 nullptr, H, scale);
+        tev.mark(2);
         chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.dh_final,
                                                                p.dh0, H, scale);
+        tev.mark(3);
         const int grid = (int)(n_items < sms ? n_items : sms);
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
             b16[2], p.a, p.cu_seqlens, d16, wsb,
             reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
             reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
+        tev.mark(4);
     } else {
-        prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
-                                                       H, dk, dv);
         if ((e = cudaFuncSetAttribute(ckpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(chain_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
             return e;
+        tev.mark(0);
+        prep_kernel<IO><<<par, kThreads, sm0, stream>>>(q, k, v, p.a, p.beta, p.cu_seqlens, prep,
+                                                       H, dk, dv);
+        tev.mark(1);
         ckpt_kernel<<<cols, kThreads, sm1, stream>>>(p.h0, p.cu_seqlens, prep, ck, H, dk, dv);
+        tev.mark(2);
         chain_kernel<IO><<<cols, kThreads, sm2, stream>>>(p.cu_seqlens, dout, p.dh_final, prep,
                                                          dck, p.dh0, H, dk, dv, scale);
+        tev.mark(3);
         local_kernel<IO><<<par, kThreads, sm3, stream>>>(
             q, k, v, p.a, p.beta, p.cu_seqlens, dout, ck, dck, (IO *)p.dq, (IO *)p.dk,
             (IO *)p.dv, p.da, p.dbeta, H, dk, dv, scale);
+        tev.mark(4);
     }
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(4);
@@ -1906,6 +1950,44 @@ size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_
 cudaError_t launch_bwd(const BwdArgs &p, cudaStream_t stream) {
     if (p.n_seq == 0) return cudaSuccess;
     return p.bf16 ? launch_bwd_t<__nv_bfloat16>(p, stream) : launch_bwd_t<float>(p, stream);
+}
+
+cudaError_t bwd_timing_start(int capacity) {
+    BwdTiming &t = bwd_timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    for (cudaEvent_t e : t.ev) cudaEventDestroy(e);
+    t.ev.assign((size_t)capacity * 5, nullptr);
+    t.capacity = t.used = 0;
+    t.active = false;
+    for (size_t i = 0; i < t.ev.size(); ++i) {
+        const cudaError_t e = cudaEventCreate(&t.ev[i]);
+        if (e != cudaSuccess) {
+            for (size_t j = 0; j < i; ++j) cudaEventDestroy(t.ev[j]);
+            t.ev.clear();
+            return e;
+        }
+    }
+    t.capacity = capacity;
+    t.active = true;
+    return cudaSuccess;
+}
+
+cudaError_t bwd_timing_read(float ms[4], int *calls) {
+    BwdTiming &t = bwd_timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    t.active = false;
+    for (int i = 0; i < 4; ++i) ms[i] = 0.f;
+    for (int c = 0; c < t.used; ++c) {
+        cudaError_t e = cudaEventSynchronize(t.ev[5 * c + 4]);
+        if (e != cudaSuccess) return e;
+        for (int i = 0; i < 4; ++i) {
+            float x = 0.f;
+            if ((e = cudaEventElapsedTime(&x, t.ev[5 * c + i], t.ev[5 * c + i + 1])) != cudaSuccess) return e;
+            ms[i] += x;
+        }
+    }
+    *calls = t.used;
+    return cudaSuccess;
 }
 
 }  // namespace kda

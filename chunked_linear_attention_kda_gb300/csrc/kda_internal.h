@@ -87,6 +87,10 @@ cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, fl
 cudaError_t read_gemm_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 // The backward serial passes' status word (bit 2); synchronises stream.
 cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream);
+// Per-kernel event timing of the next `capacity` backward calls; the read returns the
+// summed milliseconds of the four kernels and the number of calls recorded, and stops.
+cudaError_t bwd_timing_start(int capacity);
+cudaError_t bwd_timing_read(float ms[4], int *calls);
 
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);

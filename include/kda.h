@@ -246,8 +246,13 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
  * [n_tok, n_heads] float32; dh0 [n_seq, n_heads, d_k, d_v] float32, or NULL to skip.
  * workspace: caller-owned device memory of at least kda_chunk_bwd_workspace_bytes()
  * bytes, 4-byte aligned, contents ignored on entry (it receives the state at the start
- * and the state gradient at the end of every chunk). Arithmetic is fp32 throughout.
- * Alignment as for kda_chunk_fwd for the inputs; outputs aligned to their element size.
+ * and the state gradient at the end of every chunk). Arithmetic: fp32 accumulation
+ * throughout; for KDA_BF16 with d_k = d_v = 128, and the workspace, q, k, v,
+ * gate_logits and dout 16-byte aligned, the products take bf16 operands on the tensor
+ * cores (the chunk products of the state-independent part as split bf16 high and low
+ * parts), otherwise fp32 FMA. The result is deterministic: the same call gives the same
+ * bits. Alignment as for kda_chunk_fwd for the inputs; outputs aligned to their element
+ * size.
  * No output or the workspace may overlap an input or another output. Asynchronous on
  * `stream`; nothing is allocated. Errors as for kda_chunk_fwd, plus
  * KDA_ERR_INVALID_ARG for a missing gradient buffer, overlap, or a NULL or too small
@@ -262,6 +267,23 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
                          float *dh0, void *workspace, size_t workspace_bytes,
                          int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
                          int32_t d_v, kda_dtype dtype, void *stream);
+
+/*
+ * kda_bwd_timing_start / kda_bwd_timing_read -- device time of each kernel of the
+ * backward pass, for measurement (an addition of this library: the pages have no
+ * counterpart). After kda_bwd_timing_start(capacity) the next `capacity` calls of
+ * kda_chunk_bwd or kda_chunk_bwd_static_scratch record a CUDA event on their stream before
+ * their first kernel and after each of their four kernels (state-independent chunk
+ * products; forward serial pass; reverse serial pass; local gradients). Recording adds no
+ * synchronisation. kda_bwd_timing_read waits for those events, writes the milliseconds of
+ * each kernel summed over the recorded calls to ms[0..3] (host array of 4) and the number
+ * of recorded calls to *calls (host), and stops recording. One recording at a time per
+ * process; a new start discards the previous one. Errors: KDA_ERR_INVALID_ARG for
+ * capacity outside [1, 1024] or a NULL pointer; KDA_ERR_CUDA when an event cannot be
+ * created or waited for.
+ */
+kda_status kda_bwd_timing_start(int capacity);
+kda_status kda_bwd_timing_read(float *ms, int *calls);
 
 /*
  * kda_chunk_bwd_static_scratch -- kda_chunk_bwd without a caller workspace and without

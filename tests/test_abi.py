@@ -213,3 +213,15 @@ def test_gate_projection_host_validation(lib, kw, status):
 
 def test_gate_projection_nothing_to_do_is_ok(lib):
     assert proj(lib, n_tok=0) == 0
+
+
+@pytest.mark.parametrize("capacity", [0, -3, 1025])
+def test_backward_timing_rejects_capacity(lib, capacity):
+    assert lib.kda_bwd_timing_start(capacity) == 1
+
+
+def test_backward_timing_read_rejects_null(lib):
+    ms = (ctypes.c_float * 4)()
+    calls = ctypes.c_int(0)
+    assert lib.kda_bwd_timing_read(None, ctypes.byref(calls)) == 1
+    assert lib.kda_bwd_timing_read(ms, None) == 1

@@ -108,3 +108,22 @@ def test_context_64k_suffix():
     for nm, g in zip(NAMES[:5], got[:5]):
         e = rel_l2(f64(g[t1:])[:, heads], ref[nm])
         assert e <= 1e-2, f"{nm}: {e:.3e}"
+
+
+def test_kernel_timing_records_every_call():
+    """The per-kernel event timing the bench reports: four positive kernel times summed
+    over exactly the calls made while recording, and results unchanged by recording."""
+    x = K.make_inputs([70, 33], 2, 128, 128, dtype=torch.bfloat16, device=DEV, seed=8,
+                      h0_std=0.3)
+    dout, dhf = upstream(x, 8)
+    ref = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)
+    kda.bwd_timing_start(8)
+    for _ in range(3):
+        got = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)
+    ms, calls = kda.bwd_timing_read()
+    assert calls == 3 and all(t > 0 for t in ms), (ms, calls)
+    kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)  # not recorded
+    assert kda.bwd_timing_read()[1] == 3
+    torch.cuda.synchronize()
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g)
