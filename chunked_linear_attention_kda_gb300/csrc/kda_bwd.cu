@@ -698,6 +698,9 @@ __global__ void __launch_bounds__(128, 1)
     const int64_t t0 = cu[n], t1 = cu[n + 1];
     const int nc = (int)((t1 - t0 + C - 1) / C);
     const size_t st = (size_t)D * D;
+    // workspace record of chunk c: rec0 + c * REC_TC * H (the slot of chunk 0, read once)
+    unsigned char *const rec0 = ws + (((size_t)(t0 >> 4) + (size_t)n) * H + h) * REC_TC;
+    const size_t rstride = (size_t)H * REC_TC;
     auto full = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[s])); };
     auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
     if (tid == 0) {
@@ -717,7 +720,7 @@ __global__ void __launch_bounds__(128, 1)
             if (m >= NS) ok = bar_wait(empty(s), ((m / NS) & 1) ^ 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
-            const unsigned char *tr = ws + (slot_of(cu, n, c) * H + h) * REC_TC + TC_REC;
+            const unsigned char *tr = rec0 + (size_t)c * rstride + TC_REC;
             if (REVERSE) {  // K', -W, Q~, P, gamma_L; the dO rows of the CTA's 32 columns
                 const int64_t c0 = t0 + (int64_t)c * C;
                 const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(128, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t sl = sbase + s * SLOT;
         const float4 *G4 = reinterpret_cast<const float4 *>(smc + s * SLOT + SL_G);
-        write_tile(ws + (slot_of(cu, n, c) * H + h) * REC_TC + (REVERSE ? TC_DS : TC_S));
+        write_tile(rec0 + (size_t)c * rstride + (REVERSE ? TC_DS : TC_S));
         float acc[2][4];  // U^T (forward) or X^T (reverse): 16 value rows x 16 tokens
         if (!REVERSE) {
             const float *tu = reinterpret_cast<const float *>(smc + s * SLOT + SL_X);
@@ -813,6 +816,9 @@ __global__ void __launch_bounds__(128, 1)
                 oa[i] = pack2(scale * f.x, scale * f.y);
             }
         }
+        // two independent accumulator chains (even / odd state tiles) halve the dependent
+        // mma sequence of this product, the serial step's critical path
+        float acc2[2][4] = {};
 #pragma unroll
         for (int kt = 0; kt < 8; ++kt) {  // state tile kt against the chunk's 16 tokens
             uint32_t a[4];
@@ -823,15 +829,20 @@ __global__ void __launch_bounds__(128, 1)
             uint32_t bfr[4];
             // forward: B[k = channel][n = token] = -W[t][c]; reverse: = K'[t][c]; [n][k] storage
             ld_b_nk(sl + (REVERSE ? SL_K : SL_W), PB, 0, 16 * kt, bfr);
-            mma16816(acc[0], a, bfr[0], bfr[1]);
-            mma16816(acc[1], a, bfr[2], bfr[3]);
+            float (&ac)[2][4] = (kt & 1) ? acc2 : acc;
+            mma16816(ac[0], a, bfr[0], bfr[1]);
+            mma16816(ac[1], a, bfr[2], bfr[3]);
         }
         if (REVERSE) {  // + (s dO)^T P: B[k = token i][n = token r] = P[i][r], [k][n] storage
             uint32_t bfr[4];
             ld_b_kn(sl + SL_P, PS, 0, 0, bfr);
-            mma16816(acc[0], oa, bfr[0], bfr[1]);
-            mma16816(acc[1], oa, bfr[2], bfr[3]);
+            mma16816(acc2[0], oa, bfr[0], bfr[1]);
+            mma16816(acc2[1], oa, bfr[2], bfr[3]);
         }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[t][i] += acc2[t][i];
         uint32_t ua[4];  // U^T / X^T as the A fragment of the update
         ua[0] = pack2(acc[0][0], acc[0][1]);
         ua[1] = pack2(acc[0][2], acc[0][3]);
