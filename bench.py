@@ -59,6 +59,8 @@ DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
 BACKWARD_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_bwd.cu"]
 BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of HBM roofline (dominant kernel)"
 BACKWARD_KERNELS = ["prep", "forward_pass", "reverse_pass", "local_gradients"]
+# the tensor-core path runs both serial passes in one launch
+BACKWARD_KERNELS_TC = ["prep", "serial_passes", "local_gradients"]
 # fp32 FMA peak of the SIMT backward: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
@@ -95,15 +97,15 @@ def bwd_kernel_bytes(x):
         return None
     rows = [max(0, b - a) for a, b in zip(x.cu_host[:-1], x.cu_host[1:])]
     tile, rec, ops, ut = 34816, 44352, 14336, 8192
-    tot = [0, 0, 0, 0]
+    tot = [0, 0, 0]
     for n_rows in rows:
         for c0 in range(0, n_rows, 16):
             L = min(16, n_rows - c0)
             tot[0] += L * (3 * 256 + 512 + 4) + rec
-            tot[1] += 2 * 4352 + 512 + ut + tile
-            tot[2] += ops + L * 256 + tile
-            tot[3] += 2 * tile + rec + L * (2 * 256 + 512) + L * (3 * 256 + 512 + 4)
-    return [t * x.n_heads for t in tot]
+            tot[1] += 2 * 4352 + 512 + ut + tile      # forward serial pass
+            tot[1] += ops + L * 256 + tile            # reverse serial pass
+            tot[2] += 2 * tile + rec + L * (2 * 256 + 512) + L * (3 * 256 + 512 + 4)
+    return [t * x.n_heads for t in tot[:3]]
 
 
 def algorithmic_bytes(x) -> int:
@@ -599,17 +601,20 @@ def run_backward(args):
     mean_s = statistics.mean(s_.elapsed_time(e) for s_, e in zip(starts, ends)) * 1e-3
     peaks = measured_peaks()
     kbytes = bwd_kernel_bytes(x)
+    names = BACKWARD_KERNELS
+    if kbytes is not None:  # three launches: prep, both serial passes, local gradients
+        names, kernel_ms = BACKWARD_KERNELS_TC, [kernel_ms[0], kernel_ms[1] + kernel_ms[2], kernel_ms[3]]
     kernels = {nm: {"ms": round(t, 4), "share": round(t / sum(kernel_ms), 4)}
-               for nm, t in zip(BACKWARD_KERNELS, kernel_ms)}
+               for nm, t in zip(names, kernel_ms)}
     if kbytes is not None:
-        for nm, b, t in zip(BACKWARD_KERNELS, kbytes, kernel_ms):
+        for nm, b, t in zip(names, kbytes, kernel_ms):
             kernels[nm].update(bytes=b, gbs=round(b / (t * 1e-3) / 1e9, 1))
-        top = max(range(4), key=lambda i: kernel_ms[i])
+        top = max(range(len(names)), key=lambda i: kernel_ms[i])
         achieved = kbytes[top] / (kernel_ms[top] * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": BACKWARD_KERNELS[top], "achieved": round(achieved, 1),
+        roofline = {"bound": "hbm", "kernel": names[top], "achieved": round(achieved, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "traffic": recorded_traffic(f"{x.name}:{BACKWARD_KERNELS[top]}", BACKWARD_SOURCES),
+                    "traffic": recorded_traffic(f"{x.name}:{names[top]}", BACKWARD_SOURCES),
                     "algorithmic_bytes_per_launch": kbytes[top],
                     "launch_ms": round(kernel_ms[top], 4),
                     "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)"}

@@ -203,6 +203,10 @@ __device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
 }
+__device__ __forceinline__ void stsm4(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
+                 ::"r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
@@ -632,6 +636,7 @@ constexpr int PO = 40;                   // bf16 pitch of the [16][32] dO slice 
 // U~^T [32][16] fp32 (forward) or dO [16][PO] bf16 (reverse)
 constexpr int SL_K = TR_K, SL_W = TR_W, SL_Q = TR_Q, SL_P = TR_P, SL_G = TR_G, SL_X = TR_OPS;
 constexpr int SLOT = SL_X + 32 * C * 4;
+constexpr int CT_ROWS = 16 * 136 * 2;    // a chain warp's 16 rows of a bf16 state tile
 static_assert(SL_X % 16 == 0 && SLOT % 16 == 0, "16-byte aligned slot parts");
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -684,15 +689,18 @@ __device__ __forceinline__ void mul2(float &a, float &b, float ga, float gb) {
 }
 
 template <bool REVERSE>
-__global__ void __launch_bounds__(128, 1)
-    chain_tc_kernel(const int32_t *__restrict__ cu, unsigned char *__restrict__ ws,
-                    const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ init,
-                    float *__restrict__ final_state, int H, float scale) {
+__device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned long long *bars,
+                                           const int32_t *__restrict__ cu,
+                                           unsigned char *__restrict__ ws,
+                                           const __nv_bfloat16 *__restrict__ dout,
+                                           const float *__restrict__ init,
+                                           float *__restrict__ final_state, int H, float scale) {
     constexpr int D = 128;
-    extern __shared__ __align__(16) unsigned char smc[];
-    __shared__ __align__(8) unsigned long long bars[2 * NS];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int item = blockIdx.x / 4, r4 = blockIdx.x % 4;
+    // roles by warp: chain warps 0, 1 and loader warp 2 (forward); the reverse pass takes
+    // warps 2, 3 as chain warps and 0 as loader, so that a forward and a reverse CTA on
+    // one SM put their four chain warps on four different schedulers
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) ^ (REVERSE ? 2 : 0);
+    const int item = blk / 4, r4 = blk % 4;
     const int n = item / H, h = item % H;
     const int v0 = 32 * r4;  // first value column of this CTA
     const int64_t t0 = cu[n], t1 = cu[n + 1];
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(128, 1)
     const size_t rstride = (size_t)H * REC_TC;
     auto full = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[s])); };
     auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             bar_init(full(s), 1);   // the copies' issue
             bar_init(empty(s), 2);  // one arrival per chain warp
@@ -776,12 +784,26 @@ __global__ void __launch_bounds__(128, 1)
             dst[(size_t)(kc + 1) * D + v + 8] = S[j][3];
         }
     };
-    auto write_tile = [&](unsigned char *dst) {  // bf16 S^T [v][136]: rows v, key pairs
+    // this warp's 16 rows of the bf16 S^T tile [v][136]: staged in shared memory by
+    // stmatrix (a double buffer per warp), then one bulk copy of the 4352 contiguous bytes
+    const uint32_t stage = sbase + NS * SLOT + sw * 2 * CT_ROWS;
+    auto write_tile = [&](unsigned char *dst, int buf) {
+        if (lane == 0)  // the copy that last read this buffer (two chunks ago) is done
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        const uint32_t sb2 = stage + buf * CT_ROWS;
+        const int mi = lane >> 3, r = lane & 7;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int kc = 8 * j + 2 * l4, v = vr + g4;
-            *reinterpret_cast<uint32_t *>(dst + ((size_t)v * 136 + kc) * 2) = pack2(S[j][0], S[j][1]);
-            *reinterpret_cast<uint32_t *>(dst + ((size_t)(v + 8) * 136 + kc) * 2) = pack2(S[j][2], S[j][3]);
+        for (int j = 0; j < 16; j += 2)
+            stsm4(sb2 + (uint32_t)((((mi & 1) * 8 + r) * 136 + 8 * (j + (mi >> 1))) * 2),
+                  pack2(S[j][0], S[j][1]), pack2(S[j][2], S[j][3]), pack2(S[j + 1][0], S[j + 1][1]),
+                  pack2(S[j + 1][2], S[j + 1][3]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         ::"l"(dst + (size_t)vr * 272), "r"(sb2), "r"((uint32_t)CT_ROWS) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
     };
     for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
@@ -790,7 +812,7 @@ __global__ void __launch_bounds__(128, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t sl = sbase + s * SLOT;
         const float4 *G4 = reinterpret_cast<const float4 *>(smc + s * SLOT + SL_G);
-        write_tile(rec0 + (size_t)c * rstride + (REVERSE ? TC_DS : TC_S));
+        write_tile(rec0 + (size_t)c * rstride + (REVERSE ? TC_DS : TC_S), m & 1);
         float acc[2][4];  // U^T (forward) or X^T (reverse): 16 value rows x 16 tokens
         if (!REVERSE) {
             const float *tu = reinterpret_cast<const float *>(smc + s * SLOT + SL_X);
@@ -870,6 +892,23 @@ __global__ void __launch_bounds__(128, 1)
         if (lane == 0) bar_arrive(empty(s));  // this warp's reads of the slot are done
     }
     if (final_state) write_state(final_state + hidx);
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Both serial passes in one launch: they are independent (the reverse pass reads only the
+// records and dO), and each leaves most of an SM idle. Blocks [0, nfwd) run the forward
+// pass, the rest the reverse pass; two CTAs fit on an SM.
+__global__ void __launch_bounds__(128, 2)
+    chains_tc_kernel(const int32_t *__restrict__ cu, unsigned char *__restrict__ ws,
+                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ h0,
+                     const float *__restrict__ dh_final, float *__restrict__ dh0, int H,
+                     float scale, int nfwd) {
+    extern __shared__ __align__(16) unsigned char smc[];
+    __shared__ __align__(8) unsigned long long bars[2 * NS];
+    if ((int)blockIdx.x < nfwd)
+        chain_body<false>(blockIdx.x, smc, bars, cu, ws, dout, h0, nullptr, H, scale);
+    else
+        chain_body<true>(blockIdx.x - nfwd, smc, bars, cu, ws, dout, dh_final, dh0, H, scale);
 }
 
 // ---- 3. local gradients of every chunk
@@ -1892,10 +1931,9 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
         // serial passes with the state in mma fragments, then the local gradients with one
         // CTA per SM over all (chunk slot, head) items
         unsigned char *wsb = reinterpret_cast<unsigned char *>(p.workspace);
-        const int smc = NS * SLOT;
+        const int smc = NS * SLOT + 4 * CT_ROWS;
         int dev = 0, sms = 0;
-        if ((e = cudaFuncSetAttribute(chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
+        if ((e = cudaFuncSetAttribute(chains_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smc)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LS_BYTES)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PS_BYTES)) != cudaSuccess ||
             (e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -1912,11 +1950,9 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
                                                                p.cu_seqlens, wsb, H, p.n_seq,
                                                                n_items, scale);
         tev.mark(1);
-        chain_tc_kernel<false><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0,
-                                                                nullptr, H, scale);
-        tev.mark(2);
-        chain_tc_kernel<true><<<items * 4, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.dh_final,
-                                                               p.dh0, H, scale);
+        chains_tc_kernel<<<items * 8, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0, p.dh_final,
+                                                         p.dh0, H, scale, (int)(items * 4));
+        tev.mark(2);  // both serial passes in the one launch: the reverse pass's entry is 0
         tev.mark(3);
         const int grid = (int)(n_items < sms ? n_items : sms);
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
@@ -1944,7 +1980,7 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
         tev.mark(4);
     }
     e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(4);
+    if (e == cudaSuccess) count_launches(use_tc ? 3 : 4);
     return e;
 }
 

@@ -272,10 +272,11 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
  * kda_bwd_timing_start / kda_bwd_timing_read -- device time of each kernel of the
  * backward pass, for measurement (an addition of this library: the pages have no
  * counterpart). After kda_bwd_timing_start(capacity) the next `capacity` calls of
- * kda_chunk_bwd or kda_chunk_bwd_static_scratch record a CUDA event on their stream before
- * their first kernel and after each of their four kernels (state-independent chunk
- * products; forward serial pass; reverse serial pass; local gradients). Recording adds no
- * synchronisation. kda_bwd_timing_read waits for those events, writes the milliseconds of
+ * kda_chunk_bwd or kda_chunk_bwd_static_scratch record CUDA events on their stream around
+ * their kernels: ms[0] the state-independent chunk products, ms[1] the forward serial
+ * pass, ms[2] the reverse serial pass, ms[3] the local gradients. The tensor-core path
+ * runs both serial passes in one launch: its time is in ms[1] and ms[2] is about 0.
+ * Recording adds no synchronisation. kda_bwd_timing_read waits for those events, writes the milliseconds of
  * each kernel summed over the recorded calls to ms[0..3] (host array of 4) and the number
  * of recorded calls to *calls (host), and stops recording. One recording at a time per
  * process; a new start discards the previous one. Errors: KDA_ERR_INVALID_ARG for

@@ -121,7 +121,8 @@ def test_kernel_timing_records_every_call():
     for _ in range(3):
         got = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)
     ms, calls = kda.bwd_timing_read()
-    assert calls == 3 and all(t > 0 for t in ms), (ms, calls)
+    # the serial passes share one launch on this path: their time is in ms[1]
+    assert calls == 3 and ms[0] > 0 and ms[1] > 0 and ms[3] > 0 and ms[2] >= 0, (ms, calls)
     kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)  # not recorded
     assert kda.bwd_timing_read()[1] == 3
     torch.cuda.synchronize()
