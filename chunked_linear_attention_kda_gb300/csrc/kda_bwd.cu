@@ -36,6 +36,7 @@
 // strictly increasing over all chunks, below (n_tok >> 4) + n_seq + 1.
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <mutex>
 #include <vector>
 
@@ -1184,16 +1185,57 @@ __device__ bool decode_item(const int32_t *cu, int n_seq, int H, long long idx, 
     it.c = (int)(slot - ((long long)(cu[lo] >> 4) + lo));
     return it.c < (cu[lo + 1] - cu[lo] + C - 1) / C;
 }
-__device__ long long next_valid_item(const int32_t *cu, int n_seq, int H, long long i, long long end,
-                                     Item &it) {
-    while (i < end && !decode_item(cu, n_seq, H, i, it)) ++i;
-    return i;
-}
 __device__ __forceinline__ int item_rows(const int32_t *cu, const Item &it, int64_t &c0) {
     c0 = cu[it.n] + (int64_t)it.c * C;
     const int64_t left = cu[it.n + 1] - c0;
     return (int)(left < C ? left : C);
 }
+// Walks items idx = slot H + h in increasing order: one division and binary search at the
+// start, then a step per item (the next sequence's slots looked up as they are reached);
+// items of slots that hold no chunk are skipped.
+struct ItemCursor {
+    const int32_t *cu;
+    int n_seq, H, h, n, nc;
+    long long idx, end, slot, b0, b1;  // b0, b1: the first slots of sequences n and n + 1
+    __device__ void load_seq() {
+        b0 = (long long)(cu[n] >> 4) + n;
+        b1 = n + 1 < n_seq ? (long long)(cu[n + 1] >> 4) + n + 1 : LLONG_MAX;
+        nc = (cu[n + 1] - cu[n] + C - 1) / C;
+    }
+    __device__ void start(const int32_t *cu_, int n_seq_, int H_, long long beg, long long end_) {
+        cu = cu_;
+        n_seq = n_seq_;
+        H = H_;
+        end = end_;
+        idx = beg;
+        slot = beg / H;
+        h = (int)(beg - slot * H);
+        Item it;
+        decode_item(cu, n_seq, H, beg, it);
+        n = it.n;
+        load_seq();
+        skip();
+    }
+    __device__ void step() {
+        ++idx;
+        if (++h == H) {
+            h = 0;
+            ++slot;
+            while (slot >= b1) {
+                ++n;
+                load_seq();
+            }
+        }
+    }
+    __device__ void skip() {
+        while (idx < end && slot - b0 >= nc) step();
+    }
+    __device__ void advance() {
+        step();
+        skip();
+    }
+    __device__ Item item() const { return Item{n, h, (int)(slot - b0)}; }
+};
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
     local_tc_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
@@ -1222,7 +1264,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     }
     __syncthreads();
 
-    auto next_valid = [&](long long i, Item &it) { return next_valid_item(cu, n_seq, H, i, end, it); };
     auto rows_of = [&](const Item &it, int64_t &c0) { return item_rows(cu, it, c0); };
     auto rec_of = [&](const Item &it) {
         return ws + (slot_of(cu, it.n, it.c) * H + it.h) * REC_TC;
@@ -1267,14 +1308,18 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         if (lane < L) prefetch_l2(a + ((size_t)(c0 + lane) * H + it.h) * D, D * 4);
     };
 
-    Item cur, nxt;
-    long long idx = next_valid(beg, cur);
+    ItemCursor ic;
+    ic.start(cu, n_seq, H, beg, end);
+    Item cur = ic.item(), nxt;
+    long long idx = ic.idx;
     if (idx < end && warp == 0) {
         issue_rec(cur, 0);
         if (lane == 0) issue_states(cur);
     }
     for (int m = 0; idx < end; ++m) {
-        const long long nidx = next_valid(idx + 1, nxt);
+        ic.advance();
+        const long long nidx = ic.idx;
+        nxt = ic.item();
         const bool more = nidx < end;
         __syncthreads();  // the other record buffer's readers (the previous item) are done
         if (more) {
@@ -1530,7 +1575,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                 for (int e = 0; e < 2; ++e) {
                     const int fi = 2 * hh + e;
                     const float G = GS[t * GP + key + e], GL = GS[(C - 1) * GP + key + e];
-                    const float eg = expf(G), en = expf(-G), ep = expf(GL - G);
+                    const float eg = __expf(G), en = __expf(-G), ep = __expf(GL - G);
                     const float Qt = e ? q2.y : q2.x, Kt = e ? t2.y : t2.x;
                     const float Kh = e ? h2.y : h2.x, Kp = e ? p2.y : p2.x;
                     const float gq = dqa[tt][fi], gt = dkt[tt][fi], gh = dkh[tt][fi], gp = dkp[tt][fi];
@@ -1577,7 +1622,8 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                 const int t = g4 + 8 * hh;
                 if (t < L) {
                     const float2 ax = av[tt][hh];
-                    const float s0 = 1.f / (1.f + expf(-ax.x)), s1 = 1.f / (1.f + expf(-ax.y));
+                    const float s0 = __fdividef(1.f, 1.f + __expf(-ax.x));
+                    const float s1 = __fdividef(1.f, 1.f + __expf(-ax.y));
                     const size_t o = ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4;
                     *reinterpret_cast<float2 *>(da + o) =
                         make_float2(dG[tt][2 * hh] * (kGMin * s0 * (1.f - s0)),
@@ -1666,11 +1712,15 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
     };
 
-    Item cur, nxt;
-    long long idx = next_valid_item(cu, n_seq, H, beg, end, cur);
+    ItemCursor ic;
+    ic.start(cu, n_seq, H, beg, end);
+    Item cur = ic.item(), nxt;
+    long long idx = ic.idx;
     if (idx < end && warp == 0) issue_in(cur, 0);
     for (int m = 0; idx < end; ++m) {
-        const long long nidx = next_valid_item(cu, n_seq, H, idx + 1, end, nxt);
+        ic.advance();
+        const long long nidx = ic.idx;
+        nxt = ic.item();
         const bool more = nidx < end;
         int64_t c0;
         const int L = item_rows(cu, cur, c0);
@@ -1697,11 +1747,11 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             float G = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float g = r < L ? kGMin / (1.f + expf(-Ain[r * D + tid])) : 0.f;
+                const float g = r < L ? __fdividef(kGMin, 1.f + __expf(-Ain[r * D + tid])) : 0.f;
                 G += g;
                 GS[r * GP + tid] = G;
             }
-            const float gl = expf(G);
+            const float gl = __expf(G);
             reinterpret_cast<float *>(rec + TR_GL)[tid] = gl;
             reinterpret_cast<float *>(rec + TR_G)[gperm_tc(tid)] = gl;
         }
@@ -1724,10 +1774,11 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                     const int x = x0 + 2 * p2 + e;
                     const float G = GS[r * GP + x], GL = GS[(C - 1) * GP + x];
                     const float qx = e ? qf.y : qf.x, kx = e ? kf.y : kf.x;
-                    Qt[e] = qx * expf(G);
-                    Kt[e] = kx * expf(G);
-                    Kh[e] = kx * expf(-G);
-                    Kp[e] = kx * expf(GL - G);
+                    const float eg = __expf(G), en = __expf(-G);
+                    Qt[e] = qx * eg;
+                    Kt[e] = kx * eg;
+                    Kh[e] = kx * en;
+                    Kp[e] = kx * __expf(GL - G);
                 }
                 okp[p2] = pack2(Kp[0], Kp[1]);
                 split2(Qt[0], Qt[1], oqh[p2], oql[p2]);
