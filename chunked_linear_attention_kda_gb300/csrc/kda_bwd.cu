@@ -1413,7 +1413,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         // ---- phase 2 (key channels [n0, n0 + 16)): dQ~ = s dO S^T, dK' = U dS_end^T,
         // dW = -dU S^T, dgamma_L = diag(dS_end S^T); dW K~^T into the dM partial sum
         float dqa[2][4] = {}, dkp[2][4] = {}, dwa[2][4] = {}, dga[2][4] = {};
-#pragma unroll 2
+#pragma unroll
         for (int k0 = 0; k0 < D; k0 += 16) {  // k = value column
             uint32_t ao[4], au[4], adu[4], ads[4], bs[4], bd[4];
             ld_a(DO, PB, k0, ao);
@@ -1649,7 +1649,8 @@ constexpr int PS_REC = 2 * IBUF;
 constexpr int PS_QL = PS_REC + RECB, PS_KTL = PS_QL + T128;
 constexpr int PS_KHL = PS_KTL + T128, PS_A = PS_KHL + T128, PS_ML = PS_A + C * C * 4;
 constexpr int PS_BT = PS_ML + C * PS * 2;
-constexpr int PS_BYTES = PS_BT + C * 4;
+constexpr int PS_TS = PS_BT + C * 4, PS_YS = PS_TS + C * C * 4, PS_PART = PS_YS + 64 * 4;
+constexpr int PS_BYTES = PS_PART + 8 * C * C * 4;
 static_assert(IBUF % 16 == 0 && PS_QL % 16 == 0 && PS_A % 16 == 0 && 2 * (PS_BYTES + 1024) <= 228 * 1024,
               "two prep CTAs per SM");
 
@@ -1799,14 +1800,17 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
         __syncthreads();
 
-        // ---- Z = K~ K^^T (warp 0), P = Q~ K^^T (warp 1), split-bf16 products
-        if (warp < 2) {
-            const uint32_t ah_b = warp == 0 ? sb + PS_REC + TR_KT : sb + PS_REC + TR_Q;
-            const uint32_t al_b = warp == 0 ? sb + PS_KTL : sb + PS_QL;
+        // ---- Z = K~ K^^T and P = Q~ K^^T, split-bf16 products: warp w takes product w & 1
+        // over key channels [32 (w >> 1), +32); the four partial sums are added in order
+        float *part = reinterpret_cast<float *>(sp + PS_PART);  // [8 warps][16][16]
+        {
+            const int prod = warp & 1, kq = warp >> 1;
+            const uint32_t ah_b = prod == 0 ? sb + PS_REC + TR_KT : sb + PS_REC + TR_Q;
+            const uint32_t al_b = prod == 0 ? sb + PS_KTL : sb + PS_QL;
             const uint32_t bh_b = sb + PS_REC + TR_KH, bl_b = sb + PS_KHL;
             float c0a[2][4] = {}, c1a[2][4] = {}, c2a[2][4] = {};
 #pragma unroll
-            for (int k0 = 0; k0 < D; k0 += 16) {
+            for (int k0 = 32 * kq; k0 < 32 * kq + 32; k0 += 16) {
                 uint32_t ah[4], al[4], bh[4], bl[4];
                 ld_a(ah_b, PB, k0, ah);
                 ld_a(al_b, PB, k0, al);
@@ -1819,53 +1823,79 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                 mma16816(c2a[0], ah, bl[0], bl[1]);
                 mma16816(c2a[1], ah, bl[2], bl[3]);
             }
+            float *pw = part + warp * C * C;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = g4 + 8 * (i >> 1), j = 8 * tt + 2 * l4 + (i & 1);
-                    const float x = c0a[tt][i] + (c1a[tt][i] + c2a[tt][i]);
-                    if (warp == 0) {
-                        reinterpret_cast<float *>(rec + TR_Z)[r * C + j] = x;
-                        As[r * C + j] = j < r ? bts[r] * x : 0.f;
-                    } else {
-                        reinterpret_cast<__nv_bfloat16 *>(rec + TR_P)[r * PS + j] =
-                            __float2bfloat16_rn(j <= r ? x : 0.f);
-                    }
-                }
+                for (int hh = 0; hh < 2; ++hh)
+                    *reinterpret_cast<float2 *>(pw + (g4 + 8 * hh) * C + 8 * tt + 2 * l4) =
+                        make_float2(c0a[tt][2 * hh] + (c1a[tt][2 * hh] + c2a[tt][2 * hh]),
+                                    c0a[tt][2 * hh + 1] + (c1a[tt][2 * hh + 1] + c2a[tt][2 * hh + 1]));
+        }
+        __syncthreads();
+        {
+            const int r = tid >> 4, j = tid & 15;
+            const float z = part[0 * C * C + tid] + part[2 * C * C + tid] + part[4 * C * C + tid] +
+                            part[6 * C * C + tid];
+            const float pq = part[1 * C * C + tid] + part[3 * C * C + tid] + part[5 * C * C + tid] +
+                             part[7 * C * C + tid];
+            reinterpret_cast<float *>(rec + TR_Z)[tid] = z;
+            As[tid] = j < r ? bts[r] * z : 0.f;
+            reinterpret_cast<__nv_bfloat16 *>(rec + TR_P)[r * PS + j] = __float2bfloat16_rn(j <= r ? pq : 0.f);
         }
         __syncthreads();
 
-        // ---- T = (I + A)^-1 by forward substitution, lane j = column j; M = T diag(beta)
+        // ---- T = (I + A)^-1 in 8 x 8 blocks on warp 0: T11 = (I + A11)^-1 (lanes 0-7, one
+        // column each) and T22 = (I + A22)^-1 (lanes 8-15) by forward substitution, then
+        // T21 = -T22 (A21 T11); T12 = 0
+        float *Ts = reinterpret_cast<float *>(sp + PS_TS), *Ys = reinterpret_cast<float *>(sp + PS_YS);
         if (warp == 0) {
-            const int j = lane & 15;
-            float col[C];
+            const int o = lane & 8, j = lane & 7;
+            float col[8];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float x0 = r == j ? 1.f : 0.f, x1 = 0.f;
+            for (int r = 0; r < 8; ++r) {
+                float x = r == j ? 1.f : 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) {
-                    if (i & 1) x1 = fmaf(-As[r * C + i], col[i], x1);
-                    else x0 = fmaf(-As[r * C + i], col[i], x0);
-                }
-                col[r] = x0 + x1;
+                for (int i = 0; i < r; ++i) x = fmaf(-As[(o + r) * C + o + i], col[i], x);
+                col[r] = x;
             }
-            if (lane < C) {
-                float *Tr = reinterpret_cast<float *>(rec + TR_T);
-                float *TTr = reinterpret_cast<float *>(rec + TR_TT);
-                __nv_bfloat16 *Mh = reinterpret_cast<__nv_bfloat16 *>(rec + TR_M);
-                __nv_bfloat16 *Ml = reinterpret_cast<__nv_bfloat16 *>(sp + PS_ML);
-                const float bj = bts[j];
+            if (lane < 16) {
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    Tr[r * C + j] = col[r];
-                    TTr[j * C + r] = col[r];
-                    const float mv = col[r] * bj;
-                    const __nv_bfloat16 mh = __float2bfloat16_rn(mv);
-                    Mh[r * PS + j] = mh;
-                    Ml[r * PS + j] = __float2bfloat16_rn(mv - __bfloat162float(mh));
+                for (int r = 0; r < 8; ++r) {
+                    Ts[(o + r) * C + o + j] = col[r];
+                    if (o == 0) Ts[r * C + 8 + j] = 0.f;
                 }
             }
+            __syncwarp();
+#pragma unroll
+            for (int e = lane; e < 64; e += 32) {  // Y = A21 T11
+                const int r = 8 + (e >> 3), jj = e & 7;
+                float y = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y = fmaf(As[r * C + i], Ts[i * C + jj], y);
+                Ys[e] = y;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int e = lane; e < 64; e += 32) {  // T21 = -T22 Y
+                const int r = 8 + (e >> 3), jj = e & 7;
+                float t = 0.f;
+#pragma unroll
+                for (int i = 8; i < C; ++i) t = fmaf(Ts[r * C + i], Ys[(i - 8) * 8 + jj], t);
+                Ts[r * C + jj] = -t;
+            }
+        }
+        __syncthreads();
+        {  // T, T^T and M = T diag(beta) (high and low bf16 parts) into the record
+            const int r = tid >> 4, j = tid & 15;
+            const float tv = Ts[tid];
+            reinterpret_cast<float *>(rec + TR_T)[tid] = tv;
+            reinterpret_cast<float *>(rec + TR_TT)[j * C + r] = tv;
+            const float mv = tv * bts[j];
+            const __nv_bfloat16 mh = __float2bfloat16_rn(mv);
+            reinterpret_cast<__nv_bfloat16 *>(rec + TR_M)[r * PS + j] = mh;
+            reinterpret_cast<__nv_bfloat16 *>(sp + PS_ML)[r * PS + j] =
+                __float2bfloat16_rn(mv - __bfloat162float(mh));
         }
         __syncthreads();
 
