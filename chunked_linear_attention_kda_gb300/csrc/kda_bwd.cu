@@ -358,10 +358,11 @@ __device__ __forceinline__ void cp_async16(float *dst, const float *src) {
 
 // Stage one chunk's products for value columns [j0, j0 + JS): K' and W (and Q~, P when
 // chain) whole, U~ only for those columns, gamma_L. 16-byte copies when every piece is a
-// multiple of 4 floats (d_k, d_v multiples of 4), 4-byte copies otherwise.
+// multiple of 4 floats (d_k, d_v multiples of 4) and the record starts on a 16-byte
+// boundary (the workspace need only be 4-byte aligned), 4-byte copies otherwise.
 __device__ void stage(float *dst, const float *rec, int dk, int dv, int j0, bool chain) {
     const int tid = threadIdx.x;
-    const bool v4 = (dk & 3) == 0 && (dv & 3) == 0;
+    const bool v4 = (dk & 3) == 0 && (dv & 3) == 0 && (reinterpret_cast<uintptr_t>(rec) & 15) == 0;
     if (v4) {
         for (int i = tid; i < C * dk / 4; i += kThreads) {
             cp_async16(dst + 4 * i, rec + P_KP(dk) + 4 * i);
@@ -1993,9 +1994,13 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
     // bf16 I/O at d_k = d_v = 128 runs on the tensor cores (bf16 operand rounding is within
     // that I/O's precision) when the bulk copies' 16-byte alignment holds; fp32 FMA loops
     // otherwise
-    auto al16 = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
-    const bool use_tc = sizeof(IO) == 2 && dk == 128 && dv == 128 && al16(p.workspace) &&
-                        al16(p.q) && al16(p.k) && al16(p.v) && al16(p.a) && al16(p.dout);
+    // (inputs and workspace: 16-byte bulk copies; dq, dk, dv: 4-byte pair stores; dgate:
+    // 8-byte pair stores)
+    auto al = [](const void *x, uintptr_t m) { return ((uintptr_t)x & (m - 1)) == 0; };
+    const bool use_tc = sizeof(IO) == 2 && dk == 128 && dv == 128 && al(p.workspace, 16) &&
+                        al(p.q, 16) && al(p.k, 16) && al(p.v, 16) && al(p.a, 16) &&
+                        al(p.dout, 16) && al(p.dq, 4) && al(p.dk, 4) && al(p.dv, 4) &&
+                        al(p.da, 8);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) != cudaSuccess)
         return e;

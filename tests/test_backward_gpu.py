@@ -128,3 +128,50 @@ def test_kernel_timing_records_every_call():
     torch.cuda.synchronize()
     for r, g in zip(ref, got):
         assert torch.equal(r, g)
+
+
+def test_many_sequences_per_cta():
+    """Seven sequences (one empty, some shorter than a chunk) over 8 heads: about 3500
+    (chunk, head) items, so every CTA of the chunk-parallel kernels walks across sequence
+    ends and the gap slots between them. Sequences are independent: the oracle checks the
+    three short ones on two heads."""
+    lens = [2000, 0, 700, 17, 1200, 5, 3000]
+    x = K.make_inputs(lens, 8, 128, 128, dtype=torch.bfloat16, device=DEV, seed=21,
+                      h0_std=0.3)
+    dout, dhf = upstream(x, 21)
+    got = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)
+    torch.cuda.synchronize()
+    assert_finite(*got)
+    heads = [1, 6]
+    for n in (2, 3, 5):
+        t0, t1 = x.cu_host[n], x.cu_host[n + 1]
+        sel = lambda t: cpu(t)[t0:t1][:, heads].contiguous()  # noqa: E731
+        ref = B.kda_backward(sel(x.q), sel(x.k), sel(x.v), sel(x.a), sel(x.beta),
+                             cpu(x.h0)[n:n + 1][:, heads], [0, t1 - t0], sel(dout),
+                             cpu(dhf)[n:n + 1][:, heads])
+        for nm, g in zip(NAMES[:5], got[:5]):
+            e = rel_l2(f64(g[t0:t1])[:, heads], ref[nm])
+            assert e <= TOL[torch.bfloat16], f"sequence {n} {nm}: {e:.3e}"
+        e = rel_l2(f64(got[5][n:n + 1])[:, heads], ref["dh0"])
+        assert e <= TOL[torch.bfloat16], f"sequence {n} dh0: {e:.3e}"
+
+
+def test_unaligned_workspace_takes_the_fp32_kernels():
+    """A workspace 4 bytes off a 16-byte boundary (allowed: 4-byte alignment) rules out
+    the bulk copies, so bf16 d = 128 runs on the fp32 kernels: still exact to the bar."""
+    x = K.make_inputs([50, 33], 2, 128, 128, dtype=torch.bfloat16, device=DEV, seed=22,
+                      h0_std=0.3)
+    dout, dhf = upstream(x, 22)
+    lib = kda.load_library()
+    nbytes = lib.kda_chunk_bwd_workspace_bytes(x.n_tok, x.n_seq, 2, 128, 128)
+    raw = torch.empty(nbytes + 16, dtype=torch.uint8, device=DEV)
+    ws = raw[4:4 + nbytes]
+    assert ws.data_ptr() % 16 == 4
+    got = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    ref = B.kda_backward(cpu(x.q), cpu(x.k), cpu(x.v), cpu(x.a), cpu(x.beta), cpu(x.h0),
+                         x.cu_host, cpu(dout), cpu(dhf))
+    for nm, g in zip(NAMES, got):
+        e = rel_l2(f64(g), ref[nm])
+        assert e <= TOL[torch.bfloat16], f"{nm}: {e:.3e}"
