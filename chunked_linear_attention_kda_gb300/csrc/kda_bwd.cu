@@ -1342,6 +1342,20 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         const uint32_t U16 = sb + LS_U, DU16 = sb + LS_DU, DW16 = sb + LS_DW;
         const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ;
 
+        // the gate logits phase 4 needs (prefetched into L2 an item ahead): issued now, so
+        // that their latency passes under phases 1-3
+        float2 av[2][2];
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = g4 + 8 * hh;
+                av[tt][hh] = make_float2(0.f, 0.f);
+                if (t < L)
+                    av[tt][hh] = *reinterpret_cast<const float2 *>(
+                        a + ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4);
+            }
+
         // ---- phase 1 (value columns [n0, n0 + 16)): U = U~ - W S, dU = K' dS_end + s P^T dO,
         // dV = M^T dU; partial sums of dO U^T and dU V^T over these columns
         float u[2][4], du[2][4] = {}, dpp[2][4] = {}, dmp[2][4] = {};
@@ -1524,17 +1538,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         // and K' as the bf16 values the products above used: its terms cancel pairwise
         // across rows (dP_ri Q~_r K^_i enters row r through dQ~ and row i through dK^, and
         // likewise for dZ), exactly only with the same operand values on both sides.
-        float2 av[2][2];
-#pragma unroll
-        for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int t = g4 + 8 * hh;
-                av[tt][hh] = make_float2(0.f, 0.f);
-                if (t < L)
-                    av[tt][hh] = *reinterpret_cast<const float2 *>(
-                        a + ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4);
-            }
         float dkt[2][4] = {}, dkh[2][4] = {};
         {
             uint32_t bkh[4], bb[4], af[4];
@@ -1719,6 +1722,12 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
     Item cur = ic.item(), nxt;
     long long idx = ic.idx;
     if (idx < end && warp == 0) issue_in(cur, 0);
+    auto load_beta = [&](const Item &it) {  // beta of an item's rows, 0 past its end
+        int64_t cb;
+        const int Lb = item_rows(cu, it, cb);
+        return tid < Lb ? beta[(size_t)(cb + tid) * H + it.h] : 0.f;
+    };
+    float bta = (idx < end && tid < C) ? load_beta(cur) : 0.f;  // loaded an item ahead
     for (int m = 0; idx < end; ++m) {
         ic.advance();
         const long long nidx = ic.idx;
@@ -1727,8 +1736,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         int64_t c0;
         const int L = item_rows(cu, cur, c0);
         const int h = cur.h;
-        float bta = 0.f;
-        if (tid < L) bta = beta[(size_t)(c0 + tid) * H + h];
+        const float bta_next = (more && tid < C) ? load_beta(nxt) : 0.f;
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();  // the record staging is free; the other input buffer's readers are done
         if (more && warp == 0) issue_in(nxt, (m + 1) & 1);
@@ -1941,6 +1949,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
         idx = nidx;
         cur = nxt;
+        bta = bta_next;
     }
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
