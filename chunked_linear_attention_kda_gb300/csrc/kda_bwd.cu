@@ -34,7 +34,9 @@
 //      accumulates block by block.
 // The chunk of token start t in sequence n has the workspace slot (cu[n] >> 4) + c + n:
 // strictly increasing over all chunks, below (n_tok >> 4) + n_seq + 1.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include <climits>
 #include <mutex>
@@ -650,6 +652,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 __device__ __forceinline__ void bar_arrive_tx(uint32_t a, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
                  : "memory");
+}
+// a box of a 3-D tensor map (x innermost) into shared memory, completing on mbar
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(mbar) : "memory");
 }
 __device__ __forceinline__ void bar_init(uint32_t a, uint32_t c) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(c));
@@ -1640,6 +1650,19 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 }
 
 // ---- 0b. the tensor-core record (bf16 I/O, d_k = d_v = 128)
+// Phase stamps of the prep kernel (CTA 0, thread 0, first 64 items), compiled only with
+// -DKDA_BWD_TRACE; the default build has no trace code.
+#ifdef KDA_BWD_TRACE
+__device__ long long g_prep_trace[64][12];
+#define PREP_TRACE(i) \
+    do { \
+        if (blockIdx.x == 0 && tid == 0 && m < 64) g_prep_trace[m][i] = clock64(); \
+    } while (0)
+#else
+#define PREP_TRACE(i) \
+    do { \
+    } while (0)
+#endif
 // Two CTAs per SM walk contiguous ranges of items (chunk slot, head). Per item: the q, k, v
 // and gate-logit rows arrive by bulk copies one item ahead (double-buffered); G and gamma_L
 // per key channel; Q~, K~, K^, K' elementwise; Z = K~ K^^T and P = Q~ K^^T on the tensor
@@ -1648,7 +1671,8 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 // U~ = M V with M split the same way. The record is assembled in shared memory in its
 // global layout and written by one bulk copy.
 constexpr int PT_THREADS = 256;
-constexpr int IBUF = 3 * T128 + C * 128 * 4;  // q, k, v rows [16][136] bf16; a rows [16][128] fp32
+constexpr int IT16 = C * 128 * 2;               // a dense bf16 input tile [16][128]
+constexpr int IBUF = 3 * IT16 + C * 128 * 4;     // q, k, v [16][128] bf16; a [16][128] fp32
 constexpr int PS_REC = 2 * IBUF;
 constexpr int PS_QL = PS_REC + RECB, PS_KTL = PS_QL + T128;
 constexpr int PS_KHL = PS_KTL + T128, PS_A = PS_KHL + T128, PS_ML = PS_A + C * C * 4;
@@ -1666,8 +1690,8 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
 }
 
 __global__ void __launch_bounds__(PT_THREADS, 2)
-    prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                   const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
+    prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                    const float *__restrict__ beta, const int32_t *__restrict__ cu,
                    unsigned char *__restrict__ ws, int H, int n_seq, long long n_items,
                    float scale) {
@@ -1688,40 +1712,25 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // warp 0: the q, k, v and gate-logit rows of item it into input buffer b
+    // one thread: the item's 16 token rows of q, k, v and the gate logits into input buffer
+    // b, one tensor copy each (rows past the end of the tensor arrive as zeros; rows past the
+    // sequence's end hold other tokens, masked where they are used)
     auto issue_in = [&](const Item &it, int b) {
-        int64_t c0;
-        const int L = item_rows(cu, it, c0);
-        unsigned char *buf = sp + b * IBUF;
+        const int64_t c0 = cu[it.n] + (int64_t)it.c * C;
         const uint32_t bb = sb + b * IBUF;
-        if (L < C) {  // rows past the sequence's end read as zeros
-            const int pt = (C - L) * (T128 / C / 16), pa = (C - L) * (D * 4 / 16);
-            for (int i = lane; i < 3 * pt + pa; i += 32) {
-                unsigned char *dst = i < 3 * pt
-                                         ? buf + (i / pt) * T128 + L * (T128 / C) + (i % pt) * 16
-                                         : buf + 3 * T128 + L * D * 4 + (i - 3 * pt) * 16;
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        __syncwarp();
-        if (lane == 0) bar_arrive_tx(bar(b), (uint32_t)(L * (3 * D * 2 + D * 4)));
-        __syncwarp();
-        for (int i = lane; i < 4 * L; i += 32) {
-            const int t = i / L, r = i % L;
-            const size_t o = ((size_t)(c0 + r) * H + it.h) * D;
-            if (t < 3)
-                bulk_g2s(bb + t * T128 + r * (T128 / C), (t == 0 ? q : t == 1 ? k : v) + o, D * 2, bar(b));
-            else
-                bulk_g2s(bb + 3 * T128 + r * D * 4, a + o, D * 4, bar(b));
-        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bar_arrive_tx(bar(b), (uint32_t)IBUF);
+        tma_load_3d(bb, &tm_q, 0, it.h, (int)c0, bar(b));
+        tma_load_3d(bb + IT16, &tm_k, 0, it.h, (int)c0, bar(b));
+        tma_load_3d(bb + 2 * IT16, &tm_v, 0, it.h, (int)c0, bar(b));
+        tma_load_3d(bb + 3 * IT16, &tm_a, 0, it.h, (int)c0, bar(b));
     };
 
     ItemCursor ic;
     ic.start(cu, n_seq, H, beg, end);
     Item cur = ic.item(), nxt;
     long long idx = ic.idx;
-    if (idx < end && warp == 0) issue_in(cur, 0);
+    if (idx < end && tid == 0) issue_in(cur, 0);
     auto load_beta = [&](const Item &it) {  // beta of an item's rows, 0 past its end
         int64_t cb;
         const int Lb = item_rows(cu, it, cb);
@@ -1737,9 +1746,13 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         const int L = item_rows(cu, cur, c0);
         const int h = cur.h;
         const float bta_next = (more && tid < C) ? load_beta(nxt) : 0.f;
+        PREP_TRACE(0);
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        PREP_TRACE(1);
         __syncthreads();  // the record staging is free; the other input buffer's readers are done
-        if (more && warp == 0) issue_in(nxt, (m + 1) & 1);
+        PREP_TRACE(2);
+        if (more && tid == 0) issue_in(nxt, (m + 1) & 1);
+        PREP_TRACE(3);
         if (tid < C) {
             bts[tid] = bta;
             reinterpret_cast<float *>(rec + TR_B)[tid] = bta;
@@ -1747,13 +1760,14 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         const int ib = m & 1;
         const bool ok = bar_wait(bar(ib), (uint32_t)((m >> 1) & 1));
         if (__syncthreads_or(!ok)) break;
+        PREP_TRACE(4);
         const unsigned char *in = sp + ib * IBUF;
         const uint32_t inb = sb + ib * IBUF;
         float *GS = reinterpret_cast<float *>(rec + TR_GS);
 
         // ---- G = cumsum of g = -5 sigmoid(a) per key channel, gamma_L = e^{G_15}
         if (tid < D) {
-            const float *Ain = reinterpret_cast<const float *>(in + 3 * T128);
+            const float *Ain = reinterpret_cast<const float *>(in + 3 * IT16);
             float G = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
@@ -1764,14 +1778,21 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             const float gl = __expf(G);
             reinterpret_cast<float *>(rec + TR_GL)[tid] = gl;
             reinterpret_cast<float *>(rec + TR_G)[gperm_tc(tid)] = gl;
+        } else if (L < C) {  // V rows past the sequence's end to zero (they meet M's zero columns)
+            unsigned char *vt = sp + ib * IBUF + 2 * IT16;
+            for (int i = tid - D; i < (C - L) * 16; i += PT_THREADS - D)
+                *reinterpret_cast<uint4 *>(vt + L * 256 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the buffer's next copy
         }
         __syncthreads();
 
+        PREP_TRACE(5);
         // ---- Q~ = q e^G, K~ = k e^G, K^ = k e^-G, K' = k e^{G_15 - G}: 8 channels per thread
         {
             const int r = tid >> 4, x0 = (tid & 15) * 8;
-            const uint4 qr = *reinterpret_cast<const uint4 *>(in + (r * 136 + x0) * 2);
-            const uint4 kr = *reinterpret_cast<const uint4 *>(in + T128 + (r * 136 + x0) * 2);
+            uint4 qr = *reinterpret_cast<const uint4 *>(in + (r * 128 + x0) * 2);
+            uint4 kr = *reinterpret_cast<const uint4 *>(in + IT16 + (r * 128 + x0) * 2);
+            if (r >= L) qr = kr = make_uint4(0u, 0u, 0u, 0u);  // past the sequence's end
             const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w}, kw[4] = {kr.x, kr.y, kr.z, kr.w};
             uint32_t okp[4], okt[4], okh[4], oqh[4], oql[4], oktl[4], okhl[4];
 #pragma unroll
@@ -1809,6 +1830,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
         __syncthreads();
 
+        PREP_TRACE(6);
         // ---- Z = K~ K^^T and P = Q~ K^^T, split-bf16 products: warp w takes product w & 1
         // over key channels [32 (w >> 1), +32); the four partial sums are added in order
         float *part = reinterpret_cast<float *>(sp + PS_PART);  // [8 warps][16][16]
@@ -1854,6 +1876,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
         __syncthreads();
 
+        PREP_TRACE(7);
         // ---- T = (I + A)^-1 in 8 x 8 blocks on warp 0: T11 = (I + A11)^-1 (lanes 0-7, one
         // column each) and T22 = (I + A22)^-1 (lanes 8-15) by forward substitution, then
         // T21 = -T22 (A21 T11); T12 = 0
@@ -1895,6 +1918,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             }
         }
         __syncthreads();
+        PREP_TRACE(8);
         {  // T, T^T and M = T diag(beta) (high and low bf16 parts) into the record
             const int r = tid >> 4, j = tid & 15;
             const float tv = Ts[tid];
@@ -1908,6 +1932,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         }
         __syncthreads();
 
+        PREP_TRACE(9);
         // ---- W = M K~ (stored as -W, bf16) and U~ = M V (fp32, transposed): columns [n0, n0 + 16)
         {
             uint32_t mh[4], ml[4], bh[4], bl[4], bv[4];
@@ -1915,7 +1940,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             ld_a(sb + PS_ML, PS, 0, ml);
             ld_b_kn(sb + PS_REC + TR_KT, PB, 0, n0, bh);  // B[t][x] = K~[t][x]
             ld_b_kn(sb + PS_KTL, PB, 0, n0, bl);
-            ld_b_kn(inb + 2 * T128, PB, 0, n0, bv);      // B[t][v] = V[t][v]
+            ld_b_kn(inb + 2 * IT16, 128, 0, n0, bv);     // B[t][v] = V[t][v]
             float w[2][4] = {}, w2[2][4] = {}, u[2][4] = {}, u2[2][4] = {};
             mma16816(w[0], mh, bh[0], bh[1]);
             mma16816(w[1], mh, bh[2], bh[3]);
@@ -1939,6 +1964,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
             }
             store_c16(reinterpret_cast<__nv_bfloat16 *>(rec + TR_W), PB, n0, w);
         }
+        PREP_TRACE(10);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the record, to the copy
         __syncthreads();
         if (tid == 0) {
@@ -1947,11 +1973,41 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
                          ::"l"(dst), "r"(sb + PS_REC), "r"((uint32_t)RECB) : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
+        PREP_TRACE(11);
         idx = nidx;
         cur = nxt;
         bta = bta_next;
     }
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// [n_tok][H][128] row-major as a 3-D tensor (channel, head, token) with boxes of box_x
+// channels x 1 head x 16 tokens; tokens past n_tok read as zero.
+PFN_cuTensorMapEncodeTiled_v12000 map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+bool token_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x) {
+    auto enc = map_encoder();
+    if (!enc) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)n_tok};
+    cuuint64_t strides[2] = {128 * es, (cuuint64_t)H * 128 * es};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Per-kernel timing of backward calls (a measurement aid): events before the first kernel
@@ -2040,8 +2096,14 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
                                        reinterpret_cast<const __nv_bfloat16 *>(p.k),
                                        reinterpret_cast<const __nv_bfloat16 *>(p.v)};
         const int pgrid = (int)(n_items < 2 * sms ? n_items : 2 * sms);
+        CUtensorMap mq, mk, mv, ma;
+        if (!token_map(&mq, b16[0], false, p.n_tok, H, 128) ||
+            !token_map(&mk, b16[1], false, p.n_tok, H, 128) ||
+            !token_map(&mv, b16[2], false, p.n_tok, H, 128) ||
+            !token_map(&ma, p.a, true, p.n_tok, H, 128))
+            return cudaErrorInvalidValue;
         tev.mark(0);
-        prep_tc_kernel<<<pgrid, PT_THREADS, PS_BYTES, stream>>>(b16[0], b16[1], b16[2], p.a, p.beta,
+        prep_tc_kernel<<<pgrid, PT_THREADS, PS_BYTES, stream>>>(mq, mk, mv, ma, p.beta,
                                                                p.cu_seqlens, wsb, H, p.n_seq,
                                                                n_items, scale);
         tev.mark(1);
@@ -2148,3 +2210,9 @@ cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream)
     return cudaStreamSynchronize(stream);
 }
 }  // namespace kda
+
+#ifdef KDA_BWD_TRACE
+extern "C" int kda_debug_prep_trace_dump(long long *host) {
+    return (int)cudaMemcpyFromSymbol(host, kda::g_prep_trace, sizeof(kda::g_prep_trace));
+}
+#endif
