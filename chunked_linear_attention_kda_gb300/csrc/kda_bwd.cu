@@ -238,6 +238,25 @@ __device__ __forceinline__ void ld_a_t(uint32_t base, int pitch, int k0, int m0,
     const int l = threadIdx.x & 31, j = l >> 3;
     ldsm4t(base + (uint32_t)(((k0 + ((j >> 1) << 3) + (l & 7)) * pitch + m0 + ((j & 1) << 3)) * 2), a);
 }
+// A [16][128] bf16 tile stored as two [16][64] halves, each written by a tensor copy with
+// 128-byte swizzle: the 16-byte chunk k of row r of a half sits at chunk k ^ (r & 7).
+// Address of the 8 elements starting at (r, c0), c0 a multiple of 8:
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int r, int c0) {
+    return base + (uint32_t)((c0 >> 6) * (C * 128) + r * 128 + ((((c0 & 63) >> 3) ^ (r & 7)) << 4));
+}
+// the fragment loaders above, for such tiles
+__device__ __forceinline__ void ld_a_sw(uint32_t base, int k0, uint32_t (&a)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4(sw128(base, l & 15, k0 + (l >> 4) * 8), a);
+}
+__device__ __forceinline__ void ld_b_nk_sw(uint32_t base, int n0, int k0, uint32_t (&b)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4(sw128(base, n0 + (l & 7) + ((l >> 4) << 3), k0 + ((l >> 3) & 1) * 8), b);
+}
+__device__ __forceinline__ void ld_b_kn_sw(uint32_t base, int k0, int n0, uint32_t (&b)[4]) {
+    const int l = threadIdx.x & 31;
+    ldsm4t(sw128(base, k0 + (l & 7) + (((l >> 3) & 1) << 3), n0 + (l >> 4) * 8), b);
+}
 // the accumulator tile (16 rows x columns [n0, n0 + 16)) into bf16 row-major storage
 __device__ __forceinline__ void store_c16(__nv_bfloat16 *dst, int pitch, int n0,
                                           const float (&acc)[2][4]) {
@@ -1167,7 +1186,10 @@ __global__ void __launch_bounds__(kThreads)
 // gradients dq, dk, da, computed on the accumulator fragments); the 16 x 16 adjoint of the
 // solve (phase 3) is one element per thread.
 constexpr int LT_THREADS = 256;
-constexpr int RBUF = RECB + 2 * T128;  // record, then V and dO rows [16][136] bf16
+// record buffer: V and dO rows as two 128-byte-swizzled [16][64] halves each (tensor
+// copies, 1024-byte aligned), then the record
+constexpr int SWT = C * 128 * 2;        // a swizzled [16][128] bf16 tile
+constexpr int RBUF = ((2 * SWT + RECB) + 1023) / 1024 * 1024;
 constexpr int LS_S = 0, LS_DS = ST16, LS_R = 2 * ST16;
 constexpr int LS_U = LS_R + 2 * RBUF, LS_DU = LS_U + T128, LS_DW = LS_DU + T128;
 constexpr int LS_DP = LS_DW + T128, LS_DZ = LS_DP + C * PS * 2;
@@ -1175,7 +1197,8 @@ constexpr int LS_PART = LS_DZ + C * PS * 2;  // per warp: dM, dP partial sums [2
 constexpr int LS_DT = LS_PART + 8 * 2 * C * C * 4, LS_DMS = LS_DT + C * C * 4, LS_Y = LS_DMS + C * C * 4;
 constexpr int LS_DB = LS_Y + C * C * 4;
 constexpr int LS_BYTES = LS_DB + C * 4;
-static_assert(RBUF % 16 == 0 && LS_U % 16 == 0 && LS_DP % 16 == 0 && LS_BYTES <= 227 * 1024,
+static_assert(RBUF % 1024 == 0 && LS_R % 1024 == 0 && LS_U % 16 == 0 && LS_DP % 16 == 0 &&
+                  LS_BYTES <= 227 * 1024,
               "local tensor-core kernel shared memory");
 static_assert(LT_THREADS == C * C, "one thread per element of a 16 x 16 product");
 
@@ -1249,14 +1272,14 @@ struct ItemCursor {
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
-    local_tc_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
-                    const int32_t *__restrict__ cu, const __nv_bfloat16 *__restrict__ dout,
+    local_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ a,
+                    const int32_t *__restrict__ cu, const __grid_constant__ CUtensorMap tm_dout,
                     const unsigned char *__restrict__ ws, __nv_bfloat16 *__restrict__ dq,
                     __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
                     float *__restrict__ da, float *__restrict__ dbeta, int H, int n_seq,
                     long long n_items, float scale) {
     constexpr int D = 128;
-    extern __shared__ __align__(128) unsigned char sl[];
+    extern __shared__ __align__(1024) unsigned char sl[];  // 128-byte-swizzled tensor copies
     __shared__ __align__(8) unsigned long long bars[3];  // states; record buffers 0, 1
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, l4 = lane & 3, n0 = 16 * warp;
@@ -1279,32 +1302,19 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     auto rec_of = [&](const Item &it) {
         return ws + (slot_of(cu, it.n, it.c) * H + it.h) * REC_TC;
     };
-    // warp 0: the record and the V, dO rows of item it into record buffer rb
+    // one thread: the V and dO rows of item it (four tensor copies: two 64-column halves
+    // each) and its record into record buffer rb
     auto issue_rec = [&](const Item &it, int rb) {
-        int64_t c0;
-        const int L = rows_of(it, c0);
-        unsigned char *buf = sl + LS_R + rb * RBUF;
+        const int64_t c0 = cu[it.n] + (int64_t)it.c * C;
         const uint32_t bb = sb + LS_R + rb * RBUF;
-        if (L < C) {  // rows past the sequence's end read as zeros
-            const int per = (C - L) * (T128 / C / 16);  // 16-byte pieces of the missing rows
-            for (int i = lane; i < 2 * per; i += 32) {
-                const int tile = i / per, rest = i % per;
-                *reinterpret_cast<uint4 *>(buf + RECB + tile * T128 + L * (T128 / C) + rest * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bar_arrive_tx(bar(1 + rb), (uint32_t)(2 * SWT + RECB));
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            tma_load_3d(bb + x * (SWT / 2), &tm_v, 64 * x, it.h, (int)c0, bar(1 + rb));
+            tma_load_3d(bb + SWT + x * (SWT / 2), &tm_dout, 64 * x, it.h, (int)c0, bar(1 + rb));
         }
-        __syncwarp();
-        if (lane == 0) {
-            bar_arrive_tx(bar(1 + rb), (uint32_t)(RECB + 2 * L * D * 2));
-            bulk_g2s(bb, rec_of(it) + TC_REC, RECB, bar(1 + rb));
-        }
-        __syncwarp();
-        const int r = lane & 15;
-        if (r < L) {  // lane r: V row r; lane 16 + r: dO row r
-            const __nv_bfloat16 *src = (lane < 16 ? v : dout) + ((size_t)(c0 + r) * H + it.h) * D;
-            bulk_g2s(bb + RECB + (lane >> 4) * T128 + r * (T128 / C), src, D * 2, bar(1 + rb));
-        }
+        bulk_g2s(bb + 2 * SWT, rec_of(it) + TC_REC, RECB, bar(1 + rb));
     };
     auto issue_states = [&](const Item &it) {  // one thread: S and dS_end, adjacent both sides
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1323,9 +1333,9 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     ic.start(cu, n_seq, H, beg, end);
     Item cur = ic.item(), nxt;
     long long idx = ic.idx;
-    if (idx < end && warp == 0) {
+    if (idx < end && tid == 0) {
         issue_rec(cur, 0);
-        if (lane == 0) issue_states(cur);
+        issue_states(cur);
     }
     for (int m = 0; idx < end; ++m) {
         ic.advance();
@@ -1334,7 +1344,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         const bool more = nidx < end;
         __syncthreads();  // the other record buffer's readers (the previous item) are done
         if (more) {
-            if (warp == 0) issue_rec(nxt, (m + 1) & 1);
+            if (tid == 0) issue_rec(nxt, (m + 1) & 1);
             else if (warp == 1) prefetch_next(nxt);
         }
         const int rb = m & 1;
@@ -1343,12 +1353,22 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         int64_t c0;
         const int L = rows_of(cur, c0);
         const int h = cur.h;
-        const unsigned char *R = sl + LS_R + rb * RBUF;
-        const uint32_t rbase = sb + LS_R + rb * RBUF;
+        const unsigned char *R = sl + LS_R + rb * RBUF + 2 * SWT;  // the record
+        const uint32_t rbase = sb + LS_R + rb * RBUF + 2 * SWT;
+        if (L < C) {  // V, dO rows past the sequence's end (other tokens, or zeros) to zero
+            unsigned char *t2 = sl + LS_R + rb * RBUF;
+            for (int i = tid; i < 2 * 2 * (C - L) * 8; i += LT_THREADS) {  // [tile][half][row][chunk]
+                const int chunk = i & 7, row = L + (i >> 3) % (C - L), hv = (i >> 3) / (C - L);
+                *reinterpret_cast<uint4 *>(t2 + hv * (SWT / 2) + row * 128 + chunk * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before its next copy
+            __syncthreads();
+        }
         const uint32_t SB = sb + LS_S, DSB = sb + LS_DS;
         const uint32_t KP = rbase + TR_K, WN = rbase + TR_W, QT = rbase + TR_Q, P16 = rbase + TR_P;
         const uint32_t KT = rbase + TR_KT, KH = rbase + TR_KH, M16 = rbase + TR_M;
-        const uint32_t V16 = rbase + RECB, DO = rbase + RECB + T128;
+        const uint32_t V16 = sb + LS_R + rb * RBUF, DO = V16 + SWT;  // swizzled tiles
         const uint32_t U16 = sb + LS_U, DU16 = sb + LS_DU, DW16 = sb + LS_DW;
         const uint32_t DP = sb + LS_DP, DZ = sb + LS_DZ;
 
@@ -1394,7 +1414,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             uint32_t ap[4], bo[4];
             float pd[2][4] = {};
             ld_a_t(P16, PS, 0, 0, ap);         // P^T
-            ld_b_kn(DO, PB, 0, n0, bo);        // B[i][v] = dO[i][v]
+            ld_b_kn_sw(DO, 0, n0, bo);         // B[i][v] = dO[i][v]
             mma16816(pd[0], ap, bo[0], bo[1]);
             mma16816(pd[1], ap, bo[2], bo[3]);
 #pragma unroll
@@ -1405,14 +1425,14 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             store_c16(reinterpret_cast<__nv_bfloat16 *>(sl + LS_DU), PB, n0, du);
             // dO[:, cols] U[:, cols]^T: U's accumulator fragments are the B operand as they are
             uint32_t ao[4];
-            ld_a(DO, PB, n0, ao);
+            ld_a_sw(DO, n0, ao);
             mma16816(dpp[0], ao, pack2(u[0][0], u[0][1]), pack2(u[1][0], u[1][1]));
             mma16816(dpp[1], ao, pack2(u[0][2], u[0][3]), pack2(u[1][2], u[1][3]));
             // dU[:, cols] V[:, cols]^T: dU's fragments are the A operand as they are
             const uint32_t adu[4] = {pack2(du[0][0], du[0][1]), pack2(du[0][2], du[0][3]),
                                      pack2(du[1][0], du[1][1]), pack2(du[1][2], du[1][3])};
             uint32_t bv[4];
-            ld_b_nk(V16, PB, 0, n0, bv);       // B[v][t'] = V[t'][v]
+            ld_b_nk_sw(V16, 0, n0, bv);        // B[v][t'] = V[t'][v]
             mma16816(dmp[0], adu, bv[0], bv[1]);
             mma16816(dmp[1], adu, bv[2], bv[3]);
             __syncwarp();  // this warp's dU columns are in shared memory
@@ -1441,7 +1461,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 #pragma unroll
         for (int k0 = 0; k0 < D; k0 += 16) {  // k = value column
             uint32_t ao[4], au[4], adu[4], ads[4], bs[4], bd[4];
-            ld_a(DO, PB, k0, ao);
+            ld_a_sw(DO, k0, ao);
             ld_a(U16, PB, k0, au);
             ld_a(DU16, PB, k0, adu);
             ld_b_kn(SB, PB, k0, n0, bs);       // B[v][key] = S^T tile [v][key]
@@ -1996,7 +2016,8 @@ PFN_cuTensorMapEncodeTiled_v12000 map_encoder() {
     });
     return fn;
 }
-bool token_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x) {
+bool token_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H, int box_x,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     auto enc = map_encoder();
     if (!enc) return false;
     const cuuint64_t es = f32 ? 4 : 2;
@@ -2006,7 +2027,7 @@ bool token_map(CUtensorMap *m, const void *base, bool f32, int64_t n_tok, int H,
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -2112,8 +2133,12 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
         tev.mark(2);  // both serial passes in the one launch: the reverse pass's entry is 0
         tev.mark(3);
         const int grid = (int)(n_items < sms ? n_items : sms);
+        CUtensorMap mvs, mos;  // V and dO in 64-column, 128-byte-swizzled boxes
+        if (!token_map(&mvs, b16[2], false, p.n_tok, H, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !token_map(&mos, d16, false, p.n_tok, H, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
-            b16[2], p.a, p.cu_seqlens, d16, wsb,
+            mvs, p.a, p.cu_seqlens, mos, wsb,
             reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
             reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
         tev.mark(4);
