@@ -680,6 +680,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "[%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(mbar) : "memory");
 }
+// a box of a 3-D tensor map into L2
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(map), "r"(x), "r"(y), "r"(z) : "memory");
+}
 __device__ __forceinline__ void bar_init(uint32_t a, uint32_t c) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(c));
 }
@@ -1272,7 +1277,8 @@ struct ItemCursor {
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
-    local_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ a,
+    local_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
+                    const float *__restrict__ a,
                     const int32_t *__restrict__ cu, const __grid_constant__ CUtensorMap tm_dout,
                     const unsigned char *__restrict__ ws, __nv_bfloat16 *__restrict__ dq,
                     __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
@@ -1321,12 +1327,10 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         bar_arrive_tx(bar(0), 2 * ST16);
         bulk_g2s(sb + LS_S, rec_of(it) + TC_S, 2 * ST16, bar(0));
     };
-    // warp 1: the next item's states and gate-logit rows into L2
+    // one thread: the next item's states and gate-logit rows into L2
     auto prefetch_next = [&](const Item &it) {
-        int64_t c0;
-        const int L = rows_of(it, c0);
-        if (lane == 0) prefetch_l2(rec_of(it) + TC_S, 2 * ST16);
-        if (lane < L) prefetch_l2(a + ((size_t)(c0 + lane) * H + it.h) * D, D * 4);
+        prefetch_l2(rec_of(it) + TC_S, 2 * ST16);
+        tma_prefetch_3d(&tm_a, 0, it.h, (int)(cu[it.n] + (int64_t)it.c * C));
     };
 
     ItemCursor ic;
@@ -1345,7 +1349,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         __syncthreads();  // the other record buffer's readers (the previous item) are done
         if (more) {
             if (tid == 0) issue_rec(nxt, (m + 1) & 1);
-            else if (warp == 1) prefetch_next(nxt);
+            else if (tid == 32) prefetch_next(nxt);
         }
         const int rb = m & 1;
         const bool ok = bar_wait(bar(1 + rb), (uint32_t)((m >> 1) & 1)) && bar_wait(bar(0), (uint32_t)(m & 1));
@@ -2138,7 +2142,7 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
             !token_map(&mos, d16, false, p.n_tok, H, 64, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         local_tc_kernel<<<grid, LT_THREADS, LS_BYTES, stream>>>(
-            mvs, p.a, p.cu_seqlens, mos, wsb,
+            mvs, ma, p.a, p.cu_seqlens, mos, wsb,
             reinterpret_cast<__nv_bfloat16 *>(p.dq), reinterpret_cast<__nv_bfloat16 *>(p.dk),
             reinterpret_cast<__nv_bfloat16 *>(p.dv), p.da, p.dbeta, H, p.n_seq, n_items, scale);
         tev.mark(4);
