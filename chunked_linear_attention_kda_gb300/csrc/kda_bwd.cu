@@ -1190,6 +1190,19 @@ __global__ void __launch_bounds__(kThreads)
 // 16 w + 16) in phases 2 and 4 (dQ~, dK', dW, dgamma_L, dK~, dK^ and the per-channel
 // gradients dq, dk, da, computed on the accumulator fragments); the 16 x 16 adjoint of the
 // solve (phase 3) is one element per thread.
+// Phase stamps of the local-gradient kernel (CTA 0, thread 0, first 64 items), compiled
+// only with -DKDA_BWD_TRACE.
+#ifdef KDA_BWD_TRACE
+__device__ long long g_local_trace[64][9];
+#define LOCAL_TRACE(i) \
+    do { \
+        if (blockIdx.x == 0 && tid == 0 && m < 64) g_local_trace[m][i] = clock64(); \
+    } while (0)
+#else
+#define LOCAL_TRACE(i) \
+    do { \
+    } while (0)
+#endif
 constexpr int LT_THREADS = 256;
 // record buffer: V and dO rows as two 128-byte-swizzled [16][64] halves each (tensor
 // copies, 1024-byte aligned), then the record
@@ -1209,6 +1222,9 @@ static_assert(LT_THREADS == C * C, "one thread per element of a 16 x 16 product"
 
 struct Item {
     int n, h, c;
+    int L;           // the chunk's token rows (<= 16)
+    int64_t c0;      // its first token
+    long long slot;  // its workspace slot
 };
 // item idx = slot H + h; false when the slot holds no chunk (the gap after a sequence)
 __device__ bool decode_item(const int32_t *cu, int n_seq, int H, long long idx, Item &it) {
@@ -1224,11 +1240,6 @@ __device__ bool decode_item(const int32_t *cu, int n_seq, int H, long long idx, 
     it.c = (int)(slot - ((long long)(cu[lo] >> 4) + lo));
     return it.c < (cu[lo + 1] - cu[lo] + C - 1) / C;
 }
-__device__ __forceinline__ int item_rows(const int32_t *cu, const Item &it, int64_t &c0) {
-    c0 = cu[it.n] + (int64_t)it.c * C;
-    const int64_t left = cu[it.n + 1] - c0;
-    return (int)(left < C ? left : C);
-}
 // Walks items idx = slot H + h in increasing order: one division and binary search at the
 // start, then a step per item (the next sequence's slots looked up as they are reached);
 // items of slots that hold no chunk are skipped.
@@ -1236,10 +1247,13 @@ struct ItemCursor {
     const int32_t *cu;
     int n_seq, H, h, n, nc;
     long long idx, end, slot, b0, b1;  // b0, b1: the first slots of sequences n and n + 1
+    int64_t tok0, tok1;                // sequence n's tokens [tok0, tok1)
     __device__ void load_seq() {
-        b0 = (long long)(cu[n] >> 4) + n;
-        b1 = n + 1 < n_seq ? (long long)(cu[n + 1] >> 4) + n + 1 : LLONG_MAX;
-        nc = (cu[n + 1] - cu[n] + C - 1) / C;
+        tok0 = cu[n];
+        tok1 = cu[n + 1];
+        b0 = (long long)(tok0 >> 4) + n;
+        b1 = n + 1 < n_seq ? (long long)(tok1 >> 4) + n + 1 : LLONG_MAX;
+        nc = (int)((tok1 - tok0 + C - 1) / C);
     }
     __device__ void start(const int32_t *cu_, int n_seq_, int H_, long long beg, long long end_) {
         cu = cu_;
@@ -1273,7 +1287,18 @@ struct ItemCursor {
         step();
         skip();
     }
-    __device__ Item item() const { return Item{n, h, (int)(slot - b0)}; }
+    // the current item, with its rows, first token and slot (no memory access)
+    __device__ Item item() const {
+        Item it;
+        it.n = n;
+        it.h = h;
+        it.c = (int)(slot - b0);
+        it.c0 = tok0 + (int64_t)it.c * C;
+        const int64_t left = tok1 - it.c0;
+        it.L = (int)(left < C ? left : C);
+        it.slot = slot;
+        return it;
+    }
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
@@ -1304,14 +1329,11 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     }
     __syncthreads();
 
-    auto rows_of = [&](const Item &it, int64_t &c0) { return item_rows(cu, it, c0); };
-    auto rec_of = [&](const Item &it) {
-        return ws + (slot_of(cu, it.n, it.c) * H + it.h) * REC_TC;
-    };
+    auto rec_of = [&](const Item &it) { return ws + ((size_t)it.slot * H + it.h) * REC_TC; };
     // one thread: the V and dO rows of item it (four tensor copies: two 64-column halves
     // each) and its record into record buffer rb
     auto issue_rec = [&](const Item &it, int rb) {
-        const int64_t c0 = cu[it.n] + (int64_t)it.c * C;
+        const int64_t c0 = it.c0;
         const uint32_t bb = sb + LS_R + rb * RBUF;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         bar_arrive_tx(bar(1 + rb), (uint32_t)(2 * SWT + RECB));
@@ -1330,7 +1352,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
     // one thread: the next item's states and gate-logit rows into L2
     auto prefetch_next = [&](const Item &it) {
         prefetch_l2(rec_of(it) + TC_S, 2 * ST16);
-        tma_prefetch_3d(&tm_a, 0, it.h, (int)(cu[it.n] + (int64_t)it.c * C));
+        tma_prefetch_3d(&tm_a, 0, it.h, (int)it.c0);
     };
 
     ItemCursor ic;
@@ -1341,6 +1363,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
         issue_rec(cur, 0);
         issue_states(cur);
     }
+
     for (int m = 0; idx < end; ++m) {
         ic.advance();
         const long long nidx = ic.idx;
@@ -1352,10 +1375,12 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             else if (tid == 32) prefetch_next(nxt);
         }
         const int rb = m & 1;
+        LOCAL_TRACE(0);
         const bool ok = bar_wait(bar(1 + rb), (uint32_t)((m >> 1) & 1)) && bar_wait(bar(0), (uint32_t)(m & 1));
         if (__syncthreads_or(!ok)) break;
-        int64_t c0;
-        const int L = rows_of(cur, c0);
+        LOCAL_TRACE(1);
+        const int64_t c0 = cur.c0;
+        const int L = cur.L;
         const int h = cur.h;
         const unsigned char *R = sl + LS_R + rb * RBUF + 2 * SWT;  // the record
         const uint32_t rbase = sb + LS_R + rb * RBUF + 2 * SWT;
@@ -1390,6 +1415,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                         a + ((size_t)(c0 + t) * H + h) * D + n0 + 8 * tt + 2 * l4);
             }
 
+        LOCAL_TRACE(2);
         // ---- phase 1 (value columns [n0, n0 + 16)): U = U~ - W S, dU = K' dS_end + s P^T dO,
         // dV = M^T dU; partial sums of dO U^T and dU V^T over these columns
         float u[2][4], du[2][4] = {}, dpp[2][4] = {}, dmp[2][4] = {};
@@ -1457,7 +1483,9 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                             pack2(dvf[tt][2 * hh], dvf[tt][2 * hh + 1]);
                 }
         }
+        LOCAL_TRACE(3);
         __syncthreads();  // U and dU complete
+        LOCAL_TRACE(4);
 
         // ---- phase 2 (key channels [n0, n0 + 16)): dQ~ = s dO S^T, dK' = U dS_end^T,
         // dW = -dU S^T, dgamma_L = diag(dS_end S^T); dW K~^T into the dM partial sum
@@ -1517,7 +1545,9 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                         make_float2(dpp[tt][2 * hh], dpp[tt][2 * hh + 1]);
                 }
         }
+        LOCAL_TRACE(5);
         __syncthreads();  // the states' last readers are done; dM and dP sums complete
+        LOCAL_TRACE(6);
         if (more && tid == 0) issue_states(nxt);
 
         // ---- phase 3: dP = s lower(dO U^T); dT = dM diag(beta), dA = strict_lower(-T^T dT
@@ -1566,6 +1596,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
             if (j == 0 && r < L) dbeta[(size_t)(c0 + r) * H + h] = dbs[r] + x;
         }
         __syncthreads();  // dP, dZ complete
+        LOCAL_TRACE(7);
 
         // ---- phase 4 (key channels [n0, n0 + 16)): dQ~ += dP K^, dK~ = M^T dW + dZ K^,
         // dK^ = dP^T Q~ + dZ^T K~; then dq, dk and da on the fragments. dG takes Q~, K~, K^
@@ -1668,6 +1699,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
                                     dG[tt][2 * hh + 1] * (kGMin * s1 * (1.f - s1)));
                 }
             }
+        LOCAL_TRACE(8);
         idx = nidx;
         cur = nxt;
     }
@@ -1740,7 +1772,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
     // b, one tensor copy each (rows past the end of the tensor arrive as zeros; rows past the
     // sequence's end hold other tokens, masked where they are used)
     auto issue_in = [&](const Item &it, int b) {
-        const int64_t c0 = cu[it.n] + (int64_t)it.c * C;
+        const int64_t c0 = it.c0;
         const uint32_t bb = sb + b * IBUF;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         bar_arrive_tx(bar(b), (uint32_t)IBUF);
@@ -1756,9 +1788,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
     long long idx = ic.idx;
     if (idx < end && tid == 0) issue_in(cur, 0);
     auto load_beta = [&](const Item &it) {  // beta of an item's rows, 0 past its end
-        int64_t cb;
-        const int Lb = item_rows(cu, it, cb);
-        return tid < Lb ? beta[(size_t)(cb + tid) * H + it.h] : 0.f;
+        return tid < it.L ? beta[(size_t)(it.c0 + tid) * H + it.h] : 0.f;
     };
     float bta = (idx < end && tid < C) ? load_beta(cur) : 0.f;  // loaded an item ahead
     for (int m = 0; idx < end; ++m) {
@@ -1766,8 +1796,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         const long long nidx = ic.idx;
         nxt = ic.item();
         const bool more = nidx < end;
-        int64_t c0;
-        const int L = item_rows(cu, cur, c0);
+        const int L = cur.L;
         const int h = cur.h;
         const float bta_next = (more && tid < C) ? load_beta(nxt) : 0.f;
         PREP_TRACE(0);
@@ -1992,7 +2021,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the record, to the copy
         __syncthreads();
         if (tid == 0) {
-            unsigned char *dst = ws + (slot_of(cu, cur.n, cur.c) * H + h) * REC_TC + TC_REC;
+            unsigned char *dst = ws + ((size_t)cur.slot * H + h) * REC_TC + TC_REC;
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                          ::"l"(dst), "r"(sb + PS_REC), "r"((uint32_t)RECB) : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -2243,5 +2272,10 @@ cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream)
 #ifdef KDA_BWD_TRACE
 extern "C" int kda_debug_prep_trace_dump(long long *host) {
     return (int)cudaMemcpyFromSymbol(host, kda::g_prep_trace, sizeof(kda::g_prep_trace));
+}
+#endif
+#ifdef KDA_BWD_TRACE
+extern "C" int kda_debug_local_trace_dump(long long *host) {
+    return (int)cudaMemcpyFromSymbol(host, kda::g_local_trace, sizeof(kda::g_local_trace));
 }
 #endif
