@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kThreads)
 //             dS^T <- dS^T Diag(gamma_L) + (s dO)^T Q~ + X^T (-W)
 // the transposed forms of the two chains above, the state an fp32 accumulator throughout.
 constexpr int NS = 4;                    // ring slots
-constexpr int PO = 40;                   // bf16 pitch of the [16][32] dO slice (80-byte rows)
+constexpr int PO = 32;                   // bf16 pitch of the [16][32] dO slice (a dense TMA box)
 // slot layout (bytes): the record's operand part [0, TR_OPS) (K', -W, Q~, P, gamma_L), then
 // U~^T [32][16] fp32 (forward) or dO [16][PO] bf16 (reverse)
 constexpr int SL_K = TR_K, SL_W = TR_W, SL_Q = TR_Q, SL_P = TR_P, SL_G = TR_G, SL_X = TR_OPS;
@@ -728,7 +728,7 @@ template <bool REVERSE>
 __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned long long *bars,
                                            const int32_t *__restrict__ cu,
                                            unsigned char *__restrict__ ws,
-                                           const __nv_bfloat16 *__restrict__ dout,
+                                           const CUtensorMap *tm_dout,
                                            const float *__restrict__ init,
                                            float *__restrict__ final_state, int H, float scale) {
     constexpr int D = 128;
@@ -747,17 +747,49 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
     const size_t rstride = (size_t)H * REC_TC;
     auto full = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[s])); };
     auto empty = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[NS + s])); };
+    // state-tile hand-off to the writer warp: staged[w][b] (chain warp w filled staging buffer
+    // b), freed[w][b] (the writer's bulk copy has read it)
+    auto staged = [&](int w, int b) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[2 * NS + 2 * w + b])); };
+    auto freed = [&](int w, int b) { return static_cast<uint32_t>(__cvta_generic_to_shared(&bars[2 * NS + 4 + 2 * w + b])); };
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             bar_init(full(s), 1);   // the copies' issue
             bar_init(empty(s), 2);  // one arrival per chain warp
         }
+        for (int i = 0; i < 4; ++i) {
+            bar_init(staged(i >> 1, i & 1), 1);
+            bar_init(freed(i >> 1, i & 1), 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (warp >= 2) {
+    const uint32_t sbase0 = static_cast<uint32_t>(__cvta_generic_to_shared(smc));
+    if (warp == 3) {
+        // ---------------------------------------------------------------- writer warp
+        // each chunk's two staged state tiles (16 rows per chain warp) to the workspace
+        if (lane == 0) {
+            for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
+                unsigned char *dst = rec0 + (size_t)c * rstride + (REVERSE ? TC_DS : TC_S);
+                bool ok = true;
+                for (int w = 0; w < 2 && ok; ++w) {
+                    ok = bar_wait(staged(w, m & 1), (uint32_t)((m >> 1) & 1));
+                    if (!ok) break;
+                    const uint32_t src = sbase0 + NS * SLOT + (2 * w + (m & 1)) * CT_ROWS;
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                 ::"l"(dst + (size_t)(v0 + 16 * w) * 272), "r"(src), "r"((uint32_t)CT_ROWS)
+                                 : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    bar_arrive(freed(w, m & 1));
+                }
+                if (!ok) break;
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        }
+        return;
+    }
+    if (warp == 2) {
         // ---------------------------------------------------------------- loader warp
-        if (warp == 3) return;
         for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
             const int s = m % NS;
             bool ok = true;
@@ -765,24 +797,16 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t sl = static_cast<uint32_t>(__cvta_generic_to_shared(smc + s * SLOT));
             const unsigned char *tr = rec0 + (size_t)c * rstride + TC_REC;
-            if (REVERSE) {  // K', -W, Q~, P, gamma_L; the dO rows of the CTA's 32 columns
-                const int64_t c0 = t0 + (int64_t)c * C;
-                const int L = (int)(t1 - c0 < C ? t1 - c0 : C);
-                if (L < C) {  // rows past the sequence's end read as zeros
-                    for (int i = lane; i < (C - L) * 4; i += 32)
-                        *reinterpret_cast<uint4 *>(smc + s * SLOT + SL_X + (L + i / 4) * PO * 2 + (i % 4) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (REVERSE) {  // K', -W, Q~, P, gamma_L; the chunk's dO rows, this CTA's 32 columns
+                if (((sl + SL_X) & 127u) != 0) {  // a tensor copy needs 128-byte alignment:
+                    if (lane == 0) atomicOr(&g_bwd_flags, 4u);  // report it (warp-uniform
+                    break;                                      // exit; the waits give up)
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    bar_arrive_tx(full(s), TR_OPS + L * 64);
+                if (lane == 0) {  // (rows past the sequence's end are masked where used)
+                    bar_arrive_tx(full(s), TR_OPS + C * 32 * 2);
                     bulk_g2s(sl, tr, TR_OPS, full(s));
+                    tma_load_3d(sl + SL_X, tm_dout, v0, h, (int)(t0 + (int64_t)c * C), full(s));
                 }
-                __syncwarp();
-                if (lane < L)
-                    bulk_g2s(sl + SL_X + lane * PO * 2, dout + ((size_t)(c0 + lane) * H + h) * D + v0, 64,
-                             full(s));
             } else if (lane == 0) {  // K', -W; gamma_L; this CTA's block of U~^T
                 bar_arrive_tx(full(s), 2 * T128 + 128 * 4 + 32 * C * 4);
                 bulk_g2s(sl + SL_K, tr + TR_K, 2 * T128, full(s));
@@ -821,12 +845,14 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
         }
     };
     // this warp's 16 rows of the bf16 S^T tile [v][136]: staged in shared memory by
-    // stmatrix (a double buffer per warp), then one bulk copy of the 4352 contiguous bytes
+    // stmatrix (a double buffer per warp) and handed to the writer warp, which copies the
+    // 4352 contiguous bytes to the workspace
     const uint32_t stage = sbase + NS * SLOT + sw * 2 * CT_ROWS;
-    auto write_tile = [&](unsigned char *dst, int buf) {
-        if (lane == 0)  // the copy that last read this buffer (two chunks ago) is done
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        __syncwarp();
+    auto write_tile = [&](int m) {  // returns false when a wait gave up
+        const int buf = m & 1;
+        bool ok = true;
+        if (m >= 2) ok = bar_wait(freed(sw, buf), (uint32_t)(((m >> 1) - 1) & 1));
+        if (!__all_sync(0xffffffffu, ok)) return false;
         const uint32_t sb2 = stage + buf * CT_ROWS;
         const int mi = lane >> 3, r = lane & 7;
 #pragma unroll
@@ -836,11 +862,8 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
                   pack2(S[j + 1][2], S[j + 1][3]));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                         ::"l"(dst + (size_t)vr * 272), "r"(sb2), "r"((uint32_t)CT_ROWS) : "memory");
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
+        if (lane == 0) bar_arrive(staged(sw, buf));  // release: the staging is written
+        return true;
     };
     for (int c = REVERSE ? nc - 1 : 0, m = 0; REVERSE ? c >= 0 : c < nc; c += REVERSE ? -1 : 1, ++m) {
         const int s = m % NS;
@@ -848,7 +871,7 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t sl = sbase + s * SLOT;
         const float4 *G4 = reinterpret_cast<const float4 *>(smc + s * SLOT + SL_G);
-        write_tile(rec0 + (size_t)c * rstride + (REVERSE ? TC_DS : TC_S), m & 1);
+        if (!write_tile(m)) break;
         float acc[2][4];  // U^T (forward) or X^T (reverse): 16 value rows x 16 tokens
         if (!REVERSE) {
             const float *tu = reinterpret_cast<const float *>(smc + s * SLOT + SL_X);
@@ -868,10 +891,12 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
         uint32_t oa[4] = {0u, 0u, 0u, 0u};
         if (REVERSE) {
             ldsm4t(sl + SL_X + (uint32_t)((((i8 >> 1) * 8 + r8) + 0) * PO * 2 + (16 * sw + (i8 & 1) * 8) * 2), oa);
+            const int64_t left = t1 - (t0 + (int64_t)c * C);  // valid token rows of the chunk
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {  // s dO
+            for (int i = 0; i < 4; ++i) {  // s dO; tokens past the sequence's end to zero
+                const int tk = (i >> 1) * 8 + 2 * l4;
                 const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&oa[i]));
-                oa[i] = pack2(scale * f.x, scale * f.y);
+                oa[i] = pack2(tk < left ? scale * f.x : 0.f, tk + 1 < left ? scale * f.y : 0.f);
             }
         }
         // two independent accumulator chains (even / odd state tiles) halve the dependent
@@ -928,7 +953,6 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
         if (lane == 0) bar_arrive(empty(s));  // this warp's reads of the slot are done
     }
     if (final_state) write_state(final_state + hidx);
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Both serial passes in one launch: they are independent (the reverse pass reads only the
@@ -936,15 +960,15 @@ __device__ __forceinline__ void chain_body(int blk, unsigned char *smc, unsigned
 // pass, the rest the reverse pass; two CTAs fit on an SM.
 __global__ void __launch_bounds__(128, 2)
     chains_tc_kernel(const int32_t *__restrict__ cu, unsigned char *__restrict__ ws,
-                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ h0,
+                     const __grid_constant__ CUtensorMap tm_dout, const float *__restrict__ h0,
                      const float *__restrict__ dh_final, float *__restrict__ dh0, int H,
                      float scale, int nfwd) {
-    extern __shared__ __align__(16) unsigned char smc[];
-    __shared__ __align__(8) unsigned long long bars[2 * NS];
+    extern __shared__ __align__(128) unsigned char smc[];  // tensor copies land 128-byte aligned
+    __shared__ __align__(8) unsigned long long bars[2 * NS + 8];
     if ((int)blockIdx.x < nfwd)
-        chain_body<false>(blockIdx.x, smc, bars, cu, ws, dout, h0, nullptr, H, scale);
+        chain_body<false>(blockIdx.x, smc, bars, cu, ws, &tm_dout, h0, nullptr, H, scale);
     else
-        chain_body<true>(blockIdx.x - nfwd, smc, bars, cu, ws, dout, dh_final, dh0, H, scale);
+        chain_body<true>(blockIdx.x - nfwd, smc, bars, cu, ws, &tm_dout, dh_final, dh0, H, scale);
 }
 
 // ---- 3. local gradients of every chunk
@@ -2161,7 +2185,9 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
                                                                p.cu_seqlens, wsb, H, p.n_seq,
                                                                n_items, scale);
         tev.mark(1);
-        chains_tc_kernel<<<items * 8, 128, smc, stream>>>(p.cu_seqlens, wsb, d16, p.h0, p.dh_final,
+        CUtensorMap mo;
+        if (!token_map(&mo, d16, false, p.n_tok, H, 32)) return cudaErrorInvalidValue;
+        chains_tc_kernel<<<items * 8, 128, smc, stream>>>(p.cu_seqlens, wsb, mo, p.h0, p.dh_final,
                                                          p.dh0, H, scale, (int)(items * 4));
         tev.mark(2);  // both serial passes in the one launch: the reverse pass's entry is 0
         tev.mark(3);
