@@ -1758,7 +1758,8 @@ constexpr int PS_QL = PS_REC + RECB, PS_KTL = PS_QL + T128;
 constexpr int PS_KHL = PS_KTL + T128, PS_A = PS_KHL + T128, PS_ML = PS_A + C * C * 4;
 constexpr int PS_BT = PS_ML + C * PS * 2;
 constexpr int PS_TS = PS_BT + C * 4, PS_YS = PS_TS + C * C * 4, PS_PART = PS_YS + 64 * 4;
-constexpr int PS_BYTES = PS_PART + 8 * C * C * 4;
+constexpr int PS_GT = PS_PART + 8 * C * C * 4;  // first-half totals of G [128]
+constexpr int PS_BYTES = PS_GT + 128 * 4;
 static_assert(IBUF % 16 == 0 && PS_QL % 16 == 0 && PS_A % 16 == 0 && 2 * (PS_BYTES + 1024) <= 228 * 1024,
               "two prep CTAs per SM");
 
@@ -1842,22 +1843,39 @@ __global__ void __launch_bounds__(PT_THREADS, 2)
         const uint32_t inb = sb + ib * IBUF;
         float *GS = reinterpret_cast<float *>(rec + TR_GS);
 
-        // ---- G = cumsum of g = -5 sigmoid(a) per key channel, gamma_L = e^{G_15}
-        if (tid < D) {
+        // ---- G = cumsum of g = -5 sigmoid(a) per key channel, gamma_L = e^{G_15}: thread
+        // (channel x, half) sums rows [8 half, 8 half + 8); the second half then adds the
+        // first half's total
+        float *Gtot = reinterpret_cast<float *>(sp + PS_GT);
+        {
+            const int x = tid & (D - 1), half = tid >> 7;
             const float *Ain = reinterpret_cast<const float *>(in + 3 * IT16);
             float G = 0.f;
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const float g = r < L ? __fdividef(kGMin, 1.f + __expf(-Ain[r * D + tid])) : 0.f;
+            for (int r8 = 0; r8 < C / 2; ++r8) {
+                const int r = 8 * half + r8;
+                const float g = r < L ? __fdividef(kGMin, 1.f + __expf(-Ain[r * D + x])) : 0.f;
                 G += g;
-                GS[r * GP + tid] = G;
+                GS[r * GP + x] = G;
+            }
+            if (half == 0) Gtot[x] = G;
+        }
+        __syncthreads();
+        if (tid >= D) {
+            const int x = tid - D;
+            const float g0 = Gtot[x];
+            float G = 0.f;
+#pragma unroll
+            for (int r = C / 2; r < C; ++r) {
+                G = GS[r * GP + x] + g0;
+                GS[r * GP + x] = G;
             }
             const float gl = __expf(G);
-            reinterpret_cast<float *>(rec + TR_GL)[tid] = gl;
-            reinterpret_cast<float *>(rec + TR_G)[gperm_tc(tid)] = gl;
+            reinterpret_cast<float *>(rec + TR_GL)[x] = gl;
+            reinterpret_cast<float *>(rec + TR_G)[gperm_tc(x)] = gl;
         } else if (L < C) {  // V rows past the sequence's end to zero (they meet M's zero columns)
             unsigned char *vt = sp + ib * IBUF + 2 * IT16;
-            for (int i = tid - D; i < (C - L) * 16; i += PT_THREADS - D)
+            for (int i = tid; i < (C - L) * 16; i += D)
                 *reinterpret_cast<uint4 *>(vt + L * 256 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the buffer's next copy
         }
