@@ -11,16 +11,17 @@
 //   W = M K~, U~ = M V, P = lower(Q~ K^^T), U = U~ - W S
 //   O = s (Q~ S + P U),  S_end = Diag(gamma_L) S + K'^T U          (s = d_k^-1/2)
 //
-// Three kernels, fp32 arithmetic throughout, the caller's workspace holding two
-// d_k x d_v fp32 states per (chunk, head):
-//   1. checkpoints: the forward recurrence per (sequence, head), storing the state at the
-//      start of every chunk (ck);
-//   2. reverse chain per (sequence, head), last chunk first. dS, the gradient with respect
-//      to the current chunk's end state, is stored (dck), then carried to its start:
+// The workspace holds, per (chunk slot, head), the state at the start of the chunk and the
+// gradient with respect to its end state, and the chunk's state-independent products:
+//   0. chunk products, all chunks in parallel (the record: K', W, Q~, P, U~, ...);
+//   1. forward serial pass per (sequence, head): the state at the start of every chunk;
+//   2. reverse serial pass per (sequence, head), last chunk first. dS, the gradient with
+//      respect to the current chunk's end state, is stored, then carried to its start:
 //        X = K' dS + s P^T dO,   dS <- Diag(gamma_L) dS + s Q~^T dO - W^T X
 //      (the transpose of the chunk's affine state map: S_end = (Diag(gamma_L) - K'^T W)
 //      S + K'^T U~ and O = s (Q~ - P W) S + s P U~); dh0 is the dS left at the first chunk;
-//   3. local gradients, all (sequence, head, chunk) independent given ck and dck:
+//      passes 1 and 2 are independent of each other;
+//   3. local gradients, all (sequence, head, chunk) independent given S and dS_end:
 //        dU = s P^T dO + K' dS_end            dP = lower(s dO U^T)
 //        dQ~ = s dO S^T + dP K^                dK' = U dS_end^T
 //        dW = -dU S^T                          dgamma_L = rowsum(dS_end . S)
@@ -30,8 +31,11 @@
 //        dQ = dQ~ Gamma,  dK = dK~ Gamma + dK^ / Gamma + dK' gamma_L / Gamma
 //        dG = dQ~ Q~ + dK~ K~ - dK^ K^ - dK' K'  (+ gamma_L dgamma_L + colsum(dK' K') at row 15)
 //        dg = reverse cumsum of dG,  da = dg (-5) sigmoid(a) (1 - sigmoid(a))
-//      S and dS_end are read 32 columns at a time, so every sum over value columns
-//      accumulates block by block.
+// Two implementations: for bf16 I/O at d_k = d_v = 128 (16-byte aligned buffers) the
+// tensor-core kernels (prep_tc_kernel, chains_tc_kernel with both serial passes in one
+// launch, local_tc_kernel: mma.sync with bf16 operands and fp32 accumulation, bf16 state
+// tiles, TMA tensor and bulk copies); otherwise fp32 FMA kernels (prep_kernel, ckpt_kernel,
+// chain_kernel, local_kernel: fp32 states, S and dS_end read 32 columns at a time).
 // The chunk of token start t in sequence n has the workspace slot (cu[n] >> 4) + c + n:
 // strictly increasing over all chunks, below (n_tok >> 4) + n_seq + 1.
 #include <cuda.h>
