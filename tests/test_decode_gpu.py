@@ -132,6 +132,31 @@ def test_bench_batch_sampled():
     assert eo <= 1e-2 and es <= 1e-2, f"out {eo:.3e}, state {es:.3e}"
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_state_alignment_selects_either_kernel(dtype):
+    """A 16-byte aligned state with d_v a multiple of 4 takes the 16-byte-access kernel; a
+    state one float off that boundary takes the scalar kernel. Both meet the oracle's bar
+    on the same inputs and agree with each other to fp32 rounding."""
+    x = one_token_inputs(6, 5, 128, 128, dtype, seed=57, h0_std=0.5)
+    n = x.h0.numel()
+    aligned = x.h0.clone()
+    shifted = torch.empty(n + 1, device=DEV)[1:].view_as(x.h0)
+    shifted.copy_(x.h0)
+    assert aligned.data_ptr() % 16 == 0 and shifted.data_ptr() % 16 == 4
+    o_ref, s_ref = recurrence.decode_step(cpu(x.q), cpu(x.k), cpu(x.v), cpu(x.a),
+                                          cpu(x.beta), cpu(x.h0))
+    outs = []
+    for st in (aligned, shifted):
+        o = kda.decode_step(x.q, x.k, x.v, x.a, x.beta, st)
+        torch.cuda.synchronize()
+        assert_finite(o, st)
+        eo, es = rel_l2(f64(o), o_ref), rel_l2(f64(st), s_ref)
+        assert eo <= TOL[dtype] and es <= TOL[dtype], f"out {eo:.3e}, state {es:.3e}"
+        outs.append(o.float())
+    assert rel_l2(f64(aligned), f64(shifted)) <= 1e-6
+    assert rel_l2(f64(outs[0]), f64(outs[1])) <= (1e-6 if dtype == torch.float32 else 1e-2)
+
+
 def test_empty_batch_is_a_noop():
     x = torch.zeros(0, 2, 128, device=DEV)
     st = torch.zeros(0, 2, 128, 128, device=DEV)
