@@ -13,9 +13,10 @@ scaling, independent sequences: no collective on the data path; one max-reductio
 the elapsed time for the report).
 
 Reported alongside the device-timed value:
-  e2e          the same metric through ``kda_chunk_fwd_from_host`` with pinned host
-               buffers: H2D copies of the inputs, the kernel and D2H copies of the
-               outputs inside the timed region;
+  e2e          the same metric through ``kda_chunk_fwd_from_host_pipelined`` with pinned
+               host buffers: H2D copies of the inputs, the kernels and D2H copies of the
+               outputs inside the timed region, overlapped segment by segment (the
+               one-stream ``kda_chunk_fwd_from_host`` time beside it);
   roofline     algorithmic bytes per launch / CUDA-event launch time against the
                measured HBM copy bandwidth (MEASURED_PEAKS.json);
   cpu_baseline the fp64 oracle on the host cores on a bounded sample (rank 0, N = 1);
@@ -378,6 +379,9 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+E2E_SEGMENTS = 16
+
+
 def measure_e2e(x, dev, stream, steps, kda):
     """Host inputs -> device -> kernel -> host outputs, timed with CUDA events."""
     import torch
@@ -391,25 +395,45 @@ def measure_e2e(x, dev, stream, steps, kda):
     devb["out"] = torch.empty(h_out.shape, dtype=x.dtype, device=dev)
     devb["h_final"] = torch.empty(h_hf.shape, dtype=torch.float32, device=dev)
 
-    def call():
-        kda.chunk_fwd_from_host(host["q"], host["k"], host["v"], host["gate_logits"],
-                                host["beta"], host["h0"], host["cu_seqlens"], h_out, h_hf,
-                                devb, stream)
-    call()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    args = (host["q"], host["k"], host["v"], host["gate_logits"], host["beta"], host["h0"],
+            host["cu_seqlens"], h_out, h_hf, devb, stream)
+
+    def pipelined():
+        kda.chunk_fwd_from_host_pipelined(*args, n_segments=E2E_SEGMENTS)
+
+    def serial():
+        kda.chunk_fwd_from_host(*args)
+
+    def timed(call):
         call()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    def inputs_only():  # the floor: the step's host-to-device bytes alone
+        for name, t in host.items():
+            if t is not None:
+                devb[name].copy_(t, non_blocking=True)
+
+    ms = timed(pipelined)
+    ms_serial = timed(serial)
+    with torch.cuda.stream(stream):
+        ms_h2d = timed(inputs_only)
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = h_out.numel() * h_out.element_size() + h_hf.numel() * 4
     return {"value": round(x.n_tok / (ms * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "api": "kda_chunk_fwd_from_host (pinned host buffers)"}
+            "steps": steps,
+            "api": f"kda_chunk_fwd_from_host_pipelined (pinned host buffers, {E2E_SEGMENTS} "
+                   "segments: copies overlap the kernels)",
+            "unpipelined_ms_per_step": round(ms_serial, 3),
+            "h2d_only_ms_per_step": round(ms_h2d, 3)}
 
 
 # ------------------------------------------------------------------ decode step

@@ -21,7 +21,9 @@ import threading
 
 from . import build as _build_mod
 
-__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host", "affine_combine",
+__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host",
+           "chunk_fwd_from_host_pipelined", "fwd_pipeline_plan", "fwd_pipelined_workspace_bytes",
+           "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
            "bwd_timing_start", "bwd_timing_read", "chunk_fwd_variant", "gate_projection",
            "load_library",
@@ -36,7 +38,9 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_chunk_fwd_simt", "kda_chunk_fwd_from_host", "kda_affine_combine",
                     "kda_decode_step", "kda_chunk_bwd_workspace_bytes", "kda_chunk_bwd",
                     "kda_chunk_bwd_static_scratch", "kda_bwd_timing_start",
-                    "kda_bwd_timing_read", "kda_chunk_fwd_variant", "kda_gate_projection")
+                    "kda_bwd_timing_read", "kda_chunk_fwd_variant", "kda_gate_projection",
+                    "kda_chunk_fwd_from_host_pipelined", "kda_chunk_fwd_pipelined_workspace_bytes",
+                    "kda_chunk_fwd_pipeline_plan")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +85,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_from_host.argtypes = [P] * 18 + [I64, I32, I32, I32, I32,
                                                           ctypes.c_int, P]
         lib.kda_chunk_fwd_from_host.restype = ctypes.c_int
+        lib.kda_chunk_fwd_from_host_pipelined.argtypes = [P] * 19 + [
+            ctypes.c_size_t, I64, I32, I32, I32, I32, I32, ctypes.c_int, P]
+        lib.kda_chunk_fwd_from_host_pipelined.restype = ctypes.c_int
+        lib.kda_chunk_fwd_pipelined_workspace_bytes.argtypes = [I32, I32, I32, I32, I32]
+        lib.kda_chunk_fwd_pipelined_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_chunk_fwd_pipeline_plan.argtypes = [P, I32, I64, I32, P, I32]
+        lib.kda_chunk_fwd_pipeline_plan.restype = I32
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
@@ -270,6 +281,62 @@ def chunk_fwd_from_host(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final
         _ptr(dev["beta"]), _ptr(dev.get("h0")), _ptr(dev["cu_seqlens"]),
         _ptr(dev["out"]), _ptr(dev.get("h_final")),
         N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+        ctypes.c_void_p(stream.cuda_stream))
+    _check(lib, st)
+    return out, h_final
+
+
+def fwd_pipelined_workspace_bytes(n_seq, n_heads, d_k, d_v, n_segments) -> int:
+    """Bytes of device workspace ``chunk_fwd_from_host_pipelined`` needs."""
+    return int(load_library().kda_chunk_fwd_pipelined_workspace_bytes(
+        n_seq, n_heads, d_k, d_v, n_segments))
+
+
+def fwd_pipeline_plan(cu_seqlens, n_segments):
+    """The pieces ``chunk_fwd_from_host_pipelined`` runs for these sequence offsets (host
+    only, ``kda_chunk_fwd_pipeline_plan``): a list of
+    ``(t0, t1, n0, n1, h0_carried, hf_carried, segment)``."""
+    lib = load_library()
+    cu = (ctypes.c_int32 * len(cu_seqlens))(*[int(c) for c in cu_seqlens])
+    n_seq, n_tok = len(cu_seqlens) - 1, int(cu_seqlens[-1]) if len(cu_seqlens) else 0
+    count = lib.kda_chunk_fwd_pipeline_plan(ctypes.cast(cu, ctypes.c_void_p), n_seq, n_tok,
+                                            n_segments, None, 0)
+    if count < 0:
+        raise KDAError(1, "invalid cu_seqlens or n_segments")
+    buf = (ctypes.c_int64 * (7 * max(count, 1)))()
+    got = lib.kda_chunk_fwd_pipeline_plan(ctypes.cast(cu, ctypes.c_void_p), n_seq, n_tok,
+                                          n_segments, ctypes.cast(buf, ctypes.c_void_p), count)
+    assert got == count
+    return [tuple(int(buf[7 * j + i]) for i in range(7)) for j in range(count)]
+
+
+def chunk_fwd_from_host_pipelined(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final,
+                                  dev: dict, stream=None, n_segments=16):
+    """``chunk_fwd_from_host`` through ``kda_chunk_fwd_from_host_pipelined``: the copies in
+    and out overlap the computation, segment by segment. ``dev`` as for
+    ``chunk_fwd_from_host``, plus an optional ``workspace`` (a CUDA tensor of at least
+    ``fwd_pipelined_workspace_bytes`` bytes; allocated here when absent)."""
+    import torch
+    lib = load_library()
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens,
+                                device_check=False)
+    device = dev["q"].device
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    need = fwd_pipelined_workspace_bytes(n_seq, H, dk, dv, n_segments)
+    if need == 0:
+        raise KDAError(1, "invalid sizes or n_segments for the pipelined forward")
+    ws = dev.get("workspace")
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        dev["workspace"] = ws
+    st = lib.kda_chunk_fwd_from_host_pipelined(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0),
+        _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
+        _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["gate_logits"]),
+        _ptr(dev["beta"]), _ptr(dev.get("h0")), _ptr(dev["cu_seqlens"]),
+        _ptr(dev["out"]), _ptr(dev.get("h_final")), _ptr(ws), ws.numel() * ws.element_size(),
+        N, n_seq, H, dk, dv, n_segments, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
         ctypes.c_void_p(stream.cuda_stream))
     _check(lib, st)
     return out, h_final

@@ -1,10 +1,14 @@
 // kda_api.cu -- the C ABI declared in include/kda.h: argument validation, kernel
-// choice and launch. Holds no arithmetic of the method.
+// choice and launch, and the host-side schedule of the pipelined forward (its pieces, its
+// streams and the one small kernel that writes the pieces' sequence offsets). Holds no
+// arithmetic of the method.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include "../../include/kda.h"
 #include "kda_internal.h"
@@ -84,6 +88,89 @@ kda_status run(const kda::FwdArgs &p, kda_dtype dtype, void *stream, Path path) 
     if (path == Path::kAuto && kda::tc_supported(p))
         return launched(kda::launch_tc(p, st), "tensor-core kernel launch");
     return launched(kda::launch_simt(p, st), "SIMT kernel launch");
+}
+
+// ---- pipelined forward from host memory -------------------------------------------------
+//
+// The token range is cut into segments; segment i's inputs are copied in on one stream
+// while segment i-1 is computed on the caller's stream and segment i-2's outputs are copied
+// out on a third. Each boundary is placed a multiple of 16 tokens after the start of the
+// sequence that holds it, so every piece keeps its sequence's chunk grid, and the state of
+// a sequence cut by a boundary is handed from one piece to the next in fp32 through the
+// workspace: the result is the one the unsegmented call gives, bit for bit.
+
+constexpr int kMaxSegments = 64;
+
+// A piece: tokens [t0, t1) holding sequences [n0, n1) -- whole ones, or the part of one
+// sequence that lies in a segment. Its start state is the caller's h0 rows n0.. (zeros
+// without h0) or the carried state; its final state goes to the caller's h_final rows
+// n0.. (nowhere without h_final) or to the carried state.
+struct FwdPiece {
+    int64_t t0, t1;
+    int32_t n0, n1;
+    int32_t h0_carried, hf_carried;
+    int32_t segment;
+};
+
+// cu: host cu_seqlens, already checked (cu[0] = 0, non-decreasing, cu[n_seq] = n_tok).
+void plan_pieces(const int32_t *cu, int32_t n_seq, int64_t n_tok, int32_t n_segments,
+                 std::vector<FwdPiece> &out) {
+    out.clear();
+    std::vector<int64_t> bounds{0};
+    for (int32_t i = 1; i < n_segments; ++i) {
+        const int64_t b = n_tok * i / n_segments;
+        if (b <= 0 || b >= n_tok) continue;
+        // the sequence holding token b: the last n with cu[n] <= b (then cu[n + 1] > b)
+        const int32_t n = (int32_t)(std::upper_bound(cu, cu + n_seq + 1, (int32_t)b) - cu) - 1;
+        const int64_t at = cu[n] + (b - cu[n]) / 16 * 16;
+        if (at > bounds.back() && at < n_tok) bounds.push_back(at);
+    }
+    bounds.push_back(n_tok);
+    int32_t n = 0;          // first sequence whose final state is not yet written
+    bool carrying = false;  // sequence n started in an earlier segment
+    for (size_t i = 0; i + 1 < bounds.size(); ++i) {
+        const int64_t t0 = bounds[i], t1 = bounds[i + 1];
+        const int32_t seg = (int32_t)i;
+        if (carrying) {
+            const bool beyond = cu[n + 1] > t1;
+            out.push_back({t0, beyond ? t1 : (int64_t)cu[n + 1], n, n + 1, 1, beyond ? 1 : 0, seg});
+            if (beyond) continue;
+            ++n;
+            carrying = false;
+        }
+        const int32_t c0 = n;
+        while (n < n_seq && cu[n + 1] <= t1) ++n;
+        if (n > c0) out.push_back({cu[c0], cu[n], c0, n, 0, 0, seg});
+        if (n < n_seq && cu[n] < t1) {  // starts here, ends in a later segment
+            out.push_back({cu[n], t1, n, n + 1, 0, 1, seg});
+            carrying = true;
+        }
+    }
+}
+
+struct PieceTable {
+    int32_t n0[3 * kMaxSegments], count[3 * kMaxSegments], off[3 * kMaxSegments];
+    int32_t t0[3 * kMaxSegments], t1[3 * kMaxSegments];
+    int32_t n_pieces;
+};
+
+// Piece j's cu_seqlens, relative to its first token: entry k = clamp(cu[n0 + k], t0, t1) - t0,
+// k = 0 .. count (count = its number of sequences), written at table + off[j].
+__global__ void piece_offsets_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ table,
+                                     const PieceTable pt) {
+    for (int j = 0; j < pt.n_pieces; ++j)
+        for (int k = threadIdx.x; k <= pt.count[j]; k += blockDim.x)
+            table[pt.off[j] + k] = min(max(cu[pt.n0[j] + k], pt.t0[j]), pt.t1[j]) - pt.t0[j];
+}
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+size_t pipeline_workspace(int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
+                          int32_t n_segments) {
+    // two carried states, then the pieces' offset tables: at most 3 pieces per segment,
+    // 2 entries for a piece of one cut sequence, count + 1 for a run of whole ones
+    const size_t carry = align256((size_t)n_heads * d_k * d_v * 4);
+    return 2 * carry + align256(((size_t)n_seq + 5 * (size_t)n_segments + 1) * 4);
 }
 
 }  // namespace
@@ -420,6 +507,193 @@ kda_status kda_chunk_fwd_from_host(
         if (e != cudaSuccess) return launched(e, "device-to-host copy");
     }
     return ok();
+}
+
+size_t kda_chunk_fwd_pipelined_workspace_bytes(int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                               int32_t d_v, int32_t n_segments) {
+    if (n_seq < 0 || n_heads <= 0 || d_k <= 0 || d_v <= 0 || n_segments < 1 ||
+        n_segments > kMaxSegments)
+        return 0;
+    return pipeline_workspace(n_seq, n_heads, d_k, d_v, n_segments);
+}
+
+int32_t kda_chunk_fwd_pipeline_plan(const int32_t *host_cu_seqlens, int32_t n_seq,
+                                    int64_t n_tok, int32_t n_segments, int64_t *pieces,
+                                    int32_t capacity) {
+    if (!host_cu_seqlens || n_seq < 0 || n_tok < 0 || n_segments < 1 ||
+        n_segments > kMaxSegments || (n_tok > 0 && n_seq == 0) || n_tok > 0x7fffffffLL)
+        return -1;
+    if (n_seq > 0 && (host_cu_seqlens[0] != 0 || host_cu_seqlens[n_seq] != n_tok)) return -1;
+    for (int32_t n = 0; n < n_seq; ++n)
+        if (host_cu_seqlens[n + 1] < host_cu_seqlens[n]) return -1;
+    std::vector<FwdPiece> plan;
+    if (n_seq > 0) plan_pieces(host_cu_seqlens, n_seq, n_tok, n_segments, plan);
+    if (pieces) {
+        if ((int32_t)plan.size() > capacity) return -1;
+        for (size_t j = 0; j < plan.size(); ++j) {
+            int64_t *r = pieces + 7 * j;
+            r[0] = plan[j].t0; r[1] = plan[j].t1; r[2] = plan[j].n0; r[3] = plan[j].n1;
+            r[4] = plan[j].h0_carried; r[5] = plan[j].hf_carried; r[6] = plan[j].segment;
+        }
+    }
+    return (int32_t)plan.size();
+}
+
+kda_status kda_chunk_fwd_from_host_pipelined(
+    const void *host_q, const void *host_k, const void *host_v,
+    const float *host_gate_logits, const float *host_beta, const float *host_h0,
+    const int32_t *host_cu_seqlens, void *host_out, float *host_h_final, void *dev_q,
+    void *dev_k, void *dev_v, float *dev_gate_logits, float *dev_beta, float *dev_h0,
+    int32_t *dev_cu_seqlens, void *dev_out, float *dev_h_final, void *dev_workspace,
+    size_t workspace_bytes, int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
+    int32_t d_v, int32_t n_segments, kda_dtype dtype, void *stream) {
+    kda::FwdArgs whole = pack(dev_q, dev_k, dev_v, dev_gate_logits, dev_beta,
+                              host_h0 ? dev_h0 : nullptr, dev_cu_seqlens, dev_out,
+                              host_h_final ? dev_h_final : nullptr, n_tok, n_seq, n_heads, d_k,
+                              d_v, dtype);
+    kda_status s = validate(whole, dtype);
+    if (s != KDA_OK) return s;
+    if (n_segments < 1 || n_segments > kMaxSegments)
+        return fail(KDA_ERR_INVALID_ARG, "n_segments must be in [1, 64]");
+    if (n_seq > 0 && !host_cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "host_cu_seqlens is NULL");
+    if (n_tok > 0 && (!host_q || !host_k || !host_v || !host_gate_logits || !host_beta ||
+                      !host_out))
+        return fail(KDA_ERR_INVALID_ARG, "host input/output pointers are required");
+    if ((host_h0 && !dev_h0) || (host_h_final && !dev_h_final))
+        return fail(KDA_ERR_INVALID_ARG, "a host state buffer needs its device buffer");
+    if (n_seq > 0 && kda_chunk_fwd_pipeline_plan(host_cu_seqlens, n_seq, n_tok, 1, nullptr, 0) < 0)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "host_cu_seqlens must start at 0, not decrease and end at n_tok (< 2^31)");
+    const size_t need = pipeline_workspace(n_seq, n_heads, d_k, d_v, n_segments);
+    if (!dev_workspace || workspace_bytes < need || ((uintptr_t)dev_workspace & 255u))
+        return fail(KDA_ERR_INVALID_ARG, "dev_workspace must be 256-byte aligned and hold "
+                                         "kda_chunk_fwd_pipelined_workspace_bytes bytes");
+    if (n_seq == 0) return ok();
+    const size_t es = dtype == KDA_BF16 ? 2 : 4;
+    const size_t rk = (size_t)n_heads * d_k, rv = (size_t)n_heads * d_v;  // elements per token
+    const size_t ns = (size_t)n_heads * d_k * d_v;                         // floats per sequence
+    // a cut anywhere keeps every 16-byte-aligned tile of a piece aligned only if a token's
+    // rows are whole multiples of 16 bytes; otherwise the call runs as one piece
+    const bool cuttable = (rk * es) % 16 == 0 && (rv * es) % 16 == 0 && (rk * 4) % 16 == 0;
+    std::vector<FwdPiece> plan;
+    plan_pieces(host_cu_seqlens, n_seq, n_tok, cuttable ? n_segments : 1, plan);
+
+    char *ws = static_cast<char *>(dev_workspace);
+    const size_t carry_b = align256(ns * 4);
+    float *carry[2] = {reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + carry_b)};
+    int32_t *table = reinterpret_cast<int32_t *>(ws + 2 * carry_b);
+    PieceTable pt{};
+    pt.n_pieces = (int32_t)plan.size();
+    int32_t off = 0;
+    for (size_t j = 0; j < plan.size(); ++j) {
+        pt.n0[j] = plan[j].n0;
+        pt.count[j] = plan[j].n1 - plan[j].n0;
+        pt.t0[j] = (int32_t)plan[j].t0;
+        pt.t1[j] = (int32_t)plan[j].t1;
+        pt.off[j] = off;
+        off += pt.count[j] + 1;
+    }
+
+    cudaStream_t st = (cudaStream_t)stream, s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // start, inputs landed, piece done
+    struct Release {  // streams and events are freed once their queued work completes
+        cudaStream_t *a, *b; cudaEvent_t *e;
+        ~Release() {
+            for (int i = 0; i < 3; ++i) if (e[i]) cudaEventDestroy(e[i]);
+            if (*a) cudaStreamDestroy(*a);
+            if (*b) cudaStreamDestroy(*b);
+        }
+    } release{&s_in, &s_out, ev};
+    cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return launched(e, "pipeline stream or event creation");
+    // from here on, every return first makes the caller's stream wait for both side
+    // streams, so nothing queued on them outlives the call's ordering
+    auto finish = [&](kda_status r) {
+        if (cudaEventRecord(ev[1], s_in) == cudaSuccess) cudaStreamWaitEvent(st, ev[1], 0);
+        if (cudaEventRecord(ev[2], s_out) == cudaSuccess) cudaStreamWaitEvent(st, ev[2], 0);
+        return r;
+    };
+
+    auto h2d = [&](void *dst, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s_in) : cudaSuccess;
+    };
+    auto d2h = [&](void *dst, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s_out) : cudaSuccess;
+    };
+    // both side streams start after the caller's earlier work (which may still read the
+    // device buffers or the workspace)
+    e = cudaEventRecord(ev[0], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, ev[0], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev[0], 0);
+    if (e == cudaSuccess) e = h2d(dev_cu_seqlens, host_cu_seqlens, (size_t)(n_seq + 1) * 4);
+    if (e == cudaSuccess) {
+        piece_offsets_kernel<<<1, 256, 0, s_in>>>(dev_cu_seqlens, table, pt);
+        e = cudaGetLastError();
+        kda::count_launches(1);
+    }
+    if (e != cudaSuccess) return finish(launched(e, "pipeline set-up"));
+
+    const char *hq = static_cast<const char *>(host_q), *hk = static_cast<const char *>(host_k);
+    const char *hv = static_cast<const char *>(host_v);
+    char *dq = static_cast<char *>(dev_q), *dk_ = static_cast<char *>(dev_k);
+    char *dv_ = static_cast<char *>(dev_v), *dout = static_cast<char *>(dev_out);
+    char *hout = static_cast<char *>(host_out);
+    size_t j = 0;
+    while (j < plan.size()) {
+        const int32_t seg = plan[j].segment;
+        size_t j1 = j;
+        while (j1 < plan.size() && plan[j1].segment == seg) ++j1;
+        const int64_t t0 = plan[j].t0, t1 = plan[j1 - 1].t1;
+        // rows of h0 of the sequences that start in this segment; rows of h_final of the
+        // sequences that end in it (both contiguous)
+        int32_t r0 = n_seq, r1 = 0, f0 = n_seq, f1 = 0;
+        for (size_t i = j; i < j1; ++i) {
+            if (!plan[i].h0_carried) { r0 = std::min(r0, plan[i].n0); r1 = std::max(r1, plan[i].n1); }
+            if (!plan[i].hf_carried) { f0 = std::min(f0, plan[i].n0); f1 = std::max(f1, plan[i].n1); }
+        }
+        const size_t nt = (size_t)(t1 - t0);
+        if (host_h0 && r1 > r0)
+            e = h2d(dev_h0 + (size_t)r0 * ns, host_h0 + (size_t)r0 * ns, (size_t)(r1 - r0) * ns * 4);
+        if (e == cudaSuccess) e = h2d(dq + t0 * rk * es, hq + t0 * rk * es, nt * rk * es);
+        if (e == cudaSuccess) e = h2d(dk_ + t0 * rk * es, hk + t0 * rk * es, nt * rk * es);
+        if (e == cudaSuccess) e = h2d(dv_ + t0 * rv * es, hv + t0 * rv * es, nt * rv * es);
+        if (e == cudaSuccess)
+            e = h2d(dev_gate_logits + t0 * rk, host_gate_logits + t0 * rk, nt * rk * 4);
+        if (e == cudaSuccess)
+            e = h2d(dev_beta + t0 * n_heads, host_beta + t0 * n_heads, nt * n_heads * 4);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[1], s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
+        if (e != cudaSuccess) return finish(launched(e, "pipeline host-to-device copy"));
+        for (size_t i = j; i < j1; ++i) {
+            const FwdPiece &pc = plan[i];
+            const float *h0 = pc.h0_carried ? carry[seg & 1]
+                              : host_h0     ? dev_h0 + (size_t)pc.n0 * ns : nullptr;
+            float *hf = pc.hf_carried ? carry[(seg + 1) & 1]
+                        : host_h_final ? dev_h_final + (size_t)pc.n0 * ns : nullptr;
+            kda::FwdArgs p = pack(dq + pc.t0 * rk * es, dk_ + pc.t0 * rk * es,
+                                  dv_ + pc.t0 * rv * es, dev_gate_logits + pc.t0 * rk,
+                                  dev_beta + pc.t0 * n_heads, h0, table + pt.off[i],
+                                  dout + pc.t0 * rv * es, hf, pc.t1 - pc.t0, pc.n1 - pc.n0,
+                                  n_heads, d_k, d_v, dtype);
+            s = run(p, dtype, stream, Path::kAuto);
+            if (s != KDA_OK) return finish(s);
+        }
+        e = cudaEventRecord(ev[2], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev[2], 0);
+        if (e == cudaSuccess) e = d2h(hout + t0 * rv * es, dout + t0 * rv * es, nt * rv * es);
+        if (e == cudaSuccess && host_h_final && f1 > f0)
+            e = d2h(host_h_final + (size_t)f0 * ns, dev_h_final + (size_t)f0 * ns,
+                    (size_t)(f1 - f0) * ns * 4);
+        if (e != cudaSuccess) return finish(launched(e, "pipeline device-to-host copy"));
+        j = j1;
+    }
+    // the caller's stream continues after the last copy out
+    e = cudaEventRecord(ev[0], s_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[0], 0);
+    return finish(launched(e, "pipeline completion"));
 }
 
 }  // extern "C"

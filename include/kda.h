@@ -331,6 +331,63 @@ kda_status kda_chunk_fwd_from_host(
     int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
     kda_dtype dtype, void *stream);
 
+/*
+ * kda_chunk_fwd_from_host_pipelined -- kda_chunk_fwd_from_host with the copies overlapped
+ * with the computation. The token range is cut into at most n_segments segments of about
+ * n_tok / n_segments tokens (1 <= n_segments <= 64); segment i's inputs are copied in on
+ * one stream while segment i-1 is computed on `stream` and segment i-2's outputs (and
+ * the final states of the sequences that end in it) are copied out on another. Each cut
+ * lies a multiple of 16 tokens after the start of the sequence that holds it, so every
+ * piece keeps its sequence's 16-token chunk grid, and a cut sequence's state passes from
+ * one piece to the next in fp32 (chunks run serially through the state recurrence, "From
+ * Numerical Stability to Load Balancing", §2.1, so a sequence may be continued from any
+ * chunk boundary given the state there, as kda_chunk_fwd's h0 already allows): out
+ * and h_final equal those of kda_chunk_fwd on the whole input bit for bit (the same
+ * kernels run on the same chunks). Cuts are made only when a token's q/k/v/gate rows are
+ * whole multiples of 16 bytes (true for d_k = d_v = 128); otherwise the call runs as one
+ * piece with the same overlap-free schedule as kda_chunk_fwd_from_host.
+ *   host_*, dev_*  as for kda_chunk_fwd_from_host (host buffers preferably pinned: a
+ *                  pageable one makes its copy wait for the caller's earlier work);
+ *                  dev_cu_seqlens receives host_cu_seqlens.
+ *   dev_workspace  device memory, 256-byte aligned, at least
+ *                  kda_chunk_fwd_pipelined_workspace_bytes(n_seq, n_heads, d_k, d_v,
+ *                  n_segments) bytes: two carried states and the pieces' sequence
+ *                  offsets. Owned by the caller; nothing in it has to be initialised.
+ * The call creates two streams and three events, released once their queued work is done;
+ * it allocates no memory and launches one small kernel (the pieces' offsets) besides the
+ * forward kernels. `stream` waits for the last copy before its next work. The host
+ * buffers must stay valid until then. Errors as for kda_chunk_fwd_from_host, plus
+ * KDA_ERR_INVALID_ARG for n_segments outside [1, 64], a too-small or misaligned
+ * workspace, or a host_cu_seqlens that does not start at 0, decreases, or does not end
+ * at n_tok.
+ */
+kda_status kda_chunk_fwd_from_host_pipelined(
+    const void *host_q, const void *host_k, const void *host_v,
+    const float *host_gate_logits, const float *host_beta, const float *host_h0,
+    const int32_t *host_cu_seqlens, void *host_out, float *host_h_final,
+    void *dev_q, void *dev_k, void *dev_v, float *dev_gate_logits, float *dev_beta,
+    float *dev_h0, int32_t *dev_cu_seqlens, void *dev_out, float *dev_h_final,
+    void *dev_workspace, size_t workspace_bytes, int64_t n_tok, int32_t n_seq,
+    int32_t n_heads, int32_t d_k, int32_t d_v, int32_t n_segments, kda_dtype dtype,
+    void *stream);
+
+/* Workspace bytes of kda_chunk_fwd_from_host_pipelined; 0 for invalid arguments. */
+size_t kda_chunk_fwd_pipelined_workspace_bytes(int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                               int32_t d_v, int32_t n_segments);
+
+/*
+ * kda_chunk_fwd_pipeline_plan -- the pieces kda_chunk_fwd_from_host_pipelined runs, on the
+ * host only (no device work). Piece j is 7 int64 at pieces[7 j]: token range [t0, t1),
+ * sequence range [n0, n1), h0_carried (1: starts from the state carried from the previous
+ * piece of its sequence, 0: from h0), hf_carried (1: its final state is carried to the next
+ * piece, 0: it is the sequence's h_final), segment index. Returns the number of pieces
+ * (pieces may be NULL to count them), or -1 for an invalid host_cu_seqlens, n_segments
+ * outside [1, 64], or a capacity below the count.
+ */
+int32_t kda_chunk_fwd_pipeline_plan(const int32_t *host_cu_seqlens, int32_t n_seq,
+                                    int64_t n_tok, int32_t n_segments, int64_t *pieces,
+                                    int32_t capacity);
+
 #ifdef __cplusplus
 }
 #endif
