@@ -251,9 +251,10 @@ def max_over_ranks(x: float, on: bool, device) -> float:
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_sample(x, max_tokens: int, heads=None):
+def oracle_sample(x, max_tokens: int, heads=None, threads=None):
     """The oracle on the first ``max_tokens`` tokens of every sequence (and the given
-    heads). Returns (seconds, token-heads processed, threads)."""
+    heads), on ``threads`` host threads (default: all). Returns (seconds, token-heads
+    processed, threads)."""
     import kda_inputs as K
     from oracle import recurrence
     px = K.prefix(x, max_tokens)
@@ -261,7 +262,7 @@ def oracle_sample(x, max_tokens: int, heads=None):
         px = K.slice_heads(px, heads)
     cpu = lambda t: None if t is None else t.detach().to("cpu")  # noqa: E731
     args = [cpu(px.q), cpu(px.k), cpu(px.v), cpu(px.a), cpu(px.beta), cpu(px.h0)]
-    threads = recurrence.default_threads()
+    threads = threads or recurrence.default_threads()
     recurrence.build()
     t0 = time.perf_counter()
     recurrence.kda_forward(*args, px.cu_host, threads=threads)
@@ -279,11 +280,22 @@ def cpu_baseline(x, budget_s: float = 15.0):
             break
         tokens = min(tokens * 4, max(x.lengths()))
     value = th / x.n_heads / dt
+    # the same oracle once on one thread, on a smaller prefix (about budget_s / 8)
+    t1 = 64
+    while True:
+        dt1, th1, _ = oracle_sample(x, t1, threads=1)
+        if dt1 > budget_s / 16 or t1 >= max(x.lengths()):
+            break
+        t1 = min(t1 * 4, max(x.lengths()))
     return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds": dt,
             "sample": f"fp64 token-by-token oracle on the first {tokens} tokens of every "
                       f"sequence, all {x.n_heads} heads ({th} token-heads), "
-                      f"{threads} host threads"}
+                      f"{threads} host threads",
+            "single_thread": {"value": th1 / x.n_heads / dt1, "unit": UNIT, "cores": 1,
+                              "seconds": dt1,
+                              "sample": f"first {t1} tokens of every sequence, all "
+                                        f"{x.n_heads} heads ({th1} token-heads)"}}
 
 
 # ------------------------------------------------------------------ our arm
