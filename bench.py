@@ -254,7 +254,7 @@ def max_over_ranks(x: float, on: bool, device) -> float:
 def oracle_sample(x, max_tokens: int, heads=None, threads=None):
     """The oracle on the first ``max_tokens`` tokens of every sequence (and the given
     heads), on ``threads`` host threads (default: all). Returns (seconds, token-heads
-    processed, threads)."""
+    processed, threads, the oracle's outputs of the sample)."""
     import kda_inputs as K
     from oracle import recurrence
     px = K.prefix(x, max_tokens)
@@ -265,17 +265,43 @@ def oracle_sample(x, max_tokens: int, heads=None, threads=None):
     threads = threads or recurrence.default_threads()
     recurrence.build()
     t0 = time.perf_counter()
-    recurrence.kda_forward(*args, px.cu_host, threads=threads)
+    o_ref, _ = recurrence.kda_forward(*args, px.cu_host, threads=threads, want_state=False)
     dt = time.perf_counter() - t0
-    return dt, px.n_tok * px.n_heads, threads
+    return dt, px.n_tok * px.n_heads, threads, o_ref
 
 
-def cpu_baseline(x, budget_s: float = 15.0):
+def prefix_rel_l2(x, out, tokens: int, o_ref) -> float:
+    """rel-L2 of the GPU output ``out`` (the whole workload) against the oracle's output
+    ``o_ref`` on the first ``tokens`` tokens of every sequence (by causality those rows do
+    not depend on anything after them)."""
+    num = den = 0.0
+    row = 0
+    for i in range(x.n_seq):
+        s0 = x.cu_host[i]
+        n = min(x.cu_host[i + 1] - s0, tokens)
+        for c in range(0, n, 8192):
+            m = min(8192, n - c)
+            g = out[s0 + c:s0 + c + m].detach().to("cpu", torch_float64()).numpy()
+            r = o_ref[row + c:row + c + m]
+            num += float(((g - r) ** 2).sum())
+            den += float((r ** 2).sum())
+        row += n
+    return (num / den) ** 0.5 if den > 0 else num ** 0.5
+
+
+def torch_float64():
+    import torch
+    return torch.float64
+
+
+def cpu_baseline(x, budget_s: float = 15.0, out=None):
     """Time the oracle on a bounded prefix sample, growing it until it takes a few
-    seconds, scaled to the workload's tokens/s (a token counts all H heads)."""
+    seconds, scaled to the workload's tokens/s (a token counts all H heads). With the
+    GPU's output ``out`` of the same inputs, also its rel-L2 against the oracle on that
+    sample (key ``parity``)."""
     tokens = 256
     while True:
-        dt, th, threads = oracle_sample(x, tokens)
+        dt, th, threads, o_ref = oracle_sample(x, tokens)
         if dt > budget_s / 4 or tokens >= max(x.lengths()):
             break
         tokens = min(tokens * 4, max(x.lengths()))
@@ -283,12 +309,20 @@ def cpu_baseline(x, budget_s: float = 15.0):
     # the same oracle once on one thread, on a smaller prefix (about budget_s / 8)
     t1 = 64
     while True:
-        dt1, th1, _ = oracle_sample(x, t1, threads=1)
+        dt1, th1, _, _ = oracle_sample(x, t1, threads=1)
         if dt1 > budget_s / 16 or t1 >= max(x.lengths()):
             break
         t1 = min(t1 * 4, max(x.lengths()))
+    parity = None
+    if out is not None:
+        import torch
+        parity = {"rel_l2_out": prefix_rel_l2(x, out, tokens, o_ref),
+                  "bar": 1e-2 if x.dtype == torch.bfloat16 else 1e-4,
+                  "sample": f"outputs of the first {tokens} tokens of every sequence, all "
+                            f"{x.n_heads} heads, of the timed run against the fp64 oracle"}
+    del o_ref
     return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "seconds": dt,
+            "seconds": dt, "parity": parity,
             "sample": f"fp64 token-by-token oracle on the first {tokens} tokens of every "
                       f"sequence, all {x.n_heads} heads ({th} token-heads), "
                       f"{threads} host threads",
@@ -383,7 +417,9 @@ def run_ours(args):
             "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk.summary(), "kernel_digest": kernel_source_digest()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x)
+        cb = cpu_baseline(x, out=out)
+        line["parity"] = cb.pop("parity")
+        line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
     if on:
@@ -876,7 +912,7 @@ def run_reference(args):
     tokens = 512
     # size one step to about a second of host work
     while True:
-        dt, th, threads = oracle_sample(x, tokens)
+        dt, th, threads, _ = oracle_sample(x, tokens)
         if dt > 0.5 or tokens >= max(x.lengths()):
             break
         tokens = min(tokens * 2, max(x.lengths()))
@@ -885,7 +921,7 @@ def run_reference(args):
     t0 = time.perf_counter()
     total_th = 0
     for _ in range(args.steps):
-        _, th, threads = oracle_sample(x, tokens)
+        _, th, threads, _ = oracle_sample(x, tokens)
         total_th += th
     el = time.perf_counter() - t0
     value = total_th / x.n_heads / el
