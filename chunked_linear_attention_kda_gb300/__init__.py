@@ -310,16 +310,25 @@ def fwd_pipeline_plan(cu_seqlens, n_segments):
     return [tuple(int(buf[7 * j + i]) for i in range(7)) for j in range(count)]
 
 
+PIPELINE_SEGMENT_BYTES = 32 << 20   # default: about this many input bytes per segment
+PIPELINE_MAX_SEGMENTS = 16
+
+
 def chunk_fwd_from_host_pipelined(q, k, v, gate_logits, beta, h0, cu_seqlens, out, h_final,
-                                  dev: dict, stream=None, n_segments=16):
+                                  dev: dict, stream=None, n_segments=None):
     """``chunk_fwd_from_host`` through ``kda_chunk_fwd_from_host_pipelined``: the copies in
     and out overlap the computation, segment by segment. ``dev`` as for
     ``chunk_fwd_from_host``, plus an optional ``workspace`` (a CUDA tensor of at least
-    ``fwd_pipelined_workspace_bytes`` bytes; allocated here when absent)."""
+    ``fwd_pipelined_workspace_bytes`` bytes; allocated here when absent). ``n_segments``
+    defaults to one segment per ``PIPELINE_SEGMENT_BYTES`` of inputs, at most
+    ``PIPELINE_MAX_SEGMENTS``: below that size the per-segment costs outweigh the overlap."""
     import torch
     lib = load_library()
     N, H, dk, dv, n_seq = _dims(q, k, v, gate_logits, beta, h0, cu_seqlens,
                                 device_check=False)
+    if n_segments is None:
+        in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, gate_logits, beta))
+        n_segments = max(1, min(PIPELINE_MAX_SEGMENTS, in_bytes // PIPELINE_SEGMENT_BYTES))
     device = dev["q"].device
     if stream is None:
         stream = torch.cuda.current_stream(device)

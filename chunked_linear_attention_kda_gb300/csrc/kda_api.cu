@@ -577,6 +577,12 @@ kda_status kda_chunk_fwd_from_host_pipelined(
     const bool cuttable = (rk * es) % 16 == 0 && (rv * es) % 16 == 0 && (rk * 4) % 16 == 0;
     std::vector<FwdPiece> plan;
     plan_pieces(host_cu_seqlens, n_seq, n_tok, cuttable ? n_segments : 1, plan);
+    if (plan.empty() || plan.back().segment == 0)  // one segment: nothing to overlap
+        return kda_chunk_fwd_from_host(host_q, host_k, host_v, host_gate_logits, host_beta,
+                                       host_h0, host_cu_seqlens, host_out, host_h_final, dev_q,
+                                       dev_k, dev_v, dev_gate_logits, dev_beta, dev_h0,
+                                       dev_cu_seqlens, dev_out, dev_h_final, n_tok, n_seq,
+                                       n_heads, d_k, d_v, dtype, stream);
 
     char *ws = static_cast<char *>(dev_workspace);
     const size_t carry_b = align256(ns * 4);

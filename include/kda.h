@@ -344,8 +344,9 @@ kda_status kda_chunk_fwd_from_host(
  * chunk boundary given the state there, as kda_chunk_fwd's h0 already allows): out
  * and h_final equal those of kda_chunk_fwd on the whole input bit for bit (the same
  * kernels run on the same chunks). Cuts are made only when a token's q/k/v/gate rows are
- * whole multiples of 16 bytes (true for d_k = d_v = 128); otherwise the call runs as one
- * piece with the same overlap-free schedule as kda_chunk_fwd_from_host.
+ * whole multiples of 16 bytes (true for d_k = d_v = 128). When the plan has one segment
+ * (n_segments = 1, too few tokens to cut, or rows that cannot be cut) the call is
+ * kda_chunk_fwd_from_host: one stream, no overlap, the workspace unused.
  *   host_*, dev_*  as for kda_chunk_fwd_from_host (host buffers preferably pinned: a
  *                  pageable one makes its copy wait for the caller's earlier work);
  *                  dev_cu_seqlens receives host_cu_seqlens.
