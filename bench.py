@@ -15,8 +15,9 @@ the elapsed time for the report).
 Reported alongside the device-timed value:
   e2e          the same metric through ``kda_chunk_fwd_from_host_pipelined`` with pinned
                host buffers: H2D copies of the inputs, the kernels and D2H copies of the
-               outputs inside the timed region, overlapped segment by segment (the
-               one-stream ``kda_chunk_fwd_from_host`` time beside it);
+               outputs inside the timed region, overlapped segment by segment; the
+               median of event-timed calls (the mean beside it), the one-stream
+               ``kda_chunk_fwd_from_host`` time and the inputs' copy alone reported too;
   roofline     algorithmic bytes per launch / CUDA-event launch time against the
                measured HBM copy bandwidth (MEASURED_PEAKS.json);
   cpu_baseline the fp64 oracle on the host cores on a bounded sample (rank 0, N = 1);
@@ -454,31 +455,34 @@ def measure_e2e(x, dev, stream, steps, kda):
         kda.chunk_fwd_from_host(*args)
 
     def timed(call):
+        """(median, mean) over ``steps`` back-to-back calls, each bracketed by CUDA events
+        on the stream (every call ends with the stream waiting for its last copy)."""
         call()
         torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
             call()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / steps
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        return statistics.median(per), ev[0].elapsed_time(ev[steps]) / steps
 
     def inputs_only():  # the floor: the step's host-to-device bytes alone
         for name, t in host.items():
             if t is not None:
                 devb[name].copy_(t, non_blocking=True)
 
-    ms = timed(pipelined)
-    ms_serial = timed(serial)
+    ms, ms_mean = timed(pipelined)
+    ms_serial, _ = timed(serial)
     with torch.cuda.stream(stream):
-        ms_h2d = timed(inputs_only)
+        ms_h2d, _ = timed(inputs_only)
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = h_out.numel() * h_out.element_size() + h_hf.numel() * 4
     return {"value": round(x.n_tok / (ms * 1e-3), 1), "unit": UNIT,
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps,
+            "ms_per_step": round(ms, 3), "mean_ms_per_step": round(ms_mean, 3),
+            "statistic": f"median of {steps} event-timed calls",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "api": f"kda_chunk_fwd_from_host_pipelined (pinned host buffers, {segments} "
                    "segment(s): copies overlap the kernels)",
             "unpipelined_ms_per_step": round(ms_serial, 3),
