@@ -2,15 +2,19 @@
 ``kda_chunk_fwd_pipeline_plan`` returns (the ones ``kda_chunk_fwd_from_host_pipelined``
 runs) cover every token once and in order, read each sequence's h0 once and write its
 h_final once, hand a cut sequence's state from one segment to the next, cut only on the
-sequence's 16-token chunk grid, and fit the workspace's offset table; plus the pipelined
-call's host validation (no pointer is dereferenced, no kernel launched).
+sequence's 16-token chunk grid, and fit the workspace's offset table; executed piece by
+piece on the fp64 oracle with the device's offset rule and carried states, they reproduce
+one whole-input run bit for bit; plus the pipelined call's host validation (no pointer is
+dereferenced, no kernel launched).
 """
 import ctypes
 
 import numpy as np
 import pytest
+import torch
 
 import chunked_linear_attention_kda_gb300 as kda
+import kda_inputs as K
 from chunked_linear_attention_kda_gb300 import build as kbuild
 
 
@@ -142,3 +146,41 @@ def test_pipelined_host_validation(lib):
     assert b"cu_seqlens" in lib.kda_last_error()
     assert _call(lib, need, 4, cu=(0, 40, 30, 64)) == 1  # cu_seqlens decreases
     assert _call(lib, need, 4, cu=(2, 64)) == 1           # cu_seqlens does not start at 0
+
+
+def run_plan_on_the_oracle(x, n_segments):
+    """Execute the plan the way the pipelined entry point does -- each piece one forward
+    call on its token range, with cu_seqlens clamp(cu[n0 + k], t0, t1) - t0, its start state
+    from h0 or the carried state and its final state to h_final or the carried state --
+    with the fp64 oracle standing in for the kernels."""
+    from oracle import recurrence
+    cu = [int(c) for c in x.cu_host]
+    f64 = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    q, k, v, a, beta, h0 = (f64(t) for t in (x.q, x.k, x.v, x.a, x.beta, x.h0))
+    out = np.full((x.n_tok, x.n_heads, x.d_v), np.nan)
+    hf = np.full((x.n_seq, x.n_heads, x.d_k, x.d_v), np.nan)
+    carry = [None, None]
+    for (t0, t1, n0, n1, h0c, hfc, seg) in kda.fwd_pipeline_plan(cu, n_segments):
+        local = [min(max(cu[n0 + j], t0), t1) - t0 for j in range(n1 - n0 + 1)]
+        start = carry[seg & 1][None] if h0c else (None if h0 is None else h0[n0:n1])
+        o, h = recurrence.kda_forward(q[t0:t1], k[t0:t1], v[t0:t1], a[t0:t1], beta[t0:t1],
+                                      start, local)
+        out[t0:t1] = o
+        if hfc:
+            carry[(seg + 1) & 1] = h[0]
+        else:
+            hf[n0:n1] = h
+    return out, hf
+
+
+@pytest.mark.parametrize("n_segments", [2, 5, 16, 64])
+@pytest.mark.parametrize("lens,with_h0", [([2000], False), ([300, 0, 517, 33, 0], True),
+                                          ([0, 900, 16, 17, 1000], True), ([0, 0], True)])
+def test_executing_the_plan_reproduces_the_whole_run(n_segments, lens, with_h0):
+    from oracle import recurrence
+    x = K.make_inputs(lens, 2, 8, 6, dtype=torch.float32, seed=sum(lens) + n_segments,
+                      h0_std=0.3 if with_h0 else None)
+    o_ref, h_ref = recurrence.kda_forward(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_host)
+    out, hf = run_plan_on_the_oracle(x, n_segments)
+    # the carried fp64 state continues the token recurrence exactly: equal bit for bit
+    assert np.array_equal(out, o_ref) and np.array_equal(hf, h_ref)
