@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstdio>
 #include <string>
 #include <vector>
@@ -80,11 +81,23 @@ kda_status launched(cudaError_t e, const char *what) {
 
 enum class Path { kAuto, kSimt };
 
+// KDA_FWD_KERNEL=tc16 selects the 16-token-step mma.sync kernel instead of the 64-token-step
+// tcgen05 kernel (same results within rounding; kept for side-by-side measurement)
+bool use_tc16() {
+    static const bool v = [] {
+        const char *e = std::getenv("KDA_FWD_KERNEL");
+        return e && std::string(e) == "tc16";
+    }();
+    return v;
+}
+
 kda_status run(const kda::FwdArgs &p, kda_dtype dtype, void *stream, Path path) {
     kda_status s = validate(p, dtype);
     if (s != KDA_OK) return s;
     if (p.n_seq == 0) return ok();
     cudaStream_t st = (cudaStream_t)stream;
+    if (path == Path::kAuto && kda::fwd64_supported(p) && !use_tc16())
+        return launched(kda::launch_fwd64(p, st), "tensor-core kernel launch");
     if (path == Path::kAuto && kda::tc_supported(p))
         return launched(kda::launch_tc(p, st), "tensor-core kernel launch");
     return launched(kda::launch_simt(p, st), "SIMT kernel launch");
@@ -94,12 +107,15 @@ kda_status run(const kda::FwdArgs &p, kda_dtype dtype, void *stream, Path path) 
 //
 // The token range is cut into segments; segment i's inputs are copied in on one stream
 // while segment i-1 is computed on the caller's stream and segment i-2's outputs are copied
-// out on a third. Each boundary is placed a multiple of 16 tokens after the start of the
+// out on a third. Each boundary is placed a multiple of 64 tokens after the start of the
 // sequence that holds it, so every piece keeps its sequence's chunk grid, and the state of
 // a sequence cut by a boundary is handed from one piece to the next in fp32 through the
 // workspace: the result is the one the unsegmented call gives, bit for bit.
 
 constexpr int kMaxSegments = 64;
+// Cuts lie a multiple of this many tokens after their sequence's start: the serial step of
+// the tensor-core kernel (64 tokens), itself a multiple of the SIMT kernel's 16-token chunk.
+constexpr int64_t kStepGrid = 64;
 
 // A piece: tokens [t0, t1) holding sequences [n0, n1) -- whole ones, or the part of one
 // sequence that lies in a segment. Its start state is the caller's h0 rows n0.. (zeros
@@ -122,7 +138,7 @@ void plan_pieces(const int32_t *cu, int32_t n_seq, int64_t n_tok, int32_t n_segm
         if (b <= 0 || b >= n_tok) continue;
         // the sequence holding token b: the last n with cu[n] <= b (then cu[n + 1] > b)
         const int32_t n = (int32_t)(std::upper_bound(cu, cu + n_seq + 1, (int32_t)b) - cu) - 1;
-        const int64_t at = cu[n] + (b - cu[n]) / 16 * 16;
+        const int64_t at = cu[n] + (b - cu[n]) / kStepGrid * kStepGrid;
         if (at > bounds.back() && at < n_tok) bounds.push_back(at);
     }
     bounds.push_back(n_tok);
@@ -214,7 +230,10 @@ kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     unsigned int bw = 0;
     e = kda::read_bwd_flags(&bw, reset != 0, (cudaStream_t)stream);
     if (e != cudaSuccess) return launched(e, "reading the device status word");
-    *flags = v | g | bw;
+    unsigned int f64 = 0;
+    e = kda::read_fwd64_flags(&f64, reset != 0, (cudaStream_t)stream);
+    if (e != cudaSuccess) return launched(e, "reading the device status word");
+    *flags = v | g | bw | f64;
     return ok();
 }
 

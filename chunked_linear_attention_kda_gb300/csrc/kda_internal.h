@@ -31,6 +31,11 @@ cudaError_t launch_simt(const FwdArgs &args, cudaStream_t stream);
 // position-pair diagonal tile instead of the dense K~ K^^T, Q~ K^^T products.
 cudaError_t launch_simt_variant(const FwdArgs &args, int gate, bool pair, cudaStream_t stream);
 cudaError_t launch_tc(const FwdArgs &args, cudaStream_t stream);
+// The 64-token-step tcgen05 kernel (kda_fwd64.cu) and its own status word (bit 3: a
+// pipeline wait gave up; reading synchronises stream).
+cudaError_t launch_fwd64(const FwdArgs &args, cudaStream_t stream);
+bool fwd64_supported(const FwdArgs &args);
+cudaError_t read_fwd64_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 
 // True when the tensor-core kernel handles this shape and dtype.
 bool tc_supported(const FwdArgs &args);

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from oracle import recurrence
-from oracle.chunked import chunked_forward, inverse_unit_lower
+from oracle.chunked import block_forward, chunked_forward, inverse_unit_lower
 from tests import oracle_pins as P
 
 GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
@@ -130,6 +130,25 @@ def test_chunked_algebra_equals_recurrence(T, d, gate):
     for inverse in ("solve", "doubling"):
         o, hf = chunked_forward(q, k, v, a, beta, h0, cu, inverse=inverse)
         assert P.rel(o, o_ref) < 1e-12 and P.rel(hf, h_ref) < 1e-12, inverse
+
+
+@pytest.mark.parametrize("T", [1, 16, 17, 63, 64, 65, 130, 200])
+@pytest.mark.parametrize("gate", ["random", "bound", "mixed"])
+def test_block_steps_of_64_tokens_equal_recurrence(T, gate):
+    """Serial steps of 64 tokens assembled from 16-token bounded tiles (cross-tile factors
+    all <= 1) reach the recurrence's result, including partial steps, at the bound."""
+    rng = np.random.default_rng(300 + T)
+    lengths = [T, max(1, T // 3)]
+    q, k, v, a, beta, h0, cu = P._rand(rng, lengths, 2, 8, 6)
+    if gate == "bound":
+        a[:] = np.inf
+    elif gate == "mixed":
+        a[:, 0] = np.inf
+        a[:, 1] = rng.normal(-6.0, 1.0, size=a[:, 1].shape)
+    o_ref, h_ref = recurrence.kda_forward(q, k, v, a, beta, h0, cu)
+    o, hf = block_forward(q, k, v, a, beta, h0, cu)
+    assert P.rel(o, o_ref) < 1e-12 and P.rel(hf, h_ref) < 1e-12
+    assert np.isfinite(o).all() and np.isfinite(hf).all()
 
 
 def test_doubling_inverse_is_exact():

@@ -2,7 +2,7 @@
 ``kda_chunk_fwd_pipeline_plan`` returns (the ones ``kda_chunk_fwd_from_host_pipelined``
 runs) cover every token once and in order, read each sequence's h0 once and write its
 h_final once, hand a cut sequence's state from one segment to the next, cut only on the
-sequence's 16-token chunk grid, and fit the workspace's offset table; executed piece by
+sequence's 64-token step grid, and fit the workspace's offset table; executed piece by
 piece on the fp64 oracle with the device's offset rule and carried states, they reproduce
 one whole-input run bit for bit; plus the pipelined call's host validation (no pointer is
 dereferenced, no kernel launched).
@@ -63,8 +63,8 @@ def check_plan(cu, n_segments):
         else:
             hf_writes[n0:n1] += 1
             assert t1 == cu[n1]
-        # every piece starts on its first sequence's 16-token chunk grid
-        assert (t0 - cu[n0]) % 16 == 0
+        # every piece starts on its first sequence's 64-token step grid
+        assert (t0 - cu[n0]) % 64 == 0
     assert carried is None
     assert (h0_reads == 1).all() and (hf_writes == 1).all()
     # the workspace's offset table holds every piece's n1 - n0 + 1 entries
@@ -80,10 +80,14 @@ def test_one_long_sequence_cuts_into_equal_segments():
 
 
 def test_hand_worked_plan_with_an_empty_sequence():
-    # 40 tokens: sequences of 5, 0 and 35 tokens; 4 segments. Target cuts 10, 20, 30 fall
-    # in the third sequence (start 5) and move down to 5 + 16 j: 5, 5 (dropped), 21.
-    plan = check_plan([0, 5, 5, 40], 4)
-    assert plan == [(0, 5, 0, 2, 0, 0, 0), (5, 21, 2, 3, 0, 1, 1), (21, 40, 2, 3, 1, 0, 2)]
+    # 205 tokens: sequences of 5, 0 and 200 tokens; 4 segments. Target cuts 51, 102, 153
+    # fall in the third sequence (start 5) and move down to 5 + 64 j: 5, 69, 133.
+    plan = check_plan([0, 5, 5, 205], 4)
+    assert plan == [(0, 5, 0, 2, 0, 0, 0), (5, 69, 2, 3, 0, 1, 1), (69, 133, 2, 3, 1, 1, 2),
+                    (133, 205, 2, 3, 1, 0, 3)]
+    # 40 tokens cut into 4: every target lies within 64 tokens of the third sequence's
+    # start, so the only cut left is that start
+    assert check_plan([0, 5, 5, 40], 4) == [(0, 5, 0, 2, 0, 0, 0), (5, 40, 2, 3, 0, 0, 1)]
 
 
 @pytest.mark.parametrize("n_segments", [1, 2, 3, 7, 16, 64])
