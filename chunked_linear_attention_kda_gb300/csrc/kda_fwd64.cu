@@ -136,7 +136,7 @@ constexpr int PR_END = PR_BAR + 24;
 constexpr int PR_KB = PR_TILES + T_KH * TILE_BYTES;
 constexpr int PR_QB = PR_TILES + T_KP * TILE_BYTES;
 static_assert(PR_KB % 1024 == 0 && PR_QB % 1024 == 0 && PR_AT % 1024 == 0, "swizzled tiles");
-constexpr uint32_t kProTmemCols = 128;
+constexpr uint32_t kProTmemCols = 256;  // [W; -Q'] (128) and P' (64)
 static_assert(PR_STG % 1024 == 0 && PR_AT % 16 == 0, "alignment");
 constexpr int SMEM_USED = (PR_END > CH_BAR + NBARS * 8 ? PR_END : CH_BAR + NBARS * 8);
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack of the dynamic base
@@ -494,7 +494,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     auto fetch = [&](int m, int buf) {
         if (m >= nblocks) return;
         const int r0 = t0 + m * BT;
-        if (tid == 0) {
+        if (warp == 15 && lane == 0) {
             mbar_arrive_tx(rawfull, 2 * BT * D * 2 + BT * D * 4);
             tma_load_3d(sbase + PR_Q, tm_q, 0, head, r0, rawfull);
             tma_load_3d(sbase + PR_K, tm_k, 0, head, r0, rawfull);
@@ -603,11 +603,13 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             *reinterpret_cast<uint4 *>(th + cmaj(c, 0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
             *reinterpret_cast<uint4 *>(th + cmaj(c, 8)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
         }
+        if (tid == 0) F64_TRACE(m, 20);
+        if (tid == 511) F64_TRACE(m, 21);
         if (tid == 0) bulk_wait_read0();  // the previous step's copies have read the staging slot
+        if (tid == 0) F64_TRACE(m, 22);
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 10);
-        // ---- P2: decays across tiles; K'B into the slot; cross-tile K' tiles; next fetch
-        fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
+        // ---- P2: decays across tiles; K'B into the slot; cross-tile K' tiles
         {
             float pre = 1.f, post = 1.f;
 #pragma unroll
@@ -650,25 +652,27 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 11);
 
-        // ---- P3: A = strict_lower(beta K~ X^T) and P = lower(Q~ X^T) per tile pair (I, J),
-        //      mma.sync. One warp per (row tile I, A or P, 8-column half): the row operand's
-        //      fragments are loaded once and used for every column tile J <= I, whose
-        //      operand X is K^ on the diagonal and K' scaled by the decays in between off it.
-        {
-            const int Ii = warp >> 2, isP = (warp >> 1) & 1, nh = warp & 1;
-            const uint32_t rowt = tile((isP ? T_QT : T_KT) + Ii);
+        // ---- P3: A = strict_lower(beta K~ X^T) per tile pair (I, J <= I), mma.sync, on all
+        //      16 warps: warp = (row tile I, 8-column half, half of the column tiles J),
+        //      the row operand's fragments loaded once per warp. X is K^ on the diagonal and
+        //      K' scaled by the decays of the tiles in between off it.
+        auto col_tile = [&](int Ii, int Jj) -> uint32_t {
+            int ct;
+            if (Jj == Ii) ct = T_KH + Ii;
+            else if (Ii - Jj == 1) ct = T_KP + Jj;
+            else if (Ii == 2) ct = T_KX + 0;
+            else ct = T_KX + (Jj == 0 ? 1 : 2);
+            return tile(ct);
+        };
+        // rows of tile Ii times X^T for column tiles [j_lo, j_hi], 8-column half nh; the
+        // epilogue gets (Jj, r, j0, v0, v1) for this lane's two adjacent columns
+        auto pair_products = [&](uint32_t rowt, int Ii, int nh, int j_lo, int j_hi, auto &&epi) {
             uint32_t a[D / 16][4];
 #pragma unroll
             for (int kt = 0; kt < D / 16; ++kt)
                 ldsm_x4_t(rowt + cmaj(kt * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), a[kt][0], a[kt][1], a[kt][2], a[kt][3]);
-            const int j0 = nh * 8 + 2 * t4;
-            for (int Jj = 0; Jj <= Ii; ++Jj) {
-                int ct;
-                if (Jj == Ii) ct = T_KH + Ii;
-                else if (Ii - Jj == 1) ct = T_KP + Jj;
-                else if (Ii == 2) ct = T_KX + 0;
-                else ct = T_KX + (Jj == 0 ? 1 : 2);
-                const uint32_t colt = tile(ct);
+            for (int Jj = j_lo; Jj <= j_hi; ++Jj) {
+                const uint32_t colt = col_tile(Ii, Jj);
                 float acc[2][4] = {};
 #pragma unroll
                 for (int kp = 0; kp < D / 32; ++kp) {
@@ -677,58 +681,184 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                     mma16816(acc[0], a[2 * kp], b0, b1);
                     mma16816(acc[1], a[2 * kp + 1], b2, b3);
                 }
-                const bool diag = Jj == Ii;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = g + 8 * hh;
-                    const float v0 = acc[0][2 * hh] + acc[1][2 * hh];
-                    const float v1 = acc[0][2 * hh + 1] + acc[1][2 * hh + 1];
-                    if (!isP) {
-                        const float bb = bet[TL * Ii + r];
-                        float *dst = AT + (TL * Ii + r) * BT + TL * Jj + j0;
-                        *reinterpret_cast<float2 *>(dst) = make_float2((!diag || j0 < r) ? bb * v0 : 0.f,
-                                                                       (!diag || j0 + 1 < r) ? bb * v1 : 0.f);
-                    } else {
-                        *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(BT + TL * Ii + r, TL * Jj + j0)) =
-                            pack_bf16((!diag || j0 <= r) ? v0 : 0.f, (!diag || j0 + 1 <= r) ? v1 : 0.f);
-                    }
-                }
+                for (int hh = 0; hh < 2; ++hh)
+                    epi(Jj, g + 8 * hh, nh * 8 + 2 * t4, acc[0][2 * hh] + acc[1][2 * hh],
+                        acc[0][2 * hh + 1] + acc[1][2 * hh + 1]);
             }
+        };
+        {
+            const int Ii = warp >> 2, nh = (warp >> 1) & 1, hf = warp & 1;
+            const int sp = (Ii + 2) >> 1;
+            const int j_lo = hf ? sp : 0, j_hi = hf ? Ii : sp - 1;
+            if (j_lo <= j_hi)
+                pair_products(tile(T_KT + Ii), Ii, nh, j_lo, j_hi, [&](int Jj, int r, int j0, float v0, float v1) {
+                    const bool diag = Jj == Ii;
+                    const float bb = bet[TL * Ii + r];
+                    *reinterpret_cast<float2 *>(AT + (TL * Ii + r) * BT + TL * Jj + j0) =
+                        make_float2((!diag || j0 < r) ? bb * v0 : 0.f, (!diag || j0 + 1 < r) ? bb * v1 : 0.f);
+                });
         }
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 12);
-        // ---- P4: T = (I + A)^-1, A strictly lower, in 16 x 16 tiles. L = the diagonal
-        //      tiles of I + A, N = the rest, M = L^-1 N (M_IJ = T_II A_IJ, I > J; nilpotent,
-        //      M^4 = 0), so T = (I + M)^-1 L^-1 = (I - M)(I + M^2) L^-1. Diagonal tiles T_II:
-        //      fp32 forward substitution, one column per thread. Products of tiles: tensor
-        //      cores, operands rounded to bf16. TB = T diag(beta) goes to
-        //      rows 0..63 of B1 as each tile is done (the tiles above the diagonal stay 0).
-        //      Meanwhile the other threads form K~B = K~^I Gamma_I and Q~B = Q~^I Gamma_I,
-        //      [c][64 t] with the 128-byte swizzle, over the K^ / K' tiles (no longer read).
-        if (tid < 64) {
-            const int Id = tid >> 4, j = tid & 15;
-            const float *Ar = AT + (TL * Id) * BT + TL * Id;
-            float x[TL];
+        // ---- P4, two groups at once.
+        //  Warps 0-5: T = (I + A)^-1, A strictly lower, in 16 x 16 tiles. L = the diagonal
+        //   tiles of I + A, N = the rest, M = L^-1 N (M_IJ = T_II A_IJ, I > J; nilpotent,
+        //   M^4 = 0), so T = (I + M)^-1 L^-1 = (I - M)(I + M^2) L^-1. Diagonal tiles T_II:
+        //   fp32 forward substitution, one column per thread. Products of tiles: tensor
+        //   cores, operands rounded to bf16. TB = T diag(beta) goes to rows 0..63 of B1 as
+        //   each tile is done (the tiles above the diagonal stay 0).
+        //  Warps 6-15: the next step's raw tiles requested; P = lower(Q~ X^T) into rows
+        //   64..127 of B1 (zero above the diagonal tiles); then K~B = K~^I Gamma_I and
+        //   Q~B = Q~^I Gamma_I ([c][64 t], 128-byte swizzle) over the K^ / K' tiles.
+        if (warp < 6) {
+            constexpr int kSolveThreads = 192;
+            if (tid < 64) {
+                const int Id = tid >> 4, j = tid & 15;
+                const float *Ar = AT + (TL * Id) * BT + TL * Id;
+                float x[TL];
 #pragma unroll
-            for (int r = 0; r < TL; ++r) {
-                float a0 = r == j ? 1.f : 0.f, a1 = 0.f;
+                for (int r = 0; r < TL; ++r) {
+                    // row r of A_II as four 16-byte loads, independent of the solve so far
+                    float ar[TL];
 #pragma unroll
-                for (int i = 0; i < r; i += 2) {
-                    a0 = fmaf(-Ar[r * BT + i], x[i], a0);
-                    if (i + 1 < r) a1 = fmaf(-Ar[r * BT + i + 1], x[i + 1], a1);
+                    for (int q = 0; q < (r + 3) / 4; ++q) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(Ar + r * BT + 4 * q);
+                        ar[4 * q] = v4.x; ar[4 * q + 1] = v4.y; ar[4 * q + 2] = v4.z; ar[4 * q + 3] = v4.w;
+                    }
+                    float a0 = r == j ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < r; i += 2) {
+                        a0 = fmaf(-ar[i], x[i], a0);
+                        if (i + 1 < r) a1 = fmaf(-ar[i + 1], x[i + 1], a1);
+                    }
+                    x[r] = a0 + a1;
                 }
-                x[r] = a0 + a1;
-            }
-            const float bj = bet[TL * Id + j];
-            __nv_bfloat16 *b1 = reinterpret_cast<__nv_bfloat16 *>(sm + PR_STG + SL_B1);
+                const float bj = bet[TL * Id + j];
 #pragma unroll
-            for (int r = 0; r < TL; ++r) {
-                TD[(Id * TL + r) * TL + j] = x[r];
-                *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<unsigned char *>(b1) +
-                                                   sw128(TL * Id + r, TL * Id + j)) = __float2bfloat16_rn(x[r] * bj);
+                for (int r = 0; r < TL; ++r) {
+                    TD[(Id * TL + r) * TL + j] = x[r];
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + PR_STG + SL_B1 + sw128(TL * Id + r, TL * Id + j)) =
+                        __float2bfloat16_rn(x[r] * bj);
+                }
+            }
+            named_sync(2, kSolveThreads);
+            if (tid == 0) F64_TRACE(m, 16);
+            {   // M_IJ = T_II A_IJ for the six pairs I > J (one warp each)
+                const int Ir = kOffI[warp], Jc = kOffJ[warp];
+                float acc[2][4] = {};
+                mma16_f32(acc, TD + Ir * 256, TL, AT + (TL * Ir) * BT + TL * Jc, BT, g, t4);
+                store16(MM + warp * 256, acc, 1.f, g, t4);
+            }
+            named_sync(2, kSolveThreads);
+            if (tid == 0) F64_TRACE(m, 17);
+            // M^2: (2,0) = M21 M10, (3,1) = M32 M21, (3,0) = M31 M10 + M32 M20; meanwhile warps
+            // 3-5 write the constant [0; -I] operand tile over A (no longer read)
+            if (warp < 3) {
+                float acc[2][4] = {};
+                if (warp == 0) mma16_f32(acc, MM + 1 * 256, TL, MM + 0 * 256, TL, g, t4);
+                if (warp == 1) mma16_f32(acc, MM + 2 * 256, TL, MM + 1 * 256, TL, g, t4);
+                if (warp == 2) {
+                    mma16_f32(acc, MM + 4 * 256, TL, MM + 0 * 256, TL, g, t4);
+                    mma16_f32(acc, MM + 2 * 256, TL, MM + 3 * 256, TL, g, t4);
+                }
+                store16(M2 + warp * 256, acc, 1.f, g, t4);
+            } else {
+                // 128 rows x 64 k, row n >= 64 holds -1 at k = n - 64; 32 bytes per slot
+                for (int e = tid - 96; e < 512; e += 96) {
+                    const int n = e >> 2, q0 = 2 * (e & 3);
+#pragma unroll
+                    for (int q = q0; q < q0 + 2; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int k0 = 8 * q + 2 * h;
+                            w[h] = pack_bf16(n - 64 == k0 ? -1.f : 0.f, n - 64 == k0 + 1 ? -1.f : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(sm + PR_AT + sw128(n, 8 * q)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            named_sync(2, kSolveThreads);
+            if (tid == 0) F64_TRACE(m, 18);
+            {   // T_IJ = [-(M)_IJ + (M^2)_IJ - (M^3)_IJ] T_JJ, M^3 only at (3,0) = M32 (M^2)_20;
+                // TB_IJ = T_IJ diag(beta_J) straight into B1
+                const int Ir = kOffI[warp], Jc = kOffJ[warp];
+                float *ls = XS + warp * 256;  // this warp's left operand
+                const int q2 = (Ir == 2 && Jc == 0) ? 0 : (Ir == 3 && Jc == 1) ? 1 : (Ir == 3 && Jc == 0) ? 2 : -1;
+                float c3[2][4] = {};
+                if (q2 == 2) mma16_f32(c3, MM + 2 * 256, TL, M2 + 0 * 256, TL, g, t4);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = g + 8 * h, col = 8 * nt + 2 * t4;
+                        float2 v2 = *reinterpret_cast<const float2 *>(MM + warp * 256 + row * TL + col);
+                        v2.x = -v2.x;
+                        v2.y = -v2.y;
+                        if (q2 >= 0) {
+                            const float2 w2 = *reinterpret_cast<const float2 *>(M2 + q2 * 256 + row * TL + col);
+                            v2.x += w2.x;
+                            v2.y += w2.y;
+                        }
+                        v2.x -= c3[nt][2 * h];
+                        v2.y -= c3[nt][2 * h + 1];
+                        *reinterpret_cast<float2 *>(ls + row * TL + col) = v2;
+                    }
+                __syncwarp();
+                float acc[2][4] = {};
+                mma16_f32(acc, ls, TL, TD + Jc * 256, TL, g, t4);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = TL * Jc + 8 * nt + 2 * t4;
+                    const float b0 = bet[col], b1 = bet[col + 1];
+                    *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(TL * Ir + g, col)) =
+                        pack_bf16(acc[nt][0] * b0, acc[nt][1] * b1);
+                    *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(TL * Ir + g + 8, col)) =
+                        pack_bf16(acc[nt][2] * b0, acc[nt][3] * b1);
+                }
             }
         } else {
-            for (int e = tid - 64; e < NT * D; e += kThreads - 64) {
+            constexpr int kAuxThreads = 320;
+            if (warp == 15) fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
+            // P in 14 units of at most two column tiles on warps 6-15 (unit = row tile I,
+            // 8-column half, part of the column tiles); warps 6-11 take one two-tile unit,
+            // warps 12-15 two one-tile units
+            auto p_unit = [&](int Ii, int nh, int j_lo, int j_hi) {
+                pair_products(tile(T_QT + Ii), Ii, nh, j_lo, j_hi, [&](int Jj, int r, int j0, float v0, float v1) {
+                    const bool diag = Jj == Ii;
+                    *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(BT + TL * Ii + r, TL * Jj + j0)) =
+                        pack_bf16((!diag || j0 <= r) ? v0 : 0.f, (!diag || j0 + 1 <= r) ? v1 : 0.f);
+                });
+            };
+            const int w6 = warp - 6;
+            if (w6 < 6) {  // (3, nh, J 0-1), (3, nh, J 2-3), (2, nh, J 0-1)
+                const int nh = w6 & 1, u = w6 >> 1;
+                if (u == 0) p_unit(3, nh, 0, 1);
+                else if (u == 1) p_unit(3, nh, 2, 3);
+                else p_unit(2, nh, 0, 1);
+            } else {       // (2, nh, J 2) + (0, nh, J 0), (1, nh, J 0) + (1, nh, J 1)
+                const int nh = w6 & 1, u = (w6 - 6) >> 1;
+                if (u == 0) {
+                    p_unit(2, nh, 2, 2);
+                    p_unit(0, nh, 0, 0);
+                } else {
+                    p_unit(1, nh, 0, 0);
+                    p_unit(1, nh, 1, 1);
+                }
+            }
+            // tiles above the diagonal: zero (rows of tile I = w6 >> 1 for w6 < 8, both halves)
+            if (w6 < 8) {
+                const int Ii = w6 >> 1, nh = w6 & 1;
+                for (int Jj = Ii + 1; Jj < NT; ++Jj)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 +
+                                                      sw128(BT + TL * Ii + g + 8 * hh, TL * Jj + nh * 8 + 2 * t4)) = 0u;
+            }
+            named_sync(3, kAuxThreads);  // every read of the K^ / K' tiles is done
+            // K~B and Q~B over the K^ and K' tiles
+            for (int e = tid - 192; e < NT * D; e += kAuxThreads) {
                 const int cc = e & (D - 1), Ie = e >> 7;
                 const float gpre = PRE[Ie * D + cc];
 #pragma unroll
@@ -750,111 +880,42 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                 }
             }
         }
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 16);
-        // M_IJ = T_II A_IJ for the six pairs I > J (one warp each)
-        if (warp < 6) {
-            const int Ir = kOffI[warp], Jc = kOffJ[warp];
-            float acc[2][4] = {};
-            mma16_f32(acc, TD + Ir * 256, TL, AT + (TL * Ir) * BT + TL * Jc, BT, g, t4);
-            store16(MM + warp * 256, acc, 1.f, g, t4);
-        }
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 17);
-        // M^2: (2,0) = M21 M10, (3,1) = M32 M21, (3,0) = M31 M10 + M32 M20; meanwhile the
-        // other warps write the constant [0; -I] operand tile over A (no longer read)
-        if (warp < 3) {
-            float acc[2][4] = {};
-            if (warp == 0) mma16_f32(acc, MM + 1 * 256, TL, MM + 0 * 256, TL, g, t4);
-            if (warp == 1) mma16_f32(acc, MM + 2 * 256, TL, MM + 1 * 256, TL, g, t4);
-            if (warp == 2) {
-                mma16_f32(acc, MM + 4 * 256, TL, MM + 0 * 256, TL, g, t4);
-                mma16_f32(acc, MM + 2 * 256, TL, MM + 3 * 256, TL, g, t4);
-            }
-            store16(M2 + warp * 256, acc, 1.f, g, t4);
-        } else {
-            // 128 rows x 64 k, row n >= 64 holds -1 at k = n - 64; 32 bytes per slot
-            for (int e = tid - 96; e < 512; e += kThreads - 96) {
-                const int n = e >> 2, q0 = 2 * (e & 3);
-#pragma unroll
-                for (int q = q0; q < q0 + 2; ++q) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int k0 = 8 * q + 2 * h;
-                        w[h] = pack_bf16(n - 64 == k0 ? -1.f : 0.f, n - 64 == k0 + 1 ? -1.f : 0.f);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + PR_AT + sw128(n, 8 * q)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 18);
-        // T_IJ = [-(M)_IJ + (M^2)_IJ - (M^3)_IJ] T_JJ, with M^3 only at (3,0) = M32 (M^2)_20;
-        // TB_IJ = T_IJ diag(beta_J) straight into B1
-        if (warp < 6) {
-            const int Ir = kOffI[warp], Jc = kOffJ[warp];
-            float *ls = XS + warp * 256;  // this warp's left operand
-            const int q2 = (Ir == 2 && Jc == 0) ? 0 : (Ir == 3 && Jc == 1) ? 1 : (Ir == 3 && Jc == 0) ? 2 : -1;
-            float c3[2][4] = {};
-            if (q2 == 2) mma16_f32(c3, MM + 2 * 256, TL, M2 + 0 * 256, TL, g, t4);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int row = g + 8 * h, col = 8 * nt + 2 * t4;
-                    float2 v2 = *reinterpret_cast<const float2 *>(MM + warp * 256 + row * TL + col);
-                    v2.x = -v2.x;
-                    v2.y = -v2.y;
-                    if (q2 >= 0) {
-                        const float2 w2 = *reinterpret_cast<const float2 *>(M2 + q2 * 256 + row * TL + col);
-                        v2.x += w2.x;
-                        v2.y += w2.y;
-                    }
-                    v2.x -= c3[nt][2 * h];
-                    v2.y -= c3[nt][2 * h + 1];
-                    *reinterpret_cast<float2 *>(ls + row * TL + col) = v2;
-                }
-            __syncwarp();
-            float acc[2][4] = {};
-            mma16_f32(acc, ls, TL, TD + Jc * 256, TL, g, t4);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = TL * Jc + 8 * nt + 2 * t4;
-                const float b0 = bet[col], b1 = bet[col + 1];
-                *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(TL * Ir + g, col)) =
-                    pack_bf16(acc[nt][0] * b0, acc[nt][1] * b1);
-                *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(TL * Ir + g + 8, col)) =
-                    pack_bf16(acc[nt][2] * b0, acc[nt][3] * b1);
-            }
-        }
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 13);
-        // ---- P5: P' = P TB (rows 64..127 of B1), tile row Ir, column tile Jp per warp
-        {
-            const int Ir = warp >> 2, Jp = warp & 3;
-            float acc[2][4] = {};
-            if (Jp <= Ir) {
-                for (int J = Jp; J <= Ir; ++J) {
-                    uint32_t a[4], b00, b01, b10, b11;
-                    ldsm_x4(stg + SL_B1 + sw128(BT + TL * Ir + (lane & 15), TL * J + 8 * (lane >> 4)), a[0], a[1], a[2], a[3]);
-                    ldsm_x4_t(stg + SL_B1 + sw128(TL * J + r8 + 8 * (i8 & 1), TL * Jp + 8 * (i8 >> 1)), b00, b01, b10, b11);
-                    mma16816(acc[0], a, b00, b01);
-                    mma16816(acc[1], a, b10, b11);
-                }
-            }
-            __syncthreads();  // every read of P is done
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int col = TL * Jp + 8 * h2 + 2 * t4;
-                *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(BT + TL * Ir + g, col)) =
-                    pack_bf16(acc[h2][0], acc[h2][1]);
-                *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(BT + TL * Ir + g + 8, col)) =
-                    pack_bf16(acc[h2][2], acc[h2][3]);
-            }
-        }
         fence_proxy_async();  // B1, K~B, Q~B and [0; -I]: generic writes -> tensor-core reads
         tc_fence_before();
+        __syncthreads();
+        if (tid == 0) F64_TRACE(m, 13);
+        // ---- P5: P' = P TB on this CTA's tensor core: A = B1 ([TB; P], K = 64 tokens),
+        //      B = TB read MN-major from the same rows 0..63; rows 64..127 of the result
+        //      go back into rows 64..127 of B1
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t da = sdesc_sw128(stg + SL_B1, 16, 1024), db = sdesc_sw128(stg + SL_B1, 8192, 1024);
+            const uint32_t idp = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem + 128u, da + 2 * kk2, db + 128 * kk2, idp, kk2 > 0);
+            umma_commit(mmabar);
+        }
+        if ((warp & 3) >= 2 && warp < 8) {  // lane quarters 2 and 3: rows 64..127
+            const bool got = wait_bar(mmabar, 0);
+            if (__all_sync(0xffffffffu, got)) {
+                tc_fence_after();
+                const int n = ((warp & 3) << 5) + lane, ch = warp >> 2;  // row, 32-column half
+                uint32_t r[32];
+                tmem_ld32(ptmem + 128u + ((uint32_t)((warp & 3) * 32) << 16) + 32u * ch, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        w[h] = pack_bf16(__uint_as_float(r[8 * c8 + 2 * h]), __uint_as_float(r[8 * c8 + 2 * h + 1]));
+                    *reinterpret_cast<uint4 *>(sm + PR_STG + SL_B1 + sw128(n, 32 * ch + 8 * c8)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            tc_fence_before();
+        }
+        fence_proxy_async();
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 14);
         // ---- P6: [W; -Q'] = [TB | 0; P' | -I] [K~B; Q~B] (M = 128, N = 128 channels, K = 128)
@@ -871,7 +932,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             umma_commit(mmabar);
         }
         if (warp < 8) {
-            const bool got = wait_bar(mmabar, k & 1);
+            const bool got = wait_bar(mmabar, 1);
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
                 const int n = ((warp & 3) << 5) + lane, ch = warp >> 2;  // row, 64-channel half
@@ -910,7 +971,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     if (tid == 0) {
         bulk_wait_read0();  // no copy may still read this CTA's memory at exit
         umma_commit(mmabar);  // and every product has completed before the tensor memory goes
-        wait_bar(mmabar, (uint32_t)k & 1);
+        wait_bar(mmabar, 0);    // two commits per step: this is an even-numbered phase
     }
     if (warp == 15) cp_async_wait0();
     tc_fence_before();
