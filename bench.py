@@ -21,7 +21,16 @@ Reported alongside the device-timed value:
   roofline     algorithmic bytes per launch / CUDA-event launch time against the
                measured HBM copy bandwidth (MEASURED_PEAKS.json);
   cpu_baseline the fp64 oracle on the host cores on a bounded sample (rank 0, N = 1);
-  clocks       nvidia-smi samples taken during the timed region.
+  parity       the timed run's outputs against the oracle on that sample, over the whole
+               sample and for the worst (sequence, head) pair (final states too when
+               the sample covers the whole sequence);
+  diagnostics  non-finite outputs and states (the library's device counter) and the
+               Frobenius norms of the final states;
+  clocks       nvidia-smi samples taken during the timed region;
+  workloads    with the default workload, the same timing, roofline, diagnostics and
+               a prefix parity sample for the 256K-token context (B=1, H=32) and the
+               packed variable-length workload (16 sequences of 4K-131K tokens plus one
+               of 1M, H=16); the headline keys stay those of the 64K workload.
 ``--impl reference`` times the oracle alone (the reference arm of this build).
 
 ``--op decode`` measures the recurrent decode step instead (``kda_decode_step``: B = 256
@@ -55,16 +64,19 @@ METRIC = "KDA chunked-forward tokens/s (1 GB300) and % of tensor-core/HBM roofli
 DECODE_METRIC = "KDA recurrent decode tokens/s (1 GB300) and % of HBM roofline"
 DECODE_B, DECODE_H, DECODE_D = 256, 32, 128
 UNIT = "tokens/s"
-# the bench workload's kernel (bf16, d = 128 always takes the tensor-core kernel)
-KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_tc.cu"]
+# the bench workload's kernel (bf16, d = 128 takes the 64-token tensor-core kernel)
+KERNEL_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_fwd64.cu",
+                  "chunked_linear_attention_kda_gb300/csrc/kda_ptx.h"]
+# workloads timed after the headline one and reported under "workloads"
+EXTRA_WORKLOADS = {5: 16384, 4: 4096}   # workload index -> oracle prefix tokens
 DECODE_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_decode.cu"]
 BACKWARD_SOURCES = ["chunked_linear_attention_kda_gb300/csrc/kda_bwd.cu"]
 BACKWARD_METRIC = "KDA chunked-backward tokens/s (1 GB300) and % of HBM roofline (dominant kernel)"
 BACKWARD_KERNELS = ["prep", "forward_pass", "reverse_pass", "local_gradients"]
 # the tensor-core path runs both serial passes in one launch
 BACKWARD_KERNELS_TC = ["prep", "serial_passes", "local_gradients"]
-# fp32 FMA peak of the SIMT backward: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# fp32 lanes per SM on sm_100-class parts (4 sub-partitions x 32)
+FP32_LANES_PER_SM = 128
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
 
 
@@ -147,6 +159,18 @@ def recorded_traffic(workload: str, sources=None):
             except (KeyError, ValueError):
                 return None
     return None
+
+
+def fp32_alu_peak(dev, sm_max_mhz):
+    """fp32 FMA peak of this device: SM count (queried) x 128 fp32 lanes x 2 flops x the
+    maximum SM clock nvidia-smi reports during the run (2070 MHz if it reported none)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = float(sm_max_mhz) if sm_max_mhz else 2070.0
+    tf = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    src = (f"derived: {sms} SMs (device query) x {FP32_LANES_PER_SM} fp32 lanes x 2 flops x "
+           f"{mhz:.0f} MHz ({'nvidia-smi clocks.max.sm' if sm_max_mhz else 'nominal maximum'})")
+    return tf, src
 
 
 def measured_peaks():
@@ -252,10 +276,11 @@ def max_over_ranks(x: float, on: bool, device) -> float:
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_sample(x, max_tokens: int, heads=None, threads=None):
+def oracle_sample(x, max_tokens: int, heads=None, threads=None, want_state=False):
     """The oracle on the first ``max_tokens`` tokens of every sequence (and the given
     heads), on ``threads`` host threads (default: all). Returns (seconds, token-heads
-    processed, threads, the oracle's outputs of the sample)."""
+    processed, threads, the oracle's outputs of the sample); with ``want_state`` the
+    oracle's final states are appended."""
     import kda_inputs as K
     from oracle import recurrence
     px = K.prefix(x, max_tokens)
@@ -266,28 +291,62 @@ def oracle_sample(x, max_tokens: int, heads=None, threads=None):
     threads = threads or recurrence.default_threads()
     recurrence.build()
     t0 = time.perf_counter()
-    o_ref, _ = recurrence.kda_forward(*args, px.cu_host, threads=threads, want_state=False)
+    o_ref, h_ref = recurrence.kda_forward(*args, px.cu_host, threads=threads,
+                                          want_state=want_state)
     dt = time.perf_counter() - t0
+    if want_state:
+        return dt, px.n_tok * px.n_heads, threads, o_ref, h_ref
     return dt, px.n_tok * px.n_heads, threads, o_ref
 
 
-def prefix_rel_l2(x, out, tokens: int, o_ref) -> float:
+def prefix_rel_l2(x, out, tokens: int, o_ref):
     """rel-L2 of the GPU output ``out`` (the whole workload) against the oracle's output
     ``o_ref`` on the first ``tokens`` tokens of every sequence (by causality those rows do
-    not depend on anything after them)."""
+    not depend on anything after them): (over the whole sample, worst over (sequence,
+    head) pairs with at least 16 tokens in the sample)."""
+    import numpy as np
     num = den = 0.0
+    worst = 0.0
     row = 0
     for i in range(x.n_seq):
         s0 = x.cu_host[i]
         n = min(x.cu_host[i + 1] - s0, tokens)
+        hn = np.zeros(x.n_heads)
+        hd = np.zeros(x.n_heads)
         for c in range(0, n, 8192):
             m = min(8192, n - c)
             g = out[s0 + c:s0 + c + m].detach().to("cpu", torch_float64()).numpy()
             r = o_ref[row + c:row + c + m]
-            num += float(((g - r) ** 2).sum())
-            den += float((r ** 2).sum())
+            hn += ((g - r) ** 2).sum(axis=(0, 2))
+            hd += (r ** 2).sum(axis=(0, 2))
+        num += float(hn.sum())
+        den += float(hd.sum())
+        if n >= 16:
+            worst = max(worst, float(np.max(np.sqrt(hn / np.maximum(hd, 1e-300)))))
         row += n
-    return (num / den) ** 0.5 if den > 0 else num ** 0.5
+    return (num / den) ** 0.5 if den > 0 else num ** 0.5, worst
+
+
+def state_rel_l2(hf, h_ref):
+    """(whole-tensor, worst over (sequence, head)) rel-L2 of final states."""
+    import numpy as np
+    g = hf.detach().to("cpu", torch_float64()).numpy()
+    r = np.asarray(h_ref, dtype=np.float64)
+    num = ((g - r) ** 2).sum(axis=(2, 3))
+    den = (r ** 2).sum(axis=(2, 3))
+    whole = float(np.sqrt(num.sum() / max(den.sum(), 1e-300)))
+    return whole, float(np.max(np.sqrt(num / np.maximum(den, 1e-300))))
+
+
+def output_diagnostics(kda, out, hf):
+    """Non-finite count over the outputs and final states (the library's counter) and the
+    Frobenius norms of the final states, taken outside the timed region."""
+    import torch
+    nrm = torch.linalg.vector_norm(hf.float(), dim=(2, 3))
+    return {"nonfinite": int(kda.count_nonfinite(out, hf)),
+            "h_final_fro": round(float(torch.linalg.vector_norm(hf.float())), 4),
+            "h_final_fro_max_per_head": round(float(nrm.max()), 4),
+            "h_final_fro_min_per_head": round(float(nrm.min()), 4)}
 
 
 def torch_float64():
@@ -295,15 +354,17 @@ def torch_float64():
     return torch.float64
 
 
-def cpu_baseline(x, budget_s: float = 15.0, out=None):
+def cpu_baseline(x, budget_s: float = 15.0, out=None, hf=None):
     """Time the oracle on a bounded prefix sample, growing it until it takes a few
     seconds, scaled to the workload's tokens/s (a token counts all H heads). With the
     GPU's output ``out`` of the same inputs, also its rel-L2 against the oracle on that
-    sample (key ``parity``)."""
+    sample (key ``parity``), and with ``hf`` that of the final states when the sample
+    covers every sequence whole."""
     tokens = 256
     while True:
-        dt, th, threads, o_ref = oracle_sample(x, tokens)
-        if dt > budget_s / 4 or tokens >= max(x.lengths()):
+        full = tokens >= max(x.lengths())
+        dt, th, threads, o_ref, h_ref = oracle_sample(x, tokens, want_state=True)
+        if dt > budget_s / 4 or full:
             break
         tokens = min(tokens * 4, max(x.lengths()))
     value = th / x.n_heads / dt
@@ -317,11 +378,16 @@ def cpu_baseline(x, budget_s: float = 15.0, out=None):
     parity = None
     if out is not None:
         import torch
-        parity = {"rel_l2_out": prefix_rel_l2(x, out, tokens, o_ref),
+        whole, worst = prefix_rel_l2(x, out, tokens, o_ref)
+        parity = {"rel_l2_out": whole, "rel_l2_out_max_per_head": worst,
                   "bar": 1e-2 if x.dtype == torch.bfloat16 else 1e-4,
                   "sample": f"outputs of the first {tokens} tokens of every sequence, all "
-                            f"{x.n_heads} heads, of the timed run against the fp64 oracle"}
-    del o_ref
+                            f"{x.n_heads} heads, of the timed run against the fp64 oracle; "
+                            "max_per_head is the worst (sequence, head) pair"}
+        if full and hf is not None:
+            parity["rel_l2_h_final"], parity["rel_l2_h_final_max_per_head"] = \
+                state_rel_l2(hf, h_ref)
+    del o_ref, h_ref
     return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds": dt, "parity": parity,
             "sample": f"fp64 token-by-token oracle on the first {tokens} tokens of every "
@@ -335,6 +401,94 @@ def cpu_baseline(x, budget_s: float = 15.0, out=None):
 
 # ------------------------------------------------------------------ our arm
 
+def timed_forward(kda, x, dev, stream, steps, warmup, on):
+    """Warm up, then time ``steps`` forward calls over ``x`` (inputs resident) with CUDA
+    events on the launching stream, bracketed by a barrier and a synchronise; nvidia-smi
+    clocks sampled meanwhile. Returns (out, h_final, total ms (max over ranks), per-call
+    ms, kernel launches, clocks)."""
+    import torch
+    out = torch.empty((x.n_tok, x.n_heads, x.d_v), dtype=x.dtype, device=dev)
+    hf = torch.empty((x.n_seq, x.n_heads, x.d_k, x.d_v), dtype=torch.float32, device=dev)
+
+    def step():
+        kda.chunk_fwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, out=out, h_final=hf)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n0 = kda.kernel_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(on)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(on)
+    launches = kda.kernel_launch_count() - n0
+    total_ms = max_over_ranks(t_all0.elapsed_time(t_all1), on, dev)
+    per_launch_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    return out, hf, total_ms, per_launch_ms, launches, clk.summary()
+
+
+def hbm_roofline(x, per_launch_ms, launches, steps, peaks):
+    """The forward kernel's roofline entry: algorithmic bytes per launch over the mean
+    event-timed launch duration, against the measured HBM copy bandwidth."""
+    bytes_launch = algorithmic_bytes(x)
+    flops_launch = algorithmic_flops(x)
+    launches_per_step = max(1, launches // max(1, steps))
+    mean_launch_s = statistics.mean(per_launch_ms) * 1e-3 / launches_per_step
+    achieved_gbs = bytes_launch / launches_per_step / mean_launch_s / 1e9
+    return {"bound": "hbm", "achieved": round(achieved_gbs, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+            "traffic": recorded_traffic(x.name),
+            "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)",
+            "algorithmic_bytes_per_launch": bytes_launch,
+            "tensor_tflops": round(flops_launch / mean_launch_s / 1e12, 1),
+            "tensor_frac_of_bf16_peak": round(flops_launch / mean_launch_s / 1e12 /
+                                              peaks["bf16_tflops"], 4)}
+
+
+def extra_workload(kda, K, index, prefix, dev, stream, args, on, rank, world):
+    """One of the workloads reported beside the headline: the same timing, roofline and
+    output diagnostics, and (rank 0, one GPU) the oracle on the first ``prefix`` tokens of
+    every sequence, all heads, with the worst (sequence, head) rel-L2."""
+    import torch
+    x = K.make_workload(index, dev, seed=K.SEED_BASE + index + 7919 * rank)
+    out, hf, total_ms, per_ms, launches, clocks = timed_forward(
+        kda, x, dev, stream, args.steps, args.warmup, on)
+    peaks = measured_peaks()
+    entry = {"value": round(x.n_tok * world * args.steps / (total_ms * 1e-3), 1), "unit": UNIT,
+             "ms_per_step": round(total_ms / args.steps, 4), "steps": args.steps,
+             "tokens_per_gpu": x.n_tok, "heads": x.n_heads, "n_seq": x.n_seq,
+             "gpu_launches": int(launches),
+             "roofline": hbm_roofline(x, per_ms, launches, args.steps, peaks),
+             "clocks": clocks, "diagnostics": output_diagnostics(kda, out, hf)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        _, _, threads, o_ref = oracle_sample(x, prefix)
+        whole, worst = prefix_rel_l2(x, out, prefix, o_ref)
+        entry["parity"] = {"rel_l2_out": whole, "rel_l2_out_max_per_head": worst,
+                           "bar": 1e-2 if x.dtype == torch.bfloat16 else 1e-4,
+                           "oracle_seconds": round(time.perf_counter() - t0, 2),
+                           "sample": f"outputs of the first {prefix} tokens of every sequence, "
+                                     f"all {x.n_heads} heads, of the timed run against the "
+                                     f"fp64 oracle ({threads} host threads); max_per_head is "
+                                     "the worst (sequence, head) pair"}
+        del o_ref
+    del out, hf, x
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
     import chunked_linear_attention_kda_gb300 as kda
@@ -347,60 +501,17 @@ def run_ours(args):
     kda.load_library(build_if_missing=True)
 
     x = K.make_workload(args.workload, dev, seed=K.SEED_BASE + args.workload + 7919 * rank)
-    out = torch.empty((x.n_tok, x.n_heads, x.d_v), dtype=x.dtype, device=dev)
-    hf = torch.empty((x.n_seq, x.n_heads, x.d_k, x.d_v), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        kda.chunk_fwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, out=out, h_final=hf)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
-    n0 = kda.kernel_launch_count()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(on)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        t_all0 = torch.cuda.Event(enable_timing=True)
-        t_all1 = torch.cuda.Event(enable_timing=True)
-        t_all0.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        t_all1.record(stream)
-        torch.cuda.synchronize(dev)
-    barrier(on)
-    launches = kda.kernel_launch_count() - n0
-    total_ms = t_all0.elapsed_time(t_all1)
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(total_ms, on, dev)
+    out, hf, total_ms, per_launch_ms, launches, clocks = timed_forward(
+        kda, x, dev, stream, args.steps, args.warmup, on)
     ms_per_step = total_ms / args.steps
     tokens_all = x.n_tok * world
     value = tokens_all * args.steps / (total_ms * 1e-3)
-
-    # roofline for the (single) kernel of a step
-    peaks = measured_peaks()
-    bytes_launch = algorithmic_bytes(x)
-    flops_launch = algorithmic_flops(x)
-    launches_per_step = max(1, launches // max(1, args.steps))
-    mean_launch_s = statistics.mean(per_launch_ms) * 1e-3 / launches_per_step
-    achieved_gbs = bytes_launch / launches_per_step / mean_launch_s / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                "traffic": recorded_traffic(x.name),
-                "peak_source": f"{peaks['source']} (HBM copy bandwidth, MEASURED_PEAKS.json)",
-                "algorithmic_bytes_per_launch": bytes_launch,
-                "tensor_tflops": round(flops_launch / mean_launch_s / 1e12, 1),
-                "tensor_frac_of_bf16_peak": round(flops_launch / mean_launch_s / 1e12 /
-                                                  peaks["bf16_tflops"], 4)}
+    roofline = hbm_roofline(x, per_launch_ms, launches, args.steps, measured_peaks())
+    diagnostics = output_diagnostics(kda, out, hf)
 
     # end-to-end through the host-buffer entry point
-    e2e = measure_e2e(x, dev, stream, max(1, min(args.steps, 5)), kda)
+    e2e = measure_e2e(x, dev, stream, max(1, min(args.steps, 10)), kda)
     e2e["value"] = e2e["value"] * world
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -409,18 +520,27 @@ def run_ours(args):
             "dtype": "bf16" if x.dtype == torch.bfloat16 else "f32",
             "data": "synthetic",
             "config": {"workload": x.name, "tokens_per_gpu": x.n_tok, "heads": x.n_heads,
-                       "d_k": x.d_k, "d_v": x.d_v, "chunk": 16, "n_seq": x.n_seq,
-                       "global_batch_tokens": tokens_all,
+                       "d_k": x.d_k, "d_v": x.d_v, "chunk": 16, "serial_step_tokens": 64,
+                       "n_seq": x.n_seq, "global_batch_tokens": tokens_all,
                        "parallelism": f"independent replicas x{world}" if world > 1 else
                        "single GPU",
                        "l2": "inputs (%.2f GB) exceed the 129 MB L2; no flush between steps"
-                             % (bytes_launch / 1e9)},
+                             % (algorithmic_bytes(x) / 1e9)},
             "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": clk.summary(), "kernel_digest": kernel_source_digest()}
+            "clocks": clocks, "kernel_digest": kernel_source_digest(),
+            "diagnostics": diagnostics}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(x, out=out)
+        cb = cpu_baseline(x, out=out, hf=hf)
         line["parity"] = cb.pop("parity")
         line["cpu_baseline"] = cb
+    del out, hf, x
+    torch.cuda.empty_cache()
+    if args.workload == 3 and not args.no_extra_workloads:
+        line["workloads"] = {}
+        for index, prefix in EXTRA_WORKLOADS.items():
+            name = K.WORKLOADS[index]
+            line["workloads"][name] = extra_workload(kda, K, index, prefix, dev, stream, args,
+                                                     on, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if on:
@@ -698,10 +818,11 @@ def run_backward(args):
     else:  # the fp32 FMA kernels
         flops = 2 * algorithmic_flops(x)   # a gradient product for each operand of each product
         achieved = flops / mean_s / 1e12
-        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_ALU_TFLOPS, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
-                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz "
-                                   "(nominal unit counts and maximum SM clock)"}
+        clk_sum = clk.summary()
+        alu, alu_src = fp32_alu_peak(dev, clk_sum.get("sm_max_mhz"))
+        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / alu, 4), "traffic": None,
+                    "peak_source": alu_src}
 
     # end to end through the public API: inputs and upstream gradients from pinned host
     # memory, the backward, the gradients back to pinned host memory
@@ -745,7 +866,8 @@ def run_backward(args):
                        "workspace_bytes": int(ws.numel()),
                        "l2": "inputs and workspace exceed the 129 MB L2; no flush"},
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": clk.summary(), "kernel_digest": kernel_source_digest(BACKWARD_SOURCES)}
+            "clocks": clk_sum if kbytes is None else clk.summary(),
+            "kernel_digest": kernel_source_digest(BACKWARD_SOURCES)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = backward_cpu_baseline(x, dout)
     if rank == 0:
@@ -951,9 +1073,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", type=int, default=3, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--workload", type=int, default=3, choices=[0, 1, 2, 3, 4, 5, 6])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="with the default workload, skip the 256K and packed-1M lines "
+                         "reported under 'workloads'")
     ap.add_argument("--op", default="forward",
                     choices=["forward", "decode", "backward", "contrast", "projection"],
                     help="forward: the chunked forward pass (default); decode: the "

@@ -21,7 +21,7 @@ import threading
 
 from . import build as _build_mod
 
-__all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host",
+__all__ = ["validate_cu_seqlens", "count_nonfinite", "chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host",
            "chunk_fwd_from_host_pipelined", "fwd_pipeline_plan", "fwd_pipelined_workspace_bytes",
            "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
@@ -30,7 +30,8 @@ __all__ = ["chunk_fwd", "chunk_fwd_simt", "chunk_fwd_from_host",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
 
-STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA"}
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+          4: "KDA_ERR_NONFINITE"}
 KDA_F32, KDA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_kernel_launch_count", "kda_read_device_flags",
@@ -40,7 +41,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_chunk_bwd_static_scratch", "kda_bwd_timing_start",
                     "kda_bwd_timing_read", "kda_chunk_fwd_variant", "kda_gate_projection",
                     "kda_chunk_fwd_from_host_pipelined", "kda_chunk_fwd_pipelined_workspace_bytes",
-                    "kda_chunk_fwd_pipeline_plan")
+                    "kda_chunk_fwd_pipeline_plan", "kda_validate_cu_seqlens",
+                    "kda_count_nonfinite", "kda_check_outputs")
 
 _lock = threading.Lock()
 _lib = None
@@ -120,6 +122,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_bwd_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float),
                                             ctypes.POINTER(ctypes.c_int)]
         lib.kda_bwd_timing_read.restype = ctypes.c_int
+        lib.kda_validate_cu_seqlens.argtypes = [P, I32, I64, P, P]
+        lib.kda_validate_cu_seqlens.restype = ctypes.c_int
+        lib.kda_count_nonfinite.argtypes = [P, I64, ctypes.c_int, P, P]
+        lib.kda_count_nonfinite.restype = ctypes.c_int
+        lib.kda_check_outputs.argtypes = [P, I64, ctypes.c_int, P, I64, P,
+                                          ctypes.POINTER(ctypes.c_uint64), P]
+        lib.kda_check_outputs.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -356,6 +365,44 @@ def kernel_launch_count() -> int:
     return int(load_library().kda_kernel_launch_count())
 
 
+def validate_cu_seqlens(cu_seqlens, n_tok: int, stream=None):
+    """Check the layout rules of ``cu_seqlens`` (int32, on the device) on the device:
+    returns (bits, first offending index) -- bits 0 (first entry not 0), 1 (a decrease),
+    2 (last entry not n_tok); (0, 2**31 - 1) when valid. Synchronises the stream."""
+    import torch
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    cu = cu_seqlens.contiguous()
+    status = torch.empty(2, dtype=torch.int32, device=cu.device)
+    _check(lib, lib.kda_validate_cu_seqlens(_ptr(cu), cu.numel() - 1, int(n_tok), _ptr(status),
+                                            ctypes.c_void_p(stream.cuda_stream)))
+    st = status.cpu().tolist()
+    return int(st[0]), int(st[1])
+
+
+def count_nonfinite(*tensors, stream=None) -> int:
+    """Number of NaN / Inf elements over the given fp32 or bf16 CUDA tensors (None
+    skipped), counted by the library's kernel. Synchronises the stream."""
+    import torch
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    ts = [t.contiguous() for t in tensors if t is not None]
+    if not ts:
+        return 0
+    count = torch.zeros(1, dtype=torch.int64, device=ts[0].device)
+    for t in ts:
+        if t.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("count_nonfinite takes fp32 or bf16 tensors")
+        _check(lib, lib.kda_count_nonfinite(_ptr(t), t.numel(),
+                                            KDA_BF16 if t.dtype == torch.bfloat16 else KDA_F32,
+                                            _ptr(count), ctypes.c_void_p(stream.cuda_stream)))
+    return int(count.item())
+
+
 def read_device_flags(reset: bool = True, stream=None) -> int:
     """Synchronise the stream and return the library's device status word (bit 0: a
     pipeline wait in the tensor-core kernel timed out). Clears it when ``reset``."""
@@ -515,12 +562,14 @@ def chunk_bwd_static_scratch(q, k, v, gate_logits, beta, h0, cu_seqlens, dout, d
     grads = [torch.empty_like(t) for t in (q, k, v, gate_logits, beta)]
     dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 \
         else None
-    stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(lib, lib.kda_chunk_bwd_static_scratch(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
-        _ptr(dout), _ptr(dh_final), *[_ptr(g) for g in grads], _ptr(dh0),
-        N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
-        ctypes.c_void_p(stream)))
+    # the library resolves the scratch array of the CURRENT device: make it q's
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        _check(lib, lib.kda_chunk_bwd_static_scratch(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), _ptr(beta), _ptr(h0),
+            _ptr(cu_seqlens), _ptr(dout), _ptr(dh_final), *[_ptr(g) for g in grads], _ptr(dh0),
+            N, n_seq, H, dk, dv, KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+            ctypes.c_void_p(stream)))
     return (*grads, dh0)
 
 

@@ -207,6 +207,7 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: dtype or head dimension not built";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+        case KDA_ERR_NONFINITE: return "KDA_ERR_NONFINITE: non-finite values in the outputs";
     }
     return "unknown kda_status";
 }
@@ -234,6 +235,51 @@ kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream) {
     e = kda::read_fwd64_flags(&f64, reset != 0, (cudaStream_t)stream);
     if (e != cudaSuccess) return launched(e, "reading the device status word");
     *flags = v | g | bw | f64;
+    return ok();
+}
+
+kda_status kda_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seq, int64_t n_tok,
+                                   int32_t *d_status, void *stream) {
+    if (!cu_seqlens || !d_status) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens and d_status are required");
+    if (n_seq < 0 || n_tok < 0) return fail(KDA_ERR_INVALID_ARG, "n_seq and n_tok must be non-negative");
+    if (((uintptr_t)cu_seqlens & 3u) || ((uintptr_t)d_status & 3u))
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens and d_status must be 4-byte aligned");
+    return launched(kda::launch_validate_cu(cu_seqlens, n_seq, n_tok, d_status, (cudaStream_t)stream),
+                    "validation kernel launch");
+}
+
+kda_status kda_count_nonfinite(const void *x, int64_t n, kda_dtype dtype, unsigned long long *d_count,
+                               void *stream) {
+    if ((!x && n > 0) || !d_count) return fail(KDA_ERR_INVALID_ARG, "x and d_count are required");
+    if (n < 0) return fail(KDA_ERR_INVALID_ARG, "n must be non-negative");
+    if (dtype != KDA_F32 && dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "dtype must be KDA_F32 or KDA_BF16");
+    if (((uintptr_t)x & (dtype == KDA_BF16 ? 1u : 3u)) || ((uintptr_t)d_count & 7u))
+        return fail(KDA_ERR_INVALID_ARG, "x or d_count misaligned");
+    return launched(kda::launch_count_nonfinite(x, n, dtype == KDA_BF16, d_count, (cudaStream_t)stream),
+                    "non-finite count launch");
+}
+
+kda_status kda_check_outputs(const void *out, int64_t n_out, kda_dtype dtype, const float *h_final,
+                             int64_t n_h_final, unsigned long long *d_scratch, uint64_t *count,
+                             void *stream) {
+    if (!d_scratch || !count) return fail(KDA_ERR_INVALID_ARG, "d_scratch and count are required");
+    if ((!out && n_out > 0) || (!h_final && n_h_final > 0) || n_out < 0 || n_h_final < 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad output pointer or size");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(d_scratch, 0, sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return launched(e, "clearing the count");
+    kda_status s = kda_count_nonfinite(out, n_out, dtype, d_scratch, stream);
+    if (s != KDA_OK) return s;
+    s = kda_count_nonfinite(h_final, n_h_final, KDA_F32, d_scratch, stream);
+    if (s != KDA_OK) return s;
+    unsigned long long host = 0;
+    e = cudaMemcpyAsync(&host, d_scratch, sizeof(host), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return launched(e, "reading the count");
+    *count = host;
+    if (host > 0)
+        return fail(KDA_ERR_NONFINITE, std::to_string(host) + " non-finite values in out / h_final");
     return ok();
 }
 
@@ -393,8 +439,13 @@ kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void
                                         int32_t n_heads, int32_t d_k, int32_t d_v,
                                         kda_dtype dtype, void *stream) {
     static_assert(KDA_STATIC_SCRATCH_BYTES == kda::kStaticScratchBytes, "one scratch size");
-    if (n_tok >= 0 && n_seq >= 0 && n_heads > 0 && d_k > 0 && d_v > 0 &&
-        kda::bwd_workspace_bytes(n_tok, n_seq, n_heads, d_k, d_v) > kda::kStaticScratchBytes)
+    // the sizes are checked first, so the scratch comparison sees only valid ones
+    kda_status s = validate(pack(q, k, v, gate_logits, beta, h0, cu_seqlens,
+                                 const_cast<void *>(dout), nullptr, n_tok, n_seq, n_heads, d_k,
+                                 d_v, dtype),
+                            dtype);
+    if (s != KDA_OK) return s;
+    if (kda::bwd_workspace_bytes(n_tok, n_seq, n_heads, d_k, d_v) > kda::kStaticScratchBytes)
         return fail(KDA_ERR_UNSUPPORTED, "the problem needs more checkpoint space than the "
                                          "static scratch holds (KDA_STATIC_SCRATCH_BYTES)");
     void *scratch = nullptr;

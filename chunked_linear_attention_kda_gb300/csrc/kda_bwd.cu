@@ -2251,10 +2251,19 @@ cudaError_t launch_bwd_t(const BwdArgs &p, cudaStream_t stream) {
 
 size_t bwd_slots(int64_t n_tok, int32_t n_seq) { return (size_t)(n_tok >> 4) + (size_t)n_seq + 1; }
 
+// a * b, or SIZE_MAX when the product does not fit
+static size_t mul_saturating(size_t a, size_t b) {
+    return (a != 0 && b > SIZE_MAX / a) ? SIZE_MAX : a * b;
+}
+
 size_t bwd_workspace_bytes(int64_t n_tok, int32_t n_seq, int32_t n_heads, int32_t d_k,
                            int32_t d_v) {
-    return bwd_slots(n_tok, n_seq) * (size_t)n_heads *
-           ((size_t)2 * d_k * d_v + prep_floats(d_k, d_v)) * sizeof(float);
+    // saturates instead of wrapping, so that no size check passes on an overflowed figure
+    const size_t per_slot_head =
+        mul_saturating(mul_saturating(2, (size_t)d_k), (size_t)d_v) + prep_floats(d_k, d_v);
+    return mul_saturating(mul_saturating(mul_saturating(bwd_slots(n_tok, n_seq), (size_t)n_heads),
+                                         per_slot_head),
+                          sizeof(float));
 }
 
 cudaError_t launch_bwd(const BwdArgs &p, cudaStream_t stream) {

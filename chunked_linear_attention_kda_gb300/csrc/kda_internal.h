@@ -97,6 +97,14 @@ cudaError_t read_bwd_flags(unsigned int *flags, bool reset, cudaStream_t stream)
 cudaError_t bwd_timing_start(int capacity);
 cudaError_t bwd_timing_read(float ms[4], int *calls);
 
+// Layout checks of cu_seqlens on the device (status[0]: bit 0 cu[0] != 0, bit 1 a
+// decrease, bit 2 cu[n_seq] != n_tok; status[1]: first offending index) and a count of
+// non-finite elements added into *count (kda_check.cu).
+cudaError_t launch_validate_cu(const int32_t *cu, int32_t n_seq, int64_t n_tok, int32_t *status,
+                               cudaStream_t stream);
+cudaError_t launch_count_nonfinite(const void *x, int64_t n, bool bf16, unsigned long long *count,
+                                   cudaStream_t stream);
+
 // Copies (and optionally clears) the device-side status word; synchronises stream.
 cudaError_t read_device_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 

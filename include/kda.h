@@ -46,8 +46,9 @@
  * legacy default stream). The return value reports argument validation and launch
  * errors only; device-side faults surface at the next synchronising CUDA call.
  * Calls are thread-safe (the only mutable global is the launch counter below). cu_seqlens is read on the
- * device only, so its contents are not validated; breaking the rules above is
- * undefined behaviour.
+ * device only, so the forward calls do not validate its contents; breaking the rules
+ * above is undefined behaviour. kda_validate_cu_seqlens checks them on the device
+ * without trapping, for callers who cannot vouch for their offsets.
  */
 #ifndef KDA_GB300_H_
 #define KDA_GB300_H_
@@ -63,7 +64,8 @@ typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, bad layout */
     KDA_ERR_UNSUPPORTED = 2, /* valid but not built: dtype or head dimension */
-    KDA_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_NONFINITE = 4    /* kda_check_outputs found NaN or Inf in the outputs */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -85,13 +87,57 @@ uint64_t kda_kernel_launch_count(void);
 
 /*
  * kda_read_device_flags -- synchronise `stream`, then copy the library's device-side
- * status word into *flags (and clear it when `reset` is non-zero). Bit 0 set: a
- * pipeline wait inside the tensor-core kernel exceeded its time limit (about two
- * seconds); that kernel then stopped early and its outputs are unspecified. A
- * healthy run leaves the word 0. Returns KDA_ERR_INVALID_ARG for a NULL `flags`,
- * KDA_ERR_CUDA if the copy or the synchronisation fails.
+ * status word into *flags (and clear it when `reset` is non-zero). A set bit means a
+ * pipeline wait inside one of the library's kernels exceeded its time limit (about
+ * two seconds); that kernel then stopped early and its outputs are unspecified:
+ * bit 0 the 16-token-step tensor-core forward (and the self-test below), bit 1 the
+ * gate-projection GEMM, bit 2 the backward's serial passes, bit 3 the 64-token-step
+ * tensor-core forward. A healthy run leaves the word 0. Returns KDA_ERR_INVALID_ARG
+ * for a NULL `flags`, KDA_ERR_CUDA if the copy or the synchronisation fails.
  */
 kda_status kda_read_device_flags(uint32_t *flags, int reset, void *stream);
+
+/*
+ * kda_validate_cu_seqlens -- check on the device that `cu_seqlens` (device memory,
+ * n_seq + 1 int32 entries) follows the layout rules above: cu_seqlens[0] = 0,
+ * non-decreasing, cu_seqlens[n_seq] = n_tok. The forward kernels read cu_seqlens on
+ * the device without checking it; a caller who cannot vouch for its offsets runs this
+ * first and reads the result before calling them. Writes two int32 at the device
+ * address `d_status`: d_status[0] is a bit set (bit 0: cu_seqlens[0] != 0; bit 1:
+ * cu_seqlens[i + 1] < cu_seqlens[i] for some i; bit 2: cu_seqlens[n_seq] != n_tok;
+ * 0 = valid) and d_status[1] the smallest offending index (i for a decrease between
+ * i and i + 1, 0 or n_seq for the end points; INT32_MAX when valid). Only reads
+ * cu_seqlens (n_seq + 1 entries must be readable); never traps. Asynchronous on
+ * `stream`. Returns KDA_ERR_INVALID_ARG for NULL or misaligned (4 bytes) pointers or
+ * negative sizes, KDA_ERR_CUDA if a launch fails.
+ */
+kda_status kda_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seq, int64_t n_tok,
+                                   int32_t *d_status, void *stream);
+
+/*
+ * kda_count_nonfinite -- add to the uint64 at device address `d_count` the number of
+ * NaN or +-Inf elements among the `n` elements of `x` (device memory, `dtype`
+ * KDA_F32 or KDA_BF16). The bounded gate is what keeps the forward finite at the
+ * decay bound ("Demystifying Trillion-Parameter MoE Models", Verification, monitors
+ * the rate of such values); this counter measures it. The caller zeroes *d_count.
+ * Asynchronous on `stream`. Returns KDA_ERR_INVALID_ARG (NULL pointers with n > 0,
+ * n < 0, x not aligned to its element, d_count not 8-byte aligned),
+ * KDA_ERR_UNSUPPORTED (dtype), KDA_ERR_CUDA.
+ */
+kda_status kda_count_nonfinite(const void *x, int64_t n, kda_dtype dtype,
+                               unsigned long long *d_count, void *stream);
+
+/*
+ * kda_check_outputs -- the non-finite count over a forward call's outputs: `n_out`
+ * elements of `out` (`dtype`) and `n_h_final` fp32 elements of `h_final` (either may
+ * be NULL with a zero count), using the uint64 at device address `d_scratch`.
+ * Synchronises `stream`; writes the count to *count (host memory) and returns
+ * KDA_ERR_NONFINITE when it is non-zero (KDA_OK otherwise), or KDA_ERR_INVALID_ARG /
+ * KDA_ERR_CUDA as above.
+ */
+kda_status kda_check_outputs(const void *out, int64_t n_out, kda_dtype dtype, const float *h_final,
+                             int64_t n_h_final, unsigned long long *d_scratch, uint64_t *count,
+                             void *stream);
 
 /*
  * kda_selftest_bounded_wait -- failure-detection self-test; no counterpart in the
@@ -110,7 +156,10 @@ kda_status kda_selftest_bounded_wait(int64_t limit_cycles, int32_t *d_returned, 
  *
  * Kernel choice is made from the arguments, not from any global setting:
  *   dtype KDA_BF16 with d_k = d_v = 128: the tensor-core kernel (bf16 operands,
- *     fp32 accumulation and state) on thread-block clusters;
+ *     fp32 accumulation and state) on thread-block clusters. It advances the state
+ *     64 tokens (four bounded 16-token tiles) per serial step on tcgen05 tensor
+ *     cores; the environment variable KDA_FWD_KERNEL=tc16 selects the earlier
+ *     16-token-step mma.sync kernel instead (same results within rounding);
  *   any other supported case (KDA_F32, or 1 <= d_k, d_v <= 128): the fp32 SIMT
  *     kernel. Both compute the same chunked algebra.
  * Returns KDA_OK, KDA_ERR_INVALID_ARG (null required pointer, n_tok < 0,
@@ -298,7 +347,10 @@ kda_status kda_bwd_timing_read(float *ms, int *calls);
  * zero: every slot a call reads, that call has written first. The scratch is shared by
  * every call on the device: two calls that may run at the same time (different streams,
  * or host threads whose streams are not ordered) race on it and both results are
- * undefined -- order them on one stream.
+ * undefined -- order them on one stream. The scratch used is the one of the calling
+ * thread's CURRENT device (cudaGetDevice): every pointer and `stream` must belong to that
+ * device. The argument and size checks (those of kda_chunk_bwd, then the scratch size)
+ * all run before any device work.
  */
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void *v,

@@ -17,6 +17,10 @@ LLMs", §5.1, sets the lengths; there is no dataset):
     3 context-64K    B=1 H=32 T=65536   d=128  h0 = 0
     4 varlen-1M      H=16 d=128, 16 lengths ~ U{4096..131072} then one of 1,048,576,
                      per-sequence h0 ~ N(0, 0.1^2)
+    5 context-256K   B=1 H=32 T=262144  d=128  h0 = 0 (the ladder's 256K point)
+    6 delta-64K      B=1 H=32 T=65536   d=128  a ~ N(-6,1) on every head (g ~ -0.012: a
+                     near-pure delta rule, little decay to damp rounding in the state),
+                     h0 ~ N(0, 0.1^2)
 Common distributions: q, k ~ N(0,1) then L2-normalised per token and head in fp32
 (x / max(|x|_2, 1e-6)) before the cast; v ~ N(0,1); beta = sigmoid(N(0,1));
 gate logits a ~ N(0, 2^2) unless stated. q/k/v (and the output) are bf16 except in
@@ -40,6 +44,8 @@ WORKLOADS = {
     2: "decay-bound-stress-B2-H16-T8192-d128",
     3: "context-64K-B1-H32-T65536-d128",
     4: "packed-varlen-1M-H16-d128",
+    5: "context-256K-B1-H32-T262144-d128",
+    6: "near-delta-rule-64K-B1-H32-T65536-d128",
 }
 
 
@@ -143,12 +149,16 @@ def workload_lengths(index: int, gen: Optional[torch.Generator] = None) -> list:
         g.manual_seed(SEED_BASE + 4 if gen is None else gen.initial_seed())
         lens = torch.randint(4096, 131072 + 1, (16,), generator=g)
         return [int(x) for x in lens.tolist()] + [1 << 20]
+    if index == 5:
+        return [1 << 18]
+    if index == 6:
+        return [65536]
     raise ValueError(f"unknown workload {index}")
 
 
 def make_workload(index: int, device="cpu", seed: Optional[int] = None,
                   max_len: Optional[int] = None) -> KDAInputs:
-    """Workload ``index`` (0..4) exactly as listed in the module docstring.
+    """Workload ``index`` (0..6) exactly as listed in the module docstring.
     ``max_len`` truncates every sequence (same recipe, fewer tokens), for host-side
     samples of the large workloads."""
     device = torch.device(device)
@@ -174,13 +184,18 @@ def make_workload(index: int, device="cpu", seed: Optional[int] = None,
     if index == 4:
         return make_inputs(lengths, 16, 128, 128, device=device, h0_std=0.1, name=name,
                            gen=gen)
+    if index == 5:
+        return make_inputs(lengths, 32, 128, 128, device=device, name=name, gen=gen)
+    if index == 6:
+        return make_inputs(lengths, 32, 128, 128, device=device, gate_mean=-6.0, gate_std=1.0,
+                           h0_std=0.1, name=name, gen=gen)
     raise ValueError(index)
 
 
 def workload_size(index: int) -> dict:
     """Token and token-head counts without generating any tensor."""
     lens = workload_lengths(index)
-    H = {0: 1, 1: 4, 2: 16, 3: 32, 4: 16}[index]
+    H = {0: 1, 1: 4, 2: 16, 3: 32, 4: 16, 5: 32, 6: 32}[index]
     return {"tokens": sum(lens), "heads": H, "token_heads": sum(lens) * H,
             "n_seq": len(lens)}
 

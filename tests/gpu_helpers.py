@@ -48,3 +48,30 @@ def assert_finite(*ts):
     for t in ts:
         if t is not None:
             assert bool(torch.isfinite(t).all()), "non-finite values in GPU output"
+
+
+def per_seq_head_rel(x_gpu, ref, cu, min_len: int = 1):
+    """Worst rel-L2 over (sequence, head) of outputs [N, H, d] (sequences shorter than
+    ``min_len`` skipped) -- a localised error is not diluted by the whole-tensor norm."""
+    x_gpu = np.asarray(x_gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    worst = 0.0
+    for s, e in zip(cu[:-1], cu[1:]):
+        if e - s < max(1, min_len):
+            continue
+        d = x_gpu[s:e] - ref[s:e]
+        num = np.sqrt((d ** 2).sum(axis=(0, 2)))
+        den = np.sqrt((ref[s:e] ** 2).sum(axis=(0, 2)))
+        r = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+        worst = max(worst, float(r.max()))
+    return worst
+
+
+def per_state_rel(h_gpu, h_ref):
+    """Worst rel-L2 over (sequence, head) of final states [n_seq, H, d_k, d_v]."""
+    h_gpu = np.asarray(h_gpu, dtype=np.float64)
+    h_ref = np.asarray(h_ref, dtype=np.float64)
+    num = np.sqrt(((h_gpu - h_ref) ** 2).sum(axis=(2, 3)))
+    den = np.sqrt((h_ref ** 2).sum(axis=(2, 3)))
+    r = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+    return float(r.max()) if r.size else 0.0

@@ -45,7 +45,7 @@ def test_library_has_no_torch_or_python_dependency():
 
 def test_version_and_status_strings(lib):
     assert lib.kda_version() >= 100
-    for s in range(4):
+    for s in range(5):
         assert lib.kda_status_string(s).decode().startswith(kda.STATUS[s])
     assert lib.kda_status_string(99) == b"unknown kda_status"
 
@@ -225,3 +225,38 @@ def test_backward_timing_read_rejects_null(lib):
     calls = ctypes.c_int(0)
     assert lib.kda_bwd_timing_read(None, ctypes.byref(calls)) == 1
     assert lib.kda_bwd_timing_read(ms, None) == 1
+
+
+# ---------------------------------------------------------------- device-side checks
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cu=None), 1), (dict(st=None), 1), (dict(n_seq=-1), 1), (dict(n_tok=-5), 1),
+    (dict(cu=FAKE + 2), 1), (dict(st=FAKE + 1), 1),
+])
+def test_validate_cu_seqlens_host_validation(lib, kw, status):
+    a = dict(cu=FAKE, n_seq=3, n_tok=100, st=FAKE)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.kda_validate_cu_seqlens(P(a["cu"]), a["n_seq"], a["n_tok"], P(a["st"]), None)
+    assert st == status and lib.kda_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(cnt=None), 1), (dict(n=-1), 1), (dict(dtype=5), 2),
+    (dict(x=FAKE + 2, dtype=0), 1), (dict(x=FAKE + 1, dtype=1), 1), (dict(cnt=FAKE + 4), 1),
+])
+def test_count_nonfinite_host_validation(lib, kw, status):
+    a = dict(x=FAKE, n=10, dtype=1, cnt=FAKE)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.kda_count_nonfinite(P(a["x"]), a["n"], a["dtype"], P(a["cnt"]), None)
+    assert st == status and lib.kda_last_error().decode() != ""
+
+
+def test_check_outputs_host_validation(lib):
+    P = ctypes.c_void_p
+    cnt = ctypes.c_uint64(0)
+    assert lib.kda_check_outputs(P(FAKE), 10, 1, None, 0, None, ctypes.byref(cnt), None) == 1
+    assert lib.kda_check_outputs(P(FAKE), 10, 1, None, 0, P(FAKE), None, None) == 1
+    assert lib.kda_check_outputs(None, 10, 1, None, 0, P(FAKE), ctypes.byref(cnt), None) == 1
+    assert lib.kda_check_outputs(P(FAKE), -1, 1, None, 0, P(FAKE), ctypes.byref(cnt), None) == 1

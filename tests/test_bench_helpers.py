@@ -50,14 +50,37 @@ def test_prefix_parity_figure():
     tokens = 200
     px = K.prefix(x, tokens)
     o_ref, _ = recurrence.kda_forward(px.q, px.k, px.v, px.a, px.beta, px.h0, px.cu_host)
-    assert bench.prefix_rel_l2(x, out, tokens, o_ref) < 1e-6
+    whole, worst = bench.prefix_rel_l2(x, out, tokens, o_ref)
+    assert whole < 1e-6 and worst < 1e-6
     bad = out.clone()
     bad[300 + 150] += 1.0          # inside sequence 2's first 200 tokens
-    assert bench.prefix_rel_l2(x, bad, tokens, o_ref) > 1e-2
+    assert min(bench.prefix_rel_l2(x, bad, tokens, o_ref)) > 1e-2
     late = out.clone()
     late[300 + 250] += 1.0         # sequence 2 beyond the sample: not compared
-    assert bench.prefix_rel_l2(x, late, tokens, o_ref) < 1e-6
+    assert max(bench.prefix_rel_l2(x, late, tokens, o_ref)) < 1e-6
     # a whole-sequence sample compares every row
     o_all, _ = recurrence.kda_forward(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_host)
-    assert np.isclose(bench.prefix_rel_l2(x, bad, 1000, o_all),
+    assert np.isclose(bench.prefix_rel_l2(x, bad, 1000, o_all)[0],
                       np.linalg.norm(bad.numpy() - o_all) / np.linalg.norm(o_all))
+
+
+def test_worst_head_is_not_diluted():
+    """An error confined to one (sequence, head) pair: the worst-pair figure is that
+    pair's own rel-L2, several times the whole-sample figure."""
+    x = K.make_inputs([64, 64], 4, 16, 16, dtype=torch.float32, seed=4)
+    o, _ = recurrence.kda_forward(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_host)
+    bad = torch.from_numpy(o).float()
+    bad[64:128, 2] *= 1.01         # sequence 1, head 2: 1% off
+    whole, worst = bench.prefix_rel_l2(x, bad, 64, o)
+    assert np.isclose(worst, 0.01, rtol=1e-4)
+    assert whole < worst / 2
+
+
+def test_state_parity_figure():
+    r = np.random.default_rng(0).standard_normal((3, 4, 8, 8))
+    g = torch.from_numpy(r).float()
+    whole, worst = bench.state_rel_l2(g, r)
+    assert whole < 1e-6 and worst < 1e-6
+    g[1, 3] *= 1.02
+    whole, worst = bench.state_rel_l2(g, r)
+    assert np.isclose(worst, 0.02, rtol=1e-4) and whole < worst / 2

@@ -38,6 +38,11 @@ def test_same_results_as_the_workspace_entry_point_twice(dtype):
     dhf = torch.randn((x.n_seq, H, d, d), generator=g).to("cuda")
     lib = kda.load_library()
     assert lib.kda_chunk_bwd_workspace_bytes(x.n_tok, x.n_seq, H, d, d) <= (64 << 20)
+    # an unrelated, larger problem first, so the scratch holds other data when the
+    # compared calls run
+    y = K.make_inputs([300, 129], 4, d, d, dtype=dtype, device="cuda", seed=31, h0_std=0.5)
+    ydout = torch.randn((y.n_tok, 4, d), generator=g).to("cuda", dtype)
+    kda.chunk_bwd_static_scratch(y.q, y.k, y.v, y.a, y.beta, y.h0, y.cu_seqlens, ydout, None)
     ref = kda.chunk_bwd(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens, dout, dhf)
     for _ in range(2):
         got = kda.chunk_bwd_static_scratch(x.q, x.k, x.v, x.a, x.beta, x.h0, x.cu_seqlens,
@@ -45,3 +50,31 @@ def test_same_results_as_the_workspace_entry_point_twice(dtype):
         torch.cuda.synchronize()
         for r, o in zip(ref, got):
             assert torch.equal(r, o)
+
+
+@pytest.mark.gpu
+def test_a_call_allocates_no_device_memory():
+    """Around one call through the C ABI (outputs allocated beforehand), neither torch's
+    allocator nor the device's free memory changes."""
+    lengths, H, d = [100, 37], 2, 128
+    x = K.make_inputs(lengths, H, d, d, device="cuda", seed=10, h0_std=0.3)
+    dout = torch.randn((x.n_tok, H, d), device="cuda").to(x.dtype)
+    grads = [torch.empty_like(t) for t in (x.q, x.k, x.v, x.a, x.beta)]
+    dh0 = torch.empty((x.n_seq, H, d, d), dtype=torch.float32, device="cuda")
+    lib = kda.load_library()
+    P = ctypes.c_void_p
+    ptr = lambda t: P(t.data_ptr()) if t is not None else None  # noqa: E731
+
+    def call():
+        st = lib.kda_chunk_bwd_static_scratch(
+            ptr(x.q), ptr(x.k), ptr(x.v), ptr(x.a), ptr(x.beta), ptr(x.h0), ptr(x.cu_seqlens),
+            ptr(dout), None, *[ptr(t) for t in grads], ptr(dh0), x.n_tok, x.n_seq, H, d, d,
+            kda.KDA_BF16, P(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, lib.kda_last_error()
+        torch.cuda.synchronize()
+
+    call()   # modules and the scratch address resolved on the first call
+    alloc0, (free0, _) = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()
+    call()
+    alloc1, (free1, _) = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()
+    assert alloc1 == alloc0 and free1 == free0
