@@ -15,27 +15,29 @@
 //   P  = lower([Q K^T with the same factors])                        64 x 64
 //   TB = (I + A)^-1 diag(beta),   W = TB K~B,   K~B = K exp(G^B)
 //   Q' = Q~B - P W,               P' = P TB,    K'B = K exp(G^B_end - G^B)
-//   U  = TB V - W S,   O = d_k^-1/2 (P' V + Q' S),   S <- Diag(exp G^B_end) S + K'B^T U
-// (the output line is d_k^-1/2 (Q~B S + P U) with U substituted).
+//   U  = TB V - W S,   O = d_k^-1/2 (Q~B S + P U),   S <- Diag(exp G^B_end) S + K'B^T U
+// (equivalently O = d_k^-1/2 (P' V + Q' S) with U substituted).
 //
 // Work decomposition: one cluster of 1 + kPro CTAs per (sequence, head).
 //  * rank 0, the chain CTA, runs the serial recurrence. Transposed, with the state S^T
-//    (d_v x d_k) as the A operand of the tensor core: per step one group of MMAs
-//        D1 (128 x 128, tensor memory) = V^T [TB | P']^T + S^T [-W | Q']^T
-//    gives U^T (columns 0..63) and O^T / scale (64..127) at once; a second group
-//        D2 = U^T K'B
-//    gives the state increment. S^T lives in fp32 registers of eight "state" warps (two
-//    warpgroups; one value row and 64 keys per thread) and is mirrored as bf16 into
-//    tensor memory as the next A operand; U^T likewise. Four "output" warps store O.
-//    One thread issues every tcgen05.mma. A producer warp loads each step's V tile by
-//    TMA into one of two buffers; the products arrive in one of three operand slots.
-//  * ranks 1..kPro, the prologue CTAs, each compute every kPro-th step's products (the
-//    gate, the four tiles' scaled operands, A, P, the 64 x 64 solve, TB, P', and
-//    [W; -Q'] as one tcgen05 product on their own tensor core) into a staging buffer
-//    laid out exactly as the chain CTA's operand slot, and copy it there with bulk
-//    copies (shared::cta -> shared::cluster) once the chain CTA has freed the slot
-//    (with three slots and three prologue CTAs, each prologue CTA always fills the
-//    same slot).
+//    (d_v x d_k) as the A operand of the tensor core, per step:
+//        D1[:, 0..63]   = V^T TB^T + S^T (-W)^T       = U^T
+//        D1[:, 64..127] = S^T Q~B^T + U^T P^T          = O^T / scale
+//        D2             = U^T K'B                      (the state increment)
+//    Only the U^T group (N = 64) and D2 lie on the state's critical path; the O^T
+//    products fill the tensor pipe while U^T is converted and while the state is
+//    updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
+//    value row and 64 keys per thread) and is mirrored as bf16 into tensor memory as the
+//    next A operand; U^T likewise. One issuer thread (its own warp) issues every
+//    tcgen05.mma; the state warps signal it per warp through mbarriers. Four "output"
+//    warps store O. A producer warp loads each step's V tile by TMA into one of two
+//    buffers; the products arrive in one of three operand slots.
+//  * ranks 1..kPro, the prologue CTAs, each compute every kPro-th step's operands (the
+//    gate, the four tiles' scaled operands, [A; P] as one tcgen05 product, the 64 x 64
+//    solve for TB, W = TB K~B as a second tcgen05 product) into a staging buffer laid
+//    out exactly as the chain CTA's operand slot, and copy it there with bulk copies
+//    (shared::cta -> shared::cluster) once the chain CTA has freed the slot (with three
+//    slots and three prologue CTAs, each prologue CTA always fills the same slot).
 // Every wait is bounded: one that exceeds its limit sets bit 3 of the status word
 // (kda_read_device_flags); every other wait of the grid then gives up and the kernel
 // finishes with unspecified output.
@@ -58,7 +60,7 @@ __device__ unsigned int g_fwd64_flags;  // bit 3: a pipeline wait exceeded its l
 // state stored; slots 8-15 (the prologue CTA owning the step): loop top, raw tiles in,
 // gate, cross-tile decays, A and P, solve, W and Q', P' (copy issued at slot 7).
 #ifdef KDA_FWD64_TRACE
-__device__ long long g_f64_trace[64][24];
+__device__ long long g_f64_trace[64][32];
 #define F64_TRACE(n, slot)                                      \
     do {                                                        \
         if (blockIdx.x < kCluster && (n) < 64) g_f64_trace[(n)][(slot)] = clock64(); \
@@ -85,11 +87,13 @@ constexpr float kScale = 0.08838834764831845f;  // 128^-1/2
 static_assert(NT == 4, "the tile-pair tables below assume four tiles per step");
 
 // ---- operand slot (identical layout in the chain CTA's ring and a prologue's staging)
-// B1: [n][j] K-major, 128-byte swizzle: rows 0..63 = TB, rows 64..127 = P'   (K = tokens)
-// B2: [n][c] K-major, two 64-channel atom columns: rows 0..63 = -W, 64..127 = Q'
+// B1: [n][j] K-major, 128-byte swizzle: rows 0..63 = TB, rows 64..127 = P    (K = tokens)
+// B2: bytes 0..16383: -W, [t][c] K-major, two 64-channel atom columns 8 KB apart;
+//     bytes 16384..32767: Q~B, [c][t] (read MN-major: tokens along N, channels along K)
 // B3: [c][t] K-major: K'B^T (K = tokens)
 // G : gamma^B[c] = exp(G^B_end), fp32
 constexpr int SL_B1 = 0, SL_B2 = 16384, SL_B3 = 49152, SL_G = 65536;
+constexpr int B2_QB = 16384;  // offset of Q~B inside B2
 constexpr int SLOT_BYTES = SL_G + D * 4;  // 66048 (the gamma^B vector lives in its own ring)
 constexpr int SLOT_STRIDE = SL_G;         // 64 KB per slot: every slot 1024-byte aligned
 constexpr int NSLOT = 3;                  // operand slots of the chain CTA
@@ -104,12 +108,15 @@ constexpr int CH_BAR = CH_G + NSLOT * D * 4;
 static_assert(CH_V % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 // barrier indices (8 bytes each)
 constexpr int B_FULL = 0;     // [NSLOT] slot s: products (bulk copies) + V (TMA) landed
-constexpr int B_FREE = 3;     // [NSLOT] slot s: its MMAs completed and gamma read (2 arrivals)
-constexpr int B_D1FULL = 6;   // [2] D1 buffer b complete
+constexpr int B_FREE = 3;     // [NSLOT] slot s: its MMAs completed and gamma read (1 + 8 arrivals)
+constexpr int B_D1U = 6;      // [2] D1 buffer b: U^T complete
 constexpr int B_D1FREE = 8;   // [2] D1 buffer b read out by the output warps (4 arrivals)
 constexpr int B_D2FULL = 10;  // D2 complete
 constexpr int B_DRAIN = 11;   // every MMA complete (before the tensor memory is released)
-constexpr int NBARS = 12;
+constexpr int B_D1O = 12;     // [2] D1 buffer b: O^T complete
+constexpr int B_SREADY = 14;  // the state's bf16 copy is in tensor memory (8 warp arrivals)
+constexpr int B_UREADY = 15;  // U^T's bf16 copy is in tensor memory (8 warp arrivals)
+constexpr int NBARS = 16;
 static_assert(NSLOT == 3 && B_FREE == NSLOT, "barrier table");
 // tensor-memory columns
 constexpr uint32_t TM_D1 = 0;     // 2 x 128 columns
@@ -120,30 +127,36 @@ constexpr uint32_t kTmemCols = 512;
 
 // ---- prologue CTA shared memory
 constexpr int PR_Q = 0, PR_K = 16384, PR_A = 32768;  // raw tiles [64 t][128 c] (TMA)
-constexpr int PR_TILES = 65536;                      // 19 channel-major 128 x 16 tiles
-constexpr int TILE_BYTES = D * TL * 2;               // 4096
-constexpr int T_KT = 0, T_QT = 4, T_KH = 8, T_KP = 12, T_KX = 16;
-constexpr int PR_AT = PR_TILES + 19 * TILE_BYTES;    // A, then T, fp32 [64][64]
-constexpr int PR_STG = PR_AT + BT * BT * 4;          // staging slot
-constexpr int PR_GAM = PR_STG + SLOT_BYTES;          // gamma_I[c] fp32 [4][128]
-constexpr int PR_PRE = PR_GAM + NT * D * 4;          // prod_{m<I} gamma_m[c] [4][128]
-constexpr int PR_BETA = PR_PRE + NT * D * 4;         // beta [2][64]
-constexpr int PR_BAR = PR_BETA + 2 * BT * 4;         // RAWFULL, SLOTFREE, MMA done
-constexpr int PR_END = PR_BAR + 24;
-// after the A / P products the K^ and K' tiles are dead: K~B and Q~B ([c][64 t], 128-byte
-// swizzle, the B operand of the W / Q' product) take their place; after the solve the
-// fp32 A / T area holds the constant [0; -I] A-operand tile
-constexpr int PR_KB = PR_TILES + T_KH * TILE_BYTES;
-constexpr int PR_QB = PR_TILES + T_KP * TILE_BYTES;
-static_assert(PR_KB % 1024 == 0 && PR_QB % 1024 == 0 && PR_AT % 1024 == 0, "swizzled tiles");
-constexpr uint32_t kProTmemCols = 256;  // [W; -Q'] (128) and P' (64)
-static_assert(PR_STG % 1024 == 0 && PR_AT % 16 == 0, "alignment");
+// X: the operands of the A / P product, then those of the W / Q' product. Every operand
+// here is a set of 128 channel rows of 64 tokens (128-byte rows, 128-byte swizzle), which
+// the tensor core reads MN-major (tokens along M or N, channels along K) or K-major
+// (channels along N, tokens along K).
+constexpr int PR_X = 65536;
+constexpr int X_R = 0;       // [K~ | Q~] of the step's 64 tokens: two 16 KB halves (A operand)
+constexpr int X_C = 32768;   // column tiles: [K^_0..3 | K'_0..2, Kx_20 | Kx_30, Kx_31, -] (B)
+constexpr int X_KB = 0;      // after the A / P product: K~B ([c][64 t]), operand of the W product
+constexpr int X_BYTES = 81920;
+constexpr int PR_AD = PR_X + X_BYTES;             // diagonal A tiles, fp32 [4][16][16]
+constexpr int PR_AO = PR_AD + NT * TL * TL * 4;   // off-diagonal A tiles, bf16 [6][16][16]
+constexpr int PR_GAM = PR_AO + 6 * TL * TL * 2;   // gamma_I[c] fp32 [4][128]
+constexpr int PR_BETA = PR_GAM + NT * D * 4;      // beta [2][64]
+constexpr int PR_BAR = PR_BETA + 2 * BT * 4;      // RAWFULL, SLOTFREE, MMA done, A / P done
+constexpr int PR_STG = (PR_BAR + 32 + 1023) & ~1023;  // staging slot
+constexpr int PR_END = PR_STG + SLOT_BYTES;
+static_assert(PR_X % 1024 == 0 && (PR_X + X_C) % 1024 == 0 && PR_STG % 1024 == 0, "swizzled tiles");
+// tensor-memory columns of a prologue CTA
+constexpr uint32_t TP_WQ = 0;    // W (rows 0..63 of 128 x 128)
+constexpr uint32_t TP_AP = 256;  // [A; P] before masking (192)
+constexpr uint32_t kProTmemCols = 512;
 constexpr int SMEM_USED = (PR_END > CH_BAR + NBARS * 8 ? PR_END : CH_BAR + NBARS * 8);
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack of the dynamic base
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-// scratch inside the staging slot's B2 area until the W / Q' product overwrites it:
-// 19 fp32 16 x 16 tiles (per-warp left operands, M, M^2, the diagonal T tiles)
-constexpr int STG_XS = PR_STG + SL_B2;
+// fp32 16 x 16 scratch tiles of the solve in the -W part of the staging slot's B2 (-W
+// is written last): M = L^-1 N (6 tiles), M^2 (3), the diagonal T tiles (4)
+constexpr int STG_MM = PR_STG + SL_B2;
+constexpr int STG_M2 = STG_MM + 6 * 1024;
+constexpr int STG_TD = STG_M2 + 3 * 1024;
+static_assert(STG_TD + 4 * 1024 <= PR_STG + SL_B2 + B2_QB, "solve scratch stays in the -W part of B2");
 
 // registers per thread (chain CTA): the block is launched with 128; each warpgroup then
 // moves to its own share and the shares add up to the launch total
@@ -170,11 +183,11 @@ struct F64Params {
 __device__ __forceinline__ uint32_t sw128(int row, int k) {
     return (uint32_t)(row * 128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2);
 }
-// channel-major 128 x 16 bf16 tile ([c][t], 32-byte rows); the two 16-byte halves of a
-// row swap places every four rows, which keeps 8-row ldmatrix accesses conflict-free
-__device__ __forceinline__ uint32_t cmaj(int c, int t0) {
-    return (uint32_t)(c * 32 + ((((t0 >> 3) ^ (c >> 2)) & 1) << 4));
-}
+// two fp32 values -> bf16x2 (x in the lower half)
+__device__ __forceinline__ uint32_t pk2(float2 v) { return pack_bf16(v.x, v.y); }
+
+// the thread that records the chain CTA's state-warp trace points
+__device__ __forceinline__ bool elect_trace(int warp, int lane) { return warp == 4 && lane == 0; }
 
 // Bounded wait. Returns false when this or any other wait of the grid gave up.
 __device__ bool wait_bar(uint32_t a, uint32_t parity) {
@@ -252,16 +265,84 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                 const uint32_t owner = 1u + (uint32_t)((n + NSLOT) % kPro);
                 mbar_arrive_remote_relaxed(map_to_rank(sbase + PR_BAR + 8u, owner));
             }
+        } else if (warp == 2 && lane == 0) {
+            // ---------------------------------------------- MMA issuer
+            // Per step n (slot s, D1 buffer b), in tensor-pipe order:
+            //   V^T TB^T                 -> D1 columns 0..63   (issued one step ahead)
+            //   S^T (-W)^T               -> D1 columns 0..63   = U^T; commit D1U
+            //   S^T Q~B^T                -> D1 columns 64..127 (B read MN-major)
+            //   U^T K'B                  -> D2                 ; commit D2FULL
+            //   U^T P^T                  -> D1 columns 64..127 = O^T / scale; commit D1O, FREE
+            // so the state's critical path carries only the two N = 64 / 128 groups.
+            const uint32_t id_v = idesc_bf16(128, 64, 1, 0);   // A = V^T (MN-major), N = 64 tokens
+            const uint32_t id_t = idesc_bf16(128, 64, 0, 0);   // N = 64 tokens
+            const uint32_t id_q = idesc_bf16(128, 64, 0, 1);   // B = Q~B (MN-major), N = 64 tokens
+            const uint32_t id_k = idesc_bf16(128, 128, 0, 0);  // N = 128 keys
+            // slot s's descriptors are slot 0's plus s x the slot stride (16-byte units)
+            const uint64_t dV0 = sdesc_sw128(sbase + CH_V, 8192, 1024);
+            const uint64_t dB10 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
+            const uint64_t dB20 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 16, 1024);
+            const uint64_t dQB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2 + B2_QB, 8192, 1024);
+            const uint64_t dB30 = sdesc_sw128(sbase + CH_SLOT + SL_B3, 16, 1024);
+            constexpr uint64_t kSlotStep = SLOT_STRIDE >> 4, kVStep = V_BYTES >> 4;
+            constexpr uint64_t kLow = (64 * 128) >> 4;  // rows 64..127 of a K-major operand
+            auto issue_v = [&](int n) -> bool {
+                const int s = n % NSLOT, b = n & 1;
+                if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) return false;
+                if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
+                    umma_ss(d1, dV0 + b * kVStep + (uint64_t)(128 * j), dB10 + s * kSlotStep + (uint64_t)(2 * j),
+                            id_v, j > 0);
+                return true;
+            };
+            bool ok = nblocks > 0 && issue_v(0);
+            for (int n = 0; ok && n < nblocks; ++n) {
+                const int s = n % NSLOT, b = n & 1;
+                const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
+                const uint64_t b2 = dB20 + s * kSlotStep;
+                if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T (bf16) of step n is in
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // K = 16 keys per MMA
+                    umma_ts(d1, tmem + TM_AS + 8u * k, b2 + (uint64_t)((((k >> 2) * 8192) + (k & 3) * 32) >> 4),
+                            id_t, 1);
+                umma_commit(bar(B_D1U + b));
+                F64_TRACE(n, 1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // 16 channel rows (2048 bytes) per MMA
+                    umma_ts(d1 + 64u, tmem + TM_AS + 8u * k, dQB0 + s * kSlotStep + (uint64_t)(128 * k), id_q, k > 0);
+                if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
+                    umma_ts(tmem + TM_D2, tmem + TM_AU + 8u * j, dB30 + s * kSlotStep + (uint64_t)(2 * j), id_k,
+                            j > 0);
+                umma_commit(bar(B_D2FULL));
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    umma_ts(d1 + 64u, tmem + TM_AU + 8u * j, dB10 + s * kSlotStep + kLow + (uint64_t)(2 * j), id_t,
+                            1);
+                umma_commit(bar(B_D1O + b));
+                umma_commit(bar(B_FREE + s));
+                F64_TRACE(n, 4);
+                if (n + 1 < nblocks) ok = issue_v(n + 1);
+            }
+            // every MMA has completed before the tensor memory is released
+            umma_commit(bar(B_DRAIN));
+            wait_bar(bar(B_DRAIN), 0);
         }
     } else if (warp < 12) {
         regs_set<kRegsState>();
         // -------------------------------------------------- state warps (two warpgroups)
         // Thread (value row v = TMEM lane, key half kh) holds S^T[v][64 kh .. 64 kh + 63]
         // in fp32 registers; the two warpgroups split each step's conversions by half.
+        // Each warp signals the issuer on its own (SREADY, UREADY: 8 arrivals).
         const int kh = (warp - 4) >> 2;
         const int v = ((warp & 3) << 5) + lane;                 // value row = TMEM lane
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;  // lane quarter
-        const bool elect = warp == 4 && lane == 0;
         constexpr int KH = D / 2;
         float S[KH];
         {
@@ -269,59 +350,27 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
 #pragma unroll
             for (int c = 0; c < KH; ++c) S[c] = h0 ? h0[(size_t)(KH * kh + c) * D + v] : 0.f;
         }
+        auto store_state = [&]() {  // bf16 copy of this thread's 64 keys -> A operand
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            uint32_t w[16];
+            for (int q = 0; q < 2; ++q) {
+                uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = pack_bf16(S[32 * q + 2 * j], S[32 * q + 2 * j + 1]);
-            tmem_st16(tmem + lb + TM_AS + 32 * kh + 16 * q, w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        named_sync(1, 256);
-        // descriptors: only the start-address field changes along K
-        const uint32_t idesc_v = idesc_bf16(128, 128, 1, 0);  // A = V^T (MN-major)
-        const uint32_t idesc_k = idesc_bf16(128, 128, 0, 0);
-        // slot s's descriptors are slot 0's plus s x the slot stride (16-byte units)
-        const uint64_t dV0 = sdesc_sw128(sbase + CH_V, 8192, 1024);
-        const uint64_t dB10 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
-        const uint64_t dB20 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 16, 1024);
-        const uint64_t dB30 = sdesc_sw128(sbase + CH_SLOT + SL_B3, 16, 1024);
-        constexpr uint64_t kSlotStep = SLOT_STRIDE >> 4, kVStep = V_BYTES >> 4;
-        // V^T [TB | P']^T into D1 buffer n & 1 (needs step n's slot and the buffer free)
-        auto issue_v = [&](int n) -> bool {
-            const int s = n % NSLOT, b = n & 1;
-            if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) return false;
-            if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) return false;
-            tc_fence_after();
-            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
-                umma_ss(d1, dV0 + b * kVStep + (uint64_t)(128 * j), dB10 + s * kSlotStep + (uint64_t)(2 * j),
-                        idesc_v, j > 0);
-            return true;
-        };
-        bool ok = true;
-        if (elect && nblocks > 0) ok = issue_v(0);
-        __syncwarp();
-        int n = 0;
-        for (; n < nblocks; ++n) {
-            const int s = n % NSLOT, b = n & 1;
-            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
-            if (elect) F64_TRACE(n, 0);
-            if (elect && ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // S^T [-W | Q']^T, K = 16 keys per MMA
-                    umma_ts(d1, tmem + TM_AS + 8u * k,
-                            dB20 + s * kSlotStep + (uint64_t)((((k >> 2) * 16384) + (k & 3) * 32) >> 4), idesc_k, 1);
-                umma_commit(bar(B_D1FULL + b));
-                F64_TRACE(n, 1);
+                for (int j = 0; j < 16; ++j) w[j] = pack_bf16(S[32 * q + 2 * j], S[32 * q + 2 * j + 1]);
+                tmem_st16(tmem + lb + TM_AS + 32 * kh + 16 * q, w);
             }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SREADY));
+        };
+        store_state();
+        for (int n = 0; n < nblocks; ++n) {
+            const int s = n % NSLOT, b = n & 1;
+            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
+            if (elect_trace(warp, lane)) F64_TRACE(n, 0);
             // ---- U^T: columns 0..63 of D1 -> bf16 A operand, 32 tokens per warpgroup
-            const bool got1 = ok && wait_bar(bar(B_D1FULL + b), (n >> 1) & 1);
-            if (named_sync_or(1, 256, !got1)) break;
-            if (elect) F64_TRACE(n, 2);
+            if (!wait_bar(bar(B_D1U + b), (n >> 1) & 1)) break;
+            if (elect_trace(warp, lane)) F64_TRACE(n, 2);
             tc_fence_after();
             {
                 uint32_t r[32], w[16];
@@ -334,24 +383,12 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             }
             tmem_st_wait();
             tc_fence_before();
-            named_sync(1, 256);
-            if (elect) {
-                F64_TRACE(n, 3);
-                tc_fence_after();
-#pragma unroll
-                for (int j = 0; j < 4; ++j)  // U^T K'B, K = 16 tokens per MMA
-                    umma_ts(tmem + TM_D2, tmem + TM_AU + 8u * j, dB30 + s * kSlotStep + (uint64_t)(2 * j), idesc_k,
-                            j > 0);
-                umma_commit(bar(B_D2FULL));
-                umma_commit(bar(B_FREE + s));
-                if (n + 1 < nblocks) ok = issue_v(n + 1);
-                F64_TRACE(n, 4);
-            }
             __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_UREADY));
+            if (elect_trace(warp, lane)) F64_TRACE(n, 3);
             // ---- S^T <- S^T diag(gamma^B) + D2 on this warpgroup's 64 keys, then bf16
-            const bool got2 = ok && wait_bar(bar(B_D2FULL), n & 1);
-            if (named_sync_or(1, 256, !got2)) break;
-            if (elect) F64_TRACE(n, 5);
+            if (!wait_bar(bar(B_D2FULL), n & 1)) break;
+            if (elect_trace(warp, lane)) F64_TRACE(n, 5);
             tc_fence_after();
             const float4 *gam = reinterpret_cast<const float4 *>(sm + CH_G + s * D * 4) + 16 * kh;
             {
@@ -369,31 +406,16 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                     S[c + 3] = fmaf(g.w, S[c + 3], __uint_as_float(r[c + 3]));
                 }
             }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = pack_bf16(S[32 * q + 2 * j], S[32 * q + 2 * j + 1]);
-                tmem_st16(tmem + lb + TM_AS + 32 * kh + 16 * q, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(1, 256);  // every thread has read gamma^B and stored its state half
-            if (elect) {
-                mbar_arrive(bar(B_FREE + s));
-                F64_TRACE(n, 6);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FREE + s));  // this warp has read gamma^B
+            store_state();
+            if (elect_trace(warp, lane)) F64_TRACE(n, 6);
         }
         if (p.h_final) {
             float *hf = p.h_final + ((size_t)seq * H + head) * D * D;
 #pragma unroll
             for (int c = 0; c < KH; ++c) hf[(size_t)(KH * kh + c) * D + v] = S[c];
         }
-        if (elect) {  // every MMA has completed before the tensor memory is released
-            umma_commit(bar(B_DRAIN));
-            wait_bar(bar(B_DRAIN), 0);
-        }
-        __syncwarp();
     } else {
         regs_set<kRegsOut>();
         // -------------------------------------------------- output warps
@@ -401,18 +423,18 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const size_t tstride = (size_t)H * D;
         for (int n = 0; n < nblocks; ++n) {
-            const int s = n & 1;  // D1 buffer
-            const bool got = wait_bar(bar(B_D1FULL + s), (n >> 1) & 1);
+            const int b = n & 1;  // D1 buffer
+            const bool got = wait_bar(bar(B_D1O + b), (n >> 1) & 1);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
-            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)s;
+            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
             tmem_ld32(d1 + lb + 64u, r0);
             tmem_ld32(d1 + lb + 96u, r1);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_D1FREE + s));
+            if (lane == 0) mbar_arrive(bar(B_D1FREE + b));
             const int L = min(BT, t1 - (t0 + n * BT));
             __nv_bfloat16 *o = p.out + ((size_t)(t0 + n * BT) * H + head) * D + v;
 #pragma unroll
@@ -438,15 +460,33 @@ __device__ __forceinline__ int off_blk(int I, int J) {
     const int d = I - J;
     return d == 1 ? J : (d == 2 ? 3 + J : 5);
 }
-// the six off-diagonal tile pairs (I, J), in off_blk order
+// the six off-diagonal tile pairs (I, J), in the order of the off-diagonal A tiles
 __device__ __constant__ int kOffI[6] = {1, 2, 3, 2, 3, 3};
 __device__ __constant__ int kOffJ[6] = {0, 1, 2, 0, 1, 0};
+// column of the A / P product holding X_IJ, the column tile of pair (I, J <= I): K^_I on
+// the diagonal, K'_J next to it, K'_J scaled by the decays of the tiles in between
+// further out
+__device__ __forceinline__ int ap_column(int I, int J) {
+    if (I == J) return TL * I;
+    if (I - J == 1) return 64 + TL * J;
+    if (I == 2) return 112;
+    return J == 0 ? 128 : 144;
+}
 // a 16 x 16 accumulator (two m16n8 fragments) into a row-major fp32 tile, scaled
 __device__ __forceinline__ void store16(float *dst, const float (&acc)[2][4], float sc, int g, int t4) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         *reinterpret_cast<float2 *>(dst + g * 16 + 8 * nt + 2 * t4) = make_float2(sc * acc[nt][0], sc * acc[nt][1]);
         *reinterpret_cast<float2 *>(dst + (g + 8) * 16 + 8 * nt + 2 * t4) = make_float2(sc * acc[nt][2], sc * acc[nt][3]);
+    }
+}
+// the A fragment of a row-major fp32 16 x 16 tile (row pitch lp), rounded to bf16
+__device__ __forceinline__ void frag_a_f32(uint32_t (&a)[4], const float *L, int lp, int g, int t4) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int row = g + 8 * (q & 1), col = 2 * t4 + 8 * (q >> 1);
+        const float2 v = *reinterpret_cast<const float2 *>(L + row * lp + col);
+        a[q] = pack_bf16(v.x, v.y);
     }
 }
 // acc (16 x 16 as two m16n8 fragments) += L (16 x 16 fp32, row pitch lp) x R (16 x 16
@@ -456,17 +496,36 @@ __device__ __forceinline__ void store16(float *dst, const float (&acc)[2][4], fl
 __device__ __forceinline__ void mma16_f32(float (&acc)[2][4], const float *L, int lp, const float *R,
                                           int rp, int g, int t4) {
     uint32_t a[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int row = g + 8 * (q & 1), col = 2 * t4 + 8 * (q >> 1);
-        const float2 v = *reinterpret_cast<const float2 *>(L + row * lp + col);
-        a[q] = pack_bf16(v.x, v.y);
-    }
+    frag_a_f32(a, L, lp, g, t4);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int n = 8 * nt + g;
         const uint32_t b0 = pack_bf16(R[(2 * t4) * rp + n], R[(2 * t4 + 1) * rp + n]);
         const uint32_t b1 = pack_bf16(R[(2 * t4 + 8) * rp + n], R[(2 * t4 + 9) * rp + n]);
+        mma16816(acc[nt], a, b0, b1);
+    }
+}
+// acc += (A fragment a) x R (16 x 16 fp32, row pitch rp, rounded to bf16)
+__device__ __forceinline__ void mma16_ar(float (&acc)[2][4], const uint32_t (&a)[4], const float *R, int rp,
+                                         int g, int t4) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = 8 * nt + g;
+        const uint32_t b0 = pack_bf16(R[(2 * t4) * rp + n], R[(2 * t4 + 1) * rp + n]);
+        const uint32_t b1 = pack_bf16(R[(2 * t4 + 8) * rp + n], R[(2 * t4 + 9) * rp + n]);
+        mma16816(acc[nt], a, b0, b1);
+    }
+}
+// the same with R a row-major bf16 16 x 16 tile
+__device__ __forceinline__ void mma16_fb(float (&acc)[2][4], const float *L, int lp,
+                                         const unsigned short *R, int g, int t4) {
+    uint32_t a[4];
+    frag_a_f32(a, L, lp, g, t4);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = 8 * nt + g;
+        const uint32_t b0 = (uint32_t)R[(2 * t4) * TL + n] | ((uint32_t)R[(2 * t4 + 1) * TL + n] << 16);
+        const uint32_t b1 = (uint32_t)R[(2 * t4 + 8) * TL + n] | ((uint32_t)R[(2 * t4 + 9) * TL + n] << 16);
         mma16816(acc[nt], a, b0, b1);
     }
 }
@@ -478,17 +537,19 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const int nblocks = (t1 - t0 + BT - 1) / BT;
-    const uint32_t rawfull = sbase + PR_BAR, slotfree = sbase + PR_BAR + 8, mmabar = sbase + PR_BAR + 16;
+    const uint32_t rawfull = sbase + PR_BAR, slotfree = sbase + PR_BAR + 8, mmabar = sbase + PR_BAR + 16,
+                   apbar = sbase + PR_BAR + 24;
     const uint32_t stg = sbase + PR_STG;
-    const int i8 = lane >> 3, r8 = lane & 7, g = lane >> 2, t4 = lane & 3;
-    auto tile = [&](int i) { return sbase + PR_TILES + (uint32_t)(i * TILE_BYTES); };
-    float *AT = reinterpret_cast<float *>(sm + PR_AT);
-    float *XS = reinterpret_cast<float *>(sm + STG_XS);  // 6 warps x 16 x 16 fp32 scratch
-    float *MM = XS + 6 * 256;                             // M = L^-1 N, 6 tiles
-    float *M2 = MM + 6 * 256;                             // M^2: (2,0), (3,1), (3,0)
-    float *TD = M2 + 3 * 256;                             // T_II, 4 tiles
+    const int g = lane >> 2, t4 = lane & 3;
+    unsigned char *X = sm + PR_X;
+    float *AD = reinterpret_cast<float *>(sm + PR_AD);
+    const unsigned short *AO = reinterpret_cast<const unsigned short *>(sm + PR_AO);
+    float *MM = reinterpret_cast<float *>(sm + STG_MM);   // M = L^-1 N, 6 tiles
+    auto M2 = [&](int q) {                                // M^2: (2,0), (3,1), (3,0)
+        return reinterpret_cast<float *>(sm + STG_M2 + 1024 * q);
+    };
+    float *TD = reinterpret_cast<float *>(sm + STG_TD);   // T_II, 4 tiles
     float *GAM = reinterpret_cast<float *>(sm + PR_GAM);
-    float *PRE = reinterpret_cast<float *>(sm + PR_PRE);
 
     // q, k and gate-logit tiles of step m (one thread), beta (warp 15, cp.async)
     auto fetch = [&](int m, int buf) {
@@ -521,10 +582,15 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         bulk_commit();
     };
     fetch(prank, 0);
-    // tensor memory for the W / Q' product; the tiles of TB above the diagonal stay zero
+    // tensor memory for the products. B1 starts at zero: the tiles of TB above the
+    // diagonal are never written, and P' is then exactly zero there too, so every later
+    // P finds zeros above its diagonal tiles. The unused last 32 columns of the column
+    // tiles are zeroed once (their products are never read).
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kProTmemCols);
-    for (int i = tid; i < 8192 / 16; i += kThreads)
+    for (int i = tid; i < 16384 / 16; i += kThreads) {
         reinterpret_cast<uint4 *>(sm + PR_STG + SL_B1)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(X + X_C + 32768)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -542,218 +608,265 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         if (__syncthreads_or(bad)) break;
         if (tid != 0) mbar_try(rawfull, k & 1);  // observe the completed phase
         if (tid == 0) F64_TRACE(m, 9);
-        // ---- P1: gate pass, one (key channel, tile) per thread
+        // ---- P1: gate pass, one (key channel c, tile I) per thread: exp(g) of its 16
+        //      tokens and the inclusive within-tile decay Gamma_r = exp(G_r)
         const int c = tid & (D - 1), I = tid >> 7, rb = TL * I;
-        float kk[TL];
+        float eg[TL], gm[TL];
+        uint32_t kq[TL];  // k_r (low half) and q_r (high half), bf16
         {
             const float *ra = reinterpret_cast<const float *>(sm + PR_A);
-            const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(sm + PR_Q);
-            const __nv_bfloat16 *rk = reinterpret_cast<const __nv_bfloat16 *>(sm + PR_K);
-            float eg[TL], qq[TL];
+            const unsigned short *rq = reinterpret_cast<const unsigned short *>(sm + PR_Q);
+            const unsigned short *rk = reinterpret_cast<const unsigned short *>(sm + PR_K);
 #pragma unroll
             for (int r = 0; r < TL; ++r) eg[r] = ra[(rb + r) * D + c];
 #pragma unroll
             for (int r = 0; r < TL; ++r) eg[r] = __fdividef(1.f, 1.f + __expf(-eg[r]));  // sigmoid
+            float gam = 1.f;
 #pragma unroll
             for (int r = 0; r < TL; ++r) {
                 const bool in = rb + r < L;
                 const float e = __expf(kGMin * eg[r]);  // exp(g), g = -5 sigmoid(a)
                 eg[r] = in ? e : 1.f;
-                qq[r] = in ? __bfloat162float(rq[(rb + r) * D + c]) : 0.f;
-                kk[r] = in ? __bfloat162float(rk[(rb + r) * D + c]) : 0.f;
+                kq[r] = in ? ((uint32_t)rk[(rb + r) * D + c] | ((uint32_t)rq[(rb + r) * D + c] << 16)) : 0u;
+                gam *= eg[r];
+                gm[r] = gam;
             }
-            uint32_t wq[TL / 2], wk[TL / 2];
-            float gam = 1.f;
-#pragma unroll
-            for (int r = 0; r < TL; r += 2) {  // Gamma_r = exp(G_r), inclusive
-                const float g0 = gam * eg[r];
-                const float g1 = g0 * eg[r + 1];
-                gam = g1;
-                wq[r >> 1] = pack_bf16(qq[r] * g0, qq[r + 1] * g1);
-                wk[r >> 1] = pack_bf16(kk[r] * g0, kk[r + 1] * g1);
-            }
-            unsigned char *tq = sm + PR_TILES + (T_QT + I) * TILE_BYTES;
-            unsigned char *tk = sm + PR_TILES + (T_KT + I) * TILE_BYTES;
-            *reinterpret_cast<uint4 *>(tq + cmaj(c, 0)) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-            *reinterpret_cast<uint4 *>(tq + cmaj(c, 8)) = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-            *reinterpret_cast<uint4 *>(tk + cmaj(c, 0)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-            *reinterpret_cast<uint4 *>(tk + cmaj(c, 8)) = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-            GAM[I * D + c] = gam;                  // gamma_I = exp(G_end), >= exp(-80)
-            const float inv = __frcp_rn(gam);      // exp(-G_end) <= exp(80)
-            float sf = 1.f;                        // exp(G_end - G_r)
-            uint32_t wp[TL / 2], wh[TL / 2];
-            float hp = 0.f, hh = 0.f;
-#pragma unroll
-            for (int r = TL - 1; r >= 0; --r) {
-                const float kp = kk[r] * sf, kh = kk[r] * (sf * inv);
-                kk[r] = kp;                        // keep K' for the step-level operands
-                if (r & 1) {
-                    hp = kp;
-                    hh = kh;
-                } else {
-                    wp[r >> 1] = pack_bf16(kp, hp);
-                    wh[r >> 1] = pack_bf16(kh, hh);
-                }
-                sf *= eg[r];
-            }
-            unsigned char *tp = sm + PR_TILES + (T_KP + I) * TILE_BYTES;
-            unsigned char *th = sm + PR_TILES + (T_KH + I) * TILE_BYTES;
-            *reinterpret_cast<uint4 *>(tp + cmaj(c, 0)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-            *reinterpret_cast<uint4 *>(tp + cmaj(c, 8)) = make_uint4(wp[4], wp[5], wp[6], wp[7]);
-            *reinterpret_cast<uint4 *>(th + cmaj(c, 0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4 *>(th + cmaj(c, 8)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+            GAM[I * D + c] = gam;  // gamma_I = exp(G_end), >= exp(-80)
         }
         if (tid == 0) F64_TRACE(m, 20);
-        if (tid == 511) F64_TRACE(m, 21);
-        if (tid == 0) bulk_wait_read0();  // the previous step's copies have read the staging slot
-        if (tid == 0) F64_TRACE(m, 22);
+        if (tid == 511) F64_TRACE(m, 26);
         __syncthreads();
+        fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
         if (tid == 0) F64_TRACE(m, 10);
-        // ---- P2: decays across tiles; K'B into the slot; cross-tile K' tiles
+        // ---- P2: every scaled operand of this (channel, tile), from fp32 values:
+        //   R = [K~ | Q~] (K~ = K Gamma), the column tiles K^ = K / Gamma and
+        //   K' = K gamma / Gamma (and K' scaled by the decays of the tiles after it: Kx),
+        //   K'B = K' prod_{J > I} gamma_J into the slot, gamma^B; K~B and Q~B (x prod_{J < I}
+        //   gamma_J) stay in registers until the A / P product has read X.
+        uint32_t wkb[TL / 2], wqb[TL / 2], wkp[TL / 2];
+        float gB = 0.f;
         {
-            float pre = 1.f, post = 1.f;
+            float pre = 1.f, post = 1.f, gj[NT];
 #pragma unroll
             for (int J = 0; J < NT; ++J) {
-                const float gj = GAM[J * D + c];
-                if (J < I) pre *= gj;
-                if (J > I) post *= gj;
+                gj[J] = GAM[J * D + c];
+                if (J < I) pre *= gj[J];
+                if (J > I) post *= gj[J];
             }
-            PRE[I * D + c] = pre;
-            uint32_t w0[4], w1[4];
-#pragma unroll
-            for (int r = 0; r < 8; r += 2) {
-                w0[r >> 1] = pack_bf16(kk[r] * post, kk[r + 1] * post);
-                w1[r >> 1] = pack_bf16(kk[r + 8] * post, kk[r + 9] * post);
-            }
-            unsigned char *b3 = sm + PR_STG + SL_B3;
-            *reinterpret_cast<uint4 *>(b3 + sw128(c, 16 * I)) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            *reinterpret_cast<uint4 *>(b3 + sw128(c, 16 * I + 8)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            // K' of tile J scaled by the decay of the tiles strictly between J and I:
-            // x0 = K'^0 gamma_1 (pair 2,0), x1 = K'^0 gamma_1 gamma_2 (3,0), x2 = K'^1 gamma_2 (3,1)
-            auto put = [&](int x, float sc) {
-                uint32_t w[8];
-#pragma unroll
-                for (int r = 0; r < TL; r += 2) w[r >> 1] = pack_bf16(kk[r] * sc, kk[r + 1] * sc);
-                unsigned char *tx = sm + PR_TILES + (T_KX + x) * TILE_BYTES;
-                *reinterpret_cast<uint4 *>(tx + cmaj(c, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(tx + cmaj(c, 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+            const float inv = __frcp_rn(gm[TL - 1]);  // exp(-G_end) <= exp(80)
+            auto put2 = [&](unsigned char *base, int col, const uint32_t (&w)[TL / 2]) {
+                *reinterpret_cast<uint4 *>(base + sw128(c, col)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(base + sw128(c, col + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
             };
-            if (I == 0) {
-                const float g1 = GAM[D + c], g2 = GAM[2 * D + c];
-                put(0, g1);
-                put(1, g1 * g2);
-                reinterpret_cast<float *>(sm + PR_STG + SL_G)[c] =
-                    GAM[c] * g1 * g2 * GAM[3 * D + c];  // gamma^B = exp(G^B_end)
-            } else if (I == 1) {
-                put(2, GAM[2 * D + c]);
-            }
-        }
-        fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 11);
-
-        // ---- P3: A = strict_lower(beta K~ X^T) per tile pair (I, J <= I), mma.sync, on all
-        //      16 warps: warp = (row tile I, 8-column half, half of the column tiles J),
-        //      the row operand's fragments loaded once per warp. X is K^ on the diagonal and
-        //      K' scaled by the decays of the tiles in between off it.
-        auto col_tile = [&](int Ii, int Jj) -> uint32_t {
-            int ct;
-            if (Jj == Ii) ct = T_KH + Ii;
-            else if (Ii - Jj == 1) ct = T_KP + Jj;
-            else if (Ii == 2) ct = T_KX + 0;
-            else ct = T_KX + (Jj == 0 ? 1 : 2);
-            return tile(ct);
-        };
-        // rows of tile Ii times X^T for column tiles [j_lo, j_hi], 8-column half nh; the
-        // epilogue gets (Jj, r, j0, v0, v1) for this lane's two adjacent columns
-        auto pair_products = [&](uint32_t rowt, int Ii, int nh, int j_lo, int j_hi, auto &&epi) {
-            uint32_t a[D / 16][4];
+            // token pairs (r, r + 1) as float2: the products below are packed fp32x2 multiplies
+            float2 k2[TL / 2], kp[TL / 2];   // K, and K' = K exp(G_end - G_r) (suffix product of exp(g))
+            {
+                float sf[TL];
+                float acc = 1.f;
 #pragma unroll
-            for (int kt = 0; kt < D / 16; ++kt)
-                ldsm_x4_t(rowt + cmaj(kt * 16 + (i8 >> 1) * 8 + r8, (i8 & 1) * 8), a[kt][0], a[kt][1], a[kt][2], a[kt][3]);
-            for (int Jj = j_lo; Jj <= j_hi; ++Jj) {
-                const uint32_t colt = col_tile(Ii, Jj);
-                float acc[2][4] = {};
-#pragma unroll
-                for (int kp = 0; kp < D / 32; ++kp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(colt + cmaj(kp * 32 + i8 * 8 + r8, nh * 8), b0, b1, b2, b3);
-                    mma16816(acc[0], a[2 * kp], b0, b1);
-                    mma16816(acc[1], a[2 * kp + 1], b2, b3);
+                for (int r = TL - 1; r >= 0; --r) {
+                    sf[r] = acc;
+                    acc *= eg[r];
                 }
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    epi(Jj, g + 8 * hh, nh * 8 + 2 * t4, acc[0][2 * hh] + acc[1][2 * hh],
-                        acc[0][2 * hh + 1] + acc[1][2 * hh + 1]);
+                for (int i = 0; i < TL / 2; ++i) {
+                    k2[i] = make_float2(__uint_as_float(kq[2 * i] << 16), __uint_as_float(kq[2 * i + 1] << 16));
+                    kp[i] = __fmul2_rn(k2[i], make_float2(sf[2 * i], sf[2 * i + 1]));
+                }
             }
-        };
+            const float2 pre2 = make_float2(pre, pre);
+            uint32_t w[TL / 2];
+#pragma unroll
+            for (int i = 0; i < TL / 2; ++i) {
+                const float2 a = __fmul2_rn(k2[i], make_float2(gm[2 * i], gm[2 * i + 1]));  // K~
+                w[i] = pk2(a);
+                wkb[i] = pk2(__fmul2_rn(a, pre2));
+            }
+            put2(X + X_R, rb, w);                                  // K~
+#pragma unroll
+            for (int i = 0; i < TL / 2; ++i) {
+                const float2 q2 = make_float2(__uint_as_float(kq[2 * i] & 0xffff0000u),
+                                              __uint_as_float(kq[2 * i + 1] & 0xffff0000u));
+                const float2 b = __fmul2_rn(q2, make_float2(gm[2 * i], gm[2 * i + 1]));  // Q~
+                w[i] = pk2(b);
+                wqb[i] = pk2(__fmul2_rn(b, pre2));
+            }
+            put2(X + X_R + 16384, rb, w);                          // Q~
+            auto scaled = [&](float sc) {
+                const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+                for (int i = 0; i < TL / 2; ++i) w[i] = pk2(__fmul2_rn(kp[i], s2));
+            };
+            scaled(inv);
+            put2(X + X_C, rb, w);                                  // K^_I
+            if (I < NT - 1) {
+#pragma unroll
+                for (int i = 0; i < TL / 2; ++i) w[i] = pk2(kp[i]);
+                put2(X + X_C + 16384, rb, w);                      // K'_I
+            }
+            {
+                const float2 s2 = make_float2(post, post);
+#pragma unroll
+                for (int i = 0; i < TL / 2; ++i) wkp[i] = pk2(__fmul2_rn(kp[i], s2));  // K'B
+            }
+            if (I == 0) {
+                scaled(gj[1]);
+                put2(X + X_C + 16384, 48, w);                      // Kx_20 = K'_0 gamma_1
+                scaled(gj[1] * gj[2]);
+                put2(X + X_C + 32768, 0, w);                       // Kx_30 = K'_0 gamma_1 gamma_2
+                gB = gj[0] * gj[1] * gj[2] * gj[3];  // gamma^B = exp(G^B_end)
+            } else if (I == 1) {
+                scaled(gj[2]);
+                put2(X + X_C + 32768, 16, w);                      // Kx_31 = K'_1 gamma_2
+            }
+        }
+        if (tid == 0) bulk_wait_read0();  // the previous step's copies have read the staging slot
+        fence_proxy_async();  // generic writes of X -> the tensor core's reads
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) F64_TRACE(m, 11);
+        // ---- P3: [A; P] before masking = [K~; Q~] [column tiles]^T on this CTA's tensor
+        //      core (M = 128 tokens, N = 192 columns, K = 128 channels)
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t da = sdesc_sw128(sbase + PR_X + X_R, 16384, 1024);
+            const uint64_t db = sdesc_sw128(sbase + PR_X + X_C, 16384, 1024);
+            const uint32_t idap = idesc_bf16(128, 192, 1, 1);
+#pragma unroll
+            for (int kk2 = 0; kk2 < 8; ++kk2)  // K = 16 channels per MMA (+2048 bytes)
+                umma_ss(ptmem + TP_AP, da + 128 * kk2, db + 128 * kk2, idap, kk2 > 0);
+            umma_commit(apbar);
+            F64_TRACE(m, 21);
+        }
+        {   // while the product runs: K'B, Q~B ([c][64 t]) and gamma^B into the staging slot
+            // (the previous copy out of it has completed: checked before the barrier above)
+            unsigned char *b3 = sm + PR_STG + SL_B3;
+            *reinterpret_cast<uint4 *>(b3 + sw128(c, rb)) = make_uint4(wkp[0], wkp[1], wkp[2], wkp[3]);
+            *reinterpret_cast<uint4 *>(b3 + sw128(c, rb + 8)) = make_uint4(wkp[4], wkp[5], wkp[6], wkp[7]);
+            unsigned char *qb = sm + PR_STG + SL_B2 + B2_QB;
+            *reinterpret_cast<uint4 *>(qb + sw128(c, rb)) = make_uint4(wqb[0], wqb[1], wqb[2], wqb[3]);
+            *reinterpret_cast<uint4 *>(qb + sw128(c, rb + 8)) = make_uint4(wqb[4], wqb[5], wqb[6], wqb[7]);
+            if (I == 0) reinterpret_cast<float *>(sm + PR_STG + SL_G)[c] = gB;
+        }
         {
-            const int Ii = warp >> 2, nh = (warp >> 1) & 1, hf = warp & 1;
-            const int sp = (Ii + 2) >> 1;
-            const int j_lo = hf ? sp : 0, j_hi = hf ? Ii : sp - 1;
-            if (j_lo <= j_hi)
-                pair_products(tile(T_KT + Ii), Ii, nh, j_lo, j_hi, [&](int Jj, int r, int j0, float v0, float v1) {
-                    const bool diag = Jj == Ii;
-                    const float bb = bet[TL * Ii + r];
-                    *reinterpret_cast<float2 *>(AT + (TL * Ii + r) * BT + TL * Jj + j0) =
-                        make_float2((!diag || j0 < r) ? bb * v0 : 0.f, (!diag || j0 + 1 < r) ? bb * v1 : 0.f);
-                });
+            const bool got = wait_bar(apbar, k & 1);
+            if (tid == 0) F64_TRACE(m, 22);
+            if (__all_sync(0xffffffffu, got)) {
+                tc_fence_after();
+                // K~B (operand of the W product) takes X's place
+                *reinterpret_cast<uint4 *>(X + X_KB + sw128(c, rb)) = make_uint4(wkb[0], wkb[1], wkb[2], wkb[3]);
+                *reinterpret_cast<uint4 *>(X + X_KB + sw128(c, rb + 8)) = make_uint4(wkb[4], wkb[5], wkb[6], wkb[7]);
+                if (tid == 0) F64_TRACE(m, 24);
+                // A (rows 0..63: beta-scaled, strictly lower on the diagonal tiles) and P
+                // (rows 64..127: lower on the diagonal tiles) out of the product's columns.
+                // Warp = (lane quarter q, part); each part takes whole 16-column chunks.
+                const int q = warp & 3, part = warp >> 2;
+                const bool prow = q >= 2;
+                const int Il = 2 * (q & 1) + (lane >> 4), r = lane & 15;
+                int n_ch, I0, J0, I1 = 0, J1 = 0;
+                if ((q & 1) == 0) {  // row tiles 0, 1: chunks (0,0), (1,1), (1,0)
+                    n_ch = part < 3 ? 1 : 0;
+                    I0 = part == 0 ? 0 : 1;
+                    J0 = part == 1 ? 1 : 0;
+                } else {             // row tiles 2, 3: seven chunks over four parts
+                    n_ch = part < 3 ? 2 : 1;
+                    I0 = 2;
+                    J0 = part == 0 ? 2 : (part == 1 ? 1 : (part == 2 ? 0 : 1));
+                    if (part == 3) I0 = 3;
+                    I1 = 3;
+                    J1 = part == 0 ? 3 : (part == 1 ? 2 : 0);
+                }
+                const uint32_t trow = ptmem + TP_AP + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (u < n_ch) {
+                        const int Ic = u == 0 ? I0 : I1, Jc = u == 0 ? J0 : J1;
+                        uint32_t v[16];
+                        tmem_ld16(trow + (uint32_t)ap_column(Ic, Jc), v);
+                        tmem_ld_wait();
+                        if (Il == Ic) {
+                            const bool diag = Ic == Jc;
+                            if (!prow) {
+                                const float b = bet[TL * Ic + r];
+                                auto av = [&](int j) { return (!diag || j < r) ? b * __uint_as_float(v[j]) : 0.f; };
+                                if (diag) {  // column j of A_II, rows p + 4 q at [j][p][q]
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) AD[(Ic * TL + j) * TL + 4 * (r & 3) + (r >> 2)] = av(j);
+                                } else {
+                                    uint32_t w[8];
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) w[j] = pack_bf16(av(2 * j), av(2 * j + 1));
+                                    uint4 *dst = reinterpret_cast<uint4 *>(sm + PR_AO + (off_blk(Ic, Jc) * 256 + r * TL) * 2);
+                                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                                }
+                            } else {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int j = 0; j < 16; j += 2)
+                                    w[j >> 1] = pack_bf16((!diag || j <= r) ? __uint_as_float(v[j]) : 0.f,
+                                                          (!diag || j + 1 <= r) ? __uint_as_float(v[j + 1]) : 0.f);
+                                const int row = BT + TL * Ic + r;
+                                unsigned char *b1 = sm + PR_STG + SL_B1;
+                                *reinterpret_cast<uint4 *>(b1 + sw128(row, TL * Jc)) = make_uint4(w[0], w[1], w[2], w[3]);
+                                *reinterpret_cast<uint4 *>(b1 + sw128(row, TL * Jc + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
+                        }
+                    }
+                }
+            }
+            if (tid == 160) F64_TRACE(m, 23);
+            tc_fence_before();
         }
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 12);
-        // ---- P4, two groups at once.
-        //  Warps 0-5: T = (I + A)^-1, A strictly lower, in 16 x 16 tiles. L = the diagonal
-        //   tiles of I + A, N = the rest, M = L^-1 N (M_IJ = T_II A_IJ, I > J; nilpotent,
-        //   M^4 = 0), so T = (I + M)^-1 L^-1 = (I - M)(I + M^2) L^-1. Diagonal tiles T_II:
-        //   fp32 forward substitution, one column per thread. Products of tiles: tensor
-        //   cores, operands rounded to bf16. TB = T diag(beta) goes to rows 0..63 of B1 as
-        //   each tile is done (the tiles above the diagonal stay 0).
-        //  Warps 6-15: the next step's raw tiles requested; P = lower(Q~ X^T) into rows
-        //   64..127 of B1 (zero above the diagonal tiles); then K~B = K~^I Gamma_I and
-        //   Q~B = Q~^I Gamma_I ([c][64 t], 128-byte swizzle) over the K^ / K' tiles.
-        if (warp < 6) {
-            constexpr int kSolveThreads = 192;
-            if (tid < 64) {
-                const int Id = tid >> 4, j = tid & 15;
-                const float *Ar = AT + (TL * Id) * BT + TL * Id;
-                float x[TL];
+        // ---- P4 (warps 0-5): T = (I + A)^-1, A strictly lower, in 16 x 16 tiles. L = the
+        //   diagonal tiles of I + A, N = the rest, M = L^-1 N (M_IJ = T_II A_IJ, I > J;
+        //   nilpotent, M^4 = 0), so T = (I + M)^-1 L^-1 = (I - M)(I + M^2) L^-1. Diagonal
+        //   tiles T_II: fp32 forward substitution, one column per thread. Products of
+        //   tiles: tensor cores, operands rounded to bf16. TB = T diag(beta) goes to rows
+        //   0..63 of B1 as each tile is done (the tiles above the diagonal stay 0).
+        if (warp < 8) {
+            constexpr int kSolveThreads = 256;
+            {
+                // column j of T_II = (I + A_II)^-1, right-looking: once x_i is final (in the
+                // thread owning row i) it is broadcast to the column's four threads, each of
+                // which folds it into its rows p, p + 4, p + 8, p + 12
+                const int Id = tid >> 6, j = (tid >> 2) & 15, pr = tid & 3;
+                const float *Ac = AD + Id * TL * TL + 4 * pr;  // column i: Ac[16 i + q] = A[pr + 4q][i]
+                float x[4];
 #pragma unroll
-                for (int r = 0; r < TL; ++r) {
-                    // row r of A_II as four 16-byte loads, independent of the solve so far
-                    float ar[TL];
+                for (int q = 0; q < 4; ++q) x[q] = pr + 4 * q == j ? 1.f : 0.f;
 #pragma unroll
-                    for (int q = 0; q < (r + 3) / 4; ++q) {
-                        const float4 v4 = *reinterpret_cast<const float4 *>(Ar + r * BT + 4 * q);
-                        ar[4 * q] = v4.x; ar[4 * q + 1] = v4.y; ar[4 * q + 2] = v4.z; ar[4 * q + 3] = v4.w;
-                    }
-                    float a0 = r == j ? 1.f : 0.f, a1 = 0.f;
+                for (int i = 0; i < TL - 1; ++i) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Ac + TL * i);
+                    const float xi = __shfl_sync(0xffffffffu, x[i >> 2], (lane & ~3) | (i & 3));
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                    for (int i = 0; i < r; i += 2) {
-                        a0 = fmaf(-ar[i], x[i], a0);
-                        if (i + 1 < r) a1 = fmaf(-ar[i + 1], x[i + 1], a1);
-                    }
-                    x[r] = a0 + a1;
+                    for (int q = 0; q < 4; ++q)
+                        if (4 * q + 3 >= i + 1)  // some of this q's rows can lie below i
+                            x[q] = pr + 4 * q > i ? fmaf(-av[q], xi, x[q]) : x[q];
                 }
                 const float bj = bet[TL * Id + j];
 #pragma unroll
-                for (int r = 0; r < TL; ++r) {
-                    TD[(Id * TL + r) * TL + j] = x[r];
+                for (int q = 0; q < 4; ++q) {
+                    const int r = pr + 4 * q;
+                    TD[(Id * TL + r) * TL + j] = x[q];
                     *reinterpret_cast<__nv_bfloat16 *>(sm + PR_STG + SL_B1 + sw128(TL * Id + r, TL * Id + j)) =
-                        __float2bfloat16_rn(x[r] * bj);
+                        __float2bfloat16_rn(x[q] * bj);
                 }
             }
             named_sync(2, kSolveThreads);
             if (tid == 0) F64_TRACE(m, 16);
-            {   // M_IJ = T_II A_IJ for the six pairs I > J (one warp each)
-                const int Ir = kOffI[warp], Jc = kOffJ[warp];
+            if (warp < 6) {   // M_IJ = T_II A_IJ for the six pairs I > J (one warp each)
+                const int Ir = kOffI[warp];
                 float acc[2][4] = {};
-                mma16_f32(acc, TD + Ir * 256, TL, AT + (TL * Ir) * BT + TL * Jc, BT, g, t4);
+                mma16_fb(acc, TD + Ir * 256, TL, AO + warp * 256, g, t4);
                 store16(MM + warp * 256, acc, 1.f, g, t4);
             }
             named_sync(2, kSolveThreads);
             if (tid == 0) F64_TRACE(m, 17);
-            // M^2: (2,0) = M21 M10, (3,1) = M32 M21, (3,0) = M31 M10 + M32 M20; meanwhile warps
-            // 3-5 write the constant [0; -I] operand tile over A (no longer read)
+            // M^2: (2,0) = M21 M10, (3,1) = M32 M21, (3,0) = M31 M10 + M32 M20
             if (warp < 3) {
                 float acc[2][4] = {};
                 if (warp == 0) mma16_f32(acc, MM + 1 * 256, TL, MM + 0 * 256, TL, g, t4);
@@ -762,32 +875,18 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                     mma16_f32(acc, MM + 4 * 256, TL, MM + 0 * 256, TL, g, t4);
                     mma16_f32(acc, MM + 2 * 256, TL, MM + 3 * 256, TL, g, t4);
                 }
-                store16(M2 + warp * 256, acc, 1.f, g, t4);
-            } else {
-                // 128 rows x 64 k, row n >= 64 holds -1 at k = n - 64; 32 bytes per slot
-                for (int e = tid - 96; e < 512; e += 96) {
-                    const int n = e >> 2, q0 = 2 * (e & 3);
-#pragma unroll
-                    for (int q = q0; q < q0 + 2; ++q) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const int k0 = 8 * q + 2 * h;
-                            w[h] = pack_bf16(n - 64 == k0 ? -1.f : 0.f, n - 64 == k0 + 1 ? -1.f : 0.f);
-                        }
-                        *reinterpret_cast<uint4 *>(sm + PR_AT + sw128(n, 8 * q)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
+                store16(M2(warp), acc, 1.f, g, t4);
             }
             named_sync(2, kSolveThreads);
             if (tid == 0) F64_TRACE(m, 18);
-            {   // T_IJ = [-(M)_IJ + (M^2)_IJ - (M^3)_IJ] T_JJ, M^3 only at (3,0) = M32 (M^2)_20;
-                // TB_IJ = T_IJ diag(beta_J) straight into B1
+            if (warp < 6) {   // T_IJ = [-(M)_IJ + (M^2)_IJ - (M^3)_IJ] T_JJ, M^3 only at (3,0) = M32 (M^2)_20;
+                // TB_IJ = T_IJ diag(beta_J) straight into B1. The left factor is formed in
+                // the accumulator layout, which is also the A-fragment layout of a 16 x 16.
                 const int Ir = kOffI[warp], Jc = kOffJ[warp];
-                float *ls = XS + warp * 256;  // this warp's left operand
                 const int q2 = (Ir == 2 && Jc == 0) ? 0 : (Ir == 3 && Jc == 1) ? 1 : (Ir == 3 && Jc == 0) ? 2 : -1;
                 float c3[2][4] = {};
-                if (q2 == 2) mma16_f32(c3, MM + 2 * 256, TL, M2 + 0 * 256, TL, g, t4);
+                if (q2 == 2) mma16_f32(c3, MM + 2 * 256, TL, M2(0), TL, g, t4);
+                uint32_t la[4];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -797,17 +896,16 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                         v2.x = -v2.x;
                         v2.y = -v2.y;
                         if (q2 >= 0) {
-                            const float2 w2 = *reinterpret_cast<const float2 *>(M2 + q2 * 256 + row * TL + col);
+                            const float2 w2 = *reinterpret_cast<const float2 *>(M2(q2) + row * TL + col);
                             v2.x += w2.x;
                             v2.y += w2.y;
                         }
                         v2.x -= c3[nt][2 * h];
                         v2.y -= c3[nt][2 * h + 1];
-                        *reinterpret_cast<float2 *>(ls + row * TL + col) = v2;
+                        la[2 * nt + h] = pack_bf16(v2.x, v2.y);
                     }
-                __syncwarp();
                 float acc[2][4] = {};
-                mma16_f32(acc, ls, TL, TD + Jc * 256, TL, g, t4);
+                mma16_ar(acc, la, TD + Jc * 256, TL, g, t4);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int col = TL * Jc + 8 * nt + 2 * t4;
@@ -818,139 +916,39 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                         pack_bf16(acc[nt][2] * b0, acc[nt][3] * b1);
                 }
             }
-        } else {
-            constexpr int kAuxThreads = 320;
-            if (warp == 15) fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
-            // P in 14 units of at most two column tiles on warps 6-15 (unit = row tile I,
-            // 8-column half, part of the column tiles); warps 6-11 take one two-tile unit,
-            // warps 12-15 two one-tile units
-            auto p_unit = [&](int Ii, int nh, int j_lo, int j_hi) {
-                pair_products(tile(T_QT + Ii), Ii, nh, j_lo, j_hi, [&](int Jj, int r, int j0, float v0, float v1) {
-                    const bool diag = Jj == Ii;
-                    *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 + sw128(BT + TL * Ii + r, TL * Jj + j0)) =
-                        pack_bf16((!diag || j0 <= r) ? v0 : 0.f, (!diag || j0 + 1 <= r) ? v1 : 0.f);
-                });
-            };
-            const int w6 = warp - 6;
-            if (w6 < 6) {  // (3, nh, J 0-1), (3, nh, J 2-3), (2, nh, J 0-1)
-                const int nh = w6 & 1, u = w6 >> 1;
-                if (u == 0) p_unit(3, nh, 0, 1);
-                else if (u == 1) p_unit(3, nh, 2, 3);
-                else p_unit(2, nh, 0, 1);
-            } else {       // (2, nh, J 2) + (0, nh, J 0), (1, nh, J 0) + (1, nh, J 1)
-                const int nh = w6 & 1, u = (w6 - 6) >> 1;
-                if (u == 0) {
-                    p_unit(2, nh, 2, 2);
-                    p_unit(0, nh, 0, 0);
-                } else {
-                    p_unit(1, nh, 0, 0);
-                    p_unit(1, nh, 1, 1);
-                }
-            }
-            // tiles above the diagonal: zero (rows of tile I = w6 >> 1 for w6 < 8, both halves)
-            if (w6 < 8) {
-                const int Ii = w6 >> 1, nh = w6 & 1;
-                for (int Jj = Ii + 1; Jj < NT; ++Jj)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-                        *reinterpret_cast<uint32_t *>(sm + PR_STG + SL_B1 +
-                                                      sw128(BT + TL * Ii + g + 8 * hh, TL * Jj + nh * 8 + 2 * t4)) = 0u;
-            }
-            named_sync(3, kAuxThreads);  // every read of the K^ / K' tiles is done
-            // K~B and Q~B over the K^ and K' tiles
-            for (int e = tid - 192; e < NT * D; e += kAuxThreads) {
-                const int cc = e & (D - 1), Ie = e >> 7;
-                const float gpre = PRE[Ie * D + cc];
-#pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    const unsigned char *src = sm + PR_TILES + ((which ? T_QT : T_KT) + Ie) * TILE_BYTES;
-                    unsigned char *dst = sm + (which ? PR_QB : PR_KB);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(src + cmaj(cc, 8 * h));
-                        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const __nv_bfloat162 b2v = *reinterpret_cast<const __nv_bfloat162 *>(&in[q]);
-                            o[q] = pack_bf16(__low2float(b2v) * gpre, __high2float(b2v) * gpre);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + sw128(cc, TL * Ie + 8 * h)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
-            }
+            if (tid == 0) F64_TRACE(m, 27);
         }
-        fence_proxy_async();  // B1, K~B, Q~B and [0; -I]: generic writes -> tensor-core reads
+        fence_proxy_async();  // B1 and X: generic writes -> tensor-core reads
         tc_fence_before();
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 13);
-        // ---- P5: P' = P TB on this CTA's tensor core: A = B1 ([TB; P], K = 64 tokens),
-        //      B = TB read MN-major from the same rows 0..63; rows 64..127 of the result
-        //      go back into rows 64..127 of B1
+        // ---- P5: W = TB K~B on this CTA's tensor core (A = B1: rows 0..63 TB, rows 64..127
+        //      P, whose products are not read; N = 128 channels, K = 64 tokens); B2 bytes
+        //      0..16383 = -W
         if (tid == 0) {
             tc_fence_after();
-            const uint64_t da = sdesc_sw128(stg + SL_B1, 16, 1024), db = sdesc_sw128(stg + SL_B1, 8192, 1024);
-            const uint32_t idp = idesc_bf16(128, 64, 0, 1);
+            const uint64_t da = sdesc_sw128(stg + SL_B1, 16, 1024), db = sdesc_sw128(sbase + PR_X + X_KB, 16, 1024);
+            const uint32_t idk = idesc_bf16(128, 128, 0, 0);
 #pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem + 128u, da + 2 * kk2, db + 128 * kk2, idp, kk2 > 0);
+            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem + TP_WQ, da + 2 * kk2, db + 2 * kk2, idk, kk2 > 0);
             umma_commit(mmabar);
         }
-        if ((warp & 3) >= 2 && warp < 8) {  // lane quarters 2 and 3: rows 64..127
-            const bool got = wait_bar(mmabar, 0);
+        if ((warp & 3) < 2) {  // lane quarters 0 and 1: rows 0..63; 32 channels per warp
+            const bool got = wait_bar(mmabar, k & 1);
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
-                const int n = ((warp & 3) << 5) + lane, ch = warp >> 2;  // row, 32-column half
+                const int n = ((warp & 3) << 5) + lane, part = warp >> 2;
                 uint32_t r[32];
-                tmem_ld32(ptmem + 128u + ((uint32_t)((warp & 3) * 32) << 16) + 32u * ch, r);
+                tmem_ld32(ptmem + TP_WQ + ((uint32_t)((warp & 3) * 32) << 16) + 32u * part, r);
                 tmem_ld_wait();
+                unsigned char *dst = sm + PR_STG + SL_B2 + (part >> 1) * 8192;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h)
-                        w[h] = pack_bf16(__uint_as_float(r[8 * c8 + 2 * h]), __uint_as_float(r[8 * c8 + 2 * h + 1]));
-                    *reinterpret_cast<uint4 *>(sm + PR_STG + SL_B1 + sw128(n, 32 * ch + 8 * c8)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            tc_fence_before();
-        }
-        fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 14);
-        // ---- P6: [W; -Q'] = [TB | 0; P' | -I] [K~B; Q~B] (M = 128, N = 128 channels, K = 128)
-        //      on this CTA's tensor core; B2 = -(that), rows 0..63 -W, 64..127 Q'.
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t da1 = sdesc_sw128(stg + SL_B1, 16, 1024), da2 = sdesc_sw128(sbase + PR_AT, 16, 1024);
-            const uint64_t db1 = sdesc_sw128(sbase + PR_KB, 16, 1024), db2 = sdesc_sw128(sbase + PR_QB, 16, 1024);
-            const uint32_t idk = idesc_bf16(128, 128, 0, 0);
-#pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem, da1 + 2 * kk2, db1 + 2 * kk2, idk, kk2 > 0);
-#pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem, da2 + 2 * kk2, db2 + 2 * kk2, idk, 1);
-            umma_commit(mmabar);
-        }
-        if (warp < 8) {
-            const bool got = wait_bar(mmabar, 1);
-            if (__all_sync(0xffffffffu, got)) {
-                tc_fence_after();
-                const int n = ((warp & 3) << 5) + lane, ch = warp >> 2;  // row, 64-channel half
-                const uint32_t ta = ptmem + ((uint32_t)((warp & 3) * 32) << 16) + 64u * ch;
-                unsigned char *dst = sm + PR_STG + SL_B2 + ch * 16384;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t r[32];
-                    tmem_ld32(ta + 32u * q, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h)
-                            w[h] = pack_bf16(-__uint_as_float(r[8 * c8 + 2 * h]), -__uint_as_float(r[8 * c8 + 2 * h + 1]));
-                        *reinterpret_cast<uint4 *>(dst + sw128(n, 32 * q + 8 * c8)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                        w[h] = pack_bf16(-__uint_as_float(r[8 * c8 + 2 * h]), -__uint_as_float(r[8 * c8 + 2 * h + 1]));
+                    *reinterpret_cast<uint4 *>(dst + sw128(n, 32 * (part & 1) + 8 * c8)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             tc_fence_before();
@@ -958,7 +956,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         fence_proxy_async();  // generic writes of the staging slot -> the bulk copy's reads
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 15);
-        // ---- P8: into the chain CTA's slot m % NSLOT once step m - NSLOT has consumed it
+        // ---- P6: into the chain CTA's slot m % NSLOT once step m - NSLOT has consumed it
         if (tid == 0 && !bad) {
             if (m >= NSLOT) {
                 bad = !wait_bar(slotfree, nfree & 1);
@@ -971,7 +969,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     if (tid == 0) {
         bulk_wait_read0();  // no copy may still read this CTA's memory at exit
         umma_commit(mmabar);  // and every product has completed before the tensor memory goes
-        wait_bar(mmabar, 0);    // two commits per step: this is an even-numbered phase
+        wait_bar(mmabar, k & 1);  // one commit per step before this one
     }
     if (warp == 15) cp_async_wait0();
     tc_fence_before();
@@ -999,18 +997,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rank == 0) {
             for (int s = 0; s < NSLOT; ++s) {
                 mbar_init(sbase + CH_BAR + 8u * (B_FULL + s), 1);
-                mbar_init(sbase + CH_BAR + 8u * (B_FREE + s), 2);
+                mbar_init(sbase + CH_BAR + 8u * (B_FREE + s), 1 + 8);
             }
             for (int b = 0; b < 2; ++b) {
-                mbar_init(sbase + CH_BAR + 8u * (B_D1FULL + b), 1);
+                mbar_init(sbase + CH_BAR + 8u * (B_D1U + b), 1);
+                mbar_init(sbase + CH_BAR + 8u * (B_D1O + b), 1);
                 mbar_init(sbase + CH_BAR + 8u * (B_D1FREE + b), 4);
             }
             mbar_init(sbase + CH_BAR + 8u * B_D2FULL, 1);
             mbar_init(sbase + CH_BAR + 8u * B_DRAIN, 1);
+            mbar_init(sbase + CH_BAR + 8u * B_SREADY, 8);
+            mbar_init(sbase + CH_BAR + 8u * B_UREADY, 8);
         } else {
             mbar_init(sbase + PR_BAR, 1);
             mbar_init(sbase + PR_BAR + 8, 1);
             mbar_init(sbase + PR_BAR + 16, 1);
+            mbar_init(sbase + PR_BAR + 24, 1);
         }
         mbar_init_fence();
     }

@@ -216,6 +216,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t *r) {
         "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : KDA_R8(0), KDA_R8(8), KDA_R8(16), KDA_R8(24) : "r"(ta));
 }
+// 16 consecutive columns of this thread's tensor-memory lane (warp-collective)
+__device__ __forceinline__ void tmem_ld16(uint32_t ta, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : KDA_R8(0), KDA_R8(8) : "r"(ta));
+}
 __device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t *r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"

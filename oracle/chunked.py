@@ -142,9 +142,11 @@ def chunked_forward(q, k, v, a, beta, h0=None, cu_seqlens=None, *, g_min=-5.0,
 # the start state and V only (not on U).
 # ---------------------------------------------------------------------------------
 
-def block_step(q, k, v, a, beta, S, *, g_min=-5.0, scale=None, tile=C_DEFAULT):
+def block_step(q, k, v, a, beta, S, *, g_min=-5.0, scale=None, tile=C_DEFAULT, form="qs_pu"):
     """One serial step over B = q.shape[0] tokens (a multiple of ``tile``), rows past the
-    sequence already padded (q = k = v = 0, beta = 0, a = -inf). Returns (O, S_next)."""
+    sequence already padded (q = k = v = 0, beta = 0, a = -inf). Returns (O, S_next).
+    ``form`` picks one of two equal ways of writing the output: "qs_pu" =
+    scale (Q~B S + P U), "pv_qs" = scale (P' V + Q' S) with P' = P TB, Q' = Q~B - P W."""
     B, dk = q.shape
     if scale is None:
         scale = dk ** -0.5
@@ -191,10 +193,15 @@ def block_step(q, k, v, a, beta, S, *, g_min=-5.0, scale=None, tile=C_DEFAULT):
     gamB = pre
     KtB, QtB, KpB = (np.concatenate(x, axis=0) for x in (KtB, QtB, KpB))
     W = TB @ KtB
-    Qp = QtB - P @ W
-    Pp = P @ TB
     U = TB @ v - W @ S
-    O = scale * (Pp @ v + Qp @ S)
+    if form == "qs_pu":
+        O = scale * (QtB @ S + P @ U)
+    elif form == "pv_qs":
+        Qp = QtB - P @ W
+        Pp = P @ TB
+        O = scale * (Pp @ v + Qp @ S)
+    else:
+        raise ValueError(f"unknown output form {form!r}")
     S_next = gamB[:, None] * S + KpB.T @ U
     return O, S_next
 

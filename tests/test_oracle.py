@@ -151,6 +151,24 @@ def test_block_steps_of_64_tokens_equal_recurrence(T, gate):
     assert np.isfinite(o).all() and np.isfinite(hf).all()
 
 
+def test_block_step_output_forms_agree():
+    """scale (Q~B S + P U) and scale (P' V + Q' S) are the same output: one step from a
+    random state, and whole runs of steps, against the recurrence."""
+    from oracle.chunked import block_step
+    rng = np.random.default_rng(44)
+    B, dk, dv = 64, 8, 6
+    q, k, v = rng.standard_normal((B, dk)), rng.standard_normal((B, dk)), rng.standard_normal((B, dv))
+    a, beta = rng.normal(0.0, 2.0, (B, dk)), rng.uniform(0.1, 0.9, B)
+    S = rng.standard_normal((dk, dv))
+    o1, s1 = block_step(q, k, v, a, beta, S, form="qs_pu")
+    o2, s2 = block_step(q, k, v, a, beta, S, form="pv_qs")
+    assert P.rel(o1, o2) < 1e-12 and P.rel(s1, s2) < 1e-12
+    # the step from S equals the recurrence from h0 = S
+    o_ref, h_ref = recurrence.kda_forward(q[:, None], k[:, None], v[:, None], a[:, None], beta[:, None],
+                                          S[None, None], [0, B])
+    assert P.rel(o1, o_ref[:, 0]) < 1e-12 and P.rel(s1, h_ref[0, 0]) < 1e-12
+
+
 def test_doubling_inverse_is_exact():
     rng = np.random.default_rng(11)
     for _ in range(5):
