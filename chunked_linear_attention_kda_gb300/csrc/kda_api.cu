@@ -181,6 +181,41 @@ __global__ void piece_offsets_kernel(const int32_t *__restrict__ cu, int32_t *__
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// The pipelined forward's two side streams and three events, made once per (host thread,
+// device) and kept for the thread's lifetime (creating and destroying them on every call
+// put driver work on the timed path); they are released with the CUDA context. Reusing
+// them across calls is safe: each call starts both streams behind the caller's stream
+// and ends by making the caller's stream wait for both.
+struct SideStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+};
+
+cudaError_t side_streams(SideStreams **out) {
+    thread_local std::vector<std::pair<int, SideStreams>> per_device;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (auto &pd : per_device)
+        if (pd.first == dev) {
+            *out = &pd.second;
+            return cudaSuccess;
+        }
+    SideStreams ss;
+    e = cudaStreamCreateWithFlags(&ss.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ss.out, cudaStreamNonBlocking);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        for (cudaEvent_t x : ss.ev) if (x) cudaEventDestroy(x);
+        if (ss.in) cudaStreamDestroy(ss.in);
+        if (ss.out) cudaStreamDestroy(ss.out);
+        return e;
+    }
+    per_device.emplace_back(dev, ss);
+    *out = &per_device.back().second;
+    return cudaSuccess;
+}
+
 size_t pipeline_workspace(int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
                           int32_t n_segments) {
     // two carried states, then the pieces' offset tables: at most 3 pieces per segment,
@@ -671,20 +706,16 @@ kda_status kda_chunk_fwd_from_host_pipelined(
     }
 
     cudaStream_t st = (cudaStream_t)stream, s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // start, inputs landed, piece done
-    struct Release {  // streams and events are freed once their queued work completes
-        cudaStream_t *a, *b; cudaEvent_t *e;
-        ~Release() {
-            for (int i = 0; i < 3; ++i) if (e[i]) cudaEventDestroy(e[i]);
-            if (*a) cudaStreamDestroy(*a);
-            if (*b) cudaStreamDestroy(*b);
-        }
-    } release{&s_in, &s_out, ev};
-    cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
-    if (e != cudaSuccess) return launched(e, "pipeline stream or event creation");
+    cudaEvent_t *ev = nullptr;  // start, inputs landed, piece done
+    {
+        SideStreams *ss = nullptr;
+        cudaError_t e = side_streams(&ss);
+        if (e != cudaSuccess) return launched(e, "pipeline stream or event creation");
+        s_in = ss->in;
+        s_out = ss->out;
+        ev = ss->ev;
+    }
+    cudaError_t e = cudaSuccess;
     // from here on, every return first makes the caller's stream wait for both side
     // streams, so nothing queued on them outlives the call's ordering
     auto finish = [&](kda_status r) {

@@ -406,9 +406,11 @@ kda_status kda_chunk_fwd_from_host(
  *                  kda_chunk_fwd_pipelined_workspace_bytes(n_seq, n_heads, d_k, d_v,
  *                  n_segments) bytes: two carried states and the pieces' sequence
  *                  offsets. Owned by the caller; nothing in it has to be initialised.
- * The call creates two streams and three events, released once their queued work is done;
- * it allocates no memory and launches one small kernel (the pieces' offsets) besides the
- * forward kernels. `stream` waits for the last copy before its next work. The host
+ * The first call from a host thread on a device creates two streams and three events for
+ * that (thread, device); later calls reuse them, and they are released with the CUDA
+ * context. The current device (cudaGetDevice) must own every device pointer and
+ * `stream`. The call allocates no device memory and launches one small kernel (the
+ * pieces' offsets) besides the forward kernels. `stream` waits for the last copy before its next work. The host
  * buffers must stay valid until then. Errors as for kda_chunk_fwd_from_host, plus
  * KDA_ERR_INVALID_ARG for n_segments outside [1, 64], a too-small or misaligned
  * workspace, or a host_cu_seqlens that does not start at 0, decreases, or does not end
