@@ -978,6 +978,78 @@ def run_projection(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ gated forward
+
+def run_gated(args):
+    """The forward fed by the gate projection (``kda_chunk_fwd_gated``) on the 64K workload
+    with d_model = 4096, against the projection GEMM and the forward run back to back."""
+    import torch
+    import chunked_linear_attention_kda_gb300 as kda
+    import kda_inputs as K
+    dev = torch.device("cuda", 0)
+    lib = kda.load_library(build_if_missing=True)
+    x = K.make_workload(3, dev)
+    D, H = PROJ_D, x.n_heads
+    g = torch.Generator(device="cpu").manual_seed(78)
+    xx = torch.randn((x.n_tok, D), generator=g).to(dev, torch.bfloat16)
+    w = (torch.randn((H * x.d_k, D), generator=g) * D ** -0.5).to(dev, torch.bfloat16)
+    b = torch.randn((H * x.d_k,), generator=g).to(dev)
+    a = torch.empty((x.n_tok, H, x.d_k), dtype=torch.float32, device=dev)
+    out = torch.empty((x.n_tok, H, x.d_v), dtype=x.dtype, device=dev)
+    hf = torch.empty((x.n_seq, H, x.d_k, x.d_v), dtype=torch.float32, device=dev)
+    seg = args.segment_tokens
+    ws = torch.empty(lib.kda_chunk_fwd_gated_workspace_bytes(x.n_seq, H, x.d_k, x.d_v, seg),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def separate():
+        kda.gate_projection(xx, w, b, out=a.view(x.n_tok, H * x.d_k))
+        kda.chunk_fwd(x.q, x.k, x.v, a, x.beta, x.h0, x.cu_seqlens, out=out, h_final=hf)
+
+    def fused():
+        kda.chunk_fwd_gated(xx, w, b, x.q, x.k, x.v, x.beta, x.h0, x.cu_seqlens, segment_tokens=seg,
+                            out=out, h_final=hf, workspace=ws)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        n0 = kda.kernel_launch_count()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps, (kda.kernel_launch_count() - n0), clk.summary()
+
+    ms_sep, l_sep, _ = timed(separate)
+    o_sep = out.clone()
+    ms_fused, l_fused, clocks = timed(fused)
+    same = bool(torch.equal(out, o_sep))
+    a_bytes = x.n_tok * H * x.d_k * 4
+    fwd_bytes = algorithmic_bytes(x) - x.n_tok * H * (4 * x.d_k)   # the forward without a
+    line = {"metric": "KDA forward with the gate projection fused (tokens/s)",
+            "value": round(x.n_tok * args.steps / (ms_fused * args.steps * 1e-3), 1),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_fused, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"gated-{x.name}-dmodel{D}", "tokens": x.n_tok, "heads": H,
+                       "d_model": D, "segment_tokens": seg,
+                       "workspace_bytes": int(ws.numel())},
+            "separate_ms_per_step": round(ms_sep, 4),
+            "separate": "kda_gate_projection (a written, 1 GiB fp32) then kda_chunk_fwd (a read)",
+            "bitwise_equal_to_separate": same,
+            "gate_logit_bytes_not_materialised": a_bytes,
+            "hbm_bytes_algorithmic": {"separate": int(fwd_bytes + 2 * a_bytes + xx.numel() * 2 +
+                                                      w.numel() * 2),
+                                      "fused": int(fwd_bytes + xx.numel() * 2 + w.numel() * 2)},
+            "gpu_launches": int(l_fused), "gpu_launches_separate": int(l_sep), "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ contrast variants
 
 def run_contrast(args):
@@ -1080,15 +1152,25 @@ def main():
                     help="with the default workload, skip the 256K and packed-1M lines "
                          "reported under 'workloads'")
     ap.add_argument("--op", default="forward",
-                    choices=["forward", "decode", "backward", "contrast", "projection"],
+                    choices=["forward", "decode", "backward", "contrast", "projection", "gated"],
                     help="forward: the chunked forward pass (default); decode: the "
                          "recurrent decode step; backward: the backward pass; contrast: "
                          "the unbounded-gate and position-pair variants; projection: "
-                         "the gate projection GEMM")
+                         "the gate projection GEMM; gated: the forward fed by the projection "
+                         "(kda_chunk_fwd_gated) against the two run back to back")
+    ap.add_argument("--segment-tokens", type=int, default=4096,
+                    help="segment length of --op gated")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.op == "projection":
+    if args.op == "gated":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the gated line compares entry points of this library only"}),
+                  flush=True)
+        else:
+            run_gated(args)
+    elif args.op == "projection":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               "the projection line has no reference arm"}), flush=True)

@@ -26,6 +26,7 @@ __all__ = ["validate_cu_seqlens", "count_nonfinite", "chunk_fwd", "chunk_fwd_sim
            "affine_combine",
            "segmented_fwd", "decode_step", "chunk_bwd", "chunk_bwd_static_scratch",
            "bwd_timing_start", "bwd_timing_read", "chunk_fwd_variant", "gate_projection",
+           "chunk_fwd_gated",
            "load_library",
            "kernel_launch_count", "read_device_flags", "selftest_bounded_wait",
            "library_path", "KDAError", "EXPORTED_SYMBOLS", "STATUS"]
@@ -42,7 +43,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_bwd_timing_read", "kda_chunk_fwd_variant", "kda_gate_projection",
                     "kda_chunk_fwd_from_host_pipelined", "kda_chunk_fwd_pipelined_workspace_bytes",
                     "kda_chunk_fwd_pipeline_plan", "kda_validate_cu_seqlens",
-                    "kda_count_nonfinite", "kda_check_outputs")
+                    "kda_count_nonfinite", "kda_check_outputs",
+                    "kda_chunk_fwd_gated_workspace_bytes", "kda_chunk_fwd_gated")
 
 _lock = threading.Lock()
 _lib = None
@@ -129,6 +131,12 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_check_outputs.argtypes = [P, I64, ctypes.c_int, P, I64, P,
                                           ctypes.POINTER(ctypes.c_uint64), P]
         lib.kda_check_outputs.restype = ctypes.c_int
+        lib.kda_chunk_fwd_gated_workspace_bytes.argtypes = [I32, I32, I32, I32, I32]
+        lib.kda_chunk_fwd_gated_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_chunk_fwd_gated.argtypes = [P, P, P, I32] + [P] * 7 + [P, P, P, ctypes.c_size_t,
+                                                                      I64, I32, I32, I32, I32, I32,
+                                                                      ctypes.c_int, P]
+        lib.kda_chunk_fwd_gated.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -235,6 +243,56 @@ def gate_projection(x, weight, bias=None, *, out=None):
     _check(lib, lib.kda_gate_projection(_ptr(x), _ptr(weight), _ptr(bias), _ptr(out), N, D, n_out,
                                         ctypes.c_void_p(stream)))
     return out
+
+
+def chunk_fwd_gated(x, w_gate, b_gate, q, k, v, beta, h0=None, cu_seqlens=None, *,
+                    segment_tokens=4096, out=None, h_final=None, output_final_state=True,
+                    workspace=None):
+    """The forward pass fed by the gate projection through ``kda_chunk_fwd_gated``: equal
+    to ``chunk_fwd(q, k, v, gate_projection(x, w_gate, b_gate).view(N, H, d_k), ...)``, bit
+    for bit, without the whole gate-logit tensor (per ``segment_tokens`` segment, the
+    segment's logits go into one workspace slot and are consumed at once). ``x`` [N,
+    d_model] bf16, ``w_gate`` [H * d_k, d_model] bf16, ``b_gate`` [H * d_k] fp32 or None;
+    the rest as ``chunk_fwd`` (bf16). Returns ``(out, h_final)``."""
+    import torch
+    lib = load_library()
+    if q.device.type != "cuda":
+        raise ValueError("chunk_fwd_gated runs on CUDA tensors only (there is no CPU path)")
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, d_k] (packed, token-major)")
+    # the gate logits the projection will produce have q's shape: check the rest against it
+    gate_shape = torch.empty(q.shape, dtype=torch.float32, device="meta")
+    N, H, dk, dv, n_seq = _dims(q, k, v, gate_shape, beta, h0, cu_seqlens, device_check=False)
+    if x.dim() != 2 or x.shape[0] != N or x.dtype != torch.bfloat16:
+        raise ValueError(f"x must be bfloat16 with shape ({N}, d_model)")
+    D = x.shape[1]
+    if tuple(w_gate.shape) != (H * dk, D) or w_gate.dtype != torch.bfloat16:
+        raise ValueError(f"w_gate must be bfloat16 with shape {(H * dk, D)}")
+    if b_gate is not None and (tuple(b_gate.shape) != (H * dk,) or b_gate.dtype != torch.float32):
+        raise ValueError(f"b_gate must be float32 with shape {(H * dk,)}")
+    for t in (x, w_gate, b_gate, q, k, v, beta, h0, cu_seqlens):
+        if t is not None and (t.device != q.device or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous and on one device")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    host_cu = cu_seqlens.to("cpu")
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if h_final is None and output_final_state:
+        h_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
+    segment_tokens = max(64, min(int(segment_tokens), N))  # no larger slot than the call needs
+    need = lib.kda_chunk_fwd_gated_workspace_bytes(n_seq, H, dk, dv, segment_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        _check(lib, lib.kda_chunk_fwd_gated(
+            _ptr(x), _ptr(w_gate), _ptr(b_gate), D, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+            _ptr(h0), _ptr(cu_seqlens), ctypes.c_void_p(host_cu.data_ptr()), _ptr(out),
+            _ptr(h_final), _ptr(workspace), workspace.numel(), N, n_seq, H, dk, dv,
+            int(segment_tokens), KDA_BF16 if q.dtype == torch.bfloat16 else KDA_F32,
+            ctypes.c_void_p(stream)))
+    return out, (h_final if output_final_state else None)
 
 
 GATES = {"bounded": 0, "softplus": 1}

@@ -216,6 +216,15 @@ cudaError_t side_streams(SideStreams **out) {
     return cudaSuccess;
 }
 
+// gated forward: two carried states, the offset tables of up to kMaxSegments segments'
+// pieces, and one slot of gate logits for a segment of up to seg_tokens + kStepGrid tokens
+size_t gated_workspace(int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v, int32_t seg_tokens) {
+    const size_t carry = align256((size_t)n_heads * d_k * d_v * 4);
+    const size_t table = align256(((size_t)n_seq + 5 * (size_t)kMaxSegments + 1) * 4);
+    const size_t slot = align256(((size_t)seg_tokens + kStepGrid) * n_heads * d_k * 4);
+    return 2 * carry + table + slot;
+}
+
 size_t pipeline_workspace(int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
                           int32_t n_segments) {
     // two carried states, then the pieces' offset tables: at most 3 pieces per segment,
@@ -801,6 +810,123 @@ kda_status kda_chunk_fwd_from_host_pipelined(
     e = cudaEventRecord(ev[0], s_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[0], 0);
     return finish(launched(e, "pipeline completion"));
+}
+
+size_t kda_chunk_fwd_gated_workspace_bytes(int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                           int32_t d_v, int32_t segment_tokens) {
+    if (n_seq < 0 || n_heads <= 0 || d_k <= 0 || d_v <= 0 || segment_tokens < kStepGrid) return 0;
+    return gated_workspace(n_seq, n_heads, d_k, d_v, segment_tokens);
+}
+
+kda_status kda_chunk_fwd_gated(const void *x, const void *w_gate, const float *b_gate,
+                               int32_t d_model, const void *q, const void *k, const void *v,
+                               const float *beta, const float *h0, const int32_t *cu_seqlens,
+                               const int32_t *host_cu_seqlens, void *out, float *h_final,
+                               void *workspace, size_t workspace_bytes, int64_t n_tok,
+                               int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t segment_tokens, kda_dtype dtype, void *stream) {
+    if (dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "the gated forward takes bf16 x, W and q, k, v");
+    if (segment_tokens < kStepGrid)
+        return fail(KDA_ERR_INVALID_ARG, "segment_tokens must be at least 64");
+    // the forward's rules for the shared inputs (the workspace stands in for the gate logits)
+    kda::FwdArgs whole = pack(q, k, v, static_cast<const float *>(workspace), beta, h0,
+                              cu_seqlens, out, h_final, n_tok, n_seq, n_heads, d_k, d_v, dtype);
+    kda_status s = validate(whole, dtype);
+    if (s != KDA_OK) return s;
+    if (d_model <= 0 || d_model % 8 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "d_model must be a positive multiple of 8 (16-byte rows for TMA)");
+    if (n_tok > 0 && (!x || !w_gate)) return fail(KDA_ERR_INVALID_ARG, "x and w_gate are required");
+    if (!aligned16(x) || !aligned16(w_gate)) return fail(KDA_ERR_INVALID_ARG, "x and w_gate must be 16-byte aligned");
+    if (((uintptr_t)b_gate & 3u) != 0) return fail(KDA_ERR_INVALID_ARG, "b_gate must be 4-byte aligned");
+    if (n_seq > 0 && !host_cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "host_cu_seqlens is NULL");
+    if (n_seq > 0 && kda_chunk_fwd_pipeline_plan(host_cu_seqlens, n_seq, n_tok, 1, nullptr, 0) < 0)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "host_cu_seqlens must start at 0, not decrease and end at n_tok (< 2^31)");
+    const size_t need = gated_workspace(n_seq, n_heads, d_k, d_v, segment_tokens);
+    if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
+        return fail(KDA_ERR_INVALID_ARG, "workspace must be 256-byte aligned and hold "
+                                         "kda_chunk_fwd_gated_workspace_bytes bytes");
+    if (n_seq == 0 || n_tok == 0) {
+        if (n_seq > 0 && h_final) {  // no token: every h_final row is its h0 row (or zero)
+            const size_t bytes = (size_t)n_seq * n_heads * d_k * d_v * 4;
+            const cudaError_t e = h0 ? cudaMemcpyAsync(h_final, h0, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream)
+                                     : cudaMemsetAsync(h_final, 0, bytes, (cudaStream_t)stream);
+            return launched(e, "empty gated forward");
+        }
+        return ok();
+    }
+    const size_t es = 2;
+    const size_t rk = (size_t)n_heads * d_k, rv = (size_t)n_heads * d_v;  // elements per token
+    const size_t ns = (size_t)n_heads * d_k * d_v;
+    const bool cuttable = (rk * es) % 16 == 0 && (rv * es) % 16 == 0 && (rk * 4) % 16 == 0;
+    const int64_t want = (n_tok + segment_tokens - 1) / segment_tokens;
+    if (!cuttable && want > 1)
+        return fail(KDA_ERR_UNSUPPORTED, "segments need token rows of whole 16-byte multiples");
+    if (want > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many segments");
+    std::vector<FwdPiece> plan;
+    plan_pieces(host_cu_seqlens, n_seq, n_tok, (int32_t)want, plan);
+    const int64_t slot_tokens = (int64_t)segment_tokens + kStepGrid;
+
+    char *ws = static_cast<char *>(workspace);
+    const size_t carry_b = align256(ns * 4);
+    float *carry[2] = {reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + carry_b)};
+    int32_t *table = reinterpret_cast<int32_t *>(ws + 2 * carry_b);
+    float *slot = reinterpret_cast<float *>(ws + 2 * carry_b +
+                                            align256(((size_t)n_seq + 5 * (size_t)kMaxSegments + 1) * 4));
+    const cudaStream_t st = (cudaStream_t)stream;
+    const char *xq = static_cast<const char *>(x);
+    const char *cq = static_cast<const char *>(q), *ck = static_cast<const char *>(k);
+    const char *cv = static_cast<const char *>(v);
+    char *co = static_cast<char *>(out);
+    size_t j = 0;
+    while (j < plan.size()) {
+        // a batch of up to kMaxSegments segments shares one offsets-kernel launch
+        const int32_t seg0 = plan[j].segment;
+        const size_t jbase = j;
+        size_t jb = j;
+        while (jb < plan.size() && plan[jb].segment < seg0 + kMaxSegments) ++jb;
+        PieceTable pt{};
+        pt.n_pieces = (int32_t)(jb - j);
+        int32_t off = 0;
+        for (size_t i = j; i < jb; ++i) {
+            const size_t t = i - j;
+            pt.n0[t] = plan[i].n0;
+            pt.count[t] = plan[i].n1 - plan[i].n0;
+            pt.t0[t] = (int32_t)plan[i].t0;
+            pt.t1[t] = (int32_t)plan[i].t1;
+            pt.off[t] = off;
+            off += pt.count[t] + 1;
+        }
+        piece_offsets_kernel<<<1, 256, 0, st>>>(cu_seqlens, table, pt);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return launched(e, "gated forward set-up");
+        kda::count_launches(1);
+        while (j < jb) {
+            const int32_t seg = plan[j].segment;
+            size_t j1 = j;
+            while (j1 < jb && plan[j1].segment == seg) ++j1;
+            const int64_t t0 = plan[j].t0, t1 = plan[j1 - 1].t1;
+            if (t1 - t0 > slot_tokens) return fail(KDA_ERR_INVALID_ARG, "a segment outgrew its slot");
+            // this segment's gate logits, straight into the slot (kept small enough for L2)
+            e = kda::launch_gate_proj(xq + (size_t)t0 * d_model * 2, w_gate, b_gate, slot,
+                                      (int)(t1 - t0), (int)rk, d_model, st);
+            if (e != cudaSuccess) return launched(e, "gate projection launch");
+            for (size_t i = j; i < j1; ++i) {
+                const FwdPiece &pc = plan[i];
+                const float *ph0 = pc.h0_carried ? carry[seg & 1] : h0 ? h0 + (size_t)pc.n0 * ns : nullptr;
+                float *phf = pc.hf_carried ? carry[(seg + 1) & 1] : h_final ? h_final + (size_t)pc.n0 * ns : nullptr;
+                kda::FwdArgs p = pack(cq + pc.t0 * rk * es, ck + pc.t0 * rk * es, cv + pc.t0 * rv * es,
+                                      slot + (size_t)(pc.t0 - t0) * rk, beta + pc.t0 * n_heads, ph0,
+                                      table + pt.off[i - jbase], co + pc.t0 * rv * es, phf,
+                                      pc.t1 - pc.t0, pc.n1 - pc.n0, n_heads, d_k, d_v, dtype);
+                s = run(p, dtype, stream, Path::kAuto);
+                if (s != KDA_OK) return s;
+            }
+            j = j1;
+        }
+    }
+    return ok();
 }
 
 }  // extern "C"

@@ -363,6 +363,42 @@ kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void
                                         int32_t d_v, kda_dtype dtype, void *stream);
 
 /*
+ * kda_chunk_fwd_gated -- the forward pass fed directly by the gate projection
+ * ("Architecture Analysis of Ultra-Long Context Sparse MoE Models", §2.2: the gate is
+ * sigmoid(projection(x)); "From Numerical Stability to Load Balancing", §2.2): the result of
+ * kda_gate_projection(x, w_gate, b_gate) followed by kda_chunk_fwd, bit for bit, without
+ * the whole gate-logit tensor ever existing. The tokens are cut into segments of about
+ * `segment_tokens` (each cut a multiple of 64 tokens after the start of its sequence);
+ * per segment, the segment's gate logits are computed into one workspace slot sized to
+ * stay in L2 and consumed at once by the segment's forward pieces, and the state of a
+ * sequence cut by a segment boundary is carried to its next piece in fp32 through the
+ * workspace.
+ *   x          [n_tok, d_model] bf16, device, 16-byte aligned; d_model % 8 == 0
+ *   w_gate     [n_heads * d_k, d_model] bf16 (row h * d_k + c = head h, key channel c)
+ *   b_gate     [n_heads * d_k] fp32 or NULL
+ *   q .. h_final, cu_seqlens, n_tok .. d_v, stream: as kda_chunk_fwd (bf16 only)
+ *   host_cu_seqlens  the same offsets in host memory (for the segment plan)
+ *   workspace  device memory, 256-byte aligned, at least
+ *              kda_chunk_fwd_gated_workspace_bytes(n_seq, n_heads, d_k, d_v, segment_tokens)
+ *              bytes; owned by the caller, nothing in it has to be initialised
+ *   segment_tokens  >= 64; 4096 keeps a slot at 64 MiB for n_heads * d_k = 4096
+ * Runs on `stream` (current device must own every pointer and the stream); allocates no
+ * memory; launches per segment one GEMM and one forward kernel per piece, plus one small
+ * kernel per 64 segments. Errors: as kda_chunk_fwd and kda_gate_projection, plus
+ * KDA_ERR_UNSUPPORTED for a dtype other than KDA_BF16, KDA_ERR_INVALID_ARG for
+ * segment_tokens < 64, a missing or misaligned workspace or an invalid host_cu_seqlens.
+ */
+size_t kda_chunk_fwd_gated_workspace_bytes(int32_t n_seq, int32_t n_heads, int32_t d_k,
+                                           int32_t d_v, int32_t segment_tokens);
+kda_status kda_chunk_fwd_gated(const void *x, const void *w_gate, const float *b_gate,
+                               int32_t d_model, const void *q, const void *k, const void *v,
+                               const float *beta, const float *h0, const int32_t *cu_seqlens,
+                               const int32_t *host_cu_seqlens, void *out, float *h_final,
+                               void *workspace, size_t workspace_bytes, int64_t n_tok,
+                               int32_t n_seq, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t segment_tokens, kda_dtype dtype, void *stream);
+
+/*
  * kda_chunk_fwd_from_host -- end-to-end variant for callers whose inputs live in
  * host memory. Copies the inputs (host_*, preferably pinned) into the caller's
  * device buffers (dev_*) with one cudaMemcpyAsync each on `stream`, runs

@@ -260,3 +260,43 @@ def test_check_outputs_host_validation(lib):
     assert lib.kda_check_outputs(P(FAKE), 10, 1, None, 0, P(FAKE), None, None) == 1
     assert lib.kda_check_outputs(None, 10, 1, None, 0, P(FAKE), ctypes.byref(cnt), None) == 1
     assert lib.kda_check_outputs(P(FAKE), -1, 1, None, 0, P(FAKE), ctypes.byref(cnt), None) == 1
+
+
+def gated(lib, *, x=FAKE, w=2 * FAKE, b=None, D=256, q=3 * FAKE, k=4 * FAKE, v=5 * FAKE,
+          beta=6 * FAKE, h0=None, cu=7 * FAKE, host_cu="default", out=8 * FAKE, hf=None,
+          ws=9 * FAKE, ws_bytes=None, n_tok=64, n_seq=1, H=2, dk=128, dv=128, seg=64, dtype=1):
+    P = ctypes.c_void_p
+    hc = (ctypes.c_int32 * 2)(0, n_tok) if host_cu == "default" else host_cu
+    if ws_bytes is None:
+        ws_bytes = lib.kda_chunk_fwd_gated_workspace_bytes(n_seq, H, dk, dv, max(seg, 64))
+    return lib.kda_chunk_fwd_gated(P(x), P(w), P(b), D, P(q), P(k), P(v), P(beta), P(h0), P(cu),
+                                   hc, P(out), P(hf), P(ws), ws_bytes, n_tok, n_seq, H, dk, dv,
+                                   seg, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=0), 2),                       # bf16 only
+    (dict(seg=63), 1),                        # segments of at least one 64-token step
+    (dict(D=12), 2),                          # d_model a multiple of 8
+    (dict(x=None), 1), (dict(w=None), 1), (dict(x=FAKE + 8), 1), (dict(b=FAKE + 2), 1),
+    (dict(q=None), 1), (dict(dk=129), 2),     # the forward's own rules
+    (dict(host_cu=None), 1),
+    (dict(host_cu=(ctypes.c_int32 * 2)(0, 63)), 1),   # does not end at n_tok
+    (dict(ws=None), 1), (dict(ws_bytes=256), 1), (dict(ws=9 * FAKE + 16), 1),
+])
+def test_gated_forward_host_validation(lib, kw, status):
+    st = gated(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
+def test_gated_workspace_size(lib):
+    # two carried states of H x 128 x 128 fp32, the offsets table, one slot of
+    # (segment + 64) tokens x H x d_k fp32 gate logits, each 256-byte aligned
+    H, seg, n_seq = 32, 4096, 1
+    carry = H * 128 * 128 * 4
+    table = ((n_seq + 5 * 64 + 1) * 4 + 255) // 256 * 256
+    slot = (seg + 64) * H * 128 * 4
+    assert lib.kda_chunk_fwd_gated_workspace_bytes(n_seq, H, 128, 128, seg) == 2 * carry + table + slot
+    assert lib.kda_chunk_fwd_gated_workspace_bytes(n_seq, H, 128, 128, 32) == 0
+    assert lib.kda_chunk_fwd_gated_workspace_bytes(-1, H, 128, 128, seg) == 0
