@@ -15,18 +15,19 @@
 //   P  = lower([Q K^T with the same factors])                        64 x 64
 //   TB = (I + A)^-1 diag(beta),   W = TB K~B,   K~B = K exp(G^B)
 //   Q' = Q~B - P W,               P' = P TB,    K'B = K exp(G^B_end - G^B)
-//   U  = TB V - W S,   O = d_k^-1/2 (Q~B S + P U),   S <- Diag(exp G^B_end) S + K'B^T U
+//   U  = TB (V - K~B S) = TB V - W S,   O = d_k^-1/2 (Q~B S + P U),
+//   S <- Diag(exp G^B_end) S + K'B^T U
 // (equivalently O = d_k^-1/2 (P' V + Q' S) with U substituted).
 //
 // Work decomposition: one cluster of 1 + kPro CTAs per (sequence, head).
 //  * rank 0, the chain CTA, runs the serial recurrence. Transposed, with the state S^T
 //    (d_v x d_k) as the A operand of the tensor core, per step:
-//        D1[:, 0..63]   = V^T TB^T + S^T (-W)^T       = U^T
+//        D1[:, 0..63]   = S^T K~B^T = Y^T,  then  Z^T TB^T = U^T  with Z^T = V^T - Y^T
 //        D1[:, 64..127] = S^T Q~B^T + U^T P^T          = O^T / scale
 //        D2             = U^T K'B                      (the state increment)
-//    Only the U^T group (N = 64) and D2 lie on the state's critical path; the O^T
-//    products fill the tensor pipe while U^T is converted and while the state is
-//    updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
+//    (U = TB (V - K~B S) = TB V - W S.) The Y^T, U^T and D2 groups lie on the state's
+//    critical path; the O^T products fill the tensor pipe while U^T is formed and while
+//    the state is updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
 //    value row and 64 keys per thread) and is mirrored as bf16 into tensor memory as the
 //    next A operand; U^T likewise. One issuer thread (its own warp) issues every
 //    tcgen05.mma; the state warps signal it per warp through mbarriers. Four "output"
@@ -34,7 +35,7 @@
 //    buffers; the products arrive in one of three operand slots.
 //  * ranks 1..kPro, the prologue CTAs, each compute every kPro-th step's operands (the
 //    gate, the four tiles' scaled operands, [A; P] as one tcgen05 product, the 64 x 64
-//    solve for TB, W = TB K~B as a second tcgen05 product) into a staging buffer laid
+//    solve for TB) into a staging buffer laid
 //    out exactly as the chain CTA's operand slot, and copy it there with bulk copies
 //    (shared::cta -> shared::cluster) once the chain CTA has freed the slot (with three
 //    slots and three prologue CTAs, each prologue CTA always fills the same slot).
@@ -88,8 +89,8 @@ static_assert(NT == 4, "the tile-pair tables below assume four tiles per step");
 
 // ---- operand slot (identical layout in the chain CTA's ring and a prologue's staging)
 // B1: [n][j] K-major, 128-byte swizzle: rows 0..63 = TB, rows 64..127 = P    (K = tokens)
-// B2: bytes 0..16383: -W, [t][c] K-major, two 64-channel atom columns 8 KB apart;
-//     bytes 16384..32767: Q~B, [c][t] (read MN-major: tokens along N, channels along K)
+// B2: bytes 0..16383: K~B, bytes 16384..32767: Q~B, each [c][t] (128 channel rows of 64
+//     tokens, read MN-major: tokens along N, channels along K)
 // B3: [c][t] K-major: K'B^T (K = tokens)
 // G : gamma^B[c] = exp(G^B_end), fp32
 constexpr int SL_B1 = 0, SL_B2 = 16384, SL_B3 = 49152, SL_G = 65536;
@@ -109,20 +110,23 @@ static_assert(CH_V % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 // barrier indices (8 bytes each)
 constexpr int B_FULL = 0;     // [NSLOT] slot s: products (bulk copies) + V (TMA) landed
 constexpr int B_FREE = 3;     // [NSLOT] slot s: its MMAs completed and gamma read (1 + 8 arrivals)
-constexpr int B_D1U = 6;      // [2] D1 buffer b: U^T complete
+constexpr int B_D1U = 6;      // [2] D1 buffer b: Y^T = S^T K~B^T complete
 constexpr int B_D1FREE = 8;   // [2] D1 buffer b read out by the output warps (4 arrivals)
 constexpr int B_D2FULL = 10;  // D2 complete
 constexpr int B_DRAIN = 11;   // every MMA complete (before the tensor memory is released)
 constexpr int B_D1O = 12;     // [2] D1 buffer b: O^T complete
 constexpr int B_SREADY = 14;  // the state's bf16 copy is in tensor memory (8 warp arrivals)
 constexpr int B_UREADY = 15;  // U^T's bf16 copy is in tensor memory (8 warp arrivals)
-constexpr int NBARS = 16;
+constexpr int B_UFULL = 16;   // [2] D1 buffer b: U^T = Z^T TB^T complete
+constexpr int B_ZREADY = 18;  // Z^T = V^T - Y^T in bf16 is in tensor memory (8 warp arrivals)
+constexpr int NBARS = 19;
 static_assert(NSLOT == 3 && B_FREE == NSLOT, "barrier table");
 // tensor-memory columns
 constexpr uint32_t TM_D1 = 0;     // 2 x 128 columns
 constexpr uint32_t TM_D2 = 256;   // 128 columns
 constexpr uint32_t TM_AS = 384;   // S^T bf16: 64 columns (128 keys)
 constexpr uint32_t TM_AU = 448;   // U^T bf16: 32 columns (64 tokens)
+constexpr uint32_t TM_AZ = 480;   // Z^T bf16: 32 columns (64 tokens)
 constexpr uint32_t kTmemCols = 512;
 
 // ---- prologue CTA shared memory
@@ -134,7 +138,6 @@ constexpr int PR_Q = 0, PR_K = 16384, PR_A = 32768;  // raw tiles [64 t][128 c] 
 constexpr int PR_X = 65536;
 constexpr int X_R = 0;       // [K~ | Q~] of the step's 64 tokens: two 16 KB halves (A operand)
 constexpr int X_C = 32768;   // column tiles: [K^_0..3 | K'_0..2, Kx_20 | Kx_30, Kx_31, -] (B)
-constexpr int X_KB = 0;      // after the A / P product: K~B ([c][64 t]), operand of the W product
 constexpr int X_BYTES = 81920;
 constexpr int PR_AD = PR_X + X_BYTES;             // diagonal A tiles, fp32 [4][16][16]
 constexpr int PR_AO = PR_AD + NT * TL * TL * 4;   // off-diagonal A tiles, bf16 [6][16][16]
@@ -145,18 +148,17 @@ constexpr int PR_STG = (PR_BAR + 32 + 1023) & ~1023;  // staging slot
 constexpr int PR_END = PR_STG + SLOT_BYTES;
 static_assert(PR_X % 1024 == 0 && (PR_X + X_C) % 1024 == 0 && PR_STG % 1024 == 0, "swizzled tiles");
 // tensor-memory columns of a prologue CTA
-constexpr uint32_t TP_WQ = 0;    // W (rows 0..63 of 128 x 128)
-constexpr uint32_t TP_AP = 256;  // [A; P] before masking (192)
-constexpr uint32_t kProTmemCols = 512;
+constexpr uint32_t TP_AP = 0;    // [A; P] before masking (192 columns)
+constexpr uint32_t kProTmemCols = 256;
 constexpr int SMEM_USED = (PR_END > CH_BAR + NBARS * 8 ? PR_END : CH_BAR + NBARS * 8);
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack of the dynamic base
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-// fp32 16 x 16 scratch tiles of the solve in the -W part of the staging slot's B2 (-W
-// is written last): M = L^-1 N (6 tiles), M^2 (3), the diagonal T tiles (4)
-constexpr int STG_MM = PR_STG + SL_B2;
+// fp32 16 x 16 scratch tiles of the solve in X (free once the [A; P] product has read it):
+// M = L^-1 N (6 tiles), M^2 (3), the diagonal T tiles (4)
+constexpr int STG_MM = PR_X;
 constexpr int STG_M2 = STG_MM + 6 * 1024;
 constexpr int STG_TD = STG_M2 + 3 * 1024;
-static_assert(STG_TD + 4 * 1024 <= PR_STG + SL_B2 + B2_QB, "solve scratch stays in the -W part of B2");
+static_assert(STG_TD + 4 * 1024 <= PR_X + X_BYTES, "solve scratch stays in X");
 
 // registers per thread (chain CTA): the block is launched with 128; each warpgroup then
 // moves to its own share and the shares add up to the launch total
@@ -247,7 +249,7 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         regs_set<kRegsMisc>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------- producer: V tiles
-            // step m's V goes to buffer m & 1, last read by step m - 2's products
+            // step m's V goes to buffer m & 1, last read (by the state warps) in step m - 2
             for (int m = 0; m < nblocks; ++m) {
                 if (m >= 2 && !wait_bar(bar(B_FREE + (m - 2) % NSLOT), ((m - 2) / NSLOT) & 1)) break;
                 const int s = m % NSLOT;
@@ -268,67 +270,55 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------- MMA issuer
             // Per step n (slot s, D1 buffer b), in tensor-pipe order:
-            //   V^T TB^T                 -> D1 columns 0..63   (issued one step ahead)
-            //   S^T (-W)^T               -> D1 columns 0..63   = U^T; commit D1U
-            //   S^T Q~B^T                -> D1 columns 64..127 (B read MN-major)
-            //   U^T K'B                  -> D2                 ; commit D2FULL
-            //   U^T P^T                  -> D1 columns 64..127 = O^T / scale; commit D1O, FREE
-            // so the state's critical path carries only the two N = 64 / 128 groups.
-            const uint32_t id_v = idesc_bf16(128, 64, 1, 0);   // A = V^T (MN-major), N = 64 tokens
-            const uint32_t id_t = idesc_bf16(128, 64, 0, 0);   // N = 64 tokens
-            const uint32_t id_q = idesc_bf16(128, 64, 0, 1);   // B = Q~B (MN-major), N = 64 tokens
+            //   S^T K~B^T       -> D1 columns 0..63   = Y^T; commit D1U
+            //   S^T Q~B^T       -> D1 columns 64..127
+            //   Z^T TB^T        -> D1 columns 0..63   = U^T (Z^T = V^T - Y^T from the state warps); commit UFULL
+            //   U^T K'B         -> D2                 ; commit D2FULL
+            //   U^T P^T         -> D1 columns 64..127 = O^T / scale; commit D1O, FREE
+            const uint32_t id_t = idesc_bf16(128, 64, 0, 0);   // N = 64 tokens, B K-major
+            const uint32_t id_q = idesc_bf16(128, 64, 0, 1);   // N = 64 tokens, B MN-major
             const uint32_t id_k = idesc_bf16(128, 128, 0, 0);  // N = 128 keys
             // slot s's descriptors are slot 0's plus s x the slot stride (16-byte units)
-            const uint64_t dV0 = sdesc_sw128(sbase + CH_V, 8192, 1024);
             const uint64_t dB10 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
-            const uint64_t dB20 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 16, 1024);
+            const uint64_t dKB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 8192, 1024);
             const uint64_t dQB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2 + B2_QB, 8192, 1024);
             const uint64_t dB30 = sdesc_sw128(sbase + CH_SLOT + SL_B3, 16, 1024);
-            constexpr uint64_t kSlotStep = SLOT_STRIDE >> 4, kVStep = V_BYTES >> 4;
+            constexpr uint64_t kSlotStep = SLOT_STRIDE >> 4;
             constexpr uint64_t kLow = (64 * 128) >> 4;  // rows 64..127 of a K-major operand
-            auto issue_v = [&](int n) -> bool {
-                const int s = n % NSLOT, b = n & 1;
-                if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) return false;
-                if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
-                    umma_ss(d1, dV0 + b * kVStep + (uint64_t)(128 * j), dB10 + s * kSlotStep + (uint64_t)(2 * j),
-                            id_v, j > 0);
-                return true;
-            };
-            bool ok = nblocks > 0 && issue_v(0);
-            for (int n = 0; ok && n < nblocks; ++n) {
+            for (int n = 0; n < nblocks; ++n) {
                 const int s = n % NSLOT, b = n & 1;
                 const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
-                const uint64_t b2 = dB20 + s * kSlotStep;
+                const uint64_t so = s * kSlotStep;
+                if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;           // step n's operands
+                if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) break;  // D1 read out
                 if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T (bf16) of step n is in
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // K = 16 keys per MMA
-                    umma_ts(d1, tmem + TM_AS + 8u * k, b2 + (uint64_t)((((k >> 2) * 8192) + (k & 3) * 32) >> 4),
-                            id_t, 1);
+                for (int k = 0; k < 8; ++k)  // 16 channel rows (2048 bytes) per MMA
+                    umma_ts(d1, tmem + TM_AS + 8u * k, dKB0 + so + (uint64_t)(128 * k), id_q, k > 0);
                 umma_commit(bar(B_D1U + b));
                 F64_TRACE(n, 1);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // 16 channel rows (2048 bytes) per MMA
-                    umma_ts(d1 + 64u, tmem + TM_AS + 8u * k, dQB0 + s * kSlotStep + (uint64_t)(128 * k), id_q, k > 0);
-                if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
+                for (int k = 0; k < 8; ++k)
+                    umma_ts(d1 + 64u, tmem + TM_AS + 8u * k, dQB0 + so + (uint64_t)(128 * k), id_q, k > 0);
+                if (!wait_bar(bar(B_ZREADY), n & 1)) break;  // Z^T (bf16) of step n is in
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
-                    umma_ts(tmem + TM_D2, tmem + TM_AU + 8u * j, dB30 + s * kSlotStep + (uint64_t)(2 * j), id_k,
-                            j > 0);
+                    umma_ts(d1, tmem + TM_AZ + 8u * j, dB10 + so + (uint64_t)(2 * j), id_t, j > 0);
+                umma_commit(bar(B_UFULL + b));
+                if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    umma_ts(tmem + TM_D2, tmem + TM_AU + 8u * j, dB30 + so + (uint64_t)(2 * j), id_k, j > 0);
                 umma_commit(bar(B_D2FULL));
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    umma_ts(d1 + 64u, tmem + TM_AU + 8u * j, dB10 + s * kSlotStep + kLow + (uint64_t)(2 * j), id_t,
-                            1);
+                    umma_ts(d1 + 64u, tmem + TM_AU + 8u * j, dB10 + so + kLow + (uint64_t)(2 * j), id_t, 1);
                 umma_commit(bar(B_D1O + b));
                 umma_commit(bar(B_FREE + s));
                 F64_TRACE(n, 4);
-                if (n + 1 < nblocks) ok = issue_v(n + 1);
             }
             // every MMA has completed before the tensor memory is released
             umma_commit(bar(B_DRAIN));
@@ -368,9 +358,34 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             const int s = n % NSLOT, b = n & 1;
             const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
             if (elect_trace(warp, lane)) F64_TRACE(n, 0);
-            // ---- U^T: columns 0..63 of D1 -> bf16 A operand, 32 tokens per warpgroup
+            // ---- Z^T = V^T - Y^T (this thread's value row, 32 tokens) -> bf16 A operand.
+            //      The slot's FULL phase is observed here too: it makes the V tile and
+            //      gamma^B (landed by TMA / bulk copy) visible to this thread's loads.
+            if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;
             if (!wait_bar(bar(B_D1U + b), (n >> 1) & 1)) break;
             if (elect_trace(warp, lane)) F64_TRACE(n, 2);
+            tc_fence_after();
+            {
+                uint32_t r[32], w[16];
+                tmem_ld32(d1 + lb + 32u * kh, r);
+                // V tile of step n: buffer n & 1, two [64 t][64 v] 128-byte-swizzled halves
+                const unsigned char *vt = sm + CH_V + (n & 1) * V_BYTES + (v >> 6) * (V_BYTES / 2);
+                float vv[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    vv[t] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + sw128(32 * kh + t, v & 63)));
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    w[j] = pack_bf16(vv[2 * j] - __uint_as_float(r[2 * j]), vv[2 * j + 1] - __uint_as_float(r[2 * j + 1]));
+                tmem_st16(tmem + lb + TM_AZ + 16 * kh, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_ZREADY));
+            // ---- U^T: columns 0..63 of D1 -> bf16 A operand, 32 tokens per warpgroup
+            if (!wait_bar(bar(B_UFULL + b), (n >> 1) & 1)) break;
             tc_fence_after();
             {
                 uint32_t r[32], w[16];
@@ -641,8 +656,8 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         // ---- P2: every scaled operand of this (channel, tile), from fp32 values:
         //   R = [K~ | Q~] (K~ = K Gamma), the column tiles K^ = K / Gamma and
         //   K' = K gamma / Gamma (and K' scaled by the decays of the tiles after it: Kx),
-        //   K'B = K' prod_{J > I} gamma_J into the slot, gamma^B; K~B and Q~B (x prod_{J < I}
-        //   gamma_J) stay in registers until the A / P product has read X.
+        //   K'B = K' prod_{J > I} gamma_J, gamma^B, K~B and Q~B (x prod_{J < I} gamma_J) stay
+        //   in registers until the staging slot may be written.
         uint32_t wkb[TL / 2], wqb[TL / 2], wkp[TL / 2];
         float gB = 0.f;
         {
@@ -738,8 +753,11 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             umma_commit(apbar);
             F64_TRACE(m, 21);
         }
-        {   // while the product runs: K'B, Q~B ([c][64 t]) and gamma^B into the staging slot
-            // (the previous copy out of it has completed: checked before the barrier above)
+        {   // while the product runs: K'B, K~B and Q~B ([c][64 t]) and gamma^B into the staging
+            // slot (the previous copy out of it has completed: checked before the barrier above)
+            unsigned char *kb = sm + PR_STG + SL_B2;
+            *reinterpret_cast<uint4 *>(kb + sw128(c, rb)) = make_uint4(wkb[0], wkb[1], wkb[2], wkb[3]);
+            *reinterpret_cast<uint4 *>(kb + sw128(c, rb + 8)) = make_uint4(wkb[4], wkb[5], wkb[6], wkb[7]);
             unsigned char *b3 = sm + PR_STG + SL_B3;
             *reinterpret_cast<uint4 *>(b3 + sw128(c, rb)) = make_uint4(wkp[0], wkp[1], wkp[2], wkp[3]);
             *reinterpret_cast<uint4 *>(b3 + sw128(c, rb + 8)) = make_uint4(wkp[4], wkp[5], wkp[6], wkp[7]);
@@ -753,9 +771,6 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             if (tid == 0) F64_TRACE(m, 22);
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
-                // K~B (operand of the W product) takes X's place
-                *reinterpret_cast<uint4 *>(X + X_KB + sw128(c, rb)) = make_uint4(wkb[0], wkb[1], wkb[2], wkb[3]);
-                *reinterpret_cast<uint4 *>(X + X_KB + sw128(c, rb + 8)) = make_uint4(wkb[4], wkb[5], wkb[6], wkb[7]);
                 if (tid == 0) F64_TRACE(m, 24);
                 // A (rows 0..63: beta-scaled, strictly lower on the diagonal tiles) and P
                 // (rows 64..127: lower on the diagonal tiles) out of the product's columns.
@@ -918,44 +933,10 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             }
             if (tid == 0) F64_TRACE(m, 27);
         }
-        fence_proxy_async();  // B1 and X: generic writes -> tensor-core reads
+        fence_proxy_async();  // generic writes of the staging slot -> the bulk copy's reads
         tc_fence_before();
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 13);
-        // ---- P5: W = TB K~B on this CTA's tensor core (A = B1: rows 0..63 TB, rows 64..127
-        //      P, whose products are not read; N = 128 channels, K = 64 tokens); B2 bytes
-        //      0..16383 = -W
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t da = sdesc_sw128(stg + SL_B1, 16, 1024), db = sdesc_sw128(sbase + PR_X + X_KB, 16, 1024);
-            const uint32_t idk = idesc_bf16(128, 128, 0, 0);
-#pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) umma_ss(ptmem + TP_WQ, da + 2 * kk2, db + 2 * kk2, idk, kk2 > 0);
-            umma_commit(mmabar);
-        }
-        if ((warp & 3) < 2) {  // lane quarters 0 and 1: rows 0..63; 32 channels per warp
-            const bool got = wait_bar(mmabar, k & 1);
-            if (__all_sync(0xffffffffu, got)) {
-                tc_fence_after();
-                const int n = ((warp & 3) << 5) + lane, part = warp >> 2;
-                uint32_t r[32];
-                tmem_ld32(ptmem + TP_WQ + ((uint32_t)((warp & 3) * 32) << 16) + 32u * part, r);
-                tmem_ld_wait();
-                unsigned char *dst = sm + PR_STG + SL_B2 + (part >> 1) * 8192;
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        w[h] = pack_bf16(-__uint_as_float(r[8 * c8 + 2 * h]), -__uint_as_float(r[8 * c8 + 2 * h + 1]));
-                    *reinterpret_cast<uint4 *>(dst + sw128(n, 32 * (part & 1) + 8 * c8)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            tc_fence_before();
-        }
-        fence_proxy_async();  // generic writes of the staging slot -> the bulk copy's reads
-        __syncthreads();
-        if (tid == 0) F64_TRACE(m, 15);
         // ---- P6: into the chain CTA's slot m % NSLOT once step m - NSLOT has consumed it
         if (tid == 0 && !bad) {
             if (m >= NSLOT) {
@@ -969,7 +950,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     if (tid == 0) {
         bulk_wait_read0();  // no copy may still read this CTA's memory at exit
         umma_commit(mmabar);  // and every product has completed before the tensor memory goes
-        wait_bar(mmabar, k & 1);  // one commit per step before this one
+        wait_bar(mmabar, 0);      // the only commit on this barrier
     }
     if (warp == 15) cp_async_wait0();
     tc_fence_before();
@@ -1008,6 +989,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sbase + CH_BAR + 8u * B_DRAIN, 1);
             mbar_init(sbase + CH_BAR + 8u * B_SREADY, 8);
             mbar_init(sbase + CH_BAR + 8u * B_UREADY, 8);
+            mbar_init(sbase + CH_BAR + 8u * B_ZREADY, 8);
+            for (int b = 0; b < 2; ++b) mbar_init(sbase + CH_BAR + 8u * (B_UFULL + b), 1);
         } else {
             mbar_init(sbase + PR_BAR, 1);
             mbar_init(sbase + PR_BAR + 8, 1);
