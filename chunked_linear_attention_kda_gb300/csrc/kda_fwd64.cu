@@ -119,7 +119,9 @@ constexpr int B_SREADY = 14;  // the state's bf16 copy is in tensor memory (8 wa
 constexpr int B_UREADY = 15;  // U^T's bf16 copy is in tensor memory (8 warp arrivals)
 constexpr int B_UFULL = 16;   // [2] D1 buffer b: U^T = Z^T TB^T complete
 constexpr int B_ZREADY = 18;  // Z^T = V^T - Y^T in bf16 is in tensor memory (8 warp arrivals)
-constexpr int NBARS = 19;
+constexpr int B_SREADY2 = 19; // the state's keys 64..127 in bf16 (B_SREADY: keys 0..63)
+constexpr int B_D2FULL2 = 20; // D2 keys 64..127 complete (B_D2FULL: keys 0..63)
+constexpr int NBARS = 21;
 static_assert(NSLOT == 3 && B_FREE == NSLOT, "barrier table");
 // tensor-memory columns
 constexpr uint32_t TM_D1 = 0;     // 2 x 128 columns
@@ -270,14 +272,14 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------- MMA issuer
             // Per step n (slot s, D1 buffer b), in tensor-pipe order:
-            //   S^T K~B^T       -> D1 columns 0..63   = Y^T; commit D1U
+            //   S^T K~B^T       -> D1 columns 0..63   = Y^T (keys 0..63 as soon as they are
+            //                      in, then 64..127); commit D1U
             //   S^T Q~B^T       -> D1 columns 64..127
             //   Z^T TB^T        -> D1 columns 0..63   = U^T (Z^T = V^T - Y^T from the state warps); commit UFULL
-            //   U^T K'B         -> D2                 ; commit D2FULL
+            //   U^T K'B         -> D2, keys 0..63 then 64..127; commit D2FULL, D2FULL2
             //   U^T P^T         -> D1 columns 64..127 = O^T / scale; commit D1O, FREE
             const uint32_t id_t = idesc_bf16(128, 64, 0, 0);   // N = 64 tokens, B K-major
             const uint32_t id_q = idesc_bf16(128, 64, 0, 1);   // N = 64 tokens, B MN-major
-            const uint32_t id_k = idesc_bf16(128, 128, 0, 0);  // N = 128 keys
             // slot s's descriptors are slot 0's plus s x the slot stride (16-byte units)
             const uint64_t dB10 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
             const uint64_t dKB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 8192, 1024);
@@ -291,11 +293,16 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                 const uint64_t so = s * kSlotStep;
                 if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;           // step n's operands
                 if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) break;  // D1 read out
-                if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T (bf16) of step n is in
+                if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T keys 0..63 (bf16) of step n are in
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // 16 channel rows (2048 bytes) per MMA
+                for (int k = 0; k < 4; ++k)  // 16 channel rows (2048 bytes) per MMA
                     umma_ts(d1, tmem + TM_AS + 8u * k, dKB0 + so + (uint64_t)(128 * k), id_q, k > 0);
+                if (!wait_bar(bar(B_SREADY2), n & 1)) break;  // keys 64..127
+                tc_fence_after();
+#pragma unroll
+                for (int k = 4; k < 8; ++k)
+                    umma_ts(d1, tmem + TM_AS + 8u * k, dKB0 + so + (uint64_t)(128 * k), id_q, 1);
                 umma_commit(bar(B_D1U + b));
                 F64_TRACE(n, 1);
 #pragma unroll
@@ -310,9 +317,13 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                 if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    umma_ts(tmem + TM_D2, tmem + TM_AU + 8u * j, dB30 + so + (uint64_t)(2 * j), id_k, j > 0);
-                umma_commit(bar(B_D2FULL));
+                for (int h = 0; h < 2; ++h) {  // D2 keys 64 h .. 64 h + 63 (B3 rows), one commit each
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        umma_ts(tmem + TM_D2 + 64u * h, tmem + TM_AU + 8u * j, dB30 + so + h * kLow + (uint64_t)(2 * j),
+                                id_t, j > 0);
+                    umma_commit(bar(h ? B_D2FULL2 : B_D2FULL));
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     umma_ts(d1 + 64u, tmem + TM_AU + 8u * j, dB10 + so + kLow + (uint64_t)(2 * j), id_t, 1);
@@ -327,58 +338,62 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
     } else if (warp < 12) {
         regs_set<kRegsState>();
         // -------------------------------------------------- state warps (two warpgroups)
-        // Thread (value row v = TMEM lane, key half kh) holds S^T[v][64 kh .. 64 kh + 63]
-        // in fp32 registers; the two warpgroups split each step's conversions by half.
-        // Each warp signals the issuer on its own (SREADY, UREADY: 8 arrivals).
-        const int kh = (warp - 4) >> 2;
+        // Thread (value row v = TMEM lane, warpgroup wg) holds S^T[v][k] in fp32 registers
+        // for the keys k = 64 h + 32 wg + j (h = 0, 1; j < 32): each half of the keys is
+        // split over both warpgroups, so that each half is updated, converted and handed to
+        // the issuer (SREADY, SREADY2) while the other is still being produced. Each warp
+        // signals the issuer on its own (8 arrivals per barrier).
+        const int wg = (warp - 4) >> 2;
         const int v = ((warp & 3) << 5) + lane;                 // value row = TMEM lane
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;  // lane quarter
-        constexpr int KH = D / 2;
-        float S[KH];
+        float S[64];  // S[32 h + j] = S^T[v][64 h + 32 wg + j]
         {
             const float *h0 = p.h0 ? p.h0 + ((size_t)seq * H + head) * D * D : nullptr;
 #pragma unroll
-            for (int c = 0; c < KH; ++c) S[c] = h0 ? h0[(size_t)(KH * kh + c) * D + v] : 0.f;
+            for (int c = 0; c < 64; ++c) S[c] = h0 ? h0[(size_t)(64 * (c >> 5) + 32 * wg + (c & 31)) * D + v] : 0.f;
         }
-        auto store_state = [&]() {  // bf16 copy of this thread's 64 keys -> A operand
+        auto store_half = [&](int h) {  // bf16 copy of this thread's keys of half h -> A operand
+            uint32_t w[16];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = pack_bf16(S[32 * q + 2 * j], S[32 * q + 2 * j + 1]);
-                tmem_st16(tmem + lb + TM_AS + 32 * kh + 16 * q, w);
-            }
+            for (int j = 0; j < 16; ++j) w[j] = pack_bf16(S[32 * h + 2 * j], S[32 * h + 2 * j + 1]);
+            tmem_st16(tmem + lb + TM_AS + 32 * h + 16 * wg, w);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SREADY));
+            if (lane == 0) mbar_arrive(bar(h ? B_SREADY2 : B_SREADY));
         };
-        store_state();
+        store_half(0);
+        store_half(1);
         for (int n = 0; n < nblocks; ++n) {
             const int s = n % NSLOT, b = n & 1;
             const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
             if (elect_trace(warp, lane)) F64_TRACE(n, 0);
-            // ---- Z^T = V^T - Y^T (this thread's value row, 32 tokens) -> bf16 A operand.
-            //      The slot's FULL phase is observed here too: it makes the V tile and
-            //      gamma^B (landed by TMA / bulk copy) visible to this thread's loads.
+            // ---- V^T of this thread's value row and 32 tokens, loaded while Y^T is formed.
+            //      The slot's FULL phase is observed first: it makes the V tile and gamma^B
+            //      (landed by TMA / bulk copy) visible to this thread's loads.
             if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;
+            uint32_t vv[16];  // token pairs (2 j, 2 j + 1), bf16
+            {
+                // V tile of step n: buffer n & 1, two [64 t][64 v] 128-byte-swizzled halves
+                const unsigned char *vt = sm + CH_V + (n & 1) * V_BYTES + (v >> 6) * (V_BYTES / 2);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    vv[j] = (uint32_t)*reinterpret_cast<const unsigned short *>(vt + sw128(32 * wg + 2 * j, v & 63)) |
+                            ((uint32_t)*reinterpret_cast<const unsigned short *>(vt + sw128(32 * wg + 2 * j + 1, v & 63)) << 16);
+            }
+            // ---- Z^T = V^T - Y^T -> bf16 A operand
             if (!wait_bar(bar(B_D1U + b), (n >> 1) & 1)) break;
             if (elect_trace(warp, lane)) F64_TRACE(n, 2);
             tc_fence_after();
             {
                 uint32_t r[32], w[16];
-                tmem_ld32(d1 + lb + 32u * kh, r);
-                // V tile of step n: buffer n & 1, two [64 t][64 v] 128-byte-swizzled halves
-                const unsigned char *vt = sm + CH_V + (n & 1) * V_BYTES + (v >> 6) * (V_BYTES / 2);
-                float vv[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    vv[t] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + sw128(32 * kh + t, v & 63)));
+                tmem_ld32(d1 + lb + 32u * wg, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    w[j] = pack_bf16(vv[2 * j] - __uint_as_float(r[2 * j]), vv[2 * j + 1] - __uint_as_float(r[2 * j + 1]));
-                tmem_st16(tmem + lb + TM_AZ + 16 * kh, w);
+                    w[j] = pack_bf16(__uint_as_float(vv[j] << 16) - __uint_as_float(r[2 * j]),
+                                     __uint_as_float(vv[j] & 0xffff0000u) - __uint_as_float(r[2 * j + 1]));
+                tmem_st16(tmem + lb + TM_AZ + 16 * wg, w);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -389,47 +404,54 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             tc_fence_after();
             {
                 uint32_t r[32], w[16];
-                tmem_ld32(d1 + lb + 32u * kh, r);
+                tmem_ld32(d1 + lb + 32u * wg, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                tmem_st16(tmem + lb + TM_AU + 16 * kh, w);
+                tmem_st16(tmem + lb + TM_AU + 16 * wg, w);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_UREADY));
             if (elect_trace(warp, lane)) F64_TRACE(n, 3);
-            // ---- S^T <- S^T diag(gamma^B) + D2 on this warpgroup's 64 keys, then bf16
-            if (!wait_bar(bar(B_D2FULL), n & 1)) break;
-            if (elect_trace(warp, lane)) F64_TRACE(n, 5);
-            tc_fence_after();
-            const float4 *gam = reinterpret_cast<const float4 *>(sm + CH_G + s * D * 4) + 16 * kh;
-            {
-                uint32_t r[64];
-                tmem_ld32(tmem + lb + TM_D2 + 64u * kh, r);
-                tmem_ld32(tmem + lb + TM_D2 + 64u * kh + 32u, r + 32);
+            // ---- S^T <- S^T diag(gamma^B) + D2, one key half at a time, then bf16
+            bool got = true;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!wait_bar(bar(h ? B_D2FULL2 : B_D2FULL), n & 1)) {
+                    got = false;
+                    break;
+                }
+                if (h == 0 && elect_trace(warp, lane)) F64_TRACE(n, 5);
+                tc_fence_after();
+                const float4 *gam = reinterpret_cast<const float4 *>(sm + CH_G + s * D * 4 + (64 * h + 32 * wg) * 4);
+                uint32_t r[32];
+                tmem_ld32(tmem + lb + TM_D2 + 64u * h + 32u * wg, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j4 = 0; j4 < 16; ++j4) {
+                for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 g = gam[j4];
-                    const int c = 4 * j4;
-                    S[c] = fmaf(g.x, S[c], __uint_as_float(r[c]));
-                    S[c + 1] = fmaf(g.y, S[c + 1], __uint_as_float(r[c + 1]));
-                    S[c + 2] = fmaf(g.z, S[c + 2], __uint_as_float(r[c + 2]));
-                    S[c + 3] = fmaf(g.w, S[c + 3], __uint_as_float(r[c + 3]));
+                    const int c = 32 * h + 4 * j4;
+                    S[c] = fmaf(g.x, S[c], __uint_as_float(r[4 * j4]));
+                    S[c + 1] = fmaf(g.y, S[c + 1], __uint_as_float(r[4 * j4 + 1]));
+                    S[c + 2] = fmaf(g.z, S[c + 2], __uint_as_float(r[4 * j4 + 2]));
+                    S[c + 3] = fmaf(g.w, S[c + 3], __uint_as_float(r[4 * j4 + 3]));
                 }
+                if (h == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_FREE + s));  // this warp has read gamma^B
+                }
+                store_half(h);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FREE + s));  // this warp has read gamma^B
-            store_state();
+            if (!got) break;
             if (elect_trace(warp, lane)) F64_TRACE(n, 6);
         }
         if (p.h_final) {
             float *hf = p.h_final + ((size_t)seq * H + head) * D * D;
 #pragma unroll
-            for (int c = 0; c < KH; ++c) hf[(size_t)(KH * kh + c) * D + v] = S[c];
+            for (int c = 0; c < 64; ++c) hf[(size_t)(64 * (c >> 5) + 32 * wg + (c & 31)) * D + v] = S[c];
         }
     } else {
         regs_set<kRegsOut>();
@@ -990,6 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sbase + CH_BAR + 8u * B_SREADY, 8);
             mbar_init(sbase + CH_BAR + 8u * B_UREADY, 8);
             mbar_init(sbase + CH_BAR + 8u * B_ZREADY, 8);
+            mbar_init(sbase + CH_BAR + 8u * B_SREADY2, 8);
+            mbar_init(sbase + CH_BAR + 8u * B_D2FULL2, 1);
             for (int b = 0; b < 2; ++b) mbar_init(sbase + CH_BAR + 8u * (B_UFULL + b), 1);
         } else {
             mbar_init(sbase + PR_BAR, 1);
