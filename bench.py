@@ -944,6 +944,19 @@ def run_projection(args):
     flops = 2 * M * N * D
     peaks = measured_peaks()
     achieved = flops / mean_s / 1e12
+    # the same GEMM with bf16 output (kda_gate_projection_out), timed the same way
+    out16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        kda.gate_projection(x, w, b, out=out16)
+    torch.cuda.synchronize(dev)
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(args.steps):
+        kda.gate_projection(x, w, b, out=out16)
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    bf16_ms = b0.elapsed_time(b1) / args.steps
     # context: the same product through cuBLAS (torch.mm, bf16 out), not on the product path
     for _ in range(3):
         torch.mm(x, w.t())
@@ -973,6 +986,11 @@ def run_projection(args):
                                         "MEASURED_PEAKS.json)",
                          "algorithmic_flops_per_launch": flops},
             "cublas_bf16_mm_ms_context": round(cublas_ms, 4),
+            "bf16_output": {"ms_per_step": round(bf16_ms, 4),
+                            "tflops": round(flops / (bf16_ms * 1e-3) / 1e12, 1),
+                            "frac_of_bf16_peak": round(flops / (bf16_ms * 1e-3) / 1e12 /
+                                                       peaks["bf16_tflops"], 4),
+                            "api": "kda_gate_projection_out(..., KDA_BF16)"},
             "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernel_digest": kernel_source_digest(PROJ_SOURCES)}
     print(json.dumps(line), flush=True)

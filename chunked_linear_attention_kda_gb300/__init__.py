@@ -44,7 +44,8 @@ EXPORTED_SYMBOLS = ("kda_version", "kda_status_string", "kda_last_error",
                     "kda_chunk_fwd_from_host_pipelined", "kda_chunk_fwd_pipelined_workspace_bytes",
                     "kda_chunk_fwd_pipeline_plan", "kda_validate_cu_seqlens",
                     "kda_count_nonfinite", "kda_check_outputs",
-                    "kda_chunk_fwd_gated_workspace_bytes", "kda_chunk_fwd_gated")
+                    "kda_chunk_fwd_gated_workspace_bytes", "kda_chunk_fwd_gated",
+                    "kda_gate_projection_out")
 
 _lock = threading.Lock()
 _lib = None
@@ -137,6 +138,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                                                       I64, I32, I32, I32, I32, I32,
                                                                       ctypes.c_int, P]
         lib.kda_chunk_fwd_gated.restype = ctypes.c_int
+        lib.kda_gate_projection_out.argtypes = [P, P, P, P, ctypes.c_int, I64, I32, I32, P]
+        lib.kda_gate_projection_out.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -218,10 +221,11 @@ def chunk_fwd_simt(q, k, v, gate_logits, beta, h0=None, cu_seqlens=None, *, out=
                     out=out, h_final=h_final, output_final_state=output_final_state)
 
 
-def gate_projection(x, weight, bias=None, *, out=None):
-    """Gate logits ``a = x weight^T + bias`` through ``kda_gate_projection`` (tcgen05 GEMM):
-    ``x`` [N, d_model] bf16, ``weight`` [n_out, d_model] bf16, ``bias`` [n_out] fp32 or
-    None. Returns ``a`` [N, n_out] fp32 (view it as [N, H, d_k] for ``chunk_fwd``)."""
+def gate_projection(x, weight, bias=None, *, out=None, out_dtype=None):
+    """Gate logits ``a = x weight^T + bias`` through ``kda_gate_projection_out`` (tcgen05
+    GEMM): ``x`` [N, d_model] bf16, ``weight`` [n_out, d_model] bf16, ``bias`` [n_out] fp32
+    or None. Returns ``a`` [N, n_out] in ``out_dtype`` (fp32 by default -- view it as
+    [N, H, d_k] for ``chunk_fwd`` -- or bf16: the fp32 result rounded to nearest even)."""
     import torch
     lib = load_library()
     if x.device.type != "cuda":
@@ -237,11 +241,18 @@ def gate_projection(x, weight, bias=None, *, out=None):
     for t in (x, weight, bias):
         if t is not None and (not t.is_contiguous() or t.device != x.device):
             raise ValueError("all tensors must be contiguous and on one device")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be float32 or bfloat16")
     if out is None:
-        out = torch.empty((N, n_out), dtype=torch.float32, device=x.device)
+        out = torch.empty((N, n_out), dtype=out_dtype, device=x.device)
+    if out.dtype != out_dtype or tuple(out.shape) != (N, n_out) or not out.is_contiguous():
+        raise ValueError(f"out must be contiguous {out_dtype} with shape {(N, n_out)}")
     stream = torch.cuda.current_stream(x.device).cuda_stream
-    _check(lib, lib.kda_gate_projection(_ptr(x), _ptr(weight), _ptr(bias), _ptr(out), N, D, n_out,
-                                        ctypes.c_void_p(stream)))
+    _check(lib, lib.kda_gate_projection_out(_ptr(x), _ptr(weight), _ptr(bias), _ptr(out),
+                                            KDA_BF16 if out_dtype == torch.bfloat16 else KDA_F32,
+                                            N, D, n_out, ctypes.c_void_p(stream)))
     return out
 
 

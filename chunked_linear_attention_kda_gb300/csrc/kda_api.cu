@@ -502,32 +502,44 @@ kda_status kda_chunk_bwd_static_scratch(const void *q, const void *k, const void
                          n_seq, n_heads, d_k, d_v, dtype, stream);
 }
 
-kda_status kda_gate_projection(const void *x, const void *weight, const float *bias,
-                               float *gate_logits, int64_t n_tok, int32_t d_model,
-                               int32_t n_out, void *stream) {
-    if (!x || !weight || !gate_logits)
-        return n_tok == 0 ? ok() : fail(KDA_ERR_INVALID_ARG, "x, weight and gate_logits are required");
+kda_status kda_gate_projection_out(const void *x, const void *weight, const float *bias, void *out,
+                                   kda_dtype out_dtype, int64_t n_tok, int32_t d_model,
+                                   int32_t n_out, void *stream) {
+    if (out_dtype != KDA_F32 && out_dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "out_dtype must be KDA_F32 or KDA_BF16");
+    if (!x || !weight || !out)
+        return n_tok == 0 ? ok() : fail(KDA_ERR_INVALID_ARG, "x, weight and the output are required");
     if (n_tok < 0 || d_model <= 0 || n_out <= 0)
         return fail(KDA_ERR_INVALID_ARG, "n_tok must be >= 0, d_model and n_out positive");
     if (n_tok > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "n_tok above 2^31 - 1");
     if (d_model % 8 != 0)
         return fail(KDA_ERR_UNSUPPORTED, "d_model must be a multiple of 8 (16-byte rows for TMA)");
-    const void *a16[] = {x, weight, gate_logits};
+    const void *a16[] = {x, weight, out};
     for (const void *p : a16)
         if (!aligned16(p))
-            return fail(KDA_ERR_INVALID_ARG, "x, weight and gate_logits must be 16-byte aligned");
+            return fail(KDA_ERR_INVALID_ARG, "x, weight and the output must be 16-byte aligned");
     if (((uintptr_t)bias & 3u) != 0) return fail(KDA_ERR_INVALID_ARG, "bias must be 4-byte aligned");
-    const uintptr_t o = (uintptr_t)gate_logits, ob = (uintptr_t)n_tok * n_out * 4;
+    const size_t es = out_dtype == KDA_BF16 ? 2 : 4;
+    const uintptr_t o = (uintptr_t)out, ob = (uintptr_t)n_tok * n_out * es;
     struct Range { const void *p; size_t bytes; };
     const Range ins[] = {{x, (size_t)n_tok * d_model * 2}, {weight, (size_t)n_out * d_model * 2},
                          {bias, bias ? (size_t)n_out * 4 : 0}};
     for (const Range &r : ins)
         if (r.p && r.bytes && (uintptr_t)r.p < o + ob && o < (uintptr_t)r.p + r.bytes)
-            return fail(KDA_ERR_INVALID_ARG, "gate_logits may not overlap an input");
+            return fail(KDA_ERR_INVALID_ARG, "the output may not overlap an input");
     if (n_tok == 0) return ok();
-    return launched(kda::launch_gate_proj(x, weight, bias, gate_logits, (int)n_tok, n_out, d_model,
-                                          (cudaStream_t)stream),
-                    "gate projection launch");
+    const cudaError_t e =
+        out_dtype == KDA_BF16
+            ? kda::launch_gate_proj_bf16(x, weight, bias, out, (int)n_tok, n_out, d_model, (cudaStream_t)stream)
+            : kda::launch_gate_proj(x, weight, bias, static_cast<float *>(out), (int)n_tok, n_out, d_model,
+                                    (cudaStream_t)stream);
+    return launched(e, "gate projection launch");
+}
+
+kda_status kda_gate_projection(const void *x, const void *weight, const float *bias,
+                               float *gate_logits, int64_t n_tok, int32_t d_model,
+                               int32_t n_out, void *stream) {
+    return kda_gate_projection_out(x, weight, bias, gate_logits, KDA_F32, n_tok, d_model, n_out, stream);
 }
 
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,

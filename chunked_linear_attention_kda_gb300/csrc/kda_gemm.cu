@@ -11,7 +11,8 @@
 //              its lane 0 issues tcgen05.mma (M = 128, N = 256, K = 16; four per stage),
 //              committing each stage back to the producer and each finished tile to the
 //              epilogue;
-//   warps 2-5  epilogue: tcgen05.ld of their 32 accumulator lanes, + b, fp32 stores;
+//   warps 2-5  epilogue: tcgen05.ld of their 32 accumulator lanes, + b, fp32 stores (or
+//              bf16, rounded to nearest even, when the caller asks for bf16 output);
 //              tile i's epilogue overlaps tile i + 1's main loop (the second accumulator).
 // Tiles run n-fastest so that a 128-row slab of x is reused from L2 by every n tile while
 // W stays L2-resident. Out-of-range rows and the K tail are zero-filled by TMA and
@@ -118,9 +119,59 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <typename OutT>
+__device__ __forceinline__ void store_row32(OutT *dst, const uint32_t (&r)[32], const float *bias, int col0,
+                                            int N);
+// 32 consecutive outputs of one row: + bias, fp32
+template <>
+__device__ __forceinline__ void store_row32<float>(float *dst, const uint32_t (&r)[32], const float *bias,
+                                                   int col0, int N) {
+    if (col0 + 32 <= N && (N & 3) == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                   __uint_as_float(r[j + 3]));
+            if (bias) {
+                v.x += bias[col0 + j];
+                v.y += bias[col0 + j + 1];
+                v.z += bias[col0 + j + 2];
+                v.w += bias[col0 + j + 3];
+            }
+            *reinterpret_cast<float4 *>(dst + j) = v;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) dst[j] = __uint_as_float(r[j]) + (bias ? bias[col0 + j] : 0.f);
+    }
+}
+// the same rounded to bf16 (nearest even) after the bias is added in fp32
+template <>
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16 *dst, const uint32_t (&r)[32],
+                                                           const float *bias, int col0, int N) {
+    auto val = [&](int j) { return __uint_as_float(r[j]) + (bias ? bias[col0 + j] : 0.f); };
+    if (col0 + 32 <= N && (N & 7) == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(val(j + 2 * h), val(j + 2 * h + 1));
+                w[h] = *reinterpret_cast<uint32_t *>(&p2);
+            }
+            *reinterpret_cast<uint4 *>(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) dst[j] = __float2bfloat16_rn(val(j));
+    }
+}
+
+template <typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     gate_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                     const float *__restrict__ bias, float *__restrict__ out, int M, int N, int K) {
+                     const float *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K) {
     extern __shared__ unsigned char smraw[];
     __shared__ __align__(8) unsigned long long bars[2 * STAGES + 5];
     __shared__ uint32_t tmem_base;
@@ -224,27 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(ta + c * 32, r);
                 const int col0 = n0 + c * 32;
-                if (row < M) {
-                    float *dst = out + (size_t)row * N + col0;
-                    if (col0 + 32 <= N && (N & 3) == 0) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                   __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                            if (bias) {
-                                v.x += bias[col0 + j];
-                                v.y += bias[col0 + j + 1];
-                                v.z += bias[col0 + j + 2];
-                                v.w += bias[col0 + j + 3];
-                            }
-                            *reinterpret_cast<float4 *>(dst + j) = v;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) dst[j] = __uint_as_float(r[j]) + (bias ? bias[col0 + j] : 0.f);
-                    }
-                }
+                if (row < M) store_row32<OutT>(out + (size_t)row * N + col0, r, bias, col0, N);
             }
             tc_fence_before();
             __syncwarp();
@@ -288,13 +319,14 @@ bool encode_kmajor(CUtensorMap *m, const void *base, int rows, int K, int box_ro
 
 }  // namespace
 
-cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, float *out, int M,
-                             int N, int K, cudaStream_t stream) {
+template <typename OutT>
+cudaError_t launch_gate_proj_t(const void *x, const void *w, const float *bias, OutT *out, int M, int N,
+                               int K, cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     CUtensorMap mx, mw;
     if (!encode_kmajor(&mx, x, M, K, BM) || !encode_kmajor(&mw, w, N, K, BN))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gate_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gate_proj_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -303,10 +335,20 @@ cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, fl
         return e;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < sms ? tiles : sms;
-    gate_proj_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(mx, mw, bias, out, M, N, K);
+    gate_proj_kernel<OutT><<<grid, kThreads, SMEM_BYTES, stream>>>(mx, mw, bias, out, M, N, K);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
+}
+
+cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, float *out, int M,
+                             int N, int K, cudaStream_t stream) {
+    return launch_gate_proj_t<float>(x, w, bias, out, M, N, K, stream);
+}
+
+cudaError_t launch_gate_proj_bf16(const void *x, const void *w, const float *bias, void *out, int M,
+                                  int N, int K, cudaStream_t stream) {
+    return launch_gate_proj_t<__nv_bfloat16>(x, w, bias, static_cast<__nv_bfloat16 *>(out), M, N, K, stream);
 }
 
 cudaError_t read_gemm_flags(unsigned int *flags, bool reset, cudaStream_t stream) {

@@ -88,6 +88,9 @@ cudaError_t static_scratch(void **ptr);
 // (tcgen05 GEMM, kda_gemm.cu). K % 8 == 0, x, W and a 16-byte aligned.
 cudaError_t launch_gate_proj(const void *x, const void *w, const float *bias, float *out, int M,
                              int N, int K, cudaStream_t stream);
+// the same with bf16 output (the fp32 sum + bias rounded to nearest even)
+cudaError_t launch_gate_proj_bf16(const void *x, const void *w, const float *bias, void *out, int M,
+                                  int N, int K, cudaStream_t stream);
 // The GEMM's own status word (bit 1: a pipeline wait gave up); synchronises stream.
 cudaError_t read_gemm_flags(unsigned int *flags, bool reset, cudaStream_t stream);
 // The backward serial passes' status word (bit 2); synchronises stream.

@@ -237,6 +237,18 @@ kda_status kda_gate_projection(const void *x, const void *weight, const float *b
                                int32_t n_out, void *stream);
 
 /*
+ * kda_gate_projection_out -- kda_gate_projection with the output type chosen: `out` is
+ * [n_tok, n_out] of `out_dtype` (KDA_F32: as kda_gate_projection; KDA_BF16: the fp32 sum
+ * plus bias rounded to the nearest bf16, ties to even -- half the output bytes, for
+ * callers that keep activations in bf16; kda_chunk_fwd itself takes fp32 gate logits).
+ * Same arguments, alignment and errors otherwise, plus KDA_ERR_UNSUPPORTED for another
+ * out_dtype.
+ */
+kda_status kda_gate_projection_out(const void *x, const void *weight, const float *bias, void *out,
+                                   kda_dtype out_dtype, int64_t n_tok, int32_t d_model,
+                                   int32_t n_out, void *stream);
+
+/*
  * kda_affine_combine -- combine step of the segment scan for one sequence split in
  * time (an addition of this library; the pages describe only the serial recurrence,
  * "From Numerical Stability to Load Balancing", §2.1, and this step follows from it).

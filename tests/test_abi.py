@@ -215,6 +215,23 @@ def test_gate_projection_nothing_to_do_is_ok(lib):
     assert proj(lib, n_tok=0) == 0
 
 
+def proj_out(lib, *, x=FAKE, w=2 * FAKE, b=None, a=4 * FAKE, dt=1, n_tok=64, d=128, n_out=256):
+    P = ctypes.c_void_p
+    return lib.kda_gate_projection_out(P(x), P(w), P(b), P(a), dt, n_tok, d, n_out, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dt=2), 2), (dict(dt=-1), 2), (dict(a=None), 1), (dict(a=4 * FAKE + 8), 1),
+    (dict(d=100), 2), (dict(x=FAKE + 8), 1), (dict(b=3 * FAKE + 2), 1),
+    # bf16 output of 64 x 256: 32 KiB from 4 FAKE, overlapping x (64 x 128 bf16 at FAKE)
+    (dict(a=FAKE + 64), 1),
+])
+def test_gate_projection_out_host_validation(lib, kw, status):
+    st = proj_out(lib, **kw)
+    assert st == status, (kw, st, lib.kda_last_error())
+    assert lib.kda_last_error().decode() != ""
+
+
 @pytest.mark.parametrize("capacity", [0, -3, 1025])
 def test_backward_timing_rejects_capacity(lib, capacity):
     assert lib.kda_bwd_timing_start(capacity) == 1

@@ -41,6 +41,18 @@ def test_projection_shapes(M, D, N, bias):
     assert e <= 1e-5, f"{(M, D, N)}: {e:.3e}"
 
 
+@pytest.mark.parametrize("M,D,N,bias", [(128, 64, 256, True), (257, 72, 250, True),
+                                        (1, 8, 4, False), (1000, 512, 4096, True)])
+def test_bf16_output_is_the_fp32_output_rounded(M, D, N, bias):
+    """bf16 output (N a multiple of 8 takes the packed stores, else the scalar ones): the
+    fp32 result plus bias rounded to nearest even, bit for bit."""
+    x, w, b = make(M, D, N, bias, seed=M + 2 * N)
+    a32 = kda.gate_projection(x, w, b)
+    a16 = kda.gate_projection(x, w, b, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert a16.dtype == torch.bfloat16 and torch.equal(a16, a32.to(torch.bfloat16))
+
+
 def test_bench_problem_sampled_rows():
     M, D, N = 65536, 4096, 4096
     x, w, b = make(M, D, N, True, seed=3)
