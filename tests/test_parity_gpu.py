@@ -183,3 +183,30 @@ def test_no_final_state_requested():
     assert hf is None
     o2, _ = gpu_forward(x)
     assert torch.equal(out, o2)
+
+
+def test_16_token_kernel_still_matches():
+    """The previous 16-token tensor-core kernel, still selectable with KDA_FWD_KERNEL=tc16
+    (read once per process, hence the subprocess): the same parity bars on a ragged case."""
+    import os
+    import subprocess
+    import sys
+    code = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, ".")
+import kda_inputs as K
+from tests.gpu_helpers import gpu_forward, oracle_forward, per_seq_head_rel, per_state_rel, rel_l2, to_np
+x = K.make_inputs([300, 1, 1000, 64], 4, 128, 128, device="cuda", seed=19, h0_std=0.1)
+out, hf = gpu_forward(x)
+o_ref, h_ref = oracle_forward(x)
+og, hg = to_np(out), to_np(hf)
+w = max(rel_l2(og, o_ref), rel_l2(hg, h_ref), per_seq_head_rel(og, o_ref, x.cu_host, 16), per_state_rel(hg, h_ref))
+print("WORST", w)
+'''
+    env = dict(os.environ, KDA_FWD_KERNEL="tc16")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    worst = float(r.stdout.split("WORST")[-1])
+    assert worst <= 1e-2, worst
