@@ -511,7 +511,7 @@ def run_ours(args):
     diagnostics = output_diagnostics(kda, out, hf)
 
     # end-to-end through the host-buffer entry point
-    e2e = measure_e2e(x, dev, stream, max(1, min(args.steps, 10)), kda)
+    e2e = measure_e2e(x, dev, stream, max(1, min(args.steps, 20)), kda)
     e2e["value"] = e2e["value"] * world
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -575,8 +575,8 @@ def measure_e2e(x, dev, stream, steps, kda):
         kda.chunk_fwd_from_host(*args)
 
     def timed(call):
-        """(median, mean) over ``steps`` back-to-back calls, each bracketed by CUDA events
-        on the stream (every call ends with the stream waiting for its last copy)."""
+        """(median, mean, max) over ``steps`` back-to-back calls, each bracketed by CUDA
+        events on the stream (every call ends with the stream waiting for its last copy)."""
         call()
         torch.cuda.synchronize(dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
@@ -586,21 +586,22 @@ def measure_e2e(x, dev, stream, steps, kda):
             ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
         per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-        return statistics.median(per), ev[0].elapsed_time(ev[steps]) / steps
+        return statistics.median(per), ev[0].elapsed_time(ev[steps]) / steps, max(per)
 
     def inputs_only():  # the floor: the step's host-to-device bytes alone
         for name, t in host.items():
             if t is not None:
                 devb[name].copy_(t, non_blocking=True)
 
-    ms, ms_mean = timed(pipelined)
-    ms_serial, _ = timed(serial)
+    ms, ms_mean, ms_max = timed(pipelined)
+    ms_serial, _, _ = timed(serial)
     with torch.cuda.stream(stream):
-        ms_h2d, _ = timed(inputs_only)
+        ms_h2d, _, _ = timed(inputs_only)
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = h_out.numel() * h_out.element_size() + h_hf.numel() * 4
     return {"value": round(x.n_tok / (ms * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(ms, 3), "mean_ms_per_step": round(ms_mean, 3),
+            "max_ms_per_step": round(ms_max, 3),
             "statistic": f"median of {steps} event-timed calls",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "api": f"kda_chunk_fwd_from_host_pipelined (pinned host buffers, {segments} "
