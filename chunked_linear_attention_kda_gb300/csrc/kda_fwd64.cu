@@ -13,11 +13,9 @@
 // step:
 //   A  = strict_lower(diag(beta) [K K^T with the factors above])     64 x 64
 //   P  = lower([Q K^T with the same factors])                        64 x 64
-//   TB = (I + A)^-1 diag(beta),   W = TB K~B,   K~B = K exp(G^B)
-//   Q' = Q~B - P W,               P' = P TB,    K'B = K exp(G^B_end - G^B)
-//   U  = TB (V - K~B S) = TB V - W S,   O = d_k^-1/2 (Q~B S + P U),
+//   TB = (I + A)^-1 diag(beta),   K~B = K exp(G^B),   K'B = K exp(G^B_end - G^B)
+//   U  = TB (V - K~B S),   O = d_k^-1/2 (Q~B S + P U),
 //   S <- Diag(exp G^B_end) S + K'B^T U
-// (equivalently O = d_k^-1/2 (P' V + Q' S) with U substituted).
 //
 // Work decomposition: one cluster of 1 + kPro CTAs per (sequence, head).
 //  * rank 0, the chain CTA, runs the serial recurrence. Transposed, with the state S^T
@@ -25,7 +23,7 @@
 //        D1[:, 0..63]   = S^T K~B^T = Y^T,  then  Z^T TB^T = U^T  with Z^T = V^T - Y^T
 //        D1[:, 64..127] = S^T Q~B^T + U^T P^T          = O^T / scale
 //        D2             = U^T K'B                      (the state increment)
-//    (U = TB (V - K~B S) = TB V - W S.) The Y^T, U^T and D2 groups lie on the state's
+//    The Y^T, U^T and D2 groups lie on the state's
 //    critical path; the O^T products fill the tensor pipe while U^T is formed and while
 //    the state is updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
 //    value row and 64 keys per thread) and is mirrored as bf16 into tensor memory as the
@@ -35,8 +33,8 @@
 //    buffers; the products arrive in one of three operand slots.
 //  * ranks 1..kPro, the prologue CTAs, each compute every kPro-th step's operands (the
 //    gate, the four tiles' scaled operands, [A; P] as one tcgen05 product, the 64 x 64
-//    solve for TB) into a staging buffer laid
-//    out exactly as the chain CTA's operand slot, and copy it there with bulk copies
+//    solve for TB) into a staging buffer laid out exactly as the chain CTA's operand
+//    slot, and copy it there with bulk copies
 //    (shared::cta -> shared::cluster) once the chain CTA has freed the slot (with three
 //    slots and three prologue CTAs, each prologue CTA always fills the same slot).
 // Every wait is bounded: one that exceeds its limit sets bit 3 of the status word
@@ -56,10 +54,13 @@ namespace kda {
 __device__ unsigned int g_fwd64_flags;  // bit 3: a pipeline wait exceeded its limit
 
 // Phase timestamps (SM clock) of the first cluster's first 64 steps: a profiling aid
-// compiled only with -DKDA_FWD64_TRACE. Slots 0-6 (chain CTA, per step): loop top, state
-// products issued, D1 complete, U stored, state-update products issued, D2 complete,
-// state stored; slots 8-15 (the prologue CTA owning the step): loop top, raw tiles in,
-// gate, cross-tile decays, A and P, solve, W and Q', P' (copy issued at slot 7).
+// compiled only with -DKDA_FWD64_TRACE. Chain CTA, per step: 0 state-warp loop top,
+// 1 Y^T products issued, 2 Y^T complete, 3 U^T stored, 4 every product of the step
+// issued, 5 D2 keys 0..63 complete, 6 state stored. The prologue CTA owning the step:
+// 8 loop top, 9 raw tiles in, 20 / 26 gate pass done (first / last thread), 10 next
+// fetch issued, 11 operands written, 21 [A; P] issued, 22 / 24 [A; P] complete, 23 A
+// and P read out, 12 read-out barrier, 16 diagonal T tiles, 17 M, 18 M^2, 27 TB tiles,
+// 13 staging slot complete, 7 copy issued.
 #ifdef KDA_FWD64_TRACE
 __device__ long long g_f64_trace[64][32];
 #define F64_TRACE(n, slot)                                      \
@@ -133,7 +134,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // ---- prologue CTA shared memory
 constexpr int PR_Q = 0, PR_K = 16384, PR_A = 32768;  // raw tiles [64 t][128 c] (TMA)
-// X: the operands of the A / P product, then those of the W / Q' product. Every operand
+// X: the operands of the [A; P] product, then the solve's fp32 scratch tiles. Every operand
 // here is a set of 128 channel rows of 64 tokens (128-byte rows, 128-byte swizzle), which
 // the tensor core reads MN-major (tokens along M or N, channels along K) or K-major
 // (channels along N, tokens along K).
@@ -619,10 +620,9 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         bulk_commit();
     };
     fetch(prank, 0);
-    // tensor memory for the products. B1 starts at zero: the tiles of TB above the
-    // diagonal are never written, and P' is then exactly zero there too, so every later
-    // P finds zeros above its diagonal tiles. The unused last 32 columns of the column
-    // tiles are zeroed once (their products are never read).
+    // tensor memory for the products. B1 starts at zero: the tiles of TB and of P above
+    // the diagonal are never written, so they stay zero in every step's slot. The unused
+    // last 32 columns of the column tiles are zeroed once (their products are never read).
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kProTmemCols);
     for (int i = tid; i < 16384 / 16; i += kThreads) {
         reinterpret_cast<uint4 *>(sm + PR_STG + SL_B1)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -959,7 +959,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         tc_fence_before();
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 13);
-        // ---- P6: into the chain CTA's slot m % NSLOT once step m - NSLOT has consumed it
+        // ---- P5: into the chain CTA's slot m % NSLOT once step m - NSLOT has consumed it
         if (tid == 0 && !bad) {
             if (m >= NSLOT) {
                 bad = !wait_bar(slotfree, nfree & 1);
