@@ -610,6 +610,15 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             cp_async_commit();
         }
     };
+    // the raw tiles of step m into L2, two owned steps before they are loaded, so that the
+    // load issued after a gate pass finds them there
+    auto prefetch = [&](int m) {
+        if (m >= nblocks || warp != 15 || lane != 0) return;
+        const int r0 = t0 + m * BT;
+        tma_prefetch_3d(tm_a, 0, head, r0);
+        tma_prefetch_3d(tm_q, 0, head, r0);
+        tma_prefetch_3d(tm_k, 0, head, r0);
+    };
     // the staging slot into the chain CTA's slot m % NSLOT (operands) and gamma ring entry;
     // completion (SLOT_BYTES in all) is counted on that slot's FULL barrier
     auto copy_out = [&](int m) {
@@ -619,7 +628,24 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         bulk_copy_to_peer(map_to_rank(sbase + CH_G + s * D * 4, 0), stg + SL_G, D * 4, full);
         bulk_commit();
     };
+    // exp(g) = exp(-5 sigmoid(a)) in place over the raw gate-logit tile, by the threads
+    // [first, first + count): the gate pass of a step then reads exp(g) directly. The
+    // MUFU-bound exponentials of the next owned step run on the warps the solve leaves
+    // idle.
+    auto exp_gate_inplace = [&](int first, int count) {
+        float4 *ra4 = reinterpret_cast<float4 *>(sm + PR_A);
+#pragma unroll 4
+        for (int i = tid - first; i < BT * D / 4; i += count) {
+            float4 v = ra4[i];
+            v.x = __expf(kGMin * __fdividef(1.f, 1.f + __expf(-v.x)));
+            v.y = __expf(kGMin * __fdividef(1.f, 1.f + __expf(-v.y)));
+            v.z = __expf(kGMin * __fdividef(1.f, 1.f + __expf(-v.z)));
+            v.w = __expf(kGMin * __fdividef(1.f, 1.f + __expf(-v.w)));
+            ra4[i] = v;
+        }
+    };
     fetch(prank, 0);
+    prefetch(prank + kPro);
     // tensor memory for the products. B1 starts at zero: the tiles of TB and of P above
     // the diagonal are never written, so they stay zero in every step's slot. The unused
     // last 32 columns of the column tiles are zeroed once (their products are never read).
@@ -632,18 +658,23 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
     __syncthreads();
     tc_fence_after();
     const uint32_t ptmem = *tmem_slot;
-    bool bad = false;   // (thread 0) a wait gave up
+    bool bad = false;   // a wait of this thread gave up (thread 0: slots; warps 8-15: raw tiles)
     int nfree = 0;      // slot-free signals consumed (thread 0)
+    if (prank < nblocks) {  // the first owned step's raw tiles, exp(g) by every thread
+        bad = !wait_bar(rawfull, 0);
+        if (!bad) exp_gate_inplace(0, kThreads);
+        fence_proxy_async();  // generic writes of the raw tile -> the next TMA into it
+    }
     int k = 0;
     for (int m = prank; m < nblocks; m += kPro, ++k) {
         const int L = min(BT, t1 - (t0 + m * BT));
         const float *bet = reinterpret_cast<const float *>(sm + PR_BETA) + (k & 1) * BT;
-        // ---- P0: this step's raw tiles are in
+        // ---- P0: this step's raw tiles are in, exp(g) already formed over the gate tile
+        //      (before the loop, or by warps 8-15 during the previous owned step's solve)
         if (tid == 0) F64_TRACE(m, 8);
-        if (tid == 0 && !bad) bad = !wait_bar(rawfull, k & 1);
         if (warp == 15) cp_async_wait0();
         if (__syncthreads_or(bad)) break;
-        if (tid != 0) mbar_try(rawfull, k & 1);  // observe the completed phase
+        mbar_try(rawfull, k & 1);  // observe the completed phase (the q and k tiles)
         if (tid == 0) F64_TRACE(m, 9);
         // ---- P1: gate pass, one (key channel c, tile I) per thread: exp(g) of its 16
         //      tokens and the inclusive within-tile decay Gamma_r = exp(G_r)
@@ -655,14 +686,12 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             const unsigned short *rq = reinterpret_cast<const unsigned short *>(sm + PR_Q);
             const unsigned short *rk = reinterpret_cast<const unsigned short *>(sm + PR_K);
 #pragma unroll
-            for (int r = 0; r < TL; ++r) eg[r] = ra[(rb + r) * D + c];
-#pragma unroll
-            for (int r = 0; r < TL; ++r) eg[r] = __fdividef(1.f, 1.f + __expf(-eg[r]));  // sigmoid
+            for (int r = 0; r < TL; ++r) eg[r] = ra[(rb + r) * D + c];  // exp(g), g = -5 sigmoid(a)
             float gam = 1.f;
 #pragma unroll
             for (int r = 0; r < TL; ++r) {
                 const bool in = rb + r < L;
-                const float e = __expf(kGMin * eg[r]);  // exp(g), g = -5 sigmoid(a)
+                const float e = eg[r];
                 eg[r] = in ? e : 1.f;
                 kq[r] = in ? ((uint32_t)rk[(rb + r) * D + c] | ((uint32_t)rq[(rb + r) * D + c] << 16)) : 0u;
                 gam *= eg[r];
@@ -674,6 +703,7 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         if (tid == 511) F64_TRACE(m, 26);
         __syncthreads();
         fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
+        prefetch(m + 2 * kPro);
         if (tid == 0) F64_TRACE(m, 10);
         // ---- P2: every scaled operand of this (channel, tile), from fp32 values:
         //   R = [K~ | Q~] (K~ = K Gamma), the column tiles K^ = K / Gamma and
@@ -954,8 +984,15 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
                 }
             }
             if (tid == 0) F64_TRACE(m, 27);
+        } else if (m + kPro < nblocks) {
+            // warps 8-15: the next owned step's raw tiles (fetched after this step's gate
+            // pass) and exp(g) in place over its gate tile
+            bad = !wait_bar(rawfull, (k + 1) & 1);
+            if (!bad) exp_gate_inplace(8 * 32, kThreads - 8 * 32);
+            if (tid == 256) F64_TRACE(m, 28);
         }
-        fence_proxy_async();  // generic writes of the staging slot -> the bulk copy's reads
+        fence_proxy_async();  // generic writes of the staging slot (and of the gate tile) -> the
+                              // bulk copy's reads (and the next TMA into the tile)
         tc_fence_before();
         __syncthreads();
         if (tid == 0) F64_TRACE(m, 13);
