@@ -89,12 +89,14 @@ constexpr float kScale = 0.08838834764831845f;  // 128^-1/2
 static_assert(NT == 4, "the tile-pair tables below assume four tiles per step");
 
 // ---- operand slot (identical layout in the chain CTA's ring and a prologue's staging)
-// B1: [n][j] K-major, 128-byte swizzle: rows 0..63 = TB, rows 64..127 = P    (K = tokens)
+// B1: [n][j] K-major rows, 128-byte swizzle (K = tokens): rows 0..63 = TB, rows 64..127 = P,
+//     rows 128..255 = K'B^T ([c][t]); rows 64..255 are one 192-row operand [P; K'B^T]
 // B2: bytes 0..16383: K~B, bytes 16384..32767: Q~B, each [c][t] (128 channel rows of 64
-//     tokens, read MN-major: tokens along N, channels along K)
-// B3: [c][t] K-major: K'B^T (K = tokens)
+//     tokens). K~B is read K-major as the A operand of W^T = K~B^T TB^T and then
+//     overwritten in the chain CTA by -W^T; [-W^T | Q~B^T] is then read as one MN-major
+//     operand (tokens along N, channels along K)
 // G : gamma^B[c] = exp(G^B_end), fp32
-constexpr int SL_B1 = 0, SL_B2 = 16384, SL_B3 = 49152, SL_G = 65536;
+constexpr int SL_B1 = 0, SL_B3 = 16384, SL_B2 = 32768, SL_G = 65536;
 constexpr int B2_QB = 16384;  // offset of Q~B inside B2
 constexpr int SLOT_BYTES = SL_G + D * 4;  // 66048 (the gamma^B vector lives in its own ring)
 constexpr int SLOT_STRIDE = SL_G;         // 64 KB per slot: every slot 1024-byte aligned
@@ -111,25 +113,25 @@ static_assert(CH_V % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 // barrier indices (8 bytes each)
 constexpr int B_FULL = 0;     // [NSLOT] slot s: products (bulk copies) + V (TMA) landed
 constexpr int B_FREE = 3;     // [NSLOT] slot s: its MMAs completed and gamma read (1 + 8 arrivals)
-constexpr int B_D1U = 6;      // [2] D1 buffer b: Y^T = S^T K~B^T complete
-constexpr int B_D1FREE = 8;   // [2] D1 buffer b read out by the output warps (4 arrivals)
+constexpr int B_UFULL = 6;    // [U | O] += S^T [-W^T | Q~B^T] complete
+constexpr int B_WFULL = 7;    // W^T = K~B^T TB^T complete
+constexpr int B_OFREE = 8;    // O read out and zeroed (4 output-warp arrivals)
+constexpr int B_OFULL = 9;    // O^T complete
 constexpr int B_D2FULL = 10;  // D2 complete
 constexpr int B_DRAIN = 11;   // every MMA complete (before the tensor memory is released)
-constexpr int B_D1O = 12;     // [2] D1 buffer b: O^T complete
-constexpr int B_SREADY = 14;  // the state's bf16 copy is in tensor memory (8 warp arrivals)
-constexpr int B_UREADY = 15;  // U^T's bf16 copy is in tensor memory (8 warp arrivals)
-constexpr int B_UFULL = 16;   // [2] D1 buffer b: U^T = Z^T TB^T complete
-constexpr int B_ZREADY = 18;  // Z^T = V^T - Y^T in bf16 is in tensor memory (8 warp arrivals)
-constexpr int B_SREADY2 = 19; // the state's keys 64..127 in bf16 (B_SREADY: keys 0..63)
-constexpr int B_D2FULL2 = 20; // D2 keys 64..127 complete (B_D2FULL: keys 0..63)
-constexpr int NBARS = 21;
+constexpr int B_SREADY = 12;  // the state's keys 0..63 in bf16 are in tensor memory (8 warp arrivals)
+constexpr int B_SREADY2 = 13; // the state's keys 64..127 in bf16
+constexpr int B_UREADY = 14;  // U^T's bf16 copy is in tensor memory (8 warp arrivals)
+constexpr int B_WREADY = 15;  // -W^T in bf16 is in the step's slot (4 output-warp arrivals)
+constexpr int NBARS = 16;
 static_assert(NSLOT == 3 && B_FREE == NSLOT, "barrier table");
-// tensor-memory columns
-constexpr uint32_t TM_D1 = 0;     // 2 x 128 columns
-constexpr uint32_t TM_D2 = 256;   // 128 columns
-constexpr uint32_t TM_AS = 384;   // S^T bf16: 64 columns (128 keys)
-constexpr uint32_t TM_AU = 448;   // U^T bf16: 32 columns (64 tokens)
-constexpr uint32_t TM_AZ = 480;   // Z^T bf16: 32 columns (64 tokens)
+// tensor-memory columns: [U | O] and [O | D2] are each one contiguous MMA destination
+constexpr uint32_t TM_U = 0;      // U^T fp32: 64 columns (64 tokens)
+constexpr uint32_t TM_O = 64;     // O^T fp32: 64 columns
+constexpr uint32_t TM_D2 = 128;   // D2 fp32: 128 columns (keys)
+constexpr uint32_t TM_W = 256;    // W^T fp32: 64 columns (keys on the lanes)
+constexpr uint32_t TM_AS = 320;   // S^T bf16: 64 columns (128 keys)
+constexpr uint32_t TM_AU = 384;   // U^T bf16: 32 columns (64 tokens)
 constexpr uint32_t kTmemCols = 512;
 
 // ---- prologue CTA shared memory
@@ -252,7 +254,8 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         regs_set<kRegsMisc>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------- producer: V tiles
-            // step m's V goes to buffer m & 1, last read (by the state warps) in step m - 2
+            // step m's V goes to buffer m & 1; its last reader, the V^T TB^T product of step
+            // m - 2, completes before slot m - 2 is released
             for (int m = 0; m < nblocks; ++m) {
                 if (m >= 2 && !wait_bar(bar(B_FREE + (m - 2) % NSLOT), ((m - 2) / NSLOT) & 1)) break;
                 const int s = m % NSLOT;
@@ -272,65 +275,91 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             }
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------- MMA issuer
-            // Per step n (slot s, D1 buffer b), in tensor-pipe order:
-            //   S^T K~B^T       -> D1 columns 0..63   = Y^T (keys 0..63 as soon as they are
-            //                      in, then 64..127); commit D1U
-            //   S^T Q~B^T       -> D1 columns 64..127
-            //   Z^T TB^T        -> D1 columns 0..63   = U^T (Z^T = V^T - Y^T from the state warps); commit UFULL
-            //   U^T K'B         -> D2, keys 0..63 then 64..127; commit D2FULL, D2FULL2
-            //   U^T P^T         -> D1 columns 64..127 = O^T / scale; commit D1O, FREE
-            const uint32_t id_t = idesc_bf16(128, 64, 0, 0);   // N = 64 tokens, B K-major
-            const uint32_t id_q = idesc_bf16(128, 64, 0, 1);   // N = 64 tokens, B MN-major
+            // A tcgen05.mma costs about the same to issue whatever its N, so products that
+            // share an A operand go out as one wide MMA. Per step n (slot s):
+            //   [U | O]  += S^T [-W^T | Q~B^T]      N = 128, keys 0..63 as soon as they are
+            //                                       in, then 64..127; commit UFULL
+            //   W of step n + 1: K~B^T TB^T          N = 64 (once its slot is in); commit WFULL
+            //   [O | D2] += U^T [P^T | K'B]          N = 192; commit D2FULL, OFULL, FREE
+            //   U of step n + 1: V^T TB^T            N = 64 (starts the next U)
+            // O and D2 are zeroed by the warps that read them, so every product after the
+            // first of U accumulates.
+            const uint32_t id_w = idesc_bf16(128, 64, 0, 0);    // A and B K-major
+            const uint32_t id_v = idesc_bf16(128, 64, 1, 0);    // A MN-major (V^T)
+            const uint32_t id_1 = idesc_bf16(128, 128, 0, 1);   // B MN-major [-W^T | Q~B^T]
+            const uint32_t id_2 = idesc_bf16(128, 192, 0, 0);   // B K-major [P; K'B^T]
             // slot s's descriptors are slot 0's plus s x the slot stride (16-byte units)
-            const uint64_t dB10 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
-            const uint64_t dKB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 8192, 1024);
-            const uint64_t dQB0 = sdesc_sw128(sbase + CH_SLOT + SL_B2 + B2_QB, 8192, 1024);
-            const uint64_t dB30 = sdesc_sw128(sbase + CH_SLOT + SL_B3, 16, 1024);
+            const uint64_t dTB0 = sdesc_sw128(sbase + CH_SLOT + SL_B1, 16, 1024);
+            const uint64_t dPK0 = sdesc_sw128(sbase + CH_SLOT + SL_B1 + BT * 128, 16, 1024);
+            const uint64_t dWQ0 = sdesc_sw128(sbase + CH_SLOT + SL_B2, B2_QB, 1024);   // MN-major
+            const uint64_t dKA0 = sdesc_sw128(sbase + CH_SLOT + SL_B2, 16, 1024);      // K-major
+            const uint64_t dV0 = sdesc_sw128(sbase + CH_V, V_BYTES / 2, 1024);       // V^T, MN-major
             constexpr uint64_t kSlotStep = SLOT_STRIDE >> 4;
-            constexpr uint64_t kLow = (64 * 128) >> 4;  // rows 64..127 of a K-major operand
-            for (int n = 0; n < nblocks; ++n) {
-                const int s = n % NSLOT, b = n & 1;
-                const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
+            constexpr uint64_t kVStep = V_BYTES >> 4;
+            auto issue_w = [&](int m) {  // W^T of step m
+                const uint64_t so = (uint64_t)(m % NSLOT) * kSlotStep;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
+                    umma_ss(tmem + TM_W, dKA0 + so + (uint64_t)(2 * j), dTB0 + so + (uint64_t)(2 * j), id_w, j > 0);
+                umma_commit(bar(B_WFULL));
+            };
+            auto issue_vtb = [&](int m) {  // U of step m starts as V^T TB^T
+                const uint64_t so = (uint64_t)(m % NSLOT) * kSlotStep;
+                const uint64_t vo = (uint64_t)(m & 1) * kVStep;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)  // 16 token rows (2048 bytes) of V per MMA
+                    umma_ss(tmem + TM_U, dV0 + vo + (uint64_t)(128 * j), dTB0 + so + (uint64_t)(2 * j), id_v, j > 0);
+            };
+            bool ok = true;
+            if (nblocks > 0) {
+                ok = wait_bar(bar(B_FULL), 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_w(0);
+                    issue_vtb(0);
+                }
+            }
+            for (int n = 0; ok && n < nblocks; ++n) {
+                const int s = n % NSLOT;
                 const uint64_t so = s * kSlotStep;
-                if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;           // step n's operands
-                if (n >= 2 && !wait_bar(bar(B_D1FREE + b), ((n >> 1) - 1) & 1)) break;  // D1 read out
-                if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T keys 0..63 (bf16) of step n are in
+                if (!wait_bar(bar(B_WREADY), n & 1)) break;  // -W^T of step n is in slot s
+                if (!wait_bar(bar(B_OFREE), n & 1)) break;   // O read out and zeroed
+                if (!wait_bar(bar(B_SREADY), n & 1)) break;  // S^T keys 0..63 (bf16) of step n
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // 16 channel rows (2048 bytes) per MMA
-                    umma_ts(d1, tmem + TM_AS + 8u * k, dKB0 + so + (uint64_t)(128 * k), id_q, k > 0);
+                    umma_ts(tmem + TM_U, tmem + TM_AS + 8u * k, dWQ0 + so + (uint64_t)(128 * k), id_1, 1);
                 if (!wait_bar(bar(B_SREADY2), n & 1)) break;  // keys 64..127
                 tc_fence_after();
 #pragma unroll
                 for (int k = 4; k < 8; ++k)
-                    umma_ts(d1, tmem + TM_AS + 8u * k, dKB0 + so + (uint64_t)(128 * k), id_q, 1);
-                umma_commit(bar(B_D1U + b));
+                    umma_ts(tmem + TM_U, tmem + TM_AS + 8u * k, dWQ0 + so + (uint64_t)(128 * k), id_1, 1);
+                umma_commit(bar(B_UFULL));
                 F64_TRACE(n, 1);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    umma_ts(d1 + 64u, tmem + TM_AS + 8u * k, dQB0 + so + (uint64_t)(128 * k), id_q, k > 0);
-                if (!wait_bar(bar(B_ZREADY), n & 1)) break;  // Z^T (bf16) of step n is in
-                tc_fence_after();
-#pragma unroll
-                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
-                    umma_ts(d1, tmem + TM_AZ + 8u * j, dB10 + so + (uint64_t)(2 * j), id_t, j > 0);
-                umma_commit(bar(B_UFULL + b));
+                // W of the next step while the state warps convert U^T, if its slot is in
+                bool wnext = false;
+                if (n + 1 < nblocks && mbar_try(bar(B_FULL + (n + 1) % NSLOT), ((n + 1) / NSLOT) & 1)) {
+                    tc_fence_after();
+                    issue_w(n + 1);
+                    wnext = true;
+                }
                 if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // D2 keys 64 h .. 64 h + 63 (B3 rows), one commit each
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        umma_ts(tmem + TM_D2 + 64u * h, tmem + TM_AU + 8u * j, dB30 + so + h * kLow + (uint64_t)(2 * j),
-                                id_t, j > 0);
-                    umma_commit(bar(h ? B_D2FULL2 : B_D2FULL));
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    umma_ts(d1 + 64u, tmem + TM_AU + 8u * j, dB10 + so + kLow + (uint64_t)(2 * j), id_t, 1);
-                umma_commit(bar(B_D1O + b));
+                for (int j = 0; j < 4; ++j)  // K = 16 tokens per MMA
+                    umma_ts(tmem + TM_O, tmem + TM_AU + 8u * j, dPK0 + so + (uint64_t)(2 * j), id_2, 1);
+                umma_commit(bar(B_D2FULL));
+                umma_commit(bar(B_OFULL));
                 umma_commit(bar(B_FREE + s));
                 F64_TRACE(n, 4);
+                if (n + 1 < nblocks) {
+                    if (!wnext) {
+                        if (!wait_bar(bar(B_FULL + (n + 1) % NSLOT), ((n + 1) / NSLOT) & 1)) break;
+                        tc_fence_after();
+                        issue_w(n + 1);
+                    }
+                    issue_vtb(n + 1);  // U of step n has been read (UREADY above)
+                }
             }
             // every MMA has completed before the tensor memory is released
             umma_commit(bar(B_DRAIN));
@@ -342,11 +371,14 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
         // Thread (value row v = TMEM lane, warpgroup wg) holds S^T[v][k] in fp32 registers
         // for the keys k = 64 h + 32 wg + j (h = 0, 1; j < 32): each half of the keys is
         // split over both warpgroups, so that each half is updated, converted and handed to
-        // the issuer (SREADY, SREADY2) while the other is still being produced. Each warp
+        // the issuer (SREADY, SREADY2) while the other is still being updated. Each warp
         // signals the issuer on its own (8 arrivals per barrier).
         const int wg = (warp - 4) >> 2;
         const int v = ((warp & 3) << 5) + lane;                 // value row = TMEM lane
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;  // lane quarter
+        uint32_t zero[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) zero[j] = 0u;
         float S[64];  // S[32 h + j] = S^T[v][64 h + 32 wg + j]
         {
             const float *h0 = p.h0 ? p.h0 + ((size_t)seq * H + head) * D * D : nullptr;
@@ -363,49 +395,23 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(h ? B_SREADY2 : B_SREADY));
         };
+        tmem_st32(tmem + lb + TM_D2 + 32u * wg, zero);        // D2 starts at zero
+        tmem_st32(tmem + lb + TM_D2 + 64u + 32u * wg, zero);
         store_half(0);
         store_half(1);
         for (int n = 0; n < nblocks; ++n) {
-            const int s = n % NSLOT, b = n & 1;
-            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
+            const int s = n % NSLOT;
             if (elect_trace(warp, lane)) F64_TRACE(n, 0);
-            // ---- V^T of this thread's value row and 32 tokens, loaded while Y^T is formed.
-            //      The slot's FULL phase is observed first: it makes the V tile and gamma^B
-            //      (landed by TMA / bulk copy) visible to this thread's loads.
+            // ---- the slot's FULL phase is observed first: it makes gamma^B (landed by bulk
+            //      copy) visible to this thread's loads
             if (!wait_bar(bar(B_FULL + s), (n / NSLOT) & 1)) break;
-            uint32_t vv[16];  // token pairs (2 j, 2 j + 1), bf16
-            {
-                // V tile of step n: buffer n & 1, two [64 t][64 v] 128-byte-swizzled halves
-                const unsigned char *vt = sm + CH_V + (n & 1) * V_BYTES + (v >> 6) * (V_BYTES / 2);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    vv[j] = (uint32_t)*reinterpret_cast<const unsigned short *>(vt + sw128(32 * wg + 2 * j, v & 63)) |
-                            ((uint32_t)*reinterpret_cast<const unsigned short *>(vt + sw128(32 * wg + 2 * j + 1, v & 63)) << 16);
-            }
-            // ---- Z^T = V^T - Y^T -> bf16 A operand
-            if (!wait_bar(bar(B_D1U + b), (n >> 1) & 1)) break;
+            // ---- U^T = V^T TB^T - S^T W^T -> bf16 A operand, 32 tokens per warpgroup
+            if (!wait_bar(bar(B_UFULL), n & 1)) break;
             if (elect_trace(warp, lane)) F64_TRACE(n, 2);
             tc_fence_after();
             {
                 uint32_t r[32], w[16];
-                tmem_ld32(d1 + lb + 32u * wg, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    w[j] = pack_bf16(__uint_as_float(vv[j] << 16) - __uint_as_float(r[2 * j]),
-                                     __uint_as_float(vv[j] & 0xffff0000u) - __uint_as_float(r[2 * j + 1]));
-                tmem_st16(tmem + lb + TM_AZ + 16 * wg, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_ZREADY));
-            // ---- U^T: columns 0..63 of D1 -> bf16 A operand, 32 tokens per warpgroup
-            if (!wait_bar(bar(B_UFULL + b), (n >> 1) & 1)) break;
-            tc_fence_after();
-            {
-                uint32_t r[32], w[16];
-                tmem_ld32(d1 + lb + 32u * wg, r);
+                tmem_ld32(tmem + lb + TM_U + 32u * wg, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
@@ -417,20 +423,19 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_UREADY));
             if (elect_trace(warp, lane)) F64_TRACE(n, 3);
-            // ---- S^T <- S^T diag(gamma^B) + D2, one key half at a time, then bf16
-            bool got = true;
+            // ---- S^T <- S^T diag(gamma^B) + D2, one key half at a time (D2 zeroed behind
+            //      the read), then bf16
+            if (!wait_bar(bar(B_D2FULL), n & 1)) break;
+            if (elect_trace(warp, lane)) F64_TRACE(n, 5);
+            tc_fence_after();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (!wait_bar(bar(h ? B_D2FULL2 : B_D2FULL), n & 1)) {
-                    got = false;
-                    break;
-                }
-                if (h == 0 && elect_trace(warp, lane)) F64_TRACE(n, 5);
-                tc_fence_after();
                 const float4 *gam = reinterpret_cast<const float4 *>(sm + CH_G + s * D * 4 + (64 * h + 32 * wg) * 4);
                 uint32_t r[32];
-                tmem_ld32(tmem + lb + TM_D2 + 64u * h + 32u * wg, r);
+                const uint32_t col = tmem + lb + TM_D2 + 64u * h + 32u * wg;
+                tmem_ld32(col, r);
                 tmem_ld_wait();
+                tmem_st32(col, zero);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 g = gam[j4];
@@ -446,7 +451,6 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                 }
                 store_half(h);
             }
-            if (!got) break;
             if (elect_trace(warp, lane)) F64_TRACE(n, 6);
         }
         if (p.h_final) {
@@ -457,22 +461,64 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
     } else {
         regs_set<kRegsOut>();
         // -------------------------------------------------- output warps
-        const int v = threadIdx.x - 384;
+        // Each step: -W^T of the next step from tensor memory into that step's slot (over
+        // its K~B rows, which the W product has finished reading), then this step's O^T,
+        // which is zeroed behind the read for the next step's products.
+        const int v = threadIdx.x - 384;  // TMEM lane: a value row of O^T, a key row of W^T
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const size_t tstride = (size_t)H * D;
-        for (int n = 0; n < nblocks; ++n) {
-            const int b = n & 1;  // D1 buffer
-            const bool got = wait_bar(bar(B_D1O + b), (n >> 1) & 1);
+        uint32_t zero[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) zero[j] = 0u;
+        auto release_o = [&]() {  // O zeroed, then free for the next step's products
+            tmem_st32(tmem + lb + TM_O, zero);
+            tmem_st32(tmem + lb + TM_O + 32u, zero);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_OFREE));
+        };
+        auto convert_w = [&](int m) -> bool {  // -W^T of step m -> slot m % NSLOT, [c][t] bf16
+            const bool got = wait_bar(bar(B_WFULL), m & 1);
+            if (!__all_sync(0xffffffffu, got)) return false;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tmem + lb + TM_W, r0);
+            tmem_ld32(tmem + lb + TM_W + 32u, r1);
+            tmem_ld_wait();
+            unsigned char *row = sm + CH_SLOT + (m % NSLOT) * SLOT_STRIDE + SL_B2;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // 8 tokens (16 bytes) per store
+                uint4 w0, w1;
+                w0.x = pack_bf16(-__uint_as_float(r0[8 * q]), -__uint_as_float(r0[8 * q + 1]));
+                w0.y = pack_bf16(-__uint_as_float(r0[8 * q + 2]), -__uint_as_float(r0[8 * q + 3]));
+                w0.z = pack_bf16(-__uint_as_float(r0[8 * q + 4]), -__uint_as_float(r0[8 * q + 5]));
+                w0.w = pack_bf16(-__uint_as_float(r0[8 * q + 6]), -__uint_as_float(r0[8 * q + 7]));
+                w1.x = pack_bf16(-__uint_as_float(r1[8 * q]), -__uint_as_float(r1[8 * q + 1]));
+                w1.y = pack_bf16(-__uint_as_float(r1[8 * q + 2]), -__uint_as_float(r1[8 * q + 3]));
+                w1.z = pack_bf16(-__uint_as_float(r1[8 * q + 4]), -__uint_as_float(r1[8 * q + 5]));
+                w1.w = pack_bf16(-__uint_as_float(r1[8 * q + 6]), -__uint_as_float(r1[8 * q + 7]));
+                *reinterpret_cast<uint4 *>(row + sw128(v, 8 * q)) = w0;
+                *reinterpret_cast<uint4 *>(row + sw128(v, 32 + 8 * q)) = w1;
+            }
+            fence_proxy_async();  // generic writes -> the tensor core's reads of the slot
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_WREADY));
+            return true;
+        };
+        release_o();
+        bool ok = nblocks == 0 || convert_w(0);
+        for (int n = 0; ok && n < nblocks; ++n) {
+            if (n + 1 < nblocks && !convert_w(n + 1)) break;
+            const bool got = wait_bar(bar(B_OFULL), n & 1);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
-            const uint32_t d1 = tmem + TM_D1 + 128u * (uint32_t)b;
-            tmem_ld32(d1 + lb + 64u, r0);
-            tmem_ld32(d1 + lb + 96u, r1);
+            tmem_ld32(tmem + lb + TM_O, r0);
+            tmem_ld32(tmem + lb + TM_O + 32u, r1);
             tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_D1FREE + b));
+            release_o();
             const int L = min(BT, t1 - (t0 + n * BT));
             __nv_bfloat16 *o = p.out + ((size_t)(t0 + n * BT) * H + head) * D + v;
 #pragma unroll
@@ -619,12 +665,15 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         tma_prefetch_3d(tm_q, 0, head, r0);
         tma_prefetch_3d(tm_k, 0, head, r0);
     };
-    // the staging slot into the chain CTA's slot m % NSLOT (operands) and gamma ring entry;
-    // completion (SLOT_BYTES in all) is counted on that slot's FULL barrier
+    // the staging slot into the chain CTA's slot m % NSLOT (operands, as four 16 KB copies in
+    // flight together) and gamma ring entry; completion (SLOT_BYTES in all) is counted on
+    // that slot's FULL barrier
     auto copy_out = [&](int m) {
         const uint32_t s = (uint32_t)(m % NSLOT);
         const uint32_t full = map_to_rank(sbase + CH_BAR + 8u * (B_FULL + s), 0);
-        bulk_copy_to_peer(map_to_rank(sbase + CH_SLOT + s * SLOT_STRIDE, 0), stg, SL_G, full);
+        const uint32_t dst = map_to_rank(sbase + CH_SLOT + s * SLOT_STRIDE, 0);
+        for (uint32_t q = 0; q < 4; ++q)
+            bulk_copy_to_peer(dst + q * (SL_G / 4), stg + q * (SL_G / 4), SL_G / 4, full);
         bulk_copy_to_peer(map_to_rank(sbase + CH_G + s * D * 4, 0), stg + SL_G, D * 4, full);
         bulk_commit();
     };
@@ -1039,19 +1088,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(sbase + CH_BAR + 8u * (B_FULL + s), 1);
                 mbar_init(sbase + CH_BAR + 8u * (B_FREE + s), 1 + 8);
             }
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(sbase + CH_BAR + 8u * (B_D1U + b), 1);
-                mbar_init(sbase + CH_BAR + 8u * (B_D1O + b), 1);
-                mbar_init(sbase + CH_BAR + 8u * (B_D1FREE + b), 4);
-            }
+            mbar_init(sbase + CH_BAR + 8u * B_UFULL, 1);
+            mbar_init(sbase + CH_BAR + 8u * B_WFULL, 1);
+            mbar_init(sbase + CH_BAR + 8u * B_OFREE, 4);
+            mbar_init(sbase + CH_BAR + 8u * B_OFULL, 1);
             mbar_init(sbase + CH_BAR + 8u * B_D2FULL, 1);
             mbar_init(sbase + CH_BAR + 8u * B_DRAIN, 1);
             mbar_init(sbase + CH_BAR + 8u * B_SREADY, 8);
-            mbar_init(sbase + CH_BAR + 8u * B_UREADY, 8);
-            mbar_init(sbase + CH_BAR + 8u * B_ZREADY, 8);
             mbar_init(sbase + CH_BAR + 8u * B_SREADY2, 8);
-            mbar_init(sbase + CH_BAR + 8u * B_D2FULL2, 1);
-            for (int b = 0; b < 2; ++b) mbar_init(sbase + CH_BAR + 8u * (B_UFULL + b), 1);
+            mbar_init(sbase + CH_BAR + 8u * B_UREADY, 8);
+            mbar_init(sbase + CH_BAR + 8u * B_WREADY, 4);
         } else {
             mbar_init(sbase + PR_BAR, 1);
             mbar_init(sbase + PR_BAR + 8, 1);

@@ -233,6 +233,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t *r) {
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
         "%13,%14,%15,%16};" ::"r"(ta), KDA_W8(0), KDA_W8(8));
 }
+__device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(ta), KDA_W8(0), KDA_W8(8), KDA_W8(16), KDA_W8(24));
+}
 #undef KDA_R8
 #undef KDA_W8
 __device__ __forceinline__ void tmem_ld_wait() {
