@@ -576,8 +576,10 @@ def measure_e2e(x, dev, stream, steps, kda):
 
     def timed(call):
         """(median, mean, max) over ``steps`` back-to-back calls, each bracketed by CUDA
-        events on the stream (every call ends with the stream waiting for its last copy)."""
-        call()
+        events on the stream (every call ends with the stream waiting for its last copy),
+        after three untimed calls."""
+        for _ in range(3):
+            call()
         torch.cuda.synchronize(dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         ev[0].record(stream)
