@@ -279,9 +279,11 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
             // share an A operand go out as one wide MMA. Per step n (slot s):
             //   [U | O]  += S^T [-W^T | Q~B^T]      N = 128, keys 0..63 as soon as they are
             //                                       in, then 64..127; commit UFULL
-            //   W of step n + 1: K~B^T TB^T          N = 64 (once its slot is in); commit WFULL
             //   [O | D2] += U^T [P^T | K'B]          N = 192; commit D2FULL, OFULL, FREE
+            //   W of step n + 1: K~B^T TB^T          N = 64 (once its slot is in); commit WFULL
             //   U of step n + 1: V^T TB^T            N = 64 (starts the next U)
+            // W and U of the next step go out while the state warps update the state; issued
+            // earlier (between the U^T hand-off and D2) they delayed D2.
             // O and D2 are zeroed by the warps that read them, so every product after the
             // first of U accumulates.
             const uint32_t id_w = idesc_bf16(128, 64, 0, 0);    // A and B K-major
@@ -336,13 +338,6 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                     umma_ts(tmem + TM_U, tmem + TM_AS + 8u * k, dWQ0 + so + (uint64_t)(128 * k), id_1, 1);
                 umma_commit(bar(B_UFULL));
                 F64_TRACE(n, 1);
-                // W of the next step while the state warps convert U^T, if its slot is in
-                bool wnext = false;
-                if (n + 1 < nblocks && mbar_try(bar(B_FULL + (n + 1) % NSLOT), ((n + 1) / NSLOT) & 1)) {
-                    tc_fence_after();
-                    issue_w(n + 1);
-                    wnext = true;
-                }
                 if (!wait_bar(bar(B_UREADY), n & 1)) break;  // U^T (bf16) of step n is in
                 tc_fence_after();
 #pragma unroll
@@ -352,12 +347,10 @@ __device__ void chain_cta(unsigned char *sm, uint32_t sbase, const CUtensorMap *
                 umma_commit(bar(B_OFULL));
                 umma_commit(bar(B_FREE + s));
                 F64_TRACE(n, 4);
-                if (n + 1 < nblocks) {
-                    if (!wnext) {
-                        if (!wait_bar(bar(B_FULL + (n + 1) % NSLOT), ((n + 1) / NSLOT) & 1)) break;
-                        tc_fence_after();
-                        issue_w(n + 1);
-                    }
+                if (n + 1 < nblocks) {  // the next step's W and U while the state is updated
+                    if (!wait_bar(bar(B_FULL + (n + 1) % NSLOT), ((n + 1) / NSLOT) & 1)) break;
+                    tc_fence_after();
+                    issue_w(n + 1);
                     issue_vtb(n + 1);  // U of step n has been read (UREADY above)
                 }
             }
