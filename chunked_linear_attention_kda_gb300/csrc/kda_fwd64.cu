@@ -649,24 +649,12 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
             cp_async_commit();
         }
     };
-    // the raw tiles of step m into L2, two owned steps before they are loaded, so that the
-    // load issued after a gate pass finds them there
-    auto prefetch = [&](int m) {
-        if (m >= nblocks || warp != 15 || lane != 0) return;
-        const int r0 = t0 + m * BT;
-        tma_prefetch_3d(tm_a, 0, head, r0);
-        tma_prefetch_3d(tm_q, 0, head, r0);
-        tma_prefetch_3d(tm_k, 0, head, r0);
-    };
-    // the staging slot into the chain CTA's slot m % NSLOT (operands, as four 16 KB copies in
-    // flight together) and gamma ring entry; completion (SLOT_BYTES in all) is counted on
-    // that slot's FULL barrier
+    // the staging slot into the chain CTA's slot m % NSLOT (operands) and gamma ring entry;
+    // completion (SLOT_BYTES in all) is counted on that slot's FULL barrier
     auto copy_out = [&](int m) {
         const uint32_t s = (uint32_t)(m % NSLOT);
         const uint32_t full = map_to_rank(sbase + CH_BAR + 8u * (B_FULL + s), 0);
-        const uint32_t dst = map_to_rank(sbase + CH_SLOT + s * SLOT_STRIDE, 0);
-        for (uint32_t q = 0; q < 4; ++q)
-            bulk_copy_to_peer(dst + q * (SL_G / 4), stg + q * (SL_G / 4), SL_G / 4, full);
+        bulk_copy_to_peer(map_to_rank(sbase + CH_SLOT + s * SLOT_STRIDE, 0), stg, SL_G, full);
         bulk_copy_to_peer(map_to_rank(sbase + CH_G + s * D * 4, 0), stg + SL_G, D * 4, full);
         bulk_commit();
     };
@@ -687,7 +675,6 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         }
     };
     fetch(prank, 0);
-    prefetch(prank + kPro);
     // tensor memory for the products. B1 starts at zero: the tiles of TB and of P above
     // the diagonal are never written, so they stay zero in every step's slot. The unused
     // last 32 columns of the column tiles are zeroed once (their products are never read).
@@ -745,7 +732,6 @@ __device__ void prologue_cta(unsigned char *sm, uint32_t sbase, const CUtensorMa
         if (tid == 511) F64_TRACE(m, 26);
         __syncthreads();
         fetch(m + kPro, (k + 1) & 1);  // the raw tiles have been consumed
-        prefetch(m + 2 * kPro);
         if (tid == 0) F64_TRACE(m, 10);
         // ---- P2: every scaled operand of this (channel, tile), from fp32 values:
         //   R = [K~ | Q~] (K~ = K Gamma), the column tiles K^ = K / Gamma and

@@ -76,11 +76,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x
         "[%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(mbar) : "memory");
 }
-// the same box into L2 only (no shared-memory destination, no completion to wait for)
-__device__ __forceinline__ void tma_prefetch_3d(const void *map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-                 ::"l"(map), "r"(x), "r"(y), "r"(z) : "memory");
-}
 // this CTA's shared memory -> a peer's, completion (bytes) on the peer's mbarrier
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,
                                                   uint32_t bytes, uint32_t mbar_cluster) {
