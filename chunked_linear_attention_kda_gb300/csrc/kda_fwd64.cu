@@ -14,29 +14,32 @@
 //   A  = strict_lower(diag(beta) [K K^T with the factors above])     64 x 64
 //   P  = lower([Q K^T with the same factors])                        64 x 64
 //   TB = (I + A)^-1 diag(beta),   K~B = K exp(G^B),   K'B = K exp(G^B_end - G^B)
-//   U  = TB (V - K~B S),   O = d_k^-1/2 (Q~B S + P U),
+//   W  = TB K~B,   U = TB (V - K~B S) = TB V - W S,   O = d_k^-1/2 (Q~B S + P U),
 //   S <- Diag(exp G^B_end) S + K'B^T U
 //
 // Work decomposition: one cluster of 1 + kPro CTAs per (sequence, head).
 //  * rank 0, the chain CTA, runs the serial recurrence. Transposed, with the state S^T
 //    (d_v x d_k) as the A operand of the tensor core, per step:
-//        D1[:, 0..63]   = S^T K~B^T = Y^T,  then  Z^T TB^T = U^T  with Z^T = V^T - Y^T
-//        D1[:, 64..127] = S^T Q~B^T + U^T P^T          = O^T / scale
-//        D2             = U^T K'B                      (the state increment)
-//    The Y^T, U^T and D2 groups lie on the state's
-//    critical path; the O^T products fill the tensor pipe while U^T is formed and while
-//    the state is updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
+//        W^T       = K~B^T TB^T                  (issued a step ahead)
+//        [U | O]  += S^T [-W^T | Q~B^T]          (U started a step ahead as V^T TB^T)
+//        [O | D2] += U^T [P^T | K'B]             (O^T / scale, and the state increment)
+//    A tcgen05.mma costs about the same to issue whatever its N, so products sharing an A
+//    operand go out as one MMA. Only the two S^T / U^T groups lie on the state's
+//    critical path; the next step's W and V^T TB^T products run while the state is
+//    updated. S^T lives in fp32 registers of eight "state" warps (two warpgroups; one
 //    value row and 64 keys per thread) and is mirrored as bf16 into tensor memory as the
 //    next A operand; U^T likewise. One issuer thread (its own warp) issues every
 //    tcgen05.mma; the state warps signal it per warp through mbarriers. Four "output"
-//    warps store O. A producer warp loads each step's V tile by TMA into one of two
-//    buffers; the products arrive in one of three operand slots.
+//    warps write -W^T in bf16 over the K~B rows of the step's slot (the B operand of
+//    S^T W^T), read O^T, zero it for the next step's products and store O. A producer warp
+//    loads each step's V tile by TMA into one of two buffers; the products arrive in one
+//    of three operand slots.
 //  * ranks 1..kPro, the prologue CTAs, each compute every kPro-th step's operands (the
 //    gate, the four tiles' scaled operands, [A; P] as one tcgen05 product, the 64 x 64
 //    solve for TB) into a staging buffer laid out exactly as the chain CTA's operand
-//    slot, and copy it there with bulk copies
-//    (shared::cta -> shared::cluster) once the chain CTA has freed the slot (with three
-//    slots and three prologue CTAs, each prologue CTA always fills the same slot).
+//    slot, and copy it there with bulk copies (shared::cta -> shared::cluster) once the
+//    chain CTA has freed the slot (with three slots and three prologue CTAs, each
+//    prologue CTA always fills the same slot).
 // Every wait is bounded: one that exceeds its limit sets bit 3 of the status word
 // (kda_read_device_flags); every other wait of the grid then gives up and the kernel
 // finishes with unspecified output.
@@ -55,8 +58,8 @@ __device__ unsigned int g_fwd64_flags;  // bit 3: a pipeline wait exceeded its l
 
 // Phase timestamps (SM clock) of the first cluster's first 64 steps: a profiling aid
 // compiled only with -DKDA_FWD64_TRACE. Chain CTA, per step: 0 state-warp loop top,
-// 1 Y^T products issued, 2 Y^T complete, 3 U^T stored, 4 every product of the step
-// issued, 5 D2 keys 0..63 complete, 6 state stored. The prologue CTA owning the step:
+// 1 [U | O] products issued, 2 U^T complete, 3 U^T stored, 4 [O | D2] products issued,
+// 5 D2 complete, 6 state stored. The prologue CTA owning the step:
 // 8 loop top, 9 raw tiles in, 20 / 26 gate pass done (first / last thread), 10 next
 // fetch issued, 11 operands written, 21 [A; P] issued, 22 / 24 [A; P] complete, 23 A
 // and P read out, 12 read-out barrier, 16 diagonal T tiles, 17 M, 18 M^2, 27 TB tiles,
